@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Throughput of the ESM-2 650M packed encoder forward on GB300.
+
+One step = one full forward (embedding, 33 layers, final LayerNorm) over a packed batch
+of 16384 tokens (47 sequences, log-normal lengths, seed 2) already resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank encodes its own batch of the same size (the
+sequences of a packed batch are independent, so ranks need no data exchange); value =
+all tokens / max-over-ranks time.  Rank 0 prints one JSON line.  --impl reference times
+the float64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "ESM-2 650M packed fwd tokens/s on 1 GB300; achieved TFLOP/s vs dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_for_rank(rank: int):
+    from transformer_esm_layer_gb300 import synth
+    wl = synth.make_workload("esm650m")
+    if rank > 0:  # another batch of the same size and length distribution
+        rng = np.random.default_rng([wl.seed, rank])
+        wl.lengths = synth.lognormal_lengths(rng, total=16384)
+        wl.seed = wl.seed * 1000 + rank
+    return wl
+
+
+def algorithmic_flops(wl):
+    """FLOPs one forward must do: per layer 2T(4d^2 + 2df) in the four linear maps plus
+    4 d sum(L_i^2) in attention (QK^T and PV over each sequence only)."""
+    g = wl.geometry
+    T, d, f = wl.total_tokens, g.hidden, g.ffn
+    L2 = float(np.sum(np.asarray(wl.lengths, np.float64) ** 2))
+    per_class = {"gemm_qkv": 2.0 * T * 3 * d * d, "gemm_oproj": 2.0 * T * d * d, "gemm_fc1": 2.0 * T * f * d,
+                 "gemm_fc2": 2.0 * T * d * f, "attention": 4.0 * d * L2}
+    return {k: v * g.num_layers for k, v in per_class.items()}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        with open(self.f.name) as fh:
+            rows = [r.strip().split(", ") for r in fh if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gemm_traffic_record():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken on the
+    current GEMM source (null otherwise)."""
+    p = os.path.join(ROOT, "profiles", "gemm_tc_dram_traffic.json")
+    src = os.path.join(ROOT, "transformer_esm_layer_gb300", "csrc", "gemm_tc.cu")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec if rec.get("gemm_tc_sha256_16") == h else None
+
+
+def cpu_oracle_sample(wl, w64, seconds: float):
+    """Time the float64 oracle on whole sequences of the workload until `seconds` pass."""
+    from oracle import esm_oracle as O
+    from transformer_esm_layer_gb300 import synth
+    tok = synth.workload_tokens(wl)
+    cu = O.cu_seqlens(wl.lengths)
+    done, toks = [], 0
+    t0 = time.perf_counter()
+    for i in range(len(wl.lengths)):
+        O.encode_sequence(tok[cu[i]:cu[i + 1]], w64, wl.geometry.heads, final_ln=True)
+        done.append(i)
+        toks += wl.lengths[i]
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return toks, dt, done
+
+
+def f64_weights(w):
+    return {"emb": np.asarray(w["emb"], np.float64),
+            "layers": [{k: np.asarray(v, np.float64) for k, v in l.items()} for l in w["layers"]],
+            "lnf_g": np.asarray(w["lnf_g"], np.float64), "lnf_b": np.asarray(w["lnf_b"], np.float64)}
+
+
+def run_reference(args):
+    """The float64 oracle on the host cores: each step encodes one whole sequence of the
+    workload (cycling through them in order)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from oracle import esm_oracle as O
+    from transformer_esm_layer_gb300 import synth
+    wl = workload_for_rank(0)
+    w = f64_weights(synth.model_weights(wl.geometry, wl.seed, "bf16"))
+    tok = synth.workload_tokens(wl)
+    cu = O.cu_seqlens(wl.lengths)
+    B = len(wl.lengths)
+    for s in range(args.warmup):
+        i = s % B
+        O.encode_sequence(tok[cu[i]:cu[i + 1]], w, wl.geometry.heads, final_ln=True)
+    toks, t = 0, 0.0
+    for s in range(args.steps):
+        i = (args.warmup + s) % B
+        t0 = time.perf_counter()
+        O.encode_sequence(tok[cu[i]:cu[i + 1]], w, wl.geometry.heads, final_ln=True)
+        t += time.perf_counter() - t0
+        toks += wl.lengths[i]
+    value = toks / t
+    cores = len(os.sched_getaffinity(0))
+    sample = f"one whole sequence per step, cycling through the {B} sequences of the workload (seed 2); {toks} tokens timed"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "esm650m", "tokens_per_step": f"{toks / args.steps:.0f} (mean)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from transformer_esm_layer_gb300 import build as _build
+    from transformer_esm_layer_gb300 import synth
+    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    _build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    wl = workload_for_rank(rank)
+    g = wl.geometry
+    w_np = synth.model_weights(g, wl.seed, "bf16")
+    dw = DeviceWeights(w_np, "bf16", device=dev)
+    tok_np = synth.workload_tokens(wl)
+    tok, cu = packed_inputs(tok_np, wl.lengths, device=dev)
+    T, B, maxL = wl.total_tokens, len(wl.lengths), max(wl.lengths)
+    enc = EsmEncoder.from_geometry(g, "bf16", final_ln=True)
+    ws = enc.workspace(T, B, dev)
+    out = torch.empty(T, g.hidden, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        enc.forward(dw, tok, cu, maxL, out=out, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    enc.check(stream)
+
+    # ---------------------------------------------------------------- timed region
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    enc.get_profile(reset=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    launches = enc.get_profile(reset=True)["total_launches"]
+    enc.check(stream)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * T / (ms_step / 1e3)
+
+    # ---------------------------------------------------------------- per-kernel device times
+    enc.set_profiling(True)
+    prof_steps = min(args.steps, 10)
+    for _ in range(prof_steps):
+        step()
+    prof = enc.get_profile(reset=True)
+    enc.set_profiling(False)
+    flops = algorithmic_flops(wl)
+    total_flops = sum(flops.values())
+    pk, pk_src = peaks()
+    gemm_classes = ("gemm_qkv", "gemm_oproj", "gemm_fc1", "gemm_fc2")
+    gemm_ms = sum(prof[c]["ms"] for c in gemm_classes) / prof_steps
+    gemm_launches = sum(prof[c]["launches"] for c in gemm_classes) / prof_steps
+    gemm_flops = sum(flops[c] for c in gemm_classes)
+    gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12
+    peak_sust = float(pk["bf16_tflops_sustained"])
+    per_kernel = {c: {"ms_per_step": prof[c]["ms"] / prof_steps, "launches_per_step": prof[c]["launches"] / prof_steps}
+                  for c in ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other")}
+    for c in list(gemm_classes) + ["attention"]:
+        per_kernel[c]["tflops"] = flops[c] / (per_kernel[c]["ms_per_step"] / 1e3) / 1e12 if per_kernel[c]["ms_per_step"] else None
+    traffic = gemm_traffic_record()
+    roofline = {"bound": "tensor", "kernel": "gemm_tc_kernel (tcgen05 bf16, all four linear maps)",
+                "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s", "frac": gemm_tflops / peak_sust,
+                "peak_source": f"bf16_tflops_sustained, {pk_src}",
+                "flops_per_launch": gemm_flops / gemm_launches if gemm_launches else None,
+                "avg_launch_ms": gemm_ms / gemm_launches if gemm_launches else None,
+                "traffic": traffic.get("dram_bytes_per_launch") if traffic else None}
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    if world == 1 or True:
+        tok_h = torch.from_numpy(tok_np.astype(np.int32)).pin_memory()
+        cu_h = torch.from_numpy(synth.cu_seqlens_from_lengths(wl.lengths)).pin_memory()
+        out_h = torch.empty(T, g.hidden, dtype=torch.bfloat16).pin_memory()
+        out_view = out_h.view(torch.int16).numpy()
+        tok_view, cu_view = tok_h.numpy(), cu_h.numpy()
+        n_e2e = min(args.steps, 10)
+        enc.forward_host(dw, tok_view, cu_view, maxL, out_view, ws, stream=stream)
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            enc.forward_host(dw, tok_view, cu_view, maxL, out_view, ws, stream=stream)
+        dt = (time.perf_counter() - t0) / n_e2e
+        if world > 1:
+            t = torch.tensor([dt], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": 4 * T + 4 * (B + 1),
+               "d2h_bytes_per_step": 2 * T * g.hidden, "ms_per_step": dt * 1e3,
+               "call": "esm_encoder_forward_host (pinned host buffers in and out)"}
+
+    # ---------------------------------------------------------------- CPU baseline (oracle)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        toks, dt, done = cpu_oracle_sample(wl, f64_weights(w_np), args.cpu_seconds)
+        cpu = {"value": toks / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"{len(done)} whole sequence(s) of the workload (indices {done}, {toks} tokens) through all "
+                         f"33 layers in float64 numpy, {dt:.1f} s"}
+
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "esm650m: ESM-2 650M encoder (33 layers, hidden 1280, 20 heads, FFN 5120, "
+                                       "vocab 33), bf16 weights N(0,0.02), packed batch of 16384 tokens in 47 "
+                                       "sequences, log-normal lengths (median 300, sigma 0.6) clipped to [32,1024], "
+                                       "seed 2",
+                           "tokens_per_step_per_gpu": T, "sequences": B, "max_seqlen": maxL,
+                           "l2": "no flush: inputs larger than L2 (1.3 GB of weights read per step plus "
+                                 f"{ws.numel() / 2**30:.2f} GB of activations vs the 129 MB L2)",
+                           "parallelism": "single GPU" if world == 1 else f"{world} replicas, each its own batch, "
+                                                                          "no collective"},
+                "tflops": total_flops * world / (ms_step / 1e3) / 1e12,
+                "mfu_vs_sustained_bf16": total_flops / (ms_step / 1e3) / 1e12 / peak_sust,
+                "mfu_vs_burst_bf16": total_flops / (ms_step / 1e3) / 1e12 / float(pk["bf16_tflops"]),
+                "algorithmic_gflop_per_step_per_gpu": total_flops / 1e9,
+                "roofline": roofline, "per_kernel": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clocks, "gpu_launches": launches,
+                "context": "pages' own figure: 59.2% model-FLOP utilisation, ESM-2 650M training, batch 46, A100"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

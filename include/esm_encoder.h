@@ -1,0 +1,250 @@
+/*
+ * esm_encoder.h -- C ABI of the GB300 (sm_103a) ESM-2 encoder forward on packed
+ * variable-length protein sequences.
+ *
+ * What is computed (sources are web pages; page title and section are named):
+ *   * Packing: "生物大模型训练加速实战：基于PyTorch与NVIDIA BioNeMo的Transformer优化指南"
+ *     (hotelren.com), section 3.2: a batch is the concatenation of its sequences'
+ *     tokens plus cu_seqlens = cumsum([0] + lengths) and max_seqlen; the packed
+ *     forward runs the token embedding and then every encoder layer over cu_seqlens.
+ *   * The layer: same guide, section 3.1 (self-attention, LayerNorm, fc1, fc2 as one
+ *     fused TransformerEngine encoder layer, padding mask, bshd or thd input), and the
+ *     "NVIDIA ESM-2 TransformerEngine" walkthrough (mlqm.cn), sections on rotary
+ *     position embedding (size hidden / heads), the padding mask with bshd input,
+ *     fused QKV weights and the 1026-position / 33-token vocabulary.
+ *   * Bidirectional attention: BioNeMo ESM-2 model card (docs.nvda.net.cn), model
+ *     overview ("BERT-style bidirectional encoder"); output: one float vector per
+ *     residue (section "输出").
+ *   * FP8: the aikraft.ru TransformerEngine summary, "Рецепт FP8: Delayed Scaling"
+ *     (E4M3 forward, amax history 16, max algorithm), and section 4.1 of the hotelren.com
+ *     guide.
+ *
+ * Per layer (pre-LN):  y = LN1(x); [q|k|v] = y Wqkv^T + bqkv; RoPE(q, k);
+ *   o = softmax(q k^T / sqrt(64)) v within each sequence; x += o Wo^T + bo;
+ *   u = GELU(LN2(x) W1^T + b1); x += u W2^T + b2.   Output: LNf(x) (or x).
+ * Readings where the pages are silent: LayerNorm eps from the config (1e-5), biased
+ * variance; exact erf GELU; RoPE base from the config (10000), rotate-half pairs
+ * (j, j + head_dim/2), positions restart at 0 at every sequence start; no dropout.
+ *
+ * Conventions for every call:
+ *   * All device buffers belong to the caller; the library only borrows them for the
+ *     duration of the (asynchronous) call on `stream`.  Pointers marked "device" must
+ *     be device memory of the current device; "host" pointers are host memory.
+ *   * Tensors are dense row-major.  Linear weights are [out_features, in_features].
+ *     w_qkv rows are q | k | v, each block head-major (row h*64 + c).
+ *   * Parameter dtype: float32 for ESM_FP32; bfloat16 for ESM_BF16 and ESM_FP8_E4M3
+ *     (FP8 GEMM operands are quantised on the fly from the bf16 weights).
+ *   * hidden_out dtype: float32 for ESM_FP32, bfloat16 otherwise.
+ *   * Errors are returned, never thrown or trapped.  Host-side checks return at once.
+ *     Errors the kernels detect (malformed cu_seqlens, token ids out of range, a
+ *     bounded device wait that ran out) are latched in the handle and reported by
+ *     esm_encoder_check(); outputs of such a call are unspecified but every access
+ *     stays in bounds.
+ *   * A handle is not thread-safe: do not call it from two host threads at once.
+ *     Calls on one stream run in order; calls on different streams that share a
+ *     workspace race.
+ */
+#ifndef ESM_ENCODER_H_
+#define ESM_ENCODER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ESM_API __attribute__((visibility("default")))
+#else
+#define ESM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* esm_stream_t;
+
+typedef enum {
+  ESM_OK = 0,
+  ESM_ERR_INVALID_ARG = 1,    /* a pointer, size or config field is invalid          */
+  ESM_ERR_UNSUPPORTED = 2,    /* device is not sm_103, or a geometry the kernels lack */
+  ESM_ERR_BAD_CU_SEQLENS = 3, /* cu_seqlens not 0 = c0 <= c1 <= ... = T, or L > max   */
+  ESM_ERR_TOKEN_RANGE = 4,    /* a token id outside [0, vocab)                        */
+  ESM_ERR_WORKSPACE = 5,      /* workspace NULL, misaligned or smaller than required  */
+  ESM_ERR_CUDA = 6,           /* a CUDA runtime call failed                           */
+  ESM_ERR_TIMEOUT = 7         /* a bounded device-side wait gave up                   */
+} esm_status;
+
+typedef enum { ESM_FP32 = 0, ESM_BF16 = 1, ESM_FP8_E4M3 = 2 } esm_precision;
+
+/* Encoder geometry and numerics.  ESM-2 650M: {33, 1280, 20, 5120, 33, 1026, 1e-5,
+ * 10000, 1, 1, ESM_BF16, 16}.  head_dim = hidden / heads must be 64 for ESM_BF16 and
+ * ESM_FP8_E4M3 (and hidden a multiple of 256, ffn a multiple of 256); ESM_FP32 accepts
+ * any even head_dim <= 64 with hidden <= 4096. */
+typedef struct {
+  int num_layers;
+  int hidden;
+  int heads;
+  int ffn;
+  int vocab;
+  int max_positions;      /* upper bound of every sequence length (1026)            */
+  float ln_eps;
+  float rope_base;
+  float emb_scale;        /* x = emb_scale * E[token]                                */
+  int final_ln;           /* 1: apply the final LayerNorm; 0: return the residual   */
+  esm_precision precision;
+  int amax_history_len;   /* FP8 delayed scaling history length (1..1024)           */
+} esm_config;
+
+/* Device pointers to the weights.  The per-layer members point to HOST arrays of
+ * num_layers DEVICE pointers (read during the call only). */
+typedef struct {
+  const void* emb;                 /* [vocab, hidden]                   */
+  const void* const* ln1_g;        /* [hidden]                          */
+  const void* const* ln1_b;        /* [hidden]                          */
+  const void* const* w_qkv;        /* [3*hidden, hidden]                */
+  const void* const* b_qkv;        /* [3*hidden]                        */
+  const void* const* w_o;          /* [hidden, hidden]                  */
+  const void* const* b_o;          /* [hidden]                          */
+  const void* const* ln2_g;        /* [hidden]                          */
+  const void* const* ln2_b;        /* [hidden]                          */
+  const void* const* w_1;          /* [ffn, hidden]                     */
+  const void* const* b_1;          /* [ffn]                             */
+  const void* const* w_2;          /* [hidden, ffn]                     */
+  const void* const* b_2;          /* [hidden]                          */
+  const void* lnf_g;               /* [hidden] (ignored if final_ln==0) */
+  const void* lnf_b;               /* [hidden]                          */
+} esm_weights;
+
+typedef struct esm_encoder esm_encoder_t;
+
+/* Create a handle for `cfg` on the current CUDA device.  Fails with
+ * ESM_ERR_UNSUPPORTED unless the device is compute capability 10.3 (GB300) and the
+ * geometry is one the kernels implement.  Allocates a few KB of device state (the
+ * error word and the FP8 scaling state).  *out is NULL on failure. */
+ESM_API esm_status esm_encoder_create(const esm_config* cfg, esm_encoder_t** out);
+
+/* Free the handle and its device state.  NULL is accepted. */
+ESM_API void esm_encoder_destroy(esm_encoder_t* h);
+
+/* Bytes of device workspace a forward over at most max_tokens packed tokens in at most
+ * max_seqs sequences needs (for the padded call: max_tokens = B*S, max_seqs = B). */
+ESM_API esm_status esm_encoder_workspace_size(const esm_encoder_t* h, int max_tokens, int max_seqs,
+                                      size_t* bytes);
+
+/* Packed (THD) forward -- the packed model forward of section 3.2 of the hotelren.com
+ * guide: forward(input_ids, cu_seqlens, max_seqlen).
+ *   token_ids   device int32 [total_tokens], each in [0, vocab)
+ *   cu_seqlens  device int32 [num_seqs + 1], 0 = c0 <= ... <= c_B = total_tokens
+ *   max_seqlen  >= every c_{i+1} - c_i and <= max_positions
+ *   hidden_out  device [total_tokens, hidden]
+ *   workspace   device, 256-byte aligned, >= esm_encoder_workspace_size(T, B)
+ * total_tokens == 0 is a no-op. */
+ESM_API esm_status esm_encoder_forward(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids,
+                               const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                               int max_seqlen, void* hidden_out, void* workspace,
+                               size_t workspace_bytes, esm_stream_t stream);
+
+/* Same as esm_encoder_forward but token_ids, cu_seqlens and hidden_out are HOST
+ * buffers: the call copies the inputs into the workspace, runs the forward and copies
+ * the result back, all on `stream`, and returns after the stream has synchronised.
+ * Pinned host memory gives asynchronous copies; pageable memory works too. */
+ESM_API esm_status esm_encoder_forward_host(esm_encoder_t* h, const esm_weights* w,
+                                    const int32_t* token_ids_host, const int32_t* cu_seqlens_host,
+                                    int num_seqs, int total_tokens, int max_seqlen,
+                                    void* hidden_out_host, void* workspace, size_t workspace_bytes,
+                                    esm_stream_t stream);
+
+/* Padded (BSHD) forward with a key padding mask -- the padding-mask / bshd input format
+ * of the mlqm.cn walkthrough (attention-mask section) and section 3.1 of the hotelren.com
+ * guide.  token_ids device int32 [B, S] (pad id anywhere past each length);
+ * seq_lens device int32 [B], 1 <= len_b <= S <= max_positions.  Every row, padding
+ * included, goes through the GEMMs; queries attend to keys < len_b only; output rows
+ * b*S + s with s >= len_b are written as zero.  hidden_out device [B, S, hidden]. */
+ESM_API esm_status esm_encoder_forward_padded(esm_encoder_t* h, const esm_weights* w,
+                                      const int32_t* token_ids, const int32_t* seq_lens, int B,
+                                      int S, void* hidden_out, void* workspace,
+                                      size_t workspace_bytes, esm_stream_t stream);
+
+/* Synchronise `stream` and return (and clear) the first error the kernels latched
+ * since the last check: ESM_ERR_BAD_CU_SEQLENS, ESM_ERR_TOKEN_RANGE, ESM_ERR_TIMEOUT
+ * or ESM_OK. */
+ESM_API esm_status esm_encoder_check(esm_encoder_t* h, esm_stream_t stream);
+
+/* Packing indices only (bit-exact parity hook for section 3.2 packing): validates
+ * cu_seqlens like the forward and writes pos_id[t] = t - c_{seg(t)} and seg_id[t]
+ * (device int32 [total_tokens] each). */
+ESM_API esm_status esm_encoder_debug_pack_index(esm_encoder_t* h, const int32_t* cu_seqlens, int num_seqs,
+                                        int total_tokens, int max_seqlen, int32_t* pos_id,
+                                        int32_t* seg_id, void* workspace, size_t workspace_bytes,
+                                        esm_stream_t stream);
+
+/* ---- single-operation hooks (the kernels the forward uses, exposed for parity) ---- */
+
+/* y = LN(x) * gamma + beta per row.  x device float32 [rows, cols]; gamma, beta device
+ * in the handle's parameter dtype [cols]; y device in the handle's activation dtype
+ * (float32 for ESM_FP32, bfloat16 otherwise).  LayerNorm of the hotelren.com guide
+ * section 3.1 / the aikraft.ru te.LayerNorm. */
+ESM_API esm_status esm_op_layernorm(esm_encoder_t* h, const float* x, const void* gamma, const void* beta,
+                            void* y, int rows, int cols, esm_stream_t stream);
+
+typedef enum {
+  ESM_EPI_BIAS_F32 = 0,   /* out float32 [M,N] = A B^T + bias                          */
+  ESM_EPI_QKV_ROPE = 1,   /* out act [M,N], N = 3*hidden: A B^T + bias, RoPE on q|k   */
+  ESM_EPI_RESIDUAL = 2,   /* out float32 [M,N] += A B^T + bias (the residual stream)  */
+  ESM_EPI_GELU = 3        /* out act [M,N] = GELU(A B^T + bias)                        */
+} esm_epilogue;
+
+/* One GEMM of the layer with its fused epilogue: A [M,K] (activation dtype), B [N,K]
+ * (parameter dtype), bias [N] (parameter dtype).  pos_id (device int32 [M]) gives each
+ * row's position for ESM_EPI_QKV_ROPE and is ignored otherwise.  ESM_BF16 requires
+ * K % 64 == 0 and N % 256 == 0; ESM_FP32 accepts any sizes.  (ESM_FP8_E4M3 handles
+ * use the bf16 tensor-core GEMM here.) */
+ESM_API esm_status esm_op_gemm(esm_encoder_t* h, esm_epilogue epi, const void* A, const void* B,
+                       const void* bias, void* out, const int32_t* pos_id, int M, int N, int K,
+                       esm_stream_t stream);
+
+/* Variable-length bidirectional attention over packed sequences (section 3.2 of the
+ * hotelren.com guide, thd format).  qkv device [T, 3*hidden] in the activation dtype
+ * (q | k | v, head-major, RoPE already applied); o device [T, hidden].  Each token
+ * attends to all tokens of its own sequence.  Uses the workspace for the work list. */
+ESM_API esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens,
+                            int num_seqs, int total_tokens, int max_seqlen, void* o,
+                            void* workspace, size_t workspace_bytes, esm_stream_t stream);
+
+/* ---- FP8 delayed-scaling state (ESM_FP8_E4M3 handles) ----
+ * Layout, float32: for each layer l and each of the 8 quantised tensors k in the order
+ * {x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2}: scale[l][k] (num_layers*8 floats), then
+ * amax_history[l][k][amax_history_len] (newest first).  n is the number of floats in
+ * host_buf and must equal num_layers*8*(1 + amax_history_len).  Initial state: every
+ * scale 1, every history entry 0.  get synchronises the device. */
+ESM_API esm_status esm_encoder_get_fp8_state(const esm_encoder_t* h, float* host_buf, size_t n);
+ESM_API esm_status esm_encoder_set_fp8_state(esm_encoder_t* h, const float* host_buf, size_t n);
+
+/* ---- measurement hooks ----
+ * Kernel classes of the forward: 0 QKV GEMM (+bias, RoPE), 1 attention, 2 output-projection
+ * GEMM (+bias, residual), 3 fc1 GEMM (+bias, GELU), 4 fc2 GEMM (+bias, residual),
+ * 5 LayerNorm, 6 everything else (packing, work list, embedding, FP8 quantise/update). */
+#define ESM_PROFILE_CLASSES 8
+typedef struct {
+  double ms[ESM_PROFILE_CLASSES];           /* summed device time per class (profiling on)  */
+  long long launches[ESM_PROFILE_CLASSES];  /* kernel launches per class                     */
+  long long total_launches;                 /* all kernel launches since the last reset      */
+} esm_profile;
+
+/* enable != 0: bracket every kernel launch with CUDA events recorded on the launch stream,
+ * so per-class device times can be read back (adds a small per-launch cost).  Launches are
+ * counted whether or not profiling is on. */
+ESM_API esm_status esm_encoder_set_profiling(esm_encoder_t* h, int enable);
+
+/* Synchronise the device, fill *out with the totals since the last reset and, if reset is
+ * nonzero, start new totals. */
+ESM_API esm_status esm_encoder_get_profile(esm_encoder_t* h, esm_profile* out, int reset);
+
+/* Static string for a status code. */
+ESM_API const char* esm_status_string(esm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESM_ENCODER_H_ */

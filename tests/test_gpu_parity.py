@@ -1,0 +1,331 @@
+"""Parity of the CUDA path (called through the C ABI) with the float64 oracle.
+
+Tolerances (relative L2 over all compared elements): fp32 1e-4, bf16 1e-2, FP8 5e-2 for
+final hidden states; packing indices bit-exact.  Kernel-level checks use tighter bounds
+derived from the arithmetic (stated at each test)."""
+import numpy as np
+import pytest
+
+from oracle import esm_oracle as O
+from tests._util import ensure_built, rel_l2, to_np
+from transformer_esm_layer_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def _enc(g, precision, final_ln=True, **kw):
+    from transformer_esm_layer_gb300.binding import EsmEncoder
+    return EsmEncoder.from_geometry(g, precision, final_ln, **kw)
+
+
+SMALL = synth.Geometry(num_layers=2, hidden=256, heads=4, ffn=512)
+
+
+def _bf16(a):
+    return synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(np.asarray(a, np.float32)))
+
+
+def _dev(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda", dtype)
+
+
+# --------------------------------------------------------------------------- packing
+@pytest.mark.parametrize("lengths", [[17, 40, 7], [1, 2, 127, 128, 129, 1024, 3], [5, 0, 0, 9, 0], [1026, 1]])
+def test_pack_index_bit_exact(lengths):
+    enc = _enc(SMALL, "bf16")
+    cu = torch.from_numpy(synth.cu_seqlens_from_lengths(lengths)).cuda()
+    T = int(sum(lengths))
+    pos, seg = enc.debug_pack_index(cu, T, max(lengths))
+    assert enc.check_status() == 0
+    opos, oseg = O.pack_index(O.cu_seqlens(lengths))
+    assert np.array_equal(pos.cpu().numpy(), opos) and np.array_equal(seg.cpu().numpy(), oseg)
+
+
+@pytest.mark.parametrize("cu", [[1, 5, 9], [0, 6, 4, 9], [0, 4, 8], [0, 3, 9]])
+def test_bad_cu_seqlens_is_reported(cu):
+    enc = _enc(SMALL, "bf16")
+    T = 9
+    pos, seg = enc.debug_pack_index(torch.tensor(cu, dtype=torch.int32, device="cuda"), T, 5)
+    assert enc.check_status() == 3  # ESM_ERR_BAD_CU_SEQLENS
+    assert enc.check_status() == 0  # the check clears the latch
+    assert pos.min().item() >= 0 and seg.min().item() >= 0
+
+
+# --------------------------------------------------------------------------- LayerNorm
+@pytest.mark.parametrize("precision,cols,tol", [("bf16", 1280, 8e-3), ("bf16", 256, 8e-3), ("fp32", 64, 1e-6)])
+def test_layernorm(precision, cols, tol):
+    g = synth.Geometry(1, cols, cols // 64 if precision != "fp32" else 4, 4 * cols)
+    enc = _enc(g, precision)
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal((333, cols)) * 3 + rng.standard_normal((333, 1)) * 2).astype(np.float32)
+    gm = rng.standard_normal(cols).astype(np.float32)
+    bt = rng.standard_normal(cols).astype(np.float32)
+    pdt = torch.float32 if precision == "fp32" else torch.bfloat16
+    if precision != "fp32":
+        gm, bt = _bf16(gm), _bf16(bt)
+    y = torch.empty(333, cols, dtype=pdt, device="cuda")
+    enc.op_layernorm(_dev(x, torch.float32), _dev(gm, pdt), _dev(bt, pdt), y)
+    torch.cuda.synchronize()
+    ref = O.layer_norm(x.astype(np.float64), gm.astype(np.float64), bt.astype(np.float64))
+    assert rel_l2(to_np(y), ref) < tol  # bf16 output rounding: ~2^-9 / sqrt(3) rms
+
+
+# --------------------------------------------------------------------------- GEMMs
+@pytest.mark.parametrize("M", [1, 128, 300, 1000])
+def test_gemm_bias_f32_tcgen05(M):
+    """bf16 x bf16 products are exact in fp32; only the fp32 summation order differs
+    from the float64 reference: rel L2 ~ 1e-7."""
+    enc = _enc(SMALL, "bf16")
+    rng = np.random.default_rng(M)
+    K, N = 320, 512
+    A = _bf16(rng.standard_normal((M, K)))
+    B = _bf16(rng.standard_normal((N, K)))
+    b = _bf16(rng.standard_normal(N))
+    out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    enc.op_gemm("bias_f32", _dev(A, torch.bfloat16), _dev(B, torch.bfloat16), _dev(b, torch.bfloat16), out)
+    assert enc.check_status() == 0
+    ref = A.astype(np.float64) @ B.astype(np.float64).T + b
+    assert rel_l2(to_np(out), ref) < 1e-5
+
+
+def test_gemm_large_k_and_many_tiles():
+    enc = _enc(SMALL, "bf16")
+    rng = np.random.default_rng(5)
+    M, K, N = 1500, 5120, 1280
+    A = _bf16(rng.standard_normal((M, K)))
+    B = _bf16(rng.standard_normal((N, K)) * 0.02)
+    out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    enc.op_gemm("bias_f32", _dev(A, torch.bfloat16), _dev(B, torch.bfloat16), None, out)
+    assert enc.check_status() == 0
+    ref = A.astype(np.float64) @ B.astype(np.float64).T
+    assert rel_l2(to_np(out), ref) < 1e-5
+
+
+def test_gemm_epilogues():
+    g = SMALL
+    enc = _enc(g, "bf16")
+    rng = np.random.default_rng(9)
+    M, d, f = 333, g.hidden, g.ffn
+    A = _bf16(rng.standard_normal((M, d)))
+    Wqkv = _bf16(rng.standard_normal((3 * d, d)) * 0.05)
+    bqkv = _bf16(rng.standard_normal(3 * d) * 0.1)
+    pos = rng.integers(0, 1026, size=M).astype(np.int32)
+    qkv = torch.empty(M, 3 * d, dtype=torch.bfloat16, device="cuda")
+    enc.op_gemm("qkv_rope", _dev(A, torch.bfloat16), _dev(Wqkv, torch.bfloat16), _dev(bqkv, torch.bfloat16), qkv,
+                pos_id=torch.from_numpy(pos).cuda())
+    lin = A.astype(np.float64) @ Wqkv.astype(np.float64).T + bqkv
+    H = g.heads
+    ref = lin.copy()
+    ref[:, :d] = O.rope(lin[:, :d].reshape(M, H, 64), pos).reshape(M, d)
+    ref[:, d:2 * d] = O.rope(lin[:, d:2 * d].reshape(M, H, 64), pos).reshape(M, d)
+    assert rel_l2(to_np(qkv), ref) < 5e-3
+    # GELU
+    W1 = _bf16(rng.standard_normal((f, d)) * 0.05)
+    b1 = _bf16(rng.standard_normal(f) * 0.1)
+    u = torch.empty(M, f, dtype=torch.bfloat16, device="cuda")
+    enc.op_gemm("gelu", _dev(A, torch.bfloat16), _dev(W1, torch.bfloat16), _dev(b1, torch.bfloat16), u)
+    ref = O.gelu(A.astype(np.float64) @ W1.astype(np.float64).T + b1)
+    assert rel_l2(to_np(u), ref) < 5e-3
+    # residual: x += A W^T + b
+    W2 = _bf16(rng.standard_normal((d, f)) * 0.05)
+    b2 = _bf16(rng.standard_normal(d) * 0.1)
+    U = _bf16(rng.standard_normal((M, f)))
+    x0 = rng.standard_normal((M, d)).astype(np.float32)
+    x = _dev(x0, torch.float32)
+    enc.op_gemm("residual", _dev(U, torch.bfloat16), _dev(W2, torch.bfloat16), _dev(b2, torch.bfloat16), x)
+    assert enc.check_status() == 0
+    ref = x0 + U.astype(np.float64) @ W2.astype(np.float64).T + b2
+    assert rel_l2(to_np(x), ref) < 1e-5
+
+
+def test_gemm_fp32_simt():
+    enc = _enc(synth.TINY, "fp32")
+    rng = np.random.default_rng(3)
+    M, K, N = 77, 64, 192
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    b = rng.standard_normal(N).astype(np.float32)
+    out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    enc.op_gemm("bias_f32", _dev(A, torch.float32), _dev(B, torch.float32), _dev(b, torch.float32), out)
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(out), A.astype(np.float64) @ B.T.astype(np.float64) + b) < 1e-6
+
+
+# --------------------------------------------------------------------------- attention
+@pytest.mark.parametrize("lengths", [[1, 2, 63, 64, 65, 127, 128, 129, 200], [1024, 7, 333], [1]])
+def test_attention_bf16(lengths):
+    g = SMALL
+    enc = _enc(g, "bf16")
+    rng = np.random.default_rng(len(lengths))
+    T, d, H = sum(lengths), g.hidden, g.heads
+    qkv = _bf16(rng.standard_normal((T, 3 * d)) * 1.5)
+    o = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    cu = torch.from_numpy(synth.cu_seqlens_from_lengths(lengths)).cuda()
+    enc.op_attention(_dev(qkv, torch.bfloat16), cu, max(lengths), o)
+    assert enc.check_status() == 0
+    got = to_np(o)
+    c = O.cu_seqlens(lengths)
+    q64 = qkv.astype(np.float64)
+    for i, L in enumerate(lengths):
+        s = slice(c[i], c[i + 1])
+        ref = O.attention(q64[s, :d].reshape(L, H, 64), q64[s, d:2 * d].reshape(L, H, 64),
+                          q64[s, 2 * d:].reshape(L, H, 64)).reshape(L, d)
+        # P and O rounded to bf16: ~2^-9 relative each
+        assert rel_l2(got[s], ref) < 1e-2, (i, L)
+
+
+def test_attention_fp32():
+    g = synth.TINY
+    enc = _enc(g, "fp32")
+    lengths = [17, 40, 7]
+    rng = np.random.default_rng(1)
+    T, d, H = sum(lengths), g.hidden, g.heads
+    qkv = rng.standard_normal((T, 3 * d)).astype(np.float32)
+    o = torch.empty(T, d, dtype=torch.float32, device="cuda")
+    cu = torch.from_numpy(synth.cu_seqlens_from_lengths(lengths)).cuda()
+    enc.op_attention(_dev(qkv, torch.float32), cu, 40, o)
+    torch.cuda.synchronize()
+    got = to_np(o)
+    c = O.cu_seqlens(lengths)
+    dh = d // H
+    q64 = qkv.astype(np.float64)
+    for i, L in enumerate(lengths):
+        s = slice(c[i], c[i + 1])
+        ref = O.attention(q64[s, :d].reshape(L, H, dh), q64[s, d:2 * d].reshape(L, H, dh),
+                          q64[s, 2 * d:].reshape(L, H, dh)).reshape(L, d)
+        assert rel_l2(got[s], ref) < 1e-6
+
+
+# --------------------------------------------------------------------------- forward
+def _run_packed(g, precision, w, tokens, lengths, final_ln=True):
+    from transformer_esm_layer_gb300.binding import DeviceWeights, packed_inputs
+    enc = _enc(g, precision, final_ln)
+    dw = DeviceWeights(w, precision)
+    tok, cu = packed_inputs(tokens, lengths)
+    out = enc.forward(dw, tok, cu, max(lengths))
+    enc.check()
+    return enc, dw, to_np(out)
+
+
+def test_forward_tiny_fp32_config():
+    """The tiny fp32 workload: 2 layers, hidden 64, 4 heads, lengths 17/40/7."""
+    wl = synth.make_workload("tiny_fp32")
+    g = wl.geometry
+    w = synth.model_weights(g, wl.seed, "fp32")
+    tok = synth.workload_tokens(wl)
+    _, _, got = _run_packed(g, "fp32", w, tok, wl.lengths)
+    ref = O.encode_packed(tok, O.cu_seqlens(wl.lengths), w, g.heads, final_ln=True)
+    ref = np.concatenate([ref[i] for i in range(len(wl.lengths))])
+    assert rel_l2(got, ref) < 1e-4
+
+
+def test_forward_bf16_two_layers_ragged():
+    g = synth.Geometry(num_layers=2, hidden=1280, heads=20, ffn=5120)
+    lengths = [1, 2, 130, 64, 257, 1024, 33]
+    w = synth.model_weights(g, 21, "bf16", ln_random=True)
+    tok = synth.tokens_for_lengths(np.random.default_rng(21), lengths)
+    _, _, got = _run_packed(g, "bf16", w, tok, lengths)
+    ref = O.encode_packed(tok, O.cu_seqlens(lengths), w, g.heads, final_ln=True)
+    ref = np.concatenate([ref[i] for i in range(len(lengths))])
+    assert rel_l2(got, ref) < 1e-2
+
+
+def test_forward_single_layer_workload():
+    """One ESM-2 650M layer, 16 log-normal sequences, no final LN."""
+    wl = synth.make_workload("layer650m")
+    g = wl.geometry
+    w = synth.model_weights(g, wl.seed, "bf16")
+    tok = synth.workload_tokens(wl)
+    _, _, got = _run_packed(g, "bf16", w, tok, wl.lengths, final_ln=False)
+    c = O.cu_seqlens(wl.lengths)
+    ref = O.encode_packed(tok, c, w, g.heads, final_ln=False)
+    for i in range(len(wl.lengths)):
+        assert rel_l2(got[c[i]:c[i + 1]], ref[i]) < 1e-2, i
+
+
+def test_packed_equals_each_sequence_alone_bitwise():
+    g = synth.Geometry(num_layers=2, hidden=1280, heads=20, ffn=5120)
+    lengths = [70, 1, 200, 129]
+    w = synth.model_weights(g, 22, "bf16")
+    tok = synth.tokens_for_lengths(np.random.default_rng(22), lengths)
+    enc, dw, got = _run_packed(g, "bf16", w, tok, lengths)
+    from transformer_esm_layer_gb300.binding import packed_inputs
+    c = O.cu_seqlens(lengths)
+    for i, L in enumerate(lengths):
+        t1, cu1 = packed_inputs(tok[c[i]:c[i + 1]], [L])
+        alone = to_np(enc.forward(dw, t1, cu1, L))
+        assert np.array_equal(alone, got[c[i]:c[i + 1]]), i
+
+
+def test_padded_equals_packed():
+    g = synth.Geometry(num_layers=2, hidden=1280, heads=20, ffn=5120)
+    lengths = [70, 1, 200, 129]
+    S = 256
+    w = synth.model_weights(g, 23, "bf16")
+    tok = synth.tokens_for_lengths(np.random.default_rng(23), lengths)
+    enc, dw, packed = _run_packed(g, "bf16", w, tok, lengths)
+    padded = torch.from_numpy(synth.pad_tokens(tok, lengths, S)).cuda()
+    lens = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    out = to_np(enc.forward_padded(dw, padded, lens, check=True))
+    c = O.cu_seqlens(lengths)
+    for b, L in enumerate(lengths):
+        assert rel_l2(out[b, :L], packed[c[b]:c[b + 1]]) < 1e-3, b
+        assert np.all(out[b, L:] == 0)
+    ref = O.encode_padded(padded.cpu().numpy(), lengths, w, g.heads)
+    for b, L in enumerate(lengths):
+        assert rel_l2(out[b, :L], ref[b][:L]) < 1e-2
+
+
+def test_full_650m_workload_sampled_sequences():
+    """The full 33-layer 650M encoder on 16384 packed tokens (seed 2), in the launch
+    configuration the benchmark times; the oracle checks the shortest, the longest and a
+    middle sequence (packed sequences are independent, so each is exact on its own)."""
+    wl = synth.make_workload("esm650m")
+    g = wl.geometry
+    w = synth.model_weights(g, wl.seed, "bf16")
+    tok = synth.workload_tokens(wl)
+    _, _, got = _run_packed(g, "bf16", w, tok, wl.lengths)
+    assert np.isfinite(got).all()
+    order = np.argsort(wl.lengths)
+    pick = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    c = O.cu_seqlens(wl.lengths)
+    ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, seq_subset=pick)
+    for i in pick:
+        assert rel_l2(got[c[i]:c[i + 1]], ref[i]) < 1e-2, (i, wl.lengths[i])
+
+
+# --------------------------------------------------------------------------- errors
+def test_token_out_of_range_reported():
+    g = SMALL
+    enc = _enc(g, "bf16")
+    from transformer_esm_layer_gb300.binding import DeviceWeights, packed_inputs
+    dw = DeviceWeights(synth.model_weights(g, 1, "bf16"), "bf16")
+    tok, cu = packed_inputs(np.array([0, 5, 40, 2], np.int32), [4])
+    enc.forward(dw, tok, cu, 4)
+    assert enc.check_status() == 4  # ESM_ERR_TOKEN_RANGE
+
+
+def test_host_side_argument_errors():
+    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmError, packed_inputs
+    g = SMALL
+    enc = _enc(g, "bf16")
+    dw = DeviceWeights(synth.model_weights(g, 1, "bf16"), "bf16")
+    tok, cu = packed_inputs(np.array([0, 5, 6, 2], np.int32), [4])
+    small_ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(EsmError) as e:
+        enc.forward(dw, tok, cu, 4, workspace=small_ws)
+    assert e.value.status == 5
+    with pytest.raises(EsmError) as e:
+        enc.forward(dw, tok, cu, 2000)  # max_seqlen above max_positions
+    assert e.value.status == 1
+    with pytest.raises(EsmError) as e:
+        _enc(synth.Geometry(1, 96, 3, 256), "bf16")  # head_dim 32 is not a bf16 geometry
+    assert e.value.status == 2

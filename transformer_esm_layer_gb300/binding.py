@@ -1,0 +1,322 @@
+"""Thin ctypes binding of the C ABI in include/esm_encoder.h.
+
+Argument marshalling only: every step of the forward runs in the CUDA library.  torch is
+used for device memory and streams.  Loading fails loudly when the library has not been
+built; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libesm_encoder.so")
+
+ESM_OK = 0
+STATUS_NAMES = {0: "ESM_OK", 1: "ESM_ERR_INVALID_ARG", 2: "ESM_ERR_UNSUPPORTED", 3: "ESM_ERR_BAD_CU_SEQLENS",
+                4: "ESM_ERR_TOKEN_RANGE", 5: "ESM_ERR_WORKSPACE", 6: "ESM_ERR_CUDA", 7: "ESM_ERR_TIMEOUT"}
+PRECISIONS = {"fp32": 0, "bf16": 1, "fp8": 2}
+EPILOGUES = {"bias_f32": 0, "qkv_rope": 1, "residual": 2, "gelu": 3}
+
+# Every symbol the header declares (checked by the tests).
+EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_size", "esm_encoder_forward",
+           "esm_encoder_forward_host", "esm_encoder_forward_padded", "esm_encoder_check",
+           "esm_encoder_debug_pack_index", "esm_op_layernorm", "esm_op_gemm", "esm_op_attention",
+           "esm_encoder_get_fp8_state", "esm_encoder_set_fp8_state", "esm_encoder_set_profiling",
+           "esm_encoder_get_profile", "esm_status_string")
+PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
+
+
+class EsmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class EsmConfig(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("heads", ctypes.c_int),
+                ("ffn", ctypes.c_int), ("vocab", ctypes.c_int), ("max_positions", ctypes.c_int),
+                ("ln_eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("emb_scale", ctypes.c_float),
+                ("final_ln", ctypes.c_int), ("precision", ctypes.c_int), ("amax_history_len", ctypes.c_int)]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class EsmProfile(ctypes.Structure):
+    _fields_ = [("ms", ctypes.c_double * 8), ("launches", ctypes.c_longlong * 8), ("total_launches", ctypes.c_longlong)]
+
+
+class EsmWeights(ctypes.Structure):
+    _fields_ = [("emb", ctypes.c_void_p)] + \
+        [(n, _PP) for n in ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b",
+                            "w_1", "b_1", "w_2", "b_2")] + \
+        [("lnf_g", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run python -m transformer_esm_layer_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "esm_encoder_create": (i32, [ctypes.POINTER(EsmConfig), ctypes.POINTER(vp)]),
+        "esm_encoder_destroy": (None, [vp]),
+        "esm_encoder_workspace_size": (i32, [vp, i32, i32, ctypes.POINTER(sz)]),
+        "esm_encoder_forward": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, i32, vp, vp, sz, vp]),
+        "esm_encoder_forward_host": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, i32, vp, vp, sz, vp]),
+        "esm_encoder_forward_padded": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, vp, vp, sz, vp]),
+        "esm_encoder_check": (i32, [vp, vp]),
+        "esm_encoder_debug_pack_index": (i32, [vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]),
+        "esm_op_layernorm": (i32, [vp, vp, vp, vp, vp, i32, i32, vp]),
+        "esm_op_gemm": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
+        "esm_op_attention": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, sz, vp]),
+        "esm_encoder_get_fp8_state": (i32, [vp, ctypes.POINTER(ctypes.c_float), sz]),
+        "esm_encoder_set_fp8_state": (i32, [vp, ctypes.POINTER(ctypes.c_float), sz]),
+        "esm_encoder_set_profiling": (i32, [vp, i32]),
+        "esm_encoder_get_profile": (i32, [vp, ctypes.POINTER(EsmProfile), i32]),
+        "esm_status_string": (ctypes.c_char_p, [i32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+class DeviceWeights:
+    """Weights on the device in the handle's parameter dtype, plus the esm_weights struct.
+
+    ``w`` is the dict returned by synth.model_weights (float32 arrays)."""
+
+    def __init__(self, w: Dict, precision: str, device="cuda"):
+        import torch
+        dt = torch.float32 if precision == "fp32" else torch.bfloat16
+        to = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device=device, dtype=dt)
+        self.emb = to(w["emb"])
+        self.layers = [{k: to(v) for k, v in wl.items()} for wl in w["layers"]]
+        self.lnf_g = to(w["lnf_g"])
+        self.lnf_b = to(w["lnf_b"])
+        self._keep = []
+        n = len(self.layers)
+        st = EsmWeights()
+        st.emb = self.emb.data_ptr()
+        for name in ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_1", "b_1", "w_2", "b_2"):
+            arr = (ctypes.c_void_p * max(n, 1))(*[l[name].data_ptr() for l in self.layers])
+            self._keep.append(arr)
+            setattr(st, name, ctypes.cast(arr, _PP))
+        st.lnf_g = self.lnf_g.data_ptr()
+        st.lnf_b = self.lnf_b.data_ptr()
+        self.struct = st
+
+
+class EsmEncoder:
+    """One esm_encoder handle (the esm_encoder_* calls with their own names)."""
+
+    def __init__(self, num_layers: int, hidden: int, heads: int, ffn: int, vocab: int = 33,
+                 max_positions: int = 1026, precision: str = "bf16", final_ln: bool = True,
+                 ln_eps: float = 1e-5, rope_base: float = 10000.0, emb_scale: float = 1.0,
+                 amax_history_len: int = 16):
+        self.lib = load_library()
+        self.cfg = EsmConfig(num_layers, hidden, heads, ffn, vocab, max_positions, ln_eps, rope_base, emb_scale,
+                             int(final_ln), PRECISIONS[precision], amax_history_len)
+        self.precision = precision
+        self.hidden = hidden
+        self.num_layers = num_layers
+        self.amax_history_len = amax_history_len
+        h = ctypes.c_void_p()
+        self._raise(self.lib.esm_encoder_create(ctypes.byref(self.cfg), ctypes.byref(h)), "esm_encoder_create")
+        self.handle = h
+
+    @classmethod
+    def from_geometry(cls, g, precision: str, final_ln: bool = True, **kw):
+        return cls(g.num_layers, g.hidden, g.heads, g.ffn, g.vocab, g.max_positions, precision, final_ln, **kw)
+
+    @staticmethod
+    def _raise(st: int, where: str):
+        if st != ESM_OK:
+            raise EsmError(st, where)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.esm_encoder_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------ buffers
+    @property
+    def out_dtype(self):
+        import torch
+        return torch.float32 if self.precision == "fp32" else torch.bfloat16
+
+    def workspace_size(self, max_tokens: int, max_seqs: int) -> int:
+        n = ctypes.c_size_t()
+        self._raise(self.lib.esm_encoder_workspace_size(self.handle, max_tokens, max_seqs, ctypes.byref(n)),
+                    "esm_encoder_workspace_size")
+        return n.value
+
+    def workspace(self, max_tokens: int, max_seqs: int, device="cuda"):
+        import torch
+        return torch.empty(self.workspace_size(max_tokens, max_seqs), dtype=torch.uint8, device=device)
+
+    # ------------------------------------------------------------------ calls
+    def forward(self, weights: DeviceWeights, token_ids, cu_seqlens, max_seqlen: int, out=None, workspace=None,
+                stream=None, check: bool = False):
+        import torch
+        T = token_ids.numel()
+        B = cu_seqlens.numel() - 1
+        if out is None:
+            out = torch.empty(T, self.hidden, dtype=self.out_dtype, device=token_ids.device)
+        if workspace is None:
+            workspace = self.workspace(T, B, token_ids.device)
+        st = self.lib.esm_encoder_forward(self.handle, ctypes.byref(weights.struct), _ptr(token_ids),
+                                          _ptr(cu_seqlens), B, T, int(max_seqlen), _ptr(out), _ptr(workspace),
+                                          workspace.numel(), _stream_ptr(stream))
+        self._raise(st, "esm_encoder_forward")
+        if check:
+            self.check(stream)
+        return out
+
+    def forward_host(self, weights: DeviceWeights, token_ids: np.ndarray, cu_seqlens: np.ndarray, max_seqlen: int,
+                     out: np.ndarray, workspace, stream=None):
+        """Host buffers in and out (numpy arrays, or pinned torch CPU tensors via .numpy())."""
+        T = int(token_ids.size)
+        B = int(cu_seqlens.size) - 1
+        st = self.lib.esm_encoder_forward_host(self.handle, ctypes.byref(weights.struct),
+                                               token_ids.ctypes.data, cu_seqlens.ctypes.data, B, T, int(max_seqlen),
+                                               out.ctypes.data, _ptr(workspace), workspace.numel(),
+                                               _stream_ptr(stream))
+        self._raise(st, "esm_encoder_forward_host")
+        return out
+
+    def forward_padded(self, weights: DeviceWeights, token_ids, seq_lens, out=None, workspace=None, stream=None,
+                       check: bool = False):
+        import torch
+        B, S = token_ids.shape
+        if out is None:
+            out = torch.empty(B, S, self.hidden, dtype=self.out_dtype, device=token_ids.device)
+        if workspace is None:
+            workspace = self.workspace(B * S, B, token_ids.device)
+        st = self.lib.esm_encoder_forward_padded(self.handle, ctypes.byref(weights.struct), _ptr(token_ids),
+                                                 _ptr(seq_lens), B, S, _ptr(out), _ptr(workspace), workspace.numel(),
+                                                 _stream_ptr(stream))
+        self._raise(st, "esm_encoder_forward_padded")
+        if check:
+            self.check(stream)
+        return out
+
+    def check(self, stream=None) -> int:
+        st = self.lib.esm_encoder_check(self.handle, _stream_ptr(stream))
+        self._raise(st, "esm_encoder_check")
+        return st
+
+    def check_status(self, stream=None) -> int:
+        """Like check() but returns the status instead of raising."""
+        return self.lib.esm_encoder_check(self.handle, _stream_ptr(stream))
+
+    def debug_pack_index(self, cu_seqlens, total_tokens: int, max_seqlen: int, workspace=None, stream=None):
+        import torch
+        B = cu_seqlens.numel() - 1
+        pos = torch.empty(max(total_tokens, 1), dtype=torch.int32, device=cu_seqlens.device)
+        seg = torch.empty_like(pos)
+        if workspace is None:
+            workspace = self.workspace(total_tokens, B, cu_seqlens.device)
+        st = self.lib.esm_encoder_debug_pack_index(self.handle, _ptr(cu_seqlens), B, total_tokens, int(max_seqlen),
+                                                   _ptr(pos), _ptr(seg), _ptr(workspace), workspace.numel(),
+                                                   _stream_ptr(stream))
+        self._raise(st, "esm_encoder_debug_pack_index")
+        return pos[:total_tokens], seg[:total_tokens]
+
+    def op_layernorm(self, x, gamma, beta, y, stream=None):
+        rows, cols = x.shape
+        self._raise(self.lib.esm_op_layernorm(self.handle, _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, cols,
+                                              _stream_ptr(stream)), "esm_op_layernorm")
+        return y
+
+    def op_gemm(self, epi: str, A, B, bias, out, pos_id=None, stream=None):
+        M, K = A.shape
+        N = B.shape[0]
+        self._raise(self.lib.esm_op_gemm(self.handle, EPILOGUES[epi], _ptr(A), _ptr(B), _ptr(bias), _ptr(out),
+                                         _ptr(pos_id), M, N, K, _stream_ptr(stream)), "esm_op_gemm")
+        return out
+
+    def op_attention(self, qkv, cu_seqlens, max_seqlen: int, o, workspace=None, stream=None):
+        T = qkv.shape[0]
+        B = cu_seqlens.numel() - 1
+        if workspace is None:
+            workspace = self.workspace(T, B, qkv.device)
+        self._raise(self.lib.esm_op_attention(self.handle, _ptr(qkv), _ptr(cu_seqlens), B, T, int(max_seqlen),
+                                              _ptr(o), _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+                    "esm_op_attention")
+        return o
+
+    def set_profiling(self, enable: bool):
+        self._raise(self.lib.esm_encoder_set_profiling(self.handle, int(enable)), "esm_encoder_set_profiling")
+
+    def get_profile(self, reset: bool = True) -> Dict:
+        """{class: {"ms": summed device ms, "launches": n}} plus "total_launches"."""
+        p = EsmProfile()
+        self._raise(self.lib.esm_encoder_get_profile(self.handle, ctypes.byref(p), int(reset)),
+                    "esm_encoder_get_profile")
+        out = {name: {"ms": p.ms[i], "launches": int(p.launches[i])} for i, name in enumerate(PROFILE_CLASSES)}
+        out["total_launches"] = int(p.total_launches)
+        return out
+
+    def fp8_state_size(self) -> int:
+        return self.num_layers * 8 * (1 + self.amax_history_len)
+
+    def get_fp8_state(self) -> np.ndarray:
+        buf = np.zeros(self.fp8_state_size(), dtype=np.float32)
+        self._raise(self.lib.esm_encoder_get_fp8_state(self.handle, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                                       buf.size), "esm_encoder_get_fp8_state")
+        return buf
+
+    def set_fp8_state(self, buf: np.ndarray):
+        buf = np.ascontiguousarray(buf, dtype=np.float32)
+        self._raise(self.lib.esm_encoder_set_fp8_state(self.handle, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                                       buf.size), "esm_encoder_set_fp8_state")
+
+    def fp8_scales(self, buf: Optional[np.ndarray] = None) -> np.ndarray:
+        """[num_layers, 8] scales from a state buffer (tensor order x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2)."""
+        buf = self.get_fp8_state() if buf is None else buf
+        return buf[:self.num_layers * 8].reshape(self.num_layers, 8)
+
+    def fp8_history(self, buf: Optional[np.ndarray] = None) -> np.ndarray:
+        buf = self.get_fp8_state() if buf is None else buf
+        return buf[self.num_layers * 8:].reshape(self.num_layers, 8, self.amax_history_len)
+
+
+def packed_inputs(tokens: np.ndarray, lengths: Sequence[int], device="cuda"):
+    """Device token ids and cu_seqlens (int32) for a packed batch."""
+    import torch
+    from .synth import cu_seqlens_from_lengths
+    tok = torch.from_numpy(np.ascontiguousarray(tokens, dtype=np.int32)).to(device)
+    cu = torch.from_numpy(cu_seqlens_from_lengths(lengths)).to(device)
+    return tok, cu

@@ -1,0 +1,646 @@
+// Host side of the C ABI declared in include/esm_encoder.h: handle, workspace layout,
+// TMA descriptor cache and the per-layer launch sequence of the packed ESM-2 forward
+// (section 3.2 of the hotelren.com guide: embedding, then every layer over cu_seqlens).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <unordered_map>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace esm;
+
+namespace {
+
+constexpr int kNumFp8Tensors = 8;  // x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2
+enum Fp8Slot { X_QKV = 0, W_QKV, X_O, W_O, X_1, W_1, X_2, W_2 };
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+struct MapKey {
+  uintptr_t ptr;
+  uint64_t rows, cols;
+  uint32_t box_rows, elem;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_rows == o.box_rows && elem == o.elem;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<uintptr_t>()(k.ptr);
+    h ^= std::hash<uint64_t>()(k.rows * 1000003ull + k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    h ^= std::hash<uint64_t>()((uint64_t)k.box_rows << 8 | k.elem) + (h << 6) + (h >> 2);
+    return h;
+  }
+};
+
+struct WsLayout {
+  size_t pos, seg, seg_start, seg_qlen, seg_klen, work, work_count, x, y, qkv, o, u, wq, stage_tok, stage_cu, total;
+  int max_items;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+struct esm_encoder {
+  esm_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  unsigned* d_err = nullptr;     // device error word
+  float2* d_rope = nullptr;      // [max_positions][32] (cos, sin)
+  float* d_fp8 = nullptr;        // scales [L*8] | history [L*8*len] | amax [L*8]
+  size_t fp8_floats = 0;
+  std::unordered_map<MapKey, CUtensorMap, MapKeyHash> maps;
+  // measurement hooks
+  bool profiling = false;
+  long long launches[ESM_PROFILE_CLASSES] = {};
+  long long total_launches = 0;
+  struct Pending { int cls; cudaEvent_t e0, e1; };
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> event_pool;
+  double ms[ESM_PROFILE_CLASSES] = {};
+
+  cudaEvent_t take_event() {
+    if (!event_pool.empty()) {
+      cudaEvent_t e = event_pool.back();
+      event_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  // Fold finished event pairs into ms[] (synchronises on each pair's end event).
+  void drain_events() {
+    for (auto& p : pending) {
+      float t = 0.f;
+      if (cudaEventSynchronize(p.e1) == cudaSuccess && cudaEventElapsedTime(&t, p.e0, p.e1) == cudaSuccess)
+        ms[p.cls] += t;
+      event_pool.push_back(p.e0);
+      event_pool.push_back(p.e1);
+    }
+    pending.clear();
+  }
+
+  bool bf16_params() const { return cfg.precision != ESM_FP32; }
+  Act act() const { return cfg.precision == ESM_FP32 ? Act::F32 : Act::BF16; }
+  size_t act_bytes() const { return cfg.precision == ESM_FP32 ? 4 : 2; }
+  float* fp8_scale() const { return d_fp8; }
+  float* fp8_hist() const { return d_fp8 + (size_t)cfg.num_layers * kNumFp8Tensors; }
+  float* fp8_amax() const {
+    return d_fp8 + (size_t)cfg.num_layers * kNumFp8Tensors * (1 + cfg.amax_history_len);
+  }
+
+  WsLayout layout(int Tm, int Bm) const {
+    WsLayout L{};
+    const size_t d = cfg.hidden, f = cfg.ffn, T = Tm > 0 ? Tm : 1, B = Bm > 0 ? Bm : 1;
+    L.max_items = (int)((T + kAttnQTile - 1) / kAttnQTile + B);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+      size_t o = off;
+      off += align256(bytes);
+      return o;
+    };
+    L.pos = take(4 * T);
+    L.seg = take(4 * T);
+    L.seg_start = take(4 * B);
+    L.seg_qlen = take(4 * B);
+    L.seg_klen = take(4 * B);
+    L.work = take(8 * (size_t)L.max_items);
+    L.work_count = take(16);
+    L.x = take(4 * T * d);
+    L.y = take(act_bytes() * T * d);
+    L.qkv = take(act_bytes() * T * 3 * d);
+    L.o = take(act_bytes() * T * d);
+    L.u = take(act_bytes() * T * f);
+    L.wq = cfg.precision == ESM_FP8_E4M3 ? take(3 * d * d + d * d + 2 * d * f) : take(0);
+    L.stage_tok = take(4 * T);
+    L.stage_cu = take(4 * (B + 1));
+    L.total = off;
+    return L;
+  }
+
+  // Cached 2-D tensor map over a row-major [rows, cols] matrix; the box is 128 bytes of
+  // columns by box_rows rows with the 128-byte swizzle (one tcgen05 K-slice).
+  const CUtensorMap* map(const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t elem) {
+    MapKey k{reinterpret_cast<uintptr_t>(ptr), rows, cols, box_rows, elem};
+    auto it = maps.find(k);
+    if (it != maps.end()) return &it->second;
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return nullptr;
+    if (maps.size() > 4096) maps.clear();
+    CUtensorMap m;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * elem};
+    cuuint32_t box[2] = {128u / elem, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(&m, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return nullptr;
+    return &maps.emplace(k, m).first->second;
+  }
+};
+
+namespace {
+
+enum ProfClass { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_FC1 = 3, P_FC2 = 4, P_LN = 5, P_OTHER = 6 };
+
+// Counts the launches of one call site and, with profiling on, brackets them with events
+// recorded on the launch stream.
+struct ProfScope {
+  esm_encoder* h;
+  int cls;
+  cudaStream_t st;
+  cudaEvent_t e0 = nullptr;
+  ProfScope(esm_encoder* h_, int cls_, cudaStream_t st_, int n) : h(h_), cls(cls_), st(st_) {
+    h->launches[cls] += n;
+    h->total_launches += n;
+    if (h->profiling) {
+      e0 = h->take_event();
+      cudaEventRecord(e0, st);
+    }
+  }
+  ~ProfScope() {
+    if (h->profiling && e0) {
+      cudaEvent_t e1 = h->take_event();
+      cudaEventRecord(e1, st);
+      h->pending.push_back({cls, e0, e1});
+      if (h->pending.size() > 20000) h->drain_events();
+    }
+  }
+};
+#define PROF(h, cls, st, n, expr) \
+  do {                             \
+    ProfScope _ps(h, cls, st, n);  \
+    expr;                          \
+  } while (0)
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+PackBuffers pack_buffers(void* ws, const WsLayout& L) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  PackBuffers pb;
+  pb.pos_id = reinterpret_cast<int32_t*>(b + L.pos);
+  pb.seg_id = reinterpret_cast<int32_t*>(b + L.seg);
+  pb.seg_start = reinterpret_cast<int32_t*>(b + L.seg_start);
+  pb.seg_qlen = reinterpret_cast<int32_t*>(b + L.seg_qlen);
+  pb.seg_klen = reinterpret_cast<int32_t*>(b + L.seg_klen);
+  pb.work = reinterpret_cast<int32_t*>(b + L.work);
+  pb.work_count = reinterpret_cast<int32_t*>(b + L.work_count);
+  return pb;
+}
+
+esm_status check_ws(const esm_encoder* h, int T, int B, void* ws, size_t bytes, WsLayout* out) {
+  if (ws == nullptr || !aligned(ws, 256)) return ESM_ERR_WORKSPACE;
+  *out = h->layout(T, B);
+  if (bytes < out->total) return ESM_ERR_WORKSPACE;
+  return ESM_OK;
+}
+
+esm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ESM_OK : ESM_ERR_CUDA; }
+
+bool weights_ok(const esm_encoder* h, const esm_weights* w) {
+  if (!w || !w->emb) return false;
+  const void* const* arrs[] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o, w->b_o,
+                               w->ln2_g, w->ln2_b, w->w_1,   w->b_1,   w->w_2, w->b_2};
+  for (auto a : arrs) {
+    if (!a) return false;
+    for (int l = 0; l < h->cfg.num_layers; ++l)
+      if (!a[l] || !aligned(a[l], 16)) return false;
+  }
+  if (h->cfg.final_ln && (!w->lnf_g || !w->lnf_b)) return false;
+  return true;
+}
+
+// One GEMM of a layer.  A: activation [M, K]; B: weight [N, K].
+esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, const void* B, const void* bias, void* out,
+                    const int32_t* pos_id, int M, int N, int K, bool fp8, Act out_act, const float* a_scale,
+                    const float* b_scale, const float* o_scale, float* o_amax, cudaStream_t st) {
+  EpiArgs ea{};
+  ea.bias = bias;
+  ea.bias_f32 = !h->bf16_params();
+  ea.out = out;
+  ea.pos_id = pos_id;
+  ea.rope = h->d_rope;
+  ea.rope_cols = 2 * h->cfg.hidden;
+  ea.head_dim = h->cfg.hidden / h->cfg.heads;
+  ea.max_pos = h->cfg.max_positions;
+  ea.a_scale = a_scale;
+  ea.b_scale = b_scale;
+  ea.o_scale = o_scale;
+  ea.o_amax = o_amax;
+  if (M <= 0) return ESM_OK;
+  if (h->cfg.precision == ESM_FP32) {
+    PROF(h, cls, st, epi == ESM_EPI_QKV_ROPE ? 2 : 1,
+         launch_gemm_f32(epi, static_cast<const float*>(A), static_cast<const float*>(B), M, N, K, ea, st));
+    return cuda_status(cudaGetLastError());
+  }
+  const uint32_t elem = fp8 ? 1 : 2;
+  const CUtensorMap* ma = h->map(A, (uint64_t)M, (uint64_t)K, 128, elem);
+  const CUtensorMap* mb = h->map(B, (uint64_t)N, (uint64_t)K, 256, elem);
+  if (!ma || !mb) return ESM_ERR_CUDA;
+  cudaError_t e;
+  PROF(h, cls, st, 1, e = launch_gemm_tc(epi, fp8, out_act, ma, mb, M, N, K, ea, h->num_sms, h->d_err, st));
+  return cuda_status(e);
+}
+
+// The layer stack over an already indexed batch (pack buffers filled, x = embedding).
+esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items, const WsLayout& L, void* ws,
+                      void* out, bool padded, cudaStream_t st) {
+  const esm_config& c = h->cfg;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  PackBuffers pb = pack_buffers(ws, L);
+  float* x = reinterpret_cast<float*>(b + L.x);
+  void* y = b + L.y;
+  void* qkv = b + L.qkv;
+  void* o = b + L.o;
+  void* u = b + L.u;
+  const int d = c.hidden, f = c.ffn, H = c.heads;
+  const bool fp8 = c.precision == ESM_FP8_E4M3;
+  const bool pf32 = !h->bf16_params();
+  const Act act = h->act();
+  esm_status s;
+  for (int l = 0; l < c.num_layers; ++l) {
+    float* sc = h->fp8_scale() + (size_t)l * kNumFp8Tensors;
+    float* am = h->fp8_amax() + (size_t)l * kNumFp8Tensors;
+    uint8_t* wq_qkv = b + L.wq;
+    uint8_t* wq_o = wq_qkv + (size_t)3 * d * d;
+    uint8_t* wq_1 = wq_o + (size_t)d * d;
+    uint8_t* wq_2 = wq_1 + (size_t)f * d;
+    if (fp8) {
+      ProfScope _ps(h, P_OTHER, st, 4);
+      launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(w->w_qkv[l]), wq_qkv, (size_t)3 * d * d, sc + W_QKV,
+                           am + W_QKV, st);
+      launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(w->w_o[l]), wq_o, (size_t)d * d, sc + W_O, am + W_O, st);
+      launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(w->w_1[l]), wq_1, (size_t)f * d, sc + W_1, am + W_1, st);
+      launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(w->w_2[l]), wq_2, (size_t)d * f, sc + W_2, am + W_2, st);
+    }
+    // ---- attention block
+    PROF(h, P_LN, st, 1,
+         launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_QKV,
+                          am + X_QKV, nullptr, nullptr, nullptr, st));
+    s = run_gemm(h, P_QKV, ESM_EPI_QKV_ROPE, y, fp8 ? (const void*)wq_qkv : w->w_qkv[l], w->b_qkv[l], qkv, pb.pos_id, T,
+                 3 * d, d, fp8, act, sc + X_QKV, sc + W_QKV, nullptr, nullptr, st);
+    if (s != ESM_OK) return s;
+    {
+      ProfScope _ps(h, P_ATTN, st, 1);
+      if (c.precision == ESM_FP32)
+        launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(o), d, H, T, pb, st);
+      else if (fp8)
+        launch_attention_bf16_to_e4m3(static_cast<const __nv_bfloat16*>(qkv), static_cast<uint8_t*>(o), d, H,
+                                      max_items, pb, sc + X_O, am + X_O, st);
+      else
+        launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), d, H,
+                              max_items, pb, st);
+    }
+    s = run_gemm(h, P_OPROJ, ESM_EPI_RESIDUAL, o, fp8 ? (const void*)wq_o : w->w_o[l], w->b_o[l], x, nullptr, T, d, d, fp8,
+                 Act::F32, sc + X_O, sc + W_O, nullptr, nullptr, st);
+    if (s != ESM_OK) return s;
+    // ---- MLP block
+    PROF(h, P_LN, st, 1,
+         launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_1,
+                          am + X_1, nullptr, nullptr, nullptr, st));
+    s = run_gemm(h, P_FC1, ESM_EPI_GELU, y, fp8 ? (const void*)wq_1 : w->w_1[l], w->b_1[l], u, nullptr, T, f, d, fp8,
+                 fp8 ? Act::E4M3 : act, sc + X_1, sc + W_1, sc + X_2, am + X_2, st);
+    if (s != ESM_OK) return s;
+    s = run_gemm(h, P_FC2, ESM_EPI_RESIDUAL, u, fp8 ? (const void*)wq_2 : w->w_2[l], w->b_2[l], x, nullptr, T, d, f, fp8,
+                 Act::F32, sc + X_2, sc + W_2, nullptr, nullptr, st);
+    if (s != ESM_OK) return s;
+  }
+  const int32_t* vp = padded ? pb.pos_id : nullptr;
+  const int32_t* vs = padded ? pb.seg_id : nullptr;
+  const int32_t* vk = padded ? pb.seg_klen : nullptr;
+  if (c.final_ln)
+    PROF(h, P_LN, st, 1,
+         launch_layernorm(x, w->lnf_g, w->lnf_b, pf32, out, act, T, d, c.ln_eps, nullptr, nullptr, vp, vs, vk, st));
+  else
+    PROF(h, P_OTHER, st, 1, launch_copy_out(x, out, act, T, d, vp, vs, vk, st));
+  if (fp8)
+    PROF(h, P_OTHER, st, 1, launch_fp8_update(h->fp8_scale(), h->fp8_hist(), h->fp8_amax(), c.num_layers * kNumFp8Tensors,
+                      c.amax_history_len, st));
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status forward_impl(esm_encoder* h, const esm_weights* w, const int32_t* tok, const int32_t* cu, int B, int T,
+                        int max_seqlen, void* out, void* ws, size_t ws_bytes, cudaStream_t st) {
+  WsLayout L;
+  esm_status s = check_ws(h, T, B, ws, ws_bytes, &L);
+  if (s != ESM_OK) return s;
+  PackBuffers pb = pack_buffers(ws, L);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(pb.pos_id, 0, 4 * (size_t)T, st) != cudaSuccess) return ESM_ERR_CUDA;
+  if (cudaMemsetAsync(pb.seg_id, 0, 4 * (size_t)T, st) != cudaSuccess) return ESM_ERR_CUDA;
+  {
+    ProfScope _ps(h, P_OTHER, st, h->cfg.precision != ESM_FP32 ? 3 : 2);
+    launch_pack_index(cu, B, T, max_seqlen, h->cfg.max_positions, pb, h->d_err, st);
+    if (h->cfg.precision != ESM_FP32) launch_attn_worklist(B, L.max_items, pb, st);
+    launch_embed(tok, T, w->emb, !h->bf16_params(), h->cfg.vocab, h->cfg.hidden, h->cfg.emb_scale,
+                 reinterpret_cast<float*>(b + L.x), h->d_err, st);
+  }
+  return run_layers(h, w, T, L.max_items, L, ws, out, false, st);
+}
+
+bool config_ok(const esm_config* c) {
+  if (!c) return false;
+  if (c->num_layers < 0 || c->hidden <= 0 || c->heads <= 0 || c->ffn <= 0 || c->vocab <= 0) return false;
+  if (c->hidden % c->heads) return false;
+  if (c->max_positions <= 0 || c->max_positions > 65536) return false;
+  if (!(c->ln_eps >= 0.f) || !(c->rope_base > 0.f)) return false;
+  if (c->amax_history_len < 1 || c->amax_history_len > 1024) return false;
+  const int dh = c->hidden / c->heads;
+  if (c->precision == ESM_FP32) {
+    return dh % 2 == 0 && dh <= 64 && c->hidden % 4 == 0 && c->hidden <= 4096;
+  }
+  if (c->precision == ESM_BF16 || c->precision == ESM_FP8_E4M3) {
+    if (dh != 64 || c->hidden % 256 || c->ffn % 256) return false;
+    if (c->precision == ESM_FP8_E4M3 && (c->hidden % 128 || c->ffn % 128)) return false;
+    return c->hidden <= 4096 * 4;
+  }
+  return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* esm_status_string(esm_status s) {
+  switch (s) {
+    case ESM_OK: return "ok";
+    case ESM_ERR_INVALID_ARG: return "invalid argument";
+    case ESM_ERR_UNSUPPORTED: return "unsupported device or geometry";
+    case ESM_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens / sequence lengths";
+    case ESM_ERR_TOKEN_RANGE: return "token id out of range";
+    case ESM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ESM_ERR_CUDA: return "CUDA runtime error";
+    case ESM_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+esm_status esm_encoder_create(const esm_config* cfg, esm_encoder_t** out) {
+  if (!out) return ESM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return ESM_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ESM_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  if (major != 10 || minor != 3) return ESM_ERR_UNSUPPORTED;
+  if (!config_ok(cfg)) {
+    if (cfg->precision != ESM_FP32 && cfg->precision != ESM_BF16 && cfg->precision != ESM_FP8_E4M3)
+      return ESM_ERR_INVALID_ARG;
+    return (cfg->hidden > 0 && cfg->heads > 0 && cfg->num_layers >= 0) ? ESM_ERR_UNSUPPORTED : ESM_ERR_INVALID_ARG;
+  }
+  esm_encoder* h = new esm_encoder();
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = sms;
+  const size_t nf = (size_t)cfg->num_layers * kNumFp8Tensors;
+  h->fp8_floats = nf * (1 + cfg->amax_history_len);
+  bool ok = cudaMalloc(&h->d_err, sizeof(unsigned)) == cudaSuccess &&
+            cudaMalloc(&h->d_rope, sizeof(float2) * (size_t)cfg->max_positions * kRopeMaxHalf) == cudaSuccess &&
+            cudaMalloc(&h->d_fp8, sizeof(float) * (h->fp8_floats + nf + 1)) == cudaSuccess;
+  if (ok) {
+    ok = cudaMemset(h->d_err, 0, sizeof(unsigned)) == cudaSuccess &&
+         cudaMemset(h->d_fp8, 0, sizeof(float) * (h->fp8_floats + nf + 1)) == cudaSuccess;
+    std::vector<float> ones(nf, 1.0f);
+    if (ok && nf) ok = cudaMemcpy(h->d_fp8, ones.data(), nf * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
+    if (ok) {
+      launch_rope_table(h->d_rope, cfg->max_positions, (cfg->hidden / cfg->heads) / 2, cfg->rope_base, 0);
+      ok = cudaGetLastError() == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+    }
+  }
+  if (!ok) {
+    esm_encoder_destroy(h);
+    return ESM_ERR_CUDA;
+  }
+  *out = h;
+  return ESM_OK;
+}
+
+void esm_encoder_destroy(esm_encoder_t* h) {
+  if (!h) return;
+  if (h->d_err) cudaFree(h->d_err);
+  if (h->d_rope) cudaFree(h->d_rope);
+  if (h->d_fp8) cudaFree(h->d_fp8);
+  h->drain_events();
+  for (cudaEvent_t e : h->event_pool) cudaEventDestroy(e);
+  delete h;
+}
+
+esm_status esm_encoder_workspace_size(const esm_encoder_t* h, int max_tokens, int max_seqs, size_t* bytes) {
+  if (!h || !bytes || max_tokens < 0 || max_seqs < 0) return ESM_ERR_INVALID_ARG;
+  *bytes = h->layout(max_tokens, max_seqs).total;
+  return ESM_OK;
+}
+
+esm_status esm_encoder_forward(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids,
+                               const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                               void* hidden_out, void* workspace, size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || total_tokens < 0 || num_seqs < 0) return ESM_ERR_INVALID_ARG;
+  if (total_tokens == 0) return ESM_OK;
+  if (num_seqs == 0 || !token_ids || !cu_seqlens || !hidden_out || !aligned(hidden_out, 16)) return ESM_ERR_INVALID_ARG;
+  if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
+  if (!weights_ok(h, w)) return ESM_ERR_INVALID_ARG;
+  return forward_impl(h, w, token_ids, cu_seqlens, num_seqs, total_tokens, max_seqlen, hidden_out, workspace,
+                      workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+esm_status esm_encoder_forward_host(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids_host,
+                                    const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int max_seqlen,
+                                    void* hidden_out_host, void* workspace, size_t workspace_bytes,
+                                    esm_stream_t stream) {
+  if (!h || total_tokens < 0 || num_seqs < 0) return ESM_ERR_INVALID_ARG;
+  if (total_tokens == 0) return ESM_OK;
+  if (num_seqs == 0 || !token_ids_host || !cu_seqlens_host || !hidden_out_host) return ESM_ERR_INVALID_ARG;
+  if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
+  if (!weights_ok(h, w)) return ESM_ERR_INVALID_ARG;
+  WsLayout L;
+  esm_status s = check_ws(h, total_tokens, num_seqs, workspace, workspace_bytes, &L);
+  if (s != ESM_OK) return s;
+  // the output staging lives in the qkv region, which is free once the last layer ran
+  const size_t out_bytes = (size_t)total_tokens * h->cfg.hidden * (h->cfg.precision == ESM_FP32 ? 4 : 2);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  int32_t* dtok = reinterpret_cast<int32_t*>(b + L.stage_tok);
+  int32_t* dcu = reinterpret_cast<int32_t*>(b + L.stage_cu);
+  void* dout = b + L.qkv;
+  if (cudaMemcpyAsync(dtok, token_ids_host, 4 * (size_t)total_tokens, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dcu, cu_seqlens_host, 4 * (size_t)(num_seqs + 1), cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  s = forward_impl(h, w, dtok, dcu, num_seqs, total_tokens, max_seqlen, dout, workspace, workspace_bytes, st);
+  if (s != ESM_OK) return s;
+  if (cudaMemcpyAsync(hidden_out_host, dout, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return ESM_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(st));
+}
+
+esm_status esm_encoder_forward_padded(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids,
+                                      const int32_t* seq_lens, int B, int S, void* hidden_out, void* workspace,
+                                      size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || B < 0 || S < 0) return ESM_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ESM_OK;
+  if (!token_ids || !seq_lens || !hidden_out || !aligned(hidden_out, 16)) return ESM_ERR_INVALID_ARG;
+  if (S > h->cfg.max_positions || (long long)B * S > (1ll << 31) - 1) return ESM_ERR_INVALID_ARG;
+  if (!weights_ok(h, w)) return ESM_ERR_INVALID_ARG;
+  const int T = B * S;
+  WsLayout L;
+  esm_status s = check_ws(h, T, B, workspace, workspace_bytes, &L);
+  if (s != ESM_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  PackBuffers pb = pack_buffers(workspace, L);
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  {
+    ProfScope _ps(h, P_OTHER, st, h->cfg.precision != ESM_FP32 ? 3 : 2);
+    launch_pad_index(seq_lens, B, S, pb, h->d_err, st);
+    if (h->cfg.precision != ESM_FP32) launch_attn_worklist(B, L.max_items, pb, st);
+    launch_embed(token_ids, T, w->emb, !h->bf16_params(), h->cfg.vocab, h->cfg.hidden, h->cfg.emb_scale,
+                 reinterpret_cast<float*>(b + L.x), h->d_err, st);
+  }
+  return run_layers(h, w, T, L.max_items, L, workspace, hidden_out, true, st);
+}
+
+esm_status esm_encoder_check(esm_encoder_t* h, esm_stream_t stream) {
+  if (!h) return ESM_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ESM_ERR_CUDA;
+  unsigned e = 0;
+  if (cudaMemcpy(&e, h->d_err, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return ESM_ERR_CUDA;
+  if (e && cudaMemset(h->d_err, 0, sizeof(unsigned)) != cudaSuccess) return ESM_ERR_CUDA;
+  if (e & ERRBIT_CU_SEQLENS) return ESM_ERR_BAD_CU_SEQLENS;
+  if (e & ERRBIT_TOKEN) return ESM_ERR_TOKEN_RANGE;
+  if (e & ERRBIT_TIMEOUT) return ESM_ERR_TIMEOUT;
+  return ESM_OK;
+}
+
+esm_status esm_encoder_debug_pack_index(esm_encoder_t* h, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                                        int max_seqlen, int32_t* pos_id, int32_t* seg_id, void* workspace,
+                                        size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || num_seqs <= 0 || total_tokens < 0 || !cu_seqlens || !pos_id || !seg_id) return ESM_ERR_INVALID_ARG;
+  if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
+  WsLayout L;
+  esm_status s = check_ws(h, total_tokens, num_seqs, workspace, workspace_bytes, &L);
+  if (s != ESM_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  PackBuffers pb = pack_buffers(workspace, L);
+  if (total_tokens > 0) {
+    if (cudaMemsetAsync(pb.pos_id, 0, 4 * (size_t)total_tokens, st) != cudaSuccess ||
+        cudaMemsetAsync(pb.seg_id, 0, 4 * (size_t)total_tokens, st) != cudaSuccess)
+      return ESM_ERR_CUDA;
+  }
+  launch_pack_index(cu_seqlens, num_seqs, total_tokens, max_seqlen, h->cfg.max_positions, pb, h->d_err, st);
+  if (total_tokens > 0) {
+    if (cudaMemcpyAsync(pos_id, pb.pos_id, 4 * (size_t)total_tokens, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(seg_id, pb.seg_id, 4 * (size_t)total_tokens, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return ESM_ERR_CUDA;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status esm_op_layernorm(esm_encoder_t* h, const float* x, const void* gamma, const void* beta, void* y, int rows,
+                            int cols, esm_stream_t stream) {
+  if (!h || !x || !gamma || !beta || !y || rows < 0 || cols <= 0 || cols % 4 || cols > 4096)
+    return ESM_ERR_INVALID_ARG;
+  launch_layernorm(x, gamma, beta, !h->bf16_params(), y, h->act(), rows, cols, h->cfg.ln_eps, nullptr, nullptr,
+                   nullptr, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status esm_op_gemm(esm_encoder_t* h, esm_epilogue epi, const void* A, const void* B, const void* bias, void* out,
+                       const int32_t* pos_id, int M, int N, int K, esm_stream_t stream) {
+  if (!h || !A || !B || !out || M < 0 || N <= 0 || K <= 0) return ESM_ERR_INVALID_ARG;
+  if (epi < ESM_EPI_BIAS_F32 || epi > ESM_EPI_GELU) return ESM_ERR_INVALID_ARG;
+  if (epi == ESM_EPI_QKV_ROPE && (!pos_id || N != 3 * h->cfg.hidden)) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_FP32) {
+    if (K % 64 || N % 256 || !aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16)) return ESM_ERR_INVALID_ARG;
+    if (bias && !aligned(bias, 16)) return ESM_ERR_INVALID_ARG;
+  }
+  const Act out_act = (epi == ESM_EPI_BIAS_F32 || epi == ESM_EPI_RESIDUAL) ? Act::F32 : h->act();
+  return run_gemm(h, P_OTHER, epi, A, B, bias, out, pos_id, M, N, K, false, out_act, nullptr, nullptr, nullptr, nullptr,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,
+                            int total_tokens, int max_seqlen, void* o, void* workspace, size_t workspace_bytes,
+                            esm_stream_t stream) {
+  if (!h || !qkv || !cu_seqlens || !o || num_seqs <= 0 || total_tokens < 0) return ESM_ERR_INVALID_ARG;
+  if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
+  if (total_tokens == 0) return ESM_OK;
+  WsLayout L;
+  esm_status s = check_ws(h, total_tokens, num_seqs, workspace, workspace_bytes, &L);
+  if (s != ESM_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  PackBuffers pb = pack_buffers(workspace, L);
+  if (cudaMemsetAsync(pb.pos_id, 0, 4 * (size_t)total_tokens, st) != cudaSuccess ||
+      cudaMemsetAsync(pb.seg_id, 0, 4 * (size_t)total_tokens, st) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  launch_pack_index(cu_seqlens, num_seqs, total_tokens, max_seqlen, h->cfg.max_positions, pb, h->d_err, st);
+  const int d = h->cfg.hidden, H = h->cfg.heads;
+  if (h->cfg.precision == ESM_FP32) {
+    launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(o), d, H, total_tokens, pb, st);
+  } else {
+    launch_attn_worklist(num_seqs, L.max_items, pb, st);
+    launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), d, H, L.max_items,
+                          pb, st);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status esm_encoder_set_profiling(esm_encoder_t* h, int enable) {
+  if (!h) return ESM_ERR_INVALID_ARG;
+  h->profiling = enable != 0;
+  return ESM_OK;
+}
+
+esm_status esm_encoder_get_profile(esm_encoder_t* h, esm_profile* out, int reset) {
+  if (!h || !out) return ESM_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ESM_ERR_CUDA;
+  h->drain_events();
+  for (int i = 0; i < ESM_PROFILE_CLASSES; ++i) {
+    out->ms[i] = h->ms[i];
+    out->launches[i] = h->launches[i];
+  }
+  out->total_launches = h->total_launches;
+  if (reset) {
+    for (int i = 0; i < ESM_PROFILE_CLASSES; ++i) {
+      h->ms[i] = 0;
+      h->launches[i] = 0;
+    }
+    h->total_launches = 0;
+  }
+  return ESM_OK;
+}
+
+esm_status esm_encoder_get_fp8_state(const esm_encoder_t* h, float* host_buf, size_t n) {
+  if (!h || !host_buf || n != h->fp8_floats) return ESM_ERR_INVALID_ARG;
+  if (n == 0) return ESM_OK;
+  return cuda_status(cudaMemcpy(host_buf, h->d_fp8, n * sizeof(float), cudaMemcpyDeviceToHost));
+}
+
+esm_status esm_encoder_set_fp8_state(esm_encoder_t* h, const float* host_buf, size_t n) {
+  if (!h || !host_buf || n != h->fp8_floats) return ESM_ERR_INVALID_ARG;
+  if (n == 0) return ESM_OK;
+  return cuda_status(cudaMemcpy(h->d_fp8, host_buf, n * sizeof(float), cudaMemcpyHostToDevice));
+}
+
+}  // extern "C"

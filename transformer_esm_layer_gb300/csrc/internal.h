@@ -1,0 +1,100 @@
+// Internal declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/esm_encoder.h"
+
+namespace esm {
+
+// Rows of one attention query tile.
+constexpr int kAttnQTile = 64;
+// Columns per RoPE table row (head_dim / 2, head_dim <= 64).
+constexpr int kRopeMaxHalf = 32;
+
+enum class Act { F32, BF16, E4M3 };
+
+struct PackBuffers {
+  int32_t* pos_id;     // [T]
+  int32_t* seg_id;     // [T]
+  int32_t* seg_start;  // [B]
+  int32_t* seg_qlen;   // [B]  query rows of the segment
+  int32_t* seg_klen;   // [B]  visible keys of the segment
+  int32_t* work;       // [2 * max_items]: (segment, first query row)
+  int32_t* work_count; // [1]
+};
+
+// ---------------------------------------------------------------- launchers (pack.cu)
+void launch_pack_index(const int32_t* cu, int B, int T, int max_seqlen, int max_positions,
+                       const PackBuffers& pb, unsigned* err, cudaStream_t st);
+void launch_pad_index(const int32_t* seq_lens, int B, int S, const PackBuffers& pb, unsigned* err,
+                      cudaStream_t st);
+void launch_attn_worklist(int B, int max_items, const PackBuffers& pb, cudaStream_t st);
+void launch_embed(const int32_t* tok, int T, const void* emb, bool emb_f32, int vocab, int d, float scale,
+                  float* x, unsigned* err, cudaStream_t st);
+void launch_rope_table(float2* tab, int max_pos, int half, float base, cudaStream_t st);
+
+// ---------------------------------------------------------------- layernorm.cu
+// y = LN(x) * g + b. Params in f32 or bf16; output f32, bf16 or e4m3 (scaled by
+// *q_scale, max|y| into *amax).  With valid_* set, rows whose position is not below the
+// segment's visible length are written as zero.
+void launch_layernorm(const float* x, const void* g, const void* b, bool param_f32, void* y, Act out,
+                      int rows, int cols, float eps, const float* q_scale, float* amax,
+                      const int32_t* valid_pos, const int32_t* valid_seg, const int32_t* valid_klen,
+                      cudaStream_t st);
+// out = x (converted), zeroing invalid rows the same way (final_ln == 0).
+void launch_copy_out(const float* x, void* out, Act out_t, int rows, int cols, const int32_t* valid_pos,
+                     const int32_t* valid_seg, const int32_t* valid_klen, cudaStream_t st);
+
+// ---------------------------------------------------------------- GEMMs
+struct EpiArgs {
+  const void* bias;       // [N] param dtype
+  bool bias_f32;
+  void* out;              // [M, N]
+  const int32_t* pos_id;  // [M] (QKV)
+  const float2* rope;     // [max_pos][half]
+  int rope_cols;          // columns < rope_cols get RoPE (2 * hidden)
+  int head_dim;
+  int max_pos;
+  const float* a_scale;   // FP8: scale of A (device)
+  const float* b_scale;   // FP8: scale of B (device)
+  const float* o_scale;   // FP8 GELU output: quantisation scale (device)
+  float* o_amax;          // FP8 GELU output: amax (device)
+};
+
+// tcgen05 GEMM: A [M,K] bf16 (or e4m3), B [N,K] bf16 (or e4m3); K % 64 == 0 (bf16) or
+// K % 128 == 0 (e4m3); N % 256 == 0.
+int gemm_tc_smem_bytes();
+cudaError_t launch_gemm_tc(esm_epilogue epi, bool fp8, Act out_act, const CUtensorMap* tmA,
+                           const CUtensorMap* tmB, int M, int N, int K, const EpiArgs& ea, int num_sms,
+                           unsigned* err, cudaStream_t st);
+
+// SIMT fp32 GEMM (the ESM_FP32 precision): any M, N, K.
+void launch_gemm_f32(esm_epilogue epi, const float* A, const float* B, int M, int N, int K,
+                     const EpiArgs& ea, cudaStream_t st);
+// In-place RoPE on the q and k blocks of qkv [T, 3*d] (fp32).
+void launch_rope_f32(float* qkv, int T, int d, int head_dim, const int32_t* pos_id, const float2* rope,
+                     int max_pos, cudaStream_t st);
+
+// ---------------------------------------------------------------- attention.cu
+// qkv [T, 3*d] head-major, o [T, d].  Work items come from the pack buffers.
+void launch_attention_bf16(const __nv_bfloat16* qkv, __nv_bfloat16* o, int d, int heads, int max_items,
+                           const PackBuffers& pb, cudaStream_t st);
+void launch_attention_bf16_to_e4m3(const __nv_bfloat16* qkv, uint8_t* o, int d, int heads, int max_items,
+                                   const PackBuffers& pb, const float* q_scale, float* amax, cudaStream_t st);
+void launch_attention_f32(const float* qkv, float* o, int d, int heads, int T, const PackBuffers& pb,
+                          cudaStream_t st);
+
+// ---------------------------------------------------------------- fp8.cu
+// Quantise a bf16 tensor to e4m3 with *scale; record max|w| into *amax.
+void launch_quantize_e4m3(const __nv_bfloat16* w, uint8_t* q, size_t n, const float* scale, float* amax,
+                          cudaStream_t st);
+// Delayed-scaling update of n tensors: push amax[i] into hist[i][0..len), scale[i] =
+// 448 / max(hist[i]) (kept if the max is zero or not finite); amax[i] reset to 0.
+void launch_fp8_update(float* scale, float* hist, float* amax, int n, int len, cudaStream_t st);
+
+}  // namespace esm
