@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--layers", type=int, default=33, help="fewer layers: small case for profiler captures only")
+    ap.add_argument("--tokens", type=int, default=16384, help="other batch size: small case for captures only")
     return ap.parse_args()
 
 
@@ -52,13 +54,16 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_for_rank(rank: int):
+def workload_for_rank(rank: int, tokens: int = 16384, layers: int = 33):
+    import dataclasses
     from transformer_esm_layer_gb300 import synth
     wl = synth.make_workload("esm650m")
-    if rank > 0:  # another batch of the same size and length distribution
-        rng = np.random.default_rng([wl.seed, rank])
-        wl.lengths = synth.lognormal_lengths(rng, total=16384)
+    if rank > 0 or tokens != 16384:  # another batch with the same length distribution
+        rng = np.random.default_rng([wl.seed, rank, tokens])
+        wl.lengths = synth.lognormal_lengths(rng, total=tokens)
         wl.seed = wl.seed * 1000 + rank
+    if layers != wl.geometry.num_layers:
+        wl.geometry = dataclasses.replace(wl.geometry, num_layers=layers)
     return wl
 
 
@@ -213,7 +218,7 @@ def run_ours(args):
     _build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
 
-    wl = workload_for_rank(rank)
+    wl = workload_for_rank(rank, args.tokens, args.layers)
     g = wl.geometry
     w_np = synth.model_weights(g, wl.seed, "bf16")
     dw = DeviceWeights(w_np, "bf16", device=dev)
@@ -323,7 +328,7 @@ def run_ours(args):
         toks, dt, done = cpu_oracle_sample(wl, f64_weights(w_np), args.cpu_seconds)
         cpu = {"value": toks / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                "sample": f"{len(done)} whole sequence(s) of the workload (indices {done}, {toks} tokens) through all "
-                         f"33 layers in float64 numpy, {dt:.1f} s"}
+                         f"{g.num_layers} layers in float64 numpy, {dt:.1f} s"}
 
     if world > 1:
         dist.barrier()
@@ -331,8 +336,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": "esm650m: ESM-2 650M encoder (33 layers, hidden 1280, 20 heads, FFN 5120, "
-                                       "vocab 33), bf16 weights N(0,0.02), packed batch of 16384 tokens in 47 "
+                "config": {"workload": f"esm650m: ESM-2 650M encoder ({g.num_layers} layers, hidden 1280, 20 heads, FFN 5120, "
+                                       f"vocab 33), bf16 weights N(0,0.02), packed batch of {T} tokens in {B} "
                                        "sequences, log-normal lengths (median 300, sigma 0.6) clipped to [32,1024], "
                                        "seed 2",
                            "tokens_per_step_per_gpu": T, "sequences": B, "max_seqlen": maxL,
