@@ -211,6 +211,28 @@ ESM_API esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int
                             int num_seqs, int total_tokens, int max_seqlen, void* o,
                             void* workspace, size_t workspace_bytes, esm_stream_t stream);
 
+/* ---- attention without any allocation ----
+ * No counterpart on the pages: this entry point exists for callers that cannot allocate
+ * device memory (a memory pool or allocator that owns the whole device, a plugin host that
+ * hands out only its input and output buffers, a runtime that forbids allocation after
+ * start-up).  It computes exactly what esm_op_attention computes for bf16, head_dim 64
+ * (qkv device bf16 [T, 3*hidden], q | k | v head-major, RoPE applied; o device bf16
+ * [T, hidden]; cu_seqlens device int32 [num_seqs + 1]) without a handle or a workspace:
+ * its scratch is a fixed device array inside the library (about 615 KB, held by every
+ * GPU that loads the library until the process exits).
+ * Limits: total_tokens <= ESM_NOALLOC_MAX_TOKENS, num_seqs <= ESM_NOALLOC_MAX_SEQS,
+ * max_seqlen <= ESM_NOALLOC_MAX_TOKENS; larger sizes return ESM_ERR_INVALID_ARG.
+ * hidden must be 64 * heads (ESM_ERR_UNSUPPORTED otherwise, or off sm_103).
+ * The first call on each device looks up the array's device address (with that device
+ * current) and caches it: make that first call before any stream capture.  Calls share
+ * the array, so calls that overlap on the GPU (different streams) race.  Malformed
+ * cu_seqlens are clamped so every access stays in bounds; they are not reported. */
+#define ESM_NOALLOC_MAX_TOKENS 65536
+#define ESM_NOALLOC_MAX_SEQS 4096
+ESM_API esm_status esm_op_attention_noalloc(const void* qkv, const int32_t* cu_seqlens, int num_seqs,
+                                            int total_tokens, int max_seqlen, int hidden, int heads, void* o,
+                                            esm_stream_t stream);
+
 /* ---- FP8 delayed-scaling state (ESM_FP8_E4M3 handles) ----
  * Layout, float32: for each layer l and each of the 8 quantised tensors k in the order
  * {x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2}: scale[l][k] (num_layers*8 floats), then

@@ -26,7 +26,7 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_encoder_forward_host", "esm_encoder_forward_padded", "esm_encoder_check",
            "esm_encoder_debug_pack_index", "esm_op_layernorm", "esm_op_gemm", "esm_op_attention",
            "esm_encoder_get_fp8_state", "esm_encoder_set_fp8_state", "esm_encoder_set_profiling",
-           "esm_encoder_get_profile", "esm_status_string")
+           "esm_encoder_get_profile", "esm_op_attention_noalloc", "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
 
 
@@ -85,6 +85,7 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_set_fp8_state": (i32, [vp, ctypes.POINTER(ctypes.c_float), sz]),
         "esm_encoder_set_profiling": (i32, [vp, i32]),
         "esm_encoder_get_profile": (i32, [vp, ctypes.POINTER(EsmProfile), i32]),
+        "esm_op_attention_noalloc": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "esm_status_string": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -311,6 +312,14 @@ class EsmEncoder:
     def fp8_history(self, buf: Optional[np.ndarray] = None) -> np.ndarray:
         buf = self.get_fp8_state() if buf is None else buf
         return buf[self.num_layers * 8:].reshape(self.num_layers, 8, self.amax_history_len)
+
+
+def op_attention_noalloc(qkv, cu_seqlens, max_seqlen: int, hidden: int, heads: int, o, stream=None) -> int:
+    """esm_op_attention_noalloc: attention with no handle, no workspace and no allocation.
+    Returns the status code."""
+    lib = load_library()
+    return lib.esm_op_attention_noalloc(_ptr(qkv), _ptr(cu_seqlens), cu_seqlens.numel() - 1, qkv.shape[0],
+                                        int(max_seqlen), hidden, heads, _ptr(o), _stream_ptr(stream))
 
 
 def packed_inputs(tokens: np.ndarray, lengths: Sequence[int], device="cuda"):
