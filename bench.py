@@ -40,8 +40,11 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--layers", type=int, default=33, help="fewer layers: small case for profiler captures only")
-    ap.add_argument("--tokens", type=int, default=16384, help="other batch size: small case for captures only")
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers: small case for profiler captures only")
+    ap.add_argument("--tokens", type=int, default=None, help="other batch size: small case for captures only")
+    ap.add_argument("--workload", choices=("esm650m", "esm650m_padded", "esm3b_fp8"), default="esm650m",
+                    help="esm650m (the headline), esm650m_padded (same sequences as [B,1024] with a key padding "
+                         "mask), esm3b_fp8 (3B encoder, E4M3 GEMMs, 32768 tokens)")
     return ap.parse_args()
 
 
@@ -54,17 +57,33 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_for_rank(rank: int, tokens: int = 16384, layers: int = 33):
+def workload_for_rank(rank: int, tokens=None, layers=None, name: str = "esm650m"):
     import dataclasses
     from transformer_esm_layer_gb300 import synth
-    wl = synth.make_workload("esm650m")
-    if rank > 0 or tokens != 16384:  # another batch with the same length distribution
+    wl = synth.make_workload(name)
+    default_T = wl.total_tokens
+    tokens = default_T if tokens is None else tokens
+    if rank > 0 or tokens != default_T:  # another batch with the same length distribution
         rng = np.random.default_rng([wl.seed, rank, tokens])
         wl.lengths = synth.lognormal_lengths(rng, total=tokens)
         wl.seed = wl.seed * 1000 + rank
-    if layers != wl.geometry.num_layers:
+    if layers is not None and layers != wl.geometry.num_layers:
         wl.geometry = dataclasses.replace(wl.geometry, num_layers=layers)
     return wl
+
+
+def workload_text(wl) -> str:
+    g = wl.geometry
+    size = "3B" if g.hidden == 2560 else "650M"
+    txt = (f"{wl.name}: ESM-2 {size} encoder ({g.num_layers} layers, hidden {g.hidden}, {g.heads} heads, FFN {g.ffn}, "
+           f"vocab 33), {'E4M3 GEMMs with per-tensor delayed scaling (history 16)' if wl.precision == 'fp8' else 'bf16'}"
+           f", weights N(0,0.02), {wl.total_tokens} tokens in {len(wl.lengths)} sequences, log-normal lengths "
+           f"(median 300, sigma 0.6) clipped to [32,1024], seed {wl.seed}")
+    if wl.padded_len:
+        txt += f"; padded layout [{len(wl.lengths)}, {wl.padded_len}] with a key padding mask"
+    else:
+        txt += "; packed (THD)"
+    return txt
 
 
 def algorithmic_flops(wl):
@@ -139,16 +158,21 @@ def gemm_traffic_record():
     return rec if rec.get("gemm_tc_sha256_16") == h else None
 
 
-def cpu_oracle_sample(wl, w64, seconds: float):
-    """Time the float64 oracle on whole sequences of the workload until `seconds` pass."""
+def cpu_oracle_sample(wl, w64, seconds: float, prec: str = "bf16", enc=None):
+    """Time the float64 oracle on whole sequences of the workload until `seconds` pass
+    (for FP8 with the scales the GPU path holds, read back through the C ABI)."""
     from oracle import esm_oracle as O
     from transformer_esm_layer_gb300 import synth
     tok = synth.workload_tokens(wl)
     cu = O.cu_seqlens(wl.lengths)
+    kw = {}
+    if prec == "fp8" and enc is not None:
+        sc = enc.fp8_scales()
+        kw["fp8_state"] = [{k: float(sc[l, i]) for i, k in enumerate(O.FP8_TENSORS)} for l in range(sc.shape[0])]
     done, toks = [], 0
     t0 = time.perf_counter()
     for i in range(len(wl.lengths)):
-        O.encode_sequence(tok[cu[i]:cu[i + 1]], w64, wl.geometry.heads, final_ln=True)
+        O.encode_sequence(tok[cu[i]:cu[i + 1]], w64, wl.geometry.heads, final_ln=True, **kw)
         done.append(i)
         toks += wl.lengths[i]
         if time.perf_counter() - t0 >= seconds:
@@ -218,22 +242,35 @@ def run_ours(args):
     _build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
 
-    wl = workload_for_rank(rank, args.tokens, args.layers)
+    wl = workload_for_rank(rank, args.tokens, args.layers, args.workload)
     g = wl.geometry
-    w_np = synth.model_weights(g, wl.seed, "bf16")
-    dw = DeviceWeights(w_np, "bf16", device=dev)
+    prec = wl.precision
+    padded = wl.padded_len is not None
+    w_np = synth.model_weights(g, wl.seed, prec)
+    dw = DeviceWeights(w_np, prec, device=dev)
     tok_np = synth.workload_tokens(wl)
     tok, cu = packed_inputs(tok_np, wl.lengths, device=dev)
     T, B, maxL = wl.total_tokens, len(wl.lengths), max(wl.lengths)
-    enc = EsmEncoder.from_geometry(g, "bf16", final_ln=True)
-    ws = enc.workspace(T, B, dev)
-    out = torch.empty(T, g.hidden, dtype=torch.bfloat16, device=dev)
+    enc = EsmEncoder.from_geometry(g, prec, final_ln=True)
     stream = torch.cuda.current_stream()
+    if padded:
+        S = wl.padded_len
+        tok_pad = torch.from_numpy(synth.pad_tokens(tok_np, wl.lengths, S)).to(dev)
+        lens_dev = torch.tensor(wl.lengths, dtype=torch.int32, device=dev)
+        ws = enc.workspace(B * S, B, dev)
+        out = torch.empty(B, S, g.hidden, dtype=torch.bfloat16, device=dev)
 
-    def step():
-        enc.forward(dw, tok, cu, maxL, out=out, workspace=ws, stream=stream)
+        def step():
+            enc.forward_padded(dw, tok_pad, lens_dev, out=out, workspace=ws, stream=stream)
+    else:
+        ws = enc.workspace(T, B, dev)
+        out = torch.empty(T, g.hidden, dtype=torch.bfloat16, device=dev)
 
-    for _ in range(max(args.warmup, 3)):
+        def step():
+            enc.forward(dw, tok, cu, maxL, out=out, workspace=ws, stream=stream)
+
+    # FP8 delayed scaling needs a full amax history before timing
+    for _ in range(max(args.warmup, 3, 16 if prec == "fp8" else 0)):
         step()
     enc.check(stream)
 
@@ -279,28 +316,38 @@ def run_ours(args):
     enc.set_profiling(False)
     flops = algorithmic_flops(wl)
     total_flops = sum(flops.values())
+    executed = dict(flops)
+    if padded:  # the GEMMs run over all B*S rows, attention over every query row of each row
+        rows = B * wl.padded_len
+        for c in ("gemm_qkv", "gemm_oproj", "gemm_fc1", "gemm_fc2"):
+            executed[c] = flops[c] * rows / T
+        executed["attention"] = 4.0 * g.hidden * wl.padded_len * float(np.sum(wl.lengths)) * g.num_layers
     pk, pk_src = peaks()
     gemm_classes = ("gemm_qkv", "gemm_oproj", "gemm_fc1", "gemm_fc2")
     gemm_ms = sum(prof[c]["ms"] for c in gemm_classes) / prof_steps
     gemm_launches = sum(prof[c]["launches"] for c in gemm_classes) / prof_steps
-    gemm_flops = sum(flops[c] for c in gemm_classes)
+    gemm_flops = sum(executed[c] for c in gemm_classes)
     gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12
-    peak_sust = float(pk["bf16_tflops_sustained"])
+    # a contraction takes the peak of its own dtype: E4M3 = 2 x the measured bf16 (nominal 4.5 / 2.25)
+    dtype_mult = 2.0 if prec == "fp8" else 1.0
+    peak_sust = float(pk["bf16_tflops_sustained"]) * dtype_mult
+    peak_burst = float(pk["bf16_tflops"]) * dtype_mult
     per_kernel = {c: {"ms_per_step": prof[c]["ms"] / prof_steps, "launches_per_step": prof[c]["launches"] / prof_steps}
                   for c in ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other")}
     for c in list(gemm_classes) + ["attention"]:
-        per_kernel[c]["tflops"] = flops[c] / (per_kernel[c]["ms_per_step"] / 1e3) / 1e12 if per_kernel[c]["ms_per_step"] else None
+        per_kernel[c]["tflops"] = executed[c] / (per_kernel[c]["ms_per_step"] / 1e3) / 1e12 if per_kernel[c]["ms_per_step"] else None
     traffic = gemm_traffic_record()
-    roofline = {"bound": "tensor", "kernel": "gemm_tc_kernel (tcgen05 bf16, all four linear maps)",
+    roofline = {"bound": "tensor", "kernel": f"gemm_tc_kernel (tcgen05 {'e4m3' if prec == 'fp8' else 'bf16'}, "
+                                              "all four linear maps)",
                 "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s", "frac": gemm_tflops / peak_sust,
-                "peak_source": f"bf16_tflops_sustained, {pk_src}",
+                "peak_source": f"bf16_tflops_sustained, {pk_src}" + (" x 2 (E4M3/bf16 nominal ratio)" if prec == "fp8" else ""),
                 "flops_per_launch": gemm_flops / gemm_launches if gemm_launches else None,
                 "avg_launch_ms": gemm_ms / gemm_launches if gemm_launches else None,
-                "traffic": traffic.get("dram_bytes_per_launch") if traffic else None}
+                "traffic": traffic.get("dram_bytes_per_launch") if (traffic and args.workload == "esm650m") else None}
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
-    if world == 1 or True:
+    if not padded:
         tok_h = torch.from_numpy(tok_np.astype(np.int32)).pin_memory()
         cu_h = torch.from_numpy(synth.cu_seqlens_from_lengths(wl.lengths)).pin_memory()
         out_h = torch.empty(T, g.hidden, dtype=torch.bfloat16).pin_memory()
@@ -325,7 +372,7 @@ def run_ours(args):
     # ---------------------------------------------------------------- CPU baseline (oracle)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        toks, dt, done = cpu_oracle_sample(wl, f64_weights(w_np), args.cpu_seconds)
+        toks, dt, done = cpu_oracle_sample(wl, f64_weights(w_np), args.cpu_seconds, prec, enc)
         cpu = {"value": toks / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                "sample": f"{len(done)} whole sequence(s) of the workload (indices {done}, {toks} tokens) through all "
                          f"{g.num_layers} layers in float64 numpy, {dt:.1f} s"}
@@ -333,23 +380,29 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        metric = {"esm650m": METRIC,
+                  "esm650m_padded": "ESM-2 650M padded [B,1024] fwd tokens/s (real tokens) on 1 GB300; achieved "
+                                    "TFLOP/s vs dense BF16 peak",
+                  "esm3b_fp8": "ESM-2 3B packed FP8 fwd tokens/s on 1 GB300; achieved TFLOP/s vs dense FP8 peak"
+                  }[args.workload]
+        line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": f"esm650m: ESM-2 650M encoder ({g.num_layers} layers, hidden 1280, 20 heads, FFN 5120, "
-                                       f"vocab 33), bf16 weights N(0,0.02), packed batch of {T} tokens in {B} "
-                                       "sequences, log-normal lengths (median 300, sigma 0.6) clipped to [32,1024], "
-                                       "seed 2",
-                           "tokens_per_step_per_gpu": T, "sequences": B, "max_seqlen": maxL,
-                           "l2": "no flush: inputs larger than L2 (1.3 GB of weights read per step plus "
-                                 f"{ws.numel() / 2**30:.2f} GB of activations vs the 129 MB L2)",
+                "vs_baseline": None, "dtype": "e4m3" if prec == "fp8" else "bf16", "data": "synthetic",
+                "config": {"workload": workload_text(wl), "tokens_per_step_per_gpu": T, "sequences": B,
+                           "max_seqlen": maxL,
+                           "l2": "no flush: inputs larger than L2 ("
+                                 f"{sum(t.numel() * t.element_size() for l in dw.layers for t in l.values()) / 2**30:.2f} GB "
+                                 f"of weights read per step plus {ws.numel() / 2**30:.2f} GB of activations vs the "
+                                 "129 MB L2)",
                            "parallelism": "single GPU" if world == 1 else f"{world} replicas, each its own batch, "
                                                                           "no collective"},
                 "tflops": total_flops * world / (ms_step / 1e3) / 1e12,
-                "mfu_vs_sustained_bf16": total_flops / (ms_step / 1e3) / 1e12 / peak_sust,
-                "mfu_vs_burst_bf16": total_flops / (ms_step / 1e3) / 1e12 / float(pk["bf16_tflops"]),
+                "mfu_vs_sustained_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_sust,
+                "mfu_vs_burst_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_burst,
+                "peak_dtype": "e4m3 (2 x measured bf16)" if prec == "fp8" else "bf16 (measured)",
                 "algorithmic_gflop_per_step_per_gpu": total_flops / 1e9,
-                "roofline": roofline, "per_kernel": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "per_kernel": per_kernel,
+                "padded_over_packed_flops": (sum(executed.values()) / total_flops) if padded else None, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clocks, "gpu_launches": launches,
                 "context": "pages' own figure: 59.2% model-FLOP utilisation, ESM-2 650M training, batch 46, A100"}
         print(json.dumps(line), flush=True)

@@ -203,6 +203,21 @@ ESM_API esm_status esm_op_gemm(esm_encoder_t* h, esm_epilogue epi, const void* A
                        const void* bias, void* out, const int32_t* pos_id, int M, int N, int K,
                        esm_stream_t stream);
 
+/* E4M3 forms of the two hooks above, for ESM_FP8_E4M3 handles.
+ * esm_op_layernorm_e4m3: y[r, c] = E4M3(LN(x)[r, c] * (*scale)) (round to nearest even,
+ *   saturating at +-448), max |LN(x)| folded into *amax with an atomic max (set it to 0
+ *   first).  x device float32 [rows, cols]; gamma, beta device bf16; y device uint8 codes;
+ *   scale, amax device float32 scalars.
+ * esm_op_gemm_fp8: out = epilogue((A B^T) / ((*a_scale) (*b_scale)) + bias) with A
+ *   [M, K] and B [N, K] device E4M3 codes, K % 128 == 0, N % 256 == 0; bias bf16; output
+ *   as for esm_op_gemm (ESM_EPI_GELU writes bf16 here). */
+ESM_API esm_status esm_op_layernorm_e4m3(esm_encoder_t* h, const float* x, const void* gamma, const void* beta,
+                                         uint8_t* y, int rows, int cols, const float* scale, float* amax,
+                                         esm_stream_t stream);
+ESM_API esm_status esm_op_gemm_fp8(esm_encoder_t* h, esm_epilogue epi, const uint8_t* A, const uint8_t* B,
+                                   const float* a_scale, const float* b_scale, const void* bias, void* out,
+                                   const int32_t* pos_id, int M, int N, int K, esm_stream_t stream);
+
 /* Variable-length bidirectional attention over packed sequences (section 3.2 of the
  * hotelren.com guide, thd format).  qkv device [T, 3*hidden] in the activation dtype
  * (q | k | v, head-major, RoPE already applied); o device [T, hidden].  Each token

@@ -25,7 +25,8 @@ Readings where the pages are silent (each also applied by the CUDA path):
 pre-LayerNorm blocks; LayerNorm eps 1e-5 with the biased variance; exact erf GELU; RoPE
 base 10000 with rotate-half pairs (j, j + head_dim/2), applied to q and k after the bias,
 positions restarting at 0 at each sequence start; scores scaled by 1/sqrt(head_dim);
-no dropout; an optional final LayerNorm; embedding scale 1.
+no dropout; an optional final LayerNorm; embedding scale 1.  The FP8 workload states that
+attention stays in bf16: its oracle rounds the attention operands q, k, v to bfloat16.
 
 Parity pins: every function here is checked in tests/test_oracle_pins.py against closed
 forms, invariants, brute force or an independent library formulation.  The only part with
@@ -113,6 +114,17 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_keys: Optional[int]
     return o.transpose(1, 0, 2)
 
 
+# --------------------------------------------------------------------------- bf16
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value (ties to even): keep the top 8 significand bits
+    of the float32 nearest to x.  (Used where a workload fixes bf16 operands.)"""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    u = ((u + 0x7FFF + lsb) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 # --------------------------------------------------------------------------- FP8 (E4M3)
 def e4m3_round(x: np.ndarray) -> np.ndarray:
     """Round to the nearest OCP FP8 E4M3 value (ties to even), saturating at +-448.
@@ -151,7 +163,8 @@ FP8_TENSORS = ("x_qkv", "w_qkv", "x_o", "w_o", "x_1", "w_1", "x_2", "w_2")
 # --------------------------------------------------------------------------- layer / encoder
 def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], heads: int,
                   eps: float = LN_EPS, rope_base: float = ROPE_BASE, n_keys: Optional[int] = None,
-                  fp8_scales: Optional[Dict[str, float]] = None, amax_out: Optional[Dict[str, float]] = None):
+                  fp8_scales: Optional[Dict[str, float]] = None, amax_out: Optional[Dict[str, float]] = None,
+                  bf16_attention: bool = False):
     """One pre-LN encoder layer on one sequence x[L, d] (float64).
 
     y = LN1(x); [q|k|v] = y Wqkv^T + bqkv; RoPE on q, k; o = attention(q, k, v);
@@ -159,7 +172,8 @@ def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], head
 
     With ``fp8_scales`` every GEMM operand (the four activations and four weights) is
     replaced by its E4M3 fake-quantised value; ``amax_out`` then receives max|.| of each
-    operand before quantisation."""
+    operand before quantisation.  ``bf16_attention`` rounds the attention operands q, k, v
+    to bfloat16 (the FP8 workload keeps attention in bf16)."""
     L, d = x.shape
     dh = d // heads
 
@@ -180,6 +194,8 @@ def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], head
     v = qkv[:, 2 * d:].reshape(L, heads, dh)
     q = rope(q, pos, rope_base)
     k = rope(k, pos, rope_base)
+    if bf16_attention:
+        q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
     o = attention(q, k, v, n_keys).reshape(L, d)
     x = x + mm(o, "w_o", "x_o") + w["b_o"]
     z = layer_norm(x, w["ln2_g"], w["ln2_b"], eps)
@@ -196,7 +212,7 @@ def encode_sequence(tokens: np.ndarray, weights: Dict, heads: int, final_ln: boo
                     emb_scale: float = 1.0, eps: float = LN_EPS, rope_base: float = ROPE_BASE,
                     num_layers: Optional[int] = None, n_keys: Optional[int] = None,
                     fp8_state: Optional[List[Dict[str, float]]] = None,
-                    amax_out: Optional[List[Dict[str, float]]] = None) -> np.ndarray:
+                    amax_out: Optional[List[Dict[str, float]]] = None, bf16_attention: bool = False) -> np.ndarray:
     """Encode ONE sequence (token ids [L]) through the embedding, the layers and the
     optional final LayerNorm.  Positions are 0..L-1."""
     tokens = np.asarray(tokens, dtype=np.int64)
@@ -207,7 +223,7 @@ def encode_sequence(tokens: np.ndarray, weights: Dict, heads: int, final_ln: boo
     for li, wl in enumerate(layers):
         x = encoder_layer(x, pos, _f64_layer(wl), heads, eps, rope_base, n_keys,
                           None if fp8_state is None else fp8_state[li],
-                          None if amax_out is None else amax_out[li])
+                          None if amax_out is None else amax_out[li], bf16_attention)
     if final_ln:
         x = layer_norm(x, np.asarray(weights["lnf_g"], np.float64), np.asarray(weights["lnf_b"], np.float64), eps)
     return x

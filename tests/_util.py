@@ -28,3 +28,20 @@ def ensure_built():
 def to_np(t):
     import torch
     return t.detach().to(torch.float64).cpu().numpy()
+
+
+def e4m3_table():
+    """Value of every E4M3 byte from its bit fields (OCP layout: sign, 4 exponent bits with
+    bias 7, 3 mantissa bits; 0x7F / 0xFF are NaN)."""
+    vals = np.zeros(256)
+    for code in range(256):
+        s = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            vals[code] = np.nan
+        elif e == 0:
+            vals[code] = s * m * 2.0 ** -9
+        else:
+            vals[code] = s * (1 + m / 8.0) * 2.0 ** (e - 7)
+    return vals

@@ -329,3 +329,149 @@ def test_host_side_argument_errors():
     with pytest.raises(EsmError) as e:
         _enc(synth.Geometry(1, 96, 3, 256), "bf16")  # head_dim 32 is not a bf16 geometry
     assert e.value.status == 2
+
+
+# --------------------------------------------------------------------------- FP8 (E4M3)
+# E4M3 keeps 3 mantissa bits: quantising ONE operand of the forward already moves the final
+# hidden states by ~3% rel L2, and a 1e-6 perturbation anywhere upstream flips enough
+# roundings to move a multi-layer FP8 result by ~1%.  So the FP8 path is pinned exactly at
+# the operation level (E4M3 GEMM on E4M3 inputs; LayerNorm -> E4M3 codes), end to end at
+# the stated 5e-2 on one layer, and at depth by its accuracy against the exact forward.
+_FP8_G = synth.Geometry(num_layers=1, hidden=1280, heads=20, ffn=5120)
+
+
+def _fp8_codes(rng, shape, table):
+    codes = rng.integers(0, 256, size=shape).astype(np.uint8)
+    codes[np.isnan(table[codes])] = 0
+    return codes
+
+
+def test_fp8_gemm_exact_on_e4m3_inputs():
+    """tcgen05 kind::f8f6f4 GEMM: products of E4M3 values are exact in fp32, so the only
+    difference from the float64 reference is fp32 accumulation: about K/32 rounded adds of
+    partial sums whose cancellation factor sum|ab| / |sum ab| is ~sqrt(K) for random signs,
+    i.e. ~ sqrt(K/32) * 2^-24 * sqrt(K) = 5e-5 at K = 5120 in the worst case; rms well
+    below.  Bound: 2e-5."""
+    from tests._util import e4m3_table
+    table = e4m3_table()
+    enc = _enc(_FP8_G, "fp8")
+    rng = np.random.default_rng(40)
+    for M, N, K in ((300, 512, 1280), (1, 256, 5120), (1000, 1280, 1280)):
+        A = _fp8_codes(rng, (M, K), table)
+        B = _fp8_codes(rng, (N, K), table)
+        b = _bf16(rng.standard_normal(N))
+        sa, sb = 3.0, 0.25
+        out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        enc.op_gemm_fp8("bias_f32", torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(),
+                        torch.tensor([sa], device="cuda"), torch.tensor([sb], device="cuda"),
+                        _dev(b, torch.bfloat16), out)
+        assert enc.check_status() == 0
+        ref = table[A] @ table[B].T / (sa * sb) + b
+        assert rel_l2(to_np(out), ref) < 2e-5, (M, N, K)
+    # GELU epilogue (bf16 output)
+    M, N, K = 200, 5120, 1280
+    A = _fp8_codes(rng, (M, K), table)
+    B = _fp8_codes(rng, (N, K), table)
+    b = _bf16(rng.standard_normal(N))
+    u = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    enc.op_gemm_fp8("gelu", torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(),
+                    torch.tensor([1e3], device="cuda"), torch.tensor([2e2], device="cuda"),
+                    _dev(b, torch.bfloat16), u)
+    ref = O.gelu(table[A] @ table[B].T / 2e5 + b)
+    assert rel_l2(to_np(u), ref) < 5e-3
+
+
+def test_fp8_layernorm_codes_match_oracle_rounding():
+    """LayerNorm -> E4M3: the codes equal the oracle's round-to-nearest-even of LN(x)*scale
+    except where fp32 and float64 LN(x) straddle a rounding midpoint (then the two codes are
+    neighbours); the amax is max |LN(x)|."""
+    from tests._util import e4m3_table
+    table = e4m3_table()
+    enc = _enc(_FP8_G, "fp8")
+    rng = np.random.default_rng(41)
+    rows, cols = 333, 1280
+    x = (rng.standard_normal((rows, cols)) * 2 + 0.5).astype(np.float32)
+    g = _bf16(1 + 0.3 * rng.standard_normal(cols))
+    bt = _bf16(0.3 * rng.standard_normal(cols))
+    scale = 61.0
+    y = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    enc.op_layernorm_e4m3(_dev(x, torch.float32), _dev(g, torch.bfloat16), _dev(bt, torch.bfloat16), y,
+                          torch.tensor([scale], device="cuda"), amax)
+    torch.cuda.synchronize()
+    ln = O.layer_norm(x.astype(np.float64), g.astype(np.float64), bt.astype(np.float64))
+    ref = O.e4m3_round(ln * scale)
+    got = table[y.cpu().numpy()]
+    diff = got != ref
+    assert diff.mean() < 1e-3
+    if diff.any():
+        r, gv = ref[diff], got[diff]
+        assert np.all(np.abs(gv - r) <= np.abs(r) / 8 + 2.0 ** -9)  # one E4M3 step apart
+    assert abs(amax.item() / np.abs(ln).max() - 1) < 1e-5
+
+
+def _fp8_run(g, lengths, seed, calls=3):
+    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
+    w = synth.model_weights(g, seed, "fp8")
+    tok = synth.tokens_for_lengths(np.random.default_rng(seed), lengths)
+    enc = EsmEncoder.from_geometry(g, "fp8", final_ln=True, amax_history_len=16)
+    dw = DeviceWeights(w, "fp8")
+    t, cu = packed_inputs(tok, lengths)
+    st0 = enc.get_fp8_state()
+    assert np.all(enc.fp8_scales(st0) == 1.0) and np.all(enc.fp8_history(st0) == 0.0)
+    for _ in range(calls):
+        enc.forward(dw, t, cu, max(lengths))
+    enc.check()
+    st = enc.get_fp8_state()
+    out = to_np(enc.forward(dw, t, cu, max(lengths)))
+    enc.check()
+    return enc, w, tok, st, out
+
+
+def test_fp8_forward_one_layer_and_delayed_scaling():
+    """One 650M-width layer with E4M3 GEMMs (history 16, max), attention in bf16.  After
+    three warm-up calls the scales are read back; the next call matches the oracle using
+    those scales within 5e-2, and that call's state update is exact: the history rolls by
+    one, weight amaxes equal max |w|, activation amaxes match, scale = 448 / max(history)."""
+    g = _FP8_G
+    lengths = [300, 1, 129, 64, 700]
+    enc, w, tok, st, out = _fp8_run(g, lengths, 31)
+    scales, hist = enc.fp8_scales(st), enc.fp8_history(st)
+    assert np.all(scales > 1.0)
+    fp8_state = [{k: float(scales[l, i]) for i, k in enumerate(O.FP8_TENSORS)} for l in range(g.num_layers)]
+    amax = [dict() for _ in range(g.num_layers)]
+    c = O.cu_seqlens(lengths)
+    ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, fp8_state=fp8_state, amax_out=amax,
+                          bf16_attention=True)
+    ref = np.concatenate([ref[i] for i in range(len(lengths))])
+    assert rel_l2(out, ref) < 5e-2
+    st2 = enc.get_fp8_state()
+    hist2, scales2 = enc.fp8_history(st2), enc.fp8_scales(st2)
+    for l in range(g.num_layers):
+        for i, k in enumerate(O.FP8_TENSORS):
+            assert np.array_equal(hist2[l, i, 1:], hist[l, i, :-1])    # rolled by one
+            if k.startswith("w_"):
+                assert hist2[l, i, 0] == np.float32(amax[l][k])          # weights: exact
+            else:
+                assert abs(hist2[l, i, 0] / amax[l][k] - 1) < 0.05, (l, k)
+            assert scales2[l, i] == np.float32(448.0) / hist2[l, i].max()
+
+
+def test_fp8_forward_depth_accuracy():
+    """Two 650M-width layers: the GPU's FP8 forward is as close to the exact (unquantised)
+    forward as the oracle's own FP8 forward with the same scales, and the two FP8 results
+    differ by less than two independent FP8 evaluations would (sqrt(2) x the FP8 error)."""
+    g = synth.Geometry(num_layers=2, hidden=1280, heads=20, ffn=5120)
+    lengths = [300, 1, 129, 64, 700]
+    enc, w, tok, st, out = _fp8_run(g, lengths, 32)
+    scales = enc.fp8_scales(st)
+    fp8_state = [{k: float(scales[l, i]) for i, k in enumerate(O.FP8_TENSORS)} for l in range(g.num_layers)]
+    c = O.cu_seqlens(lengths)
+    cat = lambda d: np.concatenate([d[i] for i in range(len(lengths))])
+    ref8 = cat(O.encode_packed(tok, c, w, g.heads, final_ln=True, fp8_state=fp8_state, bf16_attention=True))
+    exact = cat(O.encode_packed(tok, c, w, g.heads, final_ln=True))
+    e_oracle = rel_l2(ref8, exact)
+    e_gpu = rel_l2(out, exact)
+    assert e_oracle > 1e-2                      # quantisation really happened on both sides
+    assert e_gpu < 1.25 * e_oracle, (e_gpu, e_oracle)
+    assert rel_l2(out, ref8) < np.sqrt(2) * e_oracle

@@ -334,6 +334,32 @@ def test_segment_permutation_permutes_outputs():
         assert np.array_equal(out2[j], out[i])
 
 
+# --------------------------------------------------------------------------- bf16
+def test_bf16_round_vs_torch_cast():
+    rng = np.random.default_rng(18)
+    x = np.concatenate([rng.standard_normal(50000) * s for s in (1e-3, 1.0, 300.0)])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_round(x.astype(np.float32)), ref)
+    # exact halfway cases go to the even significand
+    assert O.bf16_round(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert O.bf16_round(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
+
+
+def test_bf16_attention_operands_are_rounded():
+    g = synth.TINY
+    w = _scaled_weights(g, 19)
+    wl = {k: np.asarray(v, np.float64) for k, v in w["layers"][0].items()}
+    rng = np.random.default_rng(20)
+    x = rng.standard_normal((9, g.hidden))
+    a = O.encoder_layer(x, np.arange(9), wl, g.heads)
+    b = O.encoder_layer(x, np.arange(9), wl, g.heads, bf16_attention=True)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 0 < rel < 2e-2
+    # rounding already-bf16 operands is the identity: attention on bf16 values is unchanged
+    q = O.bf16_round(rng.standard_normal((5, 2, 8)))
+    assert np.array_equal(O.bf16_round(q), q)
+
+
 # --------------------------------------------------------------------------- FP8
 def _e4m3_decode(code: int) -> float:
     """Decode one E4M3 byte from its bit fields (OCP definition)."""

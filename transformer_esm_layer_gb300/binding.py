@@ -26,7 +26,8 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_encoder_forward_host", "esm_encoder_forward_padded", "esm_encoder_check",
            "esm_encoder_debug_pack_index", "esm_op_layernorm", "esm_op_gemm", "esm_op_attention",
            "esm_encoder_get_fp8_state", "esm_encoder_set_fp8_state", "esm_encoder_set_profiling",
-           "esm_encoder_get_profile", "esm_op_attention_noalloc", "esm_status_string")
+           "esm_encoder_get_profile", "esm_op_attention_noalloc", "esm_op_layernorm_e4m3", "esm_op_gemm_fp8",
+           "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
 
 
@@ -86,6 +87,8 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_set_profiling": (i32, [vp, i32]),
         "esm_encoder_get_profile": (i32, [vp, ctypes.POINTER(EsmProfile), i32]),
         "esm_op_attention_noalloc": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+        "esm_op_layernorm_e4m3": (i32, [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp]),
+        "esm_op_gemm_fp8": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
         "esm_status_string": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -266,6 +269,21 @@ class EsmEncoder:
         N = B.shape[0]
         self._raise(self.lib.esm_op_gemm(self.handle, EPILOGUES[epi], _ptr(A), _ptr(B), _ptr(bias), _ptr(out),
                                          _ptr(pos_id), M, N, K, _stream_ptr(stream)), "esm_op_gemm")
+        return out
+
+    def op_layernorm_e4m3(self, x, gamma, beta, y, scale, amax, stream=None):
+        rows, cols = x.shape
+        self._raise(self.lib.esm_op_layernorm_e4m3(self.handle, _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, cols,
+                                                   _ptr(scale), _ptr(amax), _stream_ptr(stream)),
+                    "esm_op_layernorm_e4m3")
+        return y
+
+    def op_gemm_fp8(self, epi: str, A, B, a_scale, b_scale, bias, out, pos_id=None, stream=None):
+        M, K = A.shape
+        N = B.shape[0]
+        self._raise(self.lib.esm_op_gemm_fp8(self.handle, EPILOGUES[epi], _ptr(A), _ptr(B), _ptr(a_scale),
+                                             _ptr(b_scale), _ptr(bias), _ptr(out), _ptr(pos_id), M, N, K,
+                                             _stream_ptr(stream)), "esm_op_gemm_fp8")
         return out
 
     def op_attention(self, qkv, cu_seqlens, max_seqlen: int, o, workspace=None, stream=None):

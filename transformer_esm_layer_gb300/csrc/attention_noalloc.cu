@@ -96,7 +96,7 @@ extern "C" esm_status esm_op_attention_noalloc(const void* qkv, const int32_t* c
     return ESM_ERR_CUDA;
   const int max_items = (total_tokens + kAttnQTile - 1) / kAttnQTile + num_seqs;
   launch_pack_index(cu_seqlens, num_seqs, total_tokens, max_seqlen, kMaxTokens, pb, err, cs);
-  launch_attn_worklist(num_seqs, max_items, pb, cs);
+  launch_attn_worklist(num_seqs, max_items, kAttnQTile, pb, cs);
   launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), hidden, heads,
                         max_items, pb, cs);
   return cudaGetLastError() == cudaSuccess ? ESM_OK : ESM_ERR_CUDA;

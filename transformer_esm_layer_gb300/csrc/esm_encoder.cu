@@ -255,8 +255,8 @@ esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, co
     return cuda_status(cudaGetLastError());
   }
   const uint32_t elem = fp8 ? 1 : 2;
-  const CUtensorMap* ma = h->map(A, (uint64_t)M, (uint64_t)K, 128, elem);
-  const CUtensorMap* mb = h->map(B, (uint64_t)N, (uint64_t)K, 256, elem);
+  const CUtensorMap* ma = h->map(A, (uint64_t)M, (uint64_t)K, (uint32_t)gemm_tc_a_box_rows(), elem);
+  const CUtensorMap* mb = h->map(B, (uint64_t)N, (uint64_t)K, (uint32_t)gemm_tc_b_box_rows(), elem);
   if (!ma || !mb) return ESM_ERR_CUDA;
   cudaError_t e;
   PROF(h, cls, st, 1, e = launch_gemm_tc(epi, fp8, out_act, ma, mb, M, N, K, ea, h->num_sms, h->d_err, st));
@@ -305,12 +305,13 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
       ProfScope _ps(h, P_ATTN, st, 1);
       if (c.precision == ESM_FP32)
         launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(o), d, H, T, pb, st);
-      else if (fp8)
-        launch_attention_bf16_to_e4m3(static_cast<const __nv_bfloat16*>(qkv), static_cast<uint8_t*>(o), d, H,
-                                      max_items, pb, sc + X_O, am + X_O, st);
-      else
-        launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), d, H,
-                              max_items, pb, st);
+      else {
+        const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
+        if (!tq) return ESM_ERR_CUDA;
+        if (launch_attention_tc(tq, o, fp8 ? Act::E4M3 : Act::BF16, d, H, max_items, pb, sc + X_O, am + X_O,
+                                h->d_err, st) != cudaSuccess)
+          return ESM_ERR_CUDA;
+      }
     }
     s = run_gemm(h, P_OPROJ, ESM_EPI_RESIDUAL, o, fp8 ? (const void*)wq_o : w->w_o[l], w->b_o[l], x, nullptr, T, d, d, fp8,
                  Act::F32, sc + X_O, sc + W_O, nullptr, nullptr, st);
@@ -352,7 +353,7 @@ esm_status forward_impl(esm_encoder* h, const esm_weights* w, const int32_t* tok
   {
     ProfScope _ps(h, P_OTHER, st, h->cfg.precision != ESM_FP32 ? 3 : 2);
     launch_pack_index(cu, B, T, max_seqlen, h->cfg.max_positions, pb, h->d_err, st);
-    if (h->cfg.precision != ESM_FP32) launch_attn_worklist(B, L.max_items, pb, st);
+    if (h->cfg.precision != ESM_FP32) launch_attn_worklist(B, L.max_items, kAttnQTileTc, pb, st);
     launch_embed(tok, T, w->emb, !h->bf16_params(), h->cfg.vocab, h->cfg.hidden, h->cfg.emb_scale,
                  reinterpret_cast<float*>(b + L.x), h->d_err, st);
   }
@@ -514,7 +515,7 @@ esm_status esm_encoder_forward_padded(esm_encoder_t* h, const esm_weights* w, co
   {
     ProfScope _ps(h, P_OTHER, st, h->cfg.precision != ESM_FP32 ? 3 : 2);
     launch_pad_index(seq_lens, B, S, pb, h->d_err, st);
-    if (h->cfg.precision != ESM_FP32) launch_attn_worklist(B, L.max_items, pb, st);
+    if (h->cfg.precision != ESM_FP32) launch_attn_worklist(B, L.max_items, kAttnQTileTc, pb, st);
     launch_embed(token_ids, T, w->emb, !h->bf16_params(), h->cfg.vocab, h->cfg.hidden, h->cfg.emb_scale,
                  reinterpret_cast<float*>(b + L.x), h->d_err, st);
   }
@@ -580,6 +581,30 @@ esm_status esm_op_gemm(esm_encoder_t* h, esm_epilogue epi, const void* A, const 
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
+esm_status esm_op_layernorm_e4m3(esm_encoder_t* h, const float* x, const void* gamma, const void* beta, uint8_t* y,
+                                 int rows, int cols, const float* scale, float* amax, esm_stream_t stream) {
+  if (!h || !x || !gamma || !beta || !y || !scale || !amax || rows < 0 || cols <= 0 || cols % 4 || cols > 4096)
+    return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_FP8_E4M3) return ESM_ERR_UNSUPPORTED;
+  launch_layernorm(x, gamma, beta, false, y, Act::E4M3, rows, cols, h->cfg.ln_eps, scale, amax, nullptr, nullptr,
+                   nullptr, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status esm_op_gemm_fp8(esm_encoder_t* h, esm_epilogue epi, const uint8_t* A, const uint8_t* B, const float* a_scale,
+                           const float* b_scale, const void* bias, void* out, const int32_t* pos_id, int M, int N,
+                           int K, esm_stream_t stream) {
+  if (!h || !A || !B || !a_scale || !b_scale || !out || M < 0 || N <= 0 || K <= 0) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_FP8_E4M3) return ESM_ERR_UNSUPPORTED;
+  if (epi < ESM_EPI_BIAS_F32 || epi > ESM_EPI_GELU) return ESM_ERR_INVALID_ARG;
+  if (epi == ESM_EPI_QKV_ROPE && (!pos_id || N != 3 * h->cfg.hidden)) return ESM_ERR_INVALID_ARG;
+  if (K % 128 || N % 256 || !aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16)) return ESM_ERR_INVALID_ARG;
+  if (bias && !aligned(bias, 16)) return ESM_ERR_INVALID_ARG;
+  const Act out_act = (epi == ESM_EPI_BIAS_F32 || epi == ESM_EPI_RESIDUAL) ? Act::F32 : Act::BF16;
+  return run_gemm(h, P_OTHER, epi, A, B, bias, out, pos_id, M, N, K, true, out_act, a_scale, b_scale, nullptr,
+                  nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
 esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,
                             int total_tokens, int max_seqlen, void* o, void* workspace, size_t workspace_bytes,
                             esm_stream_t stream) {
@@ -599,9 +624,11 @@ esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu
   if (h->cfg.precision == ESM_FP32) {
     launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(o), d, H, total_tokens, pb, st);
   } else {
-    launch_attn_worklist(num_seqs, L.max_items, pb, st);
-    launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), d, H, L.max_items,
-                          pb, st);
+    launch_attn_worklist(num_seqs, L.max_items, kAttnQTileTc, pb, st);
+    const CUtensorMap* tq = h->map(qkv, (uint64_t)total_tokens, (uint64_t)3 * d, 128, 2);
+    if (!tq) return ESM_ERR_CUDA;
+    if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st) != cudaSuccess)
+      return ESM_ERR_CUDA;
   }
   return cuda_status(cudaGetLastError());
 }

@@ -2,14 +2,18 @@
 //
 //   C[M, N] = A[M, K] * B[N, K]^T      A: activations, B: nn.Linear-style weights
 //
-// One CTA per SM walks the output tiles (128 x 256) in a static stride.  Roles:
-//   warp 0       TMA producer: A and B K-slices (128-byte rows, 128-byte swizzle) into a
-//                4-stage shared-memory ring, completion on "full" mbarriers;
-//   warp 1       MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16 for bf16 /
-//                K=32 for e4m3) into one of two TMEM accumulators; tcgen05.commit frees
-//                ring stages and signals the finished accumulator;
-//   warps 2..9   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one output row),
-//                fused bias / RoPE / GELU / residual add, stores to global memory.
+// Clusters of two CTAs (one per SM) walk the 256 x 256 output tiles in a static stride;
+// the pair multiplies with tcgen05.mma.cta_group::2 (M = 256: 128 rows per CTA, B split by
+// N between the two CTAs, so each SM streams 32 KB per 64-wide K-slice).  Roles:
+//   warp 0       TMA producer (each CTA): its A rows and its half of B, K-slices of 128
+//                bytes with the 128-byte swizzle, into a 6-stage shared-memory ring; both
+//                CTAs' copies complete on the leader CTA's "full" mbarrier;
+//   warp 1       MMA issuer (leader CTA, one thread): tcgen05.mma (K=16 for bf16, K=32 for
+//                e4m3) into one of two TMEM accumulators; tcgen05.commit multicasts to both
+//                CTAs to free ring stages and to signal the finished accumulator;
+//   warps 2..9   epilogue (each CTA): tcgen05.ld of its accumulator half (one TMEM lane =
+//                one output row), fused bias / RoPE / GELU / residual add, global stores;
+//                each warp then arrives on the leader's "accumulator free" mbarrier.
 // Two accumulators (2 x 256 of the 512 TMEM columns) let the epilogue of one tile run
 // while the tensor core works on the next.  Every mbarrier wait is bounded: on timeout
 // the kernel latches an error bit, stops issuing work and still releases its TMEM.
@@ -25,18 +29,15 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int STAGES = 4;
 constexpr int ROW_BYTES = 128;                 // one K-slice row: 64 bf16 or 128 e4m3
 constexpr int A_STAGE = BM * ROW_BYTES;        // 16 KB
-constexpr int B_STAGE = BN * ROW_BYTES;        // 32 KB
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int TMEM_COLS = 2 * BN;              // two accumulators
-constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
 
 struct Smem {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[6];
+  uint64_t empty[6];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -175,31 +176,49 @@ __device__ __forceinline__ void epilogue_group(const EpiArgs& ea, int row, int N
   }
 }
 
-template <int EPI, bool FP8, Act OUT>
+// PAIR = false: one CTA per 128 x 256 tile (tcgen05 cta_group::1, M = 128).
+// PAIR = true:  a cluster of two CTAs per 256 x 256 tile (cta_group::2, M = 256): each CTA
+//               loads its own 128 rows of A and its half (128 rows) of B, the leader CTA
+//               issues the MMAs, each CTA's TMEM receives its 128 rows x 256 columns.
+template <bool PAIR>
+struct Geo {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBStage = (PAIR ? BN / 2 : BN) * ROW_BYTES;  // B rows this CTA loads
+  static constexpr int kSmem = kStages * (A_STAGE + kBStage) + 1024 + 256;
+};
+
+template <int EPI, bool FP8, Act OUT, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
                    int N, int K, EpiArgs ea, unsigned* err) {
+  constexpr int S = Geo<PAIR>::kStages;
+  constexpr int B_ST = Geo<PAIR>::kBStage;
+  constexpr int TILE_M = PAIR ? 2 * BM : BM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
-  uint8_t* sB = base + STAGES * A_STAGE;
-  Smem* sm = reinterpret_cast<Smem*>(sB + STAGES * B_STAGE);
+  uint8_t* sB = base + S * A_STAGE;
+  Smem* sm = reinterpret_cast<Smem*>(sB + S * B_ST);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_tiles = (M + BM - 1) / BM;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // cluster (or CTA) index
+  const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int m_tiles = (M + TILE_M - 1) / TILE_M;
   const int n_tiles = N / BN;
   const int num_tiles = m_tiles * n_tiles;
   const int kb_count = K / (FP8 ? 128 : 64);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&sm->full[s], 1);
       mbar_init(&sm->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sm->tfull[a], 1);
-      mbar_init(&sm->tempty[a], 32 * NUM_EPI_WARPS);
+      mbar_init(&sm->tempty[a], NUM_EPI_WARPS * (PAIR ? 2 : 1));  // one arrival per epilogue warp
     }
     mbar_init(&sm->mma_done, 1);
     sm->abort = 0;
@@ -209,50 +228,70 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(&sm->tmem_base, TMEM_COLS);
+  if (warp == 1) {
+    if (PAIR) tmem_alloc_pair(&sm->tmem_base, TMEM_COLS);
+    else tmem_alloc(&sm->tmem_base, TMEM_COLS);
+  }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers exist before anyone signals them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int issues = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !sm->abort; tile += gridDim.x) {
-        const int m0 = (tile / n_tiles) * BM;
-        const int n0 = (tile % n_tiles) * BN;
+      for (int tile = unit; tile < num_tiles && !sm->abort; tile += units) {
+        const int m0 = (tile / n_tiles) * TILE_M + (int)rank * BM;
+        const int n0 = (tile % n_tiles) * BN + (PAIR ? (int)rank * (BN / 2) : 0);
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!mbar_wait(&sm->empty[stage], phase ^ 1)) {
             latch_error(err, ERRBIT_TIMEOUT);
             sm->abort = 1;
             break;
           }
-          mbar_arrive_expect_tx(&sm->full[stage], A_STAGE + B_STAGE);
           const int kx = kb * (FP8 ? 128 : 64);
-          tma_load_2d(sA + stage * A_STAGE, &tmA, kx, m0, &sm->full[stage]);
-          tma_load_2d(sB + stage * B_STAGE, &tmB, kx, n0, &sm->full[stage]);
+          if (PAIR) {
+            // Both CTAs' copies complete on the leader's barrier; the leader arms it with
+            // the bytes of the whole pair.
+            if (leader) mbar_arrive_expect_tx(&sm->full[stage], 2 * (A_STAGE + B_ST));
+            const uint32_t bar = map_to_rank(&sm->full[stage], 0);
+            tma_load_2d_pair(sA + stage * A_STAGE, &tmA, kx, m0, bar);
+            tma_load_2d_pair(sB + stage * B_ST, &tmB, kx, n0, bar);
+          } else {
+            mbar_arrive_expect_tx(&sm->full[stage], A_STAGE + B_ST);
+            tma_load_2d(sA + stage * A_STAGE, &tmA, kx, m0, &sm->full[stage]);
+            tma_load_2d(sB + stage * B_ST, &tmB, kx, n0, &sm->full[stage]);
+          }
           ++issues;
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
-      // The copies of the last STAGES issues may still be in flight (only when the
-      // consumer gave up early): wait, bounded, until they have landed.
-      for (int i = issues - 1; i >= 0 && i >= issues - STAGES; --i)
-        if (!mbar_wait(&sm->full[i % STAGES], (uint32_t)(i / STAGES) & 1u)) break;
+      // The copies of the last S issues may still be in flight (only when a consumer gave
+      // up early): wait, bounded, until they have landed (the leader sees the whole pair's
+      // bytes; the peer waits for its stages to be released instead).
+      for (int i = issues - 1; i >= 0 && i >= issues - S; --i) {
+        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        if (!PAIR || leader) {
+          if (!mbar_wait(&sm->full[i % S], ph)) break;
+        } else {
+          if (!mbar_wait(&sm->empty[i % S], ph)) break;
+        }
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = FP8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN);
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3(TILE_M, BN) : idesc_bf16(TILE_M, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !sm->abort; tile += gridDim.x) {
+      for (int tile = unit; tile < num_tiles && !sm->abort; tile += units) {
         if (!mbar_wait(&sm->tempty[acc], acc_phase ^ 1)) {
           latch_error(err, ERRBIT_TIMEOUT);
           sm->abort = 1;
@@ -268,45 +307,52 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
-          const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+          const uint32_t b0 = smem_u32(sB + stage * B_ST);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
             const uint64_t ad = make_sw128_desc(a0 + 32 * k);
             const uint64_t bd = make_sw128_desc(b0 + 32 * k);
-            if (FP8)
-              mma_f8_ss(d_tmem, ad, bd, idesc, (kb | k) != 0);
-            else
-              mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            if (PAIR) {
+              if (FP8) mma_f8_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+              else mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            } else {
+              if (FP8) mma_f8_ss(d_tmem, ad, bd, idesc, (kb | k) != 0);
+              else mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            }
           }
-          mma_commit(&sm->empty[stage]);
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          if (PAIR) mma_commit_pair(&sm->empty[stage]);
+          else mma_commit(&sm->empty[stage]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
         }
         if (sm->abort) break;
-        mma_commit(&sm->tfull[acc]);
+        if (PAIR) mma_commit_pair(&sm->tfull[acc]);
+        else mma_commit(&sm->tfull[acc]);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
       // All MMAs of this thread complete before TMEM may be released.
-      mma_commit(&sm->mma_done);
+      if (PAIR) mma_commit_pair(&sm->mma_done);
+      else mma_commit(&sm->mma_done);
       mbar_wait(&sm->mma_done, 0);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;                   // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;         // which 128-column half of the tile
+    const uint32_t tempty_leader = PAIR ? map_to_rank(&sm->tempty[0], 0) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
     float amax = 0.f;
     float acc_scale = 1.f;
     if (FP8) acc_scale = 1.f / (__ldg(ea.a_scale) * __ldg(ea.b_scale));
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      if (!mbar_wait(&sm->tfull[acc], acc_phase)) {
+    for (int tile = unit; tile < num_tiles; tile += units) {
+      if (!mbar_wait_warp(&sm->tfull[acc], acc_phase)) {
         latch_error(err, ERRBIT_TIMEOUT);
         sm->abort = 1;
         break;
       }
       tc_fence_after();
-      const int row = (tile / n_tiles) * BM + q * 32 + lane;
+      const int row = (tile / n_tiles) * TILE_M + (int)rank * BM + q * 32 + lane;
       const int n0 = (tile % n_tiles) * BN + half * (BN / 2);
       const uint32_t tbase = tmem_base + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
@@ -316,8 +362,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(tbase + g + 32, v1);
         if (row < M) epilogue_group<EPI, FP8, OUT>(ea, row, N, n0 + g, v0, v1, acc_scale, amax);
       }
+      // This warp is done with the accumulator: one arrival per warp on the MMA issuer's
+      // barrier (in the leader CTA for a pair).
       tc_fence_before();
-      mbar_arrive(&sm->tempty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_remote(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
+        else mbar_arrive(&sm->tempty[acc]);
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if constexpr (OUT == Act::E4M3) {
@@ -328,32 +380,65 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) cluster_sync();  // nobody leaves while the peer may still touch its shared memory
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
 template <int EPI, bool FP8, Act OUT>
 cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, const EpiArgs& ea,
                         int num_sms, unsigned* err, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<EPI, FP8, OUT>;
-  static bool configured = false;  // per instantiation; the attribute is per device function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  constexpr bool PAIR = true;
+  auto kern = gemm_tc_kernel<EPI, FP8, OUT, PAIR>;
+  constexpr int smem = Geo<PAIR>::kSmem;
+  static int max_clusters = 0;  // per instantiation: co-resident clusters of two on this device
+  if (max_clusters == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess || n <= 0) n = num_sms / 2;
+    max_clusters = n;
   }
-  const int tiles = ((M + BM - 1) / BM) * (N / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, M, N, K, ea, err);
-  return cudaGetLastError();
+  const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * (N / BN);
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, M, N, K, ea, err);
 }
 
 }  // namespace
 
-int gemm_tc_smem_bytes() { return SMEM_BYTES; }
+int gemm_tc_smem_bytes() { return Geo<true>::kSmem; }
+// Rows of the TMA boxes the launched kernel expects: its own 128 rows of A, and its half of
+// the 256-wide B tile.
+int gemm_tc_a_box_rows() { return BM; }
+int gemm_tc_b_box_rows() { return BN / 2; }
 
 cudaError_t launch_gemm_tc(esm_epilogue epi, bool fp8, Act out_act, const CUtensorMap* tmA, const CUtensorMap* tmB,
                            int M, int N, int K, const EpiArgs& ea, int num_sms, unsigned* err, cudaStream_t st) {

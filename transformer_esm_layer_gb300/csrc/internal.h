@@ -11,8 +11,9 @@
 
 namespace esm {
 
-// Rows of one attention query tile.
+// Rows of one attention query tile (mma.sync kernel; the tcgen05 kernel uses 128).
 constexpr int kAttnQTile = 64;
+constexpr int kAttnQTileTc = 128;
 // Columns per RoPE table row (head_dim / 2, head_dim <= 64).
 constexpr int kRopeMaxHalf = 32;
 
@@ -33,7 +34,8 @@ void launch_pack_index(const int32_t* cu, int B, int T, int max_seqlen, int max_
                        const PackBuffers& pb, unsigned* err, cudaStream_t st);
 void launch_pad_index(const int32_t* seq_lens, int B, int S, const PackBuffers& pb, unsigned* err,
                       cudaStream_t st);
-void launch_attn_worklist(int B, int max_items, const PackBuffers& pb, cudaStream_t st);
+// Work items (segment, first query row) in tiles of q_tile rows, longest segments first.
+void launch_attn_worklist(int B, int max_items, int q_tile, const PackBuffers& pb, cudaStream_t st);
 void launch_embed(const int32_t* tok, int T, const void* emb, bool emb_f32, int vocab, int d, float scale,
                   float* x, unsigned* err, cudaStream_t st);
 void launch_rope_table(float2* tab, int max_pos, int half, float base, cudaStream_t st);
@@ -69,6 +71,10 @@ struct EpiArgs {
 // tcgen05 GEMM: A [M,K] bf16 (or e4m3), B [N,K] bf16 (or e4m3); K % 64 == 0 (bf16) or
 // K % 128 == 0 (e4m3); N % 256 == 0.
 int gemm_tc_smem_bytes();
+// Box heights of the A and B tensor maps launch_gemm_tc expects (each CTA of a pair loads
+// 128 rows of A and 128 rows of the 256-row B tile).
+int gemm_tc_a_box_rows();
+int gemm_tc_b_box_rows();
 cudaError_t launch_gemm_tc(esm_epilogue epi, bool fp8, Act out_act, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, int M, int N, int K, const EpiArgs& ea, int num_sms,
                            unsigned* err, cudaStream_t st);
@@ -86,6 +92,12 @@ void launch_attention_bf16(const __nv_bfloat16* qkv, __nv_bfloat16* o, int d, in
                            const PackBuffers& pb, cudaStream_t st);
 void launch_attention_bf16_to_e4m3(const __nv_bfloat16* qkv, uint8_t* o, int d, int heads, int max_items,
                                    const PackBuffers& pb, const float* q_scale, float* amax, cudaStream_t st);
+// tcgen05 attention (head_dim 64): tm_qkv is a tensor map over qkv [T, 3d] bf16 with a
+// 64 x 128 box and the 128-byte swizzle; work items in tiles of kAttnQTileTc rows.
+int attention_tc_smem_bytes();
+cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int d, int heads, int max_items,
+                                const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
+                                cudaStream_t st);
 void launch_attention_f32(const float* qkv, float* o, int d, int heads, int T, const PackBuffers& pb,
                           cudaStream_t st);
 

@@ -69,7 +69,7 @@ constexpr int WL_SORT_MAX = 4096;
 // Single CTA: list the (segment, query-tile) work items of the attention kernel, longest
 // segments first so that the costliest tiles start in the first wave (when B is small
 // enough to rank in shared memory; otherwise in segment order).
-__global__ void __launch_bounds__(WL_THREADS) attn_worklist_kernel(int B, int max_items, PackBuffers pb) {
+__global__ void __launch_bounds__(WL_THREADS) attn_worklist_kernel(int B, int max_items, int q_tile, PackBuffers pb) {
   __shared__ int s_len[WL_SORT_MAX];
   __shared__ int s_order[WL_SORT_MAX];
   __shared__ int s_warp[WL_THREADS / 32];
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(WL_THREADS) attn_worklist_kernel(int B, int ma
     int seg = -1, tiles = 0;
     if (r < B) {
       seg = sorted ? s_order[r] : r;
-      tiles = (pb.seg_qlen[seg] + kAttnQTile - 1) / kAttnQTile;
+      tiles = (pb.seg_qlen[seg] + q_tile - 1) / q_tile;
     }
     // block exclusive scan of `tiles`
     int v = tiles;
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(WL_THREADS) attn_worklist_kernel(int B, int ma
       const int k = excl + t;
       if (k < max_items) {
         pb.work[2 * k] = seg;
-        pb.work[2 * k + 1] = t * kAttnQTile;
+        pb.work[2 * k + 1] = t * q_tile;
       }
     }
     __syncthreads();
@@ -194,8 +194,8 @@ void launch_pad_index(const int32_t* seq_lens, int B, int S, const PackBuffers& 
   pad_index_kernel<<<B, 256, 0, st>>>(seq_lens, B, S, pb, err);
 }
 
-void launch_attn_worklist(int B, int max_items, const PackBuffers& pb, cudaStream_t st) {
-  attn_worklist_kernel<<<1, WL_THREADS, 0, st>>>(B, max_items, pb);
+void launch_attn_worklist(int B, int max_items, int q_tile, const PackBuffers& pb, cudaStream_t st) {
+  attn_worklist_kernel<<<1, WL_THREADS, 0, st>>>(B, max_items, q_tile, pb);
 }
 
 void launch_embed(const int32_t* tok, int T, const void* emb, bool emb_f32, int vocab, int d, float scale, float* x,
