@@ -47,6 +47,14 @@ struct AttnSmem {
 };
 constexpr int SMEM_BYTES = TILE_BYTES * (1 + 2 * STG) + 1024 + 256;
 
+// 2^x on the special-function unit (the hardware ex2 instruction, flushing subnormal
+// results to zero; P values that small are below bf16 resolution of the row sum anyway).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -187,15 +195,28 @@ __global__ void __launch_bounds__(THREADS, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->s_free);
       const int kvalid = klen - j * KT;  // keys >= kvalid lie past the sequence end
-      float mt = -INFINITY;
+      // scale, mask (last tile only) and row max with 8 independent chains
+      float mx[8];
 #pragma unroll
-      for (int i = 0; i < KT; ++i) {
-        s[i] = i < kvalid ? s[i] * c : -INFINITY;
-        mt = fmaxf(mt, s[i]);
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      if (kvalid >= KT) {
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+          s[i] *= c;
+          mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+          s[i] = i < kvalid ? s[i] * c : -INFINITY;
+          mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+        }
       }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool need = mt > m_ref + kRescaleThreshold;
       const float m_new = need ? mt : m_ref;
-      const float f = need ? exp2f(m_ref - m_new) : 1.f;  // 0 on the first tile
+      const float f = need ? fast_exp2(m_ref - m_new) : 1.f;  // 0 on the first tile
       if (j > 0) {
         if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(j - 1) & 1u)) { ok = false; break; }
         tc_fence_after();
@@ -214,18 +235,22 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       l *= f;
       m_ref = m_new;
+      float ls[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < KT / 32; ++ch) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = exp2f(s[32 * ch + 2 * i] - m_ref);
-          const float p1 = exp2f(s[32 * ch + 2 * i + 1] - m_ref);
-          l += p0 + p1;
+          const float p0 = fast_exp2(s[32 * ch + 2 * i] - m_ref);
+          const float p1 = fast_exp2(s[32 * ch + 2 * i + 1] - m_ref);
+          ls[i & 7] += p0 + p1;
           w[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tmem + lane_off + COL_P + 16 * ch, w);
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -152,7 +152,10 @@ struct esm_encoder {
     cuuint64_t strides[1] = {cols * elem};
     cuuint32_t box[2] = {128u / elem, box_rows};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = fn(&m, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    const CUtensorMapDataType dt = elem == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = fn(&m, dt, 2,
                     const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return nullptr;
@@ -257,9 +260,11 @@ esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, co
   const uint32_t elem = fp8 ? 1 : 2;
   const CUtensorMap* ma = h->map(A, (uint64_t)M, (uint64_t)K, (uint32_t)gemm_tc_a_box_rows(), elem);
   const CUtensorMap* mb = h->map(B, (uint64_t)N, (uint64_t)K, (uint32_t)gemm_tc_b_box_rows(), elem);
-  if (!ma || !mb) return ESM_ERR_CUDA;
+  const uint32_t out_elem = out_act == Act::F32 ? 4u : out_act == Act::BF16 ? 2u : 1u;
+  const CUtensorMap* mo = h->map(out, (uint64_t)M, (uint64_t)N, (uint32_t)gemm_tc_out_box_rows(), out_elem);
+  if (!ma || !mb || !mo) return ESM_ERR_CUDA;
   cudaError_t e;
-  PROF(h, cls, st, 1, e = launch_gemm_tc(epi, fp8, out_act, ma, mb, M, N, K, ea, h->num_sms, h->d_err, st));
+  PROF(h, cls, st, 1, e = launch_gemm_tc(epi, fp8, out_act, ma, mb, mo, M, N, K, ea, h->num_sms, h->d_err, st));
   return cuda_status(e);
 }
 

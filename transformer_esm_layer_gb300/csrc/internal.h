@@ -75,9 +75,12 @@ int gemm_tc_smem_bytes();
 // 128 rows of A and 128 rows of the 256-row B tile).
 int gemm_tc_a_box_rows();
 int gemm_tc_b_box_rows();
+int gemm_tc_out_box_rows();
+// tmO: the output [M, N] (fp32, bf16 or e4m3) with a 128-byte x gemm_tc_out_box_rows() box
+// and the 128-byte swizzle; for ESM_EPI_RESIDUAL it is also read (the residual stream).
 cudaError_t launch_gemm_tc(esm_epilogue epi, bool fp8, Act out_act, const CUtensorMap* tmA,
-                           const CUtensorMap* tmB, int M, int N, int K, const EpiArgs& ea, int num_sms,
-                           unsigned* err, cudaStream_t st);
+                           const CUtensorMap* tmB, const CUtensorMap* tmO, int M, int N, int K, const EpiArgs& ea,
+                           int num_sms, unsigned* err, cudaStream_t st);
 
 // SIMT fp32 GEMM (the ESM_FP32 precision): any M, N, K.
 void launch_gemm_f32(esm_epilogue epi, const float* A, const float* B, int M, int N, int K,
