@@ -5,22 +5,26 @@
 // run over cu_seqlens in thd format; BioNeMo ESM-2 model card: bidirectional encoder):
 //   o_t = sum_s softmax_s(q_t . k_s / 8) v_s.
 //
-// One CTA = one (sequence, 128-query tile, head) work item of the length-ordered list.
-//   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into a 2-stage ring
-//               (128-byte rows with the 128-byte swizzle, straight from the packed qkv
-//               buffer: x = column of the head, y = token row).
-//   warp 1      one thread issues the MMAs:  S = Q K^T  (M=128, N=128, K=64) into TMEM, and
-//               O += P V  (M=128, N=64, K=128) with P read from TMEM and V as an MN-major
-//               shared-memory operand.  S of tile j+1 is issued before P V of tile j, so the
-//               tensor core works while the softmax warps exponentiate.
-//   warps 2..5  softmax: thread r owns query row r.  It loads its whole S row from TMEM,
-//               masks keys past the sequence end, and keeps a running reference max m with
-//               a lazy update: O and the running sum l are rescaled (in TMEM) only when a
-//               tile's max exceeds m by more than 8 (in log2 units), so P stays <= 2^8 and
-//               most tiles need no rescale.  P = 2^(s*log2e/8 - m) goes back to TMEM as
-//               bf16; at the end O / l is written as bf16 (or E4M3 with the FP8 scale).
-// Tensor memory: S 128 columns, P 64 (bf16 pairs), O 64 -> 256 columns, so two CTAs share
-// an SM and one CTA's softmax overlaps the other's MMAs.  Every mbarrier wait is bounded.
+// Persistent: two CTAs per SM walk the (sequence, 128-query tile, head) work items of the
+// length-ordered list in a static stride; barrier phases run on across items.
+//   warp 0      TMA: each item's Q tile (double-buffered, 128-byte swizzle) and its K and V
+//               tiles of 128 keys into a 2-stage ring, straight from the packed qkv buffer
+//               (x = column of the head, y = token row).
+//   warp 1      one thread issues the MMAs of a global sequence of key tiles g:
+//               S(g) = Q K^T (M=128, N=128, K=64) into TMEM, then O += P V for tile g-1
+//               (M=128, N=64, K=128; P read from TMEM, V an MN-major shared-memory operand),
+//               so the tensor core computes the next S while the softmax warps exponentiate,
+//               also across item boundaries.
+//   warps 2..5  softmax: thread r owns query row r.  It reads its S row from TMEM twice in
+//               32-column chunks (row max, then exponentials), masks keys past the sequence
+//               end, and keeps a running reference max m with a lazy
+//               update: O and the running sum l are rescaled (in TMEM) only when a tile's max
+//               exceeds m by more than 8 (log2 units), so P stays <= 2^8.  P = 2^(s*log2e/8
+//               - m) goes back to TMEM as bf16; after an item's last tile O / l is stored as
+//               bf16 (or E4M3 with the FP8 scale).  Writing the next item's first P happens
+//               after O was read, which is what lets that item's first P V overwrite O.
+// Tensor memory: S 128 columns, P 64 (bf16 pairs), O 64 -> 256 columns per CTA.  Every
+// mbarrier wait is bounded.
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,19 +37,20 @@ constexpr int KT = 128;
 constexpr int STG = 2;
 constexpr int TILE_BYTES = 128 * 128;  // 128 rows x 128 bytes
 constexpr int THREADS = 192;
+constexpr int CTAS_PER_SM = 2;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_S = 0, COL_P = 128, COL_O = 192;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct AttnSmem {
-  uint64_t q_full;
-  uint64_t kv_full[STG];
-  uint64_t kv_empty[STG];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[STG], kv_empty[STG];
   uint64_t s_full, s_free, p_full, pv_done, mma_done;
   uint32_t tmem_base;
   volatile int abort;
 };
-constexpr int SMEM_BYTES = TILE_BYTES * (1 + 2 * STG) + 1024 + 256;
+// [Q0][Q1][K0][V0][K1][V1] then the barriers
+constexpr int SMEM_BYTES = TILE_BYTES * (2 + 2 * STG) + 1024 + 256;
 
 // 2^x on the special-function unit (the hardware ex2 instruction, flushing subnormal
 // results to zero; P values that small are below bf16 resolution of the row sum anyway).
@@ -64,30 +69,43 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+struct Item {
+  int start, q0, qrows, klen, nkb, h;
+};
+
+__device__ __forceinline__ Item decode_item(const PackBuffers& pb, int it, int heads) {
+  Item x;
+  const int w = it / heads;
+  x.h = it - w * heads;
+  const int seg = pb.work[2 * w];
+  x.q0 = pb.work[2 * w + 1];
+  x.start = pb.seg_start[seg];
+  x.qrows = min(QT, pb.seg_qlen[seg] - x.q0);
+  x.klen = pb.seg_klen[seg];
+  x.nkb = (x.klen + KT - 1) / KT;
+  return x;
+}
+
 template <Act OUT>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm, void* __restrict__ o, int d, int heads,
                         PackBuffers pb, const float* q_scale, float* amax_out, unsigned* err) {
-  const int item = blockIdx.x / heads;
-  const int h = blockIdx.x - item * heads;
-  if (item >= *pb.work_count) return;  // whole CTA, before any barrier or TMEM use
-  const int seg = pb.work[2 * item];
-  const int q0 = pb.work[2 * item + 1];
-  const int start = pb.seg_start[seg];
-  const int qrows = min(QT, pb.seg_qlen[seg] - q0);
-  const int klen = pb.seg_klen[seg];
-  const int nkb = (klen + KT - 1) / KT;
+  const int n_items = *pb.work_count * heads;
+  if ((int)blockIdx.x >= n_items) return;  // whole CTA, before any barrier or TMEM use
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sK = base + TILE_BYTES;                 // stage s: sK + 2*s*TILE_BYTES
-  uint8_t* sV = base + 2 * TILE_BYTES;             // stage s: sV + 2*s*TILE_BYTES
-  AttnSmem* sm = reinterpret_cast<AttnSmem*>(base + TILE_BYTES * (1 + 2 * STG));
+  uint8_t* sQ = base;                       // buffer b: sQ + b * TILE_BYTES
+  uint8_t* sK = base + 2 * TILE_BYTES;      // stage s: sK + 2 * s * TILE_BYTES
+  uint8_t* sV = base + 3 * TILE_BYTES;      // stage s: sV + 2 * s * TILE_BYTES
+  AttnSmem* sm = reinterpret_cast<AttnSmem*>(base + TILE_BYTES * (2 + 2 * STG));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&sm->q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm->q_full[b], 1);
+      mbar_init(&sm->q_empty[b], 1);
+    }
     for (int s = 0; s < STG; ++s) {
       mbar_init(&sm->kv_full[s], 1);
       mbar_init(&sm->kv_empty[s], 1);
@@ -110,26 +128,35 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&sm->q_full, TILE_BYTES);
-      tma_load_2d(sQ, &tm, h * DH, start + q0, &sm->q_full);
-      int issued = 0;
-      for (int j = 0; j < nkb && !sm->abort; ++j) {
-        const int st = j % STG;
-        const uint32_t ph = (uint32_t)(j / STG) & 1u;
-        if (!mbar_wait(&sm->kv_empty[st], ph ^ 1u)) {
+      int g = 0, qi = 0;
+      for (int it = blockIdx.x; it < n_items && !sm->abort; it += gridDim.x, ++qi) {
+        const Item x = decode_item(pb, it, heads);
+        const int qb = qi & 1;
+        if (!mbar_wait(&sm->q_empty[qb], ((uint32_t)(qi >> 1) & 1u) ^ 1u)) {
           latch_error(err, ERRBIT_TIMEOUT);
           sm->abort = 1;
           break;
         }
-        mbar_arrive_expect_tx(&sm->kv_full[st], 2 * TILE_BYTES);
-        tma_load_2d(sK + 2 * st * TILE_BYTES, &tm, d + h * DH, start + j * KT, &sm->kv_full[st]);
-        tma_load_2d(sV + 2 * st * TILE_BYTES, &tm, 2 * d + h * DH, start + j * KT, &sm->kv_full[st]);
-        ++issued;
+        mbar_arrive_expect_tx(&sm->q_full[qb], TILE_BYTES);
+        tma_load_2d(sQ + qb * TILE_BYTES, &tm, x.h * DH, x.start + x.q0, &sm->q_full[qb]);
+        for (int j = 0; j < x.nkb; ++j, ++g) {
+          const int st = g % STG;
+          if (!mbar_wait(&sm->kv_empty[st], ((uint32_t)(g / STG) & 1u) ^ 1u)) {
+            latch_error(err, ERRBIT_TIMEOUT);
+            sm->abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm->kv_full[st], 2 * TILE_BYTES);
+          tma_load_2d(sK + 2 * st * TILE_BYTES, &tm, d + x.h * DH, x.start + j * KT, &sm->kv_full[st]);
+          tma_load_2d(sV + 2 * st * TILE_BYTES, &tm, 2 * d + x.h * DH, x.start + j * KT, &sm->kv_full[st]);
+        }
       }
-      // wait (bounded) for copies that may still be in flight before the CTA can exit
-      mbar_wait(&sm->q_full, 0);
-      for (int j = issued - 1; j >= 0 && j >= issued - STG; --j)
-        if (!mbar_wait(&sm->kv_full[j % STG], (uint32_t)(j / STG) & 1u)) break;
+      // Copies still in flight can only exist if a consumer gave up early: then the last
+      // STG stages are waited for (bounded) before the CTA exits.
+      if (sm->abort) {
+        for (int k = g - 1; k >= 0 && k >= g - STG; --k)
+          if (!mbar_wait(&sm->kv_full[k % STG], (uint32_t)(k / STG) & 1u)) break;
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -137,34 +164,43 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(QT, KT);
       constexpr uint32_t idesc_pv = idesc_bf16(QT, DH) | (1u << 16);  // B (= V) MN-major
-      bool ok = mbar_wait(&sm->q_full, 0);
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&sm->p_full, (uint32_t)i & 1u)) return false;
+      bool ok = true;
+      int g = 0, qi = 0;
+      bool prev_first = false;  // tile g-1 was the first tile of its item
+      auto issue_pv = [&](int gp, bool first) -> bool {
+        if (!mbar_wait(&sm->p_full, (uint32_t)gp & 1u)) return false;
         tc_fence_after();
-        const uint32_t v0 = smem_u32(sV + 2 * (i % STG) * TILE_BYTES);
+        const uint32_t v0 = smem_u32(sV + 2 * (gp % STG) * TILE_BYTES);
 #pragma unroll
         for (int k = 0; k < KT / 16; ++k)
           mma_bf16_ts(tmem + COL_O, tmem + COL_P + 8 * k, make_sw128_desc(v0 + 2048 * k), idesc_pv,
-                      (i > 0 || k > 0) ? 1u : 0u);
+                      (!first || k > 0) ? 1u : 0u);
         mma_commit(&sm->pv_done);
-        mma_commit(&sm->kv_empty[i % STG]);
+        mma_commit(&sm->kv_empty[gp % STG]);
         return true;
       };
-      for (int j = 0; j < nkb && ok; ++j) {
-        const int st = j % STG;
-        if (!mbar_wait(&sm->kv_full[st], (uint32_t)(j / STG) & 1u)) { ok = false; break; }
-        if (j > 0 && !mbar_wait(&sm->s_free, (uint32_t)(j - 1) & 1u)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(sQ);
-        const uint32_t b0 = smem_u32(sK + 2 * st * TILE_BYTES);
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++qi) {
+        const Item x = decode_item(pb, it, heads);
+        const int qb = qi & 1;
+        if (!mbar_wait(&sm->q_full[qb], (uint32_t)(qi >> 1) & 1u)) { ok = false; break; }
+        const uint32_t a0 = smem_u32(sQ + qb * TILE_BYTES);
+        for (int j = 0; j < x.nkb; ++j, ++g) {
+          const int st = g % STG;
+          if (!mbar_wait(&sm->kv_full[st], (uint32_t)(g / STG) & 1u)) { ok = false; break; }
+          if (g > 0 && !mbar_wait(&sm->s_free, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(sK + 2 * st * TILE_BYTES);
 #pragma unroll
-        for (int k = 0; k < DH / 16; ++k)
-          mma_bf16_ss(tmem + COL_S, make_sw128_desc(a0 + 32 * k), make_sw128_desc(b0 + 32 * k), idesc_s,
-                      k > 0 ? 1u : 0u);
-        mma_commit(&sm->s_full);
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+          for (int k = 0; k < DH / 16; ++k)
+            mma_bf16_ss(tmem + COL_S, make_sw128_desc(a0 + 32 * k), make_sw128_desc(b0 + 32 * k), idesc_s,
+                        k > 0 ? 1u : 0u);
+          mma_commit(&sm->s_full);
+          if (j == x.nkb - 1) mma_commit(&sm->q_empty[qb]);  // Q buffer free once these S are done
+          if (g > 0 && !issue_pv(g - 1, prev_first)) { ok = false; break; }
+          prev_first = (j == 0);
+        }
       }
-      if (ok && nkb > 0) ok = issue_pv(nkb - 1);
+      if (ok && g > 0) ok = issue_pv(g - 1, prev_first);
       if (!ok) {
         latch_error(err, ERRBIT_TIMEOUT);
         sm->abort = 1;
@@ -178,49 +214,44 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int r = (warp & 3) * 32 + lane;                 // query row of this thread
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c = 1.4426950408889634f / sqrtf((float)DH);
-    float m_ref = -INFINITY, l = 0.f;
+    const float qs = (OUT == Act::E4M3) ? __ldg(q_scale) : 1.f;
+    float amax = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkb; ++j) {
-      if (!mbar_wait_warp(&sm->s_full, (uint32_t)j & 1u)) { ok = false; break; }
-      tc_fence_after();
-      float s[KT];
-#pragma unroll
-      for (int ch = 0; ch < KT / 32; ++ch) {
-        float v[32];
-        tmem_ld32(tmem + lane_off + COL_S + 32 * ch, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * ch + i] = v[i];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->s_free);
-      const int kvalid = klen - j * KT;  // keys >= kvalid lie past the sequence end
-      // scale, mask (last tile only) and row max with 8 independent chains
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-      if (kvalid >= KT) {
-#pragma unroll
-        for (int i = 0; i < KT; ++i) {
-          s[i] *= c;
-          mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < KT; ++i) {
-          s[i] = i < kvalid ? s[i] * c : -INFINITY;
-          mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-        }
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const bool need = mt > m_ref + kRescaleThreshold;
-      const float m_new = need ? mt : m_ref;
-      const float f = need ? fast_exp2(m_ref - m_new) : 1.f;  // 0 on the first tile
-      if (j > 0) {
-        if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(j - 1) & 1u)) { ok = false; break; }
+    int g = 0;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item x = decode_item(pb, it, heads);
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < x.nkb; ++j, ++g) {
+        if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {  // warp-collective TMEM round trip of O
+        const int kvalid = x.klen - j * KT;  // keys >= kvalid lie past the sequence end
+        // pass 1: row max of the raw scores (32-column chunks straight from TMEM)
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int ch = 0; ch < KT / 32; ++ch) {
+          float sv[32];
+          tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          tmem_ld_wait();
+          if (kvalid < KT) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[i] = 32 * ch + i < kvalid ? sv[i] : -INFINITY;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+        }
+        const float mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const bool need = mt > m_ref + kRescaleThreshold;
+        const float m_new = need ? mt : m_ref;
+        const float f = need ? fast_exp2(m_ref - m_new) : 1.f;  // 0 on the first tile
+        // P (and, within an item, O) may be rewritten once the previous P V is done
+        if (g > 0) {
+          if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {  // warp-collective TMEM round trip of O
 #pragma unroll
           for (int ch = 0; ch < DH / 32; ++ch) {
             float v[32];
@@ -232,77 +263,89 @@ __global__ void __launch_bounds__(THREADS, 2)
           }
           tmem_st_wait();
         }
-      }
-      l *= f;
-      m_ref = m_new;
-      float ls[8];
+        l *= f;
+        m_ref = m_new;
+        // pass 2: P = 2^(s*c - m) chunk by chunk, back to TMEM as bf16 pairs
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+        for (int ch = 0; ch < KT / 32; ++ch) {
+          float sv[32];
+          tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          tmem_ld_wait();
+          if (kvalid < KT) {
 #pragma unroll
-      for (int ch = 0; ch < KT / 32; ++ch) {
-        uint32_t w[16];
+            for (int i = 0; i < 32; ++i) sv[i] = 32 * ch + i < kvalid ? sv[i] : -INFINITY;
+          }
+          uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(s[32 * ch + 2 * i] - m_ref);
-          const float p1 = fast_exp2(s[32 * ch + 2 * i + 1] - m_ref);
-          ls[i & 7] += p0 + p1;
-          w[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = fast_exp2(fmaf(sv[2 * i], c, -m_ref));
+            const float p1 = fast_exp2(fmaf(sv[2 * i + 1], c, -m_ref));
+            ls[i & 3] += p0 + p1;
+            w[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tmem + lane_off + COL_P + 16 * ch, w);
         }
-        tmem_st16(tmem + lane_off + COL_P + 16 * ch, w);
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm->s_free);  // S was last read in pass 2
+          mbar_arrive(&sm->p_full);
+        }
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->p_full);
-    }
-    if (ok && nkb > 0 && mbar_wait_warp(&sm->pv_done, (uint32_t)(nkb - 1) & 1u)) {
+      if (!ok) break;
+      // ---- item epilogue: O / l -> global
+      if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
       tc_fence_after();
-      float out[DH];
-#pragma unroll
-      for (int ch = 0; ch < DH / 32; ++ch) {
-        float v[32];
-        tmem_ld32(tmem + lane_off + COL_O + 32 * ch, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) out[32 * ch + i] = v[i];
-      }
+      uint32_t u[2][32];
+      tmem_ld32_nowait(tmem + lane_off + COL_O, u[0]);
+      tmem_ld32_nowait(tmem + lane_off + COL_O + 32, u[1]);
+      tmem_ld_wait();
+      tc_fence_before();
       const float inv = 1.f / l;
-      if (r < qrows) {
-        const size_t off = (size_t)(start + q0 + r) * d + h * DH;
+      if (r < x.qrows) {
+        const size_t off = (size_t)(x.start + x.q0 + r) * d + x.h * DH;
         if constexpr (OUT == Act::BF16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + off);
 #pragma unroll
           for (int i = 0; i < DH / 8; ++i) {
-            uint4 w;
-            w.x = pack_bf16x2(out[8 * i] * inv, out[8 * i + 1] * inv);
-            w.y = pack_bf16x2(out[8 * i + 2] * inv, out[8 * i + 3] * inv);
-            w.z = pack_bf16x2(out[8 * i + 4] * inv, out[8 * i + 5] * inv);
-            w.w = pack_bf16x2(out[8 * i + 6] * inv, out[8 * i + 7] * inv);
-            dst[i] = w;
+            const uint32_t* w = &u[i >> 2][(i & 3) * 8];
+            uint4 q;
+            q.x = pack_bf16x2(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv);
+            q.y = pack_bf16x2(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv);
+            q.z = pack_bf16x2(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv);
+            q.w = pack_bf16x2(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv);
+            dst[i] = q;
           }
         } else {
-          const float qs = __ldg(q_scale);
-          float amax = 0.f;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(o) + off);
 #pragma unroll
           for (int i = 0; i < DH / 16; ++i) {
-            uint32_t w[4];
+            uint32_t w4[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float* f4 = &out[16 * i + 4 * k];
-              const float a0 = f4[0] * inv, a1 = f4[1] * inv, a2 = f4[2] * inv, a3 = f4[3] * inv;
+              const uint32_t* w = &u[i >> 1][(i & 1) * 16 + 4 * k];
+              const float a0 = __uint_as_float(w[0]) * inv, a1 = __uint_as_float(w[1]) * inv;
+              const float a2 = __uint_as_float(w[2]) * inv, a3 = __uint_as_float(w[3]) * inv;
               amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
               __nv_fp8x4_e4m3 qv(make_float4(a0 * qs, a1 * qs, a2 * qs, a3 * qs));
-              w[k] = *reinterpret_cast<uint32_t*>(&qv);
+              w4[k] = *reinterpret_cast<uint32_t*>(&qv);
             }
-            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          atomic_max_nonneg(amax_out, amax);
         }
       }
-    } else if (!ok) {
+    }
+    if (!ok) {
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
+    }
+    if constexpr (OUT == Act::E4M3) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (lane == 0) atomic_max_nonneg(amax_out, amax);
     }
   }
 
@@ -322,6 +365,7 @@ cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int
                                 const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
                                 cudaStream_t st) {
   if (max_items <= 0) return cudaSuccess;
+  static int num_sms = 0;
   static bool configured[2] = {false, false};
   const int which = out == Act::E4M3 ? 1 : 0;
   if (!configured[which]) {
@@ -332,7 +376,16 @@ cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int
     if (e != cudaSuccess) return e;
     configured[which] = true;
   }
-  const unsigned grid = (unsigned)max_items * (unsigned)heads;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms <= 0)
+      num_sms = 148;
+  }
+  // persistent: at most CTAS_PER_SM CTAs per SM; CTAs past the (device-side) item count exit
+  const long long items = (long long)max_items * heads;
+  const long long cap = (long long)CTAS_PER_SM * num_sms;
+  const unsigned grid = (unsigned)(items < cap ? items : cap);
   if (which)
     attention_tc_kernel<Act::E4M3><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, err);
   else
