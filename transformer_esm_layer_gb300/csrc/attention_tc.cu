@@ -225,21 +225,25 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
         const int kvalid = x.klen - j * KT;  // keys >= kvalid lie past the sequence end
-        // pass 1: row max of the raw scores (32-column chunks straight from TMEM)
+        // pass 1: row max of the raw scores (all four 32-column chunks in flight at once)
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        {
+          uint32_t su[KT / 32][32];
 #pragma unroll
-        for (int ch = 0; ch < KT / 32; ++ch) {
-          float sv[32];
-          tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv));
-          tmem_ld_wait();
+          for (int ch = 0; ch < KT / 32; ++ch) tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * ch, su[ch]);
+#pragma unroll
+          for (int ch = 0; ch < KT / 32; ++ch) tmem_ld_wait_regs(su[ch]);
+          float sv[KT];
+#pragma unroll
+          for (int i = 0; i < KT; ++i) sv[i] = __uint_as_float(su[i >> 5][i & 31]);
           if (kvalid < KT) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] = 32 * ch + i < kvalid ? sv[i] : -INFINITY;
+            for (int i = 0; i < KT; ++i) sv[i] = i < kvalid ? sv[i] : -INFINITY;
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+          for (int i = 0; i < KT; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
         }
         const float mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -265,26 +269,32 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         }
         l *= f;
         m_ref = m_new;
-        // pass 2: P = 2^(s*c - m) chunk by chunk, back to TMEM as bf16 pairs
+        // pass 2: P = 2^(s*c - m) chunk by chunk, back to TMEM as bf16 pairs; the load of the
+        // next chunk is in flight while this one is exponentiated
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t su[2][32];
+        tmem_ld32_nowait(tmem + lane_off + COL_S, su[0]);
+        tmem_ld_wait_regs(su[0]);
 #pragma unroll
         for (int ch = 0; ch < KT / 32; ++ch) {
-          float sv[32];
-          tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv));
-          tmem_ld_wait();
+          if (ch + 1 < KT / 32) tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * (ch + 1), su[(ch + 1) & 1]);
+          float cur[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cur[i] = __uint_as_float(su[ch & 1][i]);
           if (kvalid < KT) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] = 32 * ch + i < kvalid ? sv[i] : -INFINITY;
+            for (int i = 0; i < 32; ++i) cur[i] = 32 * ch + i < kvalid ? cur[i] : -INFINITY;
           }
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = fast_exp2(fmaf(sv[2 * i], c, -m_ref));
-            const float p1 = fast_exp2(fmaf(sv[2 * i + 1], c, -m_ref));
+            const float p0 = fast_exp2(fmaf(cur[2 * i], c, -m_ref));
+            const float p1 = fast_exp2(fmaf(cur[2 * i + 1], c, -m_ref));
             ls[i & 3] += p0 + p1;
             w[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tmem + lane_off + COL_P + 16 * ch, w);
+          if (ch + 1 < KT / 32) tmem_ld_wait_regs(su[(ch + 1) & 1]);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st_wait();
@@ -302,7 +312,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       uint32_t u[2][32];
       tmem_ld32_nowait(tmem + lane_off + COL_O, u[0]);
       tmem_ld32_nowait(tmem + lane_off + COL_O + 32, u[1]);
-      tmem_ld_wait();
+      tmem_ld_wait_regs(u[0]);
+      tmem_ld_wait_regs(u[1]);
       tc_fence_before();
       const float inv = 1.f / l;
       if (r < x.qrows) {
