@@ -138,7 +138,11 @@ ESM_API esm_status esm_encoder_workspace_size(const esm_encoder_t* h, int max_to
  *   max_seqlen  >= every c_{i+1} - c_i and <= max_positions
  *   hidden_out  device [total_tokens, hidden]
  *   workspace   device, 256-byte aligned, >= esm_encoder_workspace_size(T, B)
- * total_tokens == 0 is a no-op. */
+ * total_tokens == 0 is a no-op.
+ * The call only enqueues work on `stream` (kernels and one memset), so it can be captured
+ * into a CUDA graph; make one uncaptured call with the same handle first (it performs the
+ * one-time kernel configuration).  A graph bakes in the pointers and sizes it captured;
+ * each replay also advances the FP8 delayed-scaling state. */
 ESM_API esm_status esm_encoder_forward(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids,
                                const int32_t* cu_seqlens, int num_seqs, int total_tokens,
                                int max_seqlen, void* hidden_out, void* workspace,
@@ -233,7 +237,7 @@ ESM_API esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int
  * start-up).  It computes exactly what esm_op_attention computes for bf16, head_dim 64
  * (qkv device bf16 [T, 3*hidden], q | k | v head-major, RoPE applied; o device bf16
  * [T, hidden]; cu_seqlens device int32 [num_seqs + 1]) without a handle or a workspace:
- * its scratch is a fixed device array inside the library (about 615 KB, held by every
+ * its scratch is a fixed device array inside the library (about 655 KB, held by every
  * GPU that loads the library until the process exits).
  * Limits: total_tokens <= ESM_NOALLOC_MAX_TOKENS, num_seqs <= ESM_NOALLOC_MAX_SEQS,
  * max_seqlen <= ESM_NOALLOC_MAX_TOKENS; larger sizes return ESM_ERR_INVALID_ARG.

@@ -475,3 +475,33 @@ def test_fp8_forward_depth_accuracy():
     assert e_oracle > 1e-2                      # quantisation really happened on both sides
     assert e_gpu < 1.25 * e_oracle, (e_gpu, e_oracle)
     assert rel_l2(out, ref8) < np.sqrt(2) * e_oracle
+
+
+# --------------------------------------------------------------------------- CUDA graph
+def test_forward_captured_in_cuda_graph_replays_bitwise():
+    """The whole forward (about 7 launches per layer) captured into one CUDA graph and
+    replayed gives exactly the eager result."""
+    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
+    g = synth.Geometry(num_layers=2, hidden=1280, heads=20, ffn=5120)
+    lengths = [130, 7, 300]
+    w = synth.model_weights(g, 24, "bf16")
+    tok = synth.tokens_for_lengths(np.random.default_rng(24), lengths)
+    enc = EsmEncoder.from_geometry(g, "bf16")
+    dw = DeviceWeights(w, "bf16")
+    t, cu = packed_inputs(tok, lengths)
+    ws = enc.workspace(sum(lengths), len(lengths))
+    eager = enc.forward(dw, t, cu, max(lengths), workspace=ws).clone()
+    out = torch.zeros_like(eager)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        enc.forward(dw, t, cu, max(lengths), out=out, workspace=ws)  # uncaptured call on this stream
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        enc.forward(dw, t, cu, max(lengths), out=out, workspace=ws)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    enc.check()

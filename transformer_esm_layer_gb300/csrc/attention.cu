@@ -83,14 +83,13 @@ __global__ void __launch_bounds__(ATT_THREADS)
   const int item = blockIdx.x / heads;
   const int h = blockIdx.x - item * heads;
   if (item >= *pb.work_count) return;
-  const int seg = pb.work[2 * item];
-  const int q0 = pb.work[2 * item + 1];
-  const int start = pb.seg_start[seg];
-  const int qlen = pb.seg_qlen[seg];
-  const int klen = pb.seg_klen[seg];
-  const int qrows = min(QT, qlen - q0);
+  const int4 wi = reinterpret_cast<const int4*>(pb.work)[item];
+  const int qrow0 = wi.x;
+  const int start = wi.z;
+  const int klen = wi.w;
+  const int qrows = wi.y;
   const int ld = 3 * d;
-  const __nv_bfloat16* gq = qkv + (size_t)(start + q0) * ld + h * DH;
+  const __nv_bfloat16* gq = qkv + (size_t)qrow0 * ld + h * DH;
   const __nv_bfloat16* gk = qkv + (size_t)start * ld + d + h * DH;
   const __nv_bfloat16* gv = qkv + (size_t)start * ld + 2 * d + h * DH;
   const int nkb = (klen + KT - 1) / KT;
@@ -221,19 +220,19 @@ __global__ void __launch_bounds__(ATT_THREADS)
     const float a2 = acc[j][2] * inv1, a3 = acc[j][3] * inv1;
     if constexpr (OUT == Act::BF16) {
       __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
-      if (r0 < qrows) *reinterpret_cast<uint32_t*>(ob + (size_t)(start + q0 + r0) * d + c) = pack_bf16x2(a0, a1);
-      if (r1 < qrows) *reinterpret_cast<uint32_t*>(ob + (size_t)(start + q0 + r1) * d + c) = pack_bf16x2(a2, a3);
+      if (r0 < qrows) *reinterpret_cast<uint32_t*>(ob + (size_t)(qrow0 + r0) * d + c) = pack_bf16x2(a0, a1);
+      if (r1 < qrows) *reinterpret_cast<uint32_t*>(ob + (size_t)(qrow0 + r1) * d + c) = pack_bf16x2(a2, a3);
     } else {
       uint8_t* ob = static_cast<uint8_t*>(o);
       if (r0 < qrows) {
         amax = fmaxf(amax, fmaxf(fabsf(a0), fabsf(a1)));
         __nv_fp8x2_e4m3 v(make_float2(a0 * qs, a1 * qs));
-        *reinterpret_cast<uint16_t*>(ob + (size_t)(start + q0 + r0) * d + c) = *reinterpret_cast<uint16_t*>(&v);
+        *reinterpret_cast<uint16_t*>(ob + (size_t)(qrow0 + r0) * d + c) = *reinterpret_cast<uint16_t*>(&v);
       }
       if (r1 < qrows) {
         amax = fmaxf(amax, fmaxf(fabsf(a2), fabsf(a3)));
         __nv_fp8x2_e4m3 v(make_float2(a2 * qs, a3 * qs));
-        *reinterpret_cast<uint16_t*>(ob + (size_t)(start + q0 + r1) * d + c) = *reinterpret_cast<uint16_t*>(&v);
+        *reinterpret_cast<uint16_t*>(ob + (size_t)(qrow0 + r1) * d + c) = *reinterpret_cast<uint16_t*>(&v);
       }
     }
   }

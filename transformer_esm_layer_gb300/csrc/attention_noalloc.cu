@@ -32,9 +32,9 @@ constexpr size_t kOffStart = kOffSeg + kMaxTokens;
 constexpr size_t kOffQlen = kOffStart + kMaxSeqs;
 constexpr size_t kOffKlen = kOffQlen + kMaxSeqs;
 constexpr size_t kOffWork = kOffKlen + kMaxSeqs;
-constexpr size_t kOffCount = kOffWork + 2 * (size_t)kMaxItems;
+constexpr size_t kOffCount = kOffWork + 4 * (size_t)kMaxItems;
 constexpr size_t kOffErr = kOffCount + 4;
-constexpr size_t kWords = kOffErr + 60;  // ~615 KB in total
+constexpr size_t kWords = kOffErr + 60;  // ~655 KB in total
 
 __device__ __align__(256) int32_t g_attention_scratch[kWords];
 

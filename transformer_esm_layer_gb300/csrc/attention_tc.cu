@@ -70,18 +70,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 }
 
 struct Item {
-  int start, q0, qrows, klen, nkb, h;
+  int qrow0, qrows, krow0, klen, nkb, h;
 };
 
-__device__ __forceinline__ Item decode_item(const PackBuffers& pb, int it, int heads) {
+// Work item `it` = (work-list entry it / heads, head it % heads); one 16-byte load.
+__device__ __forceinline__ int4 load_item(const PackBuffers& pb, int it, int heads) {
+  return __ldg(reinterpret_cast<const int4*>(pb.work) + it / heads);
+}
+__device__ __forceinline__ Item make_item(int4 w, int it, int heads) {
   Item x;
-  const int w = it / heads;
-  x.h = it - w * heads;
-  const int seg = pb.work[2 * w];
-  x.q0 = pb.work[2 * w + 1];
-  x.start = pb.seg_start[seg];
-  x.qrows = min(QT, pb.seg_qlen[seg] - x.q0);
-  x.klen = pb.seg_klen[seg];
+  x.h = it % heads;
+  x.qrow0 = w.x;
+  x.qrows = w.y;
+  x.krow0 = w.z;
+  x.klen = w.w;
   x.nkb = (x.klen + KT - 1) / KT;
   return x;
 }
@@ -129,8 +131,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int g = 0, qi = 0;
+      int4 nxt = load_item(pb, blockIdx.x, heads);
       for (int it = blockIdx.x; it < n_items && !sm->abort; it += gridDim.x, ++qi) {
-        const Item x = decode_item(pb, it, heads);
+        const Item x = make_item(nxt, it, heads);
+        if (it + (int)gridDim.x < n_items) nxt = load_item(pb, it + gridDim.x, heads);  // prefetch
         const int qb = qi & 1;
         if (!mbar_wait(&sm->q_empty[qb], ((uint32_t)(qi >> 1) & 1u) ^ 1u)) {
           latch_error(err, ERRBIT_TIMEOUT);
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           break;
         }
         mbar_arrive_expect_tx(&sm->q_full[qb], TILE_BYTES);
-        tma_load_2d(sQ + qb * TILE_BYTES, &tm, x.h * DH, x.start + x.q0, &sm->q_full[qb]);
+        tma_load_2d(sQ + qb * TILE_BYTES, &tm, x.h * DH, x.qrow0, &sm->q_full[qb]);
         for (int j = 0; j < x.nkb; ++j, ++g) {
           const int st = g % STG;
           if (!mbar_wait(&sm->kv_empty[st], ((uint32_t)(g / STG) & 1u) ^ 1u)) {
@@ -147,8 +151,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             break;
           }
           mbar_arrive_expect_tx(&sm->kv_full[st], 2 * TILE_BYTES);
-          tma_load_2d(sK + 2 * st * TILE_BYTES, &tm, d + x.h * DH, x.start + j * KT, &sm->kv_full[st]);
-          tma_load_2d(sV + 2 * st * TILE_BYTES, &tm, 2 * d + x.h * DH, x.start + j * KT, &sm->kv_full[st]);
+          tma_load_2d(sK + 2 * st * TILE_BYTES, &tm, d + x.h * DH, x.krow0 + j * KT, &sm->kv_full[st]);
+          tma_load_2d(sV + 2 * st * TILE_BYTES, &tm, 2 * d + x.h * DH, x.krow0 + j * KT, &sm->kv_full[st]);
         }
       }
       // Copies still in flight can only exist if a consumer gave up early: then the last
@@ -179,8 +183,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         mma_commit(&sm->kv_empty[gp % STG]);
         return true;
       };
+      int4 nxt = load_item(pb, blockIdx.x, heads);
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++qi) {
-        const Item x = decode_item(pb, it, heads);
+        const Item x = make_item(nxt, it, heads);
+        if (it + (int)gridDim.x < n_items) nxt = load_item(pb, it + gridDim.x, heads);  // prefetch
         const int qb = qi & 1;
         if (!mbar_wait(&sm->q_full[qb], (uint32_t)(qi >> 1) & 1u)) { ok = false; break; }
         const uint32_t a0 = smem_u32(sQ + qb * TILE_BYTES);
@@ -218,8 +224,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     float amax = 0.f;
     bool ok = true;
     int g = 0;
+    int4 nxt = load_item(pb, blockIdx.x, heads);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const Item x = decode_item(pb, it, heads);
+      const Item x = make_item(nxt, it, heads);
+      if (it + (int)gridDim.x < n_items) nxt = load_item(pb, it + gridDim.x, heads);  // prefetch
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < x.nkb; ++j, ++g) {
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       tc_fence_before();
       const float inv = 1.f / l;
       if (r < x.qrows) {
-        const size_t off = (size_t)(x.start + x.q0 + r) * d + x.h * DH;
+        const size_t off = (size_t)(x.qrow0 + r) * d + x.h * DH;
         if constexpr (OUT == Act::BF16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + off);
 #pragma unroll

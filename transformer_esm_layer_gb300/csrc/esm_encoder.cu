@@ -124,7 +124,7 @@ struct esm_encoder {
     L.seg_start = take(4 * B);
     L.seg_qlen = take(4 * B);
     L.seg_klen = take(4 * B);
-    L.work = take(8 * (size_t)L.max_items);
+    L.work = take(16 * (size_t)L.max_items);
     L.work_count = take(16);
     L.x = take(4 * T * d);
     L.y = take(act_bytes() * T * d);

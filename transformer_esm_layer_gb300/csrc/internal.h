@@ -25,7 +25,7 @@ struct PackBuffers {
   int32_t* seg_start;  // [B]
   int32_t* seg_qlen;   // [B]  query rows of the segment
   int32_t* seg_klen;   // [B]  visible keys of the segment
-  int32_t* work;       // [2 * max_items]: (segment, first query row)
+  int32_t* work;       // [4 * max_items]: (first query row, query rows, first key row, keys)
   int32_t* work_count; // [1]
 };
 

@@ -66,8 +66,8 @@ __global__ void pad_index_kernel(const int32_t* __restrict__ seq_lens, int B, in
 constexpr int WL_THREADS = 1024;
 constexpr int WL_SORT_MAX = 4096;
 
-// Single CTA: list the (segment, query-tile) work items of the attention kernel, longest
-// segments first so that the costliest tiles start in the first wave (when B is small
+// Single CTA: list the (segment, query-tile) work items of the attention kernel, each as
+// (first query row, query rows, first key row, visible keys), longest segments first so that the costliest tiles start in the first wave (when B is small
 // enough to rank in shared memory; otherwise in segment order).
 __global__ void __launch_bounds__(WL_THREADS) attn_worklist_kernel(int B, int max_items, int q_tile, PackBuffers pb) {
   __shared__ int s_len[WL_SORT_MAX];
@@ -119,11 +119,12 @@ __global__ void __launch_bounds__(WL_THREADS) attn_worklist_kernel(int B, int ma
     }
     __syncthreads();
     const int excl = s_base + (wid > 0 ? s_warp[wid - 1] : 0) + v - tiles;
-    for (int t = 0; t < tiles; ++t) {
-      const int k = excl + t;
-      if (k < max_items) {
-        pb.work[2 * k] = seg;
-        pb.work[2 * k + 1] = t * q_tile;
+    if (tiles > 0) {
+      const int start = pb.seg_start[seg], qlen = pb.seg_qlen[seg], klen = pb.seg_klen[seg];
+      for (int t = 0; t < tiles; ++t) {
+        const int k = excl + t;
+        if (k < max_items)
+          reinterpret_cast<int4*>(pb.work)[k] = make_int4(start + t * q_tile, min(q_tile, qlen - t * q_tile), start, klen);
       }
     }
     __syncthreads();
