@@ -182,6 +182,12 @@ ESM_API esm_status esm_encoder_debug_pack_index(esm_encoder_t* h, const int32_t*
                                         int32_t* seg_id, void* workspace, size_t workspace_bytes,
                                         esm_stream_t stream);
 
+/* Failure-detection hook: one warp waits, through the bounded wait every kernel of the
+ * library uses but with a limit of timeout_us microseconds (1..1000000), on an mbarrier
+ * nothing arrives at.  The wait gives up, ESM_ERR_TIMEOUT is latched in the handle (read
+ * it with esm_encoder_check) and the kernel returns: the context stays usable. */
+ESM_API esm_status esm_encoder_debug_wait_timeout(esm_encoder_t* h, int timeout_us, esm_stream_t stream);
+
 /* ---- single-operation hooks (the kernels the forward uses, exposed for parity) ---- */
 
 /* y = LN(x) * gamma + beta per row.  x device float32 [rows, cols]; gamma, beta device

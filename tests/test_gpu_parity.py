@@ -505,3 +505,23 @@ def test_forward_captured_in_cuda_graph_replays_bitwise():
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
     enc.check()
+
+
+# --------------------------------------------------------------------------- failure detection
+def test_bounded_wait_times_out_and_context_stays_usable():
+    """A device wait on a barrier nothing arrives at gives up after its limit (50 ms here),
+    the host reads ESM_ERR_TIMEOUT, and the next forward runs normally."""
+    import time
+    from transformer_esm_layer_gb300.binding import DeviceWeights, packed_inputs
+    g = SMALL
+    enc = _enc(g, "bf16")
+    t0 = time.perf_counter()
+    enc.debug_wait_timeout(50_000)
+    assert enc.check_status() == 7  # ESM_ERR_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    assert enc.check_status() == 0
+    dw = DeviceWeights(synth.model_weights(g, 3, "bf16"), "bf16")
+    tok, cu = packed_inputs(np.array([0, 5, 6, 9, 2], np.int32), [5])
+    out = enc.forward(dw, tok, cu, 5)
+    enc.check()
+    assert torch.isfinite(out.float()).all()

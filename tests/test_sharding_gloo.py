@@ -1,0 +1,82 @@
+"""Multi-GPU host logic on CPU: sequence sharding for independent replicas, checked with a
+world-size-2 gloo process group (no GPU needed)."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from transformer_esm_layer_gb300 import sharding, synth
+
+
+def test_shard_by_work_is_a_balanced_partition():
+    wl = synth.make_workload("esm650m")
+    g = wl.geometry
+    for world in (1, 2, 4, 8):
+        parts = sharding.shard_by_work(wl.lengths, world, g.hidden, g.ffn)
+        flat = sorted(i for p in parts for i in p)
+        assert flat == list(range(len(wl.lengths)))            # every sequence exactly once
+        costs = [sum(sharding.sequence_cost(wl.lengths[i], g.hidden, g.ffn) for i in p) for p in parts]
+        biggest = max(sharding.sequence_cost(L, g.hidden, g.ffn) for L in wl.lengths)
+        assert max(costs) - min(costs) <= biggest + 1e-6      # greedy bound: within one sequence
+
+
+def test_local_batch_keeps_sequences_intact():
+    lengths = [3, 5, 2, 7]
+    tok = np.arange(sum(lengths), dtype=np.int32)
+    t, l = sharding.local_batch(tok, lengths, [1, 3])
+    assert l == [5, 7]
+    assert t.tolist() == list(range(3, 8)) + list(range(10, 17))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # every rank builds the same global batch and takes its own share, as bench.py does
+        rng = np.random.default_rng([2, 99])
+        lengths = synth.lognormal_lengths(rng, total=world * 4096)
+        tokens = synth.tokens_for_lengths(np.random.default_rng([2, 98]), lengths)
+        parts = sharding.shard_by_work(lengths, world, 1280, 5120)
+        mine = parts[rank]
+        toks, lens = sharding.local_batch(tokens, lengths, mine)
+        # what each rank would hand to esm_encoder_forward: valid packed inputs
+        cu = synth.cu_seqlens_from_lengths(lens)
+        assert cu[0] == 0 and cu[-1] == len(toks) and np.all(np.diff(cu) >= 1)
+        # the ranks agree on the partition and together cover the batch exactly once
+        got = [None] * world
+        dist.all_gather_object(got, mine)
+        flat = sorted(i for p in got for i in p)
+        ok = flat == list(range(len(lengths))) and got == parts
+        # token counts add up to the global batch
+        n = torch.tensor([len(toks)], dtype=torch.int64)
+        dist.all_reduce(n)
+        ok = ok and int(n.item()) == len(tokens)
+        q.put((rank, ok))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_gloo_sharding():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    results = dict(q.get(timeout=10) for _ in range(world))
+    assert all(p.exitcode == 0 for p in procs)
+    assert results == {0: True, 1: True}

@@ -27,6 +27,7 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_encoder_debug_pack_index", "esm_op_layernorm", "esm_op_gemm", "esm_op_attention",
            "esm_encoder_get_fp8_state", "esm_encoder_set_fp8_state", "esm_encoder_set_profiling",
            "esm_encoder_get_profile", "esm_op_attention_noalloc", "esm_op_layernorm_e4m3", "esm_op_gemm_fp8",
+           "esm_encoder_debug_wait_timeout",
            "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
 
@@ -88,6 +89,7 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_get_profile": (i32, [vp, ctypes.POINTER(EsmProfile), i32]),
         "esm_op_attention_noalloc": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "esm_op_layernorm_e4m3": (i32, [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp]),
+        "esm_encoder_debug_wait_timeout": (i32, [vp, i32, vp]),
         "esm_op_gemm_fp8": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
         "esm_status_string": (ctypes.c_char_p, [i32]),
     }
@@ -257,6 +259,10 @@ class EsmEncoder:
                                                    _stream_ptr(stream))
         self._raise(st, "esm_encoder_debug_pack_index")
         return pos[:total_tokens], seg[:total_tokens]
+
+    def debug_wait_timeout(self, timeout_us: int, stream=None):
+        self._raise(self.lib.esm_encoder_debug_wait_timeout(self.handle, int(timeout_us), _stream_ptr(stream)),
+                    "esm_encoder_debug_wait_timeout")
 
     def op_layernorm(self, x, gamma, beta, y, stream=None):
         rows, cols = x.shape

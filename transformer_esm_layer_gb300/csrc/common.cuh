@@ -77,16 +77,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Gives up after kWaitLimitNs
-// and returns false (the caller latches ERRBIT_TIMEOUT and winds down).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete.  Gives up after limit_ns of the
+// global timer and returns false (the caller latches ERRBIT_TIMEOUT and winds down).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_limit(bar, parity, kWaitLimitNs);
 }
 
 // Warp-uniform form for code that follows with warp-collective tcgen05 instructions: every

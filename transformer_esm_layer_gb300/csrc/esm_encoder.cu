@@ -563,6 +563,12 @@ esm_status esm_encoder_debug_pack_index(esm_encoder_t* h, const int32_t* cu_seql
   return cuda_status(cudaGetLastError());
 }
 
+esm_status esm_encoder_debug_wait_timeout(esm_encoder_t* h, int timeout_us, esm_stream_t stream) {
+  if (!h || timeout_us < 1 || timeout_us > 1000000) return ESM_ERR_INVALID_ARG;
+  launch_wait_timeout(1000ull * (unsigned long long)timeout_us, h->d_err, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
 esm_status esm_op_layernorm(esm_encoder_t* h, const float* x, const void* gamma, const void* beta, void* y, int rows,
                             int cols, esm_stream_t stream) {
   if (!h || !x || !gamma || !beta || !y || rows < 0 || cols <= 0 || cols % 4 || cols > 4096)

@@ -39,6 +39,8 @@ void launch_attn_worklist(int B, int max_items, int q_tile, const PackBuffers& p
 void launch_embed(const int32_t* tok, int T, const void* emb, bool emb_f32, int vocab, int d, float scale,
                   float* x, unsigned* err, cudaStream_t st);
 void launch_rope_table(float2* tab, int max_pos, int half, float base, cudaStream_t st);
+// A bounded wait that runs out (failure-detection hook).
+void launch_wait_timeout(unsigned long long limit_ns, unsigned* err, cudaStream_t st);
 
 // ---------------------------------------------------------------- layernorm.cu
 // y = LN(x) * g + b. Params in f32 or bf16; output f32, bf16 or e4m3 (scaled by

@@ -182,7 +182,24 @@ __global__ void rope_table_kernel(float2* tab, int max_pos, int half, double bas
   tab[i] = make_float2((float)c, (float)s);
 }
 
+// One warp waits on an mbarrier that nothing will ever arrive at, through the same bounded
+// wait every kernel uses (here with a short limit): the wait gives up, the error bit is
+// latched and the kernel returns normally.
+__global__ void wait_timeout_kernel(unsigned long long limit_ns, unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (!mbar_wait_limit(&bar, 0, limit_ns) && threadIdx.x == 0) latch_error(err, ERRBIT_TIMEOUT);
+}
+
 }  // namespace
+
+void launch_wait_timeout(unsigned long long limit_ns, unsigned* err, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+}
 
 void launch_pack_index(const int32_t* cu, int B, int T, int max_seqlen, int max_positions, const PackBuffers& pb,
                        unsigned* err, cudaStream_t st) {
