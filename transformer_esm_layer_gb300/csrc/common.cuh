@@ -127,6 +127,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Pull a 2-D box of a tensor map into L2 ahead of a later load (no shared memory, no
+// completion to wait for).  Same coordinate rules as the loads.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 2-D tiled bulk-tensor load global -> shared, completing `bytes` on the mbarrier.
 // x is the innermost (contiguous) coordinate in elements, y the row.
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m, int x, int y,
@@ -326,6 +334,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Warp-collective: 32 lanes x 16 consecutive fp32 columns from TMEM (load and wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+        "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+      :
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Warp-collective: 32 lanes x 32 consecutive 32-bit columns into TMEM.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -342,5 +369,42 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // ------------------------------------------------------------------ numerics
 __device__ __forceinline__ float gelu_erf(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
+
+// Hardware special-function approximations (single instructions, subnormals flushed).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Exact-erf GELU, x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)), for the tensor-core epilogues
+// whose outputs are rounded to bf16 or E4M3.  erf(z), z >= 0, is the rational-exponential
+// form 7.1.26 of Abramowitz & Stegun, Handbook of Mathematical Functions (Hastings):
+//   1 - erf(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),  t = 1 / (1 + p z),
+// absolute error below 1.5e-7, far under the output rounding (2^-9 relative for bf16).
+// With q = (1 - erf(|x|/sqrt 2)) / 2:  GELU(x) = x (1 - q) for x >= 0 and x q for x < 0.
+// Two special-function instructions (rcp, ex2) and about a dozen FMA-pipe operations.
+__device__ __forceinline__ float gelu_as7126(float x) {
+  constexpr float kP = 0.3275911f;
+  // a1..a5 of the formula, halved so the polynomial directly yields q
+  constexpr float kA1 = 0.5f * 0.254829592f, kA2 = 0.5f * -0.284496736f, kA3 = 0.5f * 1.421413741f,
+                  kA4 = 0.5f * -1.453152027f, kA5 = 0.5f * 1.061405429f;
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(kP, z, 1.0f));
+  float poly = fmaf(t, kA5, kA4);
+  poly = fmaf(t, poly, kA3);
+  poly = fmaf(t, poly, kA2);
+  poly = fmaf(t, poly, kA1);
+  poly *= t;
+  const float e = ex2_approx((z * -1.4426950408889634f) * z);  // exp(-z^2)
+  const float q = poly * e;
+  const float xq = x * q;
+  return x >= 0.f ? x - xq : xq;
+}
 
 }  // namespace esm

@@ -65,7 +65,7 @@ struct esm_encoder {
   int device = 0;
   int num_sms = 0;
   unsigned* d_err = nullptr;     // device error word
-  float2* d_rope = nullptr;      // [max_positions][32] (cos, sin)
+  float2* d_rope = nullptr;      // [16][max_positions][2] (cos, sin)
   float* d_fp8 = nullptr;        // scales [L*8] | history [L*8*len] | amax [L*8]
   size_t fp8_floats = 0;
   std::unordered_map<MapKey, CUtensorMap, MapKeyHash> maps;

@@ -70,7 +70,7 @@ __global__ void rope_f32_kernel(float* qkv, int T, int d, int dh, const int32_t*
     const int t = (int)(th / (2 * (d / dh)));
     int p = pos_id[t];
     p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
-    const float2 cs = rope[(size_t)p * kRopeMaxHalf + j];
+    const float2 cs = rope[((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1)];
     float* u = qkv + (size_t)t * 3 * d + hh * dh;
     const float a = u[j], b = u[j + half];
     u[j] = a * cs.x - b * cs.y;

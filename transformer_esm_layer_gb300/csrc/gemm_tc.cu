@@ -16,8 +16,9 @@
 //                accumulator (tcgen05.ld), applies bias / RoPE / GELU / residual add, writes
 //                the chunk into a swizzled shared-memory staging buffer and one thread stores
 //                it with a TMA bulk-tensor store.  The fp32 residual chunks come in by TMA
-//                load into the same buffers ahead of use.  Each warp then arrives on the
-//                leader's "accumulator free" mbarrier.
+//                load into the same buffers ahead of use.  Each warp arrives on the
+//                leader's "accumulator free" mbarrier as soon as it has read its last
+//                accumulator columns, before finishing that chunk.
 // Two accumulators (2 x 256 of the 512 TMEM columns) let the epilogue of one tile run
 // while the tensor core works on the next.  Every mbarrier wait is bounded: on timeout
 // the kernel latches an error bit, stops issuing work and still releases its TMEM.
@@ -86,6 +87,35 @@ __device__ __forceinline__ void load_bias32(const EpiArgs& ea, int c, float (&b)
   }
 }
 
+// Scale the W accumulator values of columns c.. and add their bias, 8 bias values at a
+// time (keeps few registers live next to the accumulators).
+template <int W>
+__device__ __forceinline__ void scale_add_bias(const EpiArgs& ea, int c, float scale, float (&v)[W]) {
+#pragma unroll
+  for (int i8 = 0; i8 < W / 8; ++i8) {
+    float b[8];
+    if (ea.bias == nullptr) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) b[k] = 0.f;
+    } else if (ea.bias_f32) {
+      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(ea.bias) + c + 8 * i8);
+      const float4 x = __ldg(p), y = __ldg(p + 1);
+      b[0] = x.x; b[1] = x.y; b[2] = x.z; b[3] = x.w; b[4] = y.x; b[5] = y.y; b[6] = y.z; b[7] = y.w;
+    } else {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ea.bias) + c + 8 * i8));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(h[k]);
+        b[2 * k] = f.x;
+        b[2 * k + 1] = f.y;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[8 * i8 + k] = v[8 * i8 + k] * scale + b[k];
+  }
+}
+
 // Byte offset of 16-byte unit j of row r in a 128-row x 128-byte staging chunk laid out
 // with the 128-byte swizzle (the layout the TMA maps of the outputs use).
 __device__ __forceinline__ uint32_t swz_off(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
@@ -98,6 +128,19 @@ __device__ __forceinline__ void st_shared_v4(uint8_t* base, uint32_t off, uint4 
 __device__ __forceinline__ void stage_bf16x32(uint8_t* buf, int r, int u0, const float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    st_shared_v4(buf, swz_off(r, u0 + i), w);
+  }
+}
+
+// 16 fp32 values as bf16 into 16-byte units u0, u0+1.
+__device__ __forceinline__ void stage_bf16x16(uint8_t* buf, int r, int u0, const float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
     uint4 w;
     w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
     w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
@@ -289,8 +332,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int row0 = (tile / n_tiles) * TILE_M + (int)rank * BM;     // first row of this CTA
       const int col0 = (tile % n_tiles) * BN + half * (BN / 2);        // first column of this half
       const int row = row0 + r;
+      // This warp has read the whole accumulator into registers: hand it back to the MMA
+      // warp (one arrival per warp on the leader's barrier) before finishing the chunk.
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
+      };
       if constexpr (EPI == ESM_EPI_RESIDUAL) {
-        // Residual chunks 0 and 1 of this half: earlier stores must be done reading first.
+        // Residual chunks 0 and 1 of this half into the staging buffers (earlier stores must
+        // be done reading them first); the later chunks only into L2, so that their loads
+        // into the reused buffers return quickly.
         if (elect) {
           bulk_wait_read<0>();
 #pragma unroll
@@ -298,15 +350,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_arrive_expect_tx(&sm->xload[half][b], E_BUF);
             tma_load_2d(ebuf0 + b * E_BUF, &tmO, col0 + b * CH::kCols, row0, &sm->xload[half][b]);
           }
+          for (int c = 2; c < CH::kPerHalf; ++c) tma_prefetch_l2_2d(&tmO, col0 + c * CH::kCols, row0);
         }
       }
+      // RoPE: this row's (cos, sin) for the 32 pairs of a 64-wide head are the same for every
+      // q and k head of the tile; fetch them once, before the accumulator is ready.
+      float4 cs[EPI == ESM_EPI_QKV_ROPE ? 16 : 1];
       if constexpr (EPI == ESM_EPI_QKV_ROPE) {
-        // warm this row's (cos, sin) table row into L1 before the accumulator is ready
-        int p = row < M ? ea.pos_id[row] : 0;
-        p = p < 0 ? 0 : (p >= ea.max_pos ? ea.max_pos - 1 : p);
-        const char* t = reinterpret_cast<const char*>(ea.rope + (size_t)p * kRopeMaxHalf);
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(t));
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(t + 128));
+        if (col0 < ea.rope_cols) {
+          int p = row < M ? __ldg(ea.pos_id + row) : 0;
+          p = p < 0 ? 0 : (p >= ea.max_pos ? ea.max_pos - 1 : p);
+          const float4* tab = reinterpret_cast<const float4*>(ea.rope) + p;  // group g at g * max_pos
+#pragma unroll
+          for (int g = 0; g < 16; ++g) cs[g] = __ldg(tab + (size_t)g * ea.max_pos);
+        }
       }
       const bool ok = mbar_wait_warp(&sm->tfull[acc], acc_phase);
       if (!ok && lane == 0) {
@@ -320,23 +377,36 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (sm->fail[half]) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
+      float vlast[(EPI == ESM_EPI_BIAS_F32 || EPI == ESM_EPI_RESIDUAL) ? 32 : 1];
 
 #pragma unroll 1
       for (int c = 0; c < CH::kPerHalf; ++c) {
         const int b = c & 1;
         uint8_t* buf = ebuf0 + b * E_BUF;
         const int col = col0 + c * CH::kCols;
-        if constexpr (EPI == ESM_EPI_RESIDUAL) {
-          if (!mbar_wait(&sm->xload[half][b], (xphase >> b) & 1u)) latch_error(err, ERRBIT_TIMEOUT);
-          xphase ^= 1u << b;
-        } else {
+        if constexpr (EPI != ESM_EPI_RESIDUAL) {
           // the store that last used this buffer must be done reading it
           if (elect) bulk_wait_read<1>();
           named_bar_sync(bar_id, 128);
         }
         if constexpr (EPI == ESM_EPI_BIAS_F32 || EPI == ESM_EPI_RESIDUAL) {
+          // 32-column chunks: the last two are read from TMEM together, so the accumulator
+          // is released one chunk early.
           float v[32], bb[32];
-          tmem_ld32(tbase + c * CH::kCols, v);
+          if (c + 2 < CH::kPerHalf) {
+            tmem_ld32(tbase + c * CH::kCols, v);
+          } else if (c + 2 == CH::kPerHalf) {
+            tmem_ld32(tbase + c * CH::kCols, v);
+            tmem_ld32(tbase + (c + 1) * CH::kCols, vlast);
+            release_acc();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = vlast[i];
+          }
+          if constexpr (EPI == ESM_EPI_RESIDUAL) {
+            if (!mbar_wait(&sm->xload[half][b], (xphase >> b) & 1u)) latch_error(err, ERRBIT_TIMEOUT);
+            xphase ^= 1u << b;
+          }
           load_bias32(ea, col, bb);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -355,43 +425,47 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int s4 = 0; s4 < 4; ++s4) {
             float v[32], bb[32];
             tmem_ld32(tbase + 32 * s4, v);
+            if (s4 == 3) release_acc();
             load_bias32(ea, col + 32 * s4, bb);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i] * acc_scale + bb[i]);
+            for (int i = 0; i < 32; ++i) v[i] = gelu_as7126(v[i] * acc_scale + bb[i]);
             stage_e4m3x32(buf, r, 2 * s4, v, o_scale, amax);
           }
-        } else {  // bf16 output, 64 columns: QKV (+RoPE on q and k) or GELU
-          float v0[32], v1[32], bb[32];
-          tmem_ld32(tbase + c * CH::kCols, v0);
-          tmem_ld32(tbase + c * CH::kCols + 32, v1);
-          load_bias32(ea, col, bb);
+        } else if constexpr (EPI == ESM_EPI_QKV_ROPE) {
+          // bf16 output, 64 columns = one head.  RoPE pairs column j with j + 32; the head is
+          // done in two passes of 16 pairs (columns 16h.. and 32 + 16h..).
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v0[i] = v0[i] * acc_scale + bb[i];
-          load_bias32(ea, col + 32, bb);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v1[i] = v1[i] * acc_scale + bb[i];
-          if constexpr (EPI == ESM_EPI_QKV_ROPE) {
-            // head_dim 64: the chunk is one head; pair (j, j + 32) = (v0[j], v1[j]).
+          for (int h = 0; h < 2; ++h) {
+            float a[16], bq[16];
+            tmem_ld16(tbase + c * CH::kCols + 16 * h, a);
+            tmem_ld16(tbase + c * CH::kCols + 32 + 16 * h, bq);
+            if (h == 1 && c == CH::kPerHalf - 1) release_acc();
+            scale_add_bias<16>(ea, col + 16 * h, acc_scale, a);
+            scale_add_bias<16>(ea, col + 32 + 16 * h, acc_scale, bq);
             if (col < ea.rope_cols) {
-              int p = row < M ? ea.pos_id[row] : 0;
-              p = p < 0 ? 0 : (p >= ea.max_pos ? ea.max_pos - 1 : p);
-              const float4* tab = reinterpret_cast<const float4*>(ea.rope + (size_t)p * kRopeMaxHalf);
 #pragma unroll
-              for (int j2 = 0; j2 < 16; ++j2) {
-                const float4 cs = __ldg(tab + j2);  // (cos_j, sin_j, cos_j+1, sin_j+1)
-                const int j = 2 * j2;
-                float a = v0[j], bq = v1[j];
-                v0[j] = a * cs.x - bq * cs.y;
-                v1[j] = bq * cs.x + a * cs.y;
-                a = v0[j + 1]; bq = v1[j + 1];
-                v0[j + 1] = a * cs.z - bq * cs.w;
-                v1[j + 1] = bq * cs.z + a * cs.w;
+              for (int i = 0; i < 16; i += 2) {  // cs[g] = (cos, sin) of pairs 2g and 2g + 1
+                const float4 t = cs[8 * h + i / 2];
+                float x = a[i], y = bq[i];
+                a[i] = x * t.x - y * t.y;
+                bq[i] = y * t.x + x * t.y;
+                x = a[i + 1]; y = bq[i + 1];
+                a[i + 1] = x * t.z - y * t.w;
+                bq[i + 1] = y * t.z + x * t.w;
               }
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) { v0[i] = gelu_erf(v0[i]); v1[i] = gelu_erf(v1[i]); }
+            stage_bf16x16(buf, r, 2 * h, a);
+            stage_bf16x16(buf, r, 4 + 2 * h, bq);
           }
+        } else {  // bf16 output, 64 columns: GELU
+          float v0[32], v1[32];
+          tmem_ld32(tbase + c * CH::kCols, v0);
+          tmem_ld32(tbase + c * CH::kCols + 32, v1);
+          if (c == CH::kPerHalf - 1) release_acc();
+          scale_add_bias<32>(ea, col, acc_scale, v0);
+          scale_add_bias<32>(ea, col + 32, acc_scale, v1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) { v0[i] = gelu_as7126(v0[i]); v1[i] = gelu_as7126(v1[i]); }
           stage_bf16x32(buf, r, 0, v0);
           stage_bf16x32(buf, r, 4, v1);
         }
@@ -410,10 +484,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // This warp is done with the accumulator: one arrival on the leader's barrier.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if (elect) bulk_wait_all();  // stores complete before the CTA may exit

@@ -60,7 +60,7 @@ struct EpiArgs {
   bool bias_f32;
   void* out;              // [M, N]
   const int32_t* pos_id;  // [M] (QKV)
-  const float2* rope;     // [max_pos][half]
+  const float2* rope;     // [kRopeMaxHalf/2][max_pos][2] (cos, sin), see rope_table_kernel
   int rope_cols;          // columns < rope_cols get RoPE (2 * hidden)
   int head_dim;
   int max_pos;

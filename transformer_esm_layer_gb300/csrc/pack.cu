@@ -166,12 +166,14 @@ __global__ void embed_kernel(const int32_t* __restrict__ tok, int T, const void*
   }
 }
 
-// tab[p][j] = (cos, sin)(p * base^(-2j/dh)) for j < dh/2, computed in double precision
-// and rounded once to float (rows are kRopeMaxHalf wide).
+// (cos, sin)(p * base^(-2j/dh)) for j < dh/2, computed in double precision and rounded once
+// to float.  Layout [kRopeMaxHalf/2][max_pos][2] of float2: the pairs j = 2g and 2g+1 of
+// position p form one 16-byte group at index g * max_pos + p, so the 32 consecutive
+// positions of a warp read 512 contiguous bytes per group.
 __global__ void rope_table_kernel(float2* tab, int max_pos, int half, double base) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= max_pos * kRopeMaxHalf) return;
-  const int p = i / kRopeMaxHalf, j = i % kRopeMaxHalf;
+  const int g = i / (2 * max_pos), p = (i / 2) % max_pos, j = 2 * g + (i & 1);
   if (j >= half) {
     tab[i] = make_float2(1.f, 0.f);
     return;
