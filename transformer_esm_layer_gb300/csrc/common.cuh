@@ -382,29 +382,56 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// Packed fp32 pairs (Blackwell f32x2 FMA-pipe instructions: two lanes per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // Exact-erf GELU, x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)), for the tensor-core epilogues
 // whose outputs are rounded to bf16 or E4M3.  erf(z), z >= 0, is the rational-exponential
 // form 7.1.26 of Abramowitz & Stegun, Handbook of Mathematical Functions (Hastings):
 //   1 - erf(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),  t = 1 / (1 + p z),
 // absolute error below 1.5e-7, far under the output rounding (2^-9 relative for bf16).
-// With q = (1 - erf(|x|/sqrt 2)) / 2:  GELU(x) = x (1 - q) for x >= 0 and x q for x < 0.
-// Two special-function instructions (rcp, ex2) and about a dozen FMA-pipe operations.
-__device__ __forceinline__ float gelu_as7126(float x) {
+// With z = |x| / sqrt 2 and h = erf(z) / 2:  GELU(x) = x / 2 + |x| h  (odd part of Phi).
+// Two values at a time: the FMA-pipe work in f32x2 instructions, rcp and ex2 (hardware
+// special-function approximations) per value.
+__device__ __forceinline__ void gelu2_as7126(float& x0, float& x1) {
   constexpr float kP = 0.3275911f;
-  // a1..a5 of the formula, halved so the polynomial directly yields q
+  // a1..a5 of the formula, halved so the polynomial directly yields (1 - erf) / 2
   constexpr float kA1 = 0.5f * 0.254829592f, kA2 = 0.5f * -0.284496736f, kA3 = 0.5f * 1.421413741f,
                   kA4 = 0.5f * -1.453152027f, kA5 = 0.5f * 1.061405429f;
-  const float z = fabsf(x) * 0.70710678118654752f;
-  const float t = rcp_approx(fmaf(kP, z, 1.0f));
-  float poly = fmaf(t, kA5, kA4);
-  poly = fmaf(t, poly, kA3);
-  poly = fmaf(t, poly, kA2);
-  poly = fmaf(t, poly, kA1);
-  poly *= t;
-  const float e = ex2_approx((z * -1.4426950408889634f) * z);  // exp(-z^2)
-  const float q = poly * e;
-  const float xq = x * q;
-  return x >= 0.f ? x - xq : xq;
+  const uint64_t ax = f2_pack(fabsf(x0), fabsf(x1));
+  const uint64_t z = f2_mul(ax, f2_pack(0.70710678118654752f, 0.70710678118654752f));
+  float d0, d1;
+  f2_unpack(f2_fma(z, f2_pack(kP, kP), f2_pack(1.f, 1.f)), d0, d1);
+  const uint64_t t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  uint64_t poly = f2_fma(t, f2_pack(kA5, kA5), f2_pack(kA4, kA4));
+  poly = f2_fma(t, poly, f2_pack(kA3, kA3));
+  poly = f2_fma(t, poly, f2_pack(kA2, kA2));
+  poly = f2_fma(t, poly, f2_pack(kA1, kA1));
+  poly = f2_mul(poly, t);
+  float w0, w1;
+  f2_unpack(f2_mul(f2_mul(z, f2_pack(-1.4426950408889634f, -1.4426950408889634f)), z), w0, w1);
+  const uint64_t e = f2_pack(ex2_approx(w0), ex2_approx(w1));  // exp(-z^2)
+  const uint64_t negpoly = poly ^ 0x8000000080000000ull;                // -(1 - erf) / 2
+  const uint64_t h = f2_fma(negpoly, e, f2_pack(0.5f, 0.5f));           // erf(z) / 2
+  const uint64_t half_x = f2_mul(f2_pack(x0, x1), f2_pack(0.5f, 0.5f));
+  f2_unpack(f2_fma(ax, h, half_x), x0, x1);
 }
 
 }  // namespace esm

@@ -275,6 +275,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      // Descriptors of stage 0; a stage adds its byte offset >> 4 to the start-address field
+      // (every shared address here is below 256 KB, so the 14-bit field cannot carry), and
+      // each 32-byte step of K inside the 128-byte row adds 2.
+      const uint64_t adesc0 = make_sw128_desc(smem_u32(sA));
+      const uint64_t bdesc0 = make_sw128_desc(smem_u32(sB));
       for (int tile = unit; tile < num_tiles && !sm->abort; tile += units) {
         if (!mbar_wait(&sm->tempty[acc], acc_phase ^ 1)) {
           latch_error(err, ERRBIT_TIMEOUT);
@@ -290,12 +295,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
-          const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+          const uint64_t ad0 = adesc0 + (uint64_t)((stage * A_STAGE) >> 4);
+          const uint64_t bd0 = bdesc0 + (uint64_t)((stage * B_STAGE) >> 4);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
-            const uint64_t ad = make_sw128_desc(a0 + 32 * k);
-            const uint64_t bd = make_sw128_desc(b0 + 32 * k);
+            const uint64_t ad = ad0 + (uint64_t)(2 * k);
+            const uint64_t bd = bd0 + (uint64_t)(2 * k);
             if (FP8) mma_f8_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
             else mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
@@ -428,7 +433,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (s4 == 3) release_acc();
             load_bias32(ea, col + 32 * s4, bb);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu_as7126(v[i] * acc_scale + bb[i]);
+            for (int i = 0; i < 32; ++i) v[i] = v[i] * acc_scale + bb[i];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) gelu2_as7126(v[i], v[i + 1]);
             stage_e4m3x32(buf, r, 2 * s4, v, o_scale, amax);
           }
         } else if constexpr (EPI == ESM_EPI_QKV_ROPE) {
@@ -465,7 +472,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           scale_add_bias<32>(ea, col, acc_scale, v0);
           scale_add_bias<32>(ea, col + 32, acc_scale, v1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) { v0[i] = gelu_as7126(v0[i]); v1[i] = gelu_as7126(v1[i]); }
+          for (int i = 0; i < 32; i += 2) { gelu2_as7126(v0[i], v0[i + 1]); gelu2_as7126(v1[i], v1[i + 1]); }
           stage_bf16x32(buf, r, 0, v0);
           stage_bf16x32(buf, r, 4, v1);
         }
