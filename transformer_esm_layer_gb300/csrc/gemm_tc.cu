@@ -15,8 +15,10 @@
 //                128-column half of the tile.  Per chunk of 128 bytes per row it reads the
 //                accumulator (tcgen05.ld), applies bias / RoPE / GELU / residual add, writes
 //                the chunk into a swizzled shared-memory staging buffer and one thread stores
-//                it with a TMA bulk-tensor store.  The fp32 residual chunks come in by TMA
-//                load into the same buffers ahead of use.  Each warp arrives on the
+//                it with a TMA bulk-tensor store.  The fp32 residual (read and written in
+//                place) instead moves through the load/store unit, each warp copying its
+//                own rows, so it never queues behind the operand loads in the TMA engine
+//                and needs no barrier between warps.  Each warp arrives on the
 //                leader's "accumulator free" mbarrier as soon as it has read its last
 //                accumulator columns, before finishing that chunk.
 // Two accumulators (2 x 256 of the 512 TMEM columns) let the epilogue of one tile run
@@ -50,7 +52,6 @@ struct Smem {
   uint64_t empty[S];
   uint64_t tfull[2];
   uint64_t tempty[2];
-  uint64_t xload[2][2];  // [half][buffer]: residual chunk landed
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int abort;
@@ -122,6 +123,36 @@ __device__ __forceinline__ uint32_t swz_off(int r, int j) { return (uint32_t)(r 
 
 __device__ __forceinline__ void st_shared_v4(uint8_t* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
+}
+
+// Residual rows of one epilogue warp (rows 32q .. 32q+31 of the CTA's 128, one 128-byte
+// chunk of fp32 columns starting at col) between global memory and the swizzled staging
+// buffer.  Lane l moves 16-byte unit (l & 7) of rows 4i + (l >> 3): every instruction covers
+// four whole 128-byte rows.  Rows at or beyond M are zero-filled / not written.
+__device__ __forceinline__ void residual_rows_async(const EpiArgs& ea, uint8_t* buf, int q, int lane, int row0,
+                                                    int M, int N, int col) {
+  const float* x = static_cast<const float*>(ea.out);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = q * 32 + 4 * i + (lane >> 3);
+    const int u = lane & 7;
+    const int grow = row0 + rr;
+    const bool in = grow < M;
+    const float* src = x + (in ? (size_t)grow * N + col + 4 * u : 0);
+    cp_async_16(buf + swz_off(rr, u), src, in ? 16u : 0u);
+  }
+}
+__device__ __forceinline__ void residual_rows_store(const EpiArgs& ea, const uint8_t* buf, int q, int lane, int row0,
+                                                    int M, int N, int col) {
+  float* x = static_cast<float*>(ea.out);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = q * 32 + 4 * i + (lane >> 3);
+    const int u = lane & 7;
+    const int grow = row0 + rr;
+    const uint4 v = *reinterpret_cast<const uint4*>(buf + swz_off(rr, u));
+    if (grow < M) *reinterpret_cast<uint4*>(x + (size_t)grow * N + col + 4 * u) = v;
+  }
 }
 
 // 32 fp32 values (columns of this thread's row) as bf16 into 16-byte units u0..u0+3.
@@ -208,8 +239,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sm->tfull[a], 1);
       mbar_init(&sm->tempty[a], 2 * NUM_EPI_WARPS);  // one arrival per epilogue warp of the pair
-      mbar_init(&sm->xload[a][0], 1);
-      mbar_init(&sm->xload[a][1], 1);
     }
     mbar_init(&sm->mma_done, 1);
     sm->abort = 0;
@@ -325,7 +354,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar_id = 1 + (uint32_t)half;             // named barrier of the half's 4 warps
     uint8_t* const ebuf0 = sE + (2 * half) * E_BUF;  // buffer b of this half: ebuf0 + b * E_BUF
     const uint32_t tempty_leader = map_to_rank(&sm->tempty[0], 0);
-    uint32_t xphase = 0u;  // bit b: parity of the next residual load into buffer b
     int acc = 0;
     uint32_t acc_phase = 0;
     float amax = 0.f;
@@ -345,17 +373,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive_remote(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
       };
       if constexpr (EPI == ESM_EPI_RESIDUAL) {
-        // Residual chunks 0 and 1 of this half into the staging buffers (earlier stores must
-        // be done reading them first); the later chunks only into L2, so that their loads
-        // into the reused buffers return quickly.
-        if (elect) {
-          bulk_wait_read<0>();
+        // The residual goes through the load/store unit, not the TMA engine (whose queue is
+        // full of operand loads): each warp copies its own 32 rows of chunks 0 and 1 into
+        // its rows of the two staging buffers (coalesced: 4 rows x 128 bytes per
+        // instruction) and pulls its rows of the later chunks into L2.
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            mbar_arrive_expect_tx(&sm->xload[half][b], E_BUF);
-            tma_load_2d(ebuf0 + b * E_BUF, &tmO, col0 + b * CH::kCols, row0, &sm->xload[half][b]);
-          }
-          for (int c = 2; c < CH::kPerHalf; ++c) tma_prefetch_l2_2d(&tmO, col0 + c * CH::kCols, row0);
+        for (int b = 0; b < 2; ++b) {
+          residual_rows_async(ea, ebuf0 + b * E_BUF, q, lane, row0, M, N, col0 + b * CH::kCols);
+          cp_async_commit();
+        }
+        if (row < M) {
+          const float* xr = static_cast<const float*>(ea.out) + (size_t)row * N + col0;
+          for (int c = 2; c < CH::kPerHalf; ++c) prefetch_l2(xr + c * CH::kCols);
         }
       }
       // RoPE: this row's (cos, sin) for the 32 pairs of a 64-wide head are the same for every
@@ -409,8 +438,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < 32; ++i) v[i] = vlast[i];
           }
           if constexpr (EPI == ESM_EPI_RESIDUAL) {
-            if (!mbar_wait(&sm->xload[half][b], (xphase >> b) & 1u)) latch_error(err, ERRBIT_TIMEOUT);
-            xphase ^= 1u << b;
+            // this chunk's rows have landed (one younger group may still be in flight)
+            if (c + 1 < CH::kPerHalf) cp_async_wait<1>();
+            else cp_async_wait<0>();
+            __syncwarp();
           }
           load_bias32(ea, col, bb);
 #pragma unroll
@@ -424,6 +455,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             o.z = x.z + (v[4 * j + 2] * acc_scale + bb[4 * j + 2]);
             o.w = x.w + (v[4 * j + 3] * acc_scale + bb[4 * j + 3]);
             *reinterpret_cast<float4*>(buf + off) = o;
+          }
+          if constexpr (EPI == ESM_EPI_RESIDUAL) {
+            // coalesced write-back of this warp's 32 rows, then refill the buffer with the
+            // residual of chunk c + 2
+            __syncwarp();
+            residual_rows_store(ea, buf, q, lane, row0, M, N, col);
+            __syncwarp();
+            if (c + 2 < CH::kPerHalf) {
+              residual_rows_async(ea, buf, q, lane, row0, M, N, col + 2 * CH::kCols);
+              cp_async_commit();
+            }
+            continue;
           }
         } else if constexpr (OUT == Act::E4M3) {  // fc1 + GELU -> E4M3, 128 columns
 #pragma unroll 1
@@ -482,18 +525,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (elect) {
           tma_store_2d(&tmO, col, row0, buf);
           bulk_commit();
-          if constexpr (EPI == ESM_EPI_RESIDUAL) {
-            if (c + 2 < CH::kPerHalf) {  // next residual chunk for this buffer
-              bulk_wait_read<0>();
-              mbar_arrive_expect_tx(&sm->xload[half][b], E_BUF);
-              tma_load_2d(buf, &tmO, col + 2 * CH::kCols, row0, &sm->xload[half][b]);
-            }
-          }
         }
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if (elect) bulk_wait_all();  // stores complete before the CTA may exit
+    if constexpr (EPI == ESM_EPI_RESIDUAL) cp_async_wait<0>();  // (only after an early exit)
     if constexpr (OUT == Act::E4M3) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
