@@ -12,17 +12,19 @@
 //               (x = column of the head, y = token row).
 //   warp 1      one thread issues the MMAs of a global sequence of key tiles g:
 //               S(g) = Q K^T (M=128, N=128, K=64) into TMEM, then O += P V for tile g-1
-//               (M=128, N=64, K=128; P read from TMEM, V an MN-major shared-memory operand),
-//               so the tensor core computes the next S while the softmax warps exponentiate,
-//               also across item boundaries.
-//   warps 2..5  softmax: thread r owns query row r.  It reads its S row from TMEM twice in
-//               32-column chunks (row max, then exponentials), masks keys past the sequence
-//               end, and keeps a running reference max m with a lazy
-//               update: O and the running sum l are rescaled (in TMEM) only when a tile's max
-//               exceeds m by more than 8 (log2 units), so P stays <= 2^8.  P = 2^(s*log2e/8
-//               - m) goes back to TMEM as bf16; after an item's last tile O / l is stored as
-//               bf16 (or E4M3 with the FP8 scale).  Writing the next item's first P happens
-//               after O was read, which is what lets that item's first P V overwrite O.
+//               (M=128, N=64, K=128; P read from TMEM, V an MN-major shared-memory operand).
+//   warps 2, 3  no role (they complete warpgroup 0, which hands registers to warpgroup 1).
+//   warps 4..7  softmax (warpgroup 1, register budget raised with setmaxnreg): thread r owns
+//               query row r.  It reads its whole S row (128 scores) from TMEM into registers
+//               and immediately releases S, so the tensor core computes S(g+1) while this
+//               tile is exponentiated.  Keys past the sequence end are masked; a running
+//               reference max m is updated lazily: O and the running sum l are rescaled (in
+//               TMEM) only when a tile's max exceeds m by more than 8 (log2 units), so
+//               P <= 2^8.  P = 2^(s*log2e/8 - m) goes back to TMEM as bf16.  After an item's
+//               last tile O / l is written (bf16, or E4M3 with the FP8 scale) into the
+//               item's Q buffer, which the last S has finished reading, and each warp stores
+//               its 32 rows with coalesced 16-byte stores; only then is the Q buffer handed
+//               back to the TMA warp.
 // Tensor memory: S 128 columns, P 64 (bf16 pairs), O 64 -> 256 columns per CTA.  Every
 // mbarrier wait is bounded.
 #include "common.cuh"
@@ -36,7 +38,12 @@ constexpr int QT = 128;
 constexpr int KT = 128;
 constexpr int STG = 2;
 constexpr int TILE_BYTES = 128 * 128;  // 128 rows x 128 bytes
-constexpr int THREADS = 192;
+constexpr int THREADS = 256;
+// Register budget per thread at launch (2 CTAs of 256 threads per SM) and after the
+// warpgroup-wide setmaxnreg: warpgroup 0 (TMA, MMA) gives up registers to warpgroup 1
+// (softmax), 128 * kRegsWg0 + 128 * kRegsWg1 = 256 * kRegsLaunch.
+constexpr int kRegsLaunch = 128, kRegsWg0 = 56, kRegsWg1 = 200;
+static_assert(128 * kRegsWg0 + 128 * kRegsWg1 == THREADS * kRegsLaunch, "register split");
 constexpr int CTAS_PER_SM = 2;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_S = 0, COL_P = 128, COL_O = 192;
@@ -67,6 +74,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// 16-byte unit j of row r of a 128-row x 128-byte staging tile, XOR-swizzled by row so the
+// row-per-thread writes and the rows-per-instruction reads are both conflict-free.
+__device__ __forceinline__ uint32_t stage_off(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+// max of three (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 struct Item {
@@ -106,7 +124,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm->q_full[b], 1);
-      mbar_init(&sm->q_empty[b], 1);
+      mbar_init(&sm->q_empty[b], 4);  // one arrival per softmax warp after its O rows are out
     }
     for (int s = 0; s < STG; ++s) {
       mbar_init(&sm->kv_full[s], 1);
@@ -126,6 +144,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -201,7 +220,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             mma_bf16_ss(tmem + COL_S, make_sw128_desc(a0 + 32 * k), make_sw128_desc(b0 + 32 * k), idesc_s,
                         k > 0 ? 1u : 0u);
           mma_commit(&sm->s_full);
-          if (j == x.nkb - 1) mma_commit(&sm->q_empty[qb]);  // Q buffer free once these S are done
           if (g > 0 && !issue_pv(g - 1, prev_first)) { ok = false; break; }
           prev_first = (j == 0);
         }
@@ -215,46 +233,53 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       mbar_wait(&sm->mma_done, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int r = (warp & 3) * 32 + lane;                 // query row of this thread
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWg1));
+    const int wq = warp & 3;                                // TMEM lane quarter
+    const int r = wq * 32 + lane;                           // query row of this thread
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float c = 1.4426950408889634f / sqrtf((float)DH);
     const float qs = (OUT == Act::E4M3) ? __ldg(q_scale) : 1.f;
     float amax = 0.f;
     bool ok = true;
-    int g = 0;
+    int g = 0, qi = 0;
     int4 nxt = load_item(pb, blockIdx.x, heads);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++qi) {
       const Item x = make_item(nxt, it, heads);
       if (it + (int)gridDim.x < n_items) nxt = load_item(pb, it + gridDim.x, heads);  // prefetch
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < x.nkb; ++j, ++g) {
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
-        const int kvalid = x.klen - j * KT;  // keys >= kvalid lie past the sequence end
-        // pass 1: row max of the raw scores (all four 32-column chunks in flight at once)
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        // the whole S row into registers; S is then free for the next tile's Q K^T
+        float sv[KT];
         {
           uint32_t su[KT / 32][32];
 #pragma unroll
           for (int ch = 0; ch < KT / 32; ++ch) tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * ch, su[ch]);
 #pragma unroll
           for (int ch = 0; ch < KT / 32; ++ch) tmem_ld_wait_regs(su[ch]);
-          float sv[KT];
 #pragma unroll
           for (int i = 0; i < KT; ++i) sv[i] = __uint_as_float(su[i >> 5][i & 31]);
-          if (kvalid < KT) {
-#pragma unroll
-            for (int i = 0; i < KT; ++i) sv[i] = i < kvalid ? sv[i] : -INFINITY;
-          }
-#pragma unroll
-          for (int i = 0; i < KT; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
         }
-        const float mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->s_free);
+        const int kvalid = x.klen - j * KT;  // keys >= kvalid lie past the sequence end
+        if (kvalid < KT) {
+#pragma unroll
+          for (int i = 0; i < KT; ++i) sv[i] = i < kvalid ? sv[i] : -INFINITY;
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < KT; i += 8) {
+          mx[0] = fmax3(mx[0], sv[i], sv[i + 1]);
+          mx[1] = fmax3(mx[1], sv[i + 2], sv[i + 3]);
+          mx[2] = fmax3(mx[2], sv[i + 4], sv[i + 5]);
+          mx[3] = fmax3(mx[3], sv[i + 6], sv[i + 7]);
+        }
+        const float mt = c * fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
         const bool need = mt > m_ref + kRescaleThreshold;
         const float m_new = need ? mt : m_ref;
         const float f = need ? fast_exp2(m_ref - m_new) : 1.f;  // 0 on the first tile
@@ -263,58 +288,42 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
           tc_fence_after();
         }
-        if (j > 0 && __any_sync(0xffffffffu, need)) {  // warp-collective TMEM round trip of O
-#pragma unroll
-          for (int ch = 0; ch < DH / 32; ++ch) {
-            float v[32];
-            tmem_ld32(tmem + lane_off + COL_O + 32 * ch, v);
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i] * f);
-            tmem_st32(tmem + lane_off + COL_O + 32 * ch, w);
-          }
-          tmem_st_wait();
-        }
         l *= f;
         m_ref = m_new;
-        // pass 2: P = 2^(s*c - m) chunk by chunk, back to TMEM as bf16 pairs; the load of the
-        // next chunk is in flight while this one is exponentiated
+        // P = 2^(s*c - m) (hardware ex2), back to TMEM as bf16 pairs
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t su[2][32];
-        tmem_ld32_nowait(tmem + lane_off + COL_S, su[0]);
-        tmem_ld_wait_regs(su[0]);
 #pragma unroll
         for (int ch = 0; ch < KT / 32; ++ch) {
-          if (ch + 1 < KT / 32) tmem_ld32_nowait(tmem + lane_off + COL_S + 32 * (ch + 1), su[(ch + 1) & 1]);
-          float cur[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) cur[i] = __uint_as_float(su[ch & 1][i]);
-          if (kvalid < KT) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) cur[i] = 32 * ch + i < kvalid ? cur[i] : -INFINITY;
-          }
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = fast_exp2(fmaf(cur[2 * i], c, -m_ref));
-            const float p1 = fast_exp2(fmaf(cur[2 * i + 1], c, -m_ref));
+            const float p0 = fast_exp2(fmaf(sv[32 * ch + 2 * i], c, -m_ref));
+            const float p1 = fast_exp2(fmaf(sv[32 * ch + 2 * i + 1], c, -m_ref));
             ls[i & 3] += p0 + p1;
             w[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tmem + lane_off + COL_P + 16 * ch, w);
-          if (ch + 1 < KT / 32) tmem_ld_wait_regs(su[(ch + 1) & 1]);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (j > 0 && __any_sync(0xffffffffu, need)) {  // warp-collective TMEM round trip of O
+#pragma unroll
+          for (int ch = 0; ch < DH / 16; ++ch) {
+            float v[16];
+            tmem_ld16(tmem + lane_off + COL_O + 16 * ch, v);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * f);
+            tmem_st16(tmem + lane_off + COL_O + 16 * ch, w);
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sm->s_free);  // S was last read in pass 2
-          mbar_arrive(&sm->p_full);
-        }
+        if (lane == 0) mbar_arrive(&sm->p_full);
       }
       if (!ok) break;
-      // ---- item epilogue: O / l -> global
+      // ---- item epilogue: O / l through this item's Q buffer (the last S has read it) to
+      // global memory, 16 bytes per lane covering whole output rows per instruction
       if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
       tc_fence_after();
       uint32_t u[2][32];
@@ -324,38 +333,53 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       tmem_ld_wait_regs(u[1]);
       tc_fence_before();
       const float inv = 1.f / l;
-      if (r < x.qrows) {
-        const size_t off = (size_t)(x.qrow0 + r) * d + x.h * DH;
-        if constexpr (OUT == Act::BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + off);
+      uint8_t* stage = sQ + (qi & 1) * TILE_BYTES;
+      constexpr int kUnits = (OUT == Act::BF16) ? 8 : 4;  // 16-byte units per output row
+      if constexpr (OUT == Act::BF16) {
 #pragma unroll
-          for (int i = 0; i < DH / 8; ++i) {
-            const uint32_t* w = &u[i >> 2][(i & 3) * 8];
-            uint4 q;
-            q.x = pack_bf16x2(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv);
-            q.y = pack_bf16x2(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv);
-            q.z = pack_bf16x2(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv);
-            q.w = pack_bf16x2(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv);
-            dst[i] = q;
+        for (int i = 0; i < DH / 8; ++i) {
+          const uint32_t* w = &u[i >> 2][(i & 3) * 8];
+          uint4 q;
+          q.x = pack_bf16x2(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv);
+          q.y = pack_bf16x2(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv);
+          q.z = pack_bf16x2(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv);
+          q.w = pack_bf16x2(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv);
+          *reinterpret_cast<uint4*>(stage + stage_off(r, i)) = q;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < DH / 16; ++i) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t* w = &u[i >> 1][(i & 1) * 16 + 4 * k];
+            const float a0 = __uint_as_float(w[0]) * inv, a1 = __uint_as_float(w[1]) * inv;
+            const float a2 = __uint_as_float(w[2]) * inv, a3 = __uint_as_float(w[3]) * inv;
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
+            __nv_fp8x4_e4m3 qv(make_float4(a0 * qs, a1 * qs, a2 * qs, a3 * qs));
+            w4[k] = *reinterpret_cast<uint32_t*>(&qv);
           }
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(o) + off);
-#pragma unroll
-          for (int i = 0; i < DH / 16; ++i) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t* w = &u[i >> 1][(i & 1) * 16 + 4 * k];
-              const float a0 = __uint_as_float(w[0]) * inv, a1 = __uint_as_float(w[1]) * inv;
-              const float a2 = __uint_as_float(w[2]) * inv, a3 = __uint_as_float(w[3]) * inv;
-              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
-              __nv_fp8x4_e4m3 qv(make_float4(a0 * qs, a1 * qs, a2 * qs, a3 * qs));
-              w4[k] = *reinterpret_cast<uint32_t*>(&qv);
-            }
-            dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
+          *reinterpret_cast<uint4*>(stage + stage_off(r, i)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
+      __syncwarp();
+      {
+        constexpr int kRowsPerInst = 32 / kUnits;
+        constexpr size_t kElem = (OUT == Act::BF16) ? 2 : 1;
+        uint8_t* ob = static_cast<uint8_t*>(o);
+#pragma unroll
+        for (int i = 0; i < 32 / kRowsPerInst; ++i) {
+          const int rr = wq * 32 + i * kRowsPerInst + lane / kUnits;
+          const int un = lane % kUnits;
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + stage_off(rr, un));
+          if (rr < x.qrows)
+            *reinterpret_cast<uint4*>(ob + ((size_t)(x.qrow0 + rr) * d + (size_t)x.h * DH) * kElem + 16 * un) = v;
+        }
+      }
+      // generic-proxy accesses of the Q buffer are ordered before the next TMA write to it
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->q_empty[qi & 1]);
     }
     if (!ok) {
       latch_error(err, ERRBIT_TIMEOUT);

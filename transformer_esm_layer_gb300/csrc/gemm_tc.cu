@@ -6,7 +6,7 @@
 // the pair multiplies with tcgen05.mma.cta_group::2 (M = 256: 128 rows per CTA, B split by
 // N between the two CTAs, so each SM streams 32 KB per 64-wide K-slice).  Roles:
 //   warp 0       TMA producer (each CTA): its A rows and its half of B, K-slices of 128
-//                bytes with the 128-byte swizzle, into a 5-stage shared-memory ring; both
+//                bytes with the 128-byte swizzle, into a 5- or 6-stage shared-memory ring; both
 //                CTAs' copies complete on the leader CTA's "full" mbarrier;
 //   warp 1       MMA issuer (leader CTA, one thread): tcgen05.mma (K=16 for bf16, K=32 for
 //                e4m3) into one of two TMEM accumulators; tcgen05.commit multicasts to both
@@ -37,7 +37,7 @@ namespace {
 constexpr int BM = 128;                        // rows per CTA
 constexpr int BN = 256;                        // columns per tile
 constexpr int TILE_M = 2 * BM;                 // rows per CTA pair
-constexpr int S = 5;                           // ring stages
+constexpr int S_MAX = 6;                       // ring stages (at most)
 constexpr int ROW_BYTES = 128;                 // one K-slice row: 64 bf16 or 128 e4m3
 constexpr int A_STAGE = BM * ROW_BYTES;        // 16 KB
 constexpr int B_STAGE = (BN / 2) * ROW_BYTES;  // 16 KB: this CTA's half of B
@@ -45,11 +45,25 @@ constexpr int E_BUF = 128 * 128;               // 16 KB epilogue staging chunk (
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int TMEM_COLS = 2 * BN;              // two accumulators
-constexpr int SMEM_BYTES = S * (A_STAGE + B_STAGE) + 4 * E_BUF + 1024 /*align*/ + 256 /*barriers*/;
+
+// Shared-memory plan per epilogue.  The bf16 / E4M3 outputs leave through TMA stores from
+// two 16 KB staging chunks per column half (one being stored while the next is written),
+// which leaves room for a 5-stage operand ring.  The residual epilogue moves its fp32
+// chunks through the load/store unit one chunk per warp at a time, so one staging chunk
+// per half suffices and the ring gets a 6th stage (its long-K launch streams A from HBM).
+template <int EPI>
+struct Plan {
+  static constexpr int kStages = (EPI == ESM_EPI_RESIDUAL) ? 6 : 5;
+  static constexpr int kEBufs = (EPI == ESM_EPI_RESIDUAL) ? 1 : 2;  // staging chunks per half
+  static constexpr int kSmemBytes =
+      kStages * (A_STAGE + B_STAGE) + 2 * kEBufs * E_BUF + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(kStages <= S_MAX, "barrier arrays");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
 
 struct Smem {
-  uint64_t full[S];
-  uint64_t empty[S];
+  uint64_t full[S_MAX];
+  uint64_t empty[S_MAX];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -213,12 +227,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, int M, int N, int K, EpiArgs ea, unsigned* err) {
   using CH = Chunk<EPI, OUT>;
+  constexpr int S = Plan<EPI>::kStages;
+  constexpr int NB = Plan<EPI>::kEBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + S * A_STAGE;
   uint8_t* sE = sB + S * B_STAGE;  // [half][buffer] 16 KB each
-  Smem* sm = reinterpret_cast<Smem*>(sE + 4 * E_BUF);
+  Smem* sm = reinterpret_cast<Smem*>(sE + 2 * NB * E_BUF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -352,7 +368,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = q * 32 + lane;               // this thread's row inside the CTA's 128
     const bool elect = (warp == 2 + 4 * half) && lane == 0;  // issues the half's bulk copies
     const uint32_t bar_id = 1 + (uint32_t)half;             // named barrier of the half's 4 warps
-    uint8_t* const ebuf0 = sE + (2 * half) * E_BUF;  // buffer b of this half: ebuf0 + b * E_BUF
+    uint8_t* const ebuf0 = sE + (NB * half) * E_BUF;  // buffer b of this half: ebuf0 + b * E_BUF
     const uint32_t tempty_leader = map_to_rank(&sm->tempty[0], 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -378,13 +394,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         // its rows of the two staging buffers (coalesced: 4 rows x 128 bytes per
         // instruction) and pulls its rows of the later chunks into L2.
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NB; ++b) {
           residual_rows_async(ea, ebuf0 + b * E_BUF, q, lane, row0, M, N, col0 + b * CH::kCols);
           cp_async_commit();
         }
         if (row < M) {
           const float* xr = static_cast<const float*>(ea.out) + (size_t)row * N + col0;
-          for (int c = 2; c < CH::kPerHalf; ++c) prefetch_l2(xr + c * CH::kCols);
+          for (int c = NB; c < CH::kPerHalf; ++c) prefetch_l2(xr + c * CH::kCols);
         }
       }
       // RoPE: this row's (cos, sin) for the 32 pairs of a 64-wide head are the same for every
@@ -415,7 +431,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 #pragma unroll 1
       for (int c = 0; c < CH::kPerHalf; ++c) {
-        const int b = c & 1;
+        const int b = c % NB;
         uint8_t* buf = ebuf0 + b * E_BUF;
         const int col = col0 + c * CH::kCols;
         if constexpr (EPI != ESM_EPI_RESIDUAL) {
@@ -438,8 +454,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < 32; ++i) v[i] = vlast[i];
           }
           if constexpr (EPI == ESM_EPI_RESIDUAL) {
-            // this chunk's rows have landed (one younger group may still be in flight)
-            if (c + 1 < CH::kPerHalf) cp_async_wait<1>();
+            // this chunk's rows have landed (the next chunk's may still be in flight)
+            if (NB == 2 && c + 1 < CH::kPerHalf) cp_async_wait<1>();
             else cp_async_wait<0>();
             __syncwarp();
           }
@@ -458,12 +474,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if constexpr (EPI == ESM_EPI_RESIDUAL) {
             // coalesced write-back of this warp's 32 rows, then refill the buffer with the
-            // residual of chunk c + 2
+            // residual of chunk c + NB
             __syncwarp();
             residual_rows_store(ea, buf, q, lane, row0, M, N, col);
             __syncwarp();
-            if (c + 2 < CH::kPerHalf) {
-              residual_rows_async(ea, buf, q, lane, row0, M, N, col + 2 * CH::kCols);
+            if (c + NB < CH::kPerHalf) {
+              residual_rows_async(ea, buf, q, lane, row0, M, N, col + NB * CH::kCols);
               cp_async_commit();
             }
             continue;
@@ -552,7 +568,7 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
   auto kern = gemm_tc_kernel<EPI, FP8, OUT>;
   static int max_clusters = 0;  // per instantiation: co-resident clusters of two on this device
   if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan<EPI>::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -562,7 +578,7 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = Plan<EPI>::kSmemBytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
@@ -580,7 +596,7 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Plan<EPI>::kSmemBytes;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -589,7 +605,7 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
 
 }  // namespace
 
-int gemm_tc_smem_bytes() { return SMEM_BYTES; }
+int gemm_tc_smem_bytes() { return Plan<ESM_EPI_QKV_ROPE>::kSmemBytes; }
 // Rows of the TMA boxes the launched kernel expects: its own 128 rows of A, and its half of
 // the 256-wide B tile; the output map's box is 128 bytes of columns by 128 rows.
 int gemm_tc_a_box_rows() { return BM; }
