@@ -8,11 +8,12 @@
 // Persistent: two CTAs per SM walk the (sequence, 128-query tile, head) work items of the
 // length-ordered list in a static stride; barrier phases run on across items.
 //   warp 0      TMA: each item's Q tile (double-buffered, 128-byte swizzle) and its K and V
-//               tiles of 128 keys into a 2-stage ring, straight from the packed qkv buffer
-//               (x = column of the head, y = token row).
+//               tiles of 128 keys into 2-stage rings (K and V released separately),
+//               straight from the packed qkv buffer (x = column of the head, y = token row).
 //   warp 1      one thread issues the MMAs of a global sequence of key tiles g:
-//               S(g) = Q K^T (M=128, N=128, K=64) into TMEM, then O += P V for tile g-1
-//               (M=128, N=64, K=128; P read from TMEM, V an MN-major shared-memory operand).
+//               S(g) = Q K^T (M=128, N=128, K=64) into TMEM and O += P V (M=128, N=64,
+//               K=128; P read from TMEM, V an MN-major shared-memory operand), each as soon
+//               as its operands are ready.
 //   warps 2, 3  no role (they complete warpgroup 0, which hands registers to warpgroup 1).
 //   warps 4..7  softmax (warpgroup 1, register budget raised with setmaxnreg): thread r owns
 //               query row r.  It reads its whole S row (128 scores) from TMEM into registers
@@ -51,7 +52,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct AttnSmem {
   uint64_t q_full[2], q_empty[2];
-  uint64_t kv_full[STG], kv_empty[STG];
+  uint64_t k_full[STG], k_empty[STG];  // K tile landed / read by its S = Q K^T
+  uint64_t v_full[STG], v_empty[STG];  // V tile landed / read by its O += P V
   uint64_t s_full, s_free, p_full, pv_done, mma_done;
   uint32_t tmem_base;
   volatile int abort;
@@ -127,8 +129,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       mbar_init(&sm->q_empty[b], 4);  // one arrival per softmax warp after its O rows are out
     }
     for (int s = 0; s < STG; ++s) {
-      mbar_init(&sm->kv_full[s], 1);
-      mbar_init(&sm->kv_empty[s], 1);
+      mbar_init(&sm->k_full[s], 1);
+      mbar_init(&sm->k_empty[s], 1);
+      mbar_init(&sm->v_full[s], 1);
+      mbar_init(&sm->v_empty[s], 1);
     }
     mbar_init(&sm->s_full, 1);
     mbar_init(&sm->s_free, 4);
@@ -163,68 +167,112 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         mbar_arrive_expect_tx(&sm->q_full[qb], TILE_BYTES);
         tma_load_2d(sQ + qb * TILE_BYTES, &tm, x.h * DH, x.qrow0, &sm->q_full[qb]);
         for (int j = 0; j < x.nkb; ++j, ++g) {
+          // K stages free up when their S is done, V stages only after their P V: waiting
+          // for each separately lets K run a tile further ahead of the tensor core.
           const int st = g % STG;
-          if (!mbar_wait(&sm->kv_empty[st], ((uint32_t)(g / STG) & 1u) ^ 1u)) {
+          const uint32_t par = ((uint32_t)(g / STG) & 1u) ^ 1u;
+          if (!mbar_wait(&sm->k_empty[st], par)) {
             latch_error(err, ERRBIT_TIMEOUT);
             sm->abort = 1;
             break;
           }
-          mbar_arrive_expect_tx(&sm->kv_full[st], 2 * TILE_BYTES);
-          tma_load_2d(sK + 2 * st * TILE_BYTES, &tm, d + x.h * DH, x.krow0 + j * KT, &sm->kv_full[st]);
-          tma_load_2d(sV + 2 * st * TILE_BYTES, &tm, 2 * d + x.h * DH, x.krow0 + j * KT, &sm->kv_full[st]);
+          mbar_arrive_expect_tx(&sm->k_full[st], TILE_BYTES);
+          tma_load_2d(sK + 2 * st * TILE_BYTES, &tm, d + x.h * DH, x.krow0 + j * KT, &sm->k_full[st]);
+          if (!mbar_wait(&sm->v_empty[st], par)) {
+            latch_error(err, ERRBIT_TIMEOUT);
+            sm->abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm->v_full[st], TILE_BYTES);
+          tma_load_2d(sV + 2 * st * TILE_BYTES, &tm, 2 * d + x.h * DH, x.krow0 + j * KT, &sm->v_full[st]);
         }
       }
       // Copies still in flight can only exist if a consumer gave up early: then the last
       // STG stages are waited for (bounded) before the CTA exits.
       if (sm->abort) {
-        for (int k = g - 1; k >= 0 && k >= g - STG; --k)
-          if (!mbar_wait(&sm->kv_full[k % STG], (uint32_t)(k / STG) & 1u)) break;
+        for (int k = g - 1; k >= 0 && k >= g - STG; --k) {
+          if (!mbar_wait(&sm->k_full[k % STG], (uint32_t)(k / STG) & 1u)) break;
+          if (!mbar_wait(&sm->v_full[k % STG], (uint32_t)(k / STG) & 1u)) break;
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Two cursors over the global tile sequence: gs, the next S = Q K^T, and gp, the next
+    // O += P V (gp < gs).  Whichever has its operands ready is issued, the P V first: the
+    // softmax of tile gp+1 waits for it before storing its P, while S(gs) is usually ready
+    // long before it is needed.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(QT, KT);
       constexpr uint32_t idesc_pv = idesc_bf16(QT, DH) | (1u << 16);  // B (= V) MN-major
+      const uint64_t qdesc0 = make_sw128_desc(smem_u32(sQ));  // buffer b: + b * (TILE_BYTES >> 4)
+      const uint64_t kdesc0 = make_sw128_desc(smem_u32(sK));  // stage s: + 2 s (TILE_BYTES >> 4)
+      const uint64_t vdesc0 = make_sw128_desc(smem_u32(sV));
       bool ok = true;
-      int g = 0, qi = 0;
-      bool prev_first = false;  // tile g-1 was the first tile of its item
-      auto issue_pv = [&](int gp, bool first) -> bool {
-        if (!mbar_wait(&sm->p_full, (uint32_t)gp & 1u)) return false;
-        tc_fence_after();
-        const uint32_t v0 = smem_u32(sV + 2 * (gp % STG) * TILE_BYTES);
-#pragma unroll
-        for (int k = 0; k < KT / 16; ++k)
-          mma_bf16_ts(tmem + COL_O, tmem + COL_P + 8 * k, make_sw128_desc(v0 + 2048 * k), idesc_pv,
-                      (!first || k > 0) ? 1u : 0u);
-        mma_commit(&sm->pv_done);
-        mma_commit(&sm->kv_empty[gp % STG]);
-        return true;
-      };
+      int gs = 0, gp = 0;        // next S, next P V
+      int it_s = blockIdx.x, js = 0, qi_s = 0, nkb_s = 0;
+      bool have_item = false;
+      uint32_t first_bits = 0;   // bit (g & 31): tile g is the first of its item
       int4 nxt = load_item(pb, blockIdx.x, heads);
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++qi) {
-        const Item x = make_item(nxt, it, heads);
-        if (it + (int)gridDim.x < n_items) nxt = load_item(pb, it + gridDim.x, heads);  // prefetch
-        const int qb = qi & 1;
-        if (!mbar_wait(&sm->q_full[qb], (uint32_t)(qi >> 1) & 1u)) { ok = false; break; }
-        const uint32_t a0 = smem_u32(sQ + qb * TILE_BYTES);
-        for (int j = 0; j < x.nkb; ++j, ++g) {
-          const int st = g % STG;
-          if (!mbar_wait(&sm->kv_full[st], (uint32_t)(g / STG) & 1u)) { ok = false; break; }
-          if (g > 0 && !mbar_wait(&sm->s_free, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
+      unsigned long long idle_since = 0;
+      uint32_t idle = 0;
+      while (true) {
+        if (!have_item && it_s < n_items) {
+          const Item x = make_item(nxt, it_s, heads);
+          if (it_s + (int)gridDim.x < n_items) nxt = load_item(pb, it_s + gridDim.x, heads);
+          nkb_s = x.nkb;
+          js = 0;
+          have_item = true;
+        }
+        if (!have_item && gp == gs) break;  // every tile issued
+        bool progressed = false;
+        if (gp < gs && mbar_test(&sm->p_full, (uint32_t)gp & 1u) &&
+            mbar_test(&sm->v_full[gp % STG], (uint32_t)(gp / STG) & 1u)) {
           tc_fence_after();
-          const uint32_t b0 = smem_u32(sK + 2 * st * TILE_BYTES);
+          const bool first = (first_bits >> (gp & 31)) & 1u;
+          const uint64_t vd = vdesc0 + (uint64_t)((2 * (gp % STG) * TILE_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < DH / 16; ++k)
-            mma_bf16_ss(tmem + COL_S, make_sw128_desc(a0 + 32 * k), make_sw128_desc(b0 + 32 * k), idesc_s,
-                        k > 0 ? 1u : 0u);
-          mma_commit(&sm->s_full);
-          if (g > 0 && !issue_pv(g - 1, prev_first)) { ok = false; break; }
-          prev_first = (j == 0);
+          for (int k = 0; k < KT / 16; ++k)  // 16 keys = 16 rows of V = 2048 bytes
+            mma_bf16_ts(tmem + COL_O, tmem + COL_P + 8 * k, vd + (uint64_t)(128 * k), idesc_pv,
+                        (!first || k > 0) ? 1u : 0u);
+          mma_commit(&sm->pv_done);
+          mma_commit(&sm->v_empty[gp % STG]);
+          ++gp;
+          progressed = true;
+        } else if (have_item && gs - gp < 3) {
+          const int st = gs % STG;
+          const int qb = qi_s & 1;
+          if (mbar_test(&sm->k_full[st], (uint32_t)(gs / STG) & 1u) &&
+              (gs == 0 || mbar_test(&sm->s_free, (uint32_t)(gs - 1) & 1u)) &&
+              (js > 0 || mbar_test(&sm->q_full[qb], (uint32_t)(qi_s >> 1) & 1u))) {
+            tc_fence_after();
+            const uint64_t ad = qdesc0 + (uint64_t)((qb * TILE_BYTES) >> 4);
+            const uint64_t bd = kdesc0 + (uint64_t)((2 * st * TILE_BYTES) >> 4);
+#pragma unroll
+            for (int k = 0; k < DH / 16; ++k)  // 16 dims = 32 bytes of each 128-byte row
+              mma_bf16_ss(tmem + COL_S, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
+            mma_commit(&sm->s_full);
+            mma_commit(&sm->k_empty[st]);
+            if (js == 0) first_bits |= 1u << (gs & 31);
+            else first_bits &= ~(1u << (gs & 31));
+            ++gs;
+            if (++js == nkb_s) {
+              have_item = false;
+              it_s += gridDim.x;
+              ++qi_s;
+            }
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle = 0;
+        } else if ((++idle & 63u) == 1u) {  // bounded: give up after the wait limit idle
+          const unsigned long long now = globaltimer_ns();
+          if (idle == 1u) idle_since = now;
+          else if (now - idle_since > kWaitLimitNs) { ok = false; break; }
         }
       }
-      if (ok && g > 0) ok = issue_pv(g - 1, prev_first);
       if (!ok) {
         latch_error(err, ERRBIT_TIMEOUT);
         sm->abort = 1;
@@ -283,28 +331,30 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         const bool need = mt > m_ref + kRescaleThreshold;
         const float m_new = need ? mt : m_ref;
         const float f = need ? fast_exp2(m_ref - m_new) : 1.f;  // 0 on the first tile
-        // P (and, within an item, O) may be rewritten once the previous P V is done
-        if (g > 0) {
-          if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
-          tc_fence_after();
-        }
         l *= f;
         m_ref = m_new;
-        // P = 2^(s*c - m) (hardware ex2), back to TMEM as bf16 pairs
+        // P = 2^(s*c - m) (hardware ex2) as bf16 pairs, computed while the previous P V may
+        // still be reading the P columns
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t w[KT / 32][16];
 #pragma unroll
         for (int ch = 0; ch < KT / 32; ++ch) {
-          uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float p0 = fast_exp2(fmaf(sv[32 * ch + 2 * i], c, -m_ref));
             const float p1 = fast_exp2(fmaf(sv[32 * ch + 2 * i + 1], c, -m_ref));
             ls[i & 3] += p0 + p1;
-            w[i] = pack_bf16x2(p0, p1);
+            w[ch][i] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(tmem + lane_off + COL_P + 16 * ch, w);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P (and, within an item, O) may be rewritten once the previous P V is done
+        if (g > 0) {
+          if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int ch = 0; ch < KT / 32; ++ch) tmem_st16(tmem + lane_off + COL_P + 16 * ch, w[ch]);
         if (j > 0 && __any_sync(0xffffffffu, need)) {  // warp-collective TMEM round trip of O
 #pragma unroll
           for (int ch = 0; ch < DH / 16; ++ch) {
