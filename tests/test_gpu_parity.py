@@ -146,6 +146,25 @@ def test_gemm_epilogues():
     assert rel_l2(to_np(x), ref) < 1e-5
 
 
+def test_gemm_residual_with_half_width_tail_tiles():
+    """M=5000, N=1280: 100 tiles of 256 x 256 on the persistent grid, so the last ones run as
+    256 x 128 halves (and the last row band is ragged); x += A W^T + b against float64."""
+    enc = _enc(SMALL, "bf16")
+    rng = np.random.default_rng(13)
+    M, K, N = 5000, 1280, 1280
+    A = _bf16(rng.standard_normal((M, K)))
+    W = _bf16(rng.standard_normal((N, K)) * 0.05)
+    b = _bf16(rng.standard_normal(N) * 0.1)
+    x0 = rng.standard_normal((M, N)).astype(np.float32)
+    x = _dev(x0, torch.float32)
+    enc.op_gemm("residual", _dev(A, torch.bfloat16), _dev(W, torch.bfloat16), _dev(b, torch.bfloat16), x)
+    assert enc.check_status() == 0
+    ref = x0 + A.astype(np.float64) @ W.astype(np.float64).T + b
+    got = to_np(x)
+    assert rel_l2(got, ref) < 1e-5
+    assert np.max(np.abs(got - ref)) < 1e-3  # every column block, including the half tiles
+
+
 def test_gelu_epilogue_within_bf16_rounding():
     """The GELU epilogue on a sweep of 16384 bf16 inputs x (a GEMM whose only nonzero
     product per output is 1 * x, so the accumulator holds x exactly).  The epilogue's fp32

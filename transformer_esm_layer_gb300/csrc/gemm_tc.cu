@@ -212,6 +212,28 @@ __device__ __forceinline__ void stage_e4m3x32(uint8_t* buf, int r, int u0, const
   }
 }
 
+// Tile t of the static schedule.  The first full_tiles are 256 x 256 (row band t / n_tiles,
+// column tile t % n_tiles); the rest split the remaining full tiles, in order, into two
+// 256 x 128 halves each, so that a partly filled last wave of full tiles becomes a wave of
+// half-length tiles.
+struct TileXY {
+  int m, n0, bn;
+};
+__device__ __forceinline__ TileXY tile_xy(int t, int n_tiles, int full_tiles) {
+  TileXY r;
+  if (t < full_tiles) {
+    r.m = t / n_tiles;
+    r.n0 = (t % n_tiles) * BN;
+    r.bn = BN;
+  } else {
+    const int h = t - full_tiles, orig = full_tiles + (h >> 1);
+    r.m = orig / n_tiles;
+    r.n0 = (orig % n_tiles) * BN + (h & 1) * (BN / 2);
+    r.bn = BN / 2;
+  }
+  return r;
+}
+
 // Columns per staging chunk (128 bytes of one row) for each output type.
 template <int EPI, Act OUT>
 struct Chunk {
@@ -225,7 +247,8 @@ struct Chunk {
 template <int EPI, bool FP8, Act OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmO, int M, int N, int K, EpiArgs ea, unsigned* err) {
+                   const __grid_constant__ CUtensorMap tmO, int M, int N, int K, int full_tiles, int num_tiles,
+                   EpiArgs ea, unsigned* err) {
   using CH = Chunk<EPI, OUT>;
   constexpr int S = Plan<EPI>::kStages;
   constexpr int NB = Plan<EPI>::kEBufs;
@@ -242,9 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const bool leader = rank == 0;
   const int unit = (int)(blockIdx.x >> 1);  // cluster index
   const int units = (int)(gridDim.x >> 1);
-  const int m_tiles = (M + TILE_M - 1) / TILE_M;
   const int n_tiles = N / BN;
-  const int num_tiles = m_tiles * n_tiles;
   const int kb_count = K / (FP8 ? 128 : 64);
 
   if (threadIdx.x == 0) {
@@ -280,8 +301,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int issues = 0;
       for (int tile = unit; tile < num_tiles && !sm->abort; tile += units) {
-        const int m0 = (tile / n_tiles) * TILE_M + (int)rank * BM;
-        const int n0 = (tile % n_tiles) * BN + (int)rank * (BN / 2);
+        const TileXY tx = tile_xy(tile, n_tiles, full_tiles);
+        const int m0 = tx.m * TILE_M + (int)rank * BM;
+        const int n0 = tx.n0 + (int)rank * (tx.bn / 2);  // a half-width tile loads 64 surplus rows
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!mbar_wait(&sm->empty[stage], phase ^ 1)) {
             latch_error(err, ERRBIT_TIMEOUT);
@@ -315,7 +337,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = FP8 ? idesc_e4m3(TILE_M, BN) : idesc_bf16(TILE_M, BN);
+      constexpr uint32_t idesc_full = FP8 ? idesc_e4m3(TILE_M, BN) : idesc_bf16(TILE_M, BN);
+      constexpr uint32_t idesc_half = FP8 ? idesc_e4m3(TILE_M, BN / 2) : idesc_bf16(TILE_M, BN / 2);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -333,6 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t idesc = tile < full_tiles ? idesc_full : idesc_half;
         for (int kb = 0; kb < kb_count; ++kb) {
           if (!mbar_wait(&sm->full[stage], phase)) {
             latch_error(err, ERRBIT_TIMEOUT);
@@ -378,8 +402,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float o_scale = (OUT == Act::E4M3) ? __ldg(ea.o_scale) : 1.f;
 
     for (int tile = unit; tile < num_tiles; tile += units) {
-      const int row0 = (tile / n_tiles) * TILE_M + (int)rank * BM;     // first row of this CTA
-      const int col0 = (tile % n_tiles) * BN + half * (BN / 2);        // first column of this half
+      const TileXY tx = tile_xy(tile, n_tiles, full_tiles);
+      const int row0 = tx.m * TILE_M + (int)rank * BM;                 // first row of this CTA
+      const int col0 = tx.n0 + half * (tx.bn / 2);                     // first column of this half
+      const int nch = tx.bn == BN ? CH::kPerHalf : CH::kPerHalf / 2;  // chunks of this half
       const int row = row0 + r;
       // This warp has read the whole accumulator into registers: hand it back to the MMA
       // warp (one arrival per warp on the leader's barrier) before finishing the chunk.
@@ -400,7 +426,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (row < M) {
           const float* xr = static_cast<const float*>(ea.out) + (size_t)row * N + col0;
-          for (int c = NB; c < CH::kPerHalf; ++c) prefetch_l2(xr + c * CH::kCols);
+          for (int c = NB; c < nch; ++c) prefetch_l2(xr + c * CH::kCols);
         }
       }
       // RoPE: this row's (cos, sin) for the 32 pairs of a 64-wide head are the same for every
@@ -426,11 +452,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       named_bar_sync(bar_id, 128);
       if (sm->fail[half]) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
+      const uint32_t tbase = tmem_base + acc * BN + half * (tx.bn / 2) + ((uint32_t)(q * 32) << 16);
       float vlast[(EPI == ESM_EPI_BIAS_F32 || EPI == ESM_EPI_RESIDUAL) ? 32 : 1];
 
 #pragma unroll 1
-      for (int c = 0; c < CH::kPerHalf; ++c) {
+      for (int c = 0; c < nch; ++c) {
         const int b = c % NB;
         uint8_t* buf = ebuf0 + b * E_BUF;
         const int col = col0 + c * CH::kCols;
@@ -443,9 +469,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           // 32-column chunks: the last two are read from TMEM together, so the accumulator
           // is released one chunk early.
           float v[32], bb[32];
-          if (c + 2 < CH::kPerHalf) {
+          if (c + 2 < nch) {
             tmem_ld32(tbase + c * CH::kCols, v);
-          } else if (c + 2 == CH::kPerHalf) {
+          } else if (c + 2 == nch) {
             tmem_ld32(tbase + c * CH::kCols, v);
             tmem_ld32(tbase + (c + 1) * CH::kCols, vlast);
             release_acc();
@@ -455,7 +481,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if constexpr (EPI == ESM_EPI_RESIDUAL) {
             // this chunk's rows have landed (the next chunk's may still be in flight)
-            if (NB == 2 && c + 1 < CH::kPerHalf) cp_async_wait<1>();
+            if (NB == 2 && c + 1 < nch) cp_async_wait<1>();
             else cp_async_wait<0>();
             __syncwarp();
           }
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             residual_rows_store(ea, buf, q, lane, row0, M, N, col);
             __syncwarp();
-            if (c + NB < CH::kPerHalf) {
+            if (c + NB < nch) {
               residual_rows_async(ea, buf, q, lane, row0, M, N, col + NB * CH::kCols);
               cp_async_commit();
             }
@@ -505,7 +531,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             float a[16], bq[16];
             tmem_ld16(tbase + c * CH::kCols + 16 * h, a);
             tmem_ld16(tbase + c * CH::kCols + 32 + 16 * h, bq);
-            if (h == 1 && c == CH::kPerHalf - 1) release_acc();
+            if (h == 1 && c == nch - 1) release_acc();
             scale_add_bias<16>(ea, col + 16 * h, acc_scale, a);
             scale_add_bias<16>(ea, col + 32 + 16 * h, acc_scale, bq);
             if (col < ea.rope_cols) {
@@ -527,7 +553,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           float v0[32], v1[32];
           tmem_ld32(tbase + c * CH::kCols, v0);
           tmem_ld32(tbase + c * CH::kCols + 32, v1);
-          if (c == CH::kPerHalf - 1) release_acc();
+          if (c == nch - 1) release_acc();
           scale_add_bias<32>(ea, col, acc_scale, v0);
           scale_add_bias<32>(ea, col + 32, acc_scale, v1);
 #pragma unroll
@@ -562,6 +588,34 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Number r of trailing full tiles to split into half-width tiles: the static stride gives
+// cluster u the tiles u, u + clusters, ...; with full = 2 units of work and half = 1 the
+// r minimising the busiest cluster's work is found by trial (remembered per shape).
+int tail_split(int tiles, int clusters) {
+  static int last_tiles = -1, last_clusters = -1, last_split = 0;
+  if (tiles == last_tiles && clusters == last_clusters) return last_split;
+  long best = -1;
+  int split = 0;
+  for (int r = 0; r <= tiles && r <= 2 * clusters; ++r) {
+    const long f = tiles - r, total = f + 2l * r;
+    long worst = 0;
+    for (int u = 0; u < clusters; ++u) {
+      const long nf = f > u ? (f - u + clusters - 1) / clusters : 0;
+      const long all = total > u ? (total - u + clusters - 1) / clusters : 0;
+      const long w = 2 * nf + (all - nf);
+      if (w > worst) worst = w;
+    }
+    if (best < 0 || worst < best) {
+      best = worst;
+      split = r;
+    }
+  }
+  last_tiles = tiles;
+  last_clusters = clusters;
+  last_split = split;
+  return split;
+}
+
 template <int EPI, bool FP8, Act OUT>
 cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmO, int M, int N, int K,
                         const EpiArgs& ea, int num_sms, unsigned* err, cudaStream_t st) {
@@ -588,6 +642,10 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
   }
   const int tiles = ((M + TILE_M - 1) / TILE_M) * (N / BN);
   const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  // Residual epilogue (fp32 chunks of 32 columns): split the last r full tiles into halves
+  // when that shortens the longest cluster's work under the static stride.
+  const int split = EPI == ESM_EPI_RESIDUAL ? tail_split(tiles, clusters) : 0;
+  const int full_tiles = tiles - split, num_tiles = tiles + split;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -600,7 +658,7 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmO, M, N, K, ea, err);
+  return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmO, M, N, K, full_tiles, num_tiles, ea, err);
 }
 
 }  // namespace
