@@ -20,6 +20,9 @@ Sources (page title, section):
   encoder), 输出 (one embedding vector per residue).
 * "Accelerating transformer training with NVIDIA Transformer Engine" (aikraft.ru), section
   "Рецепт FP8: Delayed Scaling" (E4M3 forward format, amax history 16, max).
+* Masked-LM head: the mlqm.cn walkthrough loads the model as ``AutoModelForMaskedLM``
+  (section on usage) and the BioNeMo model card's accuracy benchmark (竞争性基准测试 / 准确率)
+  reports masked-LM perplexity; neither lists the head's layers.
 
 Readings where the pages are silent (each also applied by the CUDA path):
 pre-LayerNorm blocks; LayerNorm eps 1e-5 with the biased variance; exact erf GELU; RoPE
@@ -27,6 +30,10 @@ base 10000 with rotate-half pairs (j, j + head_dim/2), applied to q and k after 
 positions restarting at 0 at each sequence start; scores scaled by 1/sqrt(head_dim);
 no dropout; an optional final LayerNorm; embedding scale 1.  The FP8 workload states that
 attention stays in bf16: its oracle rounds the attention operands q, k, v to bfloat16.
+Masked-LM head (silent on the pages): the ESM-2 head of that model family, dense d -> d with
+bias, exact GELU, LayerNorm, then logits against the (tied) token embedding plus a vocabulary
+bias; the loss is the mean cross-entropy over the masked positions (target -100 = not
+scored), and perplexity is exp of that mean.
 
 Parity pins: every function here is checked in tests/test_oracle_pins.py against closed
 forms, invariants, brute force or an independent library formulation.  The only part with
@@ -256,3 +263,29 @@ def encode_padded(token_ids: np.ndarray, seq_lens: Sequence[int], weights: Dict,
         full[:L] = encode_sequence(token_ids[b, :L], weights, heads, final_ln, **kw)
         out[b] = full
     return out
+
+
+# --------------------------------------------------------------------------- masked-LM head
+IGNORE_INDEX = -100
+
+
+def lm_head(h: np.ndarray, w: Dict[str, np.ndarray]) -> np.ndarray:
+    """Logits [T, vocab] of final hidden states h [T, d]: dense + GELU, LayerNorm, then the
+    tied embedding as the output projection plus the vocabulary bias."""
+    h = np.asarray(h, np.float64)
+    z = gelu(h @ np.asarray(w["dense_w"], np.float64).T + np.asarray(w["dense_b"], np.float64))
+    z = layer_norm(z, np.asarray(w["ln_g"], np.float64), np.asarray(w["ln_b"], np.float64))
+    return z @ np.asarray(w["emb"], np.float64).T + np.asarray(w["bias"], np.float64)
+
+
+def masked_lm_loss(logits: np.ndarray, targets: Sequence[int]):
+    """Per-token cross-entropy log(sum_v exp(l_v)) - l_target (0 where target == -100), the
+    sum over scored tokens and their count."""
+    logits = np.asarray(logits, np.float64)
+    t = np.asarray(targets, np.int64)
+    m = logits.max(axis=1)
+    lse = m + np.log(np.exp(logits - m[:, None]).sum(axis=1))
+    scored = t != IGNORE_INDEX
+    per = np.zeros(len(t))
+    per[scored] = lse[scored] - logits[np.nonzero(scored)[0], t[scored]]
+    return per, float(per.sum()), int(scored.sum())

@@ -458,3 +458,58 @@ def test_geometry_golden():
         # the encoder layout reproduces the nominal size within 10%
         assert abs(n / G["nominal_params"] - 1) < 0.1, n
     assert gold["max_residues"] + 2 <= synth.ESM2_650M.max_positions
+
+
+# --------------------------------------------------------------------------- masked-LM head
+def _lm_weights(d=48, V=33, seed=5):
+    r = np.random.default_rng(seed)
+    return {"dense_w": r.standard_normal((d, d)) * 0.2, "dense_b": r.standard_normal(d) * 0.1,
+            "ln_g": 1 + 0.1 * r.standard_normal(d), "ln_b": 0.1 * r.standard_normal(d),
+            "emb": r.standard_normal((V, d)) * 0.3, "bias": r.standard_normal(V) * 0.1}
+
+
+def test_lm_head_zero_dense_gives_embedding_of_ln_bias():
+    """dense = 0: GELU(0) = 0, LayerNorm of a constant row is beta, so every token's logits
+    are emb . beta + bias."""
+    w = _lm_weights()
+    w["dense_w"][:] = 0
+    w["dense_b"][:] = 0
+    h = np.random.default_rng(1).standard_normal((7, 48))
+    got = O.lm_head(h, w)
+    want = w["emb"] @ w["ln_b"] + w["bias"]
+    assert np.allclose(got, np.broadcast_to(want, got.shape), atol=1e-12)
+
+
+def test_lm_head_vs_torch_formulation():
+    w = _lm_weights()
+    h = np.random.default_rng(2).standard_normal((9, 48))
+    th = torch.from_numpy(h)
+    z = F.gelu(F.linear(th, torch.from_numpy(w["dense_w"]), torch.from_numpy(w["dense_b"])))
+    z = F.layer_norm(z, (48,), torch.from_numpy(w["ln_g"]), torch.from_numpy(w["ln_b"]), eps=1e-5)
+    ref = F.linear(z, torch.from_numpy(w["emb"]), torch.from_numpy(w["bias"])).numpy()
+    assert np.allclose(O.lm_head(h, w), ref, atol=1e-12, rtol=1e-12)
+
+
+def test_masked_lm_loss_bruteforce_and_invariants():
+    r = np.random.default_rng(3)
+    logits = r.standard_normal((6, 33)) * 4
+    targets = [0, 5, O.IGNORE_INDEX, 32, 7, O.IGNORE_INDEX]
+    per, total, n = O.masked_lm_loss(logits, targets)
+    for i, t in enumerate(targets):  # plain loops with math.exp / math.log
+        if t == O.IGNORE_INDEX:
+            assert per[i] == 0.0
+            continue
+        z = sum(math.exp(v) for v in logits[i])
+        assert abs(per[i] - (math.log(z) - logits[i, t])) < 1e-12
+    assert n == 4 and abs(total - per.sum()) < 1e-12
+    # shift invariance, uniform logits -> log(V), a dominant target logit -> ~0
+    per2, _, _ = O.masked_lm_loss(logits + 123.0, targets)
+    assert np.allclose(per2, per, atol=1e-9)
+    perU, totU, _ = O.masked_lm_loss(np.zeros((3, 33)), [1, 2, 3])
+    assert np.allclose(perU, math.log(33)) and abs(totU - 3 * math.log(33)) < 1e-12
+    big = np.zeros((1, 33))
+    big[0, 4] = 60.0
+    assert O.masked_lm_loss(big, [4])[1] < 1e-20
+    # torch cross_entropy with ignore_index, summed
+    ref = F.cross_entropy(torch.from_numpy(logits), torch.tensor(targets), ignore_index=-100, reduction="sum")
+    assert abs(total - float(ref)) < 1e-10

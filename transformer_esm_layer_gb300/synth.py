@@ -210,6 +210,27 @@ def model_weights(g: Geometry, seed: int, precision: str, ln_random: bool = Fals
     return {"emb": emb, "layers": layers, "lnf_g": rnd(lnf_g), "lnf_b": rnd(lnf_b)}
 
 
+def lm_head_weights(g: Geometry, seed: int, precision: str, emb: np.ndarray, ln_random: bool = True) -> Dict:
+    """Masked-LM head weights: dense [d, d] and bias [d] ~ N(0, 0.02), LayerNorm gamma / beta
+    (random around 1 / 0 with ``ln_random``), the vocabulary bias [V] ~ N(0, 0.02), and the
+    output projection tied to the given token embedding [V, d]."""
+    d = g.hidden
+    rnd = (lambda a: bf16_bits_to_f32(f32_to_bf16_bits(a))) if precision in ("bf16", "fp8") else (lambda a: a)
+    ln_g = (1.0 + _normal([seed, 20_000, 2], (d,), 0.1)) if ln_random else np.ones(d, np.float32)
+    ln_b = _normal([seed, 20_000, 3], (d,), 0.1) if ln_random else np.zeros(d, np.float32)
+    return {"dense_w": rnd(_normal([seed, 20_000, 0], (d, d))), "dense_b": rnd(_normal([seed, 20_000, 1], (d,))),
+            "ln_g": rnd(ln_g), "ln_b": rnd(ln_b), "emb": emb,
+            "bias": rnd(_normal([seed, 20_000, 4], (g.vocab,)))}
+
+
+def mlm_targets(tokens: np.ndarray, seed: int, rate: float = 0.15) -> np.ndarray:
+    """Masked-LM targets for a token batch: each position is scored with probability
+    ``rate`` (target = its token id), otherwise -100 (not scored)."""
+    rng = np.random.default_rng([seed, 30_000])
+    pick = rng.random(len(tokens)) < rate
+    return np.where(pick, np.asarray(tokens, np.int64), -100).astype(np.int32)
+
+
 def random_lengths_case(seed: int, count: int, lo: int, hi: int) -> List[int]:
     """Uniform integer lengths in [lo, hi] for parity cases with ragged tiles."""
     rng = np.random.default_rng([seed, 77])
