@@ -169,6 +169,44 @@ ESM_API esm_status esm_encoder_forward_padded(esm_encoder_t* h, const esm_weight
                                       int S, void* hidden_out, void* workspace,
                                       size_t workspace_bytes, esm_stream_t stream);
 
+/* ---- masked-LM head (the step after the encoder) ----
+ * The mlqm.cn walkthrough loads the model as AutoModelForMaskedLM and the BioNeMo ESM-2
+ * model card (accuracy benchmark) scores it by masked-LM perplexity; the pages do not list
+ * the head's layers.  Reading: the ESM-2 head of that model family,
+ *   z = LN(GELU(h Wd^T + bd); ln_g, ln_b);  logits = z E^T + b_vocab,
+ * with E the token embedding [vocab, hidden] (tied), and the loss per scored token
+ * log(sum_v exp(logits_v)) - logits_target.
+ * Pointers are device pointers in the handle's parameter dtype (bf16, or float32 for
+ * ESM_FP32): dense_w [hidden, hidden] ([out, in]), dense_b, ln_g, ln_b [hidden],
+ * emb [vocab, hidden], bias [vocab]; 16-byte aligned. */
+typedef struct {
+  const void* dense_w;
+  const void* dense_b;
+  const void* ln_g;
+  const void* ln_b;
+  const void* emb;
+  const void* bias;
+} esm_lm_head;
+
+/* Workspace bytes esm_encoder_lm_head needs for total_tokens tokens (two [T, hidden]
+ * activation buffers and a [T] float32 scratch). */
+ESM_API esm_status esm_encoder_lm_head_workspace_size(const esm_encoder_t* h, int total_tokens, size_t* bytes);
+
+/* Logits and masked cross-entropy of final hidden states.  hidden: device [T, hidden] in
+ * the activation dtype (bf16; float32 for ESM_FP32), e.g. the output of
+ * esm_encoder_forward.  targets: device int32 [T] with a token id in [0, vocab) for
+ * scored positions and -100 elsewhere, or NULL (nothing scored).  Outputs (each may be
+ * NULL): logits device float32 [T, vocab]; token_loss device float32 [T] (0 where not
+ * scored); loss_sum device float32 scalar and count device int32 scalar (sum and number
+ * of scored tokens, reduced in a fixed order: perplexity = exp(loss_sum / count)).
+ * ESM_ERR_UNSUPPORTED when vocab > 64, the embedding does not fit shared memory (vocab x
+ * hidden x element > 200 KB) or (bf16) hidden % 256 != 0.  A target outside [0, vocab)
+ * and != -100 is not scored and latches ESM_ERR_TOKEN_RANGE (see esm_encoder_check). */
+ESM_API esm_status esm_encoder_lm_head(esm_encoder_t* h, const esm_lm_head* head, const void* hidden,
+                                       int total_tokens, const int32_t* targets, float* logits,
+                                       float* token_loss, float* loss_sum, int* count, void* workspace,
+                                       size_t workspace_bytes, esm_stream_t stream);
+
 /* Synchronise `stream` and return (and clear) the first error the kernels latched
  * since the last check: ESM_ERR_BAD_CU_SEQLENS, ESM_ERR_TOKEN_RANGE, ESM_ERR_TIMEOUT
  * or ESM_OK. */

@@ -575,3 +575,84 @@ def test_bounded_wait_times_out_and_context_stays_usable():
     out = enc.forward(dw, tok, cu, 5)
     enc.check()
     assert torch.isfinite(out.float()).all()
+
+
+# --------------------------------------------------------------------------- masked-LM head
+def _lm_case(g, precision, seed, T):
+    w = synth.model_weights(g, seed, precision, num_layers=1)
+    head = synth.lm_head_weights(g, seed, precision, w["emb"])
+    rng = np.random.default_rng(seed)
+    h = rng.standard_normal((T, g.hidden)).astype(np.float32)
+    if precision != "fp32":
+        h = _bf16(h)
+    tokens = rng.integers(0, g.vocab, size=T).astype(np.int32)
+    targets = synth.mlm_targets(tokens, seed)
+    return head, h, targets
+
+
+@pytest.mark.parametrize("precision,g,T,tol", [("bf16", synth.ESM2_650M, 1000, 1e-2), ("bf16", SMALL, 333, 1e-2),
+                                               ("fp32", synth.TINY, 77, 1e-5)])
+def test_lm_head_logits_and_loss(precision, g, T, tol):
+    """Logits (relative L2) and masked cross-entropy against the float64 oracle; the scored
+    count is exact.  bf16: the dense output and the LayerNorm output are rounded to bf16
+    (~2^-9 relative each), so logits agree to ~1e-2."""
+    from transformer_esm_layer_gb300.binding import DeviceLmHead
+    enc = _enc(g, precision)
+    head, h, targets = _lm_case(g, precision, 21, T)
+    dh = DeviceLmHead(head, precision)
+    dt = torch.float32 if precision == "fp32" else torch.bfloat16
+    hid = _dev(h, dt)
+    tg = torch.from_numpy(targets).cuda()
+    logits = torch.empty(T, g.vocab, dtype=torch.float32, device="cuda")
+    tl = torch.empty(T, dtype=torch.float32, device="cuda")
+    ls = torch.zeros(1, dtype=torch.float32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    enc.lm_head(dh, hid, targets=tg, logits=logits, token_loss=tl, loss_sum=ls, count=cnt)
+    assert enc.check_status() == 0
+    ref = O.lm_head(h.astype(np.float64), head)
+    per, total, n = O.masked_lm_loss(ref, targets)
+    assert rel_l2(to_np(logits), ref) < tol
+    assert int(cnt.item()) == n
+    got_per = to_np(tl)
+    assert np.all(got_per[targets == -100] == 0.0)
+    assert abs(float(ls.item()) - total) <= tol * total + 1e-6
+    assert abs(float(ls.item()) - float(np.sum(got_per, dtype=np.float64))) <= 1e-3 * max(1.0, total)
+
+
+def test_lm_head_after_encoder_forward_and_bad_target():
+    """The head on the encoder's own output (2 layers, ragged sequences) against the oracle
+    encode + head; a target outside the vocabulary is not scored and latches
+    ESM_ERR_TOKEN_RANGE; the loss sum is bitwise reproducible."""
+    from transformer_esm_layer_gb300.binding import DeviceLmHead, DeviceWeights, packed_inputs
+    g = SMALL
+    enc = _enc(g, "bf16")
+    w = synth.model_weights(g, 4, "bf16", ln_random=True)
+    head = synth.lm_head_weights(g, 4, "bf16", w["emb"])
+    lengths = [5, 130, 1, 77]
+    tokens = synth.tokens_for_lengths(np.random.default_rng(4), lengths)
+    tok, cu = packed_inputs(tokens, lengths)
+    T = len(tokens)
+    dw = DeviceWeights(w, "bf16")
+    out = torch.empty(T, g.hidden, dtype=torch.bfloat16, device="cuda")
+    enc.forward(dw, tok, cu, max(lengths), out)
+    targets = synth.mlm_targets(tokens, 9, rate=0.5)
+    tg = torch.from_numpy(targets).cuda()
+    dh = DeviceLmHead(head, "bf16")
+    logits = torch.empty(T, g.vocab, dtype=torch.float32, device="cuda")
+    ls = torch.zeros(1, dtype=torch.float32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    enc.lm_head(dh, out, targets=tg, logits=logits, loss_sum=ls, count=cnt)
+    assert enc.check_status() == 0
+    hid = O.encode_packed(tokens, O.cu_seqlens(lengths), w, g.heads)
+    hid = np.concatenate([hid[i] for i in range(len(lengths))])
+    ref = O.lm_head(hid, head)
+    assert rel_l2(to_np(logits), ref) < 2e-2
+    _, total, n = O.masked_lm_loss(ref, targets)
+    assert int(cnt.item()) == n and abs(float(ls.item()) - total) < 2e-2 * total
+    first = float(ls.item())
+    enc.lm_head(dh, out, targets=tg, loss_sum=ls, count=cnt)
+    assert float(ls.item()) == first
+    bad = targets.copy()
+    bad[0] = 40
+    enc.lm_head(dh, out, targets=torch.from_numpy(bad).cuda(), loss_sum=ls, count=cnt)
+    assert enc.check_status() == 4  # ESM_ERR_TOKEN_RANGE

@@ -27,7 +27,7 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_encoder_debug_pack_index", "esm_op_layernorm", "esm_op_gemm", "esm_op_attention",
            "esm_encoder_get_fp8_state", "esm_encoder_set_fp8_state", "esm_encoder_set_profiling",
            "esm_encoder_get_profile", "esm_op_attention_noalloc", "esm_op_layernorm_e4m3", "esm_op_gemm_fp8",
-           "esm_encoder_debug_wait_timeout",
+           "esm_encoder_debug_wait_timeout", "esm_encoder_lm_head_workspace_size", "esm_encoder_lm_head",
            "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
 
@@ -59,6 +59,10 @@ class EsmWeights(ctypes.Structure):
         [("lnf_g", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p)]
 
 
+class EsmLmHead(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias")]
+
+
 _lib = None
 
 
@@ -79,6 +83,8 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_forward_host": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, i32, vp, vp, sz, vp]),
         "esm_encoder_forward_padded": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, vp, vp, sz, vp]),
         "esm_encoder_check": (i32, [vp, vp]),
+        "esm_encoder_lm_head_workspace_size": (i32, [vp, i32, ctypes.POINTER(sz)]),
+        "esm_encoder_lm_head": (i32, [vp, ctypes.POINTER(EsmLmHead), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "esm_encoder_debug_pack_index": (i32, [vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]),
         "esm_op_layernorm": (i32, [vp, vp, vp, vp, vp, i32, i32, vp]),
         "esm_op_gemm": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
@@ -136,6 +142,18 @@ class DeviceWeights:
         st.lnf_g = self.lnf_g.data_ptr()
         st.lnf_b = self.lnf_b.data_ptr()
         self.struct = st
+
+
+class DeviceLmHead:
+    """Masked-LM head weights on the device (handle's parameter dtype) plus the esm_lm_head
+    struct; ``w`` is the dict of synth.lm_head_weights (its "emb" is the tied embedding)."""
+
+    def __init__(self, w: Dict, precision: str, device="cuda"):
+        import torch
+        dt = torch.float32 if precision == "fp32" else torch.bfloat16
+        to = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device=device, dtype=dt)
+        self.t = {k: to(w[k]) for k in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias")}
+        self.struct = EsmLmHead(*[self.t[k].data_ptr() for k in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias")])
 
 
 class EsmEncoder:
@@ -301,6 +319,25 @@ class EsmEncoder:
                                               _ptr(o), _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
                     "esm_op_attention")
         return o
+
+    def lm_head_workspace(self, T: int, device="cuda"):
+        import torch
+        n = ctypes.c_size_t()
+        self._raise(self.lib.esm_encoder_lm_head_workspace_size(self.handle, T, ctypes.byref(n)),
+                    "esm_encoder_lm_head_workspace_size")
+        return torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=device)
+
+    def lm_head(self, head: "DeviceLmHead", hidden, targets=None, logits=None, token_loss=None, loss_sum=None,
+                count=None, workspace=None, stream=None):
+        """esm_encoder_lm_head: logits [T, vocab] / per-token masked cross-entropy / its sum and
+        the number of scored tokens, into the given device tensors (any may be None)."""
+        T = hidden.shape[0]
+        if workspace is None:
+            workspace = self.lm_head_workspace(T, hidden.device)
+        self._raise(self.lib.esm_encoder_lm_head(self.handle, ctypes.byref(head.struct), _ptr(hidden), T, _ptr(targets),
+                                                 _ptr(logits), _ptr(token_loss), _ptr(loss_sum), _ptr(count),
+                                                 _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+                    "esm_encoder_lm_head")
 
     def set_profiling(self, enable: bool):
         self._raise(self.lib.esm_encoder_set_profiling(self.handle, int(enable)), "esm_encoder_set_profiling")

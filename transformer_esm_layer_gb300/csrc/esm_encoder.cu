@@ -474,6 +474,60 @@ esm_status esm_encoder_forward(esm_encoder_t* h, const esm_weights* w, const int
                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+static size_t lm_head_bytes(const esm_encoder* h, int T, size_t* off_z2, size_t* off_loss) {
+  const size_t es = h->cfg.precision == ESM_FP32 ? 4 : 2;
+  const size_t act = ((size_t)T * h->cfg.hidden * es + 255) & ~size_t(255);
+  *off_z2 = act;
+  *off_loss = 2 * act;
+  return 2 * act + (((size_t)T * 4 + 255) & ~size_t(255));
+}
+
+esm_status esm_encoder_lm_head_workspace_size(const esm_encoder_t* h, int total_tokens, size_t* bytes) {
+  if (!h || !bytes || total_tokens < 0) return ESM_ERR_INVALID_ARG;
+  size_t a, b;
+  *bytes = lm_head_bytes(h, total_tokens, &a, &b);
+  return ESM_OK;
+}
+
+esm_status esm_encoder_lm_head(esm_encoder_t* h, const esm_lm_head* head, const void* hidden, int total_tokens,
+                               const int32_t* targets, float* logits, float* token_loss, float* loss_sum, int* count,
+                               void* workspace, size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || !head || total_tokens < 0) return ESM_ERR_INVALID_ARG;
+  const void* p[6] = {head->dense_w, head->dense_b, head->ln_g, head->ln_b, head->emb, head->bias};
+  for (const void* q : p)
+    if (!q || !aligned(q, 16)) return ESM_ERR_INVALID_ARG;
+  const bool bf16 = h->bf16_params();
+  const int d = h->cfg.hidden, V = h->cfg.vocab, T = total_tokens;
+  if (!lm_logits_supported(V, d, bf16) || (bf16 && d % 256)) return ESM_ERR_UNSUPPORTED;
+  size_t off_z2, off_loss;
+  const size_t need = lm_head_bytes(h, T, &off_z2, &off_loss);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (loss_sum || count)
+      return cuda_status(launch_lm_logits(nullptr, bf16, head->emb, head->bias, 0, d, V, nullptr, nullptr, nullptr,
+                                          loss_sum, count, h->num_sms, h->d_err, st));
+    return ESM_OK;
+  }
+  if (!hidden || !aligned(hidden, 16) || (logits && !aligned(logits, 4))) return ESM_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ESM_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* z1 = ws;
+  void* z2 = ws + off_z2;
+  float* tl = token_loss ? token_loss : reinterpret_cast<float*>(ws + off_loss);
+  // dense + exact GELU on the encoder's GEMM (tensor cores for bf16), then LayerNorm
+  esm_status s = run_gemm(h, P_OTHER, ESM_EPI_GELU, hidden, head->dense_w, head->dense_b, z1, nullptr, T, d, d, false,
+                          h->act(), nullptr, nullptr, nullptr, nullptr, st);
+  if (s != ESM_OK) return s;
+  if (bf16)
+    launch_layernorm_bf16in(z1, head->ln_g, head->ln_b, false, z2, Act::BF16, T, d, h->cfg.ln_eps, st);
+  else
+    launch_layernorm(static_cast<const float*>(z1), head->ln_g, head->ln_b, true, z2, Act::F32, T, d, h->cfg.ln_eps,
+                     nullptr, nullptr, nullptr, nullptr, nullptr, st);
+  const bool want_loss = token_loss || loss_sum || count;
+  return cuda_status(launch_lm_logits(z2, bf16, head->emb, head->bias, T, d, V, targets, logits,
+                                      want_loss ? tl : nullptr, loss_sum, count, h->num_sms, h->d_err, st));
+}
+
 esm_status esm_encoder_forward_host(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids_host,
                                     const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int max_seqlen,
                                     void* hidden_out_host, void* workspace, size_t workspace_bytes,

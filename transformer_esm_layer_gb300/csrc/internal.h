@@ -51,6 +51,16 @@ void launch_layernorm(const float* x, const void* g, const void* b, bool param_f
                       const int32_t* valid_pos, const int32_t* valid_seg, const int32_t* valid_klen,
                       cudaStream_t st);
 // out = x (converted), zeroing invalid rows the same way (final_ln == 0).
+// LayerNorm of a bfloat16 input (same arithmetic; no FP8 output, no validity mask).
+void launch_layernorm_bf16in(const void* x, const void* g, const void* b, bool param_f32, void* y, Act out, int rows,
+                             int cols, float eps, cudaStream_t st);
+// Masked-LM head output stage (lm_head.cu): logits against the tied embedding, per-token
+// masked cross-entropy, and its deterministic sum / scored count.
+size_t lm_logits_smem_bytes(int vocab, int hidden, bool bf16);
+bool lm_logits_supported(int vocab, int hidden, bool bf16);
+cudaError_t launch_lm_logits(const void* z, bool bf16, const void* emb, const void* bias, int T, int d, int V,
+                             const int32_t* targets, float* logits, float* token_loss, float* loss_sum, int* count,
+                             int num_sms, unsigned* err, cudaStream_t st);
 void launch_copy_out(const float* x, void* out, Act out_t, int rows, int cols, const int32_t* valid_pos,
                      const int32_t* valid_seg, const int32_t* valid_klen, cudaStream_t st);
 

@@ -32,8 +32,10 @@ __device__ __forceinline__ bool row_valid(int row, const int32_t* vp, const int3
   return vp[row] < vk[vs[row]];
 }
 
-template <int N4, Act OUT>
-__global__ void layernorm_kernel(const float* __restrict__ x, const void* __restrict__ g, const void* __restrict__ b,
+// x is float32 (the residual stream) or bfloat16 (IN_BF16: an activation, e.g. the masked-LM
+// head's dense output).
+template <int N4, Act OUT, bool IN_BF16>
+__global__ void layernorm_kernel(const void* __restrict__ x, const void* __restrict__ g, const void* __restrict__ b,
                                  bool param_f32, void* __restrict__ y, int rows, int cols, float eps,
                                  const float* q_scale, float* amax_out, const int32_t* vp, const int32_t* vs,
                                  const int32_t* vk) {
@@ -41,14 +43,19 @@ __global__ void layernorm_kernel(const float* __restrict__ x, const void* __rest
   const int row = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * cols);
   const int n4 = cols >> 2;
   float4 v[N4];
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < N4; ++i) {
     const int c = i * 32 + lane;
-    v[i] = c < n4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (IN_BF16) {
+      v[i] = c < n4 ? load_param4(static_cast<const __nv_bfloat16*>(x) + (size_t)row * cols, 4 * c, false)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const float4* xr = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)row * cols);
+      v[i] = c < n4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
   }
   const float mean = warp_sum(s) / (float)cols;
@@ -117,18 +124,35 @@ __global__ void copy_out_kernel(const float* __restrict__ x, void* __restrict__ 
   }
 }
 
-template <int N4>
-void ln_dispatch_out(const float* x, const void* g, const void* b, bool pf32, void* y, Act out, int rows, int cols,
+template <int N4, bool IN_BF16>
+void ln_dispatch_out(const void* x, const void* g, const void* b, bool pf32, void* y, Act out, int rows, int cols,
                      float eps, const float* qs, float* amax, const int32_t* vp, const int32_t* vs, const int32_t* vk,
                      cudaStream_t st) {
   const int warps = 8;
   const int grid = (rows + warps - 1) / warps;
   if (out == Act::F32)
-    layernorm_kernel<N4, Act::F32><<<grid, 32 * warps, 0, st>>>(x, g, b, pf32, y, rows, cols, eps, qs, amax, vp, vs, vk);
+    layernorm_kernel<N4, Act::F32, IN_BF16>
+        <<<grid, 32 * warps, 0, st>>>(x, g, b, pf32, y, rows, cols, eps, qs, amax, vp, vs, vk);
   else if (out == Act::BF16)
-    layernorm_kernel<N4, Act::BF16><<<grid, 32 * warps, 0, st>>>(x, g, b, pf32, y, rows, cols, eps, qs, amax, vp, vs, vk);
+    layernorm_kernel<N4, Act::BF16, IN_BF16>
+        <<<grid, 32 * warps, 0, st>>>(x, g, b, pf32, y, rows, cols, eps, qs, amax, vp, vs, vk);
   else
-    layernorm_kernel<N4, Act::E4M3><<<grid, 32 * warps, 0, st>>>(x, g, b, pf32, y, rows, cols, eps, qs, amax, vp, vs, vk);
+    layernorm_kernel<N4, Act::E4M3, IN_BF16>
+        <<<grid, 32 * warps, 0, st>>>(x, g, b, pf32, y, rows, cols, eps, qs, amax, vp, vs, vk);
+}
+
+template <bool IN_BF16>
+void ln_dispatch(const void* x, const void* g, const void* b, bool pf32, void* y, Act out, int rows, int cols,
+                 float eps, const float* qs, float* amax, const int32_t* vp, const int32_t* vs, const int32_t* vk,
+                 cudaStream_t st) {
+  const int n4 = (cols / 4 + 31) / 32;  // float4 per lane
+  if (n4 <= 1) ln_dispatch_out<1, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
+  else if (n4 <= 2) ln_dispatch_out<2, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
+  else if (n4 <= 4) ln_dispatch_out<4, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
+  else if (n4 <= 8) ln_dispatch_out<8, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
+  else if (n4 <= 10) ln_dispatch_out<10, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
+  else if (n4 <= 20) ln_dispatch_out<20, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
+  else ln_dispatch_out<32, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
 }
 
 }  // namespace
@@ -137,14 +161,13 @@ void launch_layernorm(const float* x, const void* g, const void* b, bool param_f
                       int cols, float eps, const float* q_scale, float* amax, const int32_t* vp, const int32_t* vs,
                       const int32_t* vk, cudaStream_t st) {
   if (rows <= 0) return;
-  const int n4 = (cols / 4 + 31) / 32;  // float4 per lane
-  if (n4 <= 1) ln_dispatch_out<1>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
-  else if (n4 <= 2) ln_dispatch_out<2>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
-  else if (n4 <= 4) ln_dispatch_out<4>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
-  else if (n4 <= 8) ln_dispatch_out<8>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
-  else if (n4 <= 10) ln_dispatch_out<10>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
-  else if (n4 <= 20) ln_dispatch_out<20>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
-  else ln_dispatch_out<32>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
+  ln_dispatch<false>(x, g, b, param_f32, y, out, rows, cols, eps, q_scale, amax, vp, vs, vk, st);
+}
+
+void launch_layernorm_bf16in(const void* x, const void* g, const void* b, bool param_f32, void* y, Act out, int rows,
+                             int cols, float eps, cudaStream_t st) {
+  if (rows <= 0) return;
+  ln_dispatch<true>(x, g, b, param_f32, y, out, rows, cols, eps, nullptr, nullptr, nullptr, nullptr, nullptr, st);
 }
 
 void launch_copy_out(const float* x, void* out, Act out_t, int rows, int cols, const int32_t* vp, const int32_t* vs,

@@ -1,0 +1,193 @@
+// Masked-LM head output stage: logits against the tied token embedding and the masked
+// cross-entropy (the head the mlqm.cn walkthrough loads as AutoModelForMaskedLM; the BioNeMo
+// ESM-2 model card scores it by perplexity).  The dense + GELU and the LayerNorm before it
+// run on the encoder's own GEMM and LayerNorm kernels.
+//
+//   logits[t, v] = z[t] . emb[v] + bias[v]
+//   loss[t]      = log(sum_v exp(logits[t, v])) - logits[t, target[t]]   (0 if target = -100)
+//
+// One warp per token, persistent grid; the whole embedding (vocab x hidden) sits in shared
+// memory.  Lane l holds the 16-byte units l, l + 32, ... of the token's row; each logit is a
+// warp-wide sum, kept by lane v % 32.  The loss sum is a separate one-block reduction in a
+// fixed order, so it is bitwise reproducible.
+#include "common.cuh"
+#include "internal.h"
+
+namespace esm {
+namespace {
+
+constexpr int kIgnore = -100;
+
+__device__ __forceinline__ float warp_sum_all(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max_all(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// 16-byte unit of a row: 8 bf16 or 4 fp32 values
+template <bool BF16>
+__device__ __forceinline__ void unpack(const uint4& u, float* f) {
+  if constexpr (BF16) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 p = __bfloat1622float2(h[k]);
+      f[2 * k] = p.x;
+      f[2 * k + 1] = p.y;
+    }
+  } else {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+}
+
+// NU: 16-byte units of the row per lane (the row has d * es / 16 units, lane l holds units
+// l, l + 32, ...).
+template <bool BF16, int NU>
+__global__ void __launch_bounds__(256) lm_logits_kernel(const void* __restrict__ z, const void* __restrict__ emb,
+                                                        const void* __restrict__ bias, int T, int d, int V,
+                                                        const int32_t* __restrict__ targets, float* logits,
+                                                        float* token_loss, unsigned* err) {
+  extern __shared__ __align__(16) uint8_t smem_e[];
+  constexpr int kPer = BF16 ? 8 : 4;  // values per 16-byte unit
+  const int units = d / kPer;         // per row
+  {  // the embedding table into shared memory, 16 bytes per thread
+    const uint4* src = static_cast<const uint4*>(emb);
+    uint4* dst = reinterpret_cast<uint4*>(smem_e);
+    const int n16 = V * units;
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldg(src + i);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  auto bias_at = [&](int v) -> float {
+    return BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(bias)[v]) : static_cast<const float*>(bias)[v];
+  };
+  const float b_lo = lane < V ? bias_at(lane) : 0.f;
+  const float b_hi = lane + 32 < V ? bias_at(lane + 32) : 0.f;
+  const uint4* e16 = reinterpret_cast<const uint4*>(smem_e);
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
+    const uint4* z16 = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(z) + (size_t)t * units * 16);
+    uint4 row[NU];
+#pragma unroll
+    for (int i = 0; i < NU; ++i) {
+      const int c = i * 32 + lane;
+      row[i] = c < units ? __ldg(z16 + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float lo = -INFINITY, hi = -INFINITY;  // logits v = lane and v = lane + 32
+    for (int v = 0; v < V; ++v) {
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < NU; ++i) {
+        const int c = i * 32 + lane;
+        if (c < units) {
+          float a[kPer], e[kPer];
+          unpack<BF16>(row[i], a);
+          unpack<BF16>(e16[v * units + c], e);
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) acc = fmaf(a[k], e[k], acc);
+        }
+      }
+      acc = warp_sum_all(acc);
+      if (v == lane) lo = acc + b_lo;
+      if (v == lane + 32) hi = acc + b_hi;
+    }
+    if (logits) {
+      if (lane < V) logits[(size_t)t * V + lane] = lo;
+      if (lane + 32 < V) logits[(size_t)t * V + lane + 32] = hi;
+    }
+    if (token_loss) {
+      const float m = warp_max_all(fmaxf(lo, hi));
+      const float se = warp_sum_all((lane < V ? expf(lo - m) : 0.f) + (lane + 32 < V ? expf(hi - m) : 0.f));
+      int tg = targets ? targets[t] : kIgnore;
+      if (tg != kIgnore && (tg < 0 || tg >= V)) {
+        if (lane == 0) latch_error(err, ERRBIT_TOKEN);
+        tg = kIgnore;
+      }
+      const int src = tg == kIgnore ? 0 : (tg & 31);
+      const float l_src = __shfl_sync(0xffffffffu, tg >= 32 ? hi : lo, src);
+      if (lane == 0) token_loss[t] = tg == kIgnore ? 0.f : (m + logf(se)) - l_src;
+    }
+  }
+}
+
+// Sum of the per-token losses and count of scored tokens: one block, fixed order.
+__global__ void __launch_bounds__(1024) loss_reduce_kernel(const float* __restrict__ token_loss,
+                                                           const int32_t* __restrict__ targets, int T, float* loss_sum,
+                                                           int* count) {
+  __shared__ float ss[1024];
+  __shared__ int sc[1024];
+  float s = 0.f;
+  int n = 0;
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    s += token_loss[i];
+    n += (targets && targets[i] != kIgnore) ? 1 : 0;
+  }
+  ss[threadIdx.x] = s;
+  sc[threadIdx.x] = n;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) {
+      ss[threadIdx.x] += ss[threadIdx.x + w];
+      sc[threadIdx.x] += sc[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (loss_sum) *loss_sum = ss[0];
+    if (count) *count = sc[0];
+  }
+}
+
+}  // namespace
+
+size_t lm_logits_smem_bytes(int vocab, int hidden, bool bf16) { return (size_t)vocab * hidden * (bf16 ? 2 : 4); }
+
+template <bool BF16, int NU>
+void launch_nu(int grid, size_t smem, const void* z, const void* emb, const void* bias, int T, int d, int V,
+               const int32_t* targets, float* logits, float* token_loss, unsigned* err, cudaStream_t st) {
+  cudaFuncSetAttribute(lm_logits_kernel<BF16, NU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  lm_logits_kernel<BF16, NU><<<grid, 256, smem, st>>>(z, emb, bias, T, d, V, targets, logits, token_loss, err);
+}
+
+// false when the table does not fit shared memory or the row is too long for the register plan
+bool lm_logits_supported(int vocab, int hidden, bool bf16) {
+  const int per = bf16 ? 8 : 4;
+  return vocab >= 1 && vocab <= 64 && hidden % per == 0 && hidden / per <= 16 * 32 &&
+         lm_logits_smem_bytes(vocab, hidden, bf16) <= 200 * 1024;
+}
+
+cudaError_t launch_lm_logits(const void* z, bool bf16, const void* emb, const void* bias, int T, int d, int V,
+                             const int32_t* targets, float* logits, float* token_loss, float* loss_sum, int* count,
+                             int num_sms, unsigned* err, cudaStream_t st) {
+  const size_t smem = lm_logits_smem_bytes(V, d, bf16);
+  if (T > 0) {
+    const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+    int grid = num_sms * per_sm;
+    const int need = (T + 7) / 8;
+    if (grid > need) grid = need;
+    const int units = d / (bf16 ? 8 : 4);
+    const int nu = (units + 31) / 32;
+    if (bf16) {
+      if (nu <= 1) launch_nu<true, 1>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else if (nu <= 2) launch_nu<true, 2>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else if (nu <= 4) launch_nu<true, 4>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else if (nu <= 8) launch_nu<true, 8>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else launch_nu<true, 16>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+    } else {
+      if (nu <= 1) launch_nu<false, 1>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else if (nu <= 2) launch_nu<false, 2>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else if (nu <= 4) launch_nu<false, 4>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else if (nu <= 8) launch_nu<false, 8>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+      else launch_nu<false, 16>(grid, smem, z, emb, bias, T, d, V, targets, logits, token_loss, err, st);
+    }
+  }
+  if (loss_sum || count) loss_reduce_kernel<<<1, 1024, 0, st>>>(token_loss, targets, T, loss_sum, count);
+  return cudaGetLastError();
+}
+
+}  // namespace esm
