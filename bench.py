@@ -398,6 +398,32 @@ def run_ours(args):
                "d2h_bytes_per_step": 2 * T * g.hidden, "ms_per_step": dt * 1e3,
                "call": "esm_encoder_forward_host (pinned host buffers in and out)"}
 
+    # ---------------------------------------------------------------- masked-LM head (next step)
+    mlm = None
+    if not padded and prec == "bf16":
+        from transformer_esm_layer_gb300.binding import DeviceLmHead
+        head = DeviceLmHead(synth.lm_head_weights(g, wl.seed, prec, w_np["emb"]), prec, device=dev)
+        tg = torch.from_numpy(synth.mlm_targets(tok_np, wl.seed)).to(dev)
+        hws = enc.lm_head_workspace(T, dev)
+        lsum = torch.zeros(1, dtype=torch.float32, device=dev)
+        cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+        logits = torch.empty(T, g.vocab, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            enc.lm_head(head, out, targets=tg, logits=logits, loss_sum=lsum, count=cnt, workspace=hws, stream=stream)
+        n_mlm = 10
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(n_mlm):
+            enc.lm_head(head, out, targets=tg, logits=logits, loss_sum=lsum, count=cnt, workspace=hws, stream=stream)
+        m1.record(stream)
+        torch.cuda.synchronize()
+        enc.check(stream)
+        mms = m0.elapsed_time(m1) / n_mlm
+        mlm = {"call": "esm_encoder_lm_head (dense+GELU, LayerNorm, logits vs tied embedding, masked CE)",
+               "ms_per_call": mms, "tokens_per_s": T / (mms / 1e3), "scored_tokens": int(cnt.item()),
+               "mean_loss_random_weights": float(lsum.item()) / max(1, int(cnt.item()))}
+
     # ---------------------------------------------------------------- CPU baseline (oracle)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -433,6 +459,7 @@ def run_ours(args):
                 "algorithmic_gflop_per_step_per_gpu": total_flops / 1e9,
                 "roofline": roofline, "per_kernel": per_kernel,
                 "padded_over_packed_flops": (sum(executed.values()) / total_flops) if padded else None, "cpu_baseline": cpu, "e2e": e2e,
+                "mlm_head": mlm,
                 "clocks": clocks, "gpu_launches": launches,
                 "timing": "CUDA graph replay of the whole forward" if not args.no_graph else "eager launches",
                 "context": "pages' own figure: 59.2% model-FLOP utilisation, ESM-2 650M training, batch 46, A100"}
