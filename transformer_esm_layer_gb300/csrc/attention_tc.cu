@@ -6,7 +6,8 @@
 //   o_t = sum_s softmax_s(q_t . k_s / 8) v_s.
 //
 // Persistent: two CTAs per SM walk the (sequence, 128-query tile, head) work items of the
-// length-ordered list in a static stride; barrier phases run on across items.
+// length-ordered list in rounds of one item per CTA, in snake order; barrier phases run on
+// across items.
 //   warp 0      TMA: each item's Q tile (double-buffered, 128-byte swizzle) and its K and V
 //               tiles of 128 keys into 2-stage rings (K and V released separately),
 //               straight from the packed qkv buffer (x = column of the head, y = token row).
@@ -123,6 +124,11 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   AttnSmem* sm = reinterpret_cast<AttnSmem*>(base + TILE_BYTES * (2 + 2 * STG));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Items in rounds of gridDim.x, snake order: even rounds give CTA c item c of the round,
+  // odd rounds item gridDim.x - 1 - c (the list is longest first, so this evens out loads).
+  auto item_at = [&](int rnd) -> int {
+    return rnd * (int)gridDim.x + ((rnd & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  };
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm->q_full[b], 1);
@@ -154,10 +160,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int g = 0, qi = 0;
-      int4 nxt = load_item(pb, blockIdx.x, heads);
-      for (int it = blockIdx.x; it < n_items && !sm->abort; it += gridDim.x, ++qi) {
+      int4 nxt = load_item(pb, item_at(0), heads);
+      for (int rnd = 0, it = item_at(0); it < n_items && !sm->abort; it = item_at(++rnd), ++qi) {
         const Item x = make_item(nxt, it, heads);
-        if (it + (int)gridDim.x < n_items) nxt = load_item(pb, it + gridDim.x, heads);  // prefetch
+        if (item_at(rnd + 1) < n_items) nxt = load_item(pb, item_at(rnd + 1), heads);  // prefetch
         const int qb = qi & 1;
         if (!mbar_wait(&sm->q_empty[qb], ((uint32_t)(qi >> 1) & 1u) ^ 1u)) {
           latch_error(err, ERRBIT_TIMEOUT);
@@ -211,16 +217,16 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       const uint64_t vdesc0 = make_sw128_desc(smem_u32(sV));
       bool ok = true;
       int gs = 0, gp = 0;        // next S, next P V
-      int it_s = blockIdx.x, js = 0, qi_s = 0, nkb_s = 0;
+      int rnd_s = 0, it_s = item_at(0), js = 0, qi_s = 0, nkb_s = 0;
       bool have_item = false;
       uint32_t first_bits = 0;   // bit (g & 31): tile g is the first of its item
-      int4 nxt = load_item(pb, blockIdx.x, heads);
+      int4 nxt = load_item(pb, item_at(0), heads);
       unsigned long long idle_since = 0;
       uint32_t idle = 0;
       while (true) {
         if (!have_item && it_s < n_items) {
           const Item x = make_item(nxt, it_s, heads);
-          if (it_s + (int)gridDim.x < n_items) nxt = load_item(pb, it_s + gridDim.x, heads);
+          if (item_at(rnd_s + 1) < n_items) nxt = load_item(pb, item_at(rnd_s + 1), heads);
           nkb_s = x.nkb;
           js = 0;
           have_item = true;
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             ++gs;
             if (++js == nkb_s) {
               have_item = false;
-              it_s += gridDim.x;
+              it_s = item_at(++rnd_s);
               ++qi_s;
             }
             progressed = true;
@@ -292,10 +298,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     float amax = 0.f;
     bool ok = true;
     int g = 0, qi = 0;
-    int4 nxt = load_item(pb, blockIdx.x, heads);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++qi) {
+    int4 nxt = load_item(pb, item_at(0), heads);
+    for (int rnd = 0, it = item_at(0); it < n_items && ok; it = item_at(++rnd), ++qi) {
       const Item x = make_item(nxt, it, heads);
-      if (it + (int)gridDim.x < n_items) nxt = load_item(pb, it + gridDim.x, heads);  // prefetch
+      if (item_at(rnd + 1) < n_items) nxt = load_item(pb, item_at(rnd + 1), heads);  // prefetch
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < x.nkb; ++j, ++g) {
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
