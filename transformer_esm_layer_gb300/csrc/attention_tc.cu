@@ -8,14 +8,16 @@
 // Persistent: two CTAs per SM walk the (sequence, 128-query tile, head) work items of the
 // length-ordered list in rounds of one item per CTA, in snake order; barrier phases run on
 // across items.
-//   warp 0      TMA: each item's Q tile (double-buffered, 128-byte swizzle) and its K and V
-//               tiles of 128 keys into 2-stage rings (K and V released separately),
-//               straight from the packed qkv buffer (x = column of the head, y = token row).
+//   warp 0      TMA: each item's Q tile (double-buffered, 128-byte swizzle) and its K tiles
+//               of 128 keys into a 2-stage ring, straight from the packed qkv buffer
+//               (x = column of the head, y = token row);
+//   warp 2      TMA: the V tiles into their own 2-stage ring (a V stage frees only after its
+//               P V, a K stage right after its S, so K runs ahead of V).
 //   warp 1      one thread issues the MMAs of a global sequence of key tiles g:
 //               S(g) = Q K^T (M=128, N=128, K=64) into TMEM and O += P V (M=128, N=64,
 //               K=128; P read from TMEM, V an MN-major shared-memory operand), each as soon
 //               as its operands are ready.
-//   warps 2, 3  no role (they complete warpgroup 0, which hands registers to warpgroup 1).
+//   warp 3      no role (it completes warpgroup 0, which hands registers to warpgroup 1).
 //   warps 4..7  softmax (warpgroup 1, register budget raised with setmaxnreg): thread r owns
 //               query row r.  It reads its whole S row (128 scores) from TMEM into registers
 //               and immediately releases S, so the tensor core computes S(g+1) while this
@@ -156,50 +158,48 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const uint32_t tmem = sm->tmem_base;
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 0 loads each item's Q and its K tiles, warp 2 its V tiles: a K stage is free as
+    // soon as its S is done, a V stage only after its P V, so K never waits behind V.
     if (lane == 0) {
+      const bool kq = warp == 0;
       int g = 0, qi = 0;
       int4 nxt = load_item(pb, item_at(0), heads);
       for (int rnd = 0, it = item_at(0); it < n_items && !sm->abort; it = item_at(++rnd), ++qi) {
         const Item x = make_item(nxt, it, heads);
         if (item_at(rnd + 1) < n_items) nxt = load_item(pb, item_at(rnd + 1), heads);  // prefetch
-        const int qb = qi & 1;
-        if (!mbar_wait(&sm->q_empty[qb], ((uint32_t)(qi >> 1) & 1u) ^ 1u)) {
-          latch_error(err, ERRBIT_TIMEOUT);
-          sm->abort = 1;
-          break;
+        if (kq) {
+          const int qb = qi & 1;
+          if (!mbar_wait(&sm->q_empty[qb], ((uint32_t)(qi >> 1) & 1u) ^ 1u)) {
+            latch_error(err, ERRBIT_TIMEOUT);
+            sm->abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm->q_full[qb], TILE_BYTES);
+          tma_load_2d(sQ + qb * TILE_BYTES, &tm, x.h * DH, x.qrow0, &sm->q_full[qb]);
         }
-        mbar_arrive_expect_tx(&sm->q_full[qb], TILE_BYTES);
-        tma_load_2d(sQ + qb * TILE_BYTES, &tm, x.h * DH, x.qrow0, &sm->q_full[qb]);
+        uint64_t* empty = kq ? sm->k_empty : sm->v_empty;
+        uint64_t* full = kq ? sm->k_full : sm->v_full;
+        uint8_t* dst0 = kq ? sK : sV;
+        const int xcol = (kq ? d : 2 * d) + x.h * DH;
         for (int j = 0; j < x.nkb; ++j, ++g) {
-          // K stages free up when their S is done, V stages only after their P V: waiting
-          // for each separately lets K run a tile further ahead of the tensor core.
           const int st = g % STG;
-          const uint32_t par = ((uint32_t)(g / STG) & 1u) ^ 1u;
-          if (!mbar_wait(&sm->k_empty[st], par)) {
+          if (!mbar_wait(&empty[st], ((uint32_t)(g / STG) & 1u) ^ 1u)) {
             latch_error(err, ERRBIT_TIMEOUT);
             sm->abort = 1;
             break;
           }
-          mbar_arrive_expect_tx(&sm->k_full[st], TILE_BYTES);
-          tma_load_2d(sK + 2 * st * TILE_BYTES, &tm, d + x.h * DH, x.krow0 + j * KT, &sm->k_full[st]);
-          if (!mbar_wait(&sm->v_empty[st], par)) {
-            latch_error(err, ERRBIT_TIMEOUT);
-            sm->abort = 1;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm->v_full[st], TILE_BYTES);
-          tma_load_2d(sV + 2 * st * TILE_BYTES, &tm, 2 * d + x.h * DH, x.krow0 + j * KT, &sm->v_full[st]);
+          mbar_arrive_expect_tx(&full[st], TILE_BYTES);
+          tma_load_2d(dst0 + 2 * st * TILE_BYTES, &tm, xcol, x.krow0 + j * KT, &full[st]);
         }
       }
       // Copies still in flight can only exist if a consumer gave up early: then the last
       // STG stages are waited for (bounded) before the CTA exits.
       if (sm->abort) {
-        for (int k = g - 1; k >= 0 && k >= g - STG; --k) {
-          if (!mbar_wait(&sm->k_full[k % STG], (uint32_t)(k / STG) & 1u)) break;
-          if (!mbar_wait(&sm->v_full[k % STG], (uint32_t)(k / STG) & 1u)) break;
-        }
+        uint64_t* full = kq ? sm->k_full : sm->v_full;
+        for (int k = g - 1; k >= 0 && k >= g - STG; --k)
+          if (!mbar_wait(&full[k % STG], (uint32_t)(k / STG) & 1u)) break;
       }
     }
     __syncwarp();
