@@ -74,7 +74,7 @@ typedef enum {
   ESM_ERR_TIMEOUT = 7         /* a bounded device-side wait gave up                   */
 } esm_status;
 
-typedef enum { ESM_FP32 = 0, ESM_BF16 = 1, ESM_FP8_E4M3 = 2 } esm_precision;
+typedef enum { ESM_FP32 = 0, ESM_BF16 = 1, ESM_FP8_E4M3 = 2, ESM_FP4_E2M1 = 3 } esm_precision;
 
 /* Encoder geometry and numerics.  ESM-2 650M: {33, 1280, 20, 5120, 33, 1026, 1e-5,
  * 10000, 1, 1, ESM_BF16, 16}.  head_dim = hidden / heads must be 64 for ESM_BF16 and
@@ -168,6 +168,18 @@ ESM_API esm_status esm_encoder_forward_padded(esm_encoder_t* h, const esm_weight
                                       const int32_t* token_ids, const int32_t* seq_lens, int B,
                                       int S, void* hidden_out, void* workspace,
                                       size_t workspace_bytes, esm_stream_t stream);
+
+/* Per-layer GEMM precision -- the layer_precision setting and the per-layer autocast
+ * context (get_autocast_context(layer_number)) of the mlqm.cn walkthrough (mixed FP8 / FP4
+ * section): each Transformer layer may run its linear maps in its own precision.
+ * per_layer[num_layers]: for an ESM_FP8_E4M3 handle each entry is ESM_FP8_E4M3 (the
+ * layer's four GEMMs take E4M3 operands with the handle's delayed scaling) or ESM_BF16
+ * (bf16 operands; the layer's scales are then left unchanged); attention and LayerNorm stay
+ * bf16 either way.  A handle of another precision accepts only its own precision for every
+ * layer.  ESM_FP4_E2M1 (block-scaled FP4, named on that page) has no kernels here:
+ * ESM_ERR_UNSUPPORTED.  num_layers must equal the config's.  Takes effect from the next
+ * forward; default: every layer in the handle's precision. */
+ESM_API esm_status esm_encoder_set_layer_precision(esm_encoder_t* h, const esm_precision* per_layer, int num_layers);
 
 /* ---- masked-LM head (the step after the encoder) ----
  * The mlqm.cn walkthrough loads the model as AutoModelForMaskedLM and the BioNeMo ESM-2

@@ -41,6 +41,7 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.esm_encoder_forward(None, None, None, None, 0, 0, 0, None, None, 0, None) == 1
     assert lib.esm_encoder_check(None, None) == 1
     assert lib.esm_encoder_lm_head_workspace_size(None, 10, ctypes.byref(n)) == 1
+    assert lib.esm_encoder_set_layer_precision(None, None, 0) == 1
     assert lib.esm_encoder_lm_head(None, None, None, 0, None, None, None, None, None, None, 0, None) == 1
     lib.esm_encoder_destroy(None)
 

@@ -460,11 +460,13 @@ def test_fp8_layernorm_codes_match_oracle_rounding():
     assert abs(amax.item() / np.abs(ln).max() - 1) < 1e-5
 
 
-def _fp8_run(g, lengths, seed, calls=3):
+def _fp8_run(g, lengths, seed, calls=3, layer_precision=None):
     from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
     w = synth.model_weights(g, seed, "fp8")
     tok = synth.tokens_for_lengths(np.random.default_rng(seed), lengths)
     enc = EsmEncoder.from_geometry(g, "fp8", final_ln=True, amax_history_len=16)
+    if layer_precision is not None:
+        enc.set_layer_precision(layer_precision)
     dw = DeviceWeights(w, "fp8")
     t, cu = packed_inputs(tok, lengths)
     st0 = enc.get_fp8_state()
@@ -505,6 +507,44 @@ def test_fp8_forward_one_layer_and_delayed_scaling():
             else:
                 assert abs(hist2[l, i, 0] / amax[l][k] - 1) < 0.05, (l, k)
             assert scales2[l, i] == np.float32(448.0) / hist2[l, i].max()
+
+
+@pytest.mark.parametrize("layers", [("bf16", "fp8"), ("fp8", "bf16")])
+def test_per_layer_precision_mixed_bf16_and_fp8(layers):
+    """layer_precision: one layer with E4M3 GEMMs and one with bf16 GEMMs (650M width).  The
+    forward matches the oracle with E4M3 fake-quantisation on the FP8 layer only (5e-2, one
+    FP8 layer); the bf16 layer's scales stay 1 and its amax history stays empty."""
+    g = synth.Geometry(num_layers=2, hidden=1280, heads=20, ffn=5120)
+    lengths = [300, 1, 129, 64, 700]
+    enc, w, tok, st, out = _fp8_run(g, lengths, 33, layer_precision=list(layers))
+    scales, hist = enc.fp8_scales(st), enc.fp8_history(st)
+    fp8_state = [({k: float(scales[l, i]) for i, k in enumerate(O.FP8_TENSORS)} if layers[l] == "fp8" else None)
+                 for l in range(2)]
+    c = O.cu_seqlens(lengths)
+    ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, fp8_state=fp8_state, bf16_attention=True)
+    ref = np.concatenate([ref[i] for i in range(len(lengths))])
+    assert rel_l2(out, ref) < 5e-2
+    for l in range(2):
+        if layers[l] == "bf16":
+            assert np.all(scales[l] == 1.0) and np.all(hist[l] == 0.0)
+        else:
+            assert np.all(scales[l] > 1.0)
+
+
+def test_layer_precision_rejections():
+    from transformer_esm_layer_gb300.binding import EsmEncoder, EsmError
+    g = synth.Geometry(num_layers=2, hidden=256, heads=4, ffn=512)
+    enc8 = EsmEncoder.from_geometry(g, "fp8")
+    with pytest.raises(EsmError, match="UNSUPPORTED"):
+        enc8.set_layer_precision(["fp8", "fp4"])         # FP4: no kernels
+    with pytest.raises(EsmError, match="INVALID_ARG"):
+        enc8.set_layer_precision(["fp8"])                # wrong layer count
+    enc16 = EsmEncoder.from_geometry(g, "bf16")
+    with pytest.raises(EsmError, match="UNSUPPORTED"):
+        enc16.set_layer_precision(["bf16", "fp8"])       # FP8 layers need an FP8 handle
+    enc16.set_layer_precision(["bf16", "bf16"])
+    with pytest.raises(EsmError, match="UNSUPPORTED"):
+        EsmEncoder.from_geometry(g, "fp4")
 
 
 def test_fp8_forward_depth_accuracy():

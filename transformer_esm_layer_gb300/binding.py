@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libesm_encoder.so")
 ESM_OK = 0
 STATUS_NAMES = {0: "ESM_OK", 1: "ESM_ERR_INVALID_ARG", 2: "ESM_ERR_UNSUPPORTED", 3: "ESM_ERR_BAD_CU_SEQLENS",
                 4: "ESM_ERR_TOKEN_RANGE", 5: "ESM_ERR_WORKSPACE", 6: "ESM_ERR_CUDA", 7: "ESM_ERR_TIMEOUT"}
-PRECISIONS = {"fp32": 0, "bf16": 1, "fp8": 2}
+PRECISIONS = {"fp32": 0, "bf16": 1, "fp8": 2, "fp4": 3}
 EPILOGUES = {"bias_f32": 0, "qkv_rope": 1, "residual": 2, "gelu": 3}
 
 # Every symbol the header declares (checked by the tests).
@@ -28,6 +28,7 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_encoder_get_fp8_state", "esm_encoder_set_fp8_state", "esm_encoder_set_profiling",
            "esm_encoder_get_profile", "esm_op_attention_noalloc", "esm_op_layernorm_e4m3", "esm_op_gemm_fp8",
            "esm_encoder_debug_wait_timeout", "esm_encoder_lm_head_workspace_size", "esm_encoder_lm_head",
+           "esm_encoder_set_layer_precision",
            "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
 
@@ -83,6 +84,7 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_forward_host": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, i32, vp, vp, sz, vp]),
         "esm_encoder_forward_padded": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, vp, vp, sz, vp]),
         "esm_encoder_check": (i32, [vp, vp]),
+        "esm_encoder_set_layer_precision": (i32, [vp, ctypes.POINTER(ctypes.c_int), i32]),
         "esm_encoder_lm_head_workspace_size": (i32, [vp, i32, ctypes.POINTER(sz)]),
         "esm_encoder_lm_head": (i32, [vp, ctypes.POINTER(EsmLmHead), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "esm_encoder_debug_pack_index": (i32, [vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]),
@@ -319,6 +321,12 @@ class EsmEncoder:
                                               _ptr(o), _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
                     "esm_op_attention")
         return o
+
+    def set_layer_precision(self, per_layer):
+        """esm_encoder_set_layer_precision: one of "fp32", "bf16", "fp8", "fp4" per layer."""
+        arr = (ctypes.c_int * max(1, len(per_layer)))(*[PRECISIONS[p] for p in per_layer])
+        self._raise(self.lib.esm_encoder_set_layer_precision(self.handle, arr, len(per_layer)),
+                    "esm_encoder_set_layer_precision")
 
     def lm_head_workspace(self, T: int, device="cuda"):
         import torch

@@ -66,6 +66,7 @@ struct esm_encoder {
   int num_sms = 0;
   unsigned* d_err = nullptr;     // device error word
   float2* d_rope = nullptr;      // [16][max_positions][2] (cos, sin)
+  std::vector<uint8_t> layer_fp8;  // per layer: 1 = E4M3 GEMMs (FP8 handles only)
   float* d_fp8 = nullptr;        // scales [L*8] | history [L*8*len] | amax [L*8]
   size_t fp8_floats = 0;
   std::unordered_map<MapKey, CUtensorMap, MapKeyHash> maps;
@@ -280,11 +281,11 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
   void* o = b + L.o;
   void* u = b + L.u;
   const int d = c.hidden, f = c.ffn, H = c.heads;
-  const bool fp8 = c.precision == ESM_FP8_E4M3;
   const bool pf32 = !h->bf16_params();
   const Act act = h->act();
   esm_status s;
   for (int l = 0; l < c.num_layers; ++l) {
+    const bool fp8 = c.precision == ESM_FP8_E4M3 && h->layer_fp8[l];
     float* sc = h->fp8_scale() + (size_t)l * kNumFp8Tensors;
     float* am = h->fp8_amax() + (size_t)l * kNumFp8Tensors;
     uint8_t* wq_qkv = b + L.wq;
@@ -340,7 +341,7 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
          launch_layernorm(x, w->lnf_g, w->lnf_b, pf32, out, act, T, d, c.ln_eps, nullptr, nullptr, vp, vs, vk, st));
   else
     PROF(h, P_OTHER, st, 1, launch_copy_out(x, out, act, T, d, vp, vs, vk, st));
-  if (fp8)
+  if (c.precision == ESM_FP8_E4M3)
     PROF(h, P_OTHER, st, 1, launch_fp8_update(h->fp8_scale(), h->fp8_hist(), h->fp8_amax(), c.num_layers * kNumFp8Tensors,
                       c.amax_history_len, st));
   return cuda_status(cudaGetLastError());
@@ -415,12 +416,14 @@ esm_status esm_encoder_create(const esm_config* cfg, esm_encoder_t** out) {
     return ESM_ERR_CUDA;
   if (major != 10 || minor != 3) return ESM_ERR_UNSUPPORTED;
   if (!config_ok(cfg)) {
+    if (cfg->precision == ESM_FP4_E2M1) return ESM_ERR_UNSUPPORTED;  // named on the pages, no kernels here
     if (cfg->precision != ESM_FP32 && cfg->precision != ESM_BF16 && cfg->precision != ESM_FP8_E4M3)
       return ESM_ERR_INVALID_ARG;
     return (cfg->hidden > 0 && cfg->heads > 0 && cfg->num_layers >= 0) ? ESM_ERR_UNSUPPORTED : ESM_ERR_INVALID_ARG;
   }
   esm_encoder* h = new esm_encoder();
   h->cfg = *cfg;
+  h->layer_fp8.assign((size_t)(cfg->num_layers > 0 ? cfg->num_layers : 0), cfg->precision == ESM_FP8_E4M3 ? 1 : 0);
   h->device = dev;
   h->num_sms = sms;
   const size_t nf = (size_t)cfg->num_layers * kNumFp8Tensors;
@@ -480,6 +483,23 @@ static size_t lm_head_bytes(const esm_encoder* h, int T, size_t* off_z2, size_t*
   *off_z2 = act;
   *off_loss = 2 * act;
   return 2 * act + (((size_t)T * 4 + 255) & ~size_t(255));
+}
+
+esm_status esm_encoder_set_layer_precision(esm_encoder_t* h, const esm_precision* per_layer, int num_layers) {
+  if (!h || !per_layer || num_layers != h->cfg.num_layers) return ESM_ERR_INVALID_ARG;
+  std::vector<uint8_t> v((size_t)num_layers);
+  for (int l = 0; l < num_layers; ++l) {
+    const esm_precision p = per_layer[l];
+    if (p == ESM_FP4_E2M1) return ESM_ERR_UNSUPPORTED;
+    if (h->cfg.precision == ESM_FP8_E4M3) {
+      if (p != ESM_FP8_E4M3 && p != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+    } else if (p != h->cfg.precision) {
+      return ESM_ERR_UNSUPPORTED;
+    }
+    v[l] = p == ESM_FP8_E4M3 ? 1 : 0;
+  }
+  h->layer_fp8 = v;
+  return ESM_OK;
 }
 
 esm_status esm_encoder_lm_head_workspace_size(const esm_encoder_t* h, int total_tokens, size_t* bytes) {
