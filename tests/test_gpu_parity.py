@@ -353,6 +353,41 @@ def test_full_650m_workload_sampled_sequences():
 
 
 # --------------------------------------------------------------------------- errors
+def test_forward_host_matches_device_forward():
+    """esm_encoder_forward_host (host token ids / cu_seqlens in, host bf16 hidden states out,
+    copies inside the call) gives exactly the device-buffer forward."""
+    from transformer_esm_layer_gb300.binding import DeviceWeights, packed_inputs
+    g = SMALL
+    enc = _enc(g, "bf16")
+    w = synth.model_weights(g, 6, "bf16", ln_random=True)
+    lengths = [33, 1, 200, 7]
+    tok = synth.tokens_for_lengths(np.random.default_rng(6), lengths)
+    dw = DeviceWeights(w, "bf16")
+    t, cu = packed_inputs(tok, lengths)
+    dev_out = enc.forward(dw, t, cu, max(lengths)).view(torch.int16).cpu().numpy()
+    T = len(tok)
+    host_out = np.zeros((T, g.hidden), np.int16)
+    ws = enc.workspace(T, len(lengths), torch.device("cuda"))
+    enc.forward_host(dw, np.ascontiguousarray(tok, np.int32), synth.cu_seqlens_from_lengths(lengths), max(lengths),
+                     host_out, ws)
+    assert enc.check_status() == 0
+    assert np.array_equal(host_out, dev_out)
+
+
+def test_fp8_forward_one_layer_3b_width():
+    """One layer of the 3B geometry (hidden 2560, 40 heads, ffn 10240) with E4M3 GEMMs against
+    the oracle with the same scales (5e-2; attention in bf16)."""
+    g = synth.Geometry(num_layers=1, hidden=2560, heads=40, ffn=10240)
+    lengths = [300, 77, 1, 650]
+    enc, w, tok, st, out = _fp8_run(g, lengths, 34)
+    scales = enc.fp8_scales(st)
+    fp8_state = [{k: float(scales[0, i]) for i, k in enumerate(O.FP8_TENSORS)}]
+    c = O.cu_seqlens(lengths)
+    ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, fp8_state=fp8_state, bf16_attention=True)
+    ref = np.concatenate([ref[i] for i in range(len(lengths))])
+    assert rel_l2(out, ref) < 5e-2
+
+
 def test_token_out_of_range_reported():
     g = SMALL
     enc = _enc(g, "bf16")
