@@ -317,6 +317,105 @@ ESM_API esm_status esm_op_attention_noalloc(const void* qkv, const int32_t* cu_s
 ESM_API esm_status esm_encoder_get_fp8_state(const esm_encoder_t* h, float* host_buf, size_t n);
 ESM_API esm_status esm_encoder_set_fp8_state(esm_encoder_t* h, const float* host_buf, size_t n);
 
+/* ---- training: a forward that keeps its activations, and the backward pass ----
+ * The hotelren.com guide trains the packed model over cu_seqlens (section 3.2, the packed
+ * training loop; section 6, the training step with loss.backward()); the mlqm.cn walkthrough
+ * describes the same layer stack under training.  The pages do not write the backward
+ * out: it is the exact gradient of the forward above (chain rule through the final
+ * LayerNorm, every layer in reverse, and the embedding), with bf16 GEMM and attention
+ * operands and fp32 accumulation, reductions over tokens in a fixed order.
+ * ESM_BF16 handles only (others: ESM_ERR_UNSUPPORTED).
+ *
+ * Gradient buffers: device float32, same shapes as the weights ([out, in] for linear
+ * maps); the per-layer members point to HOST arrays of num_layers DEVICE pointers.
+ * Every buffer is overwritten (not accumulated into); 16-byte aligned. */
+typedef struct {
+  float* emb;                 /* [vocab, hidden]                                 */
+  float* const* ln1_g;
+  float* const* ln1_b;
+  float* const* w_qkv;        /* [3*hidden, hidden]                              */
+  float* const* b_qkv;
+  float* const* w_o;          /* [hidden, hidden]                                */
+  float* const* b_o;
+  float* const* ln2_g;
+  float* const* ln2_b;
+  float* const* w_1;          /* [ffn, hidden]                                   */
+  float* const* b_1;
+  float* const* w_2;          /* [hidden, ffn]                                   */
+  float* const* b_2;
+  float* lnf_g;               /* [hidden] (ignored if final_ln == 0)             */
+  float* lnf_b;
+} esm_grads;
+
+/* Bytes of the training buffer for up to max_tokens tokens: per layer the layer input and
+ * mid-layer residual (float32 [T, hidden]), the LayerNorm outputs, q|k|v after RoPE, the
+ * attention output (bf16), the attention log-sum-exp (float32 [T, heads]), fc1's
+ * pre-activation and GELU output (bf16 [T, ffn]); then the backward's scratch.  About
+ * 46 KB per token per layer for ESM-2 650M. */
+ESM_API esm_status esm_encoder_train_buffer_size(const esm_encoder_t* h, int max_tokens, size_t* bytes);
+
+/* The packed forward of esm_encoder_forward (same arguments, same hidden_out in bf16) that
+ * also keeps its activations in train_buf (device, 256-byte aligned, at least
+ * esm_encoder_train_buffer_size bytes).  total_tokens > 0.  The workspace and train_buf
+ * belong to the handle's next esm_encoder_backward: leave both untouched until then.
+ * Errors as esm_encoder_forward; ESM_ERR_WORKSPACE for a short train_buf. */
+ESM_API esm_status esm_encoder_forward_train(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids,
+                                             const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                                             int max_seqlen, void* hidden_out, void* train_buf, size_t train_bytes,
+                                             void* workspace, size_t workspace_bytes, esm_stream_t stream);
+
+/* Gradients of a loss L with respect to every parameter, given d_hidden_out = dL/d(hidden_out)
+ * (device float32 [T, hidden], T of the last esm_encoder_forward_train on this handle).
+ * train_buf and workspace must be the ones that forward used (ESM_ERR_INVALID_ARG
+ * otherwise); weights as in that forward.  grads->emb receives emb_scale times the sum of
+ * the embedded rows' gradients per token id. */
+ESM_API esm_status esm_encoder_backward(esm_encoder_t* h, const esm_weights* w, const float* d_hidden_out,
+                                        const esm_grads* grads, void* train_buf, size_t train_bytes,
+                                        void* workspace, size_t workspace_bytes, esm_stream_t stream);
+
+/* Backward hooks (the kernels the backward uses, exposed for parity); bf16 operands,
+ * handles of precision ESM_BF16 or ESM_FP8_E4M3.
+ * esm_op_gemm_dgrad: out[M, K] = dY[M, N] W with dY device bf16 [M, N] and W device bf16
+ *   [N, K] (a weight, [out, in]); out device float32, or bf16 with out_bf16 != 0.
+ *   N % 64 == 0, K % 256 == 0, 16-byte aligned pointers.
+ * esm_op_gemm_wgrad: dW[N, K] = dY^T X summed over the M rows of dY (bf16 [M, N]) and X
+ *   (bf16 [M, K]); dW device float32.  N % 256 == 0, K % 256 == 0, any M.  The workspace
+ *   (esm_op_gemm_wgrad_workspace_size bytes, 256-byte aligned; NULL allowed, then the
+ *   token reduction is not split) holds split partial products, added in a fixed order. */
+ESM_API esm_status esm_op_gemm_dgrad(esm_encoder_t* h, const void* dY, const void* W, void* out, int out_bf16, int M,
+                                     int N, int K, esm_stream_t stream);
+ESM_API esm_status esm_op_gemm_wgrad_workspace_size(const esm_encoder_t* h, int N, int K, size_t* bytes);
+ESM_API esm_status esm_op_gemm_wgrad(esm_encoder_t* h, const void* dY, const void* X, float* dW, int M, int N, int K,
+                                     void* workspace, size_t workspace_bytes, esm_stream_t stream);
+
+/* LayerNorm backward over rows of x (device float32 [rows, cols], cols % 4 == 0): with
+ * dy = dL/dy (float32 [rows, cols]) and gamma in the parameter dtype,
+ *   dx = dres + dL/dx (dres may be NULL or equal to dx), dgamma = sum_rows dy xhat,
+ *   dbeta = sum_rows dy (float32 [cols]).  Workspace: the size query's bytes. */
+ESM_API esm_status esm_op_layernorm_backward_workspace_size(const esm_encoder_t* h, int rows, int cols,
+                                                            size_t* bytes);
+ESM_API esm_status esm_op_layernorm_backward(esm_encoder_t* h, const float* x, const void* gamma, const float* dy,
+                                             const float* dres, float* dx, float* dgamma, float* dbeta, int rows,
+                                             int cols, void* workspace, size_t workspace_bytes,
+                                             esm_stream_t stream);
+
+/* esm_op_attention (bf16, head_dim 64) that also writes lse (device float32 [T, heads]):
+ * the natural-log softmax normaliser log sum_s exp(q_t . k_s / 8) of every query row.
+ * esm_op_attention_backward: from the same qkv (bf16 [T, 3*hidden], q | k | v as the
+ * attention read them), its output o (bf16 [T, hidden]), lse and d_o = dL/do (bf16
+ * [T, hidden]), writes dqkv = dL/d(q | k | v) (bf16 [T, 3*hidden]).  Workspace:
+ * esm_op_attention_backward_workspace_size bytes (the forward's work list plus float32
+ * scratch [T, heads] and [T, hidden]). */
+ESM_API esm_status esm_op_attention_train(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,
+                                          int total_tokens, int max_seqlen, void* o, float* lse, void* workspace,
+                                          size_t workspace_bytes, esm_stream_t stream);
+ESM_API esm_status esm_op_attention_backward_workspace_size(const esm_encoder_t* h, int total_tokens, int num_seqs,
+                                                            size_t* bytes);
+ESM_API esm_status esm_op_attention_backward(esm_encoder_t* h, const void* qkv, const void* o, const float* lse,
+                                             const void* d_o, const int32_t* cu_seqlens, int num_seqs,
+                                             int total_tokens, int max_seqlen, void* dqkv, void* workspace,
+                                             size_t workspace_bytes, esm_stream_t stream);
+
 /* ---- measurement hooks ----
  * Kernel classes of the forward: 0 QKV GEMM (+bias, RoPE), 1 attention, 2 output-projection
  * GEMM (+bias, residual), 3 fc1 GEMM (+bias, GELU), 4 fc2 GEMM (+bias, residual),

@@ -43,6 +43,17 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.esm_encoder_lm_head_workspace_size(None, 10, ctypes.byref(n)) == 1
     assert lib.esm_encoder_set_layer_precision(None, None, 0) == 1
     assert lib.esm_encoder_lm_head(None, None, None, 0, None, None, None, None, None, None, 0, None) == 1
+    assert lib.esm_encoder_train_buffer_size(None, 10, ctypes.byref(n)) == 1
+    assert lib.esm_encoder_forward_train(None, None, None, None, 1, 1, 1, None, None, 0, None, 0, None) == 1
+    assert lib.esm_encoder_backward(None, None, None, None, None, 0, None, 0, None) == 1
+    assert lib.esm_op_gemm_dgrad(None, None, None, None, 0, 1, 64, 256, None) == 1
+    assert lib.esm_op_gemm_wgrad_workspace_size(None, 256, 256, ctypes.byref(n)) == 1
+    assert lib.esm_op_gemm_wgrad(None, None, None, None, 1, 256, 256, None, 0, None) == 1
+    assert lib.esm_op_layernorm_backward_workspace_size(None, 4, 256, ctypes.byref(n)) == 1
+    assert lib.esm_op_layernorm_backward(None, None, None, None, None, None, None, None, 4, 256, None, 0, None) == 1
+    assert lib.esm_op_attention_train(None, None, None, 1, 1, 1, None, None, None, 0, None) == 1
+    assert lib.esm_op_attention_backward_workspace_size(None, 4, 1, ctypes.byref(n)) == 1
+    assert lib.esm_op_attention_backward(None, None, None, None, None, None, 1, 1, 1, None, None, 0, None) == 1
     lib.esm_encoder_destroy(None)
 
 

@@ -29,6 +29,10 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_encoder_get_profile", "esm_op_attention_noalloc", "esm_op_layernorm_e4m3", "esm_op_gemm_fp8",
            "esm_encoder_debug_wait_timeout", "esm_encoder_lm_head_workspace_size", "esm_encoder_lm_head",
            "esm_encoder_set_layer_precision",
+           "esm_encoder_train_buffer_size", "esm_encoder_forward_train", "esm_encoder_backward",
+           "esm_op_gemm_dgrad", "esm_op_gemm_wgrad_workspace_size", "esm_op_gemm_wgrad",
+           "esm_op_layernorm_backward_workspace_size", "esm_op_layernorm_backward", "esm_op_attention_train",
+           "esm_op_attention_backward_workspace_size", "esm_op_attention_backward",
            "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
 
@@ -57,6 +61,15 @@ class EsmWeights(ctypes.Structure):
     _fields_ = [("emb", ctypes.c_void_p)] + \
         [(n, _PP) for n in ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b",
                             "w_1", "b_1", "w_2", "b_2")] + \
+        [("lnf_g", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p)]
+
+
+_PF = ctypes.POINTER(ctypes.c_void_p)
+GRAD_NAMES = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_1", "b_1", "w_2", "b_2")
+
+
+class EsmGrads(ctypes.Structure):
+    _fields_ = [("emb", ctypes.c_void_p)] + [(n, _PF) for n in GRAD_NAMES] + \
         [("lnf_g", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p)]
 
 
@@ -100,6 +113,19 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_debug_wait_timeout": (i32, [vp, i32, vp]),
         "esm_op_gemm_fp8": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
         "esm_status_string": (ctypes.c_char_p, [i32]),
+        "esm_encoder_train_buffer_size": (i32, [vp, i32, ctypes.POINTER(sz)]),
+        "esm_encoder_forward_train": (i32, [vp, ctypes.POINTER(EsmWeights), vp, vp, i32, i32, i32, vp, vp, sz, vp, sz,
+                                            vp]),
+        "esm_encoder_backward": (i32, [vp, ctypes.POINTER(EsmWeights), vp, ctypes.POINTER(EsmGrads), vp, sz, vp, sz,
+                                       vp]),
+        "esm_op_gemm_dgrad": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, vp]),
+        "esm_op_gemm_wgrad_workspace_size": (i32, [vp, i32, i32, ctypes.POINTER(sz)]),
+        "esm_op_gemm_wgrad": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
+        "esm_op_layernorm_backward_workspace_size": (i32, [vp, i32, i32, ctypes.POINTER(sz)]),
+        "esm_op_layernorm_backward": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, vp]),
+        "esm_op_attention_train": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]),
+        "esm_op_attention_backward_workspace_size": (i32, [vp, i32, i32, ctypes.POINTER(sz)]),
+        "esm_op_attention_backward": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -141,6 +167,32 @@ class DeviceWeights:
             arr = (ctypes.c_void_p * max(n, 1))(*[l[name].data_ptr() for l in self.layers])
             self._keep.append(arr)
             setattr(st, name, ctypes.cast(arr, _PP))
+        st.lnf_g = self.lnf_g.data_ptr()
+        st.lnf_b = self.lnf_b.data_ptr()
+        self.struct = st
+
+
+class DeviceGrads:
+    """float32 gradient buffers on the device, shaped like the weights, plus the esm_grads
+    struct (esm_encoder_backward overwrites them)."""
+
+    def __init__(self, g, num_layers: int, device="cuda"):
+        import torch
+        z = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=device)
+        d, f = g.hidden, g.ffn
+        shapes = {"ln1_g": (d,), "ln1_b": (d,), "w_qkv": (3 * d, d), "b_qkv": (3 * d,), "w_o": (d, d), "b_o": (d,),
+                  "ln2_g": (d,), "ln2_b": (d,), "w_1": (f, d), "b_1": (f,), "w_2": (d, f), "b_2": (d,)}
+        self.emb = z(g.vocab, d)
+        self.layers = [{k: z(*s) for k, s in shapes.items()} for _ in range(num_layers)]
+        self.lnf_g = z(d)
+        self.lnf_b = z(d)
+        self._keep = []
+        st = EsmGrads()
+        st.emb = self.emb.data_ptr()
+        for name in GRAD_NAMES:
+            arr = (ctypes.c_void_p * max(num_layers, 1))(*[l[name].data_ptr() for l in self.layers])
+            self._keep.append(arr)
+            setattr(st, name, ctypes.cast(arr, _PF))
         st.lnf_g = self.lnf_g.data_ptr()
         st.lnf_b = self.lnf_b.data_ptr()
         self.struct = st
@@ -346,6 +398,98 @@ class EsmEncoder:
                                                  _ptr(logits), _ptr(token_loss), _ptr(loss_sum), _ptr(count),
                                                  _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
                     "esm_encoder_lm_head")
+
+    # ------------------------------------------------------------------ training
+    def train_buffer(self, max_tokens: int, device="cuda"):
+        import torch
+        n = ctypes.c_size_t()
+        self._raise(self.lib.esm_encoder_train_buffer_size(self.handle, max_tokens, ctypes.byref(n)),
+                    "esm_encoder_train_buffer_size")
+        return torch.empty(int(n.value), dtype=torch.uint8, device=device)
+
+    def forward_train(self, weights: DeviceWeights, token_ids, cu_seqlens, max_seqlen: int, train_buf, workspace,
+                      out=None, stream=None):
+        """esm_encoder_forward_train: the forward, keeping its activations in train_buf."""
+        import torch
+        T = token_ids.numel()
+        B = cu_seqlens.numel() - 1
+        if out is None:
+            out = torch.empty(T, self.hidden, dtype=self.out_dtype, device=token_ids.device)
+        self._raise(self.lib.esm_encoder_forward_train(self.handle, ctypes.byref(weights.struct), _ptr(token_ids),
+                                                       _ptr(cu_seqlens), B, T, int(max_seqlen), _ptr(out),
+                                                       _ptr(train_buf), train_buf.numel(), _ptr(workspace),
+                                                       workspace.numel(), _stream_ptr(stream)),
+                    "esm_encoder_forward_train")
+        return out
+
+    def backward(self, weights: DeviceWeights, d_out, grads: "DeviceGrads", train_buf, workspace, stream=None):
+        """esm_encoder_backward: parameter gradients of the last forward_train, given dL/d(out)."""
+        self._raise(self.lib.esm_encoder_backward(self.handle, ctypes.byref(weights.struct), _ptr(d_out),
+                                                  ctypes.byref(grads.struct), _ptr(train_buf), train_buf.numel(),
+                                                  _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+                    "esm_encoder_backward")
+        return grads
+
+    def op_gemm_dgrad(self, dY, W, out, stream=None):
+        import torch
+        M, N = dY.shape
+        K = W.shape[1]
+        self._raise(self.lib.esm_op_gemm_dgrad(self.handle, _ptr(dY), _ptr(W), _ptr(out),
+                                               int(out.dtype == torch.bfloat16), M, N, K, _stream_ptr(stream)),
+                    "esm_op_gemm_dgrad")
+        return out
+
+    def op_gemm_wgrad(self, dY, X, dW, workspace=None, stream=None):
+        import torch
+        M, N = dY.shape
+        K = X.shape[1]
+        if workspace is None:
+            n = ctypes.c_size_t()
+            self._raise(self.lib.esm_op_gemm_wgrad_workspace_size(self.handle, N, K, ctypes.byref(n)),
+                        "esm_op_gemm_wgrad_workspace_size")
+            workspace = torch.empty(int(n.value), dtype=torch.uint8, device=dY.device)
+        self._raise(self.lib.esm_op_gemm_wgrad(self.handle, _ptr(dY), _ptr(X), _ptr(dW), M, N, K, _ptr(workspace),
+                                               0 if workspace is None else workspace.numel(), _stream_ptr(stream)),
+                    "esm_op_gemm_wgrad")
+        return dW
+
+    def op_layernorm_backward(self, x, gamma, dy, dres, dx, dgamma, dbeta, stream=None):
+        import torch
+        rows, cols = x.shape
+        n = ctypes.c_size_t()
+        self._raise(self.lib.esm_op_layernorm_backward_workspace_size(self.handle, rows, cols, ctypes.byref(n)),
+                    "esm_op_layernorm_backward_workspace_size")
+        ws = torch.empty(int(n.value), dtype=torch.uint8, device=x.device)
+        self._raise(self.lib.esm_op_layernorm_backward(self.handle, _ptr(x), _ptr(gamma), _ptr(dy), _ptr(dres),
+                                                       _ptr(dx), _ptr(dgamma), _ptr(dbeta), rows, cols, _ptr(ws),
+                                                       ws.numel(), _stream_ptr(stream)), "esm_op_layernorm_backward")
+        return dx, dgamma, dbeta
+
+    def op_attention_train(self, qkv, cu_seqlens, max_seqlen: int, o, lse, workspace=None, stream=None):
+        T = qkv.shape[0]
+        B = cu_seqlens.numel() - 1
+        if workspace is None:
+            workspace = self.workspace(T, B, qkv.device)
+        self._raise(self.lib.esm_op_attention_train(self.handle, _ptr(qkv), _ptr(cu_seqlens), B, T, int(max_seqlen),
+                                                    _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                                    _stream_ptr(stream)), "esm_op_attention_train")
+        return o, lse
+
+    def op_attention_backward(self, qkv, o, lse, d_o, cu_seqlens, max_seqlen: int, dqkv, workspace=None,
+                              stream=None):
+        import torch
+        T = qkv.shape[0]
+        B = cu_seqlens.numel() - 1
+        if workspace is None:
+            n = ctypes.c_size_t()
+            self._raise(self.lib.esm_op_attention_backward_workspace_size(self.handle, T, B, ctypes.byref(n)),
+                        "esm_op_attention_backward_workspace_size")
+            workspace = torch.empty(int(n.value), dtype=torch.uint8, device=qkv.device)
+        self._raise(self.lib.esm_op_attention_backward(self.handle, _ptr(qkv), _ptr(o), _ptr(lse), _ptr(d_o),
+                                                       _ptr(cu_seqlens), B, T, int(max_seqlen), _ptr(dqkv),
+                                                       _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+                    "esm_op_attention_backward")
+        return dqkv
 
     def set_profiling(self, enable: bool):
         self._raise(self.lib.esm_encoder_set_profiling(self.handle, int(enable)), "esm_encoder_set_profiling")

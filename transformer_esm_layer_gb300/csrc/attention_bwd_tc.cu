@@ -1,0 +1,468 @@
+// Backward of the variable-length bidirectional attention on the tcgen05 tensor cores
+// (head_dim 64, bf16 operands, fp32 accumulation): the gradient step of the packed layer
+// stack that the hotelren.com guide trains over cu_seqlens (§3.2, §6).
+//
+// With S = Q K^T / 8, P = softmax(S) (rows: queries), O = P V and dO given, per head:
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D) with D_i = sum_c dO_ic O_ic,
+//   dK = dS^T Q / 8,  dQ = dS K / 8.
+// P is rebuilt from the forward's log-sum-exp (no softmax pass over the keys here).
+//
+// One CTA per SM walks the work items (sequence, 128-key tile, head) of the forward's work
+// list (a forward query tile is, in packed self-attention, also a key tile: its rows, and
+// the sequence's row range).  For each item it holds K and V in shared memory and loops
+// over the sequence's 128-query tiles; TMEM lanes are keys throughout:
+//   S^T  = K Q^T        (M=128 keys, N=128 queries, K=64)        TMEM cols [0,128)
+//   dP^T = V dO^T       (M=128, N=128, K=64)                       cols [128,256)
+//   dV  += P^T dO       (M=128, N=64, K=128; dO MN-major)          cols [384,448)
+//   dK  += dS^T Q       (M=128, N=64, K=128; Q MN-major)           cols [320,384)
+//   dQ_i = dS K         (M=128 queries, N=64, K=128 keys; dS and K MN-major)  cols [256,320)
+// Roles (384 threads):
+//   warp 0       TMA: the item's K and V tiles, then Q and dO tiles of each query tile into
+//                a 2-stage ring (straight from the packed qkv and dO buffers);
+//   warp 1       one thread issues the MMAs: S^T and dP^T of tile i, then the three
+//                gradient products of tile i-1 (whose P^T and dS^T are in shared memory);
+//   warps 4..7   thread r owns key r: reads its S^T and dP^T rows, forms P^T = 2^(S^T c - lse)
+//                and dS^T = P^T (dP^T - D) for the valid (key, query) pairs, writes both
+//                as bf16 into shared memory (K-major, 128-byte swizzle); at the end of the
+//                item scales dK, turns it back through RoPE and stores dK and dV (bf16);
+//   warps 8..11  thread r owns query r of the tile: reads dQ_i from TMEM and adds it into
+//                an fp32 accumulator in global memory with vector reductions (several key
+//                tiles contribute to each query row).
+// Every mbarrier wait is bounded; on timeout the kernel latches an error bit and stops.
+#include "common.cuh"
+#include "internal.h"
+
+namespace esm {
+namespace {
+
+constexpr int DH = 64;
+constexpr int TB = 128;                 // rows of a key or query tile
+constexpr int TILE = 128 * 128;         // 128 rows x 128 bytes (64 bf16)
+constexpr int THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DK = 320, COL_DV = 384;
+
+struct BwdSmem {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, s_free, p_full, p_free, dq_full, dq_free, acc_full, acc_free, mma_done;
+  uint64_t stat_full[2];  // all 128 slots of lse2 / dsum [b] written (128 arrivals)
+  uint32_t tmem_base;
+  volatile int abort;
+  float lse2[2][TB];  // query tile g (buffer g & 1): log2-sum-exp2 of the scaled scores
+  float dsum[2][TB];  // and D
+};
+// [dS^T 32K][P^T 32K][Q0][Q1][dO0][dO1][K][V] then BwdSmem
+constexpr int OFF_DS = 0, OFF_P = 2 * TILE, OFF_Q = 4 * TILE, OFF_DO = 6 * TILE, OFF_K = 8 * TILE,
+              OFF_V = 9 * TILE, OFF_BAR = 10 * TILE;
+constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(BwdSmem) + 1024;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 16-byte unit j of row r of a 128-row x 128-byte tile with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+struct BItem {
+  int k0, krows, s0, slen, h, nq;
+};
+__device__ __forceinline__ BItem bitem(const PackBuffers& pb, int it, int heads) {
+  const int4 w = __ldg(reinterpret_cast<const int4*>(pb.work) + it / heads);
+  BItem x;
+  x.h = it % heads;
+  x.k0 = w.x;
+  x.krows = w.y;
+  x.s0 = w.z;
+  x.slen = w.w;
+  x.nq = (w.w + TB - 1) / TB;
+  return x;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attention_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                            const float* __restrict__ lse, const float* __restrict__ dsum,
+                            float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dqkv, int d, int heads,
+                            PackBuffers pb, const float2* __restrict__ rope, int max_pos, unsigned* err) {
+  const int n_items = *pb.work_count * heads;
+  if ((int)blockIdx.x >= n_items) return;  // whole CTA, before any barrier or TMEM use
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdSmem* sm = reinterpret_cast<BwdSmem*>(base + OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm->kv_full, 1);
+    mbar_init(&sm->kv_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm->q_full[b], 1);
+      mbar_init(&sm->q_empty[b], 1);
+    }
+    mbar_init(&sm->s_full, 1);
+    mbar_init(&sm->s_free, 4);
+    mbar_init(&sm->p_full, 4);
+    mbar_init(&sm->p_free, 1);
+    mbar_init(&sm->dq_full, 1);
+    mbar_init(&sm->dq_free, 4);
+    mbar_init(&sm->acc_full, 1);
+    mbar_init(&sm->acc_free, 4);
+    mbar_init(&sm->mma_done, 1);
+    mbar_init(&sm->stat_full[0], 128);
+    mbar_init(&sm->stat_full[1], 128);
+    sm->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sm->tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_qkv);
+      tma_prefetch_desc(&tm_do);
+      int g = 0, n = 0;
+      for (int it = blockIdx.x; it < n_items && !sm->abort; it += gridDim.x, ++n) {
+        const BItem x = bitem(pb, it, heads);
+        if (!mbar_wait(&sm->kv_empty, (uint32_t)(n & 1) ^ 1u)) { latch_error(err, ERRBIT_TIMEOUT); sm->abort = 1; break; }
+        mbar_arrive_expect_tx(&sm->kv_full, 2 * TILE);
+        tma_load_2d(base + OFF_K, &tm_qkv, d + x.h * DH, x.k0, &sm->kv_full);
+        tma_load_2d(base + OFF_V, &tm_qkv, 2 * d + x.h * DH, x.k0, &sm->kv_full);
+        for (int i = 0; i < x.nq; ++i, ++g) {
+          const int st = g & 1;
+          if (!mbar_wait(&sm->q_empty[st], (uint32_t)((g >> 1) & 1) ^ 1u)) {
+            latch_error(err, ERRBIT_TIMEOUT);
+            sm->abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm->q_full[st], 2 * TILE);
+          tma_load_2d(base + OFF_Q + st * TILE, &tm_qkv, x.h * DH, x.s0 + i * TB, &sm->q_full[st]);
+          tma_load_2d(base + OFF_DO + st * TILE, &tm_do, x.h * DH, x.s0 + i * TB, &sm->q_full[st]);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(TB, TB);                                   // S^T, dP^T
+      constexpr uint32_t idesc_kv = idesc_bf16(TB, DH) | kIdescBMn;                      // dV, dK
+      constexpr uint32_t idesc_q = idesc_bf16(TB, DH) | kIdescAMn | kIdescBMn;           // dQ
+      const uint32_t sb = smem_u32(base);
+      const uint64_t k_kmaj = make_sw128_desc(sb + OFF_K);
+      const uint64_t v_kmaj = make_sw128_desc(sb + OFF_V);
+      const uint64_t k_mn = make_sw128_mn_desc(sb + OFF_K, TILE);
+      const uint64_t p_kmaj = make_sw128_desc(sb + OFF_P);
+      const uint64_t ds_kmaj = make_sw128_desc(sb + OFF_DS);
+      const uint64_t ds_mn = make_sw128_mn_desc(sb + OFF_DS, TILE);  // queries 64.. one tile further
+      bool ok = true;
+      int g = 0, n = 0;
+      // gradient products of global tile gb (item-local index i) from stage gb & 1
+      auto back = [&](int gb, int i, int item_n) -> bool {
+        if (!mbar_wait(&sm->p_full, (uint32_t)gb & 1u)) return false;
+        if (!mbar_wait(&sm->dq_free, (uint32_t)(gb & 1) ^ 1u)) return false;
+        if (i == 0 && !mbar_wait(&sm->acc_free, (uint32_t)(item_n & 1) ^ 1u)) return false;
+        tc_fence_after();
+        const int st = gb & 1;
+        const uint64_t q_mn = make_sw128_mn_desc(sb + OFF_Q + st * TILE, TILE);
+        const uint64_t do_mn = make_sw128_mn_desc(sb + OFF_DO + st * TILE, TILE);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // K = 128 queries in steps of 16
+          // K-major P^T / dS^T: queries 64k.. live in the second 16 KB block
+          const uint64_t koff = (uint64_t)(((k >> 2) * TILE) >> 4) + 2u * (uint64_t)(k & 3);
+          const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
+          mma_bf16_ss(tmem + COL_DV, p_kmaj + koff, do_mn + 128u * (uint64_t)k, idesc_kv, acc);
+          mma_bf16_ss(tmem + COL_DK, ds_kmaj + koff, q_mn + 128u * (uint64_t)k, idesc_kv, acc);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // K = 128 keys in steps of 16
+          mma_bf16_ss(tmem + COL_DQ, ds_mn + 128u * (uint64_t)k, k_mn + 128u * (uint64_t)k, idesc_q, k > 0 ? 1u : 0u);
+        mma_commit(&sm->p_free);
+        mma_commit(&sm->dq_full);
+        mma_commit(&sm->q_empty[st]);
+        return true;
+      };
+      for (int it = blockIdx.x; it < n_items && ok && !sm->abort; it += gridDim.x, ++n) {
+        const BItem x = bitem(pb, it, heads);
+        if (!mbar_wait(&sm->kv_full, (uint32_t)n & 1u)) { ok = false; break; }
+        for (int i = 0; i < x.nq; ++i, ++g) {
+          const int st = g & 1;
+          if (!mbar_wait(&sm->q_full[st], (uint32_t)(g >> 1) & 1u) ||
+              !mbar_wait(&sm->s_free, (uint32_t)(g & 1) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t q_kmaj = make_sw128_desc(sb + OFF_Q + st * TILE);
+          const uint64_t do_kmaj = make_sw128_desc(sb + OFF_DO + st * TILE);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16_ss(tmem + COL_S, k_kmaj + 2u * k, q_kmaj + 2u * k, idesc_s, k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16_ss(tmem + COL_DP, v_kmaj + 2u * k, do_kmaj + 2u * k, idesc_s, k > 0 ? 1u : 0u);
+          mma_commit(&sm->s_full);
+          if (i > 0 && !back(g - 1, i - 1, n)) { ok = false; break; }
+        }
+        if (!ok || !back(g - 1, x.nq - 1, n)) { ok = false; break; }
+        mma_commit(&sm->acc_full);
+        mma_commit(&sm->kv_empty);
+      }
+      if (!ok) {
+        latch_error(err, ERRBIT_TIMEOUT);
+        sm->abort = 1;
+      }
+      mma_commit(&sm->mma_done);
+      mbar_wait(&sm->mma_done, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ P^T / dS^T, dK / dV
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key row of the tile (and index of the lse / D slot)
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float c = kLog2e / 8.f;  // scores scaled by 1/sqrt(64), in log2 units
+    uint8_t* sP = base + OFF_P;
+    uint8_t* sDS = base + OFF_DS;
+    bool ok = true;
+    int g = 0, n = 0;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
+      const BItem x = bitem(pb, it, heads);
+      const bool kval = r < x.krows;
+      for (int i = 0; i < x.nq; ++i, ++g) {
+        const int q0 = x.s0 + i * TB, qvalid = min(TB, x.slen - i * TB);
+        // this tile's lse (to log2 units) and D, one slot per thread, into buffer g & 1 (its
+        // previous readers, tile g - 2, are done: every thread arrived for tile g - 1 after
+        // finishing tile g - 2)
+        const int sb = g & 1;
+        float l2 = 0.f, dd = 0.f;
+        if (r < qvalid) {
+          l2 = __ldg(lse + (size_t)(q0 + r) * heads + x.h) * kLog2e;
+          dd = __ldg(dsum + (size_t)(q0 + r) * heads + x.h);
+        }
+        sm->lse2[sb][r] = l2;
+        sm->dsum[sb][r] = dd;
+        mbar_arrive(&sm->stat_full[sb]);
+        if (!mbar_wait_warp(&sm->stat_full[sb], (uint32_t)(g >> 1) & 1u)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
+        // P^T / dS^T may be overwritten once the previous tile's gradient MMAs have read them
+        if (!mbar_wait_warp(&sm->p_free, (uint32_t)(g & 1) ^ 1u)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {  // 32 queries per chunk
+          float s[32], dp[32];
+          tmem_ld32(tmem + lane_off + COL_S + 32 * ch, s);
+          tmem_ld32(tmem + lane_off + COL_DP + 32 * ch, dp);
+          uint32_t pw[16], dw[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int q = 32 * ch + 2 * j;
+            const bool v0 = kval && q < qvalid, v1 = kval && q + 1 < qvalid;
+            const float p0 = v0 ? fast_exp2(fmaf(s[2 * j], c, -sm->lse2[sb][q])) : 0.f;
+            const float p1 = v1 ? fast_exp2(fmaf(s[2 * j + 1], c, -sm->lse2[sb][q + 1])) : 0.f;
+            pw[j] = pack_bf16x2(p0, p1);
+            dw[j] = pack_bf16x2(p0 * (dp[2 * j] - sm->dsum[sb][q]), p1 * (dp[2 * j + 1] - sm->dsum[sb][q + 1]));
+          }
+          const int blk = ch >> 1;  // queries 0-63 | 64-127
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t off = (uint32_t)(blk * TILE) + swz(r, (ch & 1) * 4 + u);
+            *reinterpret_cast<uint4*>(sP + off) = make_uint4(pw[4 * u], pw[4 * u + 1], pw[4 * u + 2], pw[4 * u + 3]);
+            *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
+          }
+        }
+        tc_fence_before();
+        fence_async_smem();  // generic-proxy writes of P^T / dS^T before the tensor core reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm->s_free);
+          mbar_arrive(&sm->p_full);
+        }
+      }
+      if (!ok) break;
+      // ---- item epilogue: dK (scaled, RoPE undone) and dV of this thread's key
+      if (!mbar_wait_warp(&sm->acc_full, (uint32_t)n & 1u)) { ok = false; break; }
+      tc_fence_after();
+      float dk[64], dv[64];
+      {
+        float t[32];
+        tmem_ld32(tmem + lane_off + COL_DK, t);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dk[j] = t[j];
+        tmem_ld32(tmem + lane_off + COL_DK + 32, t);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dk[32 + j] = t[j];
+        tmem_ld32(tmem + lane_off + COL_DV, t);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dv[j] = t[j];
+        tmem_ld32(tmem + lane_off + COL_DV + 32, t);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dv[32 + j] = t[j];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->acc_free);
+      if (kval) {
+        const int key = x.k0 + r;
+        if (rope != nullptr) {
+          int p = key - x.s0;
+          p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {  // pair (j, j + 32) turned back by its angle
+            const float2 cs = __ldg(rope + ((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1));
+            const float a = dk[j] * 0.125f, b = dk[j + 32] * 0.125f;
+            dk[j] = a * cs.x + b * cs.y;
+            dk[j + 32] = b * cs.x - a * cs.y;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) dk[j] *= 0.125f;
+        }
+        uint4* gk = reinterpret_cast<uint4*>(dqkv + (size_t)key * 3 * d + d + x.h * DH);
+        uint4* gv = reinterpret_cast<uint4*>(dqkv + (size_t)key * 3 * d + 2 * d + x.h * DH);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          gk[u] = make_uint4(pack_bf16x2(dk[8 * u], dk[8 * u + 1]), pack_bf16x2(dk[8 * u + 2], dk[8 * u + 3]),
+                             pack_bf16x2(dk[8 * u + 4], dk[8 * u + 5]), pack_bf16x2(dk[8 * u + 6], dk[8 * u + 7]));
+          gv[u] = make_uint4(pack_bf16x2(dv[8 * u], dv[8 * u + 1]), pack_bf16x2(dv[8 * u + 2], dv[8 * u + 3]),
+                             pack_bf16x2(dv[8 * u + 4], dv[8 * u + 5]), pack_bf16x2(dv[8 * u + 6], dv[8 * u + 7]));
+        }
+      }
+    }
+    if (!ok) {
+      latch_error(err, ERRBIT_TIMEOUT);
+      sm->abort = 1;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ accumulation
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query row of the tile
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    bool ok = true;
+    int g = 0;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const BItem x = bitem(pb, it, heads);
+      for (int i = 0; i < x.nq; ++i, ++g) {
+        if (!mbar_wait_warp(&sm->dq_full, (uint32_t)g & 1u)) { ok = false; break; }
+        tc_fence_after();
+        float a[32], b[32];
+        tmem_ld32(tmem + lane_off + COL_DQ, a);
+        tmem_ld32(tmem + lane_off + COL_DQ + 32, b);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->dq_free);
+        if (r < min(TB, x.slen - i * TB)) {
+          float* dst = dq_acc + (size_t)(x.s0 + i * TB + r) * d + x.h * DH;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) red_add_v4(dst + 4 * u, a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dst + 32 + 4 * u, b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+        }
+      }
+    }
+    if (!ok) {
+      latch_error(err, ERRBIT_TIMEOUT);
+      sm->abort = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// D[t, h] = sum_c dO[t, h*64 + c] * O[t, h*64 + c] (one thread per (token, head)).
+__global__ void attention_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                                          float* __restrict__ dsum, int T, int d, int heads) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)T * heads) return;
+  const long long t = i / heads;
+  const int h = (int)(i % heads);
+  const uint4* a = reinterpret_cast<const uint4*>(o + t * d + h * DH);
+  const uint4* b = reinterpret_cast<const uint4*>(dout + t * d + h * DH);
+  float acc = 0.f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 x = __ldg(a + u), y = __ldg(b + u);
+    const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&x);
+    const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&y);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 xf = __bfloat1622float2(xh[k]), yf = __bfloat1622float2(yh[k]);
+      acc = fmaf(xf.x, yf.x, acc);
+      acc = fmaf(xf.y, yf.y, acc);
+    }
+  }
+  dsum[i] = acc;
+}
+
+// dq = dq_acc / 8 with RoPE undone (pairs (j, j + 32) turned back by their angle) -> the q
+// block of dqkv (bf16).  One thread per (token, head, pair).
+__global__ void attention_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dqkv,
+                                        const int32_t* __restrict__ pos_id, const float2* __restrict__ rope,
+                                        int max_pos, int T, int d) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int half_d = d / 2;
+  if (i >= (long long)T * half_d) return;
+  const long long t = i / half_d;
+  const int rem = (int)(i % half_d);
+  const int h = rem / 32, j = rem % 32;
+  const float* src = dq_acc + t * d + h * DH;
+  float a = src[j] * 0.125f, b = src[j + 32] * 0.125f;
+  if (rope != nullptr) {
+    int p = __ldg(pos_id + t);
+    p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
+    const float2 cs = __ldg(rope + ((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1));
+    const float a2 = a * cs.x + b * cs.y;
+    b = b * cs.x - a * cs.y;
+    a = a2;
+  }
+  __nv_bfloat16* dst = dqkv + t * 3 * d + h * DH;
+  dst[j] = __float2bfloat16_rn(a);
+  dst[j + 32] = __float2bfloat16_rn(b);
+}
+
+}  // namespace
+
+int attention_bwd_tc_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const __nv_bfloat16* o,
+                                    const __nv_bfloat16* dout, const float* lse, float* dsum, float* dq_acc,
+                                    __nv_bfloat16* dqkv, int T, int d, int heads, int max_items, const PackBuffers& pb,
+                                    const float2* rope, int max_pos, int num_sms, unsigned* err, cudaStream_t st) {
+  if (T <= 0 || max_items <= 0) return cudaSuccess;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attention_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const long long th = (long long)T * heads;
+  attention_bwd_dsum_kernel<<<(unsigned)((th + 255) / 256), 256, 0, st>>>(o, dout, dsum, T, d, heads);
+  cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * d, st);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)max_items * heads;
+  const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
+  attention_bwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, *tm_do, lse, dsum, dq_acc, dqkv, d, heads, pb,
+                                                             rope, max_pos, err);
+  const long long tq = (long long)T * (d / 2);
+  attention_bwd_dq_kernel<<<(unsigned)((tq + 255) / 256), 256, 0, st>>>(dq_acc, dqkv, pb.pos_id, rope, max_pos, T, d);
+  return cudaGetLastError();
+}
+
+}  // namespace esm

@@ -114,7 +114,8 @@ __device__ __forceinline__ Item make_item(int4 w, int it, int heads) {
 template <Act OUT>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm, void* __restrict__ o, int d, int heads,
-                        PackBuffers pb, const float* q_scale, float* amax_out, unsigned* err) {
+                        PackBuffers pb, const float* q_scale, float* amax_out, float* __restrict__ lse,
+                        unsigned* err) {
   const int n_items = *pb.work_count * heads;
   if ((int)blockIdx.x >= n_items) return;  // whole CTA, before any barrier or TMEM use
 
@@ -389,6 +390,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       tmem_ld_wait_regs(u[1]);
       tc_fence_before();
       const float inv = 1.f / l;
+      // training forward: the natural-log softmax normaliser of this row and head (scores
+      // scaled by 1/sqrt(dh)), ln 2 * (m + log2 l) in the base-2 units used above
+      if (lse != nullptr && r < x.qrows) lse[(size_t)(x.qrow0 + r) * heads + x.h] = 0.6931471805599453f * (m_ref + log2f(l));
       uint8_t* stage = sQ + (qi & 1) * TILE_BYTES;
       constexpr int kUnits = (OUT == Act::BF16) ? 8 : 4;  // 16-byte units per output row
       if constexpr (OUT == Act::BF16) {
@@ -462,7 +466,7 @@ int attention_tc_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int d, int heads, int max_items,
                                 const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
-                                cudaStream_t st) {
+                                cudaStream_t st, float* lse) {
   if (max_items <= 0) return cudaSuccess;
   static int num_sms = 0;
   static bool configured[2] = {false, false};
@@ -486,9 +490,11 @@ cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int
   const long long cap = (long long)CTAS_PER_SM * num_sms;
   const unsigned grid = (unsigned)(items < cap ? items : cap);
   if (which)
-    attention_tc_kernel<Act::E4M3><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, err);
+    attention_tc_kernel<Act::E4M3><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, lse,
+                                                                      err);
   else
-    attention_tc_kernel<Act::BF16><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, err);
+    attention_tc_kernel<Act::BF16><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, lse,
+                                                                      err);
   return cudaGetLastError();
 }
 

@@ -239,6 +239,22 @@ __device__ __forceinline__ uint64_t make_sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand tile with the 128-byte swizzle: rows of
+// 128 bytes hold 64 consecutive M (or N) elements of one K index; 8 such rows (8 K indices)
+// form a 1024-byte swizzle atom, consecutive atoms along K are 1024 bytes apart (stride
+// byte offset) and the next 64 elements along M (or N) start lbo bytes further (leading
+// byte offset).  This is the canonical MN-major SW128 layout of the tcgen05 matrix
+// descriptors; one K step of 16 bf16 values is two atoms, +2048 bytes.
+__device__ __forceinline__ uint64_t make_sw128_mn_desc(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;      // leading byte offset: next 64 along M/N
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: next 8 along K
+  d |= (uint64_t)1u << 46;                          // descriptor version (tcgen05)
+  d |= (uint64_t)2u << 61;                          // swizzle mode: 128 B
+  return d;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs (kind::f16), fp32 accumulate, 1 CTA.
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -303,6 +319,10 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Operand majorness bits of the instruction descriptor: A (bit 15) or B (bit 16) stored
+// MN-major instead of K-major.
+constexpr uint32_t kIdescAMn = 1u << 15;
+constexpr uint32_t kIdescBMn = 1u << 16;
 // Instruction descriptor, kind::f8f6f4: D f32, A/B E4M3, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);

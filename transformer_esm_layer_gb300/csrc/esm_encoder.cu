@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <unordered_map>
 #include <vector>
@@ -69,7 +70,13 @@ struct esm_encoder {
   std::vector<uint8_t> layer_fp8;  // per layer: 1 = E4M3 GEMMs (FP8 handles only)
   float* d_fp8 = nullptr;        // scales [L*8] | history [L*8*len] | amax [L*8]
   size_t fp8_floats = 0;
-  std::unordered_map<MapKey, CUtensorMap, MapKeyHash> maps;
+  // Tensor-map cache.  When it grows past its cap the current generation is retired, not
+  // freed: maps handed out earlier in the same call stay valid until the next turnover.
+  std::unordered_map<MapKey, CUtensorMap, MapKeyHash> maps, retired_maps;
+  // the last training forward: its sizes and buffers, which the backward must be given
+  int train_T = 0, train_B = 0, train_items = 0;
+  const void* train_buf = nullptr;
+  const void* train_ws = nullptr;
   // measurement hooks
   bool profiling = false;
   long long launches[ESM_PROFILE_CLASSES] = {};
@@ -147,7 +154,10 @@ struct esm_encoder {
     if (it != maps.end()) return &it->second;
     EncodeTiledFn fn = encode_fn();
     if (!fn) return nullptr;
-    if (maps.size() > 4096) maps.clear();
+    if (maps.size() > 4096) {
+      retired_maps = std::move(maps);
+      maps = std::unordered_map<MapKey, CUtensorMap, MapKeyHash>();
+    }
     CUtensorMap m;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * elem};
@@ -236,9 +246,12 @@ bool weights_ok(const esm_encoder* h, const esm_weights* w) {
 }
 
 // One GEMM of a layer.  A: activation [M, K]; B: weight [N, K].
+// rope_cols >= 0 overrides the RoPE column range of ESM_EPI_QKV_ROPE (0: plain bias, bf16
+// out); res_in != NULL makes ESM_EPI_RESIDUAL read its residual there instead of from out.
 esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, const void* B, const void* bias, void* out,
                     const int32_t* pos_id, int M, int N, int K, bool fp8, Act out_act, const float* a_scale,
-                    const float* b_scale, const float* o_scale, float* o_amax, cudaStream_t st) {
+                    const float* b_scale, const float* o_scale, float* o_amax, cudaStream_t st, int rope_cols = -1,
+                    const void* res_in = nullptr) {
   EpiArgs ea{};
   ea.bias = bias;
   ea.bias_f32 = !h->bf16_params();
@@ -252,6 +265,8 @@ esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, co
   ea.b_scale = b_scale;
   ea.o_scale = o_scale;
   ea.o_amax = o_amax;
+  ea.res_in = res_in;
+  if (rope_cols >= 0) ea.rope_cols = rope_cols;
   if (M <= 0) return ESM_OK;
   if (h->cfg.precision == ESM_FP32) {
     PROF(h, cls, st, epi == ESM_EPI_QKV_ROPE ? 2 : 1,
@@ -383,6 +398,285 @@ bool config_ok(const esm_config* c) {
     return c->hidden <= 4096 * 4;
   }
   return false;
+}
+
+// ------------------------------------------------------------------ training (backward)
+// Buffer of a training forward: every activation the backward reads, per layer, plus the
+// backward's scratch.  Per-layer tensors are slabs of layers (x: layers + 1) of one size.
+struct TrainLayout {
+  size_t tok, x, xmid, y1, qkv, o, lse, y2, z, u;                        // bases
+  size_t sx, sy, sqkv, slse, sz;                                         // slab strides
+  size_t dx, dxb, dy, du, dz, dob, dqkv, dqacc, dsum, stats, partial, split, embp;  // scratch
+  size_t split_floats, total;
+};
+
+constexpr int kMaxKSplit = 8;
+
+TrainLayout train_layout(const esm_config& c, int Tm) {
+  TrainLayout L{};
+  const size_t T = Tm > 0 ? Tm : 1, d = c.hidden, f = c.ffn, H = c.heads, nl = c.num_layers > 0 ? c.num_layers : 0;
+  L.sx = align256(4 * T * d);
+  L.sy = align256(2 * T * d);
+  L.sqkv = align256(2 * T * 3 * d);
+  L.slse = align256(4 * T * H);
+  L.sz = align256(2 * T * f);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  L.tok = take(4 * T);
+  L.x = take(L.sx * (nl + 1));
+  L.xmid = take(L.sx * nl);
+  L.y1 = take(L.sy * nl);
+  L.qkv = take(L.sqkv * nl);
+  L.o = take(L.sy * nl);
+  L.lse = take(L.slse * nl);
+  L.y2 = take(L.sy * nl);
+  L.z = take(L.sz * nl);
+  L.u = take(L.sz * nl);
+  L.dx = take(4 * T * d);
+  L.dxb = take(2 * T * d);
+  L.dy = take(4 * T * d);
+  L.du = take(4 * T * f);
+  L.dz = take(2 * T * f);
+  L.dob = take(2 * T * d);
+  L.dqkv = take(2 * T * 3 * d);
+  L.dqacc = take(4 * T * d);
+  L.dsum = take(4 * T * H);
+  L.stats = take(8 * T);
+  const size_t widest = std::max(3 * d, f);
+  L.partial = take(4 * bwd_partial_floats((int)T, (int)widest));
+  L.split_floats = (size_t)kMaxKSplit * std::max(f * d, 3 * d * d);
+  L.split = take(4 * L.split_floats);
+  L.embp = take(4 * emb_bwd_partial_floats((int)T, c.vocab, (int)d));
+  L.total = off;
+  return L;
+}
+
+// Split of the token reduction of a weight gradient: tiles x splits work items over the
+// clusters, fewest rounds per unit of work (ties to fewer splits).
+int choose_ksplit(int tiles, int kb_total, int clusters) {
+  int best = 1;
+  double best_cost = 1e30;
+  for (int ks = 1; ks <= kMaxKSplit && ks <= kb_total; ++ks) {
+    const double rounds = (double)((tiles * ks + clusters - 1) / clusters);
+    const double cost = rounds / ks + 0.02 * ks;  // small charge for the partial-sum pass
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = ks;
+    }
+  }
+  return best;
+}
+
+// out[M, K] = dY[M, N] W with W stored [N, K] (bf16); fp32 or bf16 out.
+esm_status run_dgrad(esm_encoder* h, const void* dY, const void* W, void* out, bool out_bf16, int M, int N, int K,
+                     cudaStream_t st) {
+  if (M <= 0) return ESM_OK;
+  const CUtensorMap* ma = h->map(dY, (uint64_t)M, (uint64_t)N, (uint32_t)gemm_tc_a_box_rows(), 2);
+  const CUtensorMap* mb = h->map(W, (uint64_t)N, (uint64_t)K, (uint32_t)gemm_tc_mn_box_rows(), 2);
+  const CUtensorMap* mo = h->map(out, (uint64_t)M, (uint64_t)K, (uint32_t)gemm_tc_out_box_rows(), out_bf16 ? 2u : 4u);
+  if (!ma || !mb || !mo) return ESM_ERR_CUDA;
+  EpiArgs ea{};
+  ea.out = out;
+  ea.rope_cols = 0;
+  cudaError_t e;
+  PROF(h, P_OTHER, st, 1,
+       e = launch_gemm_tc_bwd(out_bf16 ? GemmBwd::DGRAD_BF16 : GemmBwd::DGRAD_F32, ma, mb, mo, M, K, N, 1, ea,
+                              h->num_sms, h->d_err, st));
+  return cuda_status(e);
+}
+
+// dW[N, K] = dY^T X over M rows: dY [M, N], X [M, K] (bf16); fp32 out.  split: scratch of
+// split_floats floats for the split-K partial products.
+esm_status run_wgrad(esm_encoder* h, const void* dY, const void* X, float* dW, int M, int N, int K, float* split,
+                     size_t split_floats, cudaStream_t st) {
+  if (M <= 0) return cuda_status(cudaMemsetAsync(dW, 0, sizeof(float) * (size_t)N * K, st));
+  const int tiles = (N / 256) * (K / 256);
+  const int kb_total = (M + 63) / 64;
+  int ks = choose_ksplit(tiles, kb_total, gemm_tc_max_clusters(h->num_sms));
+  while (ks > 1 && (size_t)ks * N * K > split_floats) --ks;
+  ks = (kb_total + (kb_total + ks - 1) / ks - 1) / ((kb_total + ks - 1) / ks);  // no empty split
+  float* out = ks > 1 ? split : dW;
+  const CUtensorMap* ma = h->map(dY, (uint64_t)M, (uint64_t)N, (uint32_t)gemm_tc_mn_box_rows(), 2);
+  const CUtensorMap* mb = h->map(X, (uint64_t)M, (uint64_t)K, (uint32_t)gemm_tc_mn_box_rows(), 2);
+  const CUtensorMap* mo = h->map(out, (uint64_t)ks * N, (uint64_t)K, (uint32_t)gemm_tc_out_box_rows(), 4);
+  if (!ma || !mb || !mo) return ESM_ERR_CUDA;
+  EpiArgs ea{};
+  ea.out = out;
+  ea.rope_cols = 0;
+  cudaError_t e;
+  PROF(h, P_OTHER, st, 1, e = launch_gemm_tc_bwd(GemmBwd::WGRAD_F32, ma, mb, mo, N, K, M, ks, ea, h->num_sms, h->d_err, st));
+  if (e != cudaSuccess) return ESM_ERR_CUDA;
+  if (ks > 1) PROF(h, P_OTHER, st, 1, launch_reduce_splits(split, ks, (size_t)N * K, dW, st));
+  return cuda_status(cudaGetLastError());
+}
+
+bool grads_ok(const esm_encoder* h, const esm_grads* g) {
+  if (!g || !g->emb || !aligned(g->emb, 16)) return false;
+  float* const* arrs[] = {g->ln1_g, g->ln1_b, g->w_qkv, g->b_qkv, g->w_o, g->b_o,
+                          g->ln2_g, g->ln2_b, g->w_1,   g->b_1,   g->w_2, g->b_2};
+  for (auto a : arrs) {
+    if (!a) return false;
+    for (int l = 0; l < h->cfg.num_layers; ++l)
+      if (!a[l] || !aligned(a[l], 16)) return false;
+  }
+  if (h->cfg.final_ln && (!g->lnf_g || !g->lnf_b)) return false;
+  return true;
+}
+
+esm_status train_forward_impl(esm_encoder* h, const esm_weights* w, const int32_t* tok, const int32_t* cu, int B, int T,
+                              int max_seqlen, void* out, void* train, void* ws, size_t ws_bytes, cudaStream_t st) {
+  WsLayout L;
+  esm_status s = check_ws(h, T, B, ws, ws_bytes, &L);
+  if (s != ESM_OK) return s;
+  const esm_config& c = h->cfg;
+  const TrainLayout R = train_layout(c, T);
+  uint8_t* tb = static_cast<uint8_t*>(train);
+  PackBuffers pb = pack_buffers(ws, L);
+  if (cudaMemsetAsync(pb.pos_id, 0, 4 * (size_t)T, st) != cudaSuccess) return ESM_ERR_CUDA;
+  if (cudaMemsetAsync(pb.seg_id, 0, 4 * (size_t)T, st) != cudaSuccess) return ESM_ERR_CUDA;
+  if (cudaMemcpyAsync(tb + R.tok, tok, 4 * (size_t)T, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return ESM_ERR_CUDA;
+  const int d = c.hidden, f = c.ffn, H = c.heads;
+  {
+    ProfScope _ps(h, P_OTHER, st, 3);
+    launch_pack_index(cu, B, T, max_seqlen, c.max_positions, pb, h->d_err, st);
+    launch_attn_worklist(B, L.max_items, kAttnQTileTc, pb, st);
+    launch_embed(tok, T, w->emb, false, c.vocab, d, c.emb_scale, reinterpret_cast<float*>(tb + R.x), h->d_err, st);
+  }
+  for (int l = 0; l < c.num_layers; ++l) {
+    float* x = reinterpret_cast<float*>(tb + R.x + R.sx * l);
+    float* xmid = reinterpret_cast<float*>(tb + R.xmid + R.sx * l);
+    float* xnext = reinterpret_cast<float*>(tb + R.x + R.sx * (l + 1));
+    void* y1 = tb + R.y1 + R.sy * l;
+    void* qkv = tb + R.qkv + R.sqkv * l;
+    void* o = tb + R.o + R.sy * l;
+    float* lse = reinterpret_cast<float*>(tb + R.lse + R.slse * l);
+    void* y2 = tb + R.y2 + R.sy * l;
+    void* z = tb + R.z + R.sz * l;
+    void* u = tb + R.u + R.sz * l;
+    PROF(h, P_LN, st, 1,
+         launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], false, y1, Act::BF16, T, d, c.ln_eps, nullptr, nullptr, nullptr,
+                          nullptr, nullptr, st));
+    s = run_gemm(h, P_QKV, ESM_EPI_QKV_ROPE, y1, w->w_qkv[l], w->b_qkv[l], qkv, pb.pos_id, T, 3 * d, d, false,
+                 Act::BF16, nullptr, nullptr, nullptr, nullptr, st);
+    if (s != ESM_OK) return s;
+    {
+      ProfScope _ps(h, P_ATTN, st, 1);
+      const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
+      if (!tq) return ESM_ERR_CUDA;
+      if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st, lse) !=
+          cudaSuccess)
+        return ESM_ERR_CUDA;
+    }
+    s = run_gemm(h, P_OPROJ, ESM_EPI_RESIDUAL, o, w->w_o[l], w->b_o[l], xmid, nullptr, T, d, d, false, Act::F32,
+                 nullptr, nullptr, nullptr, nullptr, st, -1, x);
+    if (s != ESM_OK) return s;
+    PROF(h, P_LN, st, 1,
+         launch_layernorm(xmid, w->ln2_g[l], w->ln2_b[l], false, y2, Act::BF16, T, d, c.ln_eps, nullptr, nullptr,
+                          nullptr, nullptr, nullptr, st));
+    // fc1 keeps its pre-activation z for GELU'(z); u = GELU(z) feeds fc2
+    s = run_gemm(h, P_FC1, ESM_EPI_QKV_ROPE, y2, w->w_1[l], w->b_1[l], z, nullptr, T, f, d, false, Act::BF16, nullptr,
+                 nullptr, nullptr, nullptr, st, 0);
+    if (s != ESM_OK) return s;
+    PROF(h, P_OTHER, st, 1,
+         launch_gelu_fwd(static_cast<const __nv_bfloat16*>(z), static_cast<__nv_bfloat16*>(u), (size_t)T * f, st));
+    s = run_gemm(h, P_FC2, ESM_EPI_RESIDUAL, u, w->w_2[l], w->b_2[l], xnext, nullptr, T, d, f, false, Act::F32, nullptr,
+                 nullptr, nullptr, nullptr, st, -1, xmid);
+    if (s != ESM_OK) return s;
+  }
+  const float* xl = reinterpret_cast<const float*>(tb + R.x + R.sx * c.num_layers);
+  if (c.final_ln)
+    PROF(h, P_LN, st, 1,
+         launch_layernorm(xl, w->lnf_g, w->lnf_b, false, out, Act::BF16, T, d, c.ln_eps, nullptr, nullptr, nullptr,
+                          nullptr, nullptr, st));
+  else
+    PROF(h, P_OTHER, st, 1, launch_copy_out(xl, out, Act::BF16, T, d, nullptr, nullptr, nullptr, st));
+  h->train_T = T;
+  h->train_B = B;
+  h->train_items = L.max_items;
+  h->train_buf = train;
+  h->train_ws = ws;
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status backward_impl(esm_encoder* h, const esm_weights* w, const float* d_out, const esm_grads* g, void* train,
+                         void* ws, cudaStream_t st) {
+  const esm_config& c = h->cfg;
+  const int T = h->train_T, d = c.hidden, f = c.ffn, H = c.heads;
+  const TrainLayout R = train_layout(c, T);
+  const WsLayout L = h->layout(T, h->train_B);
+  PackBuffers pb = pack_buffers(ws, L);
+  uint8_t* tb = static_cast<uint8_t*>(train);
+  float* dx = reinterpret_cast<float*>(tb + R.dx);
+  __nv_bfloat16* dxb = reinterpret_cast<__nv_bfloat16*>(tb + R.dxb);
+  float* dy = reinterpret_cast<float*>(tb + R.dy);
+  float* du = reinterpret_cast<float*>(tb + R.du);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(tb + R.dz);
+  __nv_bfloat16* dob = reinterpret_cast<__nv_bfloat16*>(tb + R.dob);
+  __nv_bfloat16* dqkv = reinterpret_cast<__nv_bfloat16*>(tb + R.dqkv);
+  float* dqacc = reinterpret_cast<float*>(tb + R.dqacc);
+  float* dsum = reinterpret_cast<float*>(tb + R.dsum);
+  float2* stats = reinterpret_cast<float2*>(tb + R.stats);
+  float* partial = reinterpret_cast<float*>(tb + R.partial);
+  float* split = reinterpret_cast<float*>(tb + R.split);
+  float* embp = reinterpret_cast<float*>(tb + R.embp);
+  esm_status s;
+  // final LayerNorm (or the identity)
+  const float* xl = reinterpret_cast<const float*>(tb + R.x + R.sx * c.num_layers);
+  if (c.final_ln) {
+    PROF(h, P_LN, st, 4,
+         launch_ln_bwd(xl, w->lnf_g, false, d_out, nullptr, dx, stats, g->lnf_g, g->lnf_b, partial, T, d, c.ln_eps, st));
+  } else if (cudaMemcpyAsync(dx, d_out, 4 * (size_t)T * d, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
+    return ESM_ERR_CUDA;
+  }
+  for (int l = c.num_layers - 1; l >= 0; --l) {
+    const float* x = reinterpret_cast<const float*>(tb + R.x + R.sx * l);
+    const float* xmid = reinterpret_cast<const float*>(tb + R.xmid + R.sx * l);
+    const void* y1 = tb + R.y1 + R.sy * l;
+    const void* qkv = tb + R.qkv + R.sqkv * l;
+    const void* o = tb + R.o + R.sy * l;
+    const float* lse = reinterpret_cast<const float*>(tb + R.lse + R.slse * l);
+    const void* y2 = tb + R.y2 + R.sy * l;
+    const void* z = tb + R.z + R.sz * l;
+    const void* u = tb + R.u + R.sz * l;
+    // ---- MLP block: x_{l+1} = xmid + GELU(LN2(xmid) W1^T + b1) W2^T + b2
+    PROF(h, P_OTHER, st, 2, launch_colsum(dx, false, T, d, g->b_2[l], partial, dxb, st));
+    if ((s = run_wgrad(h, dxb, u, g->w_2[l], T, d, f, split, R.split_floats, st)) != ESM_OK) return s;
+    if ((s = run_dgrad(h, dxb, w->w_2[l], du, false, T, d, f, st)) != ESM_OK) return s;
+    PROF(h, P_OTHER, st, 1,
+         launch_gelu_bwd(du, static_cast<const __nv_bfloat16*>(z), dz, (size_t)T * f, st));
+    PROF(h, P_OTHER, st, 2, launch_colsum(dz, true, T, f, g->b_1[l], partial, nullptr, st));
+    if ((s = run_wgrad(h, dz, y2, g->w_1[l], T, f, d, split, R.split_floats, st)) != ESM_OK) return s;
+    if ((s = run_dgrad(h, dz, w->w_1[l], dy, false, T, f, d, st)) != ESM_OK) return s;
+    PROF(h, P_LN, st, 4,
+         launch_ln_bwd(xmid, w->ln2_g[l], false, dy, dx, dx, stats, g->ln2_g[l], g->ln2_b[l], partial, T, d, c.ln_eps,
+                       st));
+    // ---- attention block: xmid = x + Attn(LN1(x)) Wo^T + bo
+    PROF(h, P_OTHER, st, 2, launch_colsum(dx, false, T, d, g->b_o[l], partial, dxb, st));
+    if ((s = run_wgrad(h, dxb, o, g->w_o[l], T, d, d, split, R.split_floats, st)) != ESM_OK) return s;
+    if ((s = run_dgrad(h, dxb, w->w_o[l], dob, true, T, d, d, st)) != ESM_OK) return s;
+    {
+      ProfScope _ps(h, P_ATTN, st, 4);
+      const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
+      const CUtensorMap* td = h->map(dob, (uint64_t)T, (uint64_t)d, 128, 2);
+      if (!tq || !td) return ESM_ERR_CUDA;
+      if (launch_attention_bwd_tc(tq, td, static_cast<const __nv_bfloat16*>(o), dob, lse, dsum, dqacc, dqkv, T, d, H,
+                                  h->train_items, pb, h->d_rope, c.max_positions, h->num_sms, h->d_err,
+                                  st) != cudaSuccess)
+        return ESM_ERR_CUDA;
+    }
+    PROF(h, P_OTHER, st, 2, launch_colsum(dqkv, true, T, 3 * d, g->b_qkv[l], partial, nullptr, st));
+    if ((s = run_wgrad(h, dqkv, y1, g->w_qkv[l], T, 3 * d, d, split, R.split_floats, st)) != ESM_OK) return s;
+    if ((s = run_dgrad(h, dqkv, w->w_qkv[l], dy, false, T, 3 * d, d, st)) != ESM_OK) return s;
+    PROF(h, P_LN, st, 4,
+         launch_ln_bwd(x, w->ln1_g[l], false, dy, dx, dx, stats, g->ln1_g[l], g->ln1_b[l], partial, T, d, c.ln_eps, st));
+  }
+  PROF(h, P_OTHER, st, 2,
+       launch_emb_bwd(dx, reinterpret_cast<const int32_t*>(tb + R.tok), T, d, c.vocab, c.emb_scale, embp, g->emb, st));
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
@@ -715,6 +1009,174 @@ esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu
     if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st) != cudaSuccess)
       return ESM_ERR_CUDA;
   }
+  return cuda_status(cudaGetLastError());
+}
+
+// ------------------------------------------------------------------ training
+esm_status esm_encoder_train_buffer_size(const esm_encoder_t* h, int max_tokens, size_t* bytes) {
+  if (!h || !bytes || max_tokens < 0) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+  *bytes = train_layout(h->cfg, max_tokens).total;
+  return ESM_OK;
+}
+
+esm_status esm_encoder_forward_train(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids,
+                                     const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                                     void* hidden_out, void* train_buf, size_t train_bytes, void* workspace,
+                                     size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || total_tokens <= 0 || num_seqs <= 0) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+  if (!token_ids || !cu_seqlens || !hidden_out || !aligned(hidden_out, 16)) return ESM_ERR_INVALID_ARG;
+  if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
+  if (!weights_ok(h, w)) return ESM_ERR_INVALID_ARG;
+  if (!train_buf || !aligned(train_buf, 256) || train_bytes < train_layout(h->cfg, total_tokens).total)
+    return ESM_ERR_WORKSPACE;
+  h->train_buf = nullptr;  // valid again only once this forward is fully enqueued
+  return train_forward_impl(h, w, token_ids, cu_seqlens, num_seqs, total_tokens, max_seqlen, hidden_out, train_buf,
+                            workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+esm_status esm_encoder_backward(esm_encoder_t* h, const esm_weights* w, const float* d_hidden_out,
+                                const esm_grads* grads, void* train_buf, size_t train_bytes, void* workspace,
+                                size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || !d_hidden_out || !aligned(d_hidden_out, 16)) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+  if (!weights_ok(h, w) || !grads_ok(h, grads)) return ESM_ERR_INVALID_ARG;
+  if (h->train_T <= 0 || train_buf != h->train_buf || workspace != h->train_ws) return ESM_ERR_INVALID_ARG;
+  if (train_bytes < train_layout(h->cfg, h->train_T).total) return ESM_ERR_WORKSPACE;
+  if (workspace_bytes < h->layout(h->train_T, h->train_B).total) return ESM_ERR_WORKSPACE;
+  return backward_impl(h, w, d_hidden_out, grads, train_buf, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+esm_status esm_op_gemm_dgrad(esm_encoder_t* h, const void* dY, const void* W, void* out, int out_bf16, int M, int N,
+                             int K, esm_stream_t stream) {
+  if (!h || !dY || !W || !out || M < 0 || N <= 0 || K <= 0) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision == ESM_FP32) return ESM_ERR_UNSUPPORTED;
+  if (N % 64 || K % 256 || !aligned(dY, 16) || !aligned(W, 16) || !aligned(out, 16)) return ESM_ERR_INVALID_ARG;
+  return run_dgrad(h, dY, W, out, out_bf16 != 0, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+esm_status esm_op_gemm_wgrad_workspace_size(const esm_encoder_t* h, int N, int K, size_t* bytes) {
+  if (!h || !bytes || N <= 0 || K <= 0) return ESM_ERR_INVALID_ARG;
+  *bytes = sizeof(float) * (size_t)kMaxKSplit * N * K;
+  return ESM_OK;
+}
+
+esm_status esm_op_gemm_wgrad(esm_encoder_t* h, const void* dY, const void* X, float* dW, int M, int N, int K,
+                             void* workspace, size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || !dW || M < 0 || N <= 0 || K <= 0 || (M > 0 && (!dY || !X))) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision == ESM_FP32) return ESM_ERR_UNSUPPORTED;
+  if (N % 256 || K % 256 || !aligned(dY, 16) || !aligned(X, 16) || !aligned(dW, 16)) return ESM_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 256)) return ESM_ERR_WORKSPACE;
+  return run_wgrad(h, dY, X, dW, M, N, K, static_cast<float*>(workspace), workspace ? workspace_bytes / 4 : 0,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+static size_t ln_bwd_ws_bytes(int rows, int cols, size_t* off_partial) {
+  *off_partial = align256(8 * (size_t)(rows > 0 ? rows : 1));
+  return *off_partial + align256(4 * bwd_partial_floats(rows, cols));
+}
+
+esm_status esm_op_layernorm_backward_workspace_size(const esm_encoder_t* h, int rows, int cols, size_t* bytes) {
+  if (!h || !bytes || rows < 0 || cols <= 0) return ESM_ERR_INVALID_ARG;
+  size_t off;
+  *bytes = ln_bwd_ws_bytes(rows, cols, &off);
+  return ESM_OK;
+}
+
+esm_status esm_op_layernorm_backward(esm_encoder_t* h, const float* x, const void* gamma, const float* dy,
+                                     const float* dres, float* dx, float* dgamma, float* dbeta, int rows, int cols,
+                                     void* workspace, size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || !x || !gamma || !dy || !dx || !dgamma || !dbeta || rows < 0 || cols <= 0 || cols % 4) return ESM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(dx, 16) || (dres && !aligned(dres, 16)) || !aligned(gamma, 16))
+    return ESM_ERR_INVALID_ARG;
+  size_t off;
+  const size_t need = ln_bwd_ws_bytes(rows, cols, &off);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ESM_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  launch_ln_bwd(x, gamma, !h->bf16_params(), dy, dres, dx, reinterpret_cast<float2*>(ws),
+                dgamma, dbeta, reinterpret_cast<float*>(ws + off), rows, cols, h->cfg.ln_eps,
+                reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+static size_t attn_bwd_ws_bytes(const esm_encoder* h, int T, int B, WsLayout* L, size_t* off_dsum, size_t* off_dq) {
+  *L = h->layout(T, B);
+  *off_dsum = L->total;
+  *off_dq = *off_dsum + align256(4 * (size_t)(T > 0 ? T : 1) * h->cfg.heads);
+  return *off_dq + align256(4 * (size_t)(T > 0 ? T : 1) * h->cfg.hidden);
+}
+
+esm_status esm_op_attention_backward_workspace_size(const esm_encoder_t* h, int total_tokens, int num_seqs,
+                                                    size_t* bytes) {
+  if (!h || !bytes || total_tokens < 0 || num_seqs < 0) return ESM_ERR_INVALID_ARG;
+  WsLayout L;
+  size_t a, b;
+  *bytes = attn_bwd_ws_bytes(h, total_tokens, num_seqs, &L, &a, &b);
+  return ESM_OK;
+}
+
+// Index the batch into the workspace's pack buffers (positions, segments, work list).
+static esm_status index_batch(esm_encoder* h, const int32_t* cu, int B, int T, int max_seqlen, const WsLayout& L,
+                              void* ws, cudaStream_t st) {
+  PackBuffers pb = pack_buffers(ws, L);
+  if (cudaMemsetAsync(pb.pos_id, 0, 4 * (size_t)T, st) != cudaSuccess ||
+      cudaMemsetAsync(pb.seg_id, 0, 4 * (size_t)T, st) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  launch_pack_index(cu, B, T, max_seqlen, h->cfg.max_positions, pb, h->d_err, st);
+  launch_attn_worklist(B, L.max_items, kAttnQTileTc, pb, st);
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status esm_op_attention_train(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,
+                                  int total_tokens, int max_seqlen, void* o, float* lse, void* workspace,
+                                  size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || !qkv || !cu_seqlens || !o || !lse || num_seqs <= 0 || total_tokens < 0) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision == ESM_FP32) return ESM_ERR_UNSUPPORTED;
+  if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
+  if (total_tokens == 0) return ESM_OK;
+  WsLayout L;
+  esm_status s = check_ws(h, total_tokens, num_seqs, workspace, workspace_bytes, &L);
+  if (s != ESM_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((s = index_batch(h, cu_seqlens, num_seqs, total_tokens, max_seqlen, L, workspace, st)) != ESM_OK) return s;
+  const int d = h->cfg.hidden;
+  const CUtensorMap* tq = h->map(qkv, (uint64_t)total_tokens, (uint64_t)3 * d, 128, 2);
+  if (!tq) return ESM_ERR_CUDA;
+  if (launch_attention_tc(tq, o, Act::BF16, d, h->cfg.heads, L.max_items, pack_buffers(workspace, L), nullptr, nullptr,
+                          h->d_err, st, lse) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
+}
+
+esm_status esm_op_attention_backward(esm_encoder_t* h, const void* qkv, const void* o, const float* lse,
+                                     const void* d_o, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                                     int max_seqlen, void* dqkv, void* workspace, size_t workspace_bytes,
+                                     esm_stream_t stream) {
+  if (!h || !qkv || !o || !lse || !d_o || !cu_seqlens || !dqkv || num_seqs <= 0 || total_tokens < 0)
+    return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision == ESM_FP32) return ESM_ERR_UNSUPPORTED;
+  if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
+  if (!aligned(qkv, 16) || !aligned(o, 16) || !aligned(d_o, 16) || !aligned(dqkv, 16)) return ESM_ERR_INVALID_ARG;
+  if (total_tokens == 0) return ESM_OK;
+  WsLayout L;
+  size_t off_dsum, off_dq;
+  const size_t need = attn_bwd_ws_bytes(h, total_tokens, num_seqs, &L, &off_dsum, &off_dq);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ESM_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  esm_status s = index_batch(h, cu_seqlens, num_seqs, total_tokens, max_seqlen, L, workspace, st);
+  if (s != ESM_OK) return s;
+  const int d = h->cfg.hidden, T = total_tokens;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
+  const CUtensorMap* td = h->map(d_o, (uint64_t)T, (uint64_t)d, 128, 2);
+  if (!tq || !td) return ESM_ERR_CUDA;
+  if (launch_attention_bwd_tc(tq, td, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse,
+                              reinterpret_cast<float*>(ws + off_dsum), reinterpret_cast<float*>(ws + off_dq),
+                              static_cast<__nv_bfloat16*>(dqkv), T, d, h->cfg.heads, L.max_items,
+                              pack_buffers(workspace, L), nullptr, h->cfg.max_positions, h->num_sms, h->d_err,
+                              st) != cudaSuccess)
+    return ESM_ERR_CUDA;
   return cuda_status(cudaGetLastError());
 }
 

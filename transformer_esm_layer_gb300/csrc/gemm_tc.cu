@@ -145,7 +145,7 @@ __device__ __forceinline__ void st_shared_v4(uint8_t* base, uint32_t off, uint4 
 // four whole 128-byte rows.  Rows at or beyond M are zero-filled / not written.
 __device__ __forceinline__ void residual_rows_async(const EpiArgs& ea, uint8_t* buf, int q, int lane, int row0,
                                                     int M, int N, int col) {
-  const float* x = static_cast<const float*>(ea.out);
+  const float* x = static_cast<const float*>(ea.res_in ? ea.res_in : ea.out);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int rr = q * 32 + 4 * i + (lane >> 3);
@@ -244,11 +244,19 @@ struct Chunk {
   static constexpr int kPerHalf = (BN / 2) / kCols;  // 4, 2 or 1
 };
 
-template <int EPI, bool FP8, Act OUT>
+// AMN / BMN: the operand is stored MN-major (its M or N index contiguous, the reduction
+// index the row), as the backward products need: A = dY^T and B = X for a weight gradient
+// (reduction over the tokens), B = W for an input gradient (reduction over the output
+// features).  Each 128-row operand stage is then two 64 x 64 TMA boxes side by side.
+// ksplit > 1 splits the K loop into ksplit ranges of kb_per K-slices; range s of tile t is
+// work item s * num_tiles + t and writes output rows s * M.. (a [ksplit * M, N] partial
+// buffer that the caller sums).
+template <int EPI, bool FP8, Act OUT, bool AMN, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmO, int M, int N, int K, int full_tiles, int num_tiles,
-                   EpiArgs ea, unsigned* err) {
+                   const __grid_constant__ CUtensorMap tmO, int M, int N, int kb_total, int kb_per, int ksplit,
+                   int full_tiles, int num_tiles, EpiArgs ea, unsigned* err) {
+  static_assert(!(FP8 && (AMN || BMN)), "MN-major operands are bf16 only");
   using CH = Chunk<EPI, OUT>;
   constexpr int S = Plan<EPI>::kStages;
   constexpr int NB = Plan<EPI>::kEBufs;
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int unit = (int)(blockIdx.x >> 1);  // cluster index
   const int units = (int)(gridDim.x >> 1);
   const int n_tiles = N / BN;
-  const int kb_count = K / (FP8 ? 128 : 64);
+  const int num_work = num_tiles * ksplit;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -300,11 +308,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int issues = 0;
-      for (int tile = unit; tile < num_tiles && !sm->abort; tile += units) {
+      for (int wk = unit; wk < num_work && !sm->abort; wk += units) {
+        const int tile = wk % num_tiles, ks = wk / num_tiles;
+        const int kb0 = ks * kb_per, kb1 = min(kb_total, kb0 + kb_per);
         const TileXY tx = tile_xy(tile, n_tiles, full_tiles);
         const int m0 = tx.m * TILE_M + (int)rank * BM;
         const int n0 = tx.n0 + (int)rank * (tx.bn / 2);  // a half-width tile loads 64 surplus rows
-        for (int kb = 0; kb < kb_count; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&sm->empty[stage], phase ^ 1)) {
             latch_error(err, ERRBIT_TIMEOUT);
             sm->abort = 1;
@@ -315,8 +325,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           // bytes of the whole pair.
           if (leader) mbar_arrive_expect_tx(&sm->full[stage], 2 * (A_STAGE + B_STAGE));
           const uint32_t bar = map_to_rank(&sm->full[stage], 0);
-          tma_load_2d_pair(sA + stage * A_STAGE, &tmA, kx, m0, bar);
-          tma_load_2d_pair(sB + stage * B_STAGE, &tmB, kx, n0, bar);
+          if (AMN) {
+            tma_load_2d_pair(sA + stage * A_STAGE, &tmA, m0, kx, bar);
+            tma_load_2d_pair(sA + stage * A_STAGE + A_STAGE / 2, &tmA, m0 + 64, kx, bar);
+          } else {
+            tma_load_2d_pair(sA + stage * A_STAGE, &tmA, kx, m0, bar);
+          }
+          if (BMN) {
+            tma_load_2d_pair(sB + stage * B_STAGE, &tmB, n0, kx, bar);
+            tma_load_2d_pair(sB + stage * B_STAGE + B_STAGE / 2, &tmB, n0 + 64, kx, bar);
+          } else {
+            tma_load_2d_pair(sB + stage * B_STAGE, &tmB, kx, n0, bar);
+          }
           ++issues;
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
@@ -337,8 +357,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc_full = FP8 ? idesc_e4m3(TILE_M, BN) : idesc_bf16(TILE_M, BN);
-      constexpr uint32_t idesc_half = FP8 ? idesc_e4m3(TILE_M, BN / 2) : idesc_bf16(TILE_M, BN / 2);
+      constexpr uint32_t kMajor = (AMN ? kIdescAMn : 0u) | (BMN ? kIdescBMn : 0u);
+      constexpr uint32_t idesc_full = (FP8 ? idesc_e4m3(TILE_M, BN) : idesc_bf16(TILE_M, BN)) | kMajor;
+      constexpr uint32_t idesc_half = (FP8 ? idesc_e4m3(TILE_M, BN / 2) : idesc_bf16(TILE_M, BN / 2)) | kMajor;
+      // K step of one MMA (32 bytes of K): +32 bytes inside a K-major row, two 1024-byte
+      // atoms (+2048 bytes) in an MN-major tile; in descriptor units of 16 bytes.
+      constexpr uint64_t kStepA = AMN ? 128 : 2, kStepB = BMN ? 128 : 2;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -346,9 +370,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Descriptors of stage 0; a stage adds its byte offset >> 4 to the start-address field
       // (every shared address here is below 256 KB, so the 14-bit field cannot carry), and
       // each 32-byte step of K inside the 128-byte row adds 2.
-      const uint64_t adesc0 = make_sw128_desc(smem_u32(sA));
-      const uint64_t bdesc0 = make_sw128_desc(smem_u32(sB));
-      for (int tile = unit; tile < num_tiles && !sm->abort; tile += units) {
+      const uint64_t adesc0 = AMN ? make_sw128_mn_desc(smem_u32(sA), A_STAGE / 2) : make_sw128_desc(smem_u32(sA));
+      const uint64_t bdesc0 = BMN ? make_sw128_mn_desc(smem_u32(sB), B_STAGE / 2) : make_sw128_desc(smem_u32(sB));
+      for (int wk = unit; wk < num_work && !sm->abort; wk += units) {
+        const int tile = wk % num_tiles, ks = wk / num_tiles;
+        const int kb_count = min(kb_total, (ks + 1) * kb_per) - ks * kb_per;
         if (!mbar_wait(&sm->tempty[acc], acc_phase ^ 1)) {
           latch_error(err, ERRBIT_TIMEOUT);
           sm->abort = 1;
@@ -368,8 +394,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t bd0 = bdesc0 + (uint64_t)((stage * B_STAGE) >> 4);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
-            const uint64_t ad = ad0 + (uint64_t)(2 * k);
-            const uint64_t bd = bd0 + (uint64_t)(2 * k);
+            const uint64_t ad = ad0 + kStepA * (uint64_t)k;
+            const uint64_t bd = bd0 + kStepB * (uint64_t)k;
             if (FP8) mma_f8_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
             else mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
@@ -401,7 +427,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (FP8) acc_scale = 1.f / (__ldg(ea.a_scale) * __ldg(ea.b_scale));
     const float o_scale = (OUT == Act::E4M3) ? __ldg(ea.o_scale) : 1.f;
 
-    for (int tile = unit; tile < num_tiles; tile += units) {
+    for (int wk = unit; wk < num_work; wk += units) {
+      const int tile = wk % num_tiles, ks = wk / num_tiles;
       const TileXY tx = tile_xy(tile, n_tiles, full_tiles);
       const int row0 = tx.m * TILE_M + (int)rank * BM;                 // first row of this CTA
       const int col0 = tx.n0 + half * (tx.bn / 2);                     // first column of this half
@@ -425,7 +452,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           cp_async_commit();
         }
         if (row < M) {
-          const float* xr = static_cast<const float*>(ea.out) + (size_t)row * N + col0;
+          const float* xr = static_cast<const float*>(ea.res_in ? ea.res_in : ea.out) + (size_t)row * N + col0;
           for (int c = NB; c < nch; ++c) prefetch_l2(xr + c * CH::kCols);
         }
       }
@@ -565,7 +592,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_async_smem();
         named_bar_sync(bar_id, 128);
         if (elect) {
-          tma_store_2d(&tmO, col, row0, buf);
+          tma_store_2d(&tmO, col, row0 + ks * M, buf);
           bulk_commit();
         }
       }
@@ -616,10 +643,10 @@ int tail_split(int tiles, int clusters) {
   return split;
 }
 
-template <int EPI, bool FP8, Act OUT>
+template <int EPI, bool FP8, Act OUT, bool AMN = false, bool BMN = false>
 cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmO, int M, int N, int K,
-                        const EpiArgs& ea, int num_sms, unsigned* err, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<EPI, FP8, OUT>;
+                        const EpiArgs& ea, int num_sms, unsigned* err, cudaStream_t st, int ksplit = 1) {
+  auto kern = gemm_tc_kernel<EPI, FP8, OUT, AMN, BMN>;
   static int max_clusters = 0;  // per instantiation: co-resident clusters of two on this device
   if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan<EPI>::kSmemBytes);
@@ -641,11 +668,14 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
     max_clusters = n;
   }
   const int tiles = ((M + TILE_M - 1) / TILE_M) * (N / BN);
-  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  const int clusters = tiles * ksplit < max_clusters ? tiles * ksplit : max_clusters;
   // Residual epilogue (fp32 chunks of 32 columns): split the last r full tiles into halves
   // when that shortens the longest cluster's work under the static stride.
-  const int split = EPI == ESM_EPI_RESIDUAL ? tail_split(tiles, clusters) : 0;
+  const int split = EPI == ESM_EPI_RESIDUAL && ksplit == 1 ? tail_split(tiles, clusters) : 0;
   const int full_tiles = tiles - split, num_tiles = tiles + split;
+  const int kb_total = (K + (FP8 ? 127 : 63)) / (FP8 ? 128 : 64);
+  const int kb_per = (kb_total + ksplit - 1) / ksplit;
+  if (ksplit < 1 || kb_per * (ksplit - 1) >= kb_total) return cudaErrorInvalidValue;  // every split non-empty
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -658,7 +688,8 @@ cudaError_t launch_impl(const CUtensorMap* tmA, const CUtensorMap* tmB, const CU
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmO, M, N, K, full_tiles, num_tiles, ea, err);
+  return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmO, M, N, kb_total, kb_per, ksplit, full_tiles, num_tiles, ea,
+                            err);
 }
 
 }  // namespace
@@ -669,6 +700,25 @@ int gemm_tc_smem_bytes() { return Plan<ESM_EPI_QKV_ROPE>::kSmemBytes; }
 int gemm_tc_a_box_rows() { return BM; }
 int gemm_tc_b_box_rows() { return BN / 2; }
 int gemm_tc_out_box_rows() { return 128; }
+int gemm_tc_mn_box_rows() { return 64; }
+
+int gemm_tc_max_clusters(int num_sms) { return num_sms / 2; }
+
+cudaError_t launch_gemm_tc_bwd(GemmBwd kind, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmO,
+                               int M, int N, int K, int ksplit, const EpiArgs& ea, int num_sms, unsigned* err,
+                               cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  switch (kind) {
+    case GemmBwd::DGRAD_F32:
+      return launch_impl<ESM_EPI_BIAS_F32, false, Act::F32, false, true>(tmA, tmB, tmO, M, N, K, ea, num_sms, err, st);
+    case GemmBwd::DGRAD_BF16:
+      return launch_impl<ESM_EPI_QKV_ROPE, false, Act::BF16, false, true>(tmA, tmB, tmO, M, N, K, ea, num_sms, err, st);
+    case GemmBwd::WGRAD_F32:
+      return launch_impl<ESM_EPI_BIAS_F32, false, Act::F32, true, true>(tmA, tmB, tmO, M, N, K, ea, num_sms, err, st,
+                                                                       ksplit);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_gemm_tc(esm_epilogue epi, bool fp8, Act out_act, const CUtensorMap* tmA, const CUtensorMap* tmB,
                            const CUtensorMap* tmO, int M, int N, int K, const EpiArgs& ea, int num_sms, unsigned* err,

@@ -78,6 +78,7 @@ struct EpiArgs {
   const float* b_scale;   // FP8: scale of B (device)
   const float* o_scale;   // FP8 GELU output: quantisation scale (device)
   float* o_amax;          // FP8 GELU output: amax (device)
+  const void* res_in;     // ESM_EPI_RESIDUAL: residual read from here instead of out (NULL: in place)
 };
 
 // tcgen05 GEMM: A [M,K] bf16 (or e4m3), B [N,K] bf16 (or e4m3); K % 64 == 0 (bf16) or
@@ -93,6 +94,21 @@ int gemm_tc_out_box_rows();
 cudaError_t launch_gemm_tc(esm_epilogue epi, bool fp8, Act out_act, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, const CUtensorMap* tmO, int M, int N, int K, const EpiArgs& ea,
                            int num_sms, unsigned* err, cudaStream_t st);
+
+// Backward products on the same kernel with MN-major operands (bf16):
+//   DGRAD_F32 / DGRAD_BF16: out[M, N] = A[M, K] * B, B stored [K, N] (a weight [out, in]
+//     read as its transpose): tmB is a [K rows, N cols] map with a 64 x 64 box
+//     (gemm_tc_mn_box_rows()); output fp32 (bias / no epilogue) or bf16 (ea.rope_cols = 0);
+//   WGRAD_F32: out[M, N] = A^T B with A stored [K, M] and B stored [K, N] (dY and X over the
+//     K tokens), both 64 x 64-box maps; with ksplit > 1 the output map covers
+//     [ksplit * M, N] partial sums (M % 256 == 0).
+// N % 256 == 0; K any (the last K-slice is zero-filled by the maps).
+enum class GemmBwd { DGRAD_F32, DGRAD_BF16, WGRAD_F32 };
+int gemm_tc_mn_box_rows();
+int gemm_tc_max_clusters(int num_sms);
+cudaError_t launch_gemm_tc_bwd(GemmBwd kind, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmO,
+                               int M, int N, int K, int ksplit, const EpiArgs& ea, int num_sms, unsigned* err,
+                               cudaStream_t st);
 
 // SIMT fp32 GEMM (the ESM_FP32 precision): any M, N, K.
 void launch_gemm_f32(esm_epilogue epi, const float* A, const float* B, int M, int N, int K,
@@ -110,11 +126,44 @@ void launch_attention_bf16_to_e4m3(const __nv_bfloat16* qkv, uint8_t* o, int d, 
 // tcgen05 attention (head_dim 64): tm_qkv is a tensor map over qkv [T, 3d] bf16 with a
 // 64 x 128 box and the 128-byte swizzle; work items in tiles of kAttnQTileTc rows.
 int attention_tc_smem_bytes();
+// lse (optional, fp32 [T, heads]): the natural-log softmax normaliser of every query row
+// (scores scaled by 1/sqrt(head_dim)), kept by the training forward for the backward.
 cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int d, int heads, int max_items,
                                 const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
-                                cudaStream_t st);
+                                cudaStream_t st, float* lse = nullptr);
 void launch_attention_f32(const float* qkv, float* o, int d, int heads, int T, const PackBuffers& pb,
                           cudaStream_t st);
+
+// tcgen05 attention backward (attention_bwd_tc.cu): dqkv (bf16 [T, 3d]) from the saved
+// qkv (RoPE applied), O, the forward's lse and dO (bf16 [T, d], tm_do a 64 x 128-box map);
+// with rope set the q and k gradients are turned back through RoPE (positions pb.pos_id).
+// Scratch: dsum [T, heads], dq_acc [T, d] (fp32).
+int attention_bwd_tc_smem_bytes();
+cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const __nv_bfloat16* o,
+                                    const __nv_bfloat16* dout, const float* lse, float* dsum, float* dq_acc,
+                                    __nv_bfloat16* dqkv, int T, int d, int heads, int max_items, const PackBuffers& pb,
+                                    const float2* rope, int max_pos, int num_sms, unsigned* err, cudaStream_t st);
+
+// ---------------------------------------------------------------- backward.cu
+// Scratch floats for the column reductions of rows x cols (LayerNorm: two sums per column).
+size_t bwd_partial_floats(int rows, int cols);
+size_t emb_bwd_partial_floats(int rows, int vocab, int d);
+// LayerNorm backward: dx = dres + dLN/dx (dres may be NULL or alias dx), dgamma, dbeta
+// (float32 [cols]); stats float2 [rows] scratch, partial bwd_partial_floats(rows, cols).
+void launch_ln_bwd(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
+                   float2* stats, float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps,
+                   cudaStream_t st);
+// out[c] = sum_r src[r][c] (fp32 or bf16 rows); copy (fp32 input only, may be NULL): the
+// rows as bf16.  partial: bwd_partial_floats(rows, cols) / 2 floats.
+void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out, float* partial, __nv_bfloat16* copy,
+                   cudaStream_t st);
+// out[i] = sum_s partial[s * n + i] (split-K partial products, in split order).
+void launch_reduce_splits(const float* partial, int splits, size_t n, float* out, cudaStream_t st);
+void launch_gelu_fwd(const __nv_bfloat16* z, __nv_bfloat16* u, size_t n, cudaStream_t st);
+void launch_gelu_bwd(const float* du, const __nv_bfloat16* z, __nv_bfloat16* dz, size_t n, cudaStream_t st);
+// demb[v] = scale * sum over tokens t with tok[t] == v of dx[t] (float32 [vocab, d]).
+void launch_emb_bwd(const float* dx, const int32_t* tok, int T, int d, int vocab, float scale, float* partial,
+                    float* demb, cudaStream_t st);
 
 // ---------------------------------------------------------------- fp8.cu
 // Quantise a bf16 tensor to e4m3 with *scale; record max|w| into *amax.
