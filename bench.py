@@ -39,6 +39,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-train", action="store_true", help="skip the training-step measurement")
     ap.add_argument("--no-graph", action="store_true", help="launch the kernels eagerly instead of replaying "
                                                              "one captured CUDA graph per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
@@ -424,6 +425,60 @@ def run_ours(args):
                "ms_per_call": mms, "tokens_per_s": T / (mms / 1e3), "scored_tokens": int(cnt.item()),
                "mean_loss_random_weights": float(lsum.item()) / max(1, int(cnt.item()))}
 
+    # ---------------------------------------------------------------- training step (forward that keeps
+    # its activations + backward: every parameter's gradient), same batch
+    train = None
+    if not padded and prec == "bf16" and not args.no_train:
+        from transformer_esm_layer_gb300.binding import DeviceGrads
+        tb = enc.train_buffer(T, dev)
+        grads = DeviceGrads(g, g.num_layers, device=dev)
+        d_out = torch.randn(T, g.hidden, dtype=torch.float32, device=dev,
+                            generator=torch.Generator(device=dev).manual_seed(wl.seed))
+
+        def train_fwd():
+            enc.forward_train(dw, tok, cu, maxL, tb, ws, out=out, stream=stream)
+
+        def train_bwd():
+            enc.backward(dw, d_out, grads, tb, ws, stream=stream)
+
+        for _ in range(2):
+            train_fwd()
+            train_bwd()
+        enc.check(stream)
+        n_tr = 5
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_tr + 1)]
+        ev[0].record(stream)
+        for i in range(n_tr):
+            train_fwd()
+            ev[2 * i + 1].record(stream)
+            train_bwd()
+            ev[2 * i + 2].record(stream)
+        torch.cuda.synchronize()
+        enc.check(stream)
+        f_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n_tr)) / n_tr
+        b_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(n_tr)) / n_tr
+        enc.set_profiling(True)
+        enc.get_profile(reset=True)
+        train_bwd()
+        bprof = enc.get_profile(reset=True)
+        enc.set_profiling(False)
+        # backward work: two products per linear map (input and weight gradient) and five
+        # per attention tile pair (S, dP, dV, dK, dQ) against the forward's two
+        bwd_flops = 2.0 * sum(flops[c] for c in gemm_classes) + 2.5 * flops["attention"]
+        bg_ms = bprof["gemm_backward"]["ms"]
+        train = {"calls": "esm_encoder_forward_train + esm_encoder_backward (all parameter gradients, fp32)",
+                 "ms_per_step": f_ms + b_ms, "ms_forward_train": f_ms, "ms_backward": b_ms,
+                 "tokens_per_s": global_tokens / ((f_ms + b_ms) / 1e3),
+                 "backward_tflops": bwd_flops / (b_ms / 1e3) / 1e12,
+                 "step_tflops": (total_flops + bwd_flops) / ((f_ms + b_ms) / 1e3) / 1e12,
+                 "backward_gemm": {"ms": bg_ms, "launches": bprof["gemm_backward"]["launches"],
+                                   "tflops": 2.0 * sum(flops[c] for c in gemm_classes) / (bg_ms / 1e3) / 1e12
+                                   if bg_ms else None},
+                 "backward_per_class_ms": {c: bprof[c]["ms"] for c in ("attention", "layernorm", "gemm_backward",
+                                                                       "other")},
+                 "train_buffer_gb": tb.numel() / 2**30}
+        del tb, grads
+
     # ---------------------------------------------------------------- CPU baseline (oracle)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -459,7 +514,7 @@ def run_ours(args):
                 "algorithmic_gflop_per_step_per_gpu": total_flops / 1e9,
                 "roofline": roofline, "per_kernel": per_kernel,
                 "padded_over_packed_flops": (sum(executed.values()) / total_flops) if padded else None, "cpu_baseline": cpu, "e2e": e2e,
-                "mlm_head": mlm,
+                "mlm_head": mlm, "train_step": train,
                 "clocks": clocks, "gpu_launches": launches,
                 "timing": "CUDA graph replay of the whole forward" if not args.no_graph else "eager launches",
                 "context": "pages' own figure: 59.2% model-FLOP utilisation, ESM-2 650M training, batch 46, A100"}

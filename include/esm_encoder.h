@@ -419,7 +419,8 @@ ESM_API esm_status esm_op_attention_backward(esm_encoder_t* h, const void* qkv, 
 /* ---- measurement hooks ----
  * Kernel classes of the forward: 0 QKV GEMM (+bias, RoPE), 1 attention, 2 output-projection
  * GEMM (+bias, residual), 3 fc1 GEMM (+bias, GELU), 4 fc2 GEMM (+bias, residual),
- * 5 LayerNorm, 6 everything else (packing, work list, embedding, FP8 quantise/update). */
+ * 5 LayerNorm, 6 everything else (packing, work list, embedding, FP8 quantise/update),
+ * 7 the backward's GEMMs (input and weight gradients, with their split-K sums). */
 #define ESM_PROFILE_CLASSES 8
 typedef struct {
   double ms[ESM_PROFILE_CLASSES];           /* summed device time per class (profiling on)  */

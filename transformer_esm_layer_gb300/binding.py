@@ -34,7 +34,8 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_op_layernorm_backward_workspace_size", "esm_op_layernorm_backward", "esm_op_attention_train",
            "esm_op_attention_backward_workspace_size", "esm_op_attention_backward",
            "esm_status_string")
-PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other", "reserved")
+PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other",
+                   "gemm_backward")
 
 
 class EsmError(RuntimeError):

@@ -176,7 +176,7 @@ struct esm_encoder {
 
 namespace {
 
-enum ProfClass { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_FC1 = 3, P_FC2 = 4, P_LN = 5, P_OTHER = 6 };
+enum ProfClass { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_FC1 = 3, P_FC2 = 4, P_LN = 5, P_OTHER = 6, P_BWD_GEMM = 7 };
 
 // Counts the launches of one call site and, with profiling on, brackets them with events
 // recorded on the launch stream.
@@ -483,7 +483,7 @@ esm_status run_dgrad(esm_encoder* h, const void* dY, const void* W, void* out, b
   ea.out = out;
   ea.rope_cols = 0;
   cudaError_t e;
-  PROF(h, P_OTHER, st, 1,
+  PROF(h, P_BWD_GEMM, st, 1,
        e = launch_gemm_tc_bwd(out_bf16 ? GemmBwd::DGRAD_BF16 : GemmBwd::DGRAD_F32, ma, mb, mo, M, K, N, 1, ea,
                               h->num_sms, h->d_err, st));
   return cuda_status(e);
@@ -508,9 +508,10 @@ esm_status run_wgrad(esm_encoder* h, const void* dY, const void* X, float* dW, i
   ea.out = out;
   ea.rope_cols = 0;
   cudaError_t e;
-  PROF(h, P_OTHER, st, 1, e = launch_gemm_tc_bwd(GemmBwd::WGRAD_F32, ma, mb, mo, N, K, M, ks, ea, h->num_sms, h->d_err, st));
+  PROF(h, P_BWD_GEMM, st, 1,
+       e = launch_gemm_tc_bwd(GemmBwd::WGRAD_F32, ma, mb, mo, N, K, M, ks, ea, h->num_sms, h->d_err, st));
   if (e != cudaSuccess) return ESM_ERR_CUDA;
-  if (ks > 1) PROF(h, P_OTHER, st, 1, launch_reduce_splits(split, ks, (size_t)N * K, dW, st));
+  if (ks > 1) PROF(h, P_BWD_GEMM, st, 1, launch_reduce_splits(split, ks, (size_t)N * K, dW, st));
   return cuda_status(cudaGetLastError());
 }
 
