@@ -459,6 +459,8 @@ def run_ours(args):
         b_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(n_tr)) / n_tr
         enc.set_profiling(True)
         enc.get_profile(reset=True)
+        train_fwd()
+        fprof = enc.get_profile(reset=True)
         train_bwd()
         bprof = enc.get_profile(reset=True)
         enc.set_profiling(False)
@@ -476,6 +478,9 @@ def run_ours(args):
                                    if bg_ms else None},
                  "backward_per_class_ms": {c: bprof[c]["ms"] for c in ("attention", "layernorm", "gemm_backward",
                                                                        "other")},
+                 "forward_train_per_class_ms": {c: fprof[c]["ms"] for c in ("gemm_qkv", "attention", "gemm_oproj",
+                                                                            "gemm_fc1", "gemm_fc2", "layernorm",
+                                                                            "other")},
                  "train_buffer_gb": tb.numel() / 2**30}
         del tb, grads
 

@@ -324,7 +324,7 @@ ESM_API esm_status esm_encoder_set_fp8_state(esm_encoder_t* h, const float* host
  * out: it is the exact gradient of the forward above (chain rule through the final
  * LayerNorm, every layer in reverse, and the embedding), with bf16 GEMM and attention
  * operands and fp32 accumulation, reductions over tokens in a fixed order.
- * ESM_BF16 handles only (others: ESM_ERR_UNSUPPORTED).
+ * ESM_BF16 handles with hidden <= 4096 only (others: ESM_ERR_UNSUPPORTED).
  *
  * Gradient buffers: device float32, same shapes as the weights ([out, in] for linear
  * maps); the per-layer members point to HOST arrays of num_layers DEVICE pointers.
@@ -388,7 +388,7 @@ ESM_API esm_status esm_op_gemm_wgrad_workspace_size(const esm_encoder_t* h, int 
 ESM_API esm_status esm_op_gemm_wgrad(esm_encoder_t* h, const void* dY, const void* X, float* dW, int M, int N, int K,
                                      void* workspace, size_t workspace_bytes, esm_stream_t stream);
 
-/* LayerNorm backward over rows of x (device float32 [rows, cols], cols % 4 == 0): with
+/* LayerNorm backward over rows of x (device float32 [rows, cols], cols % 4 == 0, cols <= 4096): with
  * dy = dL/dy (float32 [rows, cols]) and gamma in the parameter dtype,
  *   dx = dres + dL/dx (dres may be NULL or equal to dx), dgamma = sum_rows dy xhat,
  *   dbeta = sum_rows dy (float32 [cols]).  Workspace: the size query's bytes. */

@@ -16,16 +16,19 @@
 //   dV  += P^T dO       (M=128, N=64, K=128; dO MN-major)          cols [384,448)
 //   dK  += dS^T Q       (M=128, N=64, K=128; Q MN-major)           cols [320,384)
 //   dQ_i = dS K         (M=128 queries, N=64, K=128 keys; dS and K MN-major)  cols [256,320)
-// Roles (384 threads):
+// Roles (512 threads):
 //   warp 0       TMA: the item's K and V tiles, then Q and dO tiles of each query tile into
 //                a 2-stage ring (straight from the packed qkv and dO buffers);
 //   warp 1       one thread issues the MMAs: S^T and dP^T of tile i, then the three
 //                gradient products of tile i-1 (whose P^T and dS^T are in shared memory);
-//   warps 4..7   thread r owns key r: reads its S^T and dP^T rows, forms P^T = 2^(S^T c - lse)
-//                and dS^T = P^T (dP^T - D) for the valid (key, query) pairs, writes both
-//                as bf16 into shared memory (K-major, 128-byte swizzle); at the end of the
-//                item scales dK, turns it back through RoPE and stores dK and dV (bf16);
-//   warps 8..11  thread r owns query r of the tile: reads dQ_i from TMEM and adds it into
+//   warps 4..11  two warpgroups, one per 64 queries of the tile; thread r owns key r: reads
+//                its S^T and dP^T row segment, forms P^T = 2^(S^T c - lse) and
+//                dS^T = P^T (dP^T - D) for the valid (key, query) pairs in registers, hands
+//                S^T back, then (once the previous tile's gradient products have read them)
+//                writes both as bf16 into shared memory (K-major, 128-byte swizzle); at the end
+//                of the item warpgroup 0 scales dK, turns it back through RoPE and stores it,
+//                warpgroup 1 stores dV (bf16);
+//   warps 12..15 thread r owns query r of the tile: reads dQ_i from TMEM and adds it into
 //                an fp32 accumulator in global memory with vector reductions (several key
 //                tiles contribute to each query row).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error bit and stops.
@@ -38,7 +41,7 @@ namespace {
 constexpr int DH = 64;
 constexpr int TB = 128;                 // rows of a key or query tile
 constexpr int TILE = 128 * 128;         // 128 rows x 128 bytes (64 bf16)
-constexpr int THREADS = 384;
+constexpr int THREADS = 512;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DK = 320, COL_DV = 384;
 
@@ -46,7 +49,7 @@ struct BwdSmem {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full, s_free, p_full, p_free, dq_full, dq_free, acc_full, acc_free, mma_done;
-  uint64_t stat_full[2];  // all 128 slots of lse2 / dsum [b] written (128 arrivals)
+  uint64_t stat_full[2];  // all 128 slots of lse2 and of dsum [b] written (256 arrivals)
   uint32_t tmem_base;
   volatile int abort;
   float lse2[2][TB];  // query tile g (buffer g & 1): log2-sum-exp2 of the scaled scores
@@ -106,16 +109,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&sm->q_empty[b], 1);
     }
     mbar_init(&sm->s_full, 1);
-    mbar_init(&sm->s_free, 4);
-    mbar_init(&sm->p_full, 4);
+    mbar_init(&sm->s_free, 8);
+    mbar_init(&sm->p_full, 8);
     mbar_init(&sm->p_free, 1);
     mbar_init(&sm->dq_full, 1);
     mbar_init(&sm->dq_free, 4);
     mbar_init(&sm->acc_full, 1);
-    mbar_init(&sm->acc_free, 4);
+    mbar_init(&sm->acc_free, 8);
     mbar_init(&sm->mma_done, 1);
-    mbar_init(&sm->stat_full[0], 128);
-    mbar_init(&sm->stat_full[1], 128);
+    mbar_init(&sm->stat_full[0], 256);
+    mbar_init(&sm->stat_full[1], 256);
     sm->abort = 0;
     fence_barrier_init();
   }
@@ -225,15 +228,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(&sm->mma_done, 0);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P^T / dS^T, dK / dV
+    const int wg = (warp - 4) >> 2;  // warpgroup: queries 64 wg .. 64 wg + 63 of each tile
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // key row of the tile (and index of the lse / D slot)
+    const int r = wq * 32 + lane;    // key row of the tile (and index of the lse / D slot)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     constexpr float kLog2e = 1.4426950408889634f;
     const float c = kLog2e / 8.f;  // scores scaled by 1/sqrt(64), in log2 units
-    uint8_t* sP = base + OFF_P;
-    uint8_t* sDS = base + OFF_DS;
+    uint8_t* sP = base + OFF_P + wg * TILE;   // this warpgroup's 64 queries of P^T
+    uint8_t* sDS = base + OFF_DS + wg * TILE;
     bool ok = true;
     int g = 0, n = 0;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
@@ -241,109 +245,98 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool kval = r < x.krows;
       for (int i = 0; i < x.nq; ++i, ++g) {
         const int q0 = x.s0 + i * TB, qvalid = min(TB, x.slen - i * TB);
-        // this tile's lse (to log2 units) and D, one slot per thread, into buffer g & 1 (its
-        // previous readers, tile g - 2, are done: every thread arrived for tile g - 1 after
-        // finishing tile g - 2)
+        // this tile's lse (to log2 units; warpgroup 0) and D (warpgroup 1), one slot per
+        // thread, into buffer g & 1 (its previous readers, tile g - 2, are done: every thread
+        // arrived for tile g - 1 after finishing tile g - 2)
         const int sb = g & 1;
-        float l2 = 0.f, dd = 0.f;
-        if (r < qvalid) {
-          l2 = __ldg(lse + (size_t)(q0 + r) * heads + x.h) * kLog2e;
-          dd = __ldg(dsum + (size_t)(q0 + r) * heads + x.h);
-        }
-        sm->lse2[sb][r] = l2;
-        sm->dsum[sb][r] = dd;
+        if (wg == 0) sm->lse2[sb][r] = r < qvalid ? __ldg(lse + (size_t)(q0 + r) * heads + x.h) * kLog2e : 0.f;
+        else sm->dsum[sb][r] = r < qvalid ? __ldg(dsum + (size_t)(q0 + r) * heads + x.h) : 0.f;
         mbar_arrive(&sm->stat_full[sb]);
         if (!mbar_wait_warp(&sm->stat_full[sb], (uint32_t)(g >> 1) & 1u)) { ok = false; break; }
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
+        tc_fence_after();
+        // P^T and dS^T of this thread's key and 64 queries, as bf16 pairs, 16 queries at a time
+        uint32_t pw[4][8], dw[4][8];
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub) {
+          const int cq = 64 * wg + 16 * sub;  // first query (column) of the sub-chunk
+          float sv[16], dp[16];
+          tmem_ld16(tmem + lane_off + COL_S + cq, sv);
+          tmem_ld16(tmem + lane_off + COL_DP + cq, dp);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int q = cq + 2 * j;
+            const bool v0 = kval && q < qvalid, v1 = kval && q + 1 < qvalid;
+            const float p0 = v0 ? fast_exp2(fmaf(sv[2 * j], c, -sm->lse2[sb][q])) : 0.f;
+            const float p1 = v1 ? fast_exp2(fmaf(sv[2 * j + 1], c, -sm->lse2[sb][q + 1])) : 0.f;
+            pw[sub][j] = pack_bf16x2(p0, p1);
+            dw[sub][j] = pack_bf16x2(p0 * (dp[2 * j] - sm->dsum[sb][q]), p1 * (dp[2 * j + 1] - sm->dsum[sb][q + 1]));
+          }
+        }
+        // S^T / dP^T are read: the tensor core may compute the next tile's
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->s_free);
         // P^T / dS^T may be overwritten once the previous tile's gradient MMAs have read them
         if (!mbar_wait_warp(&sm->p_free, (uint32_t)(g & 1) ^ 1u)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {  // 32 queries per chunk
-          float s[32], dp[32];
-          tmem_ld32(tmem + lane_off + COL_S + 32 * ch, s);
-          tmem_ld32(tmem + lane_off + COL_DP + 32 * ch, dp);
-          uint32_t pw[16], dw[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int q = 32 * ch + 2 * j;
-            const bool v0 = kval && q < qvalid, v1 = kval && q + 1 < qvalid;
-            const float p0 = v0 ? fast_exp2(fmaf(s[2 * j], c, -sm->lse2[sb][q])) : 0.f;
-            const float p1 = v1 ? fast_exp2(fmaf(s[2 * j + 1], c, -sm->lse2[sb][q + 1])) : 0.f;
-            pw[j] = pack_bf16x2(p0, p1);
-            dw[j] = pack_bf16x2(p0 * (dp[2 * j] - sm->dsum[sb][q]), p1 * (dp[2 * j + 1] - sm->dsum[sb][q + 1]));
-          }
-          const int blk = ch >> 1;  // queries 0-63 | 64-127
+        for (int sub = 0; sub < 4; ++sub) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t off = (uint32_t)(blk * TILE) + swz(r, (ch & 1) * 4 + u);
-            *reinterpret_cast<uint4*>(sP + off) = make_uint4(pw[4 * u], pw[4 * u + 1], pw[4 * u + 2], pw[4 * u + 3]);
-            *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t off = swz(r, 2 * sub + h2);
+            *reinterpret_cast<uint4*>(sP + off) =
+                make_uint4(pw[sub][4 * h2], pw[sub][4 * h2 + 1], pw[sub][4 * h2 + 2], pw[sub][4 * h2 + 3]);
+            *reinterpret_cast<uint4*>(sDS + off) =
+                make_uint4(dw[sub][4 * h2], dw[sub][4 * h2 + 1], dw[sub][4 * h2 + 2], dw[sub][4 * h2 + 3]);
           }
         }
-        tc_fence_before();
         fence_async_smem();  // generic-proxy writes of P^T / dS^T before the tensor core reads
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sm->s_free);
-          mbar_arrive(&sm->p_full);
-        }
+        if (lane == 0) mbar_arrive(&sm->p_full);
       }
       if (!ok) break;
-      // ---- item epilogue: dK (scaled, RoPE undone) and dV of this thread's key
+      // ---- item epilogue: warpgroup 0 stores dK (scaled, RoPE undone), warpgroup 1 dV
       if (!mbar_wait_warp(&sm->acc_full, (uint32_t)n & 1u)) { ok = false; break; }
       tc_fence_after();
-      float dk[64], dv[64];
+      float a[64];
       {
-        float t[32];
-        tmem_ld32(tmem + lane_off + COL_DK, t);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dk[j] = t[j];
-        tmem_ld32(tmem + lane_off + COL_DK + 32, t);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dk[32 + j] = t[j];
-        tmem_ld32(tmem + lane_off + COL_DV, t);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dv[j] = t[j];
-        tmem_ld32(tmem + lane_off + COL_DV + 32, t);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dv[32 + j] = t[j];
+        const uint32_t col = wg == 0 ? COL_DK : COL_DV;
+        tmem_ld32(tmem + lane_off + col, *reinterpret_cast<float(*)[32]>(a));
+        tmem_ld32(tmem + lane_off + col + 32, *reinterpret_cast<float(*)[32]>(a + 32));
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->acc_free);
       if (kval) {
         const int key = x.k0 + r;
-        if (rope != nullptr) {
-          int p = key - x.s0;
-          p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
+        if (wg == 0) {
+          if (rope != nullptr) {
+            int p = key - x.s0;
+            p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {  // pair (j, j + 32) turned back by its angle
-            const float2 cs = __ldg(rope + ((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1));
-            const float a = dk[j] * 0.125f, b = dk[j + 32] * 0.125f;
-            dk[j] = a * cs.x + b * cs.y;
-            dk[j + 32] = b * cs.x - a * cs.y;
+            for (int j = 0; j < 32; ++j) {  // pair (j, j + 32) turned back by its angle
+              const float2 cs = __ldg(rope + ((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1));
+              const float u = a[j] * 0.125f, v = a[j + 32] * 0.125f;
+              a[j] = u * cs.x + v * cs.y;
+              a[j + 32] = v * cs.x - u * cs.y;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) a[j] *= 0.125f;
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 64; ++j) dk[j] *= 0.125f;
         }
-        uint4* gk = reinterpret_cast<uint4*>(dqkv + (size_t)key * 3 * d + d + x.h * DH);
-        uint4* gv = reinterpret_cast<uint4*>(dqkv + (size_t)key * 3 * d + 2 * d + x.h * DH);
+        uint4* gdst = reinterpret_cast<uint4*>(dqkv + (size_t)key * 3 * d + (wg == 0 ? d : 2 * d) + x.h * DH);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          gk[u] = make_uint4(pack_bf16x2(dk[8 * u], dk[8 * u + 1]), pack_bf16x2(dk[8 * u + 2], dk[8 * u + 3]),
-                             pack_bf16x2(dk[8 * u + 4], dk[8 * u + 5]), pack_bf16x2(dk[8 * u + 6], dk[8 * u + 7]));
-          gv[u] = make_uint4(pack_bf16x2(dv[8 * u], dv[8 * u + 1]), pack_bf16x2(dv[8 * u + 2], dv[8 * u + 3]),
-                             pack_bf16x2(dv[8 * u + 4], dv[8 * u + 5]), pack_bf16x2(dv[8 * u + 6], dv[8 * u + 7]));
-        }
+        for (int u = 0; u < 8; ++u)
+          gdst[u] = make_uint4(pack_bf16x2(a[8 * u], a[8 * u + 1]), pack_bf16x2(a[8 * u + 2], a[8 * u + 3]),
+                               pack_bf16x2(a[8 * u + 4], a[8 * u + 5]), pack_bf16x2(a[8 * u + 6], a[8 * u + 7]));
       }
     }
     if (!ok) {
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ accumulation
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // query row of the tile

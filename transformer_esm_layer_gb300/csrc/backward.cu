@@ -1,12 +1,14 @@
 // Row, column and elementwise kernels of the training step (the backward of the packed
 // layer stack that the hotelren.com guide trains over cu_seqlens, §3.2 and §6):
-//   * LayerNorm backward, by rows (dx) and by columns (dgamma, dbeta);
+//   * LayerNorm backward (dx by rows, dgamma and dbeta as column sums in the same pass);
 //   * column sums (bias gradients) with an optional bfloat16 copy of the rows (the next
 //     GEMM's operand);
-//   * the exact GELU and its derivative (the training forward keeps the pre-activation);
 //   * the embedding table's gradient (scatter-add of the embedded rows' gradient).
+// (GELU's derivative runs in the epilogue of the GEMM that produces its input gradient.)
 // Every reduction over rows runs in a fixed order: chunks of rows give partial sums, and
 // one pass adds the chunks in index order, so results do not depend on scheduling.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,98 +29,112 @@ __device__ __forceinline__ float4 ld_param4(const void* p, int c, bool f32) {
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
-// One warp per row: mean, variance (two passes), then with g = dy * gamma and xhat the
-// normalised row
+// LayerNorm backward, one warp per row, the row held in registers (N4 float4 per lane):
+// mean and variance (two passes), then with g = dy * gamma and xhat the normalised row
 //   dx = dres + rstd * (g - mean(g) - xhat * mean(g * xhat))
-// (dres may alias dx).  stats[row] = (mean, rstd) for the column pass.
-__global__ void ln_bwd_rows_kernel(const float* __restrict__ x, const void* __restrict__ gamma, bool gf32,
-                                   const float* __restrict__ dy, const float* dres, float* dx, float2* stats, int rows,
-                                   int cols, float eps) {
-  const int warps = blockDim.x >> 5;
-  const int row = blockIdx.x * warps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+// (dres may alias dx).  The parameter gradients are column sums: each warp adds its rows'
+// dy * xhat and dy into its own shared-memory slice, and at the end the block adds the
+// slices in warp order into partial[block][0 | 1][cols].
+template <int N4>
+__global__ void __launch_bounds__(256) ln_bwd_kernel(const float* __restrict__ x, const void* __restrict__ gamma,
+                                                     bool gf32, const float* __restrict__ dy, const float* dres,
+                                                     float* dx, float* __restrict__ partial, int rows, int cols,
+                                                     int rows_per_block, float eps) {
+  extern __shared__ float4 slice4[];  // [warps][2][cols / 4]
+  const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n4 = cols >> 2;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * cols);
-  const float4* dr = reinterpret_cast<const float4*>(dy + (size_t)row * cols);
-  float s = 0.f;
-  for (int c = lane; c < n4; c += 32) {
-    const float4 v = xr[c];
-    s += (v.x + v.y) + (v.z + v.w);
-  }
-  const float mu = wsum(s) / (float)cols;
-  float q = 0.f;
-  for (int c = lane; c < n4; c += 32) {
-    const float4 v = xr[c];
-    const float a = v.x - mu, b = v.y - mu, e = v.z - mu, f = v.w - mu;
-    q += (a * a + b * b) + (e * e + f * f);
-  }
-  const float rstd = rsqrtf(wsum(q) / (float)cols + eps);
-  float sg = 0.f, sgx = 0.f;
-  for (int c = lane; c < n4; c += 32) {
-    const float4 v = xr[c], d = dr[c], g = ld_param4(gamma, 4 * c, gf32);
-    const float g0 = d.x * g.x, g1 = d.y * g.y, g2 = d.z * g.z, g3 = d.w * g.w;
-    sg += (g0 + g1) + (g2 + g3);
-    sgx += (g0 * (v.x - mu) + g1 * (v.y - mu)) + (g2 * (v.z - mu) + g3 * (v.w - mu));
-  }
-  const float mg = wsum(sg) / (float)cols;
-  const float mgx = wsum(sgx) * rstd / (float)cols;
-  float4* out = reinterpret_cast<float4*>(dx + (size_t)row * cols);
-  const float4* res = dres ? reinterpret_cast<const float4*>(dres + (size_t)row * cols) : nullptr;
-  for (int c = lane; c < n4; c += 32) {
-    const float4 v = xr[c], d = dr[c], g = ld_param4(gamma, 4 * c, gf32);
-    float4 r = res ? res[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-    r.x += rstd * (d.x * g.x - mg - (v.x - mu) * rstd * mgx);
-    r.y += rstd * (d.y * g.y - mg - (v.y - mu) * rstd * mgx);
-    r.z += rstd * (d.z * g.z - mg - (v.z - mu) * rstd * mgx);
-    r.w += rstd * (d.w * g.w - mg - (v.w - mu) * rstd * mgx);
-    out[c] = r;
-  }
-  if (lane == 0) stats[row] = make_float2(mu, rstd);
-}
-
-// Column partial sums of the LayerNorm parameter gradients over one chunk of rows:
-// partial[chunk][0][c] = sum dy * xhat, partial[chunk][1][c] = sum dy.
-__global__ void ln_bwd_cols_kernel(const float* __restrict__ x, const float* __restrict__ dy,
-                                   const float2* __restrict__ stats, float* __restrict__ partial, int rows, int cols,
-                                   int chunk_rows) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  const int chunk = blockIdx.y;
-  if (c >= cols) return;
-  const int r0 = chunk * chunk_rows, r1 = min(rows, r0 + chunk_rows);
-  float a = 0.f, b = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    const float2 st = __ldg(stats + r);
-    const float g = dy[(size_t)r * cols + c];
-    a = fmaf(g, (x[(size_t)r * cols + c] - st.x) * st.y, a);
-    b += g;
-  }
-  partial[((size_t)chunk * 2) * cols + c] = a;
-  partial[((size_t)chunk * 2 + 1) * cols + c] = b;
-}
-
-// partial[chunk][c] = sum over the chunk's rows of src[r][c]; with copy (fp32 input) the
-// rows are also written as bfloat16.
-template <bool BF16IN>
-__global__ void colsum_kernel(const void* __restrict__ src, int rows, int cols, int chunk_rows,
-                              float* __restrict__ partial, __nv_bfloat16* __restrict__ copy) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  const int chunk = blockIdx.y;
-  if (c >= cols) return;
-  const int r0 = chunk * chunk_rows, r1 = min(rows, r0 + chunk_rows);
-  float a = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    const size_t i = (size_t)r * cols + c;
-    float v;
-    if (BF16IN) {
-      v = __bfloat162float(static_cast<const __nv_bfloat16*>(src)[i]);
-    } else {
-      v = static_cast<const float*>(src)[i];
-      if (copy) copy[i] = __float2bfloat16_rn(v);
+  float4* mine = slice4 + (size_t)warp * 2 * n4;
+  for (int c = lane; c < 2 * n4; c += 32) mine[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int r0 = blockIdx.x * rows_per_block, r1 = min(rows, r0 + rows_per_block);
+  for (int row = r0 + warp; row < r1; row += warps) {
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * cols);
+    const float4* dr = reinterpret_cast<const float4*>(dy + (size_t)row * cols);
+    float4 v[N4], d[N4];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < N4; ++i) {
+      const int c = i * 32 + lane;
+      v[i] = c < n4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      d[i] = c < n4 ? dr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
     }
-    a += v;
+    const float mu = wsum(s) / (float)cols;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < N4; ++i) {
+      if (i * 32 + lane < n4) {
+        v[i].x -= mu; v[i].y -= mu; v[i].z -= mu; v[i].w -= mu;
+        q += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
+      }
+    }
+    const float rstd = rsqrtf(wsum(q) / (float)cols + eps);
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int i = 0; i < N4; ++i) {  // v becomes xhat; gamma is re-read from L1 (5 KB per row)
+      v[i].x *= rstd; v[i].y *= rstd; v[i].z *= rstd; v[i].w *= rstd;
+      const float4 gm = i * 32 + lane < n4 ? ld_param4(gamma, 4 * (i * 32 + lane), gf32) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float g0 = d[i].x * gm.x, g1 = d[i].y * gm.y, g2 = d[i].z * gm.z, g3 = d[i].w * gm.w;
+      sg += (g0 + g1) + (g2 + g3);
+      sgx += (g0 * v[i].x + g1 * v[i].y) + (g2 * v[i].z + g3 * v[i].w);
+    }
+    const float mg = wsum(sg) / (float)cols, mgx = wsum(sgx) / (float)cols;
+    float4* out = reinterpret_cast<float4*>(dx + (size_t)row * cols);
+    const float4* res = dres ? reinterpret_cast<const float4*>(dres + (size_t)row * cols) : nullptr;
+#pragma unroll
+    for (int i = 0; i < N4; ++i) {
+      const int c = i * 32 + lane;
+      if (c < n4) {
+        const float4 gm = ld_param4(gamma, 4 * c, gf32);
+        float4 o = res ? res[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        o.x += rstd * (d[i].x * gm.x - mg - v[i].x * mgx);
+        o.y += rstd * (d[i].y * gm.y - mg - v[i].y * mgx);
+        o.z += rstd * (d[i].z * gm.z - mg - v[i].z * mgx);
+        o.w += rstd * (d[i].w * gm.w - mg - v[i].w * mgx);
+        out[c] = o;
+        float4 a = mine[c], b = mine[n4 + c];
+        a.x = fmaf(d[i].x, v[i].x, a.x); a.y = fmaf(d[i].y, v[i].y, a.y);
+        a.z = fmaf(d[i].z, v[i].z, a.z); a.w = fmaf(d[i].w, v[i].w, a.w);
+        b.x += d[i].x; b.y += d[i].y; b.z += d[i].z; b.w += d[i].w;
+        mine[c] = a;
+        mine[n4 + c] = b;
+      }
+    }
   }
-  partial[(size_t)chunk * cols + c] = a;
+  __syncthreads();
+  float* sl = reinterpret_cast<float*>(slice4);
+  for (int c = threadIdx.x; c < 2 * cols; c += blockDim.x) {
+    float a = 0.f;
+    for (int w = 0; w < warps; ++w) a += sl[(size_t)w * 2 * cols + c];
+    partial[(size_t)blockIdx.x * 2 * cols + c] = a;
+  }
+}
+
+// partial[chunk][c] = sum over the chunk's rows of src[r][c], four columns per thread; with
+// copy (fp32 input) the rows are also written as bfloat16.
+template <bool BF16IN>
+__global__ void __launch_bounds__(128) colsum_kernel(const void* __restrict__ src, int rows, int cols, int chunk_rows,
+                                                     float* __restrict__ partial, __nv_bfloat16* __restrict__ copy) {
+  const int c4 = blockIdx.x * blockDim.x + threadIdx.x;  // columns 4 c4 .. 4 c4 + 3
+  const int chunk = blockIdx.y;
+  if (4 * c4 >= cols) return;
+  const int r0 = chunk * chunk_rows, r1 = min(rows, r0 + chunk_rows);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int r = r0; r < r1; ++r) {
+    const size_t i = (size_t)r * cols + 4 * c4;
+    float4 v;
+    if (BF16IN) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(src) + i));
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      v = make_float4(lo.x, lo.y, hi.x, hi.y);
+    } else {
+      v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(src) + i));
+      if (copy) *reinterpret_cast<uint2*>(copy + i) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+    a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+  }
+  *reinterpret_cast<float4*>(partial + (size_t)chunk * cols + 4 * c4) = a;
 }
 
 // out[i] = scale * sum_k partial[k * stride + i], k in index order.
@@ -129,24 +145,6 @@ __global__ void reduce_chunks_kernel(const float* __restrict__ partial, int chun
   float a = 0.f;
   for (int k = 0; k < chunks; ++k) a += partial[(size_t)k * stride + i];
   out[i] = a * scale;
-}
-
-// u = GELU(z) = z Phi(z), exact (erf), bf16 -> bf16.
-__global__ void gelu_fwd_kernel(const __nv_bfloat16* __restrict__ z, __nv_bfloat16* __restrict__ u, size_t n) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const float a = __bfloat162float(z[i]);
-  u[i] = __float2bfloat16_rn(0.5f * a * (1.f + erff(a * 0.70710678118654752f)));
-}
-
-// dz = du * GELU'(z), GELU'(z) = Phi(z) + z phi(z); du fp32, z bf16, dz bf16.
-__global__ void gelu_bwd_kernel(const float* __restrict__ du, const __nv_bfloat16* __restrict__ z,
-                                __nv_bfloat16* __restrict__ dz, size_t n) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const float a = __bfloat162float(z[i]);
-  const float d = 0.5f * (1.f + erff(a * 0.70710678118654752f)) + a * 0.3989422804014327f * expf(-0.5f * a * a);
-  dz[i] = __float2bfloat16_rn(du[i] * d);
 }
 
 // partial[chunk][v][c] = sum of dx[t][c] over the chunk's tokens t with tok[t] == v (each
@@ -174,22 +172,49 @@ int chunks_for(int rows) { return rows <= 0 ? 1 : (rows + kChunkRows - 1) / kChu
 
 }  // namespace
 
-size_t bwd_partial_floats(int rows, int cols) { return (size_t)chunks_for(rows) * 2 * cols; }
+constexpr int kLnRowsPerBlock = 64;
+
+size_t bwd_partial_floats(int rows, int cols) {
+  const int blocks = rows <= 0 ? 1 : (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
+  return std::max((size_t)chunks_for(rows), (size_t)blocks) * 2 * cols;
+}
 size_t emb_bwd_partial_floats(int rows, int vocab, int d) { return (size_t)chunks_for(rows) * vocab * d; }
 
+template <int N4>
+cudaError_t ln_bwd_launch(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
+                          float* partial, int rows, int cols, float eps, cudaStream_t st) {
+  const int warps = std::max(1, std::min(8, (int)(196608 / (8 * (size_t)cols))));
+  const size_t smem = (size_t)warps * 2 * cols * sizeof(float);
+  static size_t configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(ln_bwd_kernel<N4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  const int blocks = (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
+  ln_bwd_kernel<N4><<<blocks, 32 * warps, smem, st>>>(x, gamma, gf32, dy, dres, dx, partial, rows, cols,
+                                                     kLnRowsPerBlock, eps);
+  return cudaGetLastError();
+}
+
 void launch_ln_bwd(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
-                   float2* stats, float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps,
-                   cudaStream_t st) {
+                   float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st) {
   if (rows <= 0) {
     cudaMemsetAsync(dgamma, 0, sizeof(float) * cols, st);
     cudaMemsetAsync(dbeta, 0, sizeof(float) * cols, st);
     return;
   }
-  ln_bwd_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(x, gamma, gf32, dy, dres, dx, stats, rows, cols, eps);
-  const int chunks = chunks_for(rows);
-  ln_bwd_cols_kernel<<<dim3((cols + 255) / 256, chunks), 256, 0, st>>>(x, dy, stats, partial, rows, cols, kChunkRows);
-  reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial, chunks, (size_t)2 * cols, cols, 1.f, dgamma);
-  reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial + cols, chunks, (size_t)2 * cols, cols, 1.f, dbeta);
+  const int n4 = (cols / 4 + 31) / 32;  // float4 per lane
+  if (n4 <= 2) ln_bwd_launch<2>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 4) ln_bwd_launch<4>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 8) ln_bwd_launch<8>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 10) ln_bwd_launch<10>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 16) ln_bwd_launch<16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 20) ln_bwd_launch<20>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else ln_bwd_launch<32>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  const int blocks = (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
+  reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial, blocks, (size_t)2 * cols, cols, 1.f, dgamma);
+  reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial + cols, blocks, (size_t)2 * cols, cols, 1.f, dbeta);
 }
 
 void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out, float* partial, __nv_bfloat16* copy,
@@ -199,22 +224,14 @@ void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out
     return;
   }
   const int chunks = chunks_for(rows);
-  const dim3 grid((cols + 255) / 256, chunks);
-  if (bf16_in) colsum_kernel<true><<<grid, 256, 0, st>>>(src, rows, cols, kChunkRows, partial, nullptr);
-  else colsum_kernel<false><<<grid, 256, 0, st>>>(src, rows, cols, kChunkRows, partial, copy);
+  const dim3 grid((cols / 4 + 127) / 128, chunks);
+  if (bf16_in) colsum_kernel<true><<<grid, 128, 0, st>>>(src, rows, cols, kChunkRows, partial, nullptr);
+  else colsum_kernel<false><<<grid, 128, 0, st>>>(src, rows, cols, kChunkRows, partial, copy);
   reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial, chunks, (size_t)cols, cols, 1.f, out);
 }
 
 void launch_reduce_splits(const float* partial, int splits, size_t n, float* out, cudaStream_t st) {
   reduce_chunks_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(partial, splits, n, (int)n, 1.f, out);
-}
-
-void launch_gelu_fwd(const __nv_bfloat16* z, __nv_bfloat16* u, size_t n, cudaStream_t st) {
-  if (n) gelu_fwd_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(z, u, n);
-}
-
-void launch_gelu_bwd(const float* du, const __nv_bfloat16* z, __nv_bfloat16* dz, size_t n, cudaStream_t st) {
-  if (n) gelu_bwd_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(du, z, dz, n);
 }
 
 void launch_emb_bwd(const float* dx, const int32_t* tok, int T, int d, int vocab, float scale, float* partial,

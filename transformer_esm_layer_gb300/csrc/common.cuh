@@ -452,4 +452,24 @@ __device__ __forceinline__ void gelu2_as7126(float& x0, float& x1) {
   f2_unpack(f2_fma(ax, h, half_x), x0, x1);
 }
 
+// Derivative of the exact-erf GELU, Phi(x) + x phi(x), with the same erf form (A&S 7.1.26):
+// with z = |x| / sqrt 2 the exponential of the formula, exp(-z^2) = exp(-x^2 / 2), is also
+// the one of the normal density phi(x) = exp(-x^2 / 2) / sqrt(2 pi), and
+// Phi(x) = 1/2 + sign(x) erf(z) / 2.
+__device__ __forceinline__ float gelu_grad_as7126(float x) {
+  constexpr float kP = 0.3275911f;
+  constexpr float kA1 = 0.5f * 0.254829592f, kA2 = 0.5f * -0.284496736f, kA3 = 0.5f * 1.421413741f,
+                  kA4 = 0.5f * -1.453152027f, kA5 = 0.5f * 1.061405429f;
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(z, kP, 1.f));
+  float poly = fmaf(t, kA5, kA4);
+  poly = fmaf(t, poly, kA3);
+  poly = fmaf(t, poly, kA2);
+  poly = fmaf(t, poly, kA1);
+  poly *= t;                                                   // (1 - erf(z)) / 2
+  const float e = ex2_approx(-1.4426950408889634f * z * z);    // exp(-z^2)
+  const float h = fmaf(-poly, e, 0.5f);                        // erf(z) / 2
+  return fmaf(x * 0.3989422804014327f, e, 0.5f + copysignf(h, x));
+}
+
 }  // namespace esm

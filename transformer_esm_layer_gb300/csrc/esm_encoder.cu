@@ -251,7 +251,7 @@ bool weights_ok(const esm_encoder* h, const esm_weights* w) {
 esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, const void* B, const void* bias, void* out,
                     const int32_t* pos_id, int M, int N, int K, bool fp8, Act out_act, const float* a_scale,
                     const float* b_scale, const float* o_scale, float* o_amax, cudaStream_t st, int rope_cols = -1,
-                    const void* res_in = nullptr) {
+                    const void* res_in = nullptr, void* aux = nullptr) {
   EpiArgs ea{};
   ea.bias = bias;
   ea.bias_f32 = !h->bf16_params();
@@ -266,6 +266,7 @@ esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, co
   ea.o_scale = o_scale;
   ea.o_amax = o_amax;
   ea.res_in = res_in;
+  ea.aux = aux;
   if (rope_cols >= 0) ea.rope_cols = rope_cols;
   if (M <= 0) return ESM_OK;
   if (h->cfg.precision == ESM_FP32) {
@@ -406,7 +407,7 @@ bool config_ok(const esm_config* c) {
 struct TrainLayout {
   size_t tok, x, xmid, y1, qkv, o, lse, y2, z, u;                        // bases
   size_t sx, sy, sqkv, slse, sz;                                         // slab strides
-  size_t dx, dxb, dy, du, dz, dob, dqkv, dqacc, dsum, stats, partial, split, embp;  // scratch
+  size_t dx, dxb, dy, dz, dob, dqkv, dqacc, dsum, partial, split, embp;  // scratch
   size_t split_floats, total;
 };
 
@@ -439,13 +440,11 @@ TrainLayout train_layout(const esm_config& c, int Tm) {
   L.dx = take(4 * T * d);
   L.dxb = take(2 * T * d);
   L.dy = take(4 * T * d);
-  L.du = take(4 * T * f);
   L.dz = take(2 * T * f);
   L.dob = take(2 * T * d);
   L.dqkv = take(2 * T * 3 * d);
   L.dqacc = take(4 * T * d);
   L.dsum = take(4 * T * H);
-  L.stats = take(8 * T);
   const size_t widest = std::max(3 * d, f);
   L.partial = take(4 * bwd_partial_floats((int)T, (int)widest));
   L.split_floats = (size_t)kMaxKSplit * std::max(f * d, 3 * d * d);
@@ -471,9 +470,10 @@ int choose_ksplit(int tiles, int kb_total, int clusters) {
   return best;
 }
 
-// out[M, K] = dY[M, N] W with W stored [N, K] (bf16); fp32 or bf16 out.
+// out[M, K] = dY[M, N] W with W stored [N, K] (bf16); fp32 or bf16 out; with gelu_z
+// (bf16 [M, K], the forward's fc1 pre-activation) the bf16 out is multiplied by GELU'(z).
 esm_status run_dgrad(esm_encoder* h, const void* dY, const void* W, void* out, bool out_bf16, int M, int N, int K,
-                     cudaStream_t st) {
+                     cudaStream_t st, const void* gelu_z = nullptr) {
   if (M <= 0) return ESM_OK;
   const CUtensorMap* ma = h->map(dY, (uint64_t)M, (uint64_t)N, (uint32_t)gemm_tc_a_box_rows(), 2);
   const CUtensorMap* mb = h->map(W, (uint64_t)N, (uint64_t)K, (uint32_t)gemm_tc_mn_box_rows(), 2);
@@ -482,10 +482,10 @@ esm_status run_dgrad(esm_encoder* h, const void* dY, const void* W, void* out, b
   EpiArgs ea{};
   ea.out = out;
   ea.rope_cols = 0;
+  ea.aux = const_cast<void*>(gelu_z);
+  const GemmBwd kind = gelu_z ? GemmBwd::DGRAD_GELU : out_bf16 ? GemmBwd::DGRAD_BF16 : GemmBwd::DGRAD_F32;
   cudaError_t e;
-  PROF(h, P_BWD_GEMM, st, 1,
-       e = launch_gemm_tc_bwd(out_bf16 ? GemmBwd::DGRAD_BF16 : GemmBwd::DGRAD_F32, ma, mb, mo, M, K, N, 1, ea,
-                              h->num_sms, h->d_err, st));
+  PROF(h, P_BWD_GEMM, st, 1, e = launch_gemm_tc_bwd(kind, ma, mb, mo, M, K, N, 1, ea, h->num_sms, h->d_err, st));
   return cuda_status(e);
 }
 
@@ -578,12 +578,10 @@ esm_status train_forward_impl(esm_encoder* h, const esm_weights* w, const int32_
     PROF(h, P_LN, st, 1,
          launch_layernorm(xmid, w->ln2_g[l], w->ln2_b[l], false, y2, Act::BF16, T, d, c.ln_eps, nullptr, nullptr,
                           nullptr, nullptr, nullptr, st));
-    // fc1 keeps its pre-activation z for GELU'(z); u = GELU(z) feeds fc2
-    s = run_gemm(h, P_FC1, ESM_EPI_QKV_ROPE, y2, w->w_1[l], w->b_1[l], z, nullptr, T, f, d, false, Act::BF16, nullptr,
-                 nullptr, nullptr, nullptr, st, 0);
+    // fc1: u = GELU(z) feeds fc2; the epilogue also keeps the pre-activation z for GELU'(z)
+    s = run_gemm(h, P_FC1, ESM_EPI_GELU, y2, w->w_1[l], w->b_1[l], u, nullptr, T, f, d, false, Act::BF16, nullptr,
+                 nullptr, nullptr, nullptr, st, -1, nullptr, z);
     if (s != ESM_OK) return s;
-    PROF(h, P_OTHER, st, 1,
-         launch_gelu_fwd(static_cast<const __nv_bfloat16*>(z), static_cast<__nv_bfloat16*>(u), (size_t)T * f, st));
     s = run_gemm(h, P_FC2, ESM_EPI_RESIDUAL, u, w->w_2[l], w->b_2[l], xnext, nullptr, T, d, f, false, Act::F32, nullptr,
                  nullptr, nullptr, nullptr, st, -1, xmid);
     if (s != ESM_OK) return s;
@@ -614,13 +612,11 @@ esm_status backward_impl(esm_encoder* h, const esm_weights* w, const float* d_ou
   float* dx = reinterpret_cast<float*>(tb + R.dx);
   __nv_bfloat16* dxb = reinterpret_cast<__nv_bfloat16*>(tb + R.dxb);
   float* dy = reinterpret_cast<float*>(tb + R.dy);
-  float* du = reinterpret_cast<float*>(tb + R.du);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(tb + R.dz);
   __nv_bfloat16* dob = reinterpret_cast<__nv_bfloat16*>(tb + R.dob);
   __nv_bfloat16* dqkv = reinterpret_cast<__nv_bfloat16*>(tb + R.dqkv);
   float* dqacc = reinterpret_cast<float*>(tb + R.dqacc);
   float* dsum = reinterpret_cast<float*>(tb + R.dsum);
-  float2* stats = reinterpret_cast<float2*>(tb + R.stats);
   float* partial = reinterpret_cast<float*>(tb + R.partial);
   float* split = reinterpret_cast<float*>(tb + R.split);
   float* embp = reinterpret_cast<float*>(tb + R.embp);
@@ -629,7 +625,7 @@ esm_status backward_impl(esm_encoder* h, const esm_weights* w, const float* d_ou
   const float* xl = reinterpret_cast<const float*>(tb + R.x + R.sx * c.num_layers);
   if (c.final_ln) {
     PROF(h, P_LN, st, 4,
-         launch_ln_bwd(xl, w->lnf_g, false, d_out, nullptr, dx, stats, g->lnf_g, g->lnf_b, partial, T, d, c.ln_eps, st));
+         launch_ln_bwd(xl, w->lnf_g, false, d_out, nullptr, dx, g->lnf_g, g->lnf_b, partial, T, d, c.ln_eps, st));
   } else if (cudaMemcpyAsync(dx, d_out, 4 * (size_t)T * d, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
     return ESM_ERR_CUDA;
   }
@@ -646,14 +642,13 @@ esm_status backward_impl(esm_encoder* h, const esm_weights* w, const float* d_ou
     // ---- MLP block: x_{l+1} = xmid + GELU(LN2(xmid) W1^T + b1) W2^T + b2
     PROF(h, P_OTHER, st, 2, launch_colsum(dx, false, T, d, g->b_2[l], partial, dxb, st));
     if ((s = run_wgrad(h, dxb, u, g->w_2[l], T, d, f, split, R.split_floats, st)) != ESM_OK) return s;
-    if ((s = run_dgrad(h, dxb, w->w_2[l], du, false, T, d, f, st)) != ESM_OK) return s;
-    PROF(h, P_OTHER, st, 1,
-         launch_gelu_bwd(du, static_cast<const __nv_bfloat16*>(z), dz, (size_t)T * f, st));
+    // dz = (dx W2) * GELU'(z), in the input-gradient GEMM's epilogue
+    if ((s = run_dgrad(h, dxb, w->w_2[l], dz, true, T, d, f, st, z)) != ESM_OK) return s;
     PROF(h, P_OTHER, st, 2, launch_colsum(dz, true, T, f, g->b_1[l], partial, nullptr, st));
     if ((s = run_wgrad(h, dz, y2, g->w_1[l], T, f, d, split, R.split_floats, st)) != ESM_OK) return s;
     if ((s = run_dgrad(h, dz, w->w_1[l], dy, false, T, f, d, st)) != ESM_OK) return s;
     PROF(h, P_LN, st, 4,
-         launch_ln_bwd(xmid, w->ln2_g[l], false, dy, dx, dx, stats, g->ln2_g[l], g->ln2_b[l], partial, T, d, c.ln_eps,
+         launch_ln_bwd(xmid, w->ln2_g[l], false, dy, dx, dx, g->ln2_g[l], g->ln2_b[l], partial, T, d, c.ln_eps,
                        st));
     // ---- attention block: xmid = x + Attn(LN1(x)) Wo^T + bo
     PROF(h, P_OTHER, st, 2, launch_colsum(dx, false, T, d, g->b_o[l], partial, dxb, st));
@@ -673,7 +668,7 @@ esm_status backward_impl(esm_encoder* h, const esm_weights* w, const float* d_ou
     if ((s = run_wgrad(h, dqkv, y1, g->w_qkv[l], T, 3 * d, d, split, R.split_floats, st)) != ESM_OK) return s;
     if ((s = run_dgrad(h, dqkv, w->w_qkv[l], dy, false, T, 3 * d, d, st)) != ESM_OK) return s;
     PROF(h, P_LN, st, 4,
-         launch_ln_bwd(x, w->ln1_g[l], false, dy, dx, dx, stats, g->ln1_g[l], g->ln1_b[l], partial, T, d, c.ln_eps, st));
+         launch_ln_bwd(x, w->ln1_g[l], false, dy, dx, dx, g->ln1_g[l], g->ln1_b[l], partial, T, d, c.ln_eps, st));
   }
   PROF(h, P_OTHER, st, 2,
        launch_emb_bwd(dx, reinterpret_cast<const int32_t*>(tb + R.tok), T, d, c.vocab, c.emb_scale, embp, g->emb, st));
@@ -1016,7 +1011,7 @@ esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu
 // ------------------------------------------------------------------ training
 esm_status esm_encoder_train_buffer_size(const esm_encoder_t* h, int max_tokens, size_t* bytes) {
   if (!h || !bytes || max_tokens < 0) return ESM_ERR_INVALID_ARG;
-  if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+  if (h->cfg.precision != ESM_BF16 || h->cfg.hidden > 4096) return ESM_ERR_UNSUPPORTED;
   *bytes = train_layout(h->cfg, max_tokens).total;
   return ESM_OK;
 }
@@ -1026,7 +1021,7 @@ esm_status esm_encoder_forward_train(esm_encoder_t* h, const esm_weights* w, con
                                      void* hidden_out, void* train_buf, size_t train_bytes, void* workspace,
                                      size_t workspace_bytes, esm_stream_t stream) {
   if (!h || total_tokens <= 0 || num_seqs <= 0) return ESM_ERR_INVALID_ARG;
-  if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+  if (h->cfg.precision != ESM_BF16 || h->cfg.hidden > 4096) return ESM_ERR_UNSUPPORTED;
   if (!token_ids || !cu_seqlens || !hidden_out || !aligned(hidden_out, 16)) return ESM_ERR_INVALID_ARG;
   if (max_seqlen <= 0 || max_seqlen > h->cfg.max_positions) return ESM_ERR_INVALID_ARG;
   if (!weights_ok(h, w)) return ESM_ERR_INVALID_ARG;
@@ -1074,8 +1069,8 @@ esm_status esm_op_gemm_wgrad(esm_encoder_t* h, const void* dY, const void* X, fl
 }
 
 static size_t ln_bwd_ws_bytes(int rows, int cols, size_t* off_partial) {
-  *off_partial = align256(8 * (size_t)(rows > 0 ? rows : 1));
-  return *off_partial + align256(4 * bwd_partial_floats(rows, cols));
+  *off_partial = 0;
+  return align256(4 * bwd_partial_floats(rows, cols));
 }
 
 esm_status esm_op_layernorm_backward_workspace_size(const esm_encoder_t* h, int rows, int cols, size_t* bytes) {
@@ -1088,16 +1083,16 @@ esm_status esm_op_layernorm_backward_workspace_size(const esm_encoder_t* h, int 
 esm_status esm_op_layernorm_backward(esm_encoder_t* h, const float* x, const void* gamma, const float* dy,
                                      const float* dres, float* dx, float* dgamma, float* dbeta, int rows, int cols,
                                      void* workspace, size_t workspace_bytes, esm_stream_t stream) {
-  if (!h || !x || !gamma || !dy || !dx || !dgamma || !dbeta || rows < 0 || cols <= 0 || cols % 4) return ESM_ERR_INVALID_ARG;
+  if (!h || !x || !gamma || !dy || !dx || !dgamma || !dbeta || rows < 0 || cols <= 0 || cols % 4 || cols > 4096)
+    return ESM_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(dx, 16) || (dres && !aligned(dres, 16)) || !aligned(gamma, 16))
     return ESM_ERR_INVALID_ARG;
   size_t off;
   const size_t need = ln_bwd_ws_bytes(rows, cols, &off);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ESM_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  launch_ln_bwd(x, gamma, !h->bf16_params(), dy, dres, dx, reinterpret_cast<float2*>(ws),
-                dgamma, dbeta, reinterpret_cast<float*>(ws + off), rows, cols, h->cfg.ln_eps,
-                reinterpret_cast<cudaStream_t>(stream));
+  launch_ln_bwd(x, gamma, !h->bf16_params(), dy, dres, dx, dgamma, dbeta, reinterpret_cast<float*>(ws + off), rows,
+                cols, h->cfg.ln_eps, reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 

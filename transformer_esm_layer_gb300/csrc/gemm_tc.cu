@@ -576,6 +576,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             stage_bf16x16(buf, r, 2 * h, a);
             stage_bf16x16(buf, r, 4 + 2 * h, bq);
           }
+        } else if constexpr (EPI == kEpiDgelu) {  // bf16 output, 64 columns: acc * GELU'(z)
+          float v0[32], v1[32];
+          tmem_ld32(tbase + c * CH::kCols, v0);
+          tmem_ld32(tbase + c * CH::kCols + 32, v1);
+          if (c == nch - 1) release_acc();
+          uint4 zz[8];
+          const uint4* zr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ea.aux) +
+                                                           (size_t)(row < M ? row : 0) * N + col);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) zz[u] = __ldg(zr + u);
+          const __nv_bfloat162* zh = reinterpret_cast<const __nv_bfloat162*>(zz);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 a = __bfloat1622float2(zh[i]), b = __bfloat1622float2(zh[16 + i]);
+            v0[2 * i] *= gelu_grad_as7126(a.x);
+            v0[2 * i + 1] *= gelu_grad_as7126(a.y);
+            v1[2 * i] *= gelu_grad_as7126(b.x);
+            v1[2 * i + 1] *= gelu_grad_as7126(b.y);
+          }
+          stage_bf16x32(buf, r, 0, v0);
+          stage_bf16x32(buf, r, 4, v1);
         } else {  // bf16 output, 64 columns: GELU
           float v0[32], v1[32];
           tmem_ld32(tbase + c * CH::kCols, v0);
@@ -583,6 +604,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (c == nch - 1) release_acc();
           scale_add_bias<32>(ea, col, acc_scale, v0);
           scale_add_bias<32>(ea, col + 32, acc_scale, v1);
+          if (ea.aux != nullptr && row < M) {  // training forward: keep the pre-activation
+            uint4* zr = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ea.aux) + (size_t)row * N + col);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              zr[u] = make_uint4(pack_bf16x2(v0[8 * u], v0[8 * u + 1]), pack_bf16x2(v0[8 * u + 2], v0[8 * u + 3]),
+                                 pack_bf16x2(v0[8 * u + 4], v0[8 * u + 5]), pack_bf16x2(v0[8 * u + 6], v0[8 * u + 7]));
+              zr[4 + u] = make_uint4(pack_bf16x2(v1[8 * u], v1[8 * u + 1]), pack_bf16x2(v1[8 * u + 2], v1[8 * u + 3]),
+                                     pack_bf16x2(v1[8 * u + 4], v1[8 * u + 5]), pack_bf16x2(v1[8 * u + 6], v1[8 * u + 7]));
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 32; i += 2) { gelu2_as7126(v0[i], v0[i + 1]); gelu2_as7126(v1[i], v1[i + 1]); }
           stage_bf16x32(buf, r, 0, v0);
@@ -713,6 +744,8 @@ cudaError_t launch_gemm_tc_bwd(GemmBwd kind, const CUtensorMap* tmA, const CUten
       return launch_impl<ESM_EPI_BIAS_F32, false, Act::F32, false, true>(tmA, tmB, tmO, M, N, K, ea, num_sms, err, st);
     case GemmBwd::DGRAD_BF16:
       return launch_impl<ESM_EPI_QKV_ROPE, false, Act::BF16, false, true>(tmA, tmB, tmO, M, N, K, ea, num_sms, err, st);
+    case GemmBwd::DGRAD_GELU:
+      return launch_impl<kEpiDgelu, false, Act::BF16, false, true>(tmA, tmB, tmO, M, N, K, ea, num_sms, err, st);
     case GemmBwd::WGRAD_F32:
       return launch_impl<ESM_EPI_BIAS_F32, false, Act::F32, true, true>(tmA, tmB, tmO, M, N, K, ea, num_sms, err, st,
                                                                        ksplit);

@@ -79,7 +79,11 @@ struct EpiArgs {
   const float* o_scale;   // FP8 GELU output: quantisation scale (device)
   float* o_amax;          // FP8 GELU output: amax (device)
   const void* res_in;     // ESM_EPI_RESIDUAL: residual read from here instead of out (NULL: in place)
+  void* aux;              // ESM_EPI_GELU: also store the pre-activation here (bf16 [M, N]; NULL: no);
+                          // kEpiDgelu: the forward's pre-activation z to multiply by GELU'(z)
 };
+// Epilogue of the input gradient through fc1's GELU: out = acc * GELU'(z) (bf16), z = aux.
+constexpr int kEpiDgelu = 16;
 
 // tcgen05 GEMM: A [M,K] bf16 (or e4m3), B [N,K] bf16 (or e4m3); K % 64 == 0 (bf16) or
 // K % 128 == 0 (e4m3); N % 256 == 0.
@@ -103,7 +107,8 @@ cudaError_t launch_gemm_tc(esm_epilogue epi, bool fp8, Act out_act, const CUtens
 //     K tokens), both 64 x 64-box maps; with ksplit > 1 the output map covers
 //     [ksplit * M, N] partial sums (M % 256 == 0).
 // N % 256 == 0; K any (the last K-slice is zero-filled by the maps).
-enum class GemmBwd { DGRAD_F32, DGRAD_BF16, WGRAD_F32 };
+//   DGRAD_GELU: as DGRAD_BF16, times GELU'(z) with z = ea.aux (bf16 [M, N]).
+enum class GemmBwd { DGRAD_F32, DGRAD_BF16, DGRAD_GELU, WGRAD_F32 };
 int gemm_tc_mn_box_rows();
 int gemm_tc_max_clusters(int num_sms);
 cudaError_t launch_gemm_tc_bwd(GemmBwd kind, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmO,
@@ -149,18 +154,15 @@ cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap
 size_t bwd_partial_floats(int rows, int cols);
 size_t emb_bwd_partial_floats(int rows, int vocab, int d);
 // LayerNorm backward: dx = dres + dLN/dx (dres may be NULL or alias dx), dgamma, dbeta
-// (float32 [cols]); stats float2 [rows] scratch, partial bwd_partial_floats(rows, cols).
+// (float32 [cols]); partial: bwd_partial_floats(rows, cols) floats of scratch.  cols % 4 == 0.
 void launch_ln_bwd(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
-                   float2* stats, float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps,
-                   cudaStream_t st);
+                   float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st);
 // out[c] = sum_r src[r][c] (fp32 or bf16 rows); copy (fp32 input only, may be NULL): the
-// rows as bf16.  partial: bwd_partial_floats(rows, cols) / 2 floats.
+// rows as bf16.  partial: bwd_partial_floats(rows, cols) / 2 floats.  cols % 4 == 0.
 void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out, float* partial, __nv_bfloat16* copy,
                    cudaStream_t st);
 // out[i] = sum_s partial[s * n + i] (split-K partial products, in split order).
 void launch_reduce_splits(const float* partial, int splits, size_t n, float* out, cudaStream_t st);
-void launch_gelu_fwd(const __nv_bfloat16* z, __nv_bfloat16* u, size_t n, cudaStream_t st);
-void launch_gelu_bwd(const float* du, const __nv_bfloat16* z, __nv_bfloat16* dz, size_t n, cudaStream_t st);
 // demb[v] = scale * sum over tokens t with tok[t] == v of dx[t] (float32 [vocab, d]).
 void launch_emb_bwd(const float* dx, const int32_t* tok, int T, int d, int vocab, float scale, float* partial,
                     float* demb, cudaStream_t st);
