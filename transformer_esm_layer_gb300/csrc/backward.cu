@@ -36,7 +36,7 @@ __device__ __forceinline__ float4 ld_param4(const void* p, int c, bool f32) {
 // dy * xhat and dy into its own shared-memory slice, and at the end the block adds the
 // slices in warp order into partial[block][0 | 1][cols].
 template <int N4>
-__global__ void __launch_bounds__(256) ln_bwd_kernel(const float* __restrict__ x, const void* __restrict__ gamma,
+__global__ void __launch_bounds__(256, N4 <= 10 ? 2 : 1) ln_bwd_kernel(const float* __restrict__ x, const void* __restrict__ gamma,
                                                      bool gf32, const float* __restrict__ dy, const float* dres,
                                                      float* dx, float* __restrict__ partial, int rows, int cols,
                                                      int rows_per_block, float eps) {
@@ -137,14 +137,32 @@ __global__ void __launch_bounds__(128) colsum_kernel(const void* __restrict__ sr
   *reinterpret_cast<float4*>(partial + (size_t)chunk * cols + 4 * c4) = a;
 }
 
-// out[i] = scale * sum_k partial[k * stride + i], k in index order.
-__global__ void reduce_chunks_kernel(const float* __restrict__ partial, int chunks, size_t stride, int n, float scale,
-                                     float* __restrict__ out) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
+// out[i] = scale * sum_k partial[k * stride + i] in a fixed order: a block owns 32
+// consecutive i; warp w adds the chunks k = w, w + 8, ... (lane = i, coalesced), then the
+// eight warp sums are added in warp order.
+__global__ void __launch_bounds__(256) reduce_chunks_kernel(const float* __restrict__ partial, int chunks,
+                                                            size_t stride, int n, float scale,
+                                                            float* __restrict__ out) {
+  __shared__ float part[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 32 + lane;
   float a = 0.f;
-  for (int k = 0; k < chunks; ++k) a += partial[(size_t)k * stride + i];
-  out[i] = a * scale;
+  if (i < n) {
+#pragma unroll 4
+    for (int k = warp; k < chunks; k += 8) a += __ldg(partial + (size_t)k * stride + i);
+  }
+  part[warp][lane] = a;
+  __syncthreads();
+  if (warp == 0 && i < n) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += part[w][lane];
+    out[i] = t * scale;
+  }
+}
+
+void reduce_chunks(const float* partial, int chunks, size_t stride, int n, float scale, float* out, cudaStream_t st) {
+  if (n > 0) reduce_chunks_kernel<<<(n + 31) / 32, 256, 0, st>>>(partial, chunks, stride, n, scale, out);
 }
 
 // partial[chunk][v][c] = sum of dx[t][c] over the chunk's tokens t with tok[t] == v (each
@@ -213,8 +231,8 @@ void launch_ln_bwd(const float* x, const void* gamma, bool gf32, const float* dy
   else if (n4 <= 20) ln_bwd_launch<20>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
   else ln_bwd_launch<32>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
   const int blocks = (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
-  reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial, blocks, (size_t)2 * cols, cols, 1.f, dgamma);
-  reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial + cols, blocks, (size_t)2 * cols, cols, 1.f, dbeta);
+  reduce_chunks(partial, blocks, (size_t)2 * cols, cols, 1.f, dgamma, st);
+  reduce_chunks(partial + cols, blocks, (size_t)2 * cols, cols, 1.f, dbeta, st);
 }
 
 void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out, float* partial, __nv_bfloat16* copy,
@@ -227,11 +245,11 @@ void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out
   const dim3 grid((cols / 4 + 127) / 128, chunks);
   if (bf16_in) colsum_kernel<true><<<grid, 128, 0, st>>>(src, rows, cols, kChunkRows, partial, nullptr);
   else colsum_kernel<false><<<grid, 128, 0, st>>>(src, rows, cols, kChunkRows, partial, copy);
-  reduce_chunks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(partial, chunks, (size_t)cols, cols, 1.f, out);
+  reduce_chunks(partial, chunks, (size_t)cols, cols, 1.f, out, st);
 }
 
 void launch_reduce_splits(const float* partial, int splits, size_t n, float* out, cudaStream_t st) {
-  reduce_chunks_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(partial, splits, n, (int)n, 1.f, out);
+  reduce_chunks(partial, splits, n, (int)n, 1.f, out, st);
 }
 
 void launch_emb_bwd(const float* dx, const int32_t* tok, int T, int d, int vocab, float scale, float* partial,
@@ -243,8 +261,7 @@ void launch_emb_bwd(const float* dx, const int32_t* tok, int T, int d, int vocab
   const int chunks = chunks_for(T);
   emb_bwd_kernel<<<dim3((d + 127) / 128, chunks), 128, sizeof(float) * 128 * vocab, st>>>(dx, tok, T, d, vocab,
                                                                                           kChunkRows, partial);
-  reduce_chunks_kernel<<<(vocab * d + 255) / 256, 256, 0, st>>>(partial, chunks, (size_t)vocab * d, vocab * d, scale,
-                                                                demb);
+  reduce_chunks(partial, chunks, (size_t)vocab * d, vocab * d, scale, demb, st);
 }
 
 }  // namespace esm
