@@ -73,6 +73,27 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// Two 32-lane x 16-column TMEM loads (S^T and dP^T of the same queries) and one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16], float (&b)[16]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[16 + i]);
+  }
+}
+
 struct BItem {
   int k0, krows, s0, slen, h, nq;
 };
@@ -240,18 +261,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* sDS = base + OFF_DS + wg * TILE;
     bool ok = true;
     int g = 0, n = 0;
+    // slot r of a query tile: lse (warpgroup 0, to log2 units) or D (warpgroup 1) of query r;
+    // loaded one tile ahead so the load latency overlaps the previous tile
+    auto stat = [&](const BItem& y, int i) -> float {
+      const int q0 = y.s0 + i * TB;
+      if (r >= min(TB, y.slen - i * TB)) return 0.f;
+      return wg == 0 ? __ldg(lse + (size_t)(q0 + r) * heads + y.h) * kLog2e : __ldg(dsum + (size_t)(q0 + r) * heads + y.h);
+    };
+    float st_next = (int)blockIdx.x < n_items ? stat(bitem(pb, blockIdx.x, heads), 0) : 0.f;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
       const BItem x = bitem(pb, it, heads);
       const bool kval = r < x.krows;
       for (int i = 0; i < x.nq; ++i, ++g) {
-        const int q0 = x.s0 + i * TB, qvalid = min(TB, x.slen - i * TB);
-        // this tile's lse (to log2 units; warpgroup 0) and D (warpgroup 1), one slot per
-        // thread, into buffer g & 1 (its previous readers, tile g - 2, are done: every thread
-        // arrived for tile g - 1 after finishing tile g - 2)
+        const int qvalid = min(TB, x.slen - i * TB);
+        // this tile's slots into buffer g & 1 (its previous readers, tile g - 2, are done:
+        // every thread arrived for tile g - 1 after finishing tile g - 2)
         const int sb = g & 1;
-        if (wg == 0) sm->lse2[sb][r] = r < qvalid ? __ldg(lse + (size_t)(q0 + r) * heads + x.h) * kLog2e : 0.f;
-        else sm->dsum[sb][r] = r < qvalid ? __ldg(dsum + (size_t)(q0 + r) * heads + x.h) : 0.f;
+        if (wg == 0) sm->lse2[sb][r] = st_next;
+        else sm->dsum[sb][r] = st_next;
         mbar_arrive(&sm->stat_full[sb]);
+        if (i + 1 < x.nq) st_next = stat(x, i + 1);
+        else if (it + (int)gridDim.x < n_items) st_next = stat(bitem(pb, it + gridDim.x, heads), 0);
         if (!mbar_wait_warp(&sm->stat_full[sb], (uint32_t)(g >> 1) & 1u)) { ok = false; break; }
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
@@ -261,8 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int sub = 0; sub < 4; ++sub) {
           const int cq = 64 * wg + 16 * sub;  // first query (column) of the sub-chunk
           float sv[16], dp[16];
-          tmem_ld16(tmem + lane_off + COL_S + cq, sv);
-          tmem_ld16(tmem + lane_off + COL_DP + cq, dp);
+          tmem_ld16x2(tmem + lane_off + COL_S + cq, tmem + lane_off + COL_DP + cq, sv, dp);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int q = cq + 2 * j;

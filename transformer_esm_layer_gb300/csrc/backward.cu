@@ -161,8 +161,25 @@ __global__ void __launch_bounds__(256) reduce_chunks_kernel(const float* __restr
   }
 }
 
-void reduce_chunks(const float* partial, int chunks, size_t stride, int n, float scale, float* out, cudaStream_t st) {
-  if (n > 0) reduce_chunks_kernel<<<(n + 31) / 32, 256, 0, st>>>(partial, chunks, stride, n, scale, out);
+// Few chunks over many elements (split-K partial products): one thread per element.
+__global__ void reduce_few_chunks_kernel(const float* __restrict__ partial, int chunks, size_t stride, size_t n,
+                                         float scale, float* __restrict__ out) {
+  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < chunks; ++k) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(partial + (size_t)k * stride + i));
+    a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+  }
+  *reinterpret_cast<float4*>(out + i) = make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale);
+}
+
+void reduce_chunks(const float* partial, int chunks, size_t stride, size_t n, float scale, float* out, cudaStream_t st) {
+  if (n == 0) return;
+  if (chunks <= 16 && n % 4 == 0 && stride % 4 == 0)
+    reduce_few_chunks_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, st>>>(partial, chunks, stride, n, scale, out);
+  else
+    reduce_chunks_kernel<<<(unsigned)((n + 31) / 32), 256, 0, st>>>(partial, chunks, stride, (int)n, scale, out);
 }
 
 // partial[chunk][v][c] = sum of dx[t][c] over the chunk's tokens t with tok[t] == v (each
@@ -184,9 +201,11 @@ __global__ void emb_bwd_kernel(const float* __restrict__ dx, const int32_t* __re
   }
 }
 
-constexpr int kChunkRows = 128;
+constexpr int kChunkRows = 32;
 
 int chunks_for(int rows) { return rows <= 0 ? 1 : (rows + kChunkRows - 1) / kChunkRows; }
+constexpr int kEmbChunkRows = 256;  // tokens per embedding-gradient chunk
+int emb_chunks_for(int rows) { return rows <= 0 ? 1 : (rows + kEmbChunkRows - 1) / kEmbChunkRows; }
 
 }  // namespace
 
@@ -196,7 +215,7 @@ size_t bwd_partial_floats(int rows, int cols) {
   const int blocks = rows <= 0 ? 1 : (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
   return std::max((size_t)chunks_for(rows), (size_t)blocks) * 2 * cols;
 }
-size_t emb_bwd_partial_floats(int rows, int vocab, int d) { return (size_t)chunks_for(rows) * vocab * d; }
+size_t emb_bwd_partial_floats(int rows, int vocab, int d) { return (size_t)emb_chunks_for(rows) * vocab * d; }
 
 template <int N4>
 cudaError_t ln_bwd_launch(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
@@ -258,9 +277,9 @@ void launch_emb_bwd(const float* dx, const int32_t* tok, int T, int d, int vocab
     cudaMemsetAsync(demb, 0, sizeof(float) * (size_t)vocab * d, st);
     return;
   }
-  const int chunks = chunks_for(T);
+  const int chunks = emb_chunks_for(T);
   emb_bwd_kernel<<<dim3((d + 127) / 128, chunks), 128, sizeof(float) * 128 * vocab, st>>>(dx, tok, T, d, vocab,
-                                                                                          kChunkRows, partial);
+                                                                                          kEmbChunkRows, partial);
   reduce_chunks(partial, chunks, (size_t)vocab * d, vocab * d, scale, demb, st);
 }
 
