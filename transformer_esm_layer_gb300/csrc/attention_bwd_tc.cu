@@ -28,9 +28,9 @@
 //                writes both as bf16 into shared memory (K-major, 128-byte swizzle); at the end
 //                of the item warpgroup 0 scales dK, turns it back through RoPE and stores it,
 //                warpgroup 1 stores dV (bf16);
-//   warps 12..15 thread r owns query r of the tile: reads dQ_i from TMEM and adds it into
-//                an fp32 accumulator in global memory with vector reductions (several key
-//                tiles contribute to each query row).
+//   warps 12..15 thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
+//                memory and adds it into an fp32 accumulator in global memory with TMA
+//                reduce-add (several key tiles contribute to each query row).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error bit and stops.
 #include "common.cuh"
 #include "internal.h"
@@ -55,9 +55,10 @@ struct BwdSmem {
   float lse2[2][TB];  // query tile g (buffer g & 1): log2-sum-exp2 of the scaled scores
   float dsum[2][TB];  // and D
 };
-// [dS^T 32K][P^T 32K][Q0][Q1][dO0][dO1][K][V] then BwdSmem
+// [dS^T 32K][P^T 32K][Q0][Q1][dO0][dO1][K][V][dQ staging 4 x 8K] then BwdSmem
 constexpr int OFF_DS = 0, OFF_P = 2 * TILE, OFF_Q = 4 * TILE, OFF_DO = 6 * TILE, OFF_K = 8 * TILE,
-              OFF_V = 9 * TILE, OFF_BAR = 10 * TILE;
+              OFF_V = 9 * TILE, OFF_DQ = 10 * TILE, OFF_BAR = 12 * TILE;
+constexpr int DQ_WARP_BYTES = 32 * 256;  // one dQ warp's 32 rows x 64 fp32, as two 32 x 128-byte boxes
 constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(BwdSmem) + 1024;
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -68,10 +69,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // 16-byte unit j of row r of a 128-row x 128-byte tile with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
 
 // Two 32-lane x 16-column TMEM loads (S^T and dP^T of the same queries) and one wait.
 __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16], float (&b)[16]) {
@@ -111,8 +108,8 @@ __device__ __forceinline__ BItem bitem(const PackBuffers& pb, int it, int heads)
 
 __global__ void __launch_bounds__(THREADS, 1)
     attention_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                            const float* __restrict__ lse, const float* __restrict__ dsum,
-                            float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dqkv, int d, int heads,
+                            const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+                            const float* __restrict__ dsum, __nv_bfloat16* __restrict__ dqkv, int d, int heads,
                             PackBuffers pb, const float2* __restrict__ rope, int max_pos, unsigned* err) {
   const int n_items = *pb.work_count * heads;
   if ((int)blockIdx.x >= n_items) return;  // whole CTA, before any barrier or TMEM use
@@ -367,9 +364,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ accumulation
+    // Each warp stages its 32 rows of dQ_i (fp32, 128-byte swizzle, two 32-column boxes) and
+    // adds them into the global accumulator with TMA reduce-add; rows of queries past the
+    // sequence end hold exact zeros (their dS columns are zero), so adding them is harmless.
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // query row of the tile
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    uint8_t* stage = base + OFF_DQ + wq * DQ_WARP_BYTES;
+    if (lane == 0) tma_prefetch_desc(&tm_dq);
     bool ok = true;
     int g = 0;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -383,16 +385,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->dq_free);
-        if (r < min(TB, x.slen - i * TB)) {
-          float* dst = dq_acc + (size_t)(x.s0 + i * TB + r) * d + x.h * DH;
+        // the previous tile's reduce must have finished reading the staging rows
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
 #pragma unroll
-          for (int u = 0; u < 8; ++u) red_add_v4(dst + 4 * u, a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + 32 + 4 * u, b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t off = (uint32_t)(lane * 128 + ((u ^ (lane & 7)) << 4));
+          *reinterpret_cast<float4*>(stage + off) = make_float4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+          *reinterpret_cast<float4*>(stage + 4096 + off) =
+              make_float4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row = x.s0 + i * TB + wq * 32;
+          tma_reduce_add_2d(&tm_dq, x.h * DH, row, stage);
+          tma_reduce_add_2d(&tm_dq, x.h * DH + 32, row, stage + 4096);
+          bulk_commit();
         }
       }
     }
+    if (lane == 0) bulk_wait_all();  // reduces complete before the CTA may exit
+    __syncwarp();
     if (!ok) {
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
@@ -462,7 +476,8 @@ __global__ void attention_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_b
 
 int attention_bwd_tc_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const __nv_bfloat16* o,
+cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const CUtensorMap* tm_dq,
+                                    const __nv_bfloat16* o,
                                     const __nv_bfloat16* dout, const float* lse, float* dsum, float* dq_acc,
                                     __nv_bfloat16* dqkv, int T, int d, int heads, int max_items, const PackBuffers& pb,
                                     const float2* rope, int max_pos, int num_sms, unsigned* err, cudaStream_t st) {
@@ -480,7 +495,7 @@ cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap
   if (e != cudaSuccess) return e;
   const long long items = (long long)max_items * heads;
   const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
-  attention_bwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, *tm_do, lse, dsum, dq_acc, dqkv, d, heads, pb,
+  attention_bwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, *tm_do, *tm_dq, lse, dsum, dqkv, d, heads, pb,
                                                              rope, max_pos, err);
   const long long tq = (long long)T * (d / 2);
   attention_bwd_dq_kernel<<<(unsigned)((tq + 255) / 256), 256, 0, st>>>(dq_acc, dqkv, pb.pos_id, rope, max_pos, T, d);

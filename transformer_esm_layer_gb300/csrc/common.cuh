@@ -170,6 +170,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int x, int y,
                "r"(x), "r"(y), "r"(smem_u32(smem_src))
                : "memory");
 }
+// Add a shared-memory tile element-wise into global memory through the tensor map (the TMA
+// engine performs the fp32 additions atomically per element; rows outside the tensor are
+// dropped).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, int x, int y, const void* smem_src) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups of this thread still read shared memory.
 template <int N>

@@ -658,8 +658,9 @@ esm_status backward_impl(esm_encoder* h, const esm_weights* w, const float* d_ou
       ProfScope _ps(h, P_ATTN, st, 4);
       const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
       const CUtensorMap* td = h->map(dob, (uint64_t)T, (uint64_t)d, 128, 2);
-      if (!tq || !td) return ESM_ERR_CUDA;
-      if (launch_attention_bwd_tc(tq, td, static_cast<const __nv_bfloat16*>(o), dob, lse, dsum, dqacc, dqkv, T, d, H,
+      const CUtensorMap* tdq = h->map(dqacc, (uint64_t)T, (uint64_t)d, 32, 4);
+      if (!tq || !td || !tdq) return ESM_ERR_CUDA;
+      if (launch_attention_bwd_tc(tq, td, tdq, static_cast<const __nv_bfloat16*>(o), dob, lse, dsum, dqacc, dqkv, T, d, H,
                                   h->train_items, pb, h->d_rope, c.max_positions, h->num_sms, h->d_err,
                                   st) != cudaSuccess)
         return ESM_ERR_CUDA;
@@ -1166,8 +1167,9 @@ esm_status esm_op_attention_backward(esm_encoder_t* h, const void* qkv, const vo
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
   const CUtensorMap* td = h->map(d_o, (uint64_t)T, (uint64_t)d, 128, 2);
-  if (!tq || !td) return ESM_ERR_CUDA;
-  if (launch_attention_bwd_tc(tq, td, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse,
+  const CUtensorMap* tdq = h->map(ws + off_dq, (uint64_t)T, (uint64_t)d, 32, 4);
+  if (!tq || !td || !tdq) return ESM_ERR_CUDA;
+  if (launch_attention_bwd_tc(tq, td, tdq, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse,
                               reinterpret_cast<float*>(ws + off_dsum), reinterpret_cast<float*>(ws + off_dq),
                               static_cast<__nv_bfloat16*>(dqkv), T, d, h->cfg.heads, L.max_items,
                               pack_buffers(workspace, L), nullptr, h->cfg.max_positions, h->num_sms, h->d_err,

@@ -142,9 +142,11 @@ void launch_attention_f32(const float* qkv, float* o, int d, int heads, int T, c
 // tcgen05 attention backward (attention_bwd_tc.cu): dqkv (bf16 [T, 3d]) from the saved
 // qkv (RoPE applied), O, the forward's lse and dO (bf16 [T, d], tm_do a 64 x 128-box map);
 // with rope set the q and k gradients are turned back through RoPE (positions pb.pos_id).
-// Scratch: dsum [T, heads], dq_acc [T, d] (fp32).
+// Scratch: dsum [T, heads], dq_acc [T, d] (fp32; tm_dq a map over it with a 32 x 32 box and
+// the 128-byte swizzle, the target of the dQ reduce-adds).
 int attention_bwd_tc_smem_bytes();
-cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const __nv_bfloat16* o,
+cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const CUtensorMap* tm_dq,
+                                    const __nv_bfloat16* o,
                                     const __nv_bfloat16* dout, const float* lse, float* dsum, float* dq_acc,
                                     __nv_bfloat16* dqkv, int T, int d, int heads, int max_items, const PackBuffers& pb,
                                     const float2* rope, int max_pos, int num_sms, unsigned* err, cudaStream_t st);
