@@ -16,19 +16,19 @@
 //   dV  += P^T dO       (M=128, N=64, K=128; dO MN-major)          cols [384,448)
 //   dK  += dS^T Q       (M=128, N=64, K=128; Q MN-major)           cols [320,384)
 //   dQ_i = dS K         (M=128 queries, N=64, K=128 keys; dS and K MN-major)  cols [256,320)
-// Roles (512 threads):
+// Roles (768 threads):
 //   warp 0       TMA: the item's K and V tiles, then Q and dO tiles of each query tile into
 //                a 2-stage ring (straight from the packed qkv and dO buffers);
 //   warp 1       one thread issues the MMAs: S^T and dP^T of tile i, then the three
 //                gradient products of tile i-1 (whose P^T and dS^T are in shared memory);
-//   warps 4..11  two warpgroups, one per 64 queries of the tile; thread r owns key r: reads
+//   warps 4..19  four warpgroups, one per 32 queries of the tile; thread r owns key r: reads
 //                its S^T and dP^T row segment, forms P^T = 2^(S^T c - lse) and
-//                dS^T = P^T (dP^T - D) for the valid (key, query) pairs in registers, hands
-//                S^T back, then (once the previous tile's gradient products have read them)
-//                writes both as bf16 into shared memory (K-major, 128-byte swizzle); at the end
-//                of the item warpgroup 0 scales dK, turns it back through RoPE and stores it,
-//                warpgroup 1 stores dV (bf16);
-//   warps 12..15 thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
+//                dS^T = P^T (dP^T - D) for the valid (key, query) pairs in registers (f32x2
+//                pairs), hands S^T back, then (once the previous tile's gradient products have
+//                read them) writes both as bf16 into shared memory (K-major, 128-byte swizzle);
+//                at the end of the item warpgroups 0 and 2 scale dK, turn it back through RoPE
+//                and store it, warpgroups 1 and 3 store dV (bf16), 32 columns each;
+//   warps 20..23 thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
 //                memory and adds it into an fp32 accumulator in global memory with TMA
 //                reduce-add (several key tiles contribute to each query row).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error bit and stops.
@@ -41,7 +41,8 @@ namespace {
 constexpr int DH = 64;
 constexpr int TB = 128;                 // rows of a key or query tile
 constexpr int TILE = 128 * 128;         // 128 rows x 128 bytes (64 bf16)
-constexpr int THREADS = 512;
+constexpr int kComputeWgs = 4;                      // P^T / dS^T warpgroups, 32 queries each
+constexpr int THREADS = 32 * (4 + 4 * kComputeWgs + 4);  // TMA, MMA, 2 idle; compute; dQ
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DK = 320, COL_DV = 384;
 
@@ -52,8 +53,8 @@ struct BwdSmem {
   uint64_t stat_full[2];  // all 128 slots of lse2 and of dsum [b] written (256 arrivals)
   uint32_t tmem_base;
   volatile int abort;
-  float lse2[2][TB];  // query tile g (buffer g & 1): log2-sum-exp2 of the scaled scores
-  float dsum[2][TB];  // and D
+  alignas(16) float lse2[2][TB];  // query tile g (buffer g & 1): -(log2-sum-exp2 of the scaled scores)
+  alignas(16) float dsum[2][TB];  // and -D
 };
 // [dS^T 32K][P^T 32K][Q0][Q1][dO0][dO1][K][V][dQ staging 4 x 8K] then BwdSmem
 constexpr int OFF_DS = 0, OFF_P = 2 * TILE, OFF_Q = 4 * TILE, OFF_DO = 6 * TILE, OFF_K = 8 * TILE,
@@ -127,13 +128,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&sm->q_empty[b], 1);
     }
     mbar_init(&sm->s_full, 1);
-    mbar_init(&sm->s_free, 8);
-    mbar_init(&sm->p_full, 8);
+    mbar_init(&sm->s_free, 4 * kComputeWgs);
+    mbar_init(&sm->p_full, 4 * kComputeWgs);
     mbar_init(&sm->p_free, 1);
     mbar_init(&sm->dq_full, 1);
     mbar_init(&sm->dq_free, 4);
     mbar_init(&sm->acc_full, 1);
-    mbar_init(&sm->acc_free, 8);
+    mbar_init(&sm->acc_free, 4 * kComputeWgs);
     mbar_init(&sm->mma_done, 1);
     mbar_init(&sm->stat_full[0], 256);
     mbar_init(&sm->stat_full[1], 256);
@@ -246,24 +247,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(&sm->mma_done, 0);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4 && warp < 4 + 4 * kComputeWgs) {
     // ------------------------------------------------------------ P^T / dS^T, dK / dV
-    const int wg = (warp - 4) >> 2;  // warpgroup: queries 64 wg .. 64 wg + 63 of each tile
+    const int wg = (warp - 4) >> 2;  // warpgroup: queries 32 wg .. 32 wg + 31 of each tile
     const int wq = warp & 3;
     const int r = wq * 32 + lane;    // key row of the tile (and index of the lse / D slot)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     constexpr float kLog2e = 1.4426950408889634f;
     const float c = kLog2e / 8.f;  // scores scaled by 1/sqrt(64), in log2 units
-    uint8_t* sP = base + OFF_P + wg * TILE;   // this warpgroup's 64 queries of P^T
-    uint8_t* sDS = base + OFF_DS + wg * TILE;
+    const uint64_t c2 = f2_pack(c, c);
+    // this warpgroup's 32 queries of P^T / dS^T: 16-byte units 4 (wg & 1) .. + 3 of block wg >> 1
+    uint8_t* sP = base + OFF_P + (wg >> 1) * TILE;
+    uint8_t* sDS = base + OFF_DS + (wg >> 1) * TILE;
+    const int unit0 = 4 * (wg & 1);
     bool ok = true;
     int g = 0, n = 0;
-    // slot r of a query tile: lse (warpgroup 0, to log2 units) or D (warpgroup 1) of query r;
+    // slot r of a query tile: -lse (warpgroup 0, in log2 units) or -D (warpgroup 1) of query r,
     // loaded one tile ahead so the load latency overlaps the previous tile
     auto stat = [&](const BItem& y, int i) -> float {
       const int q0 = y.s0 + i * TB;
-      if (r >= min(TB, y.slen - i * TB)) return 0.f;
-      return wg == 0 ? __ldg(lse + (size_t)(q0 + r) * heads + y.h) * kLog2e : __ldg(dsum + (size_t)(q0 + r) * heads + y.h);
+      if (wg > 1 || r >= min(TB, y.slen - i * TB)) return 0.f;
+      return wg == 0 ? -__ldg(lse + (size_t)(q0 + r) * heads + y.h) * kLog2e
+                     : -__ldg(dsum + (size_t)(q0 + r) * heads + y.h);
     };
     float st_next = (int)blockIdx.x < n_items ? stat(bitem(pb, blockIdx.x, heads), 0) : 0.f;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
@@ -274,29 +279,51 @@ __global__ void __launch_bounds__(THREADS, 1)
         // this tile's slots into buffer g & 1 (its previous readers, tile g - 2, are done:
         // every thread arrived for tile g - 1 after finishing tile g - 2)
         const int sb = g & 1;
-        if (wg == 0) sm->lse2[sb][r] = st_next;
-        else sm->dsum[sb][r] = st_next;
-        mbar_arrive(&sm->stat_full[sb]);
-        if (i + 1 < x.nq) st_next = stat(x, i + 1);
-        else if (it + (int)gridDim.x < n_items) st_next = stat(bitem(pb, it + gridDim.x, heads), 0);
+        if (wg < 2) {
+          if (wg == 0) sm->lse2[sb][r] = st_next;
+          else sm->dsum[sb][r] = st_next;
+          mbar_arrive(&sm->stat_full[sb]);
+          if (i + 1 < x.nq) st_next = stat(x, i + 1);
+          else if (it + (int)gridDim.x < n_items) st_next = stat(bitem(pb, it + gridDim.x, heads), 0);
+        }
         if (!mbar_wait_warp(&sm->stat_full[sb], (uint32_t)(g >> 1) & 1u)) { ok = false; break; }
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
-        // P^T and dS^T of this thread's key and 64 queries, as bf16 pairs, 16 queries at a time
-        uint32_t pw[4][8], dw[4][8];
+        // P^T and dS^T of this thread's key and 32 queries, as bf16 pairs, 16 queries at a time:
+        // t = s c - lse (log2 units), p = 2^t, ds = p (dp - D), in f32x2 pairs
+        const bool full = kval && qvalid == TB;
+        uint32_t pw[2][8], dw[2][8];
 #pragma unroll
-        for (int sub = 0; sub < 4; ++sub) {
-          const int cq = 64 * wg + 16 * sub;  // first query (column) of the sub-chunk
+        for (int sub = 0; sub < 2; ++sub) {
+          const int cq = 32 * wg + 16 * sub;  // first query (column) of the sub-chunk
           float sv[16], dp[16];
           tmem_ld16x2(tmem + lane_off + COL_S + cq, tmem + lane_off + COL_DP + cq, sv, dp);
+          const float4* nl4 = reinterpret_cast<const float4*>(&sm->lse2[sb][cq]);
+          const float4* nd4 = reinterpret_cast<const float4*>(&sm->dsum[sb][cq]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int q = cq + 2 * j;
-            const bool v0 = kval && q < qvalid, v1 = kval && q + 1 < qvalid;
-            const float p0 = v0 ? fast_exp2(fmaf(sv[2 * j], c, -sm->lse2[sb][q])) : 0.f;
-            const float p1 = v1 ? fast_exp2(fmaf(sv[2 * j + 1], c, -sm->lse2[sb][q + 1])) : 0.f;
-            pw[sub][j] = pack_bf16x2(p0, p1);
-            dw[sub][j] = pack_bf16x2(p0 * (dp[2 * j] - sm->dsum[sb][q]), p1 * (dp[2 * j + 1] - sm->dsum[sb][q + 1]));
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 nl = nl4[j4], nd = nd4[j4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int j = 2 * j4 + h2;  // pair j: queries cq + 2j, cq + 2j + 1
+              const uint64_t t = f2_fma(f2_pack(sv[2 * j], sv[2 * j + 1]), c2,
+                                        h2 ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
+              float t0, t1;
+              f2_unpack(t, t0, t1);
+              float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+              if (!full) {
+                const int q = cq + 2 * j;
+                p0 = (kval && q < qvalid) ? p0 : 0.f;
+                p1 = (kval && q + 1 < qvalid) ? p1 : 0.f;
+              }
+              const uint64_t pp = f2_pack(p0, p1);
+              const uint64_t dd = f2_mul(pp, f2_add(f2_pack(dp[2 * j], dp[2 * j + 1]),
+                                                    h2 ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y)));
+              float d0, d1;
+              f2_unpack(dd, d0, d1);
+              pw[sub][j] = pack_bf16x2(p0, p1);
+              dw[sub][j] = pack_bf16x2(d0, d1);
+            }
           }
         }
         // S^T / dP^T are read: the tensor core may compute the next tile's
@@ -306,10 +333,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // P^T / dS^T may be overwritten once the previous tile's gradient MMAs have read them
         if (!mbar_wait_warp(&sm->p_free, (uint32_t)(g & 1) ^ 1u)) { ok = false; break; }
 #pragma unroll
-        for (int sub = 0; sub < 4; ++sub) {
+        for (int sub = 0; sub < 2; ++sub) {
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const uint32_t off = swz(r, 2 * sub + h2);
+            const uint32_t off = swz(r, unit0 + 2 * sub + h2);
             *reinterpret_cast<uint4*>(sP + off) =
                 make_uint4(pw[sub][4 * h2], pw[sub][4 * h2 + 1], pw[sub][4 * h2 + 2], pw[sub][4 * h2 + 3]);
             *reinterpret_cast<uint4*>(sDS + off) =
@@ -321,48 +348,64 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(&sm->p_full);
       }
       if (!ok) break;
-      // ---- item epilogue: warpgroup 0 stores dK (scaled, RoPE undone), warpgroup 1 dV
+      // ---- item epilogue: 32 of the 64 gradient columns per thread.  Warpgroups 0 and 2
+      // store dK (scaled, RoPE undone: warpgroup 0 the pairs (j, j + 32) for j < 16,
+      // warpgroup 2 for j >= 16), warpgroups 1 and 3 dV columns 0-31 and 32-63.
       if (!mbar_wait_warp(&sm->acc_full, (uint32_t)n & 1u)) { ok = false; break; }
       tc_fence_after();
-      float a[64];
-      {
-        const uint32_t col = wg == 0 ? COL_DK : COL_DV;
-        tmem_ld32(tmem + lane_off + col, *reinterpret_cast<float(*)[32]>(a));
-        tmem_ld32(tmem + lane_off + col + 32, *reinterpret_cast<float(*)[32]>(a + 32));
-      }
+      const bool is_k = (wg & 1) == 0;
+      const int c0 = is_k ? 16 * (wg >> 1) : 32 * (wg >> 1);  // dK: j0 (and j0 + 32); dV: first column
+      float a[16], b[16];
+      if (is_k) tmem_ld16x2(tmem + lane_off + COL_DK + c0, tmem + lane_off + COL_DK + 32 + c0, a, b);
+      else tmem_ld16x2(tmem + lane_off + COL_DV + c0, tmem + lane_off + COL_DV + c0 + 16, a, b);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->acc_free);
       if (kval) {
         const int key = x.k0 + r;
-        if (wg == 0) {
-          if (rope != nullptr) {
-            int p = key - x.s0;
-            p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
+        __nv_bfloat16* row = dqkv + (size_t)key * 3 * d + x.h * DH;
+        if (is_k) {
+          int p = key - x.s0;
+          p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {  // pair (j, j + 32) turned back by its angle
-              const float2 cs = __ldg(rope + ((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1));
-              const float u = a[j] * 0.125f, v = a[j + 32] * 0.125f;
+          for (int j = 0; j < 16; ++j) {  // pair (c0 + j, c0 + j + 32) turned back by its angle
+            const float u = a[j] * 0.125f, v = b[j] * 0.125f;
+            if (rope != nullptr) {
+              const int jj = c0 + j;
+              const float2 cs = __ldg(rope + ((size_t)(jj >> 1) * max_pos + p) * 2 + (jj & 1));
               a[j] = u * cs.x + v * cs.y;
-              a[j + 32] = v * cs.x - u * cs.y;
+              b[j] = v * cs.x - u * cs.y;
+            } else {
+              a[j] = u;
+              b[j] = v;
             }
-          } else {
+          }
+          uint4* lo = reinterpret_cast<uint4*>(row + d + c0);
+          uint4* hi = reinterpret_cast<uint4*>(row + d + c0 + 32);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) a[j] *= 0.125f;
+          for (int u = 0; u < 2; ++u) {
+            lo[u] = make_uint4(pack_bf16x2(a[8 * u], a[8 * u + 1]), pack_bf16x2(a[8 * u + 2], a[8 * u + 3]),
+                               pack_bf16x2(a[8 * u + 4], a[8 * u + 5]), pack_bf16x2(a[8 * u + 6], a[8 * u + 7]));
+            hi[u] = make_uint4(pack_bf16x2(b[8 * u], b[8 * u + 1]), pack_bf16x2(b[8 * u + 2], b[8 * u + 3]),
+                               pack_bf16x2(b[8 * u + 4], b[8 * u + 5]), pack_bf16x2(b[8 * u + 6], b[8 * u + 7]));
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(row + 2 * d + c0);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            dst[u] = make_uint4(pack_bf16x2(a[8 * u], a[8 * u + 1]), pack_bf16x2(a[8 * u + 2], a[8 * u + 3]),
+                                pack_bf16x2(a[8 * u + 4], a[8 * u + 5]), pack_bf16x2(a[8 * u + 6], a[8 * u + 7]));
+            dst[2 + u] = make_uint4(pack_bf16x2(b[8 * u], b[8 * u + 1]), pack_bf16x2(b[8 * u + 2], b[8 * u + 3]),
+                                    pack_bf16x2(b[8 * u + 4], b[8 * u + 5]), pack_bf16x2(b[8 * u + 6], b[8 * u + 7]));
           }
         }
-        uint4* gdst = reinterpret_cast<uint4*>(dqkv + (size_t)key * 3 * d + (wg == 0 ? d : 2 * d) + x.h * DH);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          gdst[u] = make_uint4(pack_bf16x2(a[8 * u], a[8 * u + 1]), pack_bf16x2(a[8 * u + 2], a[8 * u + 3]),
-                               pack_bf16x2(a[8 * u + 4], a[8 * u + 5]), pack_bf16x2(a[8 * u + 6], a[8 * u + 7]));
       }
     }
     if (!ok) {
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 4 + 4 * kComputeWgs) {
     // ------------------------------------------------------------ dQ accumulation
     // Each warp stages its 32 rows of dQ_i (fp32, 128-byte swizzle, two 32-column boxes) and
     // adds them into the global accumulator with TMA reduce-add; rows of queries past the
@@ -379,22 +422,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < x.nq; ++i, ++g) {
         if (!mbar_wait_warp(&sm->dq_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
-        float a[32], b[32];
-        tmem_ld32(tmem + lane_off + COL_DQ, a);
-        tmem_ld32(tmem + lane_off + COL_DQ + 32, b);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->dq_free);
         // the previous tile's reduce must have finished reading the staging rows
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t off = (uint32_t)(lane * 128 + ((u ^ (lane & 7)) << 4));
-          *reinterpret_cast<float4*>(stage + off) = make_float4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-          *reinterpret_cast<float4*>(stage + 4096 + off) =
-              make_float4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+        for (int ch = 0; ch < 4; ++ch) {  // 16 columns at a time: box ch >> 1, units 4 (ch & 1) ..
+          float a[16];
+          tmem_ld16(tmem + lane_off + COL_DQ + 16 * ch, a);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int unit = 4 * (ch & 1) + u;
+            const uint32_t off = (uint32_t)((ch >> 1) * 4096 + lane * 128 + ((unit ^ (lane & 7)) << 4));
+            *reinterpret_cast<float4*>(stage + off) = make_float4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->dq_free);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
