@@ -16,21 +16,21 @@
 //   dV  += P^T dO       (M=128, N=64, K=128; dO MN-major)          cols [384,448)
 //   dK  += dS^T Q       (M=128, N=64, K=128; Q MN-major)           cols [320,384)
 //   dQ_i = dS K         (M=128 queries, N=64, K=128 keys; dS and K MN-major)  cols [256,320)
-// Roles (768 threads):
+// Roles (704 threads):
 //   warp 0       TMA: the item's K and V tiles, then Q and dO tiles of each query tile into
 //                a 2-stage ring (straight from the packed qkv and dO buffers);
 //   warp 1       one thread issues the MMAs: S^T and dP^T of tile i, then the three
 //                gradient products of tile i-1 (whose P^T and dS^T are in shared memory);
-//   warps 4..19  four warpgroups, one per 32 queries of the tile; thread r owns key r: reads
+//   warps 2..5   thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
+//                memory and adds it into an fp32 accumulator in global memory with TMA
+//                reduce-add (several key tiles contribute to each query row);
+//   warps 6..21  four warpgroups, one per 32 queries of the tile; thread r owns key r: reads
 //                its S^T and dP^T row segment, forms P^T = 2^(S^T c - lse) and
 //                dS^T = P^T (dP^T - D) for the valid (key, query) pairs in registers (f32x2
 //                pairs), hands S^T back, then (once the previous tile's gradient products have
 //                read them) writes both as bf16 into shared memory (K-major, 128-byte swizzle);
 //                at the end of the item warpgroups 0 and 2 scale dK, turn it back through RoPE
-//                and store it, warpgroups 1 and 3 store dV (bf16), 32 columns each;
-//   warps 20..23 thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
-//                memory and adds it into an fp32 accumulator in global memory with TMA
-//                reduce-add (several key tiles contribute to each query row).
+//                and store it, warpgroups 1 and 3 store dV (bf16), 32 columns each.
 // Every mbarrier wait is bounded; on timeout the kernel latches an error bit and stops.
 #include "common.cuh"
 #include "internal.h"
@@ -42,7 +42,10 @@ constexpr int DH = 64;
 constexpr int TB = 128;                 // rows of a key or query tile
 constexpr int TILE = 128 * 128;         // 128 rows x 128 bytes (64 bf16)
 constexpr int kComputeWgs = 4;                      // P^T / dS^T warpgroups, 32 queries each
-constexpr int THREADS = 32 * (4 + 4 * kComputeWgs + 4);  // TMA, MMA, 2 idle; compute; dQ
+// Warps: 0 TMA, 1 MMA, 2..5 dQ, then the compute warpgroups.  A warp reaches the TMEM lanes
+// 32 (warp % 4) .. + 31, so any four consecutive warps cover all 128 lanes.
+constexpr int kWarpDq = 2, kWarpCompute = 6;
+constexpr int THREADS = 32 * (kWarpCompute + 4 * kComputeWgs);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DK = 320, COL_DV = 384;
 
@@ -247,9 +250,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(&sm->mma_done, 0);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 4 + 4 * kComputeWgs) {
+  } else if (warp >= kWarpCompute) {
     // ------------------------------------------------------------ P^T / dS^T, dK / dV
-    const int wg = (warp - 4) >> 2;  // warpgroup: queries 32 wg .. 32 wg + 31 of each tile
+    const int wg = (warp - kWarpCompute) >> 2;  // warpgroup: queries 32 wg .. 32 wg + 31 of each tile
     const int wq = warp & 3;
     const int r = wq * 32 + lane;    // key row of the tile (and index of the lse / D slot)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
     }
-  } else if (warp >= 4 + 4 * kComputeWgs) {
+  } else if (warp >= kWarpDq) {
     // ------------------------------------------------------------ dQ accumulation
     // Each warp stages its 32 rows of dQ_i (fp32, 128-byte swizzle, two 32-column boxes) and
     // adds them into the global accumulator with TMA reduce-add; rows of queries past the
