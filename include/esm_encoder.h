@@ -349,7 +349,7 @@ typedef struct {
 
 /* Bytes of the training buffer for up to max_tokens tokens: per layer the layer input and
  * mid-layer residual (float32 [T, hidden]), the LayerNorm outputs, q|k|v after RoPE, the
- * attention output (bf16), the attention log-sum-exp (float32 [T, heads]), fc1's
+ * attention output (bf16), the attention log-sum-exp (float32 [heads, T]), fc1's
  * pre-activation and GELU output (bf16 [T, ffn]); then the backward's scratch.  About
  * 46 KB per token per layer for ESM-2 650M. */
 ESM_API esm_status esm_encoder_train_buffer_size(const esm_encoder_t* h, int max_tokens, size_t* bytes);
@@ -399,13 +399,14 @@ ESM_API esm_status esm_op_layernorm_backward(esm_encoder_t* h, const float* x, c
                                              int cols, void* workspace, size_t workspace_bytes,
                                              esm_stream_t stream);
 
-/* esm_op_attention (bf16, head_dim 64) that also writes lse (device float32 [T, heads]):
- * the natural-log softmax normaliser log sum_s exp(q_t . k_s / 8) of every query row.
+/* esm_op_attention (bf16, head_dim 64) that also writes lse (device float32 [heads, T],
+ * head-major): the natural-log softmax normaliser log sum_s exp(q_t . k_s / 8) of every query
+ * row.
  * esm_op_attention_backward: from the same qkv (bf16 [T, 3*hidden], q | k | v as the
  * attention read them), its output o (bf16 [T, hidden]), lse and d_o = dL/do (bf16
  * [T, hidden]), writes dqkv = dL/d(q | k | v) (bf16 [T, 3*hidden]).  Workspace:
  * esm_op_attention_backward_workspace_size bytes (the forward's work list plus float32
- * scratch [T, heads] and [T, hidden]). */
+ * scratch [heads, T] and [T, hidden]). */
 ESM_API esm_status esm_op_attention_train(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,
                                           int total_tokens, int max_seqlen, void* o, float* lse, void* workspace,
                                           size_t workspace_bytes, esm_stream_t stream);

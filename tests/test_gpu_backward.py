@@ -123,7 +123,7 @@ def test_attention_lse_and_backward(lengths):
     cu = torch.from_numpy(synth.cu_seqlens_from_lengths(lengths)).cuda()
     tq = _dev(qkv, torch.bfloat16)
     o = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    lse = torch.empty(H, T, dtype=torch.float32, device="cuda")  # head-major
     enc.op_attention_train(tq, cu, max(lengths), o, lse)
     dqkv = torch.full((T, 3 * d), float("nan"), dtype=torch.bfloat16, device="cuda")
     enc.op_attention_backward(tq, o, lse, _dev(dO, torch.bfloat16), cu, max(lengths), dqkv)
@@ -140,7 +140,7 @@ def test_attention_lse_and_backward(lengths):
         ref_lse[a:b] = B.attention_lse(q, k)
         dq, dk, dv = B.attention_backward(q, k, v, dO[a:b].reshape(L, H, 64).astype(np.float64))
         ref[a:b] = np.concatenate([dq.reshape(L, d), dk.reshape(L, d), dv.reshape(L, d)], axis=1)
-    assert np.abs(to_np(lse) - ref_lse).max() < 1e-4 * np.abs(ref_lse).max() + 1e-5
+    assert np.abs(to_np(lse).T - ref_lse).max() < 1e-4 * np.abs(ref_lse).max() + 1e-5
     got = to_np(dqkv)
     for name, sl in (("dq", slice(0, d)), ("dk", slice(d, 2 * d)), ("dv", slice(2 * d, 3 * d))):
         assert rel_l2(got[:, sl], ref[:, sl]) < 1e-2, name

@@ -16,21 +16,21 @@
 //   dV  += P^T dO       (M=128, N=64, K=128; dO MN-major)          cols [384,448)
 //   dK  += dS^T Q       (M=128, N=64, K=128; Q MN-major)           cols [320,384)
 //   dQ_i = dS K         (M=128 queries, N=64, K=128 keys; dS and K MN-major)  cols [256,320)
-// Roles (704 threads):
+// Roles (768 threads, registers rebalanced per warpgroup with setmaxnreg):
 //   warp 0       TMA: the item's K and V tiles, then Q and dO tiles of each query tile into
 //                a 2-stage ring (straight from the packed qkv and dO buffers);
 //   warp 1       one thread issues the MMAs: S^T and dP^T of tile i, then the three
 //                gradient products of tile i-1 (whose P^T and dS^T are in shared memory);
-//   warps 2..5   thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
-//                memory and adds it into an fp32 accumulator in global memory with TMA
-//                reduce-add (several key tiles contribute to each query row);
-//   warps 6..21  four warpgroups, one per 32 queries of the tile; thread r owns key r: reads
+//   warps 4..19  four warpgroups, one per 32 queries of the tile; thread r owns key r: reads
 //                its S^T and dP^T row segment, forms P^T = 2^(S^T c - lse) and
 //                dS^T = P^T (dP^T - D) for the valid (key, query) pairs in registers (f32x2
 //                pairs), hands S^T back, then (once the previous tile's gradient products have
 //                read them) writes both as bf16 into shared memory (K-major, 128-byte swizzle);
 //                at the end of the item warpgroups 0 and 2 scale dK, turn it back through RoPE
-//                and store it, warpgroups 1 and 3 store dV (bf16), 32 columns each.
+//                and store it, warpgroups 1 and 3 store dV (bf16), 32 columns each;
+//   warps 20..23 thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
+//                memory and adds it into an fp32 accumulator in global memory with TMA
+//                reduce-add (several key tiles contribute to each query row).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error bit and stops.
 #include "common.cuh"
 #include "internal.h"
@@ -42,10 +42,16 @@ constexpr int DH = 64;
 constexpr int TB = 128;                 // rows of a key or query tile
 constexpr int TILE = 128 * 128;         // 128 rows x 128 bytes (64 bf16)
 constexpr int kComputeWgs = 4;                      // P^T / dS^T warpgroups, 32 queries each
-// Warps: 0 TMA, 1 MMA, 2..5 dQ, then the compute warpgroups.  A warp reaches the TMEM lanes
-// 32 (warp % 4) .. + 31, so any four consecutive warps cover all 128 lanes.
-constexpr int kWarpDq = 2, kWarpCompute = 6;
-constexpr int THREADS = 32 * (kWarpCompute + 4 * kComputeWgs);
+// Warpgroups: 0 = TMA (warp 0), MMA (warp 1), two idle warps; 1..kComputeWgs = compute;
+// the last = dQ.  Warp w reaches the TMEM lanes 32 (w % 4) .. + 31.
+constexpr int kWarpCompute = 4, kWarpDq = 4 + 4 * kComputeWgs;
+constexpr int THREADS = 32 * (kWarpDq + 4);
+// Registers per thread at launch and after the warpgroup-wide setmaxnreg: warpgroup 0 and the
+// dQ warpgroup give registers to the compute warpgroups (their P^T / dS^T pairs stay in
+// registers until the shared buffers are free).
+constexpr int kRegsLaunch = 80, kRegsWg0 = 64, kRegsCompute = 88, kRegsDq = 64;
+static_assert(128 * (kRegsWg0 + kRegsDq) + 128 * kComputeWgs * kRegsCompute <= THREADS * kRegsLaunch,
+              "register split");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DK = 320, COL_DV = 384;
 
@@ -53,11 +59,11 @@ struct BwdSmem {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full, s_free, p_full, p_free, dq_full, dq_free, acc_full, acc_free, mma_done;
-  uint64_t stat_full[2];  // all 128 slots of lse2 and of dsum [b] written (256 arrivals)
   uint32_t tmem_base;
   volatile int abort;
-  alignas(16) float lse2[2][TB];  // query tile g (buffer g & 1): -(log2-sum-exp2 of the scaled scores)
-  alignas(16) float dsum[2][TB];  // and -D
+  // per compute warp: -(log2-sum-exp2 of the scaled scores) and -D of its warpgroup's 32
+  // queries of the current tile
+  alignas(16) float wstat[4 * kComputeWgs][2][32];
 };
 // [dS^T 32K][P^T 32K][Q0][Q1][dO0][dO1][K][V][dQ staging 4 x 8K] then BwdSmem
 constexpr int OFF_DS = 0, OFF_P = 2 * TILE, OFF_Q = 4 * TILE, OFF_DO = 6 * TILE, OFF_K = 8 * TILE,
@@ -113,7 +119,7 @@ __device__ __forceinline__ BItem bitem(const PackBuffers& pb, int it, int heads)
 __global__ void __launch_bounds__(THREADS, 1)
     attention_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                             const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
-                            const float* __restrict__ dsum, __nv_bfloat16* __restrict__ dqkv, int d, int heads,
+                            const float* __restrict__ dsum, __nv_bfloat16* __restrict__ dqkv, int T, int d, int heads,
                             PackBuffers pb, const float2* __restrict__ rope, int max_pos, unsigned* err) {
   const int n_items = *pb.work_count * heads;
   if ((int)blockIdx.x >= n_items) return;  // whole CTA, before any barrier or TMEM use
@@ -139,8 +145,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&sm->acc_full, 1);
     mbar_init(&sm->acc_free, 4 * kComputeWgs);
     mbar_init(&sm->mma_done, 1);
-    mbar_init(&sm->stat_full[0], 256);
-    mbar_init(&sm->stat_full[1], 256);
     sm->abort = 0;
     fence_barrier_init();
   }
@@ -149,6 +153,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -250,8 +255,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(&sm->mma_done, 0);
     }
     __syncwarp();
-  } else if (warp >= kWarpCompute) {
+  } else if (warp < kWarpDq) {
     // ------------------------------------------------------------ P^T / dS^T, dK / dV
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
     const int wg = (warp - kWarpCompute) >> 2;  // warpgroup: queries 32 wg .. 32 wg + 31 of each tile
     const int wq = warp & 3;
     const int r = wq * 32 + lane;    // key row of the tile (and index of the lse / D slot)
@@ -265,31 +271,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int unit0 = 4 * (wg & 1);
     bool ok = true;
     int g = 0, n = 0;
-    // slot r of a query tile: -lse (warpgroup 0, in log2 units) or -D (warpgroup 1) of query r,
-    // loaded one tile ahead so the load latency overlaps the previous tile
-    auto stat = [&](const BItem& y, int i) -> float {
-      const int q0 = y.s0 + i * TB;
-      if (wg > 1 || r >= min(TB, y.slen - i * TB)) return 0.f;
-      return wg == 0 ? -__ldg(lse + (size_t)(q0 + r) * heads + y.h) * kLog2e
-                     : -__ldg(dsum + (size_t)(q0 + r) * heads + y.h);
+    // -lse (log2 units) and -D of query 32 wg + lane of a tile (lse and D are head-major
+    // [heads, T], so a warp reads 128 contiguous bytes of each); loaded one tile ahead so the
+    // load latency overlaps the previous tile, then shared with the warp through its slot
+    float* slot = &sm->wstat[warp - kWarpCompute][0][0];
+    auto stat = [&](const BItem& y, int i, float& nl, float& nd) {
+      const int q = 32 * wg + lane;
+      nl = 0.f;
+      nd = 0.f;
+      if (q < min(TB, y.slen - i * TB)) {
+        const size_t at = (size_t)y.h * T + y.s0 + i * TB + q;
+        nl = -__ldg(lse + at) * kLog2e;
+        nd = -__ldg(dsum + at);
+      }
     };
-    float st_next = (int)blockIdx.x < n_items ? stat(bitem(pb, blockIdx.x, heads), 0) : 0.f;
+    float nl_next = 0.f, nd_next = 0.f;
+    if ((int)blockIdx.x < n_items) stat(bitem(pb, blockIdx.x, heads), 0, nl_next, nd_next);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
       const BItem x = bitem(pb, it, heads);
       const bool kval = r < x.krows;
       for (int i = 0; i < x.nq; ++i, ++g) {
         const int qvalid = min(TB, x.slen - i * TB);
-        // this tile's slots into buffer g & 1 (its previous readers, tile g - 2, are done:
-        // every thread arrived for tile g - 1 after finishing tile g - 2)
-        const int sb = g & 1;
-        if (wg < 2) {
-          if (wg == 0) sm->lse2[sb][r] = st_next;
-          else sm->dsum[sb][r] = st_next;
-          mbar_arrive(&sm->stat_full[sb]);
-          if (i + 1 < x.nq) st_next = stat(x, i + 1);
-          else if (it + (int)gridDim.x < n_items) st_next = stat(bitem(pb, it + gridDim.x, heads), 0);
-        }
-        if (!mbar_wait_warp(&sm->stat_full[sb], (uint32_t)(g >> 1) & 1u)) { ok = false; break; }
+        __syncwarp();  // the warp is done reading the previous tile's slot
+        slot[lane] = nl_next;
+        slot[32 + lane] = nd_next;
+        __syncwarp();
+        if (i + 1 < x.nq) stat(x, i + 1, nl_next, nd_next);
+        else if (it + (int)gridDim.x < n_items) stat(bitem(pb, it + gridDim.x, heads), 0, nl_next, nd_next);
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
         // P^T and dS^T of this thread's key and 32 queries, as bf16 pairs, 16 queries at a time:
@@ -301,8 +309,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int cq = 32 * wg + 16 * sub;  // first query (column) of the sub-chunk
           float sv[16], dp[16];
           tmem_ld16x2(tmem + lane_off + COL_S + cq, tmem + lane_off + COL_DP + cq, sv, dp);
-          const float4* nl4 = reinterpret_cast<const float4*>(&sm->lse2[sb][cq]);
-          const float4* nd4 = reinterpret_cast<const float4*>(&sm->dsum[sb][cq]);
+          const float4* nl4 = reinterpret_cast<const float4*>(slot + 16 * sub);
+          const float4* nd4 = reinterpret_cast<const float4*>(slot + 32 + 16 * sub);
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
             const float4 nl = nl4[j4], nd = nd4[j4];
@@ -408,8 +416,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
     }
-  } else if (warp >= kWarpDq) {
+  } else {
     // ------------------------------------------------------------ dQ accumulation
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDq));
     // Each warp stages its 32 rows of dQ_i (fp32, 128-byte swizzle, two 32-column boxes) and
     // adds them into the global accumulator with TMA reduce-add; rows of queries past the
     // sequence end hold exact zeros (their dS columns are zero), so adding them is harmless.
@@ -468,7 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// D[t, h] = sum_c dO[t, h*64 + c] * O[t, h*64 + c] (one thread per (token, head)).
+// D[h, t] = sum_c dO[t, h*64 + c] * O[t, h*64 + c] (one thread per (token, head); head-major).
 __global__ void attention_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                           float* __restrict__ dsum, int T, int d, int heads) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -490,7 +499,7 @@ __global__ void attention_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ o, c
       acc = fmaf(xf.y, yf.y, acc);
     }
   }
-  dsum[i] = acc;
+  dsum[(size_t)h * T + t] = acc;
 }
 
 // dq = dq_acc / 8 with RoPE undone (pairs (j, j + 32) turned back by their angle) -> the q
@@ -542,7 +551,7 @@ cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap
   if (e != cudaSuccess) return e;
   const long long items = (long long)max_items * heads;
   const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
-  attention_bwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, *tm_do, *tm_dq, lse, dsum, dqkv, d, heads, pb,
+  attention_bwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, *tm_do, *tm_dq, lse, dsum, dqkv, T, d, heads, pb,
                                                              rope, max_pos, err);
   const long long tq = (long long)T * (d / 2);
   attention_bwd_dq_kernel<<<(unsigned)((tq + 255) / 256), 256, 0, st>>>(dq_acc, dqkv, pb.pos_id, rope, max_pos, T, d);

@@ -115,7 +115,7 @@ template <Act OUT>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm, void* __restrict__ o, int d, int heads,
                         PackBuffers pb, const float* q_scale, float* amax_out, float* __restrict__ lse,
-                        unsigned* err) {
+                        int lse_stride, unsigned* err) {
   const int n_items = *pb.work_count * heads;
   if ((int)blockIdx.x >= n_items) return;  // whole CTA, before any barrier or TMEM use
 
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       const float inv = 1.f / l;
       // training forward: the natural-log softmax normaliser of this row and head (scores
       // scaled by 1/sqrt(dh)), ln 2 * (m + log2 l) in the base-2 units used above
-      if (lse != nullptr && r < x.qrows) lse[(size_t)(x.qrow0 + r) * heads + x.h] = 0.6931471805599453f * (m_ref + log2f(l));
+      if (lse != nullptr && r < x.qrows) lse[(size_t)x.h * lse_stride + x.qrow0 + r] = 0.6931471805599453f * (m_ref + log2f(l));
       uint8_t* stage = sQ + (qi & 1) * TILE_BYTES;
       constexpr int kUnits = (OUT == Act::BF16) ? 8 : 4;  // 16-byte units per output row
       if constexpr (OUT == Act::BF16) {
@@ -466,7 +466,7 @@ int attention_tc_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int d, int heads, int max_items,
                                 const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
-                                cudaStream_t st, float* lse) {
+                                cudaStream_t st, float* lse, int lse_stride) {
   if (max_items <= 0) return cudaSuccess;
   static int num_sms = 0;
   static bool configured[2] = {false, false};
@@ -491,10 +491,10 @@ cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int
   const unsigned grid = (unsigned)(items < cap ? items : cap);
   if (which)
     attention_tc_kernel<Act::E4M3><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, lse,
-                                                                      err);
+                                                                      lse_stride, err);
   else
     attention_tc_kernel<Act::BF16><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, lse,
-                                                                      err);
+                                                                      lse_stride, err);
   return cudaGetLastError();
 }
 

@@ -568,7 +568,7 @@ esm_status train_forward_impl(esm_encoder* h, const esm_weights* w, const int32_
       ProfScope _ps(h, P_ATTN, st, 1);
       const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
       if (!tq) return ESM_ERR_CUDA;
-      if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st, lse) !=
+      if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st, lse, T) !=
           cudaSuccess)
         return ESM_ERR_CUDA;
     }
@@ -1141,7 +1141,7 @@ esm_status esm_op_attention_train(esm_encoder_t* h, const void* qkv, const int32
   const CUtensorMap* tq = h->map(qkv, (uint64_t)total_tokens, (uint64_t)3 * d, 128, 2);
   if (!tq) return ESM_ERR_CUDA;
   if (launch_attention_tc(tq, o, Act::BF16, d, h->cfg.heads, L.max_items, pack_buffers(workspace, L), nullptr, nullptr,
-                          h->d_err, st, lse) != cudaSuccess)
+                          h->d_err, st, lse, total_tokens) != cudaSuccess)
     return ESM_ERR_CUDA;
   return cuda_status(cudaGetLastError());
 }

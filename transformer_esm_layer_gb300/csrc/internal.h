@@ -131,18 +131,20 @@ void launch_attention_bf16_to_e4m3(const __nv_bfloat16* qkv, uint8_t* o, int d, 
 // tcgen05 attention (head_dim 64): tm_qkv is a tensor map over qkv [T, 3d] bf16 with a
 // 64 x 128 box and the 128-byte swizzle; work items in tiles of kAttnQTileTc rows.
 int attention_tc_smem_bytes();
-// lse (optional, fp32 [T, heads]): the natural-log softmax normaliser of every query row
-// (scores scaled by 1/sqrt(head_dim)), kept by the training forward for the backward.
+// lse (optional, fp32 [heads, lse_stride], head-major): the natural-log softmax normaliser of
+// every query row (scores scaled by 1/sqrt(head_dim)), kept by the training forward for the
+// backward; lse_stride >= T.
 cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int d, int heads, int max_items,
                                 const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
-                                cudaStream_t st, float* lse = nullptr);
+                                cudaStream_t st, float* lse = nullptr, int lse_stride = 0);
 void launch_attention_f32(const float* qkv, float* o, int d, int heads, int T, const PackBuffers& pb,
                           cudaStream_t st);
 
 // tcgen05 attention backward (attention_bwd_tc.cu): dqkv (bf16 [T, 3d]) from the saved
-// qkv (RoPE applied), O, the forward's lse and dO (bf16 [T, d], tm_do a 64 x 128-box map);
+// qkv (RoPE applied), O, the forward's lse ([heads, T]) and dO (bf16 [T, d], tm_do a
+// 64 x 128-box map);
 // with rope set the q and k gradients are turned back through RoPE (positions pb.pos_id).
-// Scratch: dsum [T, heads], dq_acc [T, d] (fp32; tm_dq a map over it with a 32 x 32 box and
+// Scratch: dsum [heads, T], dq_acc [T, d] (fp32; tm_dq a map over it with a 32 x 32 box and
 // the 128-byte swizzle, the target of the dQ reduce-adds).
 int attention_bwd_tc_smem_bytes();
 cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const CUtensorMap* tm_dq,
