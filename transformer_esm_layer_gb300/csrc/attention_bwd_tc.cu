@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(&sm->mma_done, 0);
     }
     __syncwarp();
-  } else if (warp < kWarpDq) {
+  } else if (warp >= kWarpCompute && warp < kWarpDq) {
     // ------------------------------------------------------------ P^T / dS^T, dK / dV
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
     const int wg = (warp - kWarpCompute) >> 2;  // warpgroup: queries 32 wg .. 32 wg + 31 of each tile
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
     }
-  } else {
+  } else if (warp >= kWarpDq) {
     // ------------------------------------------------------------ dQ accumulation
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDq));
     // Each warp stages its 32 rows of dQ_i (fp32, 128-byte swizzle, two 32-column boxes) and
@@ -503,29 +503,46 @@ __global__ void attention_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ o, c
 }
 
 // dq = dq_acc / 8 with RoPE undone (pairs (j, j + 32) turned back by their angle) -> the q
-// block of dqkv (bf16).  One thread per (token, head, pair).
+// block of dqkv (bf16).  One thread per (token, head, 8 consecutive pairs): 16-byte loads
+// of columns j0..j0+7 and j0+32..j0+39, two 16-byte stores.
 __global__ void attention_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dqkv,
                                         const int32_t* __restrict__ pos_id, const float2* __restrict__ rope,
                                         int max_pos, int T, int d) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int half_d = d / 2;
-  if (i >= (long long)T * half_d) return;
-  const long long t = i / half_d;
-  const int rem = (int)(i % half_d);
-  const int h = rem / 32, j = rem % 32;
+  const int per_tok = d / 16;  // (heads) x (4 groups of 8 pairs)
+  if (i >= (long long)T * per_tok) return;
+  const long long t = i / per_tok;
+  const int rem = (int)(i % per_tok);
+  const int h = rem >> 2, j0 = (rem & 3) * 8;
   const float* src = dq_acc + t * d + h * DH;
-  float a = src[j] * 0.125f, b = src[j + 32] * 0.125f;
+  float a[8], b[8];
+  *reinterpret_cast<float4*>(a) = __ldg(reinterpret_cast<const float4*>(src + j0));
+  *reinterpret_cast<float4*>(a + 4) = __ldg(reinterpret_cast<const float4*>(src + j0 + 4));
+  *reinterpret_cast<float4*>(b) = __ldg(reinterpret_cast<const float4*>(src + j0 + 32));
+  *reinterpret_cast<float4*>(b + 4) = __ldg(reinterpret_cast<const float4*>(src + j0 + 36));
+  int p = 0;
   if (rope != nullptr) {
-    int p = __ldg(pos_id + t);
+    p = __ldg(pos_id + t);
     p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
-    const float2 cs = __ldg(rope + ((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1));
-    const float a2 = a * cs.x + b * cs.y;
-    b = b * cs.x - a * cs.y;
-    a = a2;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float u = a[k] * 0.125f, v = b[k] * 0.125f;
+    if (rope != nullptr) {
+      const int j = j0 + k;
+      const float2 cs = __ldg(rope + ((size_t)(j >> 1) * max_pos + p) * 2 + (j & 1));
+      a[k] = u * cs.x + v * cs.y;
+      b[k] = v * cs.x - u * cs.y;
+    } else {
+      a[k] = u;
+      b[k] = v;
+    }
   }
   __nv_bfloat16* dst = dqkv + t * 3 * d + h * DH;
-  dst[j] = __float2bfloat16_rn(a);
-  dst[j + 32] = __float2bfloat16_rn(b);
+  *reinterpret_cast<uint4*>(dst + j0) =
+      make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+  *reinterpret_cast<uint4*>(dst + j0 + 32) =
+      make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]), pack_bf16x2(b[4], b[5]), pack_bf16x2(b[6], b[7]));
 }
 
 }  // namespace
@@ -553,7 +570,7 @@ cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap
   const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
   attention_bwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, *tm_do, *tm_dq, lse, dsum, dqkv, T, d, heads, pb,
                                                              rope, max_pos, err);
-  const long long tq = (long long)T * (d / 2);
+  const long long tq = (long long)T * (d / 16);
   attention_bwd_dq_kernel<<<(unsigned)((tq + 255) / 256), 256, 0, st>>>(dq_acc, dqkv, pb.pos_id, rope, max_pos, T, d);
   return cudaGetLastError();
 }
