@@ -77,6 +77,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^t for two values with one special-function instruction in half precision: t is rounded
+// to fp16 (relative error 2^-11, so 2^t carries an absolute error below 2e-4 for t <= 0),
+// the result is returned in fp32.  P is rounded to bf16 (2^-9) for the tensor cores anyway.
+__device__ __forceinline__ void exp2_pair_f16(float t0, float t1, float& p0, float& p1) {
+  uint32_t h, e;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(t1), "f"(t0));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
+  const __half2 r = *reinterpret_cast<const __half2*>(&e);
+  p0 = __low2float(r);
+  p1 = __high2float(r);
+}
+
 // 16-byte unit j of row r of a 128-row x 128-byte tile with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
 
@@ -319,9 +331,9 @@ __global__ void __launch_bounds__(THREADS, 1)
               const int j = 2 * j4 + h2;  // pair j: queries cq + 2j, cq + 2j + 1
               const uint64_t t = f2_fma(f2_pack(sv[2 * j], sv[2 * j + 1]), c2,
                                         h2 ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
-              float t0, t1;
+              float t0, t1, p0, p1;
               f2_unpack(t, t0, t1);
-              float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+              exp2_pair_f16(t0, t1, p0, p1);
               if (!full) {
                 const int q = cq + 2 * j;
                 p0 = (kval && q < qvalid) ? p0 : 0.f;
