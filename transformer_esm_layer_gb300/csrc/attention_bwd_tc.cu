@@ -41,15 +41,19 @@ namespace {
 constexpr int DH = 64;
 constexpr int TB = 128;                 // rows of a key or query tile
 constexpr int TILE = 128 * 128;         // 128 rows x 128 bytes (64 bf16)
-constexpr int kComputeWgs = 4;                      // P^T / dS^T warpgroups, 32 queries each
+constexpr int kComputeWgs = 2;                      // P^T / dS^T warpgroups
+constexpr int QPW = 128 / kComputeWgs;               // queries of a tile per compute warpgroup
+constexpr int NSUB = QPW / 16;                       // 16-query sub-chunks per thread
 // Warpgroups: 0 = TMA (warp 0), MMA (warp 1), two idle warps; 1..kComputeWgs = compute;
 // the last = dQ.  Warp w reaches the TMEM lanes 32 (w % 4) .. + 31.
 constexpr int kWarpCompute = 4, kWarpDq = 4 + 4 * kComputeWgs;
 constexpr int THREADS = 32 * (kWarpDq + 4);
-// Registers per thread at launch and after the warpgroup-wide setmaxnreg: warpgroup 0 and the
-// dQ warpgroup give registers to the compute warpgroups (their P^T / dS^T pairs stay in
-// registers until the shared buffers are free).
-constexpr int kRegsLaunch = 80, kRegsWg0 = 64, kRegsCompute = 88, kRegsDq = 64;
+// Registers per thread at launch and after the warpgroup-wide setmaxnreg: the dQ warpgroup
+// gives registers to the compute warpgroups (their P^T / dS^T pairs stay in registers until
+// the shared buffers are free); warpgroup 0 (TMA, MMA) keeps its launch count.  The compute
+// warpgroups' increase equals what the dQ warpgroup releases, so it never waits long.
+constexpr int kRegsLaunch = 65536 / THREADS / 8 * 8, kRegsWg0 = kRegsLaunch, kRegsDq = 80;
+constexpr int kRegsCompute = (THREADS * kRegsLaunch - 128 * (kRegsWg0 + kRegsDq)) / (128 * kComputeWgs) / 8 * 8;
 static_assert(128 * (kRegsWg0 + kRegsDq) + 128 * kComputeWgs * kRegsCompute <= THREADS * kRegsLaunch,
               "register split");
 constexpr uint32_t TMEM_COLS = 512;
@@ -63,7 +67,7 @@ struct BwdSmem {
   volatile int abort;
   // per compute warp: -(log2-sum-exp2 of the scaled scores) and -D of its warpgroup's 32
   // queries of the current tile
-  alignas(16) float wstat[4 * kComputeWgs][2][32];
+  alignas(16) float wstat[4 * kComputeWgs][2][QPW];
 };
 // [dS^T 32K][P^T 32K][Q0][Q1][dO0][dO1][K][V][dQ staging 4 x 8K] then BwdSmem
 constexpr int OFF_DS = 0, OFF_P = 2 * TILE, OFF_Q = 4 * TILE, OFF_DO = 6 * TILE, OFF_K = 8 * TILE,
@@ -75,18 +79,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^t for two values with one special-function instruction in half precision: t is rounded
-// to fp16 (relative error 2^-11, so 2^t carries an absolute error below 2e-4 for t <= 0),
-// the result is returned in fp32.  P is rounded to bf16 (2^-9) for the tensor cores anyway.
-__device__ __forceinline__ void exp2_pair_f16(float t0, float t1, float& p0, float& p1) {
-  uint32_t h, e;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(t1), "f"(t0));
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
-  const __half2 r = *reinterpret_cast<const __half2*>(&e);
-  p0 = __low2float(r);
-  p1 = __high2float(r);
 }
 
 // 16-byte unit j of row r of a 128-row x 128-byte tile with the 128-byte swizzle.
@@ -165,7 +157,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
-  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
+  if constexpr (kRegsWg0 < kRegsLaunch) {
+    if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -270,34 +264,41 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= kWarpCompute && warp < kWarpDq) {
     // ------------------------------------------------------------ P^T / dS^T, dK / dV
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
-    const int wg = (warp - kWarpCompute) >> 2;  // warpgroup: queries 32 wg .. 32 wg + 31 of each tile
+    const int wg = (warp - kWarpCompute) >> 2;  // warpgroup: queries QPW wg .. QPW wg + QPW - 1 of each tile
     const int wq = warp & 3;
     const int r = wq * 32 + lane;    // key row of the tile (and index of the lse / D slot)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     constexpr float kLog2e = 1.4426950408889634f;
     const float c = kLog2e / 8.f;  // scores scaled by 1/sqrt(64), in log2 units
     const uint64_t c2 = f2_pack(c, c);
-    // this warpgroup's 32 queries of P^T / dS^T: 16-byte units 4 (wg & 1) .. + 3 of block wg >> 1
-    uint8_t* sP = base + OFF_P + (wg >> 1) * TILE;
-    uint8_t* sDS = base + OFF_DS + (wg >> 1) * TILE;
-    const int unit0 = 4 * (wg & 1);
+    // this warpgroup's QPW queries of P^T / dS^T: 16-byte units unit0 .. of 64-query block
+    uint8_t* sP = base + OFF_P + ((QPW * wg) >> 6) * TILE;
+    uint8_t* sDS = base + OFF_DS + ((QPW * wg) >> 6) * TILE;
+    const int unit0 = ((QPW * wg) & 63) >> 3;
     bool ok = true;
     int g = 0, n = 0;
-    // -lse (log2 units) and -D of query 32 wg + lane of a tile (lse and D are head-major
-    // [heads, T], so a warp reads 128 contiguous bytes of each); loaded one tile ahead so the
-    // load latency overlaps the previous tile, then shared with the warp through its slot
+    // -lse (log2 units) and -D of queries QPW wg + 32 k + lane of a tile (lse and D are
+    // head-major [heads, T], so a warp reads 128 contiguous bytes of each per k); loaded one
+    // tile ahead so the load latency overlaps the previous tile, then shared with the warp
+    // through its slot
+    constexpr int KS = QPW / 32;
     float* slot = &sm->wstat[warp - kWarpCompute][0][0];
-    auto stat = [&](const BItem& y, int i, float& nl, float& nd) {
-      const int q = 32 * wg + lane;
-      nl = 0.f;
-      nd = 0.f;
-      if (q < min(TB, y.slen - i * TB)) {
-        const size_t at = (size_t)y.h * T + y.s0 + i * TB + q;
-        nl = -__ldg(lse + at) * kLog2e;
-        nd = -__ldg(dsum + at);
+    auto stat = [&](const BItem& y, int i, float (&nl)[KS], float (&nd)[KS]) {
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        const int q = QPW * wg + 32 * k + lane;
+        nl[k] = 0.f;
+        nd[k] = 0.f;
+        if (q < min(TB, y.slen - i * TB)) {
+          const size_t at = (size_t)y.h * T + y.s0 + i * TB + q;
+          nl[k] = -__ldg(lse + at) * kLog2e;
+          nd[k] = -__ldg(dsum + at);
+        }
       }
     };
-    float nl_next = 0.f, nd_next = 0.f;
+    float nl_next[KS], nd_next[KS];
+#pragma unroll
+    for (int k = 0; k < KS; ++k) nl_next[k] = nd_next[k] = 0.f;
     if ((int)blockIdx.x < n_items) stat(bitem(pb, blockIdx.x, heads), 0, nl_next, nd_next);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
       const BItem x = bitem(pb, it, heads);
@@ -305,24 +306,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < x.nq; ++i, ++g) {
         const int qvalid = min(TB, x.slen - i * TB);
         __syncwarp();  // the warp is done reading the previous tile's slot
-        slot[lane] = nl_next;
-        slot[32 + lane] = nd_next;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          slot[32 * k + lane] = nl_next[k];
+          slot[QPW + 32 * k + lane] = nd_next[k];
+        }
         __syncwarp();
         if (i + 1 < x.nq) stat(x, i + 1, nl_next, nd_next);
         else if (it + (int)gridDim.x < n_items) stat(bitem(pb, it + gridDim.x, heads), 0, nl_next, nd_next);
         if (!mbar_wait_warp(&sm->s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
-        // P^T and dS^T of this thread's key and 32 queries, as bf16 pairs, 16 queries at a time:
+        // P^T and dS^T of this thread's key and QPW queries, as bf16 pairs, 16 queries at a time:
         // t = s c - lse (log2 units), p = 2^t, ds = p (dp - D), in f32x2 pairs
         const bool full = kval && qvalid == TB;
-        uint32_t pw[2][8], dw[2][8];
+        uint32_t pw[NSUB][8], dw[NSUB][8];
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          const int cq = 32 * wg + 16 * sub;  // first query (column) of the sub-chunk
+        for (int sub = 0; sub < NSUB; ++sub) {
+          const int cq = QPW * wg + 16 * sub;  // first query (column) of the sub-chunk
           float sv[16], dp[16];
           tmem_ld16x2(tmem + lane_off + COL_S + cq, tmem + lane_off + COL_DP + cq, sv, dp);
           const float4* nl4 = reinterpret_cast<const float4*>(slot + 16 * sub);
-          const float4* nd4 = reinterpret_cast<const float4*>(slot + 32 + 16 * sub);
+          const float4* nd4 = reinterpret_cast<const float4*>(slot + QPW + 16 * sub);
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
             const float4 nl = nl4[j4], nd = nd4[j4];
@@ -331,9 +335,9 @@ __global__ void __launch_bounds__(THREADS, 1)
               const int j = 2 * j4 + h2;  // pair j: queries cq + 2j, cq + 2j + 1
               const uint64_t t = f2_fma(f2_pack(sv[2 * j], sv[2 * j + 1]), c2,
                                         h2 ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
-              float t0, t1, p0, p1;
+              float t0, t1;
               f2_unpack(t, t0, t1);
-              exp2_pair_f16(t0, t1, p0, p1);
+              float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
               if (!full) {
                 const int q = cq + 2 * j;
                 p0 = (kval && q < qvalid) ? p0 : 0.f;
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // P^T / dS^T may be overwritten once the previous tile's gradient MMAs have read them
         if (!mbar_wait_warp(&sm->p_free, (uint32_t)(g & 1) ^ 1u)) { ok = false; break; }
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
+        for (int sub = 0; sub < NSUB; ++sub) {
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             const uint32_t off = swz(r, unit0 + 2 * sub + h2);
@@ -371,36 +375,40 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(&sm->p_full);
       }
       if (!ok) break;
-      // ---- item epilogue: 32 of the 64 gradient columns per thread.  Warpgroups 0 and 2
-      // store dK (scaled, RoPE undone: warpgroup 0 the pairs (j, j + 32) for j < 16,
-      // warpgroup 2 for j >= 16), warpgroups 1 and 3 dV columns 0-31 and 32-63.
+      // ---- item epilogue, in four parts of 32 gradient values per key: part v = 0, 2 store dK
+      // (scaled, RoPE undone) for the pairs (j, j + 32), j in 16 (v / 2) .. + 15; part v = 1, 3
+      // store dV columns 32 (v / 2) .. + 31.  Warpgroup wg takes parts wg, wg + kComputeWgs, ...
       if (!mbar_wait_warp(&sm->acc_full, (uint32_t)n & 1u)) { ok = false; break; }
       tc_fence_after();
-      const bool is_k = (wg & 1) == 0;
-      const int c0 = is_k ? 16 * (wg >> 1) : 32 * (wg >> 1);  // dK: j0 (and j0 + 32); dV: first column
-      float a[16], b[16];
-      if (is_k) tmem_ld16x2(tmem + lane_off + COL_DK + c0, tmem + lane_off + COL_DK + 32 + c0, a, b);
-      else tmem_ld16x2(tmem + lane_off + COL_DV + c0, tmem + lane_off + COL_DV + c0 + 16, a, b);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->acc_free);
-      if (kval) {
-        const int key = x.k0 + r;
-        __nv_bfloat16* row = dqkv + (size_t)key * 3 * d + x.h * DH;
+      const int key = x.k0 + r;
+      int p = key - x.s0;
+      p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
+      __nv_bfloat16* row = dqkv + (size_t)key * 3 * d + x.h * DH;
+#pragma unroll
+      for (int v = wg; v < 4; v += kComputeWgs) {
+        const bool is_k = (v & 1) == 0;
+        const int c0 = is_k ? 16 * (v >> 1) : 32 * (v >> 1);  // dK: first pair j0; dV: first column
+        float a[16], b[16];
+        if (is_k) tmem_ld16x2(tmem + lane_off + COL_DK + c0, tmem + lane_off + COL_DK + 32 + c0, a, b);
+        else tmem_ld16x2(tmem + lane_off + COL_DV + c0, tmem + lane_off + COL_DV + c0 + 16, a, b);
+        if (v + kComputeWgs >= 4) {  // this warp's last TMEM read of the item
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->acc_free);
+        }
+        if (!kval) continue;
         if (is_k) {
-          int p = key - x.s0;
-          p = p < 0 ? 0 : (p >= max_pos ? max_pos - 1 : p);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {  // pair (c0 + j, c0 + j + 32) turned back by its angle
-            const float u = a[j] * 0.125f, v = b[j] * 0.125f;
+            const float u = a[j] * 0.125f, w = b[j] * 0.125f;
             if (rope != nullptr) {
               const int jj = c0 + j;
               const float2 cs = __ldg(rope + ((size_t)(jj >> 1) * max_pos + p) * 2 + (jj & 1));
-              a[j] = u * cs.x + v * cs.y;
-              b[j] = v * cs.x - u * cs.y;
+              a[j] = u * cs.x + w * cs.y;
+              b[j] = w * cs.x - u * cs.y;
             } else {
               a[j] = u;
-              b[j] = v;
+              b[j] = w;
             }
           }
           uint4* lo = reinterpret_cast<uint4*>(row + d + c0);
