@@ -237,3 +237,46 @@ def test_backward_rejects_mismatched_buffers_and_other_precisions():
     enc8 = _enc(g, "fp8")
     with pytest.raises(EsmError):
         enc8.train_buffer(50)
+
+
+def test_encoder_backward_3b_width_one_layer():
+    """One ESM-2 3B layer (hidden 2560, 40 heads, ffn 10240): the wider LayerNorm backward
+    and GEMM shapes."""
+    g = synth.Geometry(num_layers=1, hidden=2560, heads=40, ffn=10240)
+    enc, w, tok, out, grads, ref = _train_case(g, [300, 129, 1, 64], 44)
+    _check_grads(grads, ref, g, 2e-2)
+
+
+def test_backward_is_repeatable():
+    """Every reduction over tokens runs in a fixed order: gradients computed before the first
+    attention backward (the last layer's fc2 and final LayerNorm) are bitwise identical across
+    calls; the rest differ only by the arrival order of the fp32 dQ additions."""
+    from transformer_esm_layer_gb300.binding import DeviceGrads, DeviceWeights, packed_inputs
+    g = SMALL
+    lengths = [200, 57, 3]
+    rng = np.random.default_rng(3)
+    w = synth.model_weights(g, 3, "bf16", ln_random=True)
+    tok = synth.tokens_for_lengths(rng, lengths)
+    T = int(sum(lengths))
+    d_out = _dev(rng.standard_normal((T, g.hidden)), torch.float32)
+    enc = _enc(g)
+    dw = DeviceWeights(w, "bf16")
+    t_tok, t_cu = packed_inputs(tok, lengths)
+    ws = enc.workspace(T, len(lengths))
+    tb = enc.train_buffer(T)
+    runs = []
+    for _ in range(2):
+        enc.forward_train(dw, t_tok, t_cu, max(lengths), tb, ws)
+        gr = DeviceGrads(g, g.num_layers)
+        enc.backward(dw, d_out, gr, tb, ws)
+        runs.append(gr)
+    assert enc.check_status() == 0
+    a, b = runs
+    last = g.num_layers - 1
+    for n in ("w_2", "b_2"):
+        assert torch.equal(a.layers[last][n], b.layers[last][n]), n
+    assert torch.equal(a.lnf_g, b.lnf_g) and torch.equal(a.lnf_b, b.lnf_b)
+    for li in range(g.num_layers):
+        for n in B.PARAM_NAMES:
+            assert rel_l2(to_np(a.layers[li][n]), to_np(b.layers[li][n])) < 1e-5, (li, n)
+    assert rel_l2(to_np(a.emb), to_np(b.emb)) < 1e-5
