@@ -357,7 +357,9 @@ ESM_API esm_status esm_encoder_train_buffer_size(const esm_encoder_t* h, int max
 /* The packed forward of esm_encoder_forward (same arguments, same hidden_out in bf16) that
  * also keeps its activations in train_buf (device, 256-byte aligned, at least
  * esm_encoder_train_buffer_size bytes).  total_tokens > 0.  The workspace and train_buf
- * belong to the handle's next esm_encoder_backward: leave both untouched until then.
+ * belong to the handle's next esm_encoder_backward: leave both untouched until then (another
+ * call of this handle with the same workspace withdraws that backward, which then returns
+ * ESM_ERR_INVALID_ARG).
  * Errors as esm_encoder_forward; ESM_ERR_WORKSPACE for a short train_buf. */
 ESM_API esm_status esm_encoder_forward_train(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids,
                                              const int32_t* cu_seqlens, int num_seqs, int total_tokens,

@@ -234,6 +234,10 @@ def test_backward_rejects_mismatched_buffers_and_other_precisions():
         for t in l.values():
             assert torch.count_nonzero(t).item() == 0
     assert torch.count_nonzero(grads.emb).item() == 0
+    # an inference forward on the same workspace withdraws the pending backward
+    enc.forward(dw, t_tok, t_cu, 30, workspace=ws)
+    with pytest.raises(EsmError):
+        enc.backward(dw, d_out, grads, tb, ws)
     enc8 = _enc(g, "fp8")
     with pytest.raises(EsmError):
         enc8.train_buffer(50)

@@ -567,8 +567,6 @@ __global__ void attention_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_b
 
 }  // namespace
 
-int attention_bwd_tc_smem_bytes() { return SMEM_BYTES; }
-
 cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const CUtensorMap* tm_dq,
                                     const __nv_bfloat16* o,
                                     const __nv_bfloat16* dout, const float* lse, float* dsum, float* dq_acc,

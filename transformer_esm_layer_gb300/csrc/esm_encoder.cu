@@ -223,7 +223,12 @@ PackBuffers pack_buffers(void* ws, const WsLayout& L) {
   return pb;
 }
 
-esm_status check_ws(const esm_encoder* h, int T, int B, void* ws, size_t bytes, WsLayout* out) {
+// Every call that indexes a batch into a workspace goes through here: one that reuses the
+// workspace of the last training forward overwrites its pack buffers, so the pending
+// backward of that forward is withdrawn (esm_encoder_backward then returns
+// ESM_ERR_INVALID_ARG); a training forward re-arms it once it is fully enqueued.
+esm_status check_ws(esm_encoder* h, int T, int B, void* ws, size_t bytes, WsLayout* out) {
+  if (ws != nullptr && ws == h->train_ws) h->train_buf = nullptr;
   if (ws == nullptr || !aligned(ws, 256)) return ESM_ERR_WORKSPACE;
   *out = h->layout(T, B);
   if (bytes < out->total) return ESM_ERR_WORKSPACE;

@@ -146,7 +146,6 @@ void launch_attention_f32(const float* qkv, float* o, int d, int heads, int T, c
 // with rope set the q and k gradients are turned back through RoPE (positions pb.pos_id).
 // Scratch: dsum [heads, T], dq_acc [T, d] (fp32; tm_dq a map over it with a 32 x 32 box and
 // the 128-byte swizzle, the target of the dQ reduce-adds).
-int attention_bwd_tc_smem_bytes();
 cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap* tm_do, const CUtensorMap* tm_dq,
                                     const __nv_bfloat16* o,
                                     const __nv_bfloat16* dout, const float* lse, float* dsum, float* dq_acc,
