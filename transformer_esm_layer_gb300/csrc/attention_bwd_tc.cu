@@ -105,6 +105,14 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)
   }
 }
 
+// Read-only global load issued exactly where it stands in the program (a prefetch whose
+// value is consumed one tile later must not be scheduled next to its use).
+__device__ __forceinline__ float ld_nc_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 struct BItem {
   int k0, krows, s0, slen, h, nq;
 };
@@ -291,8 +299,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         nd[k] = 0.f;
         if (q < min(TB, y.slen - i * TB)) {
           const size_t at = (size_t)y.h * T + y.s0 + i * TB + q;
-          nl[k] = -__ldg(lse + at) * kLog2e;
-          nd[k] = -__ldg(dsum + at);
+          nl[k] = ld_nc_early(lse + at);
+          nd[k] = ld_nc_early(dsum + at);
         }
       }
     };
@@ -307,9 +315,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int qvalid = min(TB, x.slen - i * TB);
         __syncwarp();  // the warp is done reading the previous tile's slot
 #pragma unroll
-        for (int k = 0; k < KS; ++k) {
-          slot[32 * k + lane] = nl_next[k];
-          slot[QPW + 32 * k + lane] = nd_next[k];
+        for (int k = 0; k < KS; ++k) {  // (the loads return lse and D; stored negated, lse in log2 units)
+          slot[32 * k + lane] = -nl_next[k] * kLog2e;
+          slot[QPW + 32 * k + lane] = -nd_next[k];
         }
         __syncwarp();
         if (i + 1 < x.nq) stat(x, i + 1, nl_next, nd_next);
