@@ -438,8 +438,14 @@ def run_ours(args):
         def train_fwd():
             enc.forward_train(dw, tok, cu, maxL, tb, ws, out=out, stream=stream)
 
+        allreduce_bytes = 0
+
         def train_bwd():
+            nonlocal allreduce_bytes
             enc.backward(dw, d_out, grads, tb, ws, stream=stream)
+            if world > 1:  # data parallel: every rank holds the gradient of the whole global batch
+                from transformer_esm_layer_gb300 import sharding as _sh
+                allreduce_bytes = _sh.allreduce_gradients(grads.tensors())
 
         for _ in range(2):
             train_fwd()
@@ -468,7 +474,9 @@ def run_ours(args):
         # per attention tile pair (S, dP, dV, dK, dQ) against the forward's two
         bwd_flops = 2.0 * sum(flops[c] for c in gemm_classes) + 2.5 * flops["attention"]
         bg_ms = bprof["gemm_backward"]["ms"]
-        train = {"calls": "esm_encoder_forward_train + esm_encoder_backward (all parameter gradients, fp32)",
+        train = {"calls": "esm_encoder_forward_train + esm_encoder_backward (all parameter gradients, fp32)"
+                          + (" + NCCL all-reduce (sum) of the gradients" if world > 1 else ""),
+                 "gradient_allreduce_bytes_per_rank": allreduce_bytes if world > 1 else 0,
                  "ms_per_step": f_ms + b_ms, "ms_forward_train": f_ms, "ms_backward": b_ms,
                  "tokens_per_s": global_tokens / ((f_ms + b_ms) / 1e3),
                  "backward_tflops": bwd_flops / (b_ms / 1e3) / 1e12,

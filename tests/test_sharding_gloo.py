@@ -80,3 +80,57 @@ def test_two_rank_gloo_sharding():
     results = dict(q.get(timeout=10) for _ in range(world))
     assert all(p.exitcode == 0 for p in procs)
     assert results == {0: True, 1: True}
+
+
+SMALL = synth.Geometry(num_layers=2, hidden=16, heads=2, ffn=32, vocab=33)
+
+
+def _grad_worker(rank, world, port, q):
+    """Each rank backpropagates its share of one packed batch (float64 oracle), the gradients
+    are summed with allreduce_gradients, and every rank compares with the gradient of the
+    whole batch."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from oracle import backward as B
+        from oracle import esm_oracle as O
+        rng = np.random.default_rng(5)
+        lengths = [9, 4, 7, 1, 12]
+        tokens = synth.tokens_for_lengths(rng, lengths).astype(np.int64)
+        w = synth.model_weights(SMALL, 5, "fp32", ln_random=True)
+        T = len(tokens)
+        d_out = np.random.default_rng(6).standard_normal((T, SMALL.hidden))
+        cu = O.cu_seqlens(lengths)
+        mine = sharding.shard_by_work(lengths, world, SMALL.hidden, SMALL.ffn)[rank]
+        toks, lens = sharding.local_batch(tokens, lengths, mine)
+        d_mine = np.concatenate([d_out[cu[i]:cu[i + 1]] for i in mine]) if mine else np.zeros((0, SMALL.hidden))
+
+        def flat(g):
+            return [g["emb"]] + [l[n] for l in g["layers"] for n in B.PARAM_NAMES] + [g["lnf_g"], g["lnf_b"]]
+
+        if lens:
+            part = flat(B.encode_packed_backward(toks.astype(np.int64), O.cu_seqlens(lens), w, SMALL.heads, d_mine))
+        else:
+            part = [np.zeros_like(a) for a in flat(B.encode_packed_backward(tokens, cu, w, SMALL.heads, d_out))]
+        tens = [torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)) for a in part]
+        nbytes = sharding.allreduce_gradients(tens, bucket_bytes=4096)  # several buckets
+        full = flat(B.encode_packed_backward(tokens, cu, w, SMALL.heads, d_out))
+        err = max(float(np.abs(t.numpy() - f).max() / (np.abs(f).max() + 1e-300)) for t, f in zip(tens, full))
+        q.put((rank, err < 1e-12 and nbytes == sum(a.size * 8 for a in full)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_gloo_gradient_allreduce_equals_whole_batch_gradient():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_grad_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+    results = dict(q.get(timeout=10) for _ in range(world))
+    assert results == {0: True, 1: True}

@@ -198,6 +198,10 @@ class DeviceGrads:
         st.lnf_b = self.lnf_b.data_ptr()
         self.struct = st
 
+    def tensors(self):
+        """Every gradient tensor in a fixed order (embedding, layers, final LayerNorm)."""
+        return [self.emb] + [l[n] for l in self.layers for n in GRAD_NAMES] + [self.lnf_g, self.lnf_b]
+
 
 class DeviceLmHead:
     """Masked-LM head weights on the device (handle's parameter dtype) plus the esm_lm_head

@@ -6,11 +6,16 @@ sequences: no collective is needed on the data path.  The split balances work, n
 tokens: a sequence of length L costs 2 L (4 d^2 + 2 d f) GEMM FLOPs plus 4 d L^2 attention
 FLOPs per layer.  Longest-first greedy assignment to the least-loaded rank is the
 sort-then-bucket idea of the length-aware sampler in section 5.2 of the hotelren.com guide.
+
+Training adds one exchange: the parameters are shared by every sequence and the gradient of
+a packed batch is the sum of its sequences' gradients, so ranks that each backpropagated
+their own share hold partial sums, and one all-reduce (sum) of the gradients gives every
+rank the batch gradient (data parallelism of the hotelren.com guide's training loop).
 """
 from __future__ import annotations
 
 import heapq
-from typing import List, Sequence, Tuple
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -43,3 +48,40 @@ def local_batch(tokens: np.ndarray, lengths: Sequence[int], indices: Sequence[in
     parts = [tokens[cu[i]:cu[i + 1]] for i in indices]
     toks = np.concatenate(parts).astype(np.int32) if parts else np.zeros(0, np.int32)
     return toks, [int(lengths[i]) for i in indices]
+
+
+def allreduce_gradients(tensors: Sequence, group=None, bucket_bytes: int = 256 << 20) -> int:
+    """Sum the gradient tensors over the ranks of the process group, in place.
+
+    Every rank passes tensors of the same shapes, dtypes and order.  They are packed in that
+    order into flat buckets of at most bucket_bytes (a tensor larger than that is a bucket on
+    its own) and each bucket is one all-reduce, so the collective sequence is identical on
+    every rank.  Returns the number of bytes reduced per rank."""
+    import torch
+    import torch.distributed as dist
+
+    total = 0
+    bucket: List = []
+    size = 0
+
+    def flush(b: List) -> None:
+        if not b:
+            return
+        flat = torch.cat([t.reshape(-1) for t in b])
+        dist.all_reduce(flat, op=dist.ReduceOp.SUM, group=group)
+        off = 0
+        for t in b:
+            n = t.numel()
+            t.copy_(flat[off:off + n].view_as(t))
+            off += n
+
+    for t in tensors:
+        nbytes = t.numel() * t.element_size()
+        total += nbytes
+        if bucket and (size + nbytes > bucket_bytes or t.dtype != bucket[0].dtype or t.device != bucket[0].device):
+            flush(bucket)
+            bucket, size = [], 0
+        bucket.append(t)
+        size += nbytes
+    flush(bucket)
+    return total
