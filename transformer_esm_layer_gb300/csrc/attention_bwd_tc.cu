@@ -16,19 +16,20 @@
 //   dV  += P^T dO       (M=128, N=64, K=128; dO MN-major)          cols [384,448)
 //   dK  += dS^T Q       (M=128, N=64, K=128; Q MN-major)           cols [320,384)
 //   dQ_i = dS K         (M=128 queries, N=64, K=128 keys; dS and K MN-major)  cols [256,320)
-// Roles (768 threads, registers rebalanced per warpgroup with setmaxnreg):
+// Roles (512 threads; registers rebalanced per warpgroup with setmaxnreg):
 //   warp 0       TMA: the item's K and V tiles, then Q and dO tiles of each query tile into
 //                a 2-stage ring (straight from the packed qkv and dO buffers);
 //   warp 1       one thread issues the MMAs: S^T and dP^T of tile i, then the three
 //                gradient products of tile i-1 (whose P^T and dS^T are in shared memory);
-//   warps 4..19  four warpgroups, one per 32 queries of the tile; thread r owns key r: reads
+//   warps 2, 3   no role (they complete warpgroup 0);
+//   warps 4..11  two warpgroups, one per 64 queries of the tile; thread r owns key r: reads
 //                its S^T and dP^T row segment, forms P^T = 2^(S^T c - lse) and
 //                dS^T = P^T (dP^T - D) for the valid (key, query) pairs in registers (f32x2
 //                pairs), hands S^T back, then (once the previous tile's gradient products have
 //                read them) writes both as bf16 into shared memory (K-major, 128-byte swizzle);
-//                at the end of the item warpgroups 0 and 2 scale dK, turn it back through RoPE
-//                and store it, warpgroups 1 and 3 store dV (bf16), 32 columns each;
-//   warps 20..23 thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
+//                at the end of the item they scale dK, turn it back through RoPE and store it,
+//                and store dV (bf16), 32 values per key and pass;
+//   warps 12..15 thread r owns query r of the tile: reads dQ_i from TMEM, stages it in shared
 //                memory and adds it into an fp32 accumulator in global memory with TMA
 //                reduce-add (several key tiles contribute to each query row).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error bit and stops.
@@ -65,7 +66,7 @@ struct BwdSmem {
   uint64_t s_full, s_free, p_full, p_free, dq_full, dq_free, acc_full, acc_free, mma_done;
   uint32_t tmem_base;
   volatile int abort;
-  // per compute warp: -(log2-sum-exp2 of the scaled scores) and -D of its warpgroup's 32
+  // per compute warp: -(log2-sum-exp2 of the scaled scores) and -D of its warpgroup's QPW
   // queries of the current tile
   alignas(16) float wstat[4 * kComputeWgs][2][QPW];
 };
