@@ -197,3 +197,43 @@ def encode_packed_backward(token_ids: np.ndarray, cu: Sequence[int], weights: Di
                     lt[n] = lt[n] + lg[n]
     total["x0"] = x0
     return total
+
+
+# --------------------------------------------------------------------------- masked-LM head
+def lm_head_backward(h: np.ndarray, w: Dict[str, np.ndarray], targets: Sequence[int]):
+    """Gradients of the mean masked-LM loss L = sum_scored CE / count (the forward of
+    ``esm_oracle.lm_head`` and ``masked_lm_loss``) with respect to the hidden states h [T, d]
+    and the head's parameters.  The embedding E is tied: the gradient returned for it is the
+    head's part only (the encoder's embedding gradient adds to it).
+
+    With logits l = z E^T + b, z = LN(u), u = GELU(a), a = h Wd^T + bd:
+    dl = (softmax(l) - onehot(target)) / count on scored rows (0 elsewhere),
+    dE = dl^T z, db = sum dl, dz = dl E, then LayerNorm, GELU' and the dense map backward."""
+    from .esm_oracle import IGNORE_INDEX
+    h = np.asarray(h, np.float64)
+    wd = np.asarray(w["dense_w"], np.float64)
+    E = np.asarray(w["emb"], np.float64)
+    a = h @ wd.T + np.asarray(w["dense_b"], np.float64)
+    u = gelu(a)
+    lg, lb = np.asarray(w["ln_g"], np.float64), np.asarray(w["ln_b"], np.float64)
+    z = layer_norm(u, lg, lb)
+    logits = z @ E.T + np.asarray(w["bias"], np.float64)
+    t = np.asarray(targets, np.int64)
+    scored = t != IGNORE_INDEX
+    count = int(scored.sum())
+    dl = np.zeros_like(logits)
+    if count:
+        m = logits.max(axis=1, keepdims=True)
+        p = np.exp(logits - m)
+        p /= p.sum(axis=1, keepdims=True)
+        rows = np.nonzero(scored)[0]
+        dl[rows] = p[rows]
+        dl[rows, t[scored]] -= 1.0
+        dl /= count
+    g = {"emb": dl.T @ z, "bias": dl.sum(axis=0)}
+    du, g["ln_g"], g["ln_b"] = layer_norm_backward(u, lg, dl @ E)
+    da = du * gelu_grad(a)
+    g["dense_w"] = da.T @ h
+    g["dense_b"] = da.sum(axis=0)
+    g["hidden"] = da @ wd
+    return g

@@ -221,3 +221,59 @@ def test_encoder_backward_vs_torch_autograd():
     for li, lp in enumerate(params["layers"]):
         for name in B.PARAM_NAMES:
             assert np.allclose(g["layers"][li][name], lp[name].grad.numpy(), rtol=1e-9, atol=1e-10), (li, name)
+
+
+# --------------------------------------------------------------------------- masked-LM head
+def _lm_weights(d=16, V=33, seed=21):
+    rng = np.random.default_rng(seed)
+    return {"dense_w": rng.standard_normal((d, d)) * 0.4, "dense_b": rng.standard_normal(d) * 0.2,
+            "ln_g": 1 + 0.1 * rng.standard_normal(d), "ln_b": 0.1 * rng.standard_normal(d),
+            "emb": rng.standard_normal((V, d)), "bias": 0.1 * rng.standard_normal(V)}
+
+
+def _mean_loss(h, w, t):
+    _, s, n = O.masked_lm_loss(O.lm_head(h, w), t)
+    return s / n
+
+
+def test_lm_head_backward_finite_differences():
+    rng = np.random.default_rng(22)
+    w = _lm_weights()
+    h = rng.standard_normal((9, 16)) * 1.5
+    t = rng.integers(0, 33, 9)
+    t[[1, 4, 7]] = -100
+    g = B.lm_head_backward(h, w, t)
+    for idx in _sample_idx(rng, h.shape, 10):
+        assert g["hidden"][idx] == pytest.approx(_fd(lambda hh: _mean_loss(hh, w, t), h, idx), rel=1e-6, abs=1e-8)
+    for name in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias"):
+        def J(pp, name=name):
+            ww = dict(w)
+            ww[name] = pp
+            return _mean_loss(h, ww, t)
+        for idx in _sample_idx(rng, w[name].shape, 6):
+            assert g[name][idx] == pytest.approx(_fd(J, w[name], idx), rel=1e-6, abs=1e-8), name
+    # the loss gradient of each scored row of logits sums to zero, so the bias gradient does too
+    assert abs(g["bias"].sum()) < 1e-12
+
+
+def test_lm_head_backward_vs_torch_autograd_and_unscored_rows():
+    rng = np.random.default_rng(23)
+    w = _lm_weights(seed=24)
+    h = rng.standard_normal((7, 16))
+    t = np.array([3, -100, 5, 32, -100, 0, 7])
+    g = B.lm_head_backward(h, w, t)
+    T_ = lambda a: torch.tensor(np.asarray(a, np.float64), requires_grad=True)
+    P = {k: T_(v) for k, v in w.items()}
+    H = T_(h)
+    a = F.linear(H, P["dense_w"], P["dense_b"])
+    z = F.layer_norm(F.gelu(a), (16,), P["ln_g"], P["ln_b"], 1e-5)
+    logits = F.linear(z, P["emb"], P["bias"])
+    loss = F.cross_entropy(logits, torch.from_numpy(t), ignore_index=-100, reduction="mean")
+    loss.backward()
+    assert np.allclose(g["hidden"], H.grad.numpy(), rtol=1e-10, atol=1e-12)
+    for k in P:
+        assert np.allclose(g[k], P[k].grad.numpy(), rtol=1e-10, atol=1e-12), k
+    # unscored rows get no gradient; nothing scored gives zero everywhere
+    assert np.all(g["hidden"][[1, 4]] == 0)
+    g0 = B.lm_head_backward(h, w, np.full(7, -100))
+    assert all(np.all(v == 0) for v in g0.values())
