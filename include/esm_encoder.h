@@ -219,6 +219,33 @@ ESM_API esm_status esm_encoder_lm_head(esm_encoder_t* h, const esm_lm_head* head
                                        float* token_loss, float* loss_sum, int* count, void* workspace,
                                        size_t workspace_bytes, esm_stream_t stream);
 
+/* ---- masked-LM head backward (the loss end of a training step) ----
+ * Gradients of the mean masked-LM loss L = loss_sum / count (the head and loss of
+ * esm_encoder_lm_head) with respect to the hidden states and the head's parameters, so that
+ * a training step runs from the loss: esm_encoder_forward_train -> esm_encoder_lm_head_backward
+ * (d_hidden) -> esm_encoder_backward (d_hidden_out = d_hidden).  The head's forward is
+ * recomputed inside the call.  ESM_BF16 handles (hidden % 256 == 0, vocab <= 64).
+ * hidden: device bf16 [T, hidden] (e.g. hidden_out of the training forward); targets as for
+ * esm_encoder_lm_head; d_hidden: device float32 [T, hidden] (overwritten); grads: device
+ * float32 buffers shaped like the head's parameters (overwritten; grads->emb is the head's
+ * part of the tied embedding's gradient: add esm_encoder_backward's grads->emb for the
+ * total); loss_sum, count: device scalars or NULL.  Unscored rows (target -100) get zero
+ * gradient; with nothing scored every gradient is zero.  Workspace: the size query's bytes. */
+typedef struct {
+  float* dense_w;
+  float* dense_b;
+  float* ln_g;
+  float* ln_b;
+  float* emb;
+  float* bias;
+} esm_lm_head_grads;
+ESM_API esm_status esm_encoder_lm_head_backward_workspace_size(const esm_encoder_t* h, int total_tokens,
+                                                               size_t* bytes);
+ESM_API esm_status esm_encoder_lm_head_backward(esm_encoder_t* h, const esm_lm_head* head, const void* hidden,
+                                                int total_tokens, const int32_t* targets, float* d_hidden,
+                                                const esm_lm_head_grads* grads, float* loss_sum, int* count,
+                                                void* workspace, size_t workspace_bytes, esm_stream_t stream);
+
 /* Synchronise `stream` and return (and clear) the first error the kernels latched
  * since the last check: ESM_ERR_BAD_CU_SEQLENS, ESM_ERR_TOKEN_RANGE, ESM_ERR_TIMEOUT
  * or ESM_OK. */

@@ -284,3 +284,71 @@ def test_backward_is_repeatable():
         for n in B.PARAM_NAMES:
             assert rel_l2(to_np(a.layers[li][n]), to_np(b.layers[li][n])) < 1e-5, (li, n)
     assert rel_l2(to_np(a.emb), to_np(b.emb)) < 1e-5
+
+
+# --------------------------------------------------------------------------- masked-LM head
+def _head_case(g, T, seed, rate=0.3):
+    from transformer_esm_layer_gb300.binding import DeviceLmHead
+    rng = np.random.default_rng(seed)
+    w = synth.model_weights(g, seed, "bf16")
+    head = synth.lm_head_weights(g, seed, "bf16", w["emb"])
+    tok = rng.integers(4, 24, T).astype(np.int32)
+    targets = synth.mlm_targets(tok, seed, rate=rate)
+    h = _bf16(rng.standard_normal((T, g.hidden)))
+    return head, DeviceLmHead(head, "bf16"), targets, h
+
+
+@pytest.mark.parametrize("T,rate", [(300, 0.3), (37, 1.0), (64, 0.0)])
+def test_lm_head_backward(T, rate):
+    g = SMALL
+    head, dh, targets, h = _head_case(g, T, 31, rate)
+    enc = _enc(g)
+    lsum = torch.zeros(1, dtype=torch.float32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_hidden, grads = enc.lm_head_backward(dh, _dev(h, torch.bfloat16), torch.from_numpy(targets).cuda(),
+                                           loss_sum=lsum, count=cnt)
+    assert enc.check_status() == 0
+    ref = B.lm_head_backward(h.astype(np.float64), head, targets)
+    n = int((targets != -100).sum())
+    assert int(cnt.item()) == n
+    if n == 0:
+        assert torch.count_nonzero(d_hidden).item() == 0
+        assert all(torch.count_nonzero(v).item() == 0 for v in grads.values())
+        return
+    assert rel_l2(to_np(d_hidden), ref["hidden"]) < 2e-2
+    for k in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias"):
+        assert rel_l2(to_np(grads[k]), ref[k]) < 2e-2, k
+
+
+def test_training_step_from_masked_lm_loss():
+    """forward_train -> masked-LM head backward -> encoder backward, against the oracle chain
+    (the tied embedding's gradient is the head's part plus the encoder's part)."""
+    from transformer_esm_layer_gb300.binding import DeviceGrads, DeviceLmHead, DeviceWeights, packed_inputs
+    g = SMALL
+    lengths = [90, 33, 140]
+    rng = np.random.default_rng(41)
+    w = synth.model_weights(g, 41, "bf16", ln_random=True)
+    head = synth.lm_head_weights(g, 41, "bf16", w["emb"])
+    tok = synth.tokens_for_lengths(rng, lengths)
+    targets = synth.mlm_targets(tok, 41, rate=0.25)
+    T = int(sum(lengths))
+    enc = _enc(g)
+    dw = DeviceWeights(w, "bf16")
+    t_tok, t_cu = packed_inputs(tok, lengths)
+    ws = enc.workspace(T, len(lengths))
+    tb = enc.train_buffer(T)
+    out = enc.forward_train(dw, t_tok, t_cu, max(lengths), tb, ws)
+    d_hidden, hg = enc.lm_head_backward(DeviceLmHead(head, "bf16"), out, torch.from_numpy(targets).cuda())
+    grads = DeviceGrads(g, g.num_layers)
+    enc.backward(dw, d_hidden, grads, tb, ws)
+    assert enc.check_status() == 0
+    cu = O.cu_seqlens(lengths)
+    hid = O.encode_packed(tok, cu, w, g.heads)
+    hid = np.concatenate([hid[i] for i in range(len(lengths))])
+    rh = B.lm_head_backward(hid, head, targets)
+    ref = B.encode_packed_backward(tok, cu, w, g.heads, rh["hidden"])
+    assert rel_l2(to_np(d_hidden), rh["hidden"]) < 2e-2
+    for k in ("dense_w", "dense_b", "ln_g", "ln_b", "bias"):
+        assert rel_l2(to_np(hg[k]), rh[k]) < 2e-2, k
+    assert rel_l2(to_np(hg["emb"]) + to_np(grads.emb), rh["emb"] + ref["emb"]) < 2e-2
+    _check_grads(grads, ref, g, 2e-2)

@@ -33,6 +33,7 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_op_gemm_dgrad", "esm_op_gemm_wgrad_workspace_size", "esm_op_gemm_wgrad",
            "esm_op_layernorm_backward_workspace_size", "esm_op_layernorm_backward", "esm_op_attention_train",
            "esm_op_attention_backward_workspace_size", "esm_op_attention_backward",
+           "esm_encoder_lm_head_backward_workspace_size", "esm_encoder_lm_head_backward",
            "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other",
                    "gemm_backward")
@@ -74,8 +75,15 @@ class EsmGrads(ctypes.Structure):
         [("lnf_g", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p)]
 
 
+LM_HEAD_NAMES = ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias")
+
+
 class EsmLmHead(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias")]
+    _fields_ = [(n, ctypes.c_void_p) for n in LM_HEAD_NAMES]
+
+
+class EsmLmHeadGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in LM_HEAD_NAMES]
 
 
 _lib = None
@@ -127,6 +135,9 @@ def load_library() -> ctypes.CDLL:
         "esm_op_attention_train": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]),
         "esm_op_attention_backward_workspace_size": (i32, [vp, i32, i32, ctypes.POINTER(sz)]),
         "esm_op_attention_backward": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp]),
+        "esm_encoder_lm_head_backward_workspace_size": (i32, [vp, i32, ctypes.POINTER(sz)]),
+        "esm_encoder_lm_head_backward": (i32, [vp, ctypes.POINTER(EsmLmHead), vp, i32, vp, vp,
+                                               ctypes.POINTER(EsmLmHeadGrads), vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -495,6 +506,31 @@ class EsmEncoder:
                                                        _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
                     "esm_op_attention_backward")
         return dqkv
+
+    def lm_head_backward(self, head: "DeviceLmHead", hidden, targets, d_hidden=None, grads=None, loss_sum=None,
+                         count=None, workspace=None, stream=None):
+        """esm_encoder_lm_head_backward: dL/d(hidden) (float32 [T, hidden]) and the head's
+        gradients (dict of float32 device tensors shaped like the head's parameters) of the
+        mean masked-LM loss."""
+        import torch
+        T = hidden.shape[0]
+        dev = hidden.device
+        if d_hidden is None:
+            d_hidden = torch.empty(T, self.hidden, dtype=torch.float32, device=dev)
+        if grads is None:
+            grads = {k: torch.empty(tuple(head.t[k].shape), dtype=torch.float32, device=dev) for k in LM_HEAD_NAMES}
+        if workspace is None:
+            n = ctypes.c_size_t()
+            self._raise(self.lib.esm_encoder_lm_head_backward_workspace_size(self.handle, T, ctypes.byref(n)),
+                        "esm_encoder_lm_head_backward_workspace_size")
+            workspace = torch.empty(int(n.value), dtype=torch.uint8, device=dev)
+        gs = EsmLmHeadGrads(*[grads[k].data_ptr() for k in LM_HEAD_NAMES])
+        self._raise(self.lib.esm_encoder_lm_head_backward(self.handle, ctypes.byref(head.struct), _ptr(hidden), T,
+                                                          _ptr(targets), _ptr(d_hidden), ctypes.byref(gs),
+                                                          _ptr(loss_sum), _ptr(count), _ptr(workspace),
+                                                          workspace.numel(), _stream_ptr(stream)),
+                    "esm_encoder_lm_head_backward")
+        return d_hidden, grads
 
     def set_profiling(self, enable: bool):
         self._raise(self.lib.esm_encoder_set_profiling(self.handle, int(enable)), "esm_encoder_set_profiling")

@@ -35,8 +35,8 @@ __device__ __forceinline__ float4 ld_param4(const void* p, int c, bool f32) {
 // (dres may alias dx).  The parameter gradients are column sums: each warp adds its rows'
 // dy * xhat and dy into its own shared-memory slice, and at the end the block adds the
 // slices in warp order into partial[block][0 | 1][cols].
-template <int N4>
-__global__ void __launch_bounds__(256, N4 <= 10 ? 2 : 1) ln_bwd_kernel(const float* __restrict__ x, const void* __restrict__ gamma,
+template <int N4, bool XBF16 = false>
+__global__ void __launch_bounds__(256, N4 <= 10 ? 2 : 1) ln_bwd_kernel(const void* __restrict__ xv, const void* __restrict__ gamma,
                                                      bool gf32, const float* __restrict__ dy, const float* dres,
                                                      float* dx, float* __restrict__ partial, int rows, int cols,
                                                      int rows_per_block, float eps) {
@@ -47,14 +47,19 @@ __global__ void __launch_bounds__(256, N4 <= 10 ? 2 : 1) ln_bwd_kernel(const flo
   for (int c = lane; c < 2 * n4; c += 32) mine[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int r0 = blockIdx.x * rows_per_block, r1 = min(rows, r0 + rows_per_block);
   for (int row = r0 + warp; row < r1; row += warps) {
-    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * cols);
     const float4* dr = reinterpret_cast<const float4*>(dy + (size_t)row * cols);
     float4 v[N4], d[N4];
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < N4; ++i) {
       const int c = i * 32 + lane;
-      v[i] = c < n4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (XBF16) {  // x is a bf16 activation (the masked-LM head's GELU output)
+        v[i] = c < n4 ? ld_param4(static_cast<const __nv_bfloat16*>(xv) + (size_t)row * cols, 4 * c, false)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        const float4* xr = reinterpret_cast<const float4*>(static_cast<const float*>(xv) + (size_t)row * cols);
+        v[i] = c < n4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       d[i] = c < n4 ? dr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
       s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
     }
@@ -174,12 +179,16 @@ __global__ void reduce_few_chunks_kernel(const float* __restrict__ partial, int 
   *reinterpret_cast<float4*>(out + i) = make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale);
 }
 
-void reduce_chunks(const float* partial, int chunks, size_t stride, size_t n, float scale, float* out, cudaStream_t st) {
-  if (n == 0) return;
-  if (chunks <= 16 && n % 4 == 0 && stride % 4 == 0)
-    reduce_few_chunks_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, st>>>(partial, chunks, stride, n, scale, out);
-  else
-    reduce_chunks_kernel<<<(unsigned)((n + 31) / 32), 256, 0, st>>>(partial, chunks, stride, (int)n, scale, out);
+
+// dz = du * GELU'(a), GELU'(a) = Phi(a) + a phi(a); du fp32, a bf16 (the pre-activation),
+// dz bf16.
+__global__ void gelu_bwd_kernel(const float* __restrict__ du, const __nv_bfloat16* __restrict__ a,
+                                __nv_bfloat16* __restrict__ dz, size_t n) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float x = __bfloat162float(a[i]);
+  const float g = 0.5f * (1.f + erff(x * 0.70710678118654752f)) + x * 0.3989422804014327f * expf(-0.5f * x * x);
+  dz[i] = __float2bfloat16_rn(du[i] * g);
 }
 
 // partial[chunk][v][c] = sum of dx[t][c] over the chunk's tokens t with tok[t] == v (each
@@ -209,6 +218,14 @@ int emb_chunks_for(int rows) { return rows <= 0 ? 1 : (rows + kEmbChunkRows - 1)
 
 }  // namespace
 
+void reduce_chunks(const float* partial, int chunks, size_t stride, size_t n, float scale, float* out, cudaStream_t st) {
+  if (n == 0) return;
+  if (chunks <= 16 && n % 4 == 0 && stride % 4 == 0)
+    reduce_few_chunks_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, st>>>(partial, chunks, stride, n, scale, out);
+  else
+    reduce_chunks_kernel<<<(unsigned)((n + 31) / 32), 256, 0, st>>>(partial, chunks, stride, (int)n, scale, out);
+}
+
 constexpr int kLnRowsPerBlock = 64;
 
 size_t bwd_partial_floats(int rows, int cols) {
@@ -217,41 +234,52 @@ size_t bwd_partial_floats(int rows, int cols) {
 }
 size_t emb_bwd_partial_floats(int rows, int vocab, int d) { return (size_t)emb_chunks_for(rows) * vocab * d; }
 
-template <int N4>
-cudaError_t ln_bwd_launch(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
+template <int N4, bool XBF16>
+cudaError_t ln_bwd_launch(const void* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
                           float* partial, int rows, int cols, float eps, cudaStream_t st) {
   const int warps = std::max(1, std::min(8, (int)(196608 / (8 * (size_t)cols))));
   const size_t smem = (size_t)warps * 2 * cols * sizeof(float);
   static size_t configured = 0;
   if (smem > 48 * 1024 && smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(ln_bwd_kernel<N4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(ln_bwd_kernel<N4, XBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
   const int blocks = (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
-  ln_bwd_kernel<N4><<<blocks, 32 * warps, smem, st>>>(x, gamma, gf32, dy, dres, dx, partial, rows, cols,
-                                                     kLnRowsPerBlock, eps);
+  ln_bwd_kernel<N4, XBF16><<<blocks, 32 * warps, smem, st>>>(x, gamma, gf32, dy, dres, dx, partial, rows, cols,
+                                                            kLnRowsPerBlock, eps);
   return cudaGetLastError();
 }
 
-void launch_ln_bwd(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
-                   float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st) {
+template <bool XBF16>
+void ln_bwd_any(const void* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
+                float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st) {
   if (rows <= 0) {
     cudaMemsetAsync(dgamma, 0, sizeof(float) * cols, st);
     cudaMemsetAsync(dbeta, 0, sizeof(float) * cols, st);
     return;
   }
   const int n4 = (cols / 4 + 31) / 32;  // float4 per lane
-  if (n4 <= 2) ln_bwd_launch<2>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
-  else if (n4 <= 4) ln_bwd_launch<4>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
-  else if (n4 <= 8) ln_bwd_launch<8>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
-  else if (n4 <= 10) ln_bwd_launch<10>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
-  else if (n4 <= 16) ln_bwd_launch<16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
-  else if (n4 <= 20) ln_bwd_launch<20>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
-  else ln_bwd_launch<32>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  if (n4 <= 2) ln_bwd_launch<2, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 4) ln_bwd_launch<4, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 8) ln_bwd_launch<8, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 10) ln_bwd_launch<10, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 16) ln_bwd_launch<16, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else if (n4 <= 20) ln_bwd_launch<20, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
+  else ln_bwd_launch<32, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
   const int blocks = (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
   reduce_chunks(partial, blocks, (size_t)2 * cols, cols, 1.f, dgamma, st);
   reduce_chunks(partial + cols, blocks, (size_t)2 * cols, cols, 1.f, dbeta, st);
+}
+
+void launch_ln_bwd(const float* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
+                   float* dgamma, float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st) {
+  ln_bwd_any<false>(x, gamma, gf32, dy, dres, dx, dgamma, dbeta, partial, rows, cols, eps, st);
+}
+
+void launch_ln_bwd_bf16in(const void* x, const void* gamma, bool gf32, const float* dy, float* dx, float* dgamma,
+                          float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st) {
+  ln_bwd_any<true>(x, gamma, gf32, dy, nullptr, dx, dgamma, dbeta, partial, rows, cols, eps, st);
 }
 
 void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out, float* partial, __nv_bfloat16* copy,
@@ -269,6 +297,10 @@ void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out
 
 void launch_reduce_splits(const float* partial, int splits, size_t n, float* out, cudaStream_t st) {
   reduce_chunks(partial, splits, n, (int)n, 1.f, out, st);
+}
+
+void launch_gelu_bwd(const float* du, const __nv_bfloat16* a, __nv_bfloat16* dz, size_t n, cudaStream_t st) {
+  if (n) gelu_bwd_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(du, a, dz, n);
 }
 
 void launch_emb_bwd(const float* dx, const int32_t* tok, int T, int d, int vocab, float scale, float* partial,

@@ -844,6 +844,100 @@ esm_status esm_encoder_lm_head(esm_encoder_t* h, const esm_lm_head* head, const 
                                       want_loss ? tl : nullptr, loss_sum, count, h->num_sms, h->d_err, st));
 }
 
+// Workspace of esm_encoder_lm_head_backward: the recomputed forward (pre-activation a,
+// GELU output u, LayerNorm output z: bf16 [T, d]; logits fp32 [T, V]; per-token loss; loss
+// sum and count) and the backward's scratch (dlogits, dz and du fp32 [T, d], da bf16, partial
+// sums, split-K partial products).
+struct LmBwdLayout {
+  size_t a, u, z, logits, tl, scal, dl, dz, du, da, partial, split, split_floats, total;
+};
+static LmBwdLayout lm_bwd_layout(const esm_config& c, int Tm) {
+  LmBwdLayout L{};
+  const size_t T = Tm > 0 ? Tm : 1, d = c.hidden, V = c.vocab;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  L.a = take(2 * T * d);
+  L.u = take(2 * T * d);
+  L.z = take(2 * T * d);
+  L.logits = take(4 * T * V);
+  L.tl = take(4 * T);
+  L.scal = take(8);
+  L.dl = take(4 * T * V);
+  L.dz = take(4 * T * d);
+  L.du = take(4 * T * d);
+  L.da = take(2 * T * d);
+  L.partial = take(4 * std::max(lm_backward_partial_floats((int)T, (int)V, (int)d), bwd_partial_floats((int)T, (int)d)));
+  L.split_floats = (size_t)kMaxKSplit * d * d;
+  L.split = take(4 * L.split_floats);
+  L.total = off;
+  return L;
+}
+
+esm_status esm_encoder_lm_head_backward_workspace_size(const esm_encoder_t* h, int total_tokens, size_t* bytes) {
+  if (!h || !bytes || total_tokens < 0) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+  *bytes = lm_bwd_layout(h->cfg, total_tokens).total;
+  return ESM_OK;
+}
+
+esm_status esm_encoder_lm_head_backward(esm_encoder_t* h, const esm_lm_head* head, const void* hidden,
+                                        int total_tokens, const int32_t* targets, float* d_hidden,
+                                        const esm_lm_head_grads* grads, float* loss_sum, int* count, void* workspace,
+                                        size_t workspace_bytes, esm_stream_t stream) {
+  if (!h || !head || !grads || total_tokens <= 0 || !hidden || !d_hidden) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+  const void* p[6] = {head->dense_w, head->dense_b, head->ln_g, head->ln_b, head->emb, head->bias};
+  for (const void* q : p)
+    if (!q || !aligned(q, 16)) return ESM_ERR_INVALID_ARG;
+  float* gp[6] = {grads->dense_w, grads->dense_b, grads->ln_g, grads->ln_b, grads->emb, grads->bias};
+  for (float* q : gp)
+    if (!q || !aligned(q, 16)) return ESM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(d_hidden, 16)) return ESM_ERR_INVALID_ARG;
+  const int d = h->cfg.hidden, V = h->cfg.vocab, T = total_tokens;
+  if (!lm_logits_supported(V, d, true) || d % 256) return ESM_ERR_UNSUPPORTED;
+  const LmBwdLayout L = lm_bwd_layout(h->cfg, T);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return ESM_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
+  __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(ws + L.u);
+  __nv_bfloat16* z = reinterpret_cast<__nv_bfloat16*>(ws + L.z);
+  float* logits = reinterpret_cast<float*>(ws + L.logits);
+  float* tl = reinterpret_cast<float*>(ws + L.tl);
+  float* lsum = reinterpret_cast<float*>(ws + L.scal);
+  int* cnt = reinterpret_cast<int*>(ws + L.scal + 4);
+  float* dl = reinterpret_cast<float*>(ws + L.dl);
+  float* dz = reinterpret_cast<float*>(ws + L.dz);
+  float* du = reinterpret_cast<float*>(ws + L.du);
+  __nv_bfloat16* da = reinterpret_cast<__nv_bfloat16*>(ws + L.da);
+  float* partial = reinterpret_cast<float*>(ws + L.partial);
+  float* split = reinterpret_cast<float*>(ws + L.split);
+  // forward, keeping the pre-activation: u = GELU(a), a = hidden Wd^T + bd; z = LN(u); logits
+  esm_status s = run_gemm(h, P_OTHER, ESM_EPI_GELU, hidden, head->dense_w, head->dense_b, u, nullptr, T, d, d, false,
+                          Act::BF16, nullptr, nullptr, nullptr, nullptr, st, -1, nullptr, a);
+  if (s != ESM_OK) return s;
+  launch_layernorm_bf16in(u, head->ln_g, head->ln_b, false, z, Act::BF16, T, d, h->cfg.ln_eps, st);
+  if (launch_lm_logits(z, true, head->emb, head->bias, T, d, V, targets, logits, tl, lsum, cnt, h->num_sms, h->d_err,
+                       st) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  if (loss_sum && cudaMemcpyAsync(loss_sum, lsum, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return ESM_ERR_CUDA;
+  if (count && cudaMemcpyAsync(count, cnt, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return ESM_ERR_CUDA;
+  // backward of the mean masked cross-entropy
+  if (launch_lm_backward_head(logits, targets, cnt, head->emb, z, T, d, V, dl, dz, grads->emb, grads->bias, partial,
+                              h->num_sms, st) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  launch_ln_bwd_bf16in(u, head->ln_g, false, dz, du, grads->ln_g, grads->ln_b, partial, T, d, h->cfg.ln_eps, st);
+  launch_gelu_bwd(du, a, da, (size_t)T * d, st);
+  launch_colsum(da, true, T, d, grads->dense_b, partial, nullptr, st);
+  if ((s = run_wgrad(h, da, hidden, grads->dense_w, T, d, d, split, L.split_floats, st)) != ESM_OK) return s;
+  if ((s = run_dgrad(h, da, head->dense_w, d_hidden, false, T, d, d, st)) != ESM_OK) return s;
+  return cuda_status(cudaGetLastError());
+}
+
 esm_status esm_encoder_forward_host(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids_host,
                                     const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int max_seqlen,
                                     void* hidden_out_host, void* workspace, size_t workspace_bytes,

@@ -164,6 +164,21 @@ void launch_ln_bwd(const float* x, const void* gamma, bool gf32, const float* dy
 // rows as bf16.  partial: bwd_partial_floats(rows, cols) / 2 floats.  cols % 4 == 0.
 void launch_colsum(const void* src, bool bf16_in, int rows, int cols, float* out, float* partial, __nv_bfloat16* copy,
                    cudaStream_t st);
+// out[i] = scale * sum_k partial[k * stride + i] over k = 0..chunks-1, in index order.
+void reduce_chunks(const float* partial, int chunks, size_t stride, size_t n, float scale, float* out, cudaStream_t st);
+// LayerNorm backward of a bf16 input x (no residual gradient added): dx, dgamma, dbeta.
+void launch_ln_bwd_bf16in(const void* x, const void* gamma, bool gf32, const float* dy, float* dx, float* dgamma,
+                          float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st);
+// dz = du * GELU'(a) (a: bf16 pre-activation; dz bf16).
+void launch_gelu_bwd(const float* du, const __nv_bfloat16* a, __nv_bfloat16* dz, size_t n, cudaStream_t st);
+// Masked-LM head backward, output stage: dlogits of the mean masked cross-entropy (count =
+// number of scored tokens, device), dz = dlogits * emb (fp32 [T, d]), the tied embedding's
+// and the vocabulary bias's gradients (fp32, fixed-order sums over token chunks).  emb bf16,
+// z (the LayerNorm output) bf16.  partial: lm_backward_partial_floats floats.
+size_t lm_backward_partial_floats(int T, int V, int d);
+cudaError_t launch_lm_backward_head(const float* logits, const int32_t* targets, const int* count, const void* emb,
+                                    const __nv_bfloat16* z, int T, int d, int V, float* dl, float* dz, float* demb,
+                                    float* dbias, float* partial, int num_sms, cudaStream_t st);
 // out[i] = sum_s partial[s * n + i] (split-K partial products, in split order).
 void launch_reduce_splits(const float* partial, int splits, size_t n, float* out, cudaStream_t st);
 // demb[v] = scale * sum over tokens t with tok[t] == v of dx[t] (float32 [vocab, d]).

@@ -143,7 +143,156 @@ __global__ void __launch_bounds__(1024) loss_reduce_kernel(const float* __restri
   }
 }
 
+// ---------------------------------------------------------------- backward of the mean loss
+// dl[t, v] = (softmax(logits[t])[v] - [v == target[t]]) / count for scored tokens, 0 for the
+// others (and everywhere when nothing is scored).  One warp per token, lanes v and v + 32.
+__global__ void __launch_bounds__(256) lm_dlogits_kernel(const float* __restrict__ logits,
+                                                         const int32_t* __restrict__ targets,
+                                                         const int* __restrict__ count, int T, int V,
+                                                         float* __restrict__ dl) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int n = *count;
+  int tg = targets ? targets[t] : kIgnore;
+  if (tg != kIgnore && (tg < 0 || tg >= V)) tg = kIgnore;  // latched by the forward pass
+  const float* row = logits + (size_t)t * V;
+  float* out = dl + (size_t)t * V;
+  if (tg == kIgnore || n <= 0) {
+    if (lane < V) out[lane] = 0.f;
+    if (lane + 32 < V) out[lane + 32] = 0.f;
+    return;
+  }
+  const float lo = lane < V ? row[lane] : -INFINITY, hi = lane + 32 < V ? row[lane + 32] : -INFINITY;
+  const float m = warp_max_all(fmaxf(lo, hi));
+  const float elo = lane < V ? expf(lo - m) : 0.f, ehi = lane + 32 < V ? expf(hi - m) : 0.f;
+  const float inv = 1.f / warp_sum_all(elo + ehi);
+  const float sc = 1.f / (float)n;
+  if (lane < V) out[lane] = (elo * inv - (lane == tg ? 1.f : 0.f)) * sc;
+  if (lane + 32 < V) out[lane + 32] = (ehi * inv - (lane + 32 == tg ? 1.f : 0.f)) * sc;
+}
+
+// dz[t, :] = sum_v dl[t, v] emb[v, :] (bf16 table in shared memory, fp32 out).  One warp per
+// token; lane l owns the 8-column units l, l + 32, ... of the row.
+template <int NU>
+__global__ void __launch_bounds__(256) lm_dz_kernel(const float* __restrict__ dl, const void* __restrict__ emb,
+                                                    int T, int d, int V, float* __restrict__ dz) {
+  extern __shared__ __align__(16) uint8_t smem_e[];
+  const int units = d / 8;
+  {
+    const uint4* src = static_cast<const uint4*>(emb);
+    uint4* dst = reinterpret_cast<uint4*>(smem_e);
+    for (int i = threadIdx.x; i < V * units; i += blockDim.x) dst[i] = __ldg(src + i);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+  const uint4* e16 = reinterpret_cast<const uint4*>(smem_e);
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
+    const float dlo = lane < V ? dl[(size_t)t * V + lane] : 0.f;
+    const float dhi = lane + 32 < V ? dl[(size_t)t * V + lane + 32] : 0.f;
+    float acc[NU][8];
+#pragma unroll
+    for (int i = 0; i < NU; ++i)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
+    for (int v = 0; v < V; ++v) {
+      const float g = __shfl_sync(0xffffffffu, v < 32 ? dlo : dhi, v & 31);
+#pragma unroll
+      for (int i = 0; i < NU; ++i) {
+        const int c = i * 32 + lane;
+        if (c < units) {
+          float e[8];
+          unpack<true>(e16[v * units + c], e);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(g, e[k], acc[i][k]);
+        }
+      }
+    }
+    float4* out = reinterpret_cast<float4*>(dz + (size_t)t * d);
+#pragma unroll
+    for (int i = 0; i < NU; ++i) {
+      const int c = i * 32 + lane;
+      if (c < units) {
+        out[2 * c] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        out[2 * c + 1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+      }
+    }
+  }
+}
+
+// Partial sums over one chunk of tokens of the tied embedding's gradient
+// demb[v, c] = sum_t dl[t, v] z[t, c] (z bf16) and, in the blocks of column tile 0, of the
+// vocabulary bias's gradient dbias[v] = sum_t dl[t, v]; each thread owns one column and adds
+// the chunk's tokens in order.
+__global__ void __launch_bounds__(128) lm_demb_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ z,
+                                                      int T, int d, int V, int chunk_rows, float* __restrict__ pe,
+                                                      float* __restrict__ pb) {
+  extern __shared__ float sdl[];  // [chunk_rows][V] then acc [V][blockDim.x]
+  float* acc = sdl + (size_t)chunk_rows * V;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int chunk = blockIdx.y;
+  const int t0 = chunk * chunk_rows, t1 = min(T, t0 + chunk_rows);
+  for (int i = threadIdx.x; i < (t1 - t0) * V; i += blockDim.x) sdl[i] = dl[(size_t)t0 * V + i];
+  for (int v = 0; v < V; ++v) acc[v * blockDim.x + threadIdx.x] = 0.f;
+  __syncthreads();
+  if (c < d) {
+    for (int t = t0; t < t1; ++t) {
+      const float zv = __bfloat162float(z[(size_t)t * d + c]);
+      const float* g = sdl + (size_t)(t - t0) * V;
+      for (int v = 0; v < V; ++v) acc[v * blockDim.x + threadIdx.x] = fmaf(g[v], zv, acc[v * blockDim.x + threadIdx.x]);
+    }
+    for (int v = 0; v < V; ++v) pe[((size_t)chunk * V + v) * d + c] = acc[v * blockDim.x + threadIdx.x];
+  }
+  if (blockIdx.x == 0 && (int)threadIdx.x < V) {
+    float b = 0.f;
+    for (int t = 0; t < t1 - t0; ++t) b += sdl[(size_t)t * V + threadIdx.x];
+    pb[(size_t)chunk * V + threadIdx.x] = b;
+  }
+}
+
 }  // namespace
+
+constexpr int kLmChunkRows = 256;
+
+size_t lm_backward_partial_floats(int T, int V, int d) {
+  const size_t chunks = T <= 0 ? 1 : (T + kLmChunkRows - 1) / kLmChunkRows;
+  return chunks * V * (size_t)d + chunks * V;
+}
+
+cudaError_t launch_lm_backward_head(const float* logits, const int32_t* targets, const int* count, const void* emb,
+                                    const __nv_bfloat16* z, int T, int d, int V, float* dl, float* dz, float* demb,
+                                    float* dbias, float* partial, int num_sms, cudaStream_t st) {
+  if (T <= 0) {
+    cudaMemsetAsync(demb, 0, sizeof(float) * (size_t)V * d, st);
+    cudaMemsetAsync(dbias, 0, sizeof(float) * V, st);
+    return cudaGetLastError();
+  }
+  lm_dlogits_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, targets, count, T, V, dl);
+  const size_t smem = (size_t)V * d * 2;
+  const int nu = (d / 8 + 31) / 32;
+  int grid = num_sms * (smem <= 100 * 1024 ? 2 : 1);
+  if (grid > (T + 7) / 8) grid = (T + 7) / 8;
+#define ESM_LM_DZ(N)                                                                                   \
+  do {                                                                                                 \
+    cudaFuncSetAttribute(lm_dz_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
+    lm_dz_kernel<N><<<grid, 256, smem, st>>>(dl, emb, T, d, V, dz);                                   \
+  } while (0)
+  if (nu <= 1) ESM_LM_DZ(1);
+  else if (nu <= 2) ESM_LM_DZ(2);
+  else if (nu <= 4) ESM_LM_DZ(4);
+  else if (nu <= 8) ESM_LM_DZ(8);
+  else ESM_LM_DZ(16);
+#undef ESM_LM_DZ
+  const int chunks = (T + kLmChunkRows - 1) / kLmChunkRows;
+  float* pe = partial;
+  float* pb = partial + (size_t)chunks * V * d;
+  const size_t smem2 = sizeof(float) * ((size_t)kLmChunkRows * V + (size_t)V * 128);
+  cudaFuncSetAttribute(lm_demb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+  lm_demb_kernel<<<dim3((d + 127) / 128, chunks), 128, smem2, st>>>(dl, z, T, d, V, kLmChunkRows, pe, pb);
+  reduce_chunks(pe, chunks, (size_t)V * d, (size_t)V * d, 1.f, demb, st);
+  reduce_chunks(pb, chunks, (size_t)V, (size_t)V, 1.f, dbias, st);
+  return cudaGetLastError();
+}
 
 size_t lm_logits_smem_bytes(int vocab, int hidden, bool bf16) { return (size_t)vocab * hidden * (bf16 ? 2 : 4); }
 
