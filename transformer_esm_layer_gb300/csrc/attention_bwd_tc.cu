@@ -451,8 +451,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Each warp stages its 32 rows of dQ_i (fp32, 128-byte swizzle, two 32-column boxes) and
     // adds them into the global accumulator with TMA reduce-add; rows of queries past the
     // sequence end hold exact zeros (their dS columns are zero), so adding them is harmless.
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // query row of the tile
+    const int wq = warp & 3;  // lane l owns query row 32 wq + l of the tile
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     uint8_t* stage = base + OFF_DQ + wq * DQ_WARP_BYTES;
     if (lane == 0) tma_prefetch_desc(&tm_dq);
