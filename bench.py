@@ -184,6 +184,29 @@ def cpu_oracle_sample(wl, w64, seconds: float, prec: str = "bf16", enc=None):
     return toks, dt, done
 
 
+def cpu_oracle_train_sample(wl, w64, seconds: float, seed: int = 0):
+    """Time the float64 oracle's training step (forward recomputed, then every gradient) on
+    whole sequences of the workload, with a seeded dL/d(output), until `seconds` pass."""
+    from oracle import backward as B
+    from oracle import esm_oracle as O
+    from transformer_esm_layer_gb300 import synth
+    tok = synth.workload_tokens(wl)
+    cu = O.cu_seqlens(wl.lengths)
+    rng = np.random.default_rng(seed)
+    done, toks = [], 0
+    t0 = time.perf_counter()
+    for i in range(len(wl.lengths)):
+        L = int(wl.lengths[i])
+        B.encode_sequence_backward(tok[cu[i]:cu[i + 1]], w64, wl.geometry.heads,
+                                   rng.standard_normal((L, wl.geometry.hidden)), final_ln=True)
+        done.append(i)
+        toks += L
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return toks, dt, done
+
+
 def f64_weights(w):
     return {"emb": np.asarray(w["emb"], np.float64),
             "layers": [{k: np.asarray(v, np.float64) for k, v in l.items()} for l in w["layers"]],
@@ -490,6 +513,13 @@ def run_ours(args):
                                                                             "gemm_fc1", "gemm_fc2", "layernorm",
                                                                             "other")},
                  "train_buffer_gb": tb.numel() / 2**30}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            toks_c, dt_c, done_c = cpu_oracle_train_sample(wl, f64_weights(w_np), args.cpu_seconds, wl.seed)
+            train["cpu_baseline"] = {"value": toks_c / dt_c, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                                     "kind": "oracle",
+                                     "sample": f"{len(done_c)} whole sequence(s) of the workload ({toks_c} tokens): "
+                                               f"forward and every gradient through all {g.num_layers} layers in "
+                                               f"float64 numpy, {dt_c:.1f} s"}
         del tb, grads
 
     # ---------------------------------------------------------------- CPU baseline (oracle)
