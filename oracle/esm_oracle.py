@@ -168,10 +168,23 @@ FP8_TENSORS = ("x_qkv", "w_qkv", "x_o", "w_o", "x_1", "w_1", "x_2", "w_2")
 
 
 # --------------------------------------------------------------------------- layer / encoder
+FP8_WEIGHTS = ("w_qkv", "w_o", "w_1", "w_2")
+
+
+def fp8_quantised_weights(w: Dict[str, np.ndarray], fp8_scales: Dict[str, float]) -> Dict[str, np.ndarray]:
+    """The four linear weights of one layer as the FP8 path sees them, deq(q(w * s_w)) / s_w
+    with each weight's own per-tensor scale.  A weight has one scale per call, so this is
+    the same for every sequence of the call; the other entries are returned unchanged."""
+    out = dict(w)
+    for k in FP8_WEIGHTS:
+        out[k] = fp8_fake_quant(np.asarray(w[k], np.float64), fp8_scales[k])
+    return out
+
+
 def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], heads: int,
                   eps: float = LN_EPS, rope_base: float = ROPE_BASE, n_keys: Optional[int] = None,
                   fp8_scales: Optional[Dict[str, float]] = None, amax_out: Optional[Dict[str, float]] = None,
-                  bf16_attention: bool = False):
+                  bf16_attention: bool = False, weights_quantised: bool = False):
     """One pre-LN encoder layer on one sequence x[L, d] (float64).
 
     y = LN1(x); [q|k|v] = y Wqkv^T + bqkv; RoPE on q, k; o = attention(q, k, v);
@@ -179,7 +192,9 @@ def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], head
 
     With ``fp8_scales`` every GEMM operand (the four activations and four weights) is
     replaced by its E4M3 fake-quantised value; ``amax_out`` then receives max|.| of each
-    operand before quantisation.  ``bf16_attention`` rounds the attention operands q, k, v
+    operand before quantisation.  ``weights_quantised`` says the four weights in ``w`` are
+    already fake-quantised with these scales (``fp8_quantised_weights``), so only the
+    activations are quantised here.  ``bf16_attention`` rounds the attention operands q, k, v
     to bfloat16 (the FP8 workload keeps attention in bf16)."""
     L, d = x.shape
     dh = d // heads
@@ -189,9 +204,11 @@ def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], head
         if fp8_scales is not None:
             if amax_out is not None:
                 amax_out[aname] = max(amax_out.get(aname, 0.0), float(np.abs(a).max(initial=0.0)))
-                amax_out[wname] = float(np.abs(wt).max())
+                if not weights_quantised:
+                    amax_out[wname] = float(np.abs(wt).max())
             a = fp8_fake_quant(a, fp8_scales[aname])
-            wt = fp8_fake_quant(wt, fp8_scales[wname])
+            if not weights_quantised:
+                wt = fp8_fake_quant(wt, fp8_scales[wname])
         return a @ wt.T
 
     y = layer_norm(x, w["ln1_g"], w["ln1_b"], eps)
@@ -237,16 +254,36 @@ def encode_sequence(tokens: np.ndarray, weights: Dict, heads: int, final_ln: boo
 
 
 def encode_packed(token_ids: np.ndarray, cu: Sequence[int], weights: Dict, heads: int,
-                  final_ln: bool = True, seq_subset: Optional[Sequence[int]] = None, **kw) -> Dict[int, np.ndarray]:
-    """The packed forward: every sequence [cu[i], cu[i+1]) is encoded on its own.
-
-    Returns {sequence index: [L_i, d] float64}.  ``seq_subset`` limits the work to some
-    sequences (packed sequences never interact, so each output is exact on its own)."""
-    idx = range(len(cu) - 1) if seq_subset is None else seq_subset
-    out = {}
-    for i in idx:
-        out[i] = encode_sequence(token_ids[int(cu[i]):int(cu[i + 1])], weights, heads, final_ln, **kw)
-    return out
+                  final_ln: bool = True, seq_subset: Optional[Sequence[int]] = None,
+                  emb_scale: float = 1.0, eps: float = LN_EPS, rope_base: float = ROPE_BASE,
+                  num_layers: Optional[int] = None, n_keys: Optional[int] = None,
+                  fp8_state: Optional[List[Dict[str, float]]] = None,
+                  amax_out: Optional[List[Dict[str, float]]] = None,
+                  bf16_attention: bool = False) -> Dict[int, np.ndarray]:
+    """The packed forward: every sequence [cu[i], cu[i+1]) is encoded on its own, with the
+    same steps as ``encode_sequence``; the loop runs layer by layer over the sequences so
+    that a layer's weights are converted (and, with an FP8 state, fake-quantised with their
+    per-tensor scales) once for the whole call, as the weights are the same for every
+    sequence.  Returns {sequence index: [L_i, d] float64}.  ``seq_subset`` limits the work to
+    some sequences (packed sequences never interact, so each output is exact on its own)."""
+    idx = list(range(len(cu) - 1)) if seq_subset is None else list(seq_subset)
+    emb = np.asarray(weights["emb"], dtype=np.float64)
+    xs = {i: emb_scale * emb[np.asarray(token_ids[int(cu[i]):int(cu[i + 1])], dtype=np.int64)] for i in idx}
+    layers = weights["layers"] if num_layers is None else weights["layers"][:num_layers]
+    for li, wl in enumerate(layers):
+        scales = None if fp8_state is None else fp8_state[li]
+        wl64 = _f64_layer(wl)
+        pre = scales is not None and amax_out is None
+        if pre:
+            wl64 = fp8_quantised_weights(wl64, scales)
+        for i in idx:
+            xs[i] = encoder_layer(xs[i], np.arange(len(xs[i])), wl64, heads, eps, rope_base, n_keys, scales,
+                                  None if amax_out is None else amax_out[li], bf16_attention, weights_quantised=pre)
+        del wl64
+    if final_ln:
+        g, b = np.asarray(weights["lnf_g"], np.float64), np.asarray(weights["lnf_b"], np.float64)
+        xs = {i: layer_norm(x, g, b, eps) for i, x in xs.items()}
+    return xs
 
 
 def encode_padded(token_ids: np.ndarray, seq_lens: Sequence[int], weights: Dict, heads: int,

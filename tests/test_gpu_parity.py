@@ -265,7 +265,7 @@ def _run_packed(g, precision, w, tokens, lengths, final_ln=True):
     return enc, dw, to_np(out)
 
 
-def test_forward_tiny_fp32_config():
+def test_forward_tiny_fp32_config(margin):
     """The tiny fp32 workload: 2 layers, hidden 64, 4 heads, lengths 17/40/7."""
     wl = synth.make_workload("tiny_fp32")
     g = wl.geometry
@@ -274,10 +274,10 @@ def test_forward_tiny_fp32_config():
     _, _, got = _run_packed(g, "fp32", w, tok, wl.lengths)
     ref = O.encode_packed(tok, O.cu_seqlens(wl.lengths), w, g.heads, final_ln=True)
     ref = np.concatenate([ref[i] for i in range(len(wl.lengths))])
-    assert rel_l2(got, ref) < 1e-4
+    assert margin("tiny fp32 encoder", rel_l2(got, ref), 1e-4) < 1e-4
 
 
-def test_forward_bf16_two_layers_ragged():
+def test_forward_bf16_two_layers_ragged(margin):
     g = synth.Geometry(num_layers=2, hidden=1280, heads=20, ffn=5120)
     lengths = [1, 2, 130, 64, 257, 1024, 33]
     w = synth.model_weights(g, 21, "bf16", ln_random=True)
@@ -285,10 +285,10 @@ def test_forward_bf16_two_layers_ragged():
     _, _, got = _run_packed(g, "bf16", w, tok, lengths)
     ref = O.encode_packed(tok, O.cu_seqlens(lengths), w, g.heads, final_ln=True)
     ref = np.concatenate([ref[i] for i in range(len(lengths))])
-    assert rel_l2(got, ref) < 1e-2
+    assert margin("650M width x2, ragged lengths", rel_l2(got, ref), 1e-2) < 1e-2
 
 
-def test_forward_single_layer_workload():
+def test_forward_single_layer_workload(margin):
     """One ESM-2 650M layer, 16 log-normal sequences, no final LN."""
     wl = synth.make_workload("layer650m")
     g = wl.geometry
@@ -297,8 +297,8 @@ def test_forward_single_layer_workload():
     _, _, got = _run_packed(g, "bf16", w, tok, wl.lengths, final_ln=False)
     c = O.cu_seqlens(wl.lengths)
     ref = O.encode_packed(tok, c, w, g.heads, final_ln=False)
-    for i in range(len(wl.lengths)):
-        assert rel_l2(got[c[i]:c[i + 1]], ref[i]) < 1e-2, i
+    worst = max(rel_l2(got[c[i]:c[i + 1]], ref[i]) for i in range(len(wl.lengths)))
+    assert margin("one 650M layer workload, worst of 16 sequences", worst, 1e-2) < 1e-2
 
 
 def test_packed_equals_each_sequence_alone_bitwise():
@@ -334,24 +334,6 @@ def test_padded_equals_packed():
         assert rel_l2(out[b, :L], ref[b][:L]) < 1e-2
 
 
-def test_full_650m_workload_sampled_sequences():
-    """The full 33-layer 650M encoder on 16384 packed tokens (seed 2), in the launch
-    configuration the benchmark times; the oracle checks the shortest, the longest and a
-    middle sequence (packed sequences are independent, so each is exact on its own)."""
-    wl = synth.make_workload("esm650m")
-    g = wl.geometry
-    w = synth.model_weights(g, wl.seed, "bf16")
-    tok = synth.workload_tokens(wl)
-    _, _, got = _run_packed(g, "bf16", w, tok, wl.lengths)
-    assert np.isfinite(got).all()
-    order = np.argsort(wl.lengths)
-    pick = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
-    c = O.cu_seqlens(wl.lengths)
-    ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, seq_subset=pick)
-    for i in pick:
-        assert rel_l2(got[c[i]:c[i + 1]], ref[i]) < 1e-2, (i, wl.lengths[i])
-
-
 # --------------------------------------------------------------------------- errors
 def test_forward_host_matches_device_forward():
     """esm_encoder_forward_host (host token ids / cu_seqlens in, host bf16 hidden states out,
@@ -374,7 +356,7 @@ def test_forward_host_matches_device_forward():
     assert np.array_equal(host_out, dev_out)
 
 
-def test_fp8_forward_one_layer_3b_width():
+def test_fp8_forward_one_layer_3b_width(margin):
     """One layer of the 3B geometry (hidden 2560, 40 heads, ffn 10240) with E4M3 GEMMs against
     the oracle with the same scales (5e-2; attention in bf16)."""
     g = synth.Geometry(num_layers=1, hidden=2560, heads=40, ffn=10240)
@@ -385,7 +367,7 @@ def test_fp8_forward_one_layer_3b_width():
     c = O.cu_seqlens(lengths)
     ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, fp8_state=fp8_state, bf16_attention=True)
     ref = np.concatenate([ref[i] for i in range(len(lengths))])
-    assert rel_l2(out, ref) < 5e-2
+    assert margin("one 3B-width FP8 layer", rel_l2(out, ref), 5e-2) < 5e-2
 
 
 def test_token_out_of_range_reported():
@@ -515,7 +497,7 @@ def _fp8_run(g, lengths, seed, calls=3, layer_precision=None):
     return enc, w, tok, st, out
 
 
-def test_fp8_forward_one_layer_and_delayed_scaling():
+def test_fp8_forward_one_layer_and_delayed_scaling(margin):
     """One 650M-width layer with E4M3 GEMMs (history 16, max), attention in bf16.  After
     three warm-up calls the scales are read back; the next call matches the oracle using
     those scales within 5e-2, and that call's state update is exact: the history rolls by
@@ -531,7 +513,7 @@ def test_fp8_forward_one_layer_and_delayed_scaling():
     ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, fp8_state=fp8_state, amax_out=amax,
                           bf16_attention=True)
     ref = np.concatenate([ref[i] for i in range(len(lengths))])
-    assert rel_l2(out, ref) < 5e-2
+    assert margin("one 650M-width FP8 layer", rel_l2(out, ref), 5e-2) < 5e-2
     st2 = enc.get_fp8_state()
     hist2, scales2 = enc.fp8_history(st2), enc.fp8_scales(st2)
     for l in range(g.num_layers):
@@ -582,7 +564,7 @@ def test_layer_precision_rejections():
         EsmEncoder.from_geometry(g, "fp4")
 
 
-def test_fp8_forward_depth_accuracy():
+def test_fp8_forward_depth_accuracy(margin):
     """Two 650M-width layers: the GPU's FP8 forward is as close to the exact (unquantised)
     forward as the oracle's own FP8 forward with the same scales, and the two FP8 results
     differ by less than two independent FP8 evaluations would (sqrt(2) x the FP8 error)."""
@@ -597,6 +579,7 @@ def test_fp8_forward_depth_accuracy():
     exact = cat(O.encode_packed(tok, c, w, g.heads, final_ln=True))
     e_oracle = rel_l2(ref8, exact)
     e_gpu = rel_l2(out, exact)
+    margin("two 650M-width FP8 layers vs the oracle's FP8 forward", rel_l2(out, ref8), 5e-2)
     assert e_oracle > 1e-2                      # quantisation really happened on both sides
     assert e_gpu < 1.25 * e_oracle, (e_gpu, e_oracle)
     assert rel_l2(out, ref8) < np.sqrt(2) * e_oracle

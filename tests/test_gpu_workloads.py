@@ -1,0 +1,127 @@
+"""Parity at the configured workload sizes, in the launch configuration the benchmark times.
+
+* ESM-2 650M packed, 33 layers, 16384 tokens (47 sequences, seed 2), bf16: sampled whole
+  sequences against the float64 oracle at 1e-2 relative L2.
+* The same sequences in the padded [47, 1024] layout with a key padding mask: sampled rows
+  against the oracle at 1e-2, every pad row exactly zero, and every sequence's valid rows
+  against the packed forward of the same batch.
+* ESM-2 3B, 36 layers, 32768 tokens (seed 3), E4M3 GEMMs with per-tensor delayed scaling
+  (history 16): after 16 warm-up calls on the batch (full history) the scales are read
+  back and the next call is compared, on sampled whole sequences, with the oracle's FP8
+  forward using those scales (attention in bf16), at the stated 5e-2.
+
+Packed sequences never interact, so the oracle encodes only the sampled sequences and each
+is exact on its own.  Every check records the error it reached (listed at the end of the
+run)."""
+import numpy as np
+import pytest
+
+from oracle import esm_oracle as O
+from tests._util import ensure_built, rel_l2, to_np
+from transformer_esm_layer_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def _sample(lengths, k):
+    """k sequences spread over the length order: shortest, longest and evenly spaced ranks."""
+    order = np.argsort(np.asarray(lengths), kind="stable")
+    ranks = np.unique(np.round(np.linspace(0, len(order) - 1, k)).astype(int))
+    return [int(order[r]) for r in ranks]
+
+
+@pytest.fixture(scope="module")
+def esm650m():
+    """The 33-layer 650M workload: weights, tokens and the packed forward's output."""
+    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
+    wl = synth.make_workload("esm650m")
+    g = wl.geometry
+    w = synth.model_weights(g, wl.seed, "bf16")
+    tok = synth.workload_tokens(wl)
+    enc = EsmEncoder.from_geometry(g, "bf16", final_ln=True)
+    dw = DeviceWeights(w, "bf16")
+    t, cu = packed_inputs(tok, wl.lengths)
+    out = enc.forward(dw, t, cu, max(wl.lengths))
+    enc.check()
+    return {"wl": wl, "w": w, "tok": tok, "enc": enc, "dw": dw, "packed": to_np(out)}
+
+
+def test_esm650m_workload_sampled_sequences(esm650m, margin):
+    wl, w, tok, got = esm650m["wl"], esm650m["w"], esm650m["tok"], esm650m["packed"]
+    assert np.isfinite(got).all()
+    pick = _sample(wl.lengths, 7)
+    c = O.cu_seqlens(wl.lengths)
+    ref = O.encode_packed(tok, c, w, wl.geometry.heads, final_ln=True, seq_subset=pick)
+    worst = max(rel_l2(got[c[i]:c[i + 1]], ref[i]) for i in pick)
+    joint = rel_l2(np.concatenate([got[c[i]:c[i + 1]] for i in pick]), np.concatenate([ref[i] for i in pick]))
+    margin(f"650M x33 packed, worst of {len(pick)} sequences (lengths {[wl.lengths[i] for i in pick]})", worst, 1e-2)
+    margin("650M x33 packed, sampled tokens jointly", joint, 1e-2)
+    assert worst < 1e-2
+
+
+def test_esm650m_padded_workload(esm650m, margin):
+    """[47, 1024] padded layout of the same sequences, all 33 layers."""
+    wl, w, tok, enc, dw = esm650m["wl"], esm650m["w"], esm650m["tok"], esm650m["enc"], esm650m["dw"]
+    S = 1024
+    padded = torch.from_numpy(synth.pad_tokens(tok, wl.lengths, S)).cuda()
+    lens = torch.tensor(wl.lengths, dtype=torch.int32, device="cuda")
+    out = enc.forward_padded(dw, padded, lens)
+    enc.check()
+    out = to_np(out)
+    packed = esm650m["packed"]
+    c = O.cu_seqlens(wl.lengths)
+    worst_pp = 0.0
+    for b, L in enumerate(wl.lengths):
+        assert np.all(out[b, L:] == 0), b                    # pad rows are written as zero
+        worst_pp = max(worst_pp, rel_l2(out[b, :L], packed[c[b]:c[b + 1]]))
+    margin("650M x33 padded vs packed, worst of all 47 sequences", worst_pp, 1e-3)
+    assert worst_pp < 1e-3
+    pick = _sample(wl.lengths, 5)
+    ref = O.encode_padded(padded.cpu().numpy(), wl.lengths, w, wl.geometry.heads, seq_subset=pick)
+    worst = max(rel_l2(out[b, :wl.lengths[b]], ref[b][:wl.lengths[b]]) for b in pick)
+    margin(f"650M x33 padded vs oracle, worst of {len(pick)} sequences", worst, 1e-2)
+    assert worst < 1e-2
+
+
+def test_esm3b_fp8_workload_sampled_sequences(margin):
+    """The configured FP8 workload end to end at the stated bound (no relative criterion)."""
+    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
+    wl = synth.make_workload("esm3b_fp8")
+    g = wl.geometry
+    w = synth.model_weights(g, wl.seed, "fp8")
+    tok = synth.workload_tokens(wl)
+    enc = EsmEncoder.from_geometry(g, "fp8", final_ln=True, amax_history_len=16)
+    dw = DeviceWeights(w, "fp8")
+    t, cu = packed_inputs(tok, wl.lengths)
+    ws = enc.workspace(len(tok), len(wl.lengths))
+    out = torch.empty(len(tok), g.hidden, dtype=torch.bfloat16, device="cuda")
+    for _ in range(16):                                       # fill the 16-entry amax history
+        enc.forward(dw, t, cu, max(wl.lengths), out=out, workspace=ws)
+    enc.check()
+    scales = enc.fp8_scales(enc.get_fp8_state())
+    enc.forward(dw, t, cu, max(wl.lengths), out=out, workspace=ws)
+    enc.check()
+    got = to_np(out)
+    del dw, ws, out
+    torch.cuda.empty_cache()
+    assert np.isfinite(got).all()
+    assert np.all(scales > 0) and np.all(np.isfinite(scales))
+    fp8_state = [{k: float(scales[l, i]) for i, k in enumerate(O.FP8_TENSORS)} for l in range(g.num_layers)]
+    pick = _sample(wl.lengths, 3)
+    c = O.cu_seqlens(wl.lengths)
+    ref = O.encode_packed(tok, c, w, g.heads, final_ln=True, seq_subset=pick, fp8_state=fp8_state,
+                          bf16_attention=True)
+    errs = {wl.lengths[i]: rel_l2(got[c[i]:c[i + 1]], ref[i]) for i in pick}
+    joint = rel_l2(np.concatenate([got[c[i]:c[i + 1]] for i in pick]), np.concatenate([ref[i] for i in pick]))
+    for L, e in errs.items():
+        margin(f"3B x36 FP8, sequence of length {L}", e, 5e-2)
+    margin("3B x36 FP8, sampled tokens jointly", joint, 5e-2)
+    assert max(errs.values()) < 5e-2, errs
