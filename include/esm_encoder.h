@@ -229,8 +229,14 @@ ESM_API esm_status esm_encoder_lm_head(esm_encoder_t* h, const esm_lm_head* head
  * esm_encoder_lm_head; d_hidden: device float32 [T, hidden] (overwritten); grads: device
  * float32 buffers shaped like the head's parameters (overwritten; grads->emb is the head's
  * part of the tied embedding's gradient: add esm_encoder_backward's grads->emb for the
- * total); loss_sum, count: device scalars or NULL.  Unscored rows (target -100) get zero
- * gradient; with nothing scored every gradient is zero.  Workspace: the size query's bytes. */
+ * total); loss_sum, count: device scalars or NULL (this call's scored-token loss sum and
+ * count).  loss_count: device int32 scalar or NULL: the number of scored tokens the mean is
+ * taken over.  NULL means this call's own count.  A data-parallel step passes the scored count
+ * of the whole global batch (all ranks' counts summed first), so that every rank
+ * differentiates the same loss, sum over all scored tokens / global count, and the ranks'
+ * gradients summed over ranks are the batch gradient.  Unscored rows (target -100) get zero
+ * gradient; with nothing scored (or loss_count <= 0) every gradient is zero.  Workspace: the
+ * size query's bytes. */
 typedef struct {
   float* dense_w;
   float* dense_b;
@@ -244,7 +250,8 @@ ESM_API esm_status esm_encoder_lm_head_backward_workspace_size(const esm_encoder
 ESM_API esm_status esm_encoder_lm_head_backward(esm_encoder_t* h, const esm_lm_head* head, const void* hidden,
                                                 int total_tokens, const int32_t* targets, float* d_hidden,
                                                 const esm_lm_head_grads* grads, float* loss_sum, int* count,
-                                                void* workspace, size_t workspace_bytes, esm_stream_t stream);
+                                                const int* loss_count, void* workspace, size_t workspace_bytes,
+                                                esm_stream_t stream);
 
 /* Synchronise `stream` and return (and clear) the first error the kernels latched
  * since the last check: ESM_ERR_BAD_CU_SEQLENS, ESM_ERR_TOKEN_RANGE, ESM_ERR_TIMEOUT
@@ -317,23 +324,27 @@ ESM_API esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int
  * No counterpart on the pages: this entry point exists for callers that cannot allocate
  * device memory (a memory pool or allocator that owns the whole device, a plugin host that
  * hands out only its input and output buffers, a runtime that forbids allocation after
- * start-up).  It computes exactly what esm_op_attention computes for bf16, head_dim 64
- * (qkv device bf16 [T, 3*hidden], q | k | v head-major, RoPE applied; o device bf16
- * [T, hidden]; cu_seqlens device int32 [num_seqs + 1]) without a handle or a workspace:
- * its scratch is a fixed device array inside the library (about 655 KB, held by every
- * GPU that loads the library until the process exits).
+ * start-up).  It runs the same tcgen05 attention kernel as esm_op_attention on a bf16
+ * handle, head_dim 64 (qkv device bf16 [T, 3*hidden], q | k | v head-major, RoPE applied,
+ * 16-byte aligned; o device bf16 [T, hidden]; cu_seqlens device int32 [num_seqs + 1]),
+ * without a handle or a workspace: its scratch is a fixed device array inside the library
+ * (about 650 KB, held by every GPU that loads the library until the process exits), and
+ * the kernel's TMA descriptor is encoded on the host for each call.
  * Limits: total_tokens <= ESM_NOALLOC_MAX_TOKENS, num_seqs <= ESM_NOALLOC_MAX_SEQS,
  * max_seqlen <= ESM_NOALLOC_MAX_TOKENS; larger sizes return ESM_ERR_INVALID_ARG.
  * hidden must be 64 * heads (ESM_ERR_UNSUPPORTED otherwise, or off sm_103).
+ * status: device int32 or NULL.  When given, it receives (in stream order, after the
+ * attention) ESM_OK, ESM_ERR_BAD_CU_SEQLENS if cu_seqlens was malformed (the offsets are
+ * then clamped so every access stays in bounds, and o is not meaningful), or
+ * ESM_ERR_TIMEOUT if a bounded device wait gave up.
  * The first call on each device looks up the array's device address (with that device
  * current) and caches it: make that first call before any stream capture.  Calls share
- * the array, so calls that overlap on the GPU (different streams) race.  Malformed
- * cu_seqlens are clamped so every access stays in bounds; they are not reported. */
+ * the array, so calls that overlap on the GPU (different streams) race. */
 #define ESM_NOALLOC_MAX_TOKENS 65536
 #define ESM_NOALLOC_MAX_SEQS 4096
 ESM_API esm_status esm_op_attention_noalloc(const void* qkv, const int32_t* cu_seqlens, int num_seqs,
                                             int total_tokens, int max_seqlen, int hidden, int heads, void* o,
-                                            esm_stream_t stream);
+                                            int32_t* status, esm_stream_t stream);
 
 /* ---- FP8 delayed-scaling state (ESM_FP8_E4M3 handles) ----
  * Layout, float32: for each layer l and each of the 8 quantised tensors k in the order

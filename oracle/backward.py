@@ -200,11 +200,17 @@ def encode_packed_backward(token_ids: np.ndarray, cu: Sequence[int], weights: Di
 
 
 # --------------------------------------------------------------------------- masked-LM head
-def lm_head_backward(h: np.ndarray, w: Dict[str, np.ndarray], targets: Sequence[int]):
+def lm_head_backward(h: np.ndarray, w: Dict[str, np.ndarray], targets: Sequence[int],
+                     count: Optional[int] = None):
     """Gradients of the mean masked-LM loss L = sum_scored CE / count (the forward of
     ``esm_oracle.lm_head`` and ``masked_lm_loss``) with respect to the hidden states h [T, d]
     and the head's parameters.  The embedding E is tied: the gradient returned for it is the
     head's part only (the encoder's embedding gradient adds to it).
+
+    ``count`` is the number of scored tokens the mean is taken over: by default those of
+    ``targets``.  When a batch is split over data-parallel ranks, each rank passes the
+    scored count of the whole batch, so that every rank differentiates its own share of the
+    same loss and the ranks' gradients add up to the batch gradient.
 
     With logits l = z E^T + b, z = LN(u), u = GELU(a), a = h Wd^T + bd:
     dl = (softmax(l) - onehot(target)) / count on scored rows (0 elsewhere),
@@ -220,9 +226,10 @@ def lm_head_backward(h: np.ndarray, w: Dict[str, np.ndarray], targets: Sequence[
     logits = z @ E.T + np.asarray(w["bias"], np.float64)
     t = np.asarray(targets, np.int64)
     scored = t != IGNORE_INDEX
-    count = int(scored.sum())
+    if count is None:
+        count = int(scored.sum())
     dl = np.zeros_like(logits)
-    if count:
+    if count > 0 and scored.any():
         m = logits.max(axis=1, keepdims=True)
         p = np.exp(logits - m)
         p /= p.sum(axis=1, keepdims=True)

@@ -55,7 +55,7 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.esm_op_attention_backward_workspace_size(None, 4, 1, ctypes.byref(n)) == 1
     assert lib.esm_op_attention_backward(None, None, None, None, None, None, 1, 1, 1, None, None, 0, None) == 1
     assert lib.esm_encoder_lm_head_backward_workspace_size(None, 4, ctypes.byref(n)) == 1
-    assert lib.esm_encoder_lm_head_backward(None, None, None, 1, None, None, None, None, None, None, 0, None) == 1
+    assert lib.esm_encoder_lm_head_backward(None, None, None, 1, None, None, None, None, None, None, None, 0, None) == 1
     lib.esm_encoder_destroy(None)
 
 

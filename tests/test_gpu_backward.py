@@ -320,6 +320,23 @@ def test_lm_head_backward(T, rate):
         assert rel_l2(to_np(grads[k]), ref[k]) < 2e-2, k
 
 
+def test_lm_head_backward_with_a_global_count():
+    """loss_count: the mean is taken over a count given by the caller (the scored tokens of a
+    whole data-parallel batch) instead of this call's own."""
+    g = SMALL
+    head, dh, targets, h = _head_case(g, 200, 32, 0.3)
+    enc = _enc(g)
+    n_local = int((targets != -100).sum())
+    n_global = 3 * n_local + 5
+    d_hidden, grads = enc.lm_head_backward(dh, _dev(h, torch.bfloat16), torch.from_numpy(targets).cuda(),
+                                           loss_count=torch.tensor([n_global], dtype=torch.int32, device="cuda"))
+    assert enc.check_status() == 0
+    ref = B.lm_head_backward(h.astype(np.float64), head, targets, count=n_global)
+    assert rel_l2(to_np(d_hidden), ref["hidden"]) < 2e-2
+    for k in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias"):
+        assert rel_l2(to_np(grads[k]), ref[k]) < 2e-2, k
+
+
 def test_training_step_from_masked_lm_loss():
     """forward_train -> masked-LM head backward -> encoder backward, against the oracle chain
     (the tied embedding's gradient is the head's part plus the encoder's part)."""

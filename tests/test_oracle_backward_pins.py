@@ -277,3 +277,51 @@ def test_lm_head_backward_vs_torch_autograd_and_unscored_rows():
     assert np.all(g["hidden"][[1, 4]] == 0)
     g0 = B.lm_head_backward(h, w, np.full(7, -100))
     assert all(np.all(v == 0) for v in g0.values())
+
+
+def test_lm_head_backward_with_a_global_count():
+    """With the mean taken over a given count N (the scored tokens of a whole data-parallel
+    batch), the gradient is that of sum_scored CE / N: checked by finite differences of that
+    loss, and torch autograd of cross-entropy with reduction "sum" divided by N.  Two shares
+    of a batch with uneven scored counts, each differentiated with the batch's count, add up
+    to the whole batch's gradient."""
+    rng = np.random.default_rng(25)
+    w = _lm_weights(seed=26)
+    h = rng.standard_normal((11, 16))
+    t = rng.integers(0, 33, 11)
+    t[[0, 2, 3, 9]] = -100
+    N = 17
+    g = B.lm_head_backward(h, w, t, count=N)
+
+    def loss_over_n(hh, ww):
+        _, s, _ = O.masked_lm_loss(O.lm_head(hh, ww), t)
+        return s / N
+
+    for idx in _sample_idx(rng, h.shape, 8):
+        assert g["hidden"][idx] == pytest.approx(_fd(lambda hh: loss_over_n(hh, w), h, idx), rel=1e-6, abs=1e-8)
+    for idx in _sample_idx(rng, w["emb"].shape, 4):
+        def J(pp):
+            ww = dict(w)
+            ww["emb"] = pp
+            return loss_over_n(h, ww)
+        assert g["emb"][idx] == pytest.approx(_fd(J, w["emb"], idx), rel=1e-6, abs=1e-8)
+    T_ = lambda a: torch.tensor(np.asarray(a, np.float64), requires_grad=True)
+    P = {k: T_(v) for k, v in w.items()}
+    H = T_(h)
+    z = F.layer_norm(F.gelu(F.linear(H, P["dense_w"], P["dense_b"])), (16,), P["ln_g"], P["ln_b"], 1e-5)
+    loss = F.cross_entropy(F.linear(z, P["emb"], P["bias"]), torch.from_numpy(t), ignore_index=-100,
+                           reduction="sum") / N
+    loss.backward()
+    assert np.allclose(g["hidden"], H.grad.numpy(), rtol=1e-10, atol=1e-12)
+    for k in P:
+        assert np.allclose(g[k], P[k].grad.numpy(), rtol=1e-10, atol=1e-12), k
+    # split into two shares with 4 and 3 scored tokens: each uses the batch count
+    whole = B.lm_head_backward(h, w, t)
+    n_all = int((t != -100).sum())
+    a, b = slice(0, 6), slice(6, 11)
+    ga = B.lm_head_backward(h[a], w, t[a], count=n_all)
+    gb = B.lm_head_backward(h[b], w, t[b], count=n_all)
+    assert int((t[a] != -100).sum()) != int((t[b] != -100).sum())
+    assert np.allclose(np.concatenate([ga["hidden"], gb["hidden"]]), whole["hidden"], rtol=0, atol=1e-14)
+    for k in ("dense_w", "dense_b", "ln_g", "ln_b", "emb", "bias"):
+        assert np.allclose(ga[k] + gb[k], whole[k], rtol=1e-12, atol=1e-14), k

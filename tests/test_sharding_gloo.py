@@ -134,3 +134,60 @@ def test_two_rank_gloo_gradient_allreduce_equals_whole_batch_gradient():
         p.join(timeout=180)
     results = dict(q.get(timeout=10) for _ in range(world))
     assert results == {0: True, 1: True}
+
+
+def _loss_grad_worker(rank, world, port, q):
+    """A data-parallel step from the masked-LM loss: each rank encodes its share, takes the
+    loss backward with the global scored count (all-reduced first), backpropagates through
+    the encoder, and the gradients are summed.  Every rank compares with the gradient of the
+    whole batch's mean loss (float64 oracle); the shares have different scored counts."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from oracle import backward as B
+        from oracle import esm_oracle as O
+        lengths = [9, 4, 7, 1, 12]
+        tokens = synth.tokens_for_lengths(np.random.default_rng(7), lengths).astype(np.int64)
+        w = synth.model_weights(SMALL, 7, "fp32", ln_random=True)
+        head = synth.lm_head_weights(SMALL, 7, "fp32", w["emb"])
+        targets = synth.mlm_targets(tokens, 7, rate=0.4).astype(np.int64)
+        cu = O.cu_seqlens(lengths)
+        mine = sharding.shard_by_work(lengths, world, SMALL.hidden, SMALL.ffn)[rank]
+        toks, lens = sharding.local_batch(tokens, lengths, mine)
+        t_mine = np.concatenate([targets[cu[i]:cu[i + 1]] for i in mine])
+        n_global = int(sharding.global_scored_count(torch.from_numpy(t_mine)).item())
+        counts = [None] * world
+        dist.all_gather_object(counts, int((t_mine != -100).sum()))
+
+        def step(tk, cuv, tg, count):
+            hid = O.encode_packed(tk, cuv, w, SMALL.heads)
+            hid = np.concatenate([hid[i] for i in range(len(cuv) - 1)])
+            rh = B.lm_head_backward(hid, head, tg, count=count)
+            ge = B.encode_packed_backward(tk, cuv, w, SMALL.heads, rh["hidden"])
+            flat = [ge["emb"] + rh["emb"]] + [rh[k] for k in ("dense_w", "dense_b", "ln_g", "ln_b", "bias")]
+            return flat + [l[n] for l in ge["layers"] for n in B.PARAM_NAMES] + [ge["lnf_g"], ge["lnf_b"]]
+
+        part = step(toks.astype(np.int64), O.cu_seqlens(lens), t_mine, n_global)
+        tens = [torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)) for a in part]
+        sharding.allreduce_gradients(tens, bucket_bytes=4096)
+        full = step(tokens, cu, targets, None)
+        err = max(float(np.abs(t.numpy() - f).max() / (np.abs(f).max() + 1e-300)) for t, f in zip(tens, full))
+        ok = err < 1e-12 and n_global == int((targets != -100).sum()) and counts[0] != counts[1]
+        q.put((rank, ok))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_gloo_training_step_from_the_loss_equals_whole_batch_gradient():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_loss_grad_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+    results = dict(q.get(timeout=10) for _ in range(world))
+    assert results == {0: True, 1: True}

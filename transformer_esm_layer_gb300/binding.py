@@ -117,7 +117,7 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_set_fp8_state": (i32, [vp, ctypes.POINTER(ctypes.c_float), sz]),
         "esm_encoder_set_profiling": (i32, [vp, i32]),
         "esm_encoder_get_profile": (i32, [vp, ctypes.POINTER(EsmProfile), i32]),
-        "esm_op_attention_noalloc": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+        "esm_op_attention_noalloc": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "esm_op_layernorm_e4m3": (i32, [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp]),
         "esm_encoder_debug_wait_timeout": (i32, [vp, i32, vp]),
         "esm_op_gemm_fp8": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
@@ -137,7 +137,7 @@ def load_library() -> ctypes.CDLL:
         "esm_op_attention_backward": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp]),
         "esm_encoder_lm_head_backward_workspace_size": (i32, [vp, i32, ctypes.POINTER(sz)]),
         "esm_encoder_lm_head_backward": (i32, [vp, ctypes.POINTER(EsmLmHead), vp, i32, vp, vp,
-                                               ctypes.POINTER(EsmLmHeadGrads), vp, vp, vp, sz, vp]),
+                                               ctypes.POINTER(EsmLmHeadGrads), vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -508,10 +508,11 @@ class EsmEncoder:
         return dqkv
 
     def lm_head_backward(self, head: "DeviceLmHead", hidden, targets, d_hidden=None, grads=None, loss_sum=None,
-                         count=None, workspace=None, stream=None):
+                         count=None, workspace=None, stream=None, loss_count=None):
         """esm_encoder_lm_head_backward: dL/d(hidden) (float32 [T, hidden]) and the head's
         gradients (dict of float32 device tensors shaped like the head's parameters) of the
-        mean masked-LM loss."""
+        mean masked-LM loss.  ``loss_count`` (device int32 scalar): the scored-token count the
+        mean divides by, e.g. the global batch's in data-parallel training (None: this call's)."""
         import torch
         T = hidden.shape[0]
         dev = hidden.device
@@ -527,8 +528,8 @@ class EsmEncoder:
         gs = EsmLmHeadGrads(*[grads[k].data_ptr() for k in LM_HEAD_NAMES])
         self._raise(self.lib.esm_encoder_lm_head_backward(self.handle, ctypes.byref(head.struct), _ptr(hidden), T,
                                                           _ptr(targets), _ptr(d_hidden), ctypes.byref(gs),
-                                                          _ptr(loss_sum), _ptr(count), _ptr(workspace),
-                                                          workspace.numel(), _stream_ptr(stream)),
+                                                          _ptr(loss_sum), _ptr(count), _ptr(loss_count),
+                                                          _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
                     "esm_encoder_lm_head_backward")
         return d_hidden, grads
 
@@ -568,12 +569,36 @@ class EsmEncoder:
         return buf[self.num_layers * 8:].reshape(self.num_layers, 8, self.amax_history_len)
 
 
-def op_attention_noalloc(qkv, cu_seqlens, max_seqlen: int, hidden: int, heads: int, o, stream=None) -> int:
+def op_attention_noalloc(qkv, cu_seqlens, max_seqlen: int, hidden: int, heads: int, o, status=None,
+                         stream=None) -> int:
     """esm_op_attention_noalloc: attention with no handle, no workspace and no allocation.
-    Returns the status code."""
+
+    qkv: contiguous CUDA bf16 [T, 3*hidden]; o: contiguous CUDA bf16 [T, hidden];
+    cu_seqlens: contiguous int32 [B + 1] on the same device; status: optional int32 device
+    tensor of one element that receives the call's device-side outcome (ESM_OK,
+    ESM_ERR_BAD_CU_SEQLENS or ESM_ERR_TIMEOUT).  Raises ValueError on tensors the C side
+    cannot check (wrong dtype, device, layout or shape); returns the call's status code."""
+    import torch
+
+    def need(ok, what):
+        if not ok:
+            raise ValueError(f"op_attention_noalloc: {what}")
+
+    for name, t in (("qkv", qkv), ("o", o), ("cu_seqlens", cu_seqlens)):
+        need(isinstance(t, torch.Tensor) and t.is_cuda, f"{name} must be a CUDA tensor")
+        need(t.is_contiguous(), f"{name} must be contiguous")
+        need(t.device == qkv.device, f"{name} must be on {qkv.device}")
+    need(qkv.dtype == torch.bfloat16 and o.dtype == torch.bfloat16, "qkv and o must be bfloat16")
+    need(cu_seqlens.dtype == torch.int32 and cu_seqlens.dim() == 1 and cu_seqlens.numel() >= 2,
+         "cu_seqlens must be a 1-D int32 tensor of at least two offsets")
+    need(qkv.dim() == 2 and qkv.shape[1] == 3 * hidden, f"qkv must be [T, {3 * hidden}]")
+    need(o.dim() == 2 and tuple(o.shape) == (qkv.shape[0], hidden), f"o must be [{qkv.shape[0]}, {hidden}]")
+    if status is not None:
+        need(isinstance(status, torch.Tensor) and status.device == qkv.device and status.dtype == torch.int32
+             and status.numel() >= 1, "status must be an int32 tensor on the device of qkv")
     lib = load_library()
     return lib.esm_op_attention_noalloc(_ptr(qkv), _ptr(cu_seqlens), cu_seqlens.numel() - 1, qkv.shape[0],
-                                        int(max_seqlen), hidden, heads, _ptr(o), _stream_ptr(stream))
+                                        int(max_seqlen), hidden, heads, _ptr(o), _ptr(status), _stream_ptr(stream))
 
 
 def packed_inputs(tokens: np.ndarray, lengths: Sequence[int], device="cuda"):

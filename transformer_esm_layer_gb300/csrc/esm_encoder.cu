@@ -683,6 +683,18 @@ esm_status backward_impl(esm_encoder* h, const esm_weights* w, const float* d_ou
 
 }  // namespace
 
+bool esm::encode_attention_qkv_map(const void* qkv, int total_tokens, int hidden, CUtensorMap* out) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !qkv || !out || total_tokens <= 0 || hidden <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)3 * hidden, (cuuint64_t)total_tokens};
+  cuuint64_t strides[1] = {(cuuint64_t)3 * hidden * 2};
+  cuuint32_t box[2] = {64u, 128u};
+  cuuint32_t es[2] = {1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 extern "C" {
 
 const char* esm_status_string(esm_status s) {
@@ -886,8 +898,9 @@ esm_status esm_encoder_lm_head_backward_workspace_size(const esm_encoder_t* h, i
 
 esm_status esm_encoder_lm_head_backward(esm_encoder_t* h, const esm_lm_head* head, const void* hidden,
                                         int total_tokens, const int32_t* targets, float* d_hidden,
-                                        const esm_lm_head_grads* grads, float* loss_sum, int* count, void* workspace,
-                                        size_t workspace_bytes, esm_stream_t stream) {
+                                        const esm_lm_head_grads* grads, float* loss_sum, int* count,
+                                        const int* loss_count, void* workspace, size_t workspace_bytes,
+                                        esm_stream_t stream) {
   if (!h || !head || !grads || total_tokens <= 0 || !hidden || !d_hidden) return ESM_ERR_INVALID_ARG;
   if (h->cfg.precision != ESM_BF16) return ESM_ERR_UNSUPPORTED;
   const void* p[6] = {head->dense_w, head->dense_b, head->ln_g, head->ln_b, head->emb, head->bias};
@@ -926,8 +939,10 @@ esm_status esm_encoder_lm_head_backward(esm_encoder_t* h, const esm_lm_head* hea
     return ESM_ERR_CUDA;
   if (loss_sum && cudaMemcpyAsync(loss_sum, lsum, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return ESM_ERR_CUDA;
   if (count && cudaMemcpyAsync(count, cnt, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return ESM_ERR_CUDA;
-  // backward of the mean masked cross-entropy
-  if (launch_lm_backward_head(logits, targets, cnt, head->emb, z, T, d, V, dl, dz, grads->emb, grads->bias, partial,
+  // backward of the mean masked cross-entropy (over this call's scored tokens, or over the
+  // caller's global count)
+  if (loss_count && !aligned(loss_count, 4)) return ESM_ERR_INVALID_ARG;
+  if (launch_lm_backward_head(logits, targets, loss_count ? loss_count : cnt, head->emb, z, T, d, V, dl, dz, grads->emb, grads->bias, partial,
                               h->num_sms, st) != cudaSuccess)
     return ESM_ERR_CUDA;
   launch_ln_bwd_bf16in(u, head->ln_g, false, dz, du, grads->ln_g, grads->ln_b, partial, T, d, h->cfg.ln_eps, st);

@@ -123,17 +123,15 @@ void launch_rope_f32(float* qkv, int T, int d, int head_dim, const int32_t* pos_
                      int max_pos, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention.cu
-// qkv [T, 3*d] head-major, o [T, d].  Work items come from the pack buffers.
-void launch_attention_bf16(const __nv_bfloat16* qkv, __nv_bfloat16* o, int d, int heads, int max_items,
-                           const PackBuffers& pb, cudaStream_t st);
-void launch_attention_bf16_to_e4m3(const __nv_bfloat16* qkv, uint8_t* o, int d, int heads, int max_items,
-                                   const PackBuffers& pb, const float* q_scale, float* amax, cudaStream_t st);
 // tcgen05 attention (head_dim 64): tm_qkv is a tensor map over qkv [T, 3d] bf16 with a
 // 64 x 128 box and the 128-byte swizzle; work items in tiles of kAttnQTileTc rows.
 int attention_tc_smem_bytes();
 // lse (optional, fp32 [heads, lse_stride], head-major): the natural-log softmax normaliser of
 // every query row (scores scaled by 1/sqrt(head_dim)), kept by the training forward for the
 // backward; lse_stride >= T.
+// The tensor map launch_attention_tc expects over qkv [T, 3d] bf16, encoded on the host
+// (no allocation); false if the driver's encoder is unavailable or rejects the layout.
+bool encode_attention_qkv_map(const void* qkv, int total_tokens, int hidden, CUtensorMap* out);
 cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int d, int heads, int max_items,
                                 const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
                                 cudaStream_t st, float* lse = nullptr, int lse_stride = 0);

@@ -11,6 +11,13 @@ Training adds one exchange: the parameters are shared by every sequence and the 
 a packed batch is the sum of its sequences' gradients, so ranks that each backpropagated
 their own share hold partial sums, and one all-reduce (sum) of the gradients gives every
 rank the batch gradient (data parallelism of the hotelren.com guide's training loop).
+
+The masked-LM loss is a mean over the scored tokens of the whole batch, so its normaliser
+is global: a data-parallel step first sums the ranks' scored counts (``global_scored_count``)
+and passes that count to the loss backward (``EsmEncoder.lm_head_backward(...,
+loss_count=...)``); each rank then differentiates its share of the same loss, and the
+all-reduce of the gradients gives the batch gradient.  With each rank's own count instead,
+the sum would be the sum of the ranks' means, wrong by about the world size.
 """
 from __future__ import annotations
 
@@ -85,3 +92,16 @@ def allreduce_gradients(tensors: Sequence, group=None, bucket_bytes: int = 256 <
         size += nbytes
     flush(bucket)
     return total
+
+
+def global_scored_count(targets, group=None, ignore_index: int = -100):
+    """Number of scored masked-LM targets over all ranks (an all-reduce sum of each rank's
+    count): the normaliser of the batch's mean loss.  ``targets`` is this rank's int tensor
+    (any device the process group serves); returns an int32 tensor of one element on the
+    same device, ready to pass as ``loss_count``."""
+    import torch
+    import torch.distributed as dist
+
+    n = (targets != ignore_index).sum().to(torch.int64).reshape(1)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM, group=group)
+    return n.to(torch.int32)
