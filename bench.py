@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-train", action="store_true", help="skip the training-step measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configured workloads (tiny fp32, one "
+                                                               "650M layer, padded 650M, 3B FP8)")
     ap.add_argument("--no-graph", action="store_true", help="launch the kernels eagerly instead of replaying "
                                                              "one captured CUDA graph per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
@@ -77,11 +79,13 @@ def workload_for_rank(rank: int, tokens=None, layers=None, name: str = "esm650m"
 
 def workload_text(wl) -> str:
     g = wl.geometry
-    size = "3B" if g.hidden == 2560 else "650M"
-    txt = (f"{wl.name}: ESM-2 {size} encoder ({g.num_layers} layers, hidden {g.hidden}, {g.heads} heads, FFN {g.ffn}, "
-           f"vocab 33), {'E4M3 GEMMs with per-tensor delayed scaling (history 16)' if wl.precision == 'fp8' else 'bf16'}"
-           f", weights N(0,0.02), {wl.total_tokens} tokens in {len(wl.lengths)} sequences, log-normal lengths "
-           f"(median 300, sigma 0.6) clipped to [32,1024], seed {wl.seed}")
+    size = {2560: "ESM-2 3B", 1280: "ESM-2 650M"}.get(g.hidden, "tiny ESM-style")
+    prec = {"fp8": "E4M3 GEMMs with per-tensor delayed scaling (history 16)", "fp32": "fp32"}.get(wl.precision, "bf16")
+    lengths = (f"lengths {list(wl.lengths)}" if len(wl.lengths) <= 4 else
+               "log-normal lengths (median 300, sigma 0.6) clipped to [32,1024]")
+    txt = (f"{wl.name}: {size} encoder ({g.num_layers} layers, hidden {g.hidden}, {g.heads} heads, FFN {g.ffn}, "
+           f"vocab 33), {prec}, weights N(0,0.02), {wl.total_tokens} tokens in {len(wl.lengths)} sequences, "
+           f"{lengths}, seed {wl.seed}" + ("" if wl.final_ln else ", no final LayerNorm"))
     if wl.padded_len:
         txt += f"; padded layout [{len(wl.lengths)}, {wl.padded_len}] with a key padding mask"
     else:
@@ -249,13 +253,205 @@ def run_reference(args):
     return 0
 
 
+def _timed_replays(step, steps, stream):
+    """Time `steps` calls of step() with one CUDA event between consecutive calls (on the
+    launching stream): returns the per-step durations in ms and their sum."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return per, ev[0].elapsed_time(ev[-1])
+
+
+def attention_roofline(wl, ms_per_step, executed_flops, pk, clock_mhz, num_sms):
+    """The attention kernel against its three ceilings: tensor (bf16 MMA FLOPs), the
+    exponential unit (one 2^x per score; 32 results per SM per clock, the ex2.approx.f32
+    rate measured on GB300 with a throughput probe) and HBM (Q, K, V read once and O
+    written once)."""
+    g = wl.geometry
+    L2 = float(np.sum(np.asarray(wl.lengths, np.float64) ** 2))
+    T = wl.total_tokens
+    exps = L2 * g.heads * g.num_layers
+    bytes_ = T * 4.0 * g.hidden * 2 * g.num_layers
+    sec = ms_per_step / 1e3
+    clock = clock_mhz if clock_mhz else float(pk.get("sm_max_mhz", 2070.0))
+    exp_peak = 32.0 * num_sms * clock * 1e6
+    return {"kernel": "attention_tc_kernel (tcgen05, bf16)", "ms_per_step": ms_per_step,
+            "tensor": {"achieved_tflops": executed_flops / sec / 1e12, "peak": float(pk["bf16_tflops"]),
+                       "frac": executed_flops / sec / 1e12 / float(pk["bf16_tflops"]),
+                       "flops_per_step": executed_flops, "peak_source": "bf16_tflops (burst), measured"},
+            "exp_unit": {"achieved_per_s": exps / sec, "peak_per_s": exp_peak, "frac": exps / sec / exp_peak,
+                         "exps_per_step": exps,
+                         "peak_source": f"32 per SM per clock (measured ex2.approx.f32 rate) x {num_sms} SMs x "
+                                        f"{clock:.0f} MHz (sampled median)"},
+            "hbm": {"achieved_gbs": bytes_ / sec / 1e9, "peak": float(pk["hbm_gbs"]),
+                    "frac": bytes_ / sec / 1e9 / float(pk["hbm_gbs"]), "bytes_per_step": bytes_}}
+
+
+def measure_forward(wl, dev, args, w_np=None, want_e2e=False, world=1, rank=0, global_tokens=None,
+                    tok_np=None, clock_sampler=None):
+    """One workload's forward: warm-up, CUDA-graph capture, `args.steps` timed replays with an
+    event between replays (median / min / mean), then an eager pass with the library's
+    per-kernel event profile.  Returns (result dict, state for the headline's extra legs)."""
+    import torch
+    import torch.distributed as dist
+
+    from transformer_esm_layer_gb300 import synth
+    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
+
+    g = wl.geometry
+    prec = wl.precision
+    padded = wl.padded_len is not None
+    if w_np is None:
+        w_np = synth.model_weights(g, wl.seed, prec)
+    dw = DeviceWeights(w_np, prec, device=dev)
+    if tok_np is None:
+        tok_np = synth.workload_tokens(wl)
+    global_tokens = wl.total_tokens if global_tokens is None else global_tokens
+    tok, cu = packed_inputs(tok_np, wl.lengths, device=dev)
+    T, B, maxL = wl.total_tokens, len(wl.lengths), max(wl.lengths)
+    enc = EsmEncoder.from_geometry(g, prec, final_ln=wl.final_ln)
+    stream = torch.cuda.current_stream()
+    torch.cuda.reset_peak_memory_stats(dev)
+    if padded:
+        S = wl.padded_len
+        tok_pad = torch.from_numpy(synth.pad_tokens(tok_np, wl.lengths, S)).to(dev)
+        lens_dev = torch.tensor(wl.lengths, dtype=torch.int32, device=dev)
+        ws = enc.workspace(B * S, B, dev)
+        out = torch.empty(B, S, g.hidden, dtype=enc.out_dtype, device=dev)
+
+        def eager_step(st=stream):
+            enc.forward_padded(dw, tok_pad, lens_dev, out=out, workspace=ws, stream=st)
+    else:
+        ws = enc.workspace(T, B, dev)
+        out = torch.empty(T, g.hidden, dtype=enc.out_dtype, device=dev)
+
+        def eager_step(st=stream):
+            enc.forward(dw, tok, cu, maxL, out=out, workspace=ws, stream=st)
+
+    # FP8 delayed scaling needs a full amax history before timing
+    for _ in range(max(args.warmup, 3, 16 if prec == "fp8" else 0)):
+        eager_step()
+    enc.check(stream)
+    step = eager_step
+    launches_per_step = None
+    if not args.no_graph:
+        # one step = one replay of the captured forward (all of its kernels, same work)
+        graph = torch.cuda.CUDAGraph()
+        enc.get_profile(reset=True)
+        with torch.cuda.graph(graph):
+            eager_step(None)  # None: the capturing stream torch makes current
+        launches_per_step = enc.get_profile(reset=True)["total_launches"]
+        graph.replay()
+        torch.cuda.synchronize()
+        enc.check(stream)
+
+        def step():
+            graph.replay()
+
+    # ---------------------------------------------------------------- timed region
+    enc.get_profile(reset=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = clock_sampler() if clock_sampler else None
+    if sampler:
+        time.sleep(0.4)
+    per, total_ms = _timed_replays(step, args.steps, stream)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    launches = enc.get_profile(reset=True)["total_launches"]
+    if launches_per_step is not None:  # graph replays do not pass through the library
+        launches = launches_per_step * args.steps
+    enc.check(stream)
+    ms = total_ms
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+
+    # ---------------------------------------------------------------- per-kernel device times
+    enc.set_profiling(True)
+    prof_steps = min(args.steps, 10)
+    for _ in range(prof_steps):
+        eager_step()
+    prof = enc.get_profile(reset=True)
+    enc.set_profiling(False)
+    flops = algorithmic_flops(wl)
+    total_flops = sum(flops.values())
+    executed = dict(flops)
+    if padded:  # the GEMMs run over all B*S rows, attention over every query row of each row
+        rows = B * wl.padded_len
+        for c_ in ("gemm_qkv", "gemm_oproj", "gemm_fc1", "gemm_fc2"):
+            executed[c_] = flops[c_] * rows / T
+        executed["attention"] = 4.0 * g.hidden * wl.padded_len * float(np.sum(wl.lengths)) * g.num_layers
+    pk, pk_src = peaks()
+    gemm_classes = ("gemm_qkv", "gemm_oproj", "gemm_fc1", "gemm_fc2")
+    per_kernel = {c_: {"ms_per_step": prof[c_]["ms"] / prof_steps,
+                       "launches_per_step": prof[c_]["launches"] / prof_steps}
+                  for c_ in ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other")}
+    for c_ in list(gemm_classes) + ["attention"]:
+        m_ = per_kernel[c_]["ms_per_step"]
+        per_kernel[c_]["tflops"] = executed[c_] / (m_ / 1e3) / 1e12 if m_ else None
+    # a contraction takes the peak of its own dtype: E4M3 = 2 x the measured bf16 (nominal 4.5 / 2.25)
+    dtype_mult = 2.0 if prec == "fp8" else 1.0
+    peak_burst = float(pk["bf16_tflops"]) * dtype_mult
+    peak_sust = float(pk["bf16_tflops_sustained"]) * dtype_mult
+    roofline = None
+    attn = None
+    if prec != "fp32":
+        gemm_ms = sum(prof[c_]["ms"] for c_ in gemm_classes) / prof_steps
+        gemm_launches = sum(prof[c_]["launches"] for c_ in gemm_classes) / prof_steps
+        gemm_flops = sum(executed[c_] for c_ in gemm_classes)
+        gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12
+        traffic = gemm_traffic_record()
+        roofline = {"bound": "tensor", "kernel": f"gemm_tc_kernel (tcgen05 {'e4m3' if prec == 'fp8' else 'bf16'}, "
+                                                  "all four linear maps)",
+                    "achieved": gemm_tflops, "peak": peak_burst, "unit": "TFLOP/s", "frac": gemm_tflops / peak_burst,
+                    "peak_source": f"bf16_tflops (burst), {pk_src}" + (" x 2 (E4M3/bf16 nominal ratio)" if prec == "fp8" else ""),
+                    "peak_sustained": peak_sust, "frac_vs_sustained": gemm_tflops / peak_sust,
+                    "flops_per_launch": gemm_flops / gemm_launches if gemm_launches else None,
+                    "avg_launch_ms": gemm_ms / gemm_launches if gemm_launches else None,
+                    "traffic": traffic.get("dram_bytes_per_launch") if (traffic and wl.name == "esm650m"
+                                                                        and args.layers is None
+                                                                        and args.tokens is None) else None,
+                    "traffic_source": traffic.get("source") if traffic else None}
+        clock = clocks.get("sm_mhz") if clocks else None
+        attn = attention_roofline(wl, per_kernel["attention"]["ms_per_step"], executed["attention"], pk, clock,
+                                  torch.cuda.get_device_properties(dev).multi_processor_count)
+    srt = sorted(per)
+    res = {"workload": workload_text(wl), "tokens_per_s": global_tokens / (ms_step / 1e3),
+           "tokens_per_s_median_step": global_tokens / (statistics.median(per) / 1e3),
+           "ms_per_step": ms_step, "ms_per_step_median": statistics.median(per), "ms_per_step_min": srt[0],
+           "steps": args.steps, "tflops": total_flops * (global_tokens / T) / (ms_step / 1e3) / 1e12,
+           "mfu_vs_burst_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_burst,
+           "mfu_vs_sustained_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_sust,
+           "peak_dtype": "e4m3 (2 x measured bf16)" if prec == "fp8" else "bf16 (measured)",
+           "algorithmic_gflop_per_step_per_gpu": total_flops / 1e9,
+           "padded_over_packed_flops": (sum(executed.values()) / total_flops) if padded else None,
+           "max_memory_allocated_gb": peak_mem / 2**30, "roofline": roofline, "attention_roofline": attn,
+           "per_kernel": per_kernel, "launches_per_step": launches_per_step, "gpu_launches": launches,
+           "clocks": clocks, "dtype": {"fp8": "e4m3", "fp32": "f32"}.get(prec, "bf16"),
+           "timing": "CUDA graph replay of the whole forward" if not args.no_graph else "eager launches"}
+    state = {"enc": enc, "dw": dw, "tok": tok, "cu": cu, "ws": ws, "out": out, "w_np": w_np, "tok_np": tok_np,
+             "T": T, "B": B, "maxL": maxL, "stream": stream, "flops": flops, "total_flops": total_flops,
+             "gemm_classes": gemm_classes}
+    return res, state
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     from transformer_esm_layer_gb300 import build as _build
     from transformer_esm_layer_gb300 import synth
-    from transformer_esm_layer_gb300.binding import DeviceWeights, EsmEncoder, packed_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -272,8 +468,6 @@ def run_ours(args):
     g = wl.geometry
     prec = wl.precision
     padded = wl.padded_len is not None
-    w_np = synth.model_weights(g, wl.seed, prec)
-    dw = DeviceWeights(w_np, prec, device=dev)
     tok_np = synth.workload_tokens(wl)
     global_tokens = wl.total_tokens
     if world > 1:
@@ -285,126 +479,28 @@ def run_ours(args):
         mine = sharding.shard_by_work(g_lengths, world, g.hidden, g.ffn)[rank]
         tok_np, wl.lengths = sharding.local_batch(g_tokens, g_lengths, mine)
         global_tokens = len(g_tokens)
-    tok, cu = packed_inputs(tok_np, wl.lengths, device=dev)
-    T, B, maxL = wl.total_tokens, len(wl.lengths), max(wl.lengths)
-    enc = EsmEncoder.from_geometry(g, prec, final_ln=True)
-    stream = torch.cuda.current_stream()
-    if padded:
-        S = wl.padded_len
-        tok_pad = torch.from_numpy(synth.pad_tokens(tok_np, wl.lengths, S)).to(dev)
-        lens_dev = torch.tensor(wl.lengths, dtype=torch.int32, device=dev)
-        ws = enc.workspace(B * S, B, dev)
-        out = torch.empty(B, S, g.hidden, dtype=torch.bfloat16, device=dev)
-
-        def step(st=stream):
-            enc.forward_padded(dw, tok_pad, lens_dev, out=out, workspace=ws, stream=st)
-    else:
-        ws = enc.workspace(T, B, dev)
-        out = torch.empty(T, g.hidden, dtype=torch.bfloat16, device=dev)
-
-        def step(st=stream):
-            enc.forward(dw, tok, cu, maxL, out=out, workspace=ws, stream=st)
-
-    # FP8 delayed scaling needs a full amax history before timing
-    for _ in range(max(args.warmup, 3, 16 if prec == "fp8" else 0)):
-        step()
-    enc.check(stream)
-    eager_step = step
-    launches_per_step = None
-    if not args.no_graph:
-        # one step = one replay of the captured forward (all of its kernels, same work)
-        graph = torch.cuda.CUDAGraph()
-        enc.get_profile(reset=True)
-        with torch.cuda.graph(graph):
-            eager_step(None)  # None: the capturing stream torch makes current
-        launches_per_step = enc.get_profile(reset=True)["total_launches"]
-        graph.replay()
-        torch.cuda.synchronize()
-        enc.check(stream)
-
-        def step(st=None):
-            graph.replay()
-
-    # ---------------------------------------------------------------- timed region
     gpu_id = None
     try:
         gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
         gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
     except Exception:
         gpu_id = None
-    enc.get_profile(reset=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(gpu_id)
-    time.sleep(0.4)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    launches = enc.get_profile(reset=True)["total_launches"]
-    if launches_per_step is not None:  # graph replays do not pass through the library
-        launches = launches_per_step * args.steps
-    enc.check(stream)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_step = ms / args.steps
-    value = global_tokens / (ms_step / 1e3)
 
-    # ---------------------------------------------------------------- per-kernel device times
-    enc.set_profiling(True)
-    prof_steps = min(args.steps, 10)
-    for _ in range(prof_steps):
-        eager_step()
-    prof = enc.get_profile(reset=True)
-    enc.set_profiling(False)
-    flops = algorithmic_flops(wl)
-    total_flops = sum(flops.values())
-    executed = dict(flops)
-    if padded:  # the GEMMs run over all B*S rows, attention over every query row of each row
-        rows = B * wl.padded_len
-        for c in ("gemm_qkv", "gemm_oproj", "gemm_fc1", "gemm_fc2"):
-            executed[c] = flops[c] * rows / T
-        executed["attention"] = 4.0 * g.hidden * wl.padded_len * float(np.sum(wl.lengths)) * g.num_layers
-    pk, pk_src = peaks()
-    gemm_classes = ("gemm_qkv", "gemm_oproj", "gemm_fc1", "gemm_fc2")
-    gemm_ms = sum(prof[c]["ms"] for c in gemm_classes) / prof_steps
-    gemm_launches = sum(prof[c]["launches"] for c in gemm_classes) / prof_steps
-    gemm_flops = sum(executed[c] for c in gemm_classes)
-    gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12
-    # a contraction takes the peak of its own dtype: E4M3 = 2 x the measured bf16 (nominal 4.5 / 2.25)
-    dtype_mult = 2.0 if prec == "fp8" else 1.0
-    peak_sust = float(pk["bf16_tflops_sustained"]) * dtype_mult
-    peak_burst = float(pk["bf16_tflops"]) * dtype_mult
-    per_kernel = {c: {"ms_per_step": prof[c]["ms"] / prof_steps, "launches_per_step": prof[c]["launches"] / prof_steps}
-                  for c in ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other")}
-    for c in list(gemm_classes) + ["attention"]:
-        per_kernel[c]["tflops"] = executed[c] / (per_kernel[c]["ms_per_step"] / 1e3) / 1e12 if per_kernel[c]["ms_per_step"] else None
-    traffic = gemm_traffic_record()
-    roofline = {"bound": "tensor", "kernel": f"gemm_tc_kernel (tcgen05 {'e4m3' if prec == 'fp8' else 'bf16'}, "
-                                              "all four linear maps)",
-                "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s", "frac": gemm_tflops / peak_sust,
-                "peak_source": f"bf16_tflops_sustained, {pk_src}" + (" x 2 (E4M3/bf16 nominal ratio)" if prec == "fp8" else ""),
-                "flops_per_launch": gemm_flops / gemm_launches if gemm_launches else None,
-                "avg_launch_ms": gemm_ms / gemm_launches if gemm_launches else None,
-                "traffic": traffic.get("dram_bytes_per_launch") if (traffic and args.workload == "esm650m") else None}
+    head, st = measure_forward(wl, dev, args, world=world, rank=rank, global_tokens=global_tokens, tok_np=tok_np,
+                               clock_sampler=lambda: ClockSampler(gpu_id))
+    enc, dw, tok, cu, ws, out = st["enc"], st["dw"], st["tok"], st["cu"], st["ws"], st["out"]
+    T, B, maxL, stream, w_np = st["T"], st["B"], st["maxL"], st["stream"], st["w_np"]
+    flops, total_flops, gemm_classes = st["flops"], st["total_flops"], st["gemm_classes"]
+    ms_step = head["ms_per_step"]
+    value = head["tokens_per_s"]
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
     if not padded:
         tok_h = torch.from_numpy(tok_np.astype(np.int32)).pin_memory()
         cu_h = torch.from_numpy(synth.cu_seqlens_from_lengths(wl.lengths)).pin_memory()
-        out_h = torch.empty(T, g.hidden, dtype=torch.bfloat16).pin_memory()
-        out_view = out_h.view(torch.int16).numpy()
+        out_h = torch.empty(T, g.hidden, dtype=enc.out_dtype).pin_memory()
+        out_view = out_h.view(torch.int16 if enc.out_dtype == torch.bfloat16 else torch.int32).numpy()
         tok_view, cu_view = tok_h.numpy(), cu_h.numpy()
         n_e2e = min(args.steps, 10)
         enc.forward_host(dw, tok_view, cu_view, maxL, out_view, ws, stream=stream)
@@ -419,34 +515,30 @@ def run_ours(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             dt = float(t.item())
         e2e = {"value": global_tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": 4 * T + 4 * (B + 1),
-               "d2h_bytes_per_step": 2 * T * g.hidden, "ms_per_step": dt * 1e3,
+               "d2h_bytes_per_step": out.element_size() * T * g.hidden, "ms_per_step": dt * 1e3,
                "call": "esm_encoder_forward_host (pinned host buffers in and out)"}
 
     # ---------------------------------------------------------------- masked-LM head (next step)
     mlm = None
     if not padded and prec == "bf16":
         from transformer_esm_layer_gb300.binding import DeviceLmHead
-        head = DeviceLmHead(synth.lm_head_weights(g, wl.seed, prec, w_np["emb"]), prec, device=dev)
+        lm = DeviceLmHead(synth.lm_head_weights(g, wl.seed, prec, w_np["emb"]), prec, device=dev)
         tg = torch.from_numpy(synth.mlm_targets(tok_np, wl.seed)).to(dev)
         hws = enc.lm_head_workspace(T, dev)
         lsum = torch.zeros(1, dtype=torch.float32, device=dev)
         cnt = torch.zeros(1, dtype=torch.int32, device=dev)
         logits = torch.empty(T, g.vocab, dtype=torch.float32, device=dev)
         for _ in range(3):
-            enc.lm_head(head, out, targets=tg, logits=logits, loss_sum=lsum, count=cnt, workspace=hws, stream=stream)
-        n_mlm = 10
-        m0 = torch.cuda.Event(enable_timing=True)
-        m1 = torch.cuda.Event(enable_timing=True)
-        m0.record(stream)
-        for _ in range(n_mlm):
-            enc.lm_head(head, out, targets=tg, logits=logits, loss_sum=lsum, count=cnt, workspace=hws, stream=stream)
-        m1.record(stream)
-        torch.cuda.synchronize()
+            enc.lm_head(lm, out, targets=tg, logits=logits, loss_sum=lsum, count=cnt, workspace=hws, stream=stream)
+        per, tot = _timed_replays(lambda: enc.lm_head(lm, out, targets=tg, logits=logits, loss_sum=lsum, count=cnt,
+                                                      workspace=hws, stream=stream), 10, stream)
         enc.check(stream)
-        mms = m0.elapsed_time(m1) / n_mlm
+        mms = tot / 10
         mlm = {"call": "esm_encoder_lm_head (dense+GELU, LayerNorm, logits vs tied embedding, masked CE)",
-               "ms_per_call": mms, "tokens_per_s": T / (mms / 1e3), "scored_tokens": int(cnt.item()),
+               "ms_per_call": mms, "ms_per_call_median": statistics.median(per), "tokens_per_s": T / (mms / 1e3),
+               "scored_tokens": int(cnt.item()),
                "mean_loss_random_weights": float(lsum.item()) / max(1, int(cnt.item()))}
+        del hws, logits
 
     # ---------------------------------------------------------------- training step (forward that keeps
     # its activations + backward: every parameter's gradient), same batch
@@ -484,8 +576,9 @@ def run_ours(args):
             ev[2 * i + 2].record(stream)
         torch.cuda.synchronize()
         enc.check(stream)
-        f_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n_tr)) / n_tr
-        b_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(n_tr)) / n_tr
+        f_all = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n_tr)]
+        b_all = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(n_tr)]
+        f_ms, b_ms = sum(f_all) / n_tr, sum(b_all) / n_tr
         enc.set_profiling(True)
         enc.get_profile(reset=True)
         train_fwd()
@@ -500,7 +593,8 @@ def run_ours(args):
         train = {"calls": "esm_encoder_forward_train + esm_encoder_backward (all parameter gradients, fp32)"
                           + (" + NCCL all-reduce (sum) of the gradients" if world > 1 else ""),
                  "gradient_allreduce_bytes_per_rank": allreduce_bytes if world > 1 else 0,
-                 "ms_per_step": f_ms + b_ms, "ms_forward_train": f_ms, "ms_backward": b_ms,
+                 "ms_per_step": f_ms + b_ms, "ms_per_step_min": min(f + b for f, b in zip(f_all, b_all)),
+                 "ms_forward_train": f_ms, "ms_backward": b_ms,
                  "tokens_per_s": global_tokens / ((f_ms + b_ms) / 1e3),
                  "backward_tflops": bwd_flops / (b_ms / 1e3) / 1e12,
                  "step_tflops": (total_flops + bwd_flops) / ((f_ms + b_ms) / 1e3) / 1e12,
@@ -532,6 +626,23 @@ def run_ours(args):
                "sample": f"{len(done)} whole sequence(s) of the workload (indices {done}, {toks} tokens) through all "
                          f"{g.num_layers} layers in float64 numpy, {dt:.1f} s"}
 
+    # ---------------------------------------------------------------- the other configured workloads
+    configs = None
+    if world == 1 and not args.no_configs and args.workload == "esm650m" and args.layers is None \
+            and args.tokens is None:
+        del st
+        configs = {}
+        for name in ("tiny_fp32", "layer650m", "esm650m_padded", "esm3b_fp8"):
+            try:  # a side measurement: a failure here must not cost the benchmark line
+                wl2 = synth.make_workload(name)
+                reuse = w_np if name == "esm650m_padded" else None  # same model and seed as the headline
+                r2, st2 = measure_forward(wl2, dev, args, w_np=reuse)
+                del st2
+                torch.cuda.empty_cache()
+                configs[name] = r2
+            except Exception as e:  # noqa: BLE001
+                configs[name] = {"error": f"{type(e).__name__}: {e}"}
+
     if world > 1:
         dist.barrier()
     if rank == 0:
@@ -541,9 +652,10 @@ def run_ours(args):
                   "esm3b_fp8": "ESM-2 3B packed FP8 fwd tokens/s on 1 GB300; achieved TFLOP/s vs dense FP8 peak"
                   }[args.workload]
         line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "e4m3" if prec == "fp8" else "bf16", "data": "synthetic",
-                "config": {"workload": workload_text(wl), "tokens_per_step_per_gpu": T, "sequences": B,
+                "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": head["ms_per_step_median"],
+                "ms_per_step_min": head["ms_per_step_min"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+                "config": {"workload": head["workload"], "tokens_per_step_per_gpu": T, "sequences": B,
                            "max_seqlen": maxL,
                            "l2": "no flush: inputs larger than L2 ("
                                  f"{sum(t.numel() * t.element_size() for l in dw.layers for t in l.values()) / 2**30:.2f} GB "
@@ -552,16 +664,14 @@ def run_ours(args):
                            "parallelism": "single GPU" if world == 1 else
                            f"{world} replicas, one global batch of {global_tokens} tokens split by work "
                            "(longest-first greedy), no collective on the data path"},
-                "tflops": total_flops * (global_tokens / T) / (ms_step / 1e3) / 1e12,
-                "mfu_vs_sustained_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_sust,
-                "mfu_vs_burst_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_burst,
-                "peak_dtype": "e4m3 (2 x measured bf16)" if prec == "fp8" else "bf16 (measured)",
-                "algorithmic_gflop_per_step_per_gpu": total_flops / 1e9,
-                "roofline": roofline, "per_kernel": per_kernel,
-                "padded_over_packed_flops": (sum(executed.values()) / total_flops) if padded else None, "cpu_baseline": cpu, "e2e": e2e,
-                "mlm_head": mlm, "train_step": train,
-                "clocks": clocks, "gpu_launches": launches,
-                "timing": "CUDA graph replay of the whole forward" if not args.no_graph else "eager launches",
+                "tflops": head["tflops"], "mfu_vs_burst_peak": head["mfu_vs_burst_peak"],
+                "mfu_vs_sustained_peak": head["mfu_vs_sustained_peak"], "peak_dtype": head["peak_dtype"],
+                "algorithmic_gflop_per_step_per_gpu": head["algorithmic_gflop_per_step_per_gpu"],
+                "max_memory_allocated_gb": head["max_memory_allocated_gb"],
+                "roofline": head["roofline"], "attention_roofline": head["attention_roofline"],
+                "per_kernel": head["per_kernel"], "padded_over_packed_flops": head["padded_over_packed_flops"],
+                "cpu_baseline": cpu, "e2e": e2e, "mlm_head": mlm, "train_step": train, "configs": configs,
+                "clocks": head["clocks"], "gpu_launches": head["gpu_launches"], "timing": head["timing"],
                 "context": "pages' own figure: 59.2% model-FLOP utilisation, ESM-2 650M training, batch 46, A100"}
         print(json.dumps(line), flush=True)
     if world > 1:
