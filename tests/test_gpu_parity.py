@@ -210,7 +210,8 @@ def test_gemm_fp32_simt():
 
 
 # --------------------------------------------------------------------------- attention
-@pytest.mark.parametrize("lengths", [[1, 2, 63, 64, 65, 127, 128, 129, 200], [1024, 7, 333], [1]])
+@pytest.mark.parametrize("lengths", [[1, 2, 63, 64, 65, 127, 128, 129, 200], [1024, 7, 333], [1],
+                                     [256, 257, 383, 384, 385, 3, 512, 640]])
 def test_attention_bf16(lengths):
     g = SMALL
     enc = _enc(g, "bf16")

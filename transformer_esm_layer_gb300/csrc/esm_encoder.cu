@@ -53,7 +53,8 @@ struct MapKeyHash {
 };
 
 struct WsLayout {
-  size_t pos, seg, seg_start, seg_qlen, seg_klen, work, work_count, x, y, qkv, o, u, wq, stage_tok, stage_cu, total;
+  size_t pos, seg, seg_start, seg_qlen, seg_klen, work, work_count, x, y, qkv, o, u, wq, ln_stats, ln_fold, stage_tok,
+      stage_cu, total;
   int max_items;
 };
 
@@ -140,6 +141,10 @@ struct esm_encoder {
     L.o = take(act_bytes() * T * d);
     L.u = take(act_bytes() * T * f);
     L.wq = cfg.precision == ESM_FP8_E4M3 ? take(3 * d * d + d * d + 2 * d * f) : take(0);
+    // folded LayerNorm (bf16 forward): row statistics per 64-column group, and per layer the
+    // QKV and fc1 constants c and b' (fp32 [3d] + [3d] + [f] + [f])
+    L.ln_stats = cfg.precision == ESM_BF16 ? take(8 * T * (d / 64)) : take(0);
+    L.ln_fold = cfg.precision == ESM_BF16 ? take(4 * (6 * d + 2 * f) * (size_t)cfg.num_layers) : take(0);
     L.stage_tok = take(4 * T);
     L.stage_cu = take(4 * (B + 1));
     L.total = off;
@@ -250,14 +255,35 @@ bool weights_ok(const esm_encoder* h, const esm_weights* w) {
   return true;
 }
 
+// The folded-LayerNorm side of a GEMM launch (see EpiArgs).
+struct LnFoldArgs {
+  float2* stats_out = nullptr;
+  const void* gamma = nullptr;
+  void* a_out = nullptr;
+  const float2* stats_in = nullptr;
+  const float* c = nullptr;
+  const float* b = nullptr;
+};
+
 // One GEMM of a layer.  A: activation [M, K]; B: weight [N, K].
 // rope_cols >= 0 overrides the RoPE column range of ESM_EPI_QKV_ROPE (0: plain bias, bf16
-// out); res_in != NULL makes ESM_EPI_RESIDUAL read its residual there instead of from out.
+// out); res_in != NULL makes ESM_EPI_RESIDUAL read its residual there instead of from out;
+// ln != NULL adds the folded-LayerNorm outputs (residual) or inputs (QKV / GELU).
 esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, const void* B, const void* bias, void* out,
                     const int32_t* pos_id, int M, int N, int K, bool fp8, Act out_act, const float* a_scale,
                     const float* b_scale, const float* o_scale, float* o_amax, cudaStream_t st, int rope_cols = -1,
-                    const void* res_in = nullptr, void* aux = nullptr) {
+                    const void* res_in = nullptr, void* aux = nullptr, const LnFoldArgs* ln = nullptr) {
   EpiArgs ea{};
+  if (ln != nullptr) {
+    ea.ln_stats_out = ln->stats_out;
+    ea.ln_gamma = ln->gamma;
+    ea.ln_a_out = ln->a_out;
+    ea.ln_stats_in = ln->stats_in;
+    ea.ln_c = ln->c;
+    ea.ln_b = ln->b;
+    ea.ln_groups = K / 64;
+    ea.ln_eps = h->cfg.ln_eps;
+  }
   ea.bias = bias;
   ea.bias_f32 = !h->bf16_params();
   ea.out = out;
@@ -305,6 +331,30 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
   const bool pf32 = !h->bf16_params();
   const Act act = h->act();
   esm_status s;
+  // bf16 forward: every LayerNorm but the first and the final one is folded into the GEMMs
+  // around it.  The residual epilogue of the out-projection (fc2) leaves the row statistics
+  // and bf16(x * gamma2) (bf16(x * gamma1) of the next layer); fc1 (the next QKV projection)
+  // applies rstd (acc - mean c) + b' with the per-layer constants computed here.
+  const bool fold = c.precision == ESM_BF16 && d <= 4096;
+  float2* ln_stats = reinterpret_cast<float2*>(b + L.ln_stats);
+  float* ln_fold = reinterpret_cast<float*>(b + L.ln_fold);
+  auto fold_c = [&](int l, int which) -> float* {  // which: 0 c_qkv, 1 b'_qkv, 2 c_1, 3 b'_1
+    float* base = ln_fold + (size_t)l * (6 * d + 2 * f);
+    return which < 2 ? base + (size_t)which * 3 * d : base + 6 * (size_t)d + (size_t)(which - 2) * f;
+  };
+  if (fold) {
+    ProfScope _ps(h, P_OTHER, st, (2 * c.num_layers + kLnFoldMaxJobs - 1) / kLnFoldMaxJobs);
+    LnFoldJob jobs[kLnFoldMaxJobs];
+    int n = 0;
+    for (int l = 0; l < c.num_layers; ++l) {
+      jobs[n++] = LnFoldJob{w->w_qkv[l], w->ln1_g[l], w->ln1_b[l], w->b_qkv[l], fold_c(l, 0), fold_c(l, 1), 3 * d};
+      jobs[n++] = LnFoldJob{w->w_1[l], w->ln2_g[l], w->ln2_b[l], w->b_1[l], fold_c(l, 2), fold_c(l, 3), f};
+      if (n + 2 > kLnFoldMaxJobs || l + 1 == c.num_layers) {
+        launch_ln_fold(jobs, n, d, st);
+        n = 0;
+      }
+    }
+  }
   for (int l = 0; l < c.num_layers; ++l) {
     const bool fp8 = c.precision == ESM_FP8_E4M3 && h->layer_fp8[l];
     float* sc = h->fp8_scale() + (size_t)l * kNumFp8Tensors;
@@ -322,11 +372,19 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
       launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(w->w_2[l]), wq_2, (size_t)d * f, sc + W_2, am + W_2, st);
     }
     // ---- attention block
-    PROF(h, P_LN, st, 1,
-         launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_QKV,
-                          am + X_QKV, nullptr, nullptr, nullptr, st));
+    LnFoldArgs ln_qkv;
+    if (fold && l > 0) {  // y = bf16(x * gamma1) and the row statistics from the last fc2
+      ln_qkv.stats_in = ln_stats;
+      ln_qkv.c = fold_c(l, 0);
+      ln_qkv.b = fold_c(l, 1);
+    } else {
+      PROF(h, P_LN, st, 1,
+           launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_QKV,
+                            am + X_QKV, nullptr, nullptr, nullptr, st));
+    }
     s = run_gemm(h, P_QKV, ESM_EPI_QKV_ROPE, y, fp8 ? (const void*)wq_qkv : w->w_qkv[l], w->b_qkv[l], qkv, pb.pos_id, T,
-                 3 * d, d, fp8, act, sc + X_QKV, sc + W_QKV, nullptr, nullptr, st);
+                 3 * d, d, fp8, act, sc + X_QKV, sc + W_QKV, nullptr, nullptr, st, -1, nullptr, nullptr,
+                 fold && l > 0 ? &ln_qkv : nullptr);
     if (s != ESM_OK) return s;
     {
       ProfScope _ps(h, P_ATTN, st, 1);
@@ -340,18 +398,39 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
           return ESM_ERR_CUDA;
       }
     }
+    LnFoldArgs ln_out;  // out-projection: statistics and bf16(x * gamma2) for fc1
+    if (fold) {
+      ln_out.stats_out = ln_stats;
+      ln_out.gamma = w->ln2_g[l];
+      ln_out.a_out = y;
+    }
     s = run_gemm(h, P_OPROJ, ESM_EPI_RESIDUAL, o, fp8 ? (const void*)wq_o : w->w_o[l], w->b_o[l], x, nullptr, T, d, d, fp8,
-                 Act::F32, sc + X_O, sc + W_O, nullptr, nullptr, st);
+                 Act::F32, sc + X_O, sc + W_O, nullptr, nullptr, st, -1, nullptr, nullptr, fold ? &ln_out : nullptr);
     if (s != ESM_OK) return s;
     // ---- MLP block
-    PROF(h, P_LN, st, 1,
-         launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_1,
-                          am + X_1, nullptr, nullptr, nullptr, st));
+    LnFoldArgs ln_fc1;
+    if (fold) {
+      ln_fc1.stats_in = ln_stats;
+      ln_fc1.c = fold_c(l, 2);
+      ln_fc1.b = fold_c(l, 3);
+    } else {
+      PROF(h, P_LN, st, 1,
+           launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_1,
+                            am + X_1, nullptr, nullptr, nullptr, st));
+    }
     s = run_gemm(h, P_FC1, ESM_EPI_GELU, y, fp8 ? (const void*)wq_1 : w->w_1[l], w->b_1[l], u, nullptr, T, f, d, fp8,
-                 fp8 ? Act::E4M3 : act, sc + X_1, sc + W_1, sc + X_2, am + X_2, st);
+                 fp8 ? Act::E4M3 : act, sc + X_1, sc + W_1, sc + X_2, am + X_2, st, -1, nullptr, nullptr,
+                 fold ? &ln_fc1 : nullptr);
     if (s != ESM_OK) return s;
+    LnFoldArgs ln_fc2;  // fc2: statistics and bf16(x * gamma1) for the next layer's QKV
+    const bool fold_next = fold && l + 1 < c.num_layers;
+    if (fold_next) {
+      ln_fc2.stats_out = ln_stats;
+      ln_fc2.gamma = w->ln1_g[l + 1];
+      ln_fc2.a_out = y;
+    }
     s = run_gemm(h, P_FC2, ESM_EPI_RESIDUAL, u, fp8 ? (const void*)wq_2 : w->w_2[l], w->b_2[l], x, nullptr, T, d, f, fp8,
-                 Act::F32, sc + X_2, sc + W_2, nullptr, nullptr, st);
+                 Act::F32, sc + X_2, sc + W_2, nullptr, nullptr, st, -1, nullptr, nullptr, fold_next ? &ln_fc2 : nullptr);
     if (s != ESM_OK) return s;
   }
   const int32_t* vp = padded ? pb.pos_id : nullptr;
@@ -1093,6 +1172,35 @@ esm_status esm_op_gemm_fp8(esm_encoder_t* h, esm_epilogue epi, const uint8_t* A,
   const Act out_act = (epi == ESM_EPI_BIAS_F32 || epi == ESM_EPI_RESIDUAL) ? Act::F32 : Act::BF16;
   return run_gemm(h, P_OTHER, epi, A, B, bias, out, pos_id, M, N, K, true, out_act, a_scale, b_scale, nullptr,
                   nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+esm_status esm_op_quantize_nvfp4(esm_encoder_t* h, const void* x, int rows, int cols, uint8_t* codes,
+                                 uint8_t* scales, float* amax, float* scale, esm_stream_t stream) {
+  if (!h || !x || !codes || !scales || !amax || !scale || rows < 0 || cols <= 0) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision == ESM_FP32) return ESM_ERR_UNSUPPORTED;
+  if (rows % 128 || cols % 256 || !aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 16) ||
+      !aligned(amax, 4) || !aligned(scale, 4))
+    return ESM_ERR_INVALID_ARG;
+  if (rows == 0) return ESM_OK;
+  return cuda_status(launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(x), rows, cols, codes, scales, amax,
+                                           scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, const uint8_t* a_codes, const uint8_t* a_scales, const float* a_scale,
+                             const uint8_t* b_codes, const uint8_t* b_scales, const float* b_scale, const void* bias,
+                             float* out, int M, int N, int K, esm_stream_t stream) {
+  if (!h || !a_codes || !a_scales || !a_scale || !b_codes || !b_scales || !b_scale || !out) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision == ESM_FP32) return ESM_ERR_UNSUPPORTED;
+  if (M < 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 256) return ESM_ERR_INVALID_ARG;
+  if (!aligned(a_codes, 16) || !aligned(b_codes, 16) || !aligned(a_scales, 16) || !aligned(b_scales, 16) ||
+      !aligned(out, 16) || (bias && !aligned(bias, 16)))
+    return ESM_ERR_INVALID_ARG;
+  if (M == 0) return ESM_OK;
+  const CUtensorMap* ma = h->map(a_codes, (uint64_t)M, (uint64_t)K / 2, 128, 1);
+  const CUtensorMap* mb = h->map(b_codes, (uint64_t)N, (uint64_t)K / 2, 128, 1);
+  if (!ma || !mb) return ESM_ERR_CUDA;
+  return cuda_status(launch_gemm_nvfp4(ma, mb, a_scales, b_scales, a_scale, b_scale, bias, false, out, M, N, K,
+                                       h->d_err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,

@@ -159,13 +159,72 @@ __device__ __forceinline__ void residual_rows_async(const EpiArgs& ea, uint8_t* 
 __device__ __forceinline__ void residual_rows_store(const EpiArgs& ea, const uint8_t* buf, int q, int lane, int row0,
                                                     int M, int N, int col) {
   float* x = static_cast<float*>(ea.out);
+  const int u = lane & 7;
+  // folded LayerNorm: the next GEMM's operand bf16(x * gamma), 4 columns (8 bytes) per lane,
+  // so each instruction writes 64 contiguous bytes of four rows
+  float4 gm = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (ea.ln_a_out != nullptr) {
+    const uint2 g = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(ea.ln_gamma) + col + 4 * u));
+    const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
+    const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
+    gm = make_float4(g0.x, g0.y, g1.x, g1.y);
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int rr = q * 32 + 4 * i + (lane >> 3);
-    const int u = lane & 7;
     const int grow = row0 + rr;
     const uint4 v = *reinterpret_cast<const uint4*>(buf + swz_off(rr, u));
-    if (grow < M) *reinterpret_cast<uint4*>(x + (size_t)grow * N + col + 4 * u) = v;
+    if (grow < M) {
+      *reinterpret_cast<uint4*>(x + (size_t)grow * N + col + 4 * u) = v;
+      if (ea.ln_a_out != nullptr) {
+        const float4 f = *reinterpret_cast<const float4*>(&v);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(ea.ln_a_out) + (size_t)grow * N + col + 4 * u) =
+            make_uint2(pack_bf16x2(f.x * gm.x, f.y * gm.y), pack_bf16x2(f.z * gm.z, f.w * gm.w));
+      }
+    }
+  }
+}
+
+// Folded LayerNorm, consumer side: rstd and mean * rstd of row `row` from the (mean, sum of
+// squared deviations) of its ln_groups groups of 64 columns (the parallel-variance
+// combination: M2 = sum M2_g + 64 sum (mean_g - mean)^2, var = M2 / (64 groups)).  One pass
+// over 16-byte loads (two groups each) issued together; the group means enter as deviations
+// from the first one, so the between-group term has no cancellation.
+__device__ __forceinline__ float2 ln_row_stats(const EpiArgs& ea, int row, int M) {
+  if (row >= M) return make_float2(0.f, 0.f);
+  const float4* st = reinterpret_cast<const float4*>(ea.ln_stats_in + (size_t)row * ea.ln_groups);
+  const int pairs = ea.ln_groups >> 1;  // ln_groups is even (hidden % 128 == 0)
+  const float m0 = __ldg(reinterpret_cast<const float*>(st));
+  float sd = 0.f, sd2 = 0.f, sm2 = 0.f;
+  constexpr int kMaxPairs = 32;  // hidden <= 4096
+#pragma unroll
+  for (int p = 0; p < kMaxPairs; ++p) {
+    if (p < pairs) {
+      const float4 v = __ldg(st + p);  // (mean, M2) of groups 2p and 2p + 1
+      const float d0 = v.x - m0, d1 = v.z - m0;
+      sd += d0 + d1;
+      sd2 += d0 * d0 + d1 * d1;
+      sm2 += v.y + v.w;
+    }
+  }
+  const float G = (float)ea.ln_groups;
+  const float dmean = sd / G;
+  const float m2 = sm2 + 64.f * fmaxf(sd2 - sd * dmean, 0.f);
+  const float rstd = rsqrtf(m2 / (64.f * G) + ea.ln_eps);
+  return make_float2(rstd, (m0 + dmean) * rstd);
+}
+
+// Folded LayerNorm applied to W accumulator values of columns c..: v = rstd v - mr c_n + b'_n.
+template <int W>
+__device__ __forceinline__ void ln_fold_apply(const EpiArgs& ea, int c, float2 rs, float (&v)[W]) {
+#pragma unroll
+  for (int i4 = 0; i4 < W / 4; ++i4) {
+    const float4 cc = __ldg(reinterpret_cast<const float4*>(ea.ln_c + c) + i4);
+    const float4 bb = __ldg(reinterpret_cast<const float4*>(ea.ln_b + c) + i4);
+    v[4 * i4 + 0] = fmaf(v[4 * i4 + 0], rs.x, fmaf(-rs.y, cc.x, bb.x));
+    v[4 * i4 + 1] = fmaf(v[4 * i4 + 1], rs.x, fmaf(-rs.y, cc.y, bb.y));
+    v[4 * i4 + 2] = fmaf(v[4 * i4 + 2], rs.x, fmaf(-rs.y, cc.z, bb.z));
+    v[4 * i4 + 3] = fmaf(v[4 * i4 + 3], rs.x, fmaf(-rs.y, cc.w, bb.w));
   }
 }
 
@@ -468,6 +527,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int g = 0; g < 16; ++g) cs[g] = __ldg(tab + (size_t)g * ea.max_pos);
         }
       }
+      // folded LayerNorm: this row's statistics (QKV / GELU epilogues of a bf16 forward)
+      float2 ln_rs = make_float2(1.f, 0.f);
+      if constexpr (!FP8 && (EPI == ESM_EPI_QKV_ROPE || EPI == ESM_EPI_GELU)) {
+        if (ea.ln_stats_in != nullptr) ln_rs = ln_row_stats(ea, row, M);
+      }
       const bool ok = mbar_wait_warp(&sm->tfull[acc], acc_phase);
       if (!ok && lane == 0) {
         latch_error(err, ERRBIT_TIMEOUT);
@@ -481,6 +545,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + acc * BN + half * (tx.bn / 2) + ((uint32_t)(q * 32) << 16);
       float vlast[(EPI == ESM_EPI_BIAS_F32 || EPI == ESM_EPI_RESIDUAL) ? 32 : 1];
+      float2 ln_pend = make_float2(0.f, 0.f);  // residual: statistics of the group's first chunk
 
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
@@ -513,6 +578,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
           }
           load_bias32(ea, col, bb);
+          // folded LayerNorm statistics of the new residual: sums of deviations from the
+          // chunk's first value (shifted sums keep the variance free of cancellation)
+          float k0 = 0.f, s1 = 0.f, s2 = 0.f;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t off = swz_off(r, j);
@@ -524,6 +592,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             o.z = x.z + (v[4 * j + 2] * acc_scale + bb[4 * j + 2]);
             o.w = x.w + (v[4 * j + 3] * acc_scale + bb[4 * j + 3]);
             *reinterpret_cast<float4*>(buf + off) = o;
+            if constexpr (EPI == ESM_EPI_RESIDUAL) {
+              if (j == 0) k0 = o.x;
+              const float a0 = o.x - k0, a1 = o.y - k0, a2 = o.z - k0, a3 = o.w - k0;
+              s1 += (a0 + a1) + (a2 + a3);
+              s2 += (a0 * a0 + a1 * a1) + (a2 * a2 + a3 * a3);
+            }
+          }
+          if constexpr (EPI == ESM_EPI_RESIDUAL) {
+            if (ea.ln_stats_out != nullptr) {
+              // chunk statistics (32 columns), merged in pairs into 64-column groups
+              const float cm = k0 + s1 * (1.f / 32.f);
+              const float cm2 = fmaxf(s2 - s1 * s1 * (1.f / 32.f), 0.f);
+              if ((c & 1) == 0) {
+                ln_pend = make_float2(cm, cm2);
+              } else if (row < M) {
+                const float dm = ln_pend.x - cm;
+                ea.ln_stats_out[(size_t)row * (N / 64) + (col - 32) / 64] =
+                    make_float2(0.5f * (ln_pend.x + cm), ln_pend.y + cm2 + 16.f * dm * dm);
+              }
+            }
           }
           if constexpr (EPI == ESM_EPI_RESIDUAL) {
             // coalesced write-back of this warp's 32 rows, then refill the buffer with the
@@ -559,8 +647,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld16(tbase + c * CH::kCols + 16 * h, a);
             tmem_ld16(tbase + c * CH::kCols + 32 + 16 * h, bq);
             if (h == 1 && c == nch - 1) release_acc();
-            scale_add_bias<16>(ea, col + 16 * h, acc_scale, a);
-            scale_add_bias<16>(ea, col + 32 + 16 * h, acc_scale, bq);
+            if (!FP8 && ea.ln_stats_in != nullptr) {
+              ln_fold_apply<16>(ea, col + 16 * h, ln_rs, a);
+              ln_fold_apply<16>(ea, col + 32 + 16 * h, ln_rs, bq);
+            } else {
+              scale_add_bias<16>(ea, col + 16 * h, acc_scale, a);
+              scale_add_bias<16>(ea, col + 32 + 16 * h, acc_scale, bq);
+            }
             if (col < ea.rope_cols) {
 #pragma unroll
               for (int i = 0; i < 16; i += 2) {  // cs[g] = (cos, sin) of pairs 2g and 2g + 1
@@ -602,8 +695,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tbase + c * CH::kCols, v0);
           tmem_ld32(tbase + c * CH::kCols + 32, v1);
           if (c == nch - 1) release_acc();
-          scale_add_bias<32>(ea, col, acc_scale, v0);
-          scale_add_bias<32>(ea, col + 32, acc_scale, v1);
+          if (!FP8 && ea.ln_stats_in != nullptr) {
+            ln_fold_apply<32>(ea, col, ln_rs, v0);
+            ln_fold_apply<32>(ea, col + 32, ln_rs, v1);
+          } else {
+            scale_add_bias<32>(ea, col, acc_scale, v0);
+            scale_add_bias<32>(ea, col + 32, acc_scale, v1);
+          }
           if (ea.aux != nullptr && row < M) {  // training forward: keep the pre-activation
             uint4* zr = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ea.aux) + (size_t)row * N + col);
 #pragma unroll

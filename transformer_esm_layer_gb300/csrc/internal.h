@@ -81,6 +81,20 @@ struct EpiArgs {
   const void* res_in;     // ESM_EPI_RESIDUAL: residual read from here instead of out (NULL: in place)
   void* aux;              // ESM_EPI_GELU: also store the pre-activation here (bf16 [M, N]; NULL: no);
                           // kEpiDgelu: the forward's pre-activation z to multiply by GELU'(z)
+  // LayerNorm folded into the next GEMM (bf16 forward).  The residual epilogue writes, for
+  // the updated rows, the statistics of every 64-column group (mean, sum of squared
+  // deviations: float2 [M, N / 64]) and, with ln_a_out, the next GEMM's operand
+  // bf16(x * gamma) ([M, N]).  The consumer (QKV / GELU epilogue) reads the statistics of
+  // its A rows and applies LN(x) W^T + b = rstd (acc - mean c) + b' per row, with
+  // c_n = sum_k gamma_k W_nk and b'_n = b_n + sum_k beta_k W_nk (fp32 [N]) in place of the bias.
+  float2* ln_stats_out;   // ESM_EPI_RESIDUAL: statistics of the new residual rows (NULL: none)
+  const void* ln_gamma;   // ESM_EPI_RESIDUAL: gamma (bf16 [N]) of the LayerNorm that follows
+  void* ln_a_out;         // ESM_EPI_RESIDUAL: bf16(x * gamma) [M, N] (NULL: not written)
+  const float2* ln_stats_in;  // QKV / GELU: statistics of the A rows [M, ln_groups] (NULL: no fold)
+  const float* ln_c;      // [N] sum_k gamma_k W_nk
+  const float* ln_b;      // [N] b_n + sum_k beta_k W_nk
+  int ln_groups;          // K / 64
+  float ln_eps;
 };
 // Epilogue of the input gradient through fc1's GELU: out = acc * GELU'(z) (bf16), z = aux.
 constexpr int kEpiDgelu = 16;
@@ -121,6 +135,35 @@ void launch_gemm_f32(esm_epilogue epi, const float* A, const float* B, int M, in
 // In-place RoPE on the q and k blocks of qkv [T, 3*d] (fp32).
 void launch_rope_f32(float* qkv, int T, int d, int head_dim, const int32_t* pos_id, const float2* rope,
                      int max_pos, cudaStream_t st);
+
+// Folded-LayerNorm constants of one linear map W [n, k] (bf16) that follows a LayerNorm
+// (gamma, beta [k], bf16) with bias (bf16 [n]): c_out[i] = sum_j gamma_j W_ij and
+// b_out[i] = bias_i + sum_j beta_j W_ij (fp32).
+struct LnFoldJob {
+  const void* w;
+  const void* gamma;
+  const void* beta;
+  const void* bias;
+  float* c_out;
+  float* b_out;
+  int n;
+};
+constexpr int kLnFoldMaxJobs = 96;
+void launch_ln_fold(const LnFoldJob* jobs, int num_jobs, int k, cudaStream_t st);
+
+// ---------------------------------------------------------------- fp4.cu
+// NVFP4 operand of x [rows, K] bf16 (rows % 128 == 0, K % 256 == 0): E2M1 codes [rows, K/2]
+// bytes, E4M3 block scales in 512-byte atoms of 128 rows x 64 values, the tensor scale S and
+// the tensor's amax (device scalars).
+cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                                  float* amax, float* scale, cudaStream_t st);
+// out [M, N] fp32 = (A B^T) / (a_scale b_scale) + bias for NVFP4 operands A [M, K], B [N, K]
+// (tensor maps over the code bytes [rows, K/2] with a 128 x 128 box and the 128-byte swizzle);
+// M % 128 == 0, N % 128 == 0, K % 256 == 0.
+int gemm_nvfp4_smem_bytes();
+cudaError_t launch_gemm_nvfp4(const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa, const uint8_t* sfb,
+                              const float* a_scale, const float* b_scale, const void* bias, bool bias_f32, float* out,
+                              int M, int N, int K, unsigned* err, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention.cu
 // tcgen05 attention (head_dim 64): tm_qkv is a tensor map over qkv [T, 3d] bf16 with a

@@ -155,7 +155,53 @@ void ln_dispatch(const void* x, const void* g, const void* b, bool pf32, void* y
   else ln_dispatch_out<32, IN_BF16>(x, g, b, pf32, y, out, rows, cols, eps, qs, amax, vp, vs, vk, st);
 }
 
+struct LnFoldJobs {
+  LnFoldJob j[kLnFoldMaxJobs];
+};
+
+// One warp per output row i of job blockIdx.y: the dot products of W's row with gamma and
+// with beta (fp32 accumulation of the bf16 products), 8 columns per lane per step.
+__global__ void __launch_bounds__(256) ln_fold_kernel(const __grid_constant__ LnFoldJobs jobs, int k) {
+  const LnFoldJob& jb = jobs.j[blockIdx.y];
+  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= jb.n) return;
+  const uint4* wr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(jb.w) + (size_t)i * k);
+  const uint4* gr = reinterpret_cast<const uint4*>(jb.gamma);
+  const uint4* br = reinterpret_cast<const uint4*>(jb.beta);
+  float sc = 0.f, sb = 0.f;
+  for (int u = lane; u < k / 8; u += 32) {
+    const uint4 wv = __ldg(wr + u), gv = __ldg(gr + u), bv = __ldg(br + u);
+    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 w = __bfloat1622float2(w2[t]), g = __bfloat1622float2(g2[t]), b = __bfloat1622float2(b2[t]);
+      sc = fmaf(w.x, g.x, fmaf(w.y, g.y, sc));
+      sb = fmaf(w.x, b.x, fmaf(w.y, b.y, sb));
+    }
+  }
+  sc = warp_sum(sc);
+  sb = warp_sum(sb);
+  if (lane == 0) {
+    jb.c_out[i] = sc;
+    jb.b_out[i] = sb + (jb.bias ? __bfloat162float(static_cast<const __nv_bfloat16*>(jb.bias)[i]) : 0.f);
+  }
+}
+
 }  // namespace
+
+void launch_ln_fold(const LnFoldJob* jobs, int num_jobs, int k, cudaStream_t st) {
+  if (num_jobs <= 0) return;
+  LnFoldJobs p{};
+  int max_n = 0;
+  for (int i = 0; i < num_jobs && i < kLnFoldMaxJobs; ++i) {
+    p.j[i] = jobs[i];
+    max_n = jobs[i].n > max_n ? jobs[i].n : max_n;
+  }
+  ln_fold_kernel<<<dim3((max_n + 7) / 8, num_jobs < kLnFoldMaxJobs ? num_jobs : kLnFoldMaxJobs), 256, 0, st>>>(p, k);
+}
 
 void launch_layernorm(const float* x, const void* g, const void* b, bool param_f32, void* y, Act out, int rows,
                       int cols, float eps, const float* q_scale, float* amax, const int32_t* vp, const int32_t* vs,
