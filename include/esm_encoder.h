@@ -346,6 +346,32 @@ ESM_API esm_status esm_op_attention_noalloc(const void* qkv, const int32_t* cu_s
                                             int total_tokens, int max_seqlen, int hidden, int heads, void* o,
                                             int32_t* status, esm_stream_t stream);
 
+/* ---- NVFP4 (block-scaled E2M1) operands and GEMM ----
+ * The mlqm.cn walkthrough (section FP8与FP4混合精度支持) gives the encoder an fp4_recipe beside
+ * the FP8 one; the pages give no FP4 format.  The format read here is the block-scaled FP4 of
+ * the tensor cores: E2M1 values (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), one E4M3 scale per
+ * block of 16 consecutive values along K, one fp32 tensor scale S = 448 * 6 / amax:
+ *   sb = E4M3(max|block| / 6 * S),  q = E2M1(x * S / sb) (0 for an all-zero block),  x ~ q sb / S,
+ * both roundings to nearest even, saturating.
+ * esm_op_quantize_nvfp4: x device bf16 [rows, cols] (rows % 128 == 0, cols % 256 == 0, 16-byte
+ *   aligned) -> codes device [rows, cols / 2] bytes (value k in the low nibble of byte k / 2 for
+ *   even k), scales device [rows * cols / 16] bytes in 512-byte atoms of 128 rows x 64 values
+ *   (atom (r / 128, k / 64) at ((r / 128) * (cols / 64) + k / 64) * 512, row r and 16-value block
+ *   b inside it at (r % 32) * 16 + ((r % 128) / 32) * 4 + b), amax and scale device float scalars
+ *   (overwritten: the tensor's max |x| and S).  Two kernels (amax, then codes and scales).
+ * esm_op_gemm_nvfp4: out device float32 [M, N] = (A B^T) / (a_scale b_scale) + bias for NVFP4
+ *   operands from esm_op_quantize_nvfp4 (A [M, K], B [N, K]; a_scale, b_scale their device
+ *   tensor scales; bias device bf16 [N] or NULL); M % 128, N % 128, K % 256 all 0 (else
+ *   ESM_ERR_INVALID_ARG).  tcgen05.mma kind::mxf4nvf4 with block scaling (the E4M3 block scales
+ *   multiply on the tensor core).  Needs an ESM_BF16 or ESM_FP8_E4M3 handle (for its error word
+ *   and tensor-map cache). */
+ESM_API esm_status esm_op_quantize_nvfp4(esm_encoder_t* h, const void* x, int rows, int cols, uint8_t* codes,
+                                         uint8_t* scales, float* amax, float* scale, esm_stream_t stream);
+ESM_API esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, const uint8_t* a_codes, const uint8_t* a_scales,
+                                     const float* a_scale, const uint8_t* b_codes, const uint8_t* b_scales,
+                                     const float* b_scale, const void* bias, float* out, int M, int N, int K,
+                                     esm_stream_t stream);
+
 /* ---- FP8 delayed-scaling state (ESM_FP8_E4M3 handles) ----
  * Layout, float32: for each layer l and each of the 8 quantised tensors k in the order
  * {x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2}: scale[l][k] (num_layers*8 floats), then

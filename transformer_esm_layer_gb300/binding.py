@@ -34,7 +34,7 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_op_layernorm_backward_workspace_size", "esm_op_layernorm_backward", "esm_op_attention_train",
            "esm_op_attention_backward_workspace_size", "esm_op_attention_backward",
            "esm_encoder_lm_head_backward_workspace_size", "esm_encoder_lm_head_backward",
-           "esm_status_string")
+           "esm_op_quantize_nvfp4", "esm_op_gemm_nvfp4", "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other",
                    "gemm_backward")
 
@@ -118,6 +118,8 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_set_profiling": (i32, [vp, i32]),
         "esm_encoder_get_profile": (i32, [vp, ctypes.POINTER(EsmProfile), i32]),
         "esm_op_attention_noalloc": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
+        "esm_op_quantize_nvfp4": (i32, [vp, vp, i32, i32, vp, vp, vp, vp, vp]),
+        "esm_op_gemm_nvfp4": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
         "esm_op_layernorm_e4m3": (i32, [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp]),
         "esm_encoder_debug_wait_timeout": (i32, [vp, i32, vp]),
         "esm_op_gemm_fp8": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
@@ -532,6 +534,33 @@ class EsmEncoder:
                                                           _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
                     "esm_encoder_lm_head_backward")
         return d_hidden, grads
+
+    def op_quantize_nvfp4(self, x, stream=None):
+        """esm_op_quantize_nvfp4 of a contiguous bf16 [rows, cols] CUDA tensor: returns (codes uint8
+        [rows, cols/2], scales uint8 [rows * cols / 16] in the tensor-core atom order, amax and
+        scale as float32 one-element tensors)."""
+        import torch
+        rows, cols = x.shape
+        codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=x.device)
+        scales = torch.empty(rows * cols // 16, dtype=torch.uint8, device=x.device)
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+        self._raise(self.lib.esm_op_quantize_nvfp4(self.handle, _ptr(x), rows, cols, _ptr(codes), _ptr(scales),
+                                                   _ptr(amax), _ptr(scale), _stream_ptr(stream)), "esm_op_quantize_nvfp4")
+        return codes, scales, amax, scale
+
+    def op_gemm_nvfp4(self, a, b, bias=None, out=None, stream=None):
+        """esm_op_gemm_nvfp4 of two operands returned by op_quantize_nvfp4 (A [M, K], B [N, K]):
+        float32 [M, N] = (A B^T) / (S_A S_B) + bias."""
+        import torch
+        (ac, asf, _, asc), (bc, bsf, _, bsc) = a, b
+        M, N, K = ac.shape[0], bc.shape[0], 2 * ac.shape[1]
+        if out is None:
+            out = torch.empty(M, N, dtype=torch.float32, device=ac.device)
+        self._raise(self.lib.esm_op_gemm_nvfp4(self.handle, _ptr(ac), _ptr(asf), _ptr(asc), _ptr(bc), _ptr(bsf),
+                                               _ptr(bsc), _ptr(bias), _ptr(out), M, N, K, _stream_ptr(stream)),
+                    "esm_op_gemm_nvfp4")
+        return out
 
     def set_profiling(self, enable: bool):
         self._raise(self.lib.esm_encoder_set_profiling(self.handle, int(enable)), "esm_encoder_set_profiling")

@@ -1,0 +1,324 @@
+// NVFP4 (block-scaled E2M1) GEMM operands and their product on the 5th-generation tensor
+// cores (tcgen05.mma kind::mxf4nvf4 with block scaling).
+//
+// The mlqm.cn walkthrough ("深入源码NVIDIA ESM-2 TransformerEngine优化的实现原理与技术细节",
+// section FP8与FP4混合精度支持) gives NVEsmEncoder an fp4_recipe beside the FP8 one; the pages
+// give no FP4 format.  Reading (the block-scaled FP4 of the tensor cores): every value is
+// E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3,
+// 4, 6), every block of 16 consecutive values along the reduction axis has one E4M3 scale,
+// and the tensor has one fp32 scale S = 448 * 6 / amax chosen so that the largest block scale
+// is representable:
+//   sb = E4M3(max|block| / 6 * S),   q = E2M1(x * S / sb)   (0 for an all-zero block),
+//   x ~ q * sb / S.
+// The GEMM multiplies the E2M1 codes with their block scales on the tensor core (the E4M3
+// block scales enter the MMA through tensor memory) and divides by S_A * S_B in the epilogue.
+//
+// Layouts (this library's):
+//   codes  [rows, K / 2] bytes, value k of a row in the low nibble of byte k / 2 for even k;
+//   scales one byte per 16 values, in 512-byte atoms of 128 rows x 64 values: atom
+//          (row / 128, k / 64) at byte ((row / 128) * (K / 64) + k / 64) * 512, and inside it
+//          row r (of the 128) and 16-value block b (of the 4) at (r % 32) * 16 + (r / 32) * 4 + b
+//          -- the arrangement tcgen05.cp.32x128b.warpx4 copies into tensor memory as the scale
+//          factors of one M = 128 MMA (lane r % 32 of every lane quarter, column r / 32).
+#include "common.cuh"
+#include "internal.h"
+
+namespace esm {
+namespace {
+
+constexpr int BM = 128, BN = 128;   // output tile of one CTA
+constexpr int STAGE_K = 256;        // E2M1 values per row per stage (128 bytes)
+constexpr int STAGES = 4;
+constexpr int ROW_BYTES = 128;
+constexpr int TILE_BYTES = 128 * ROW_BYTES;  // 16 KB: 128 rows of one stage
+constexpr int ATOM_BYTES = 512;              // scales of 128 rows x 64 values
+constexpr int SF_STAGE_BYTES = 4 * ATOM_BYTES;  // 4 MMA k-steps of 64 values
+constexpr int THREADS = 128;
+constexpr uint32_t TMEM_COLS = 256;  // accumulator 128 + scale-factor ring 4 x (16 + 16)
+constexpr uint32_t COL_SF = 128;
+
+struct Fp4Smem {
+  uint64_t full[STAGES], empty[STAGES], done;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+constexpr int A_OFF = 0, B_OFF = STAGES * TILE_BYTES, SFA_OFF = 2 * STAGES * TILE_BYTES,
+              SFB_OFF = SFA_OFF + STAGES * SF_STAGE_BYTES, BAR_OFF = SFB_OFF + STAGES * SF_STAGE_BYTES;
+constexpr int SMEM_BYTES = BAR_OFF + 1024 + 256;
+
+__device__ __forceinline__ size_t sf_offset(int row, int k16, int K) {
+  const int rb = row >> 7, r = row & 127, ks = k16 >> 2, b = k16 & 3;
+  return ((size_t)rb * (K / 64) + ks) * ATOM_BYTES + (r & 31) * 16 + (r >> 5) * 4 + b;
+}
+
+// E2M1 code of v (round to nearest, ties to the even code, saturating at 6): the 3-bit
+// magnitude code grows with the value (0, 0.5, 1, 1.5, 2, 3, 4, 6), so it counts the rounding
+// midpoints below |v|; a midpoint into an odd code is exclusive, into an even code inclusive.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const float a = fabsf(v);
+  const uint32_t m = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+                     (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.f);
+  return (v < 0.f ? 8u : 0u) | m;
+}
+
+__device__ __forceinline__ void bf16x8(uint4 u, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __nv_bfloat16* __restrict__ x, size_t n8,
+                                                         float* amax) {
+  float m = 0.f;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    float f[8];
+    bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + i), f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomic_max_nonneg(amax, m);
+}
+
+// One thread per block of 16 values: the block's E4M3 scale and its eight code bytes.
+__global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int K,
+                                                             const float* amax, uint8_t* __restrict__ codes,
+                                                             uint8_t* __restrict__ sf, float* scale_out) {
+  const size_t blk = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const int kb = K / 16;
+  const float a = __ldg(amax);
+  const float S = a > 0.f ? (448.f * 6.f) / a : 1.f;
+  if (blk == 0 && scale_out) *scale_out = S;
+  if (blk >= (size_t)rows * kb) return;
+  const int row = (int)(blk / kb), k16 = (int)(blk % kb);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * K + (size_t)k16 * 16);
+  float v[16];
+  {
+    float f[8];
+    bf16x8(__ldg(src), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = f[i];
+    bf16x8(__ldg(src + 1), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 + i] = f[i];
+  }
+  float bmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+  const __nv_fp8_e4m3 sb8(bmax / 6.f * S);  // round to nearest even, saturating at 448
+  const float sb = static_cast<float>(sb8);
+  uint32_t w[2] = {0u, 0u};
+  if (sb > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i >> 3] |= e2m1_code(v[i] * S / sb) << (4 * (i & 7));
+  }
+  *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + (size_t)k16 * 8) = make_uint2(w[0], w[1]);
+  sf[sf_offset(row, k16, K)] = *reinterpret_cast<const uint8_t*>(&sb8);
+}
+
+// 1-D bulk copy global -> shared completing `bytes` on the mbarrier (16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared-memory descriptor of one 512-byte scale-factor atom (32 rows of 16 bytes, no
+// swizzle): 8-row core matrices of 128 bytes, consecutive along the rows.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)(128u >> 4) << 16;          // leading byte offset
+  d |= (uint64_t)(128u >> 4) << 32;          // stride byte offset: next 8 rows
+  d |= (uint64_t)1u << 46;                   // descriptor version (tcgen05)
+  return d;                                  // swizzle mode 0: none
+}
+
+// Instruction descriptor, kind::mxf4nvf4 with block scaling: D f32, A and B E2M1 (format 1),
+// both K-major, scale factors UE4M3 (scale format 0), scale-factor data ids 0, M x N.
+__host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <bool BIAS_F32>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, const float* a_scale,
+                      const float* b_scale, const void* __restrict__ bias, float* __restrict__ out, int M, int N,
+                      int K, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Fp4Smem* sm = reinterpret_cast<Fp4Smem*>(base + BAR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int kb_total = K / STAGE_K;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sm->full[s], 1);
+      mbar_init(&sm->empty[s], 1);
+    }
+    mbar_init(&sm->done, 1);
+    sm->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(&sm->tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: A and B code tiles by TMA, their scale-factor atoms by bulk copy
+    int issued = 0;
+    for (int kb = 0; kb < kb_total && !sm->abort; ++kb, ++issued) {
+      const int s = kb % STAGES;
+      if (!mbar_wait(&sm->empty[s], ((uint32_t)(kb / STAGES) & 1u) ^ 1u)) {
+        latch_error(err, ERRBIT_TIMEOUT);
+        sm->abort = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&sm->full[s], 2 * TILE_BYTES + 2 * SF_STAGE_BYTES);
+      tma_load_2d(base + A_OFF + s * TILE_BYTES, &tmA, kb * ROW_BYTES, m0, &sm->full[s]);
+      tma_load_2d(base + B_OFF + s * TILE_BYTES, &tmB, kb * ROW_BYTES, n0, &sm->full[s]);
+      bulk_load(base + SFA_OFF + s * SF_STAGE_BYTES, sfa + ((size_t)(m0 / 128) * (K / 64) + 4 * kb) * ATOM_BYTES,
+                SF_STAGE_BYTES, &sm->full[s]);
+      bulk_load(base + SFB_OFF + s * SF_STAGE_BYTES, sfb + ((size_t)(n0 / 128) * (K / 64) + 4 * kb) * ATOM_BYTES,
+                SF_STAGE_BYTES, &sm->full[s]);
+    }
+    if (sm->abort)  // copies in flight land before the CTA may exit (bounded)
+      for (int k = issued - 1; k >= 0 && k >= issued - STAGES; --k)
+        if (!mbar_wait(&sm->full[k % STAGES], (uint32_t)(k / STAGES) & 1u)) break;
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer: per stage, the 8 scale-factor atoms into tensor memory, then the 4
+    // block-scaled MMAs of 64 values each (tcgen05.cp and tcgen05.mma of one thread execute
+    // in issue order)
+    constexpr uint32_t idesc = idesc_nvfp4(BM, BN);
+    const uint64_t adesc0 = make_sw128_desc(smem_u32(base + A_OFF));
+    const uint64_t bdesc0 = make_sw128_desc(smem_u32(base + B_OFF));
+    for (int kb = 0; kb < kb_total; ++kb) {
+      const int s = kb % STAGES;
+      if (!mbar_wait(&sm->full[s], (uint32_t)(kb / STAGES) & 1u)) {
+        latch_error(err, ERRBIT_TIMEOUT);
+        sm->abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sf_col = tmem + COL_SF + 32u * (uint32_t)s;  // SFA at +4 ks, SFB at +16 + 4 ks
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint32_t sa = smem_u32(base + SFA_OFF + s * SF_STAGE_BYTES + ks * ATOM_BYTES);
+        const uint32_t sb = smem_u32(base + SFB_OFF + s * SF_STAGE_BYTES + ks * ATOM_BYTES);
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 4 * ks), "l"(sf_desc(sa))
+                     : "memory");
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 16 + 4 * ks), "l"(sf_desc(sb))
+                     : "memory");
+      }
+      const uint64_t ad = adesc0 + (uint64_t)((s * TILE_BYTES) >> 4);
+      const uint64_t bd = bdesc0 + (uint64_t)((s * TILE_BYTES) >> 4);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {  // 64 values = 32 bytes of each 128-byte row
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                tmem),
+            "l"(ad + (uint64_t)(2 * ks)), "l"(bd + (uint64_t)(2 * ks)), "r"(idesc), "r"(sf_col + 4 * ks),
+            "r"(sf_col + 16 + 4 * ks), "r"((kb | ks) != 0 ? 1u : 0u)
+            : "memory");
+      }
+      mma_commit(&sm->empty[s]);
+    }
+    mma_commit(&sm->done);
+  }
+  __syncwarp();
+  // ---- epilogue (all four warps): row 32 w + lane of the tile, 128 fp32 columns
+  const bool ok = mbar_wait_warp(&sm->done, 0);
+  if (!ok && lane == 0) latch_error(err, ERRBIT_TIMEOUT);
+  if (ok && !sm->abort) {
+    tc_fence_after();
+    const float inv = 1.f / (__ldg(a_scale) * __ldg(b_scale));
+    const int row = m0 + warp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      float v[32];
+      tmem_ld32(tmem + lane_off + (uint32_t)c, v);
+      if (row < M) {
+        float4* dst = reinterpret_cast<float4*>(out + (size_t)row * N + n0 + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float b4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = n0 + c + 4 * j + i;
+            b4[i] = bias == nullptr ? 0.f
+                                    : (BIAS_F32 ? __ldg(static_cast<const float*>(bias) + col)
+                                                : __bfloat162float(static_cast<const __nv_bfloat16*>(bias)[col]));
+          }
+          dst[j] = make_float4(v[4 * j] * inv + b4[0], v[4 * j + 1] * inv + b4[1], v[4 * j + 2] * inv + b4[2],
+                               v[4 * j + 3] * inv + b4[3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                                  float* amax_scratch, float* scale, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  const size_t n8 = (size_t)rows * K / 8;
+  int grid = (int)((n8 + 255) / 256);
+  if (grid > 4096) grid = 4096;
+  nvfp4_amax_kernel<<<grid, 256, 0, st>>>(x, n8, amax_scratch);
+  const size_t blocks = (size_t)rows * (K / 16);
+  nvfp4_quantize_kernel<<<(unsigned)((blocks + 255) / 256), 256, 0, st>>>(x, rows, K, amax_scratch, codes, sf, scale);
+  return cudaGetLastError();
+}
+
+int gemm_nvfp4_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_gemm_nvfp4(const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa, const uint8_t* sfb,
+                              const float* a_scale, const float* b_scale, const void* bias, bool bias_f32, float* out,
+                              int M, int N, int K, unsigned* err, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  static bool configured[2] = {false, false};
+  if (!configured[bias_f32]) {
+    cudaError_t e = bias_f32 ? cudaFuncSetAttribute(gemm_nvfp4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    SMEM_BYTES)
+                             : cudaFuncSetAttribute(gemm_nvfp4_kernel<false>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured[bias_f32] = true;
+  }
+  const dim3 grid(N / BN, M / BM);
+  if (bias_f32)
+    gemm_nvfp4_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, sfa, sfb, a_scale, b_scale, bias, out, M, N,
+                                                               K, err);
+  else
+    gemm_nvfp4_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, sfa, sfb, a_scale, b_scale, bias, out, M,
+                                                                N, K, err);
+  return cudaGetLastError();
+}
+
+}  // namespace esm
