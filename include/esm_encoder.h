@@ -173,13 +173,22 @@ ESM_API esm_status esm_encoder_forward_padded(esm_encoder_t* h, const esm_weight
  * context (get_autocast_context(layer_number)) of the mlqm.cn walkthrough (mixed FP8 / FP4
  * section): each Transformer layer may run its linear maps in its own precision.
  * per_layer[num_layers]: for an ESM_FP8_E4M3 handle each entry is ESM_FP8_E4M3 (the
- * layer's four GEMMs take E4M3 operands with the handle's delayed scaling) or ESM_BF16
- * (bf16 operands; the layer's scales are then left unchanged); attention and LayerNorm stay
- * bf16 either way.  A handle of another precision accepts only its own precision for every
- * layer.  ESM_FP4_E2M1 (block-scaled FP4, named on that page) has no kernels here:
+ * layer's four GEMMs take E4M3 operands with the handle's delayed scaling), ESM_BF16
+ * (bf16 operands; the layer's scales are then left unchanged) or ESM_FP4_E2M1 (the layer's
+ * four GEMMs take NVFP4 operands -- see esm_op_quantize_nvfp4 -- quantised in the call from
+ * the bf16 LayerNorm outputs, attention output and GELU output and from the bf16 weights,
+ * each tensor with its own current scale S = 448 * 6 / amax; block-scaled tcgen05 GEMMs);
+ * attention and LayerNorm stay bf16 in every layer.  A handle of another precision accepts
+ * only its own precision for every layer; ESM_FP4_E2M1 as a handle precision is
  * ESM_ERR_UNSUPPORTED.  num_layers must equal the config's.  Takes effect from the next
  * forward; default: every layer in the handle's precision. */
 ESM_API esm_status esm_encoder_set_layer_precision(esm_encoder_t* h, const esm_precision* per_layer, int num_layers);
+
+/* The NVFP4 tensor scales S of the last forward's FP4 layers (ESM_FP8_E4M3 handles): host_buf
+ * float32 [num_layers * 8] in the tensor order {x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2}
+ * (zero for layers that did not run in FP4); n must equal num_layers * 8.  Synchronises the
+ * device. */
+ESM_API esm_status esm_encoder_get_fp4_scales(const esm_encoder_t* h, float* host_buf, size_t n);
 
 /* ---- masked-LM head (the step after the encoder) ----
  * The mlqm.cn walkthrough loads the model as AutoModelForMaskedLM and the BioNeMo ESM-2
@@ -359,18 +368,25 @@ ESM_API esm_status esm_op_attention_noalloc(const void* qkv, const int32_t* cu_s
  *   (atom (r / 128, k / 64) at ((r / 128) * (cols / 64) + k / 64) * 512, row r and 16-value block
  *   b inside it at (r % 32) * 16 + ((r % 128) / 32) * 4 + b), amax and scale device float scalars
  *   (overwritten: the tensor's max |x| and S).  Two kernels (amax, then codes and scales).
- * esm_op_gemm_nvfp4: out device float32 [M, N] = (A B^T) / (a_scale b_scale) + bias for NVFP4
- *   operands from esm_op_quantize_nvfp4 (A [M, K], B [N, K]; a_scale, b_scale their device
- *   tensor scales; bias device bf16 [N] or NULL); M % 128, N % 128, K % 256 all 0 (else
+ * esm_op_gemm_nvfp4: v = (A B^T) / (a_scale b_scale) + bias for NVFP4 operands from
+ *   esm_op_quantize_nvfp4 (A [M, K], B [N, K]; a_scale, b_scale their device tensor scales;
+ *   bias device bf16 [N] or NULL), then the epilogue an FP4 layer uses:
+ *     ESM_EPI_BIAS_F32  out device float32 [M, N] = v;
+ *     ESM_EPI_RESIDUAL  out device float32 [M, N] += v;
+ *     ESM_EPI_GELU      out device bf16 [M, N] = GELU(v);
+ *     ESM_EPI_QKV_ROPE  out device bf16 [M, N] = v with RoPE on the q and k columns at the
+ *                       row's position pos_id[row] (device int32 [M], clamped to the handle's
+ *                       max_positions); N must equal 3 * hidden of the handle.
+ *   pos_id is ignored by the other epilogues.  M % 128, N % 128, K % 256 all 0 (else
  *   ESM_ERR_INVALID_ARG).  tcgen05.mma kind::mxf4nvf4 with block scaling (the E4M3 block scales
- *   multiply on the tensor core).  Needs an ESM_BF16 or ESM_FP8_E4M3 handle (for its error word
- *   and tensor-map cache). */
+ *   multiply on the tensor core).  Needs an ESM_BF16 or ESM_FP8_E4M3 handle (for its error word,
+ *   tensor-map cache and RoPE table). */
 ESM_API esm_status esm_op_quantize_nvfp4(esm_encoder_t* h, const void* x, int rows, int cols, uint8_t* codes,
                                          uint8_t* scales, float* amax, float* scale, esm_stream_t stream);
-ESM_API esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, const uint8_t* a_codes, const uint8_t* a_scales,
-                                     const float* a_scale, const uint8_t* b_codes, const uint8_t* b_scales,
-                                     const float* b_scale, const void* bias, float* out, int M, int N, int K,
-                                     esm_stream_t stream);
+ESM_API esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, esm_epilogue epi, const uint8_t* a_codes,
+                                     const uint8_t* a_scales, const float* a_scale, const uint8_t* b_codes,
+                                     const uint8_t* b_scales, const float* b_scale, const void* bias,
+                                     const int32_t* pos_id, void* out, int M, int N, int K, esm_stream_t stream);
 
 /* ---- FP8 delayed-scaling state (ESM_FP8_E4M3 handles) ----
  * Layout, float32: for each layer l and each of the 8 quantised tensors k in the order

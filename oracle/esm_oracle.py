@@ -184,7 +184,8 @@ def fp8_quantised_weights(w: Dict[str, np.ndarray], fp8_scales: Dict[str, float]
 def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], heads: int,
                   eps: float = LN_EPS, rope_base: float = ROPE_BASE, n_keys: Optional[int] = None,
                   fp8_scales: Optional[Dict[str, float]] = None, amax_out: Optional[Dict[str, float]] = None,
-                  bf16_attention: bool = False, weights_quantised: bool = False):
+                  bf16_attention: bool = False, weights_quantised: bool = False,
+                  fp4_scales: Optional[Dict[str, float]] = None):
     """One pre-LN encoder layer on one sequence x[L, d] (float64).
 
     y = LN1(x); [q|k|v] = y Wqkv^T + bqkv; RoPE on q, k; o = attention(q, k, v);
@@ -195,13 +196,22 @@ def encoder_layer(x: np.ndarray, pos: np.ndarray, w: Dict[str, np.ndarray], head
     operand before quantisation.  ``weights_quantised`` says the four weights in ``w`` are
     already fake-quantised with these scales (``fp8_quantised_weights``), so only the
     activations are quantised here.  ``bf16_attention`` rounds the attention operands q, k, v
-    to bfloat16 (the FP8 workload keeps attention in bf16)."""
+    to bfloat16 (the FP8 workload keeps attention in bf16).
+
+    With ``fp4_scales`` (tensor scales S of the eight operands, named as for FP8) every GEMM
+    operand is replaced by its NVFP4 value (``fp4.nvfp4_fake_quant`` along the reduction axis
+    with that S); the activations are the bf16 tensors the layer holds (LayerNorm outputs,
+    attention output, GELU output), so they are rounded to bfloat16 before quantisation."""
     L, d = x.shape
     dh = d // heads
 
     def mm(a, wname, aname):
         wt = w[wname]
-        if fp8_scales is not None:
+        if fp4_scales is not None:
+            from . import fp4
+            a = fp4.nvfp4_fake_quant(bf16_round(a), S=fp4_scales[aname])[0]
+            wt = fp4.nvfp4_fake_quant(wt, S=fp4_scales[wname])[0]
+        elif fp8_scales is not None:
             if amax_out is not None:
                 amax_out[aname] = max(amax_out.get(aname, 0.0), float(np.abs(a).max(initial=0.0)))
                 if not weights_quantised:
@@ -236,18 +246,21 @@ def encode_sequence(tokens: np.ndarray, weights: Dict, heads: int, final_ln: boo
                     emb_scale: float = 1.0, eps: float = LN_EPS, rope_base: float = ROPE_BASE,
                     num_layers: Optional[int] = None, n_keys: Optional[int] = None,
                     fp8_state: Optional[List[Dict[str, float]]] = None,
-                    amax_out: Optional[List[Dict[str, float]]] = None, bf16_attention: bool = False) -> np.ndarray:
+                    amax_out: Optional[List[Dict[str, float]]] = None, bf16_attention: bool = False,
+                    fp4_state: Optional[List[Optional[Dict[str, float]]]] = None) -> np.ndarray:
     """Encode ONE sequence (token ids [L]) through the embedding, the layers and the
-    optional final LayerNorm.  Positions are 0..L-1."""
+    optional final LayerNorm.  Positions are 0..L-1.  ``fp4_state[l]`` (tensor scales, or
+    None) makes layer l an NVFP4 layer."""
     tokens = np.asarray(tokens, dtype=np.int64)
     emb = np.asarray(weights["emb"], dtype=np.float64)
     x = emb_scale * emb[tokens]
     pos = np.arange(len(tokens))
     layers = weights["layers"] if num_layers is None else weights["layers"][:num_layers]
     for li, wl in enumerate(layers):
+        f4 = None if fp4_state is None else fp4_state[li]
         x = encoder_layer(x, pos, _f64_layer(wl), heads, eps, rope_base, n_keys,
-                          None if fp8_state is None else fp8_state[li],
-                          None if amax_out is None else amax_out[li], bf16_attention)
+                          None if (fp8_state is None or f4 is not None) else fp8_state[li],
+                          None if amax_out is None else amax_out[li], bf16_attention, fp4_scales=f4)
     if final_ln:
         x = layer_norm(x, np.asarray(weights["lnf_g"], np.float64), np.asarray(weights["lnf_b"], np.float64), eps)
     return x
@@ -259,7 +272,8 @@ def encode_packed(token_ids: np.ndarray, cu: Sequence[int], weights: Dict, heads
                   num_layers: Optional[int] = None, n_keys: Optional[int] = None,
                   fp8_state: Optional[List[Dict[str, float]]] = None,
                   amax_out: Optional[List[Dict[str, float]]] = None,
-                  bf16_attention: bool = False) -> Dict[int, np.ndarray]:
+                  bf16_attention: bool = False,
+                  fp4_state: Optional[List[Optional[Dict[str, float]]]] = None) -> Dict[int, np.ndarray]:
     """The packed forward: every sequence [cu[i], cu[i+1]) is encoded on its own, with the
     same steps as ``encode_sequence``; the loop runs layer by layer over the sequences so
     that a layer's weights are converted (and, with an FP8 state, fake-quantised with their
@@ -271,14 +285,16 @@ def encode_packed(token_ids: np.ndarray, cu: Sequence[int], weights: Dict, heads
     xs = {i: emb_scale * emb[np.asarray(token_ids[int(cu[i]):int(cu[i + 1])], dtype=np.int64)] for i in idx}
     layers = weights["layers"] if num_layers is None else weights["layers"][:num_layers]
     for li, wl in enumerate(layers):
-        scales = None if fp8_state is None else fp8_state[li]
+        f4 = None if fp4_state is None else fp4_state[li]
+        scales = None if (fp8_state is None or f4 is not None) else fp8_state[li]
         wl64 = _f64_layer(wl)
         pre = scales is not None and amax_out is None
         if pre:
             wl64 = fp8_quantised_weights(wl64, scales)
         for i in idx:
             xs[i] = encoder_layer(xs[i], np.arange(len(xs[i])), wl64, heads, eps, rope_base, n_keys, scales,
-                                  None if amax_out is None else amax_out[li], bf16_attention, weights_quantised=pre)
+                                  None if amax_out is None else amax_out[li], bf16_attention, weights_quantised=pre,
+                                  fp4_scales=f4)
         del wl64
     if final_ln:
         g, b = np.asarray(weights["lnf_g"], np.float64), np.asarray(weights["lnf_b"], np.float64)

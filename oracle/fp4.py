@@ -1,7 +1,7 @@
 """Float64 CPU oracle of FP4 (E2M1) block-scaled quantisation of GEMM operands.
 
-TEST INFRASTRUCTURE ONLY (same rules as ``esm_oracle``).  The CUDA library has no FP4 kernels
-yet; this module fixes what an FP4 layer would compute so that a kernel can be checked
+TEST INFRASTRUCTURE ONLY (same rules as ``esm_oracle``).  This module fixes what an FP4
+operand and an FP4 layer compute, so that the CUDA library's NVFP4 kernels can be checked
 against it.
 
 Source: the mlqm.cn walkthrough ("深入源码NVIDIA ESM-2 TransformerEngine优化的实现原理与技术细节"),
@@ -42,20 +42,23 @@ def e2m1_round(x: np.ndarray) -> np.ndarray:
     return np.copysign(E2M1_VALUES[code], x)
 
 
-def nvfp4_fake_quant(a: np.ndarray, axis: int = -1):
+def nvfp4_fake_quant(a: np.ndarray, axis: int = -1, S: float = None):
     """An operand as a block-scaled FP4 GEMM sees it: blocks of 16 along `axis` (its length a
     multiple of 16).  Returns (dequantised values, per-block E4M3 scales, tensor scale S).
 
-    S = 448 * 6 / amax(a) (1 when a is all zero); block scale sb = E4M3(amax_block / 6 * S);
-    q = E2M1(a * S / sb) (0 for an all-zero block); dequantised a ~ q * sb / S."""
+    S = 448 * 6 / amax(a) (1 when a is all zero), or the given S (a tensor whose amax spans
+    more than the values passed here, e.g. a whole packed batch of which `a` is one sequence);
+    block scale sb = E4M3(amax_block / 6 * S); q = E2M1(a * S / sb) (0 for an all-zero block);
+    dequantised a ~ q * sb / S."""
     a = np.asarray(a, dtype=np.float64)
     x = np.moveaxis(a, axis, -1)
     K = x.shape[-1]
     if K % BLOCK:
         raise ValueError("the blocked axis must be a multiple of 16")
     xb = x.reshape(x.shape[:-1] + (K // BLOCK, BLOCK))
-    amax = float(np.abs(a).max(initial=0.0))
-    S = E4M3_MAX * E2M1_MAX / amax if amax > 0 else 1.0
+    if S is None:
+        amax = float(np.abs(a).max(initial=0.0))
+        S = E4M3_MAX * E2M1_MAX / amax if amax > 0 else 1.0
     bmax = np.abs(xb).max(axis=-1)
     sb = e4m3_round(bmax / E2M1_MAX * S)
     safe = np.where(sb > 0, sb, 1.0)

@@ -553,13 +553,16 @@ def test_layer_precision_rejections():
     from transformer_esm_layer_gb300.binding import EsmEncoder, EsmError
     g = synth.Geometry(num_layers=2, hidden=256, heads=4, ffn=512)
     enc8 = EsmEncoder.from_geometry(g, "fp8")
+    enc8.set_layer_precision(["fp8", "fp4"])             # NVFP4 layers on an FP8 handle
     with pytest.raises(EsmError, match="UNSUPPORTED"):
-        enc8.set_layer_precision(["fp8", "fp4"])         # FP4: no kernels
+        enc8.set_layer_precision(["fp8", "fp32"])
     with pytest.raises(EsmError, match="INVALID_ARG"):
         enc8.set_layer_precision(["fp8"])                # wrong layer count
     enc16 = EsmEncoder.from_geometry(g, "bf16")
     with pytest.raises(EsmError, match="UNSUPPORTED"):
         enc16.set_layer_precision(["bf16", "fp8"])       # FP8 layers need an FP8 handle
+    with pytest.raises(EsmError, match="UNSUPPORTED"):
+        enc16.set_layer_precision(["bf16", "fp4"])       # so do NVFP4 layers
     enc16.set_layer_precision(["bf16", "bf16"])
     with pytest.raises(EsmError, match="UNSUPPORTED"):
         EsmEncoder.from_geometry(g, "fp4")

@@ -71,3 +71,75 @@ def test_zero_blocks_and_axis():
     assert np.array_equal(d0, d1.T)
     with pytest.raises(ValueError):
         F4.nvfp4_fake_quant(np.ones((2, 10)))
+
+
+def test_fp4_layer_tensor_to_scale_mapping(monkeypatch):
+    """The NVFP4 layer of the oracle: each of the eight tensor scales meets exactly the operand
+    of its GEMM (activations as the bf16 tensors the layer holds, weights as given), and the
+    layer output follows an independent torch float64 composition of the recorded quantised
+    operands (LayerNorm, RoPE as a complex rotation, SDPA, exact GELU, residuals)."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(13)
+    L, d, heads, f = 5, 32, 2, 64
+    w = {"ln1_g": 1 + 0.2 * rng.standard_normal(d), "ln1_b": 0.2 * rng.standard_normal(d),
+         "w_qkv": 0.2 * rng.standard_normal((3 * d, d)), "b_qkv": 0.1 * rng.standard_normal(3 * d),
+         "w_o": 0.2 * rng.standard_normal((d, d)), "b_o": 0.1 * rng.standard_normal(d),
+         "ln2_g": 1 + 0.2 * rng.standard_normal(d), "ln2_b": 0.2 * rng.standard_normal(d),
+         "w_1": 0.2 * rng.standard_normal((f, d)), "b_1": 0.1 * rng.standard_normal(f),
+         "w_2": 0.2 * rng.standard_normal((d, f)), "b_2": 0.1 * rng.standard_normal(d)}
+    x = rng.standard_normal((L, d))
+    scales = dict(zip(O.FP8_TENSORS, (3.0, 5.0, 7.0, 11.0, 13.0, 17.0, 19.0, 23.0)))
+    calls = []
+    real = F4.nvfp4_fake_quant
+
+    def recording(a, axis=-1, S=None):
+        out = real(a, axis, S)
+        calls.append((float(S), np.array(a, copy=True), out[0]))
+        return out
+
+    monkeypatch.setattr(F4, "nvfp4_fake_quant", recording)
+    got = O.encoder_layer(x, np.arange(L), w, heads, bf16_attention=True, fp4_scales=scales)
+    monkeypatch.setattr(F4, "nvfp4_fake_quant", real)
+    assert len(calls) == 8
+    by = {s: (a, q) for s, a, q in calls}
+    assert sorted(by) == sorted(scales.values())
+    t = lambda a: torch.as_tensor(np.asarray(a, np.float64))
+    bf = lambda u: u.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    q = lambda name: t(by[scales[name]][1])
+    for name in ("w_qkv", "w_o", "w_1", "w_2"):
+        assert np.array_equal(by[scales[name]][0], w[name]), name
+    X = t(x)
+    y = F.layer_norm(X, (d,), t(w["ln1_g"]), t(w["ln1_b"]), eps=1e-5)
+    assert np.allclose(by[scales["x_qkv"]][0], bf(y).numpy(), rtol=0, atol=0)
+    qkv = q("x_qkv") @ q("w_qkv").T + t(w["b_qkv"])
+    dh = d // heads
+    qh, kh, vh = (qkv[:, i * d:(i + 1) * d].reshape(L, heads, dh) for i in range(3))
+    half = dh // 2
+    theta = 10000.0 ** (-2.0 * torch.arange(half, dtype=torch.float64) / dh)
+    rot = torch.polar(torch.ones(L, half, dtype=torch.float64), torch.arange(L, dtype=torch.float64)[:, None] * theta)
+
+    def rope(u):
+        zc = torch.complex(u[..., :half], u[..., half:]) * rot[:, None, :]
+        return torch.cat([zc.real, zc.imag], dim=-1)
+
+    o = F.scaled_dot_product_attention(bf(rope(qh)).transpose(0, 1), bf(rope(kh)).transpose(0, 1),
+                                       bf(vh).transpose(0, 1)).transpose(0, 1).reshape(L, d)
+    assert np.allclose(by[scales["x_o"]][0], bf(o).numpy(), rtol=0, atol=1e-12)
+    X = X + q("x_o") @ q("w_o").T + t(w["b_o"])
+    z = F.layer_norm(X, (d,), t(w["ln2_g"]), t(w["ln2_b"]), eps=1e-5)
+    assert np.allclose(by[scales["x_1"]][0], bf(z).numpy(), rtol=0, atol=1e-12)
+    u = F.gelu(q("x_1") @ q("w_1").T + t(w["b_1"]))
+    assert np.allclose(by[scales["x_2"]][0], bf(u).numpy(), rtol=0, atol=1e-12)
+    X = X + q("x_2") @ q("w_2").T + t(w["b_2"])
+    assert np.allclose(got, X.numpy(), rtol=0, atol=1e-12)
+
+
+def test_fp4_given_scale_equals_own_scale():
+    """nvfp4_fake_quant with S given as the tensor's own 448 * 6 / amax is the default."""
+    rng = np.random.default_rng(14)
+    a = rng.standard_normal((3, 64))
+    S = 448.0 * 6.0 / np.abs(a).max()
+    d0, s0, S0 = F4.nvfp4_fake_quant(a)
+    d1, s1, S1 = F4.nvfp4_fake_quant(a, S=S)
+    assert S0 == S1 and np.array_equal(d0, d1) and np.array_equal(s0, s1)

@@ -34,7 +34,7 @@ EXPORTS = ("esm_encoder_create", "esm_encoder_destroy", "esm_encoder_workspace_s
            "esm_op_layernorm_backward_workspace_size", "esm_op_layernorm_backward", "esm_op_attention_train",
            "esm_op_attention_backward_workspace_size", "esm_op_attention_backward",
            "esm_encoder_lm_head_backward_workspace_size", "esm_encoder_lm_head_backward",
-           "esm_op_quantize_nvfp4", "esm_op_gemm_nvfp4", "esm_status_string")
+           "esm_op_quantize_nvfp4", "esm_op_gemm_nvfp4", "esm_encoder_get_fp4_scales", "esm_status_string")
 PROFILE_CLASSES = ("gemm_qkv", "attention", "gemm_oproj", "gemm_fc1", "gemm_fc2", "layernorm", "other",
                    "gemm_backward")
 
@@ -119,7 +119,8 @@ def load_library() -> ctypes.CDLL:
         "esm_encoder_get_profile": (i32, [vp, ctypes.POINTER(EsmProfile), i32]),
         "esm_op_attention_noalloc": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "esm_op_quantize_nvfp4": (i32, [vp, vp, i32, i32, vp, vp, vp, vp, vp]),
-        "esm_op_gemm_nvfp4": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
+        "esm_encoder_get_fp4_scales": (i32, [vp, ctypes.POINTER(ctypes.c_float), sz]),
+        "esm_op_gemm_nvfp4": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
         "esm_op_layernorm_e4m3": (i32, [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp]),
         "esm_encoder_debug_wait_timeout": (i32, [vp, i32, vp]),
         "esm_op_gemm_fp8": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
@@ -549,17 +550,20 @@ class EsmEncoder:
                                                    _ptr(amax), _ptr(scale), _stream_ptr(stream)), "esm_op_quantize_nvfp4")
         return codes, scales, amax, scale
 
-    def op_gemm_nvfp4(self, a, b, bias=None, out=None, stream=None):
+    def op_gemm_nvfp4(self, a, b, bias=None, out=None, epi="bias_f32", pos_id=None, stream=None):
         """esm_op_gemm_nvfp4 of two operands returned by op_quantize_nvfp4 (A [M, K], B [N, K]):
-        float32 [M, N] = (A B^T) / (S_A S_B) + bias."""
+        v = (A B^T) / (S_A S_B) + bias, then the epilogue `epi` ("bias_f32": float32 out = v;
+        "residual": float32 out += v; "gelu": bf16 out = GELU(v); "qkv_rope": bf16 out = v with
+        RoPE at the rows' positions pos_id)."""
         import torch
         (ac, asf, _, asc), (bc, bsf, _, bsc) = a, b
         M, N, K = ac.shape[0], bc.shape[0], 2 * ac.shape[1]
         if out is None:
-            out = torch.empty(M, N, dtype=torch.float32, device=ac.device)
-        self._raise(self.lib.esm_op_gemm_nvfp4(self.handle, _ptr(ac), _ptr(asf), _ptr(asc), _ptr(bc), _ptr(bsf),
-                                               _ptr(bsc), _ptr(bias), _ptr(out), M, N, K, _stream_ptr(stream)),
-                    "esm_op_gemm_nvfp4")
+            dt = torch.float32 if epi in ("bias_f32", "residual") else torch.bfloat16
+            out = torch.zeros(M, N, dtype=dt, device=ac.device)
+        self._raise(self.lib.esm_op_gemm_nvfp4(self.handle, EPILOGUES[epi], _ptr(ac), _ptr(asf), _ptr(asc), _ptr(bc),
+                                               _ptr(bsf), _ptr(bsc), _ptr(bias), _ptr(pos_id), _ptr(out), M, N, K,
+                                               _stream_ptr(stream)), "esm_op_gemm_nvfp4")
         return out
 
     def set_profiling(self, enable: bool):
@@ -587,6 +591,14 @@ class EsmEncoder:
         buf = np.ascontiguousarray(buf, dtype=np.float32)
         self._raise(self.lib.esm_encoder_set_fp8_state(self.handle, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
                                                        buf.size), "esm_encoder_set_fp8_state")
+
+    def fp4_scales(self) -> np.ndarray:
+        """[num_layers, 8] NVFP4 tensor scales of the last forward's FP4 layers (tensor order
+        x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2; zero for other layers)."""
+        buf = np.zeros(self.num_layers * 8, dtype=np.float32)
+        self._raise(self.lib.esm_encoder_get_fp4_scales(self.handle, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                                        buf.size), "esm_encoder_get_fp4_scales")
+        return buf.reshape(self.num_layers, 8)
 
     def fp8_scales(self, buf: Optional[np.ndarray] = None) -> np.ndarray:
         """[num_layers, 8] scales from a state buffer (tensor order x_qkv, w_qkv, x_o, w_o, x_1, w_1, x_2, w_2)."""

@@ -53,8 +53,8 @@ struct MapKeyHash {
 };
 
 struct WsLayout {
-  size_t pos, seg, seg_start, seg_qlen, seg_klen, work, work_count, x, y, qkv, o, u, wq, ln_stats, ln_fold, stage_tok,
-      stage_cu, total;
+  size_t pos, seg, seg_start, seg_qlen, seg_klen, work, work_count, x, y, qkv, o, u, wq, fp4, ln_stats, ln_fold,
+      stage_tok, stage_cu, total;
   int max_items;
 };
 
@@ -68,8 +68,9 @@ struct esm_encoder {
   int num_sms = 0;
   unsigned* d_err = nullptr;     // device error word
   float2* d_rope = nullptr;      // [16][max_positions][2] (cos, sin)
-  std::vector<uint8_t> layer_fp8;  // per layer: 1 = E4M3 GEMMs (FP8 handles only)
+  std::vector<uint8_t> layer_fp8;  // per layer: 1 = E4M3 GEMMs, 2 = NVFP4 GEMMs (FP8 handles only)
   float* d_fp8 = nullptr;        // scales [L*8] | history [L*8*len] | amax [L*8]
+  float* d_fp4 = nullptr;        // NVFP4 tensor scales of the last forward [L*8] | amax [L*8]
   size_t fp8_floats = 0;
   // Tensor-map cache.  When it grows past its cap the current generation is retired, not
   // freed: maps handed out earlier in the same call stay valid until the next turnover.
@@ -141,6 +142,10 @@ struct esm_encoder {
     L.o = take(act_bytes() * T * d);
     L.u = take(act_bytes() * T * f);
     L.wq = cfg.precision == ESM_FP8_E4M3 ? take(3 * d * d + d * d + 2 * d * f) : take(0);
+    // NVFP4 layers (FP8 handles): one activation operand of up to [T rounded up to 128, ffn]
+    // (codes and block scales); its weights reuse the E4M3 weight region
+    const size_t tp = (T + 127) / 128 * 128;
+    L.fp4 = cfg.precision == ESM_FP8_E4M3 ? take(tp * f / 2 + 256 + tp * f / 16) : take(0);
     // folded LayerNorm (bf16 forward): row statistics per 64-column group, and per layer the
     // QKV and fc1 constants c and b' (fp32 [3d] + [3d] + [f] + [f])
     L.ln_stats = cfg.precision == ESM_BF16 ? take(8 * T * (d / 64)) : take(0);
@@ -316,6 +321,73 @@ esm_status run_gemm(esm_encoder* h, int cls, esm_epilogue epi, const void* A, co
   return cuda_status(e);
 }
 
+// One layer with NVFP4 GEMMs (an FP8 handle's per-layer precision): LayerNorm -> bf16, then
+// every GEMM quantises its bf16 activation and its weight to NVFP4 (current scaling: S from
+// the tensor's amax in this call) and runs the block-scaled tensor-core GEMM with the layer's
+// epilogue; attention stays bf16.  The tensor scales are kept in the handle (get_fp4_scales).
+esm_status run_fp4_layer(esm_encoder* h, const esm_weights* w, int l, int T, const WsLayout& L, void* ws,
+                         const PackBuffers& pb, cudaStream_t st) {
+  const esm_config& c = h->cfg;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  float* x = reinterpret_cast<float*>(b + L.x);
+  void* y = b + L.y;
+  void* qkv = b + L.qkv;
+  void* o = b + L.o;
+  void* u = b + L.u;
+  const int d = c.hidden, f = c.ffn, H = c.heads;
+  const int tp = (T + 127) / 128 * 128;
+  const size_t nf = (size_t)c.num_layers * kNumFp8Tensors;
+  float* sc = h->d_fp4 + (size_t)l * kNumFp8Tensors;
+  float* am = h->d_fp4 + nf + (size_t)l * kNumFp8Tensors;
+  uint8_t* a_codes = b + L.fp4;
+  uint8_t* a_sf = a_codes + align256((size_t)tp * f / 2);
+  uint8_t* w_codes = b + L.wq;
+  auto gemm = [&](int cls, int epi, const void* act, int K, const void* wt, int N, int sx, int sw, const void* bias,
+                  void* out) -> esm_status {
+    uint8_t* w_sf = w_codes + align256((size_t)N * K / 2);
+    {
+      ProfScope _ps(h, P_OTHER, st, 4);
+      if (launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(act), tp, T, K, a_codes, a_sf, am + sx, sc + sx,
+                                st) != cudaSuccess ||
+          launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(wt), N, N, K, w_codes, w_sf, am + sw, sc + sw,
+                                st) != cudaSuccess)
+        return ESM_ERR_CUDA;
+    }
+    const CUtensorMap* ma = h->map(a_codes, (uint64_t)tp, (uint64_t)K / 2, 128, 1);
+    const CUtensorMap* mb = h->map(w_codes, (uint64_t)N, (uint64_t)K / 2, 128, 1);
+    if (!ma || !mb) return ESM_ERR_CUDA;
+    Fp4Epi ea{};
+    ea.bias = bias;
+    ea.out = out;
+    ea.rows_valid = T;
+    ea.pos_id = pb.pos_id;
+    ea.rope = h->d_rope;
+    ea.rope_cols = 2 * d;
+    ea.max_pos = c.max_positions;
+    cudaError_t e;
+    PROF(h, cls, st, 1, e = launch_gemm_nvfp4(epi, ma, mb, a_sf, w_sf, sc + sx, sc + sw, ea, tp, N, K, h->d_err, st));
+    return cuda_status(e);
+  };
+  esm_status s;
+  PROF(h, P_LN, st, 1,
+       launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, st));
+  if ((s = gemm(P_QKV, kFp4QkvRope, y, d, w->w_qkv[l], 3 * d, X_QKV, W_QKV, w->b_qkv[l], qkv)) != ESM_OK) return s;
+  {
+    ProfScope _ps(h, P_ATTN, st, 1);
+    const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
+    if (!tq) return ESM_ERR_CUDA;
+    if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st) != cudaSuccess)
+      return ESM_ERR_CUDA;
+  }
+  if ((s = gemm(P_OPROJ, kFp4Residual, o, d, w->w_o[l], d, X_O, W_O, w->b_o[l], x)) != ESM_OK) return s;
+  PROF(h, P_LN, st, 1,
+       launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, st));
+  if ((s = gemm(P_FC1, kFp4Gelu, y, d, w->w_1[l], f, X_1, W_1, w->b_1[l], u)) != ESM_OK) return s;
+  return gemm(P_FC2, kFp4Residual, u, f, w->w_2[l], d, X_2, W_2, w->b_2[l], x);
+}
+
 // The layer stack over an already indexed batch (pack buffers filled, x = embedding).
 esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items, const WsLayout& L, void* ws,
                       void* out, bool padded, cudaStream_t st) {
@@ -356,7 +428,11 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
     }
   }
   for (int l = 0; l < c.num_layers; ++l) {
-    const bool fp8 = c.precision == ESM_FP8_E4M3 && h->layer_fp8[l];
+    const bool fp8 = c.precision == ESM_FP8_E4M3 && h->layer_fp8[l] == 1;
+    if (c.precision == ESM_FP8_E4M3 && h->layer_fp8[l] == 2) {
+      if ((s = run_fp4_layer(h, w, l, T, L, ws, pb, st)) != ESM_OK) return s;
+      continue;
+    }
     float* sc = h->fp8_scale() + (size_t)l * kNumFp8Tensors;
     float* am = h->fp8_amax() + (size_t)l * kNumFp8Tensors;
     uint8_t* wq_qkv = b + L.wq;
@@ -817,10 +893,12 @@ esm_status esm_encoder_create(const esm_config* cfg, esm_encoder_t** out) {
   h->fp8_floats = nf * (1 + cfg->amax_history_len);
   bool ok = cudaMalloc(&h->d_err, sizeof(unsigned)) == cudaSuccess &&
             cudaMalloc(&h->d_rope, sizeof(float2) * (size_t)cfg->max_positions * kRopeMaxHalf) == cudaSuccess &&
-            cudaMalloc(&h->d_fp8, sizeof(float) * (h->fp8_floats + nf + 1)) == cudaSuccess;
+            cudaMalloc(&h->d_fp8, sizeof(float) * (h->fp8_floats + nf + 1)) == cudaSuccess &&
+            cudaMalloc(&h->d_fp4, sizeof(float) * (2 * nf + 1)) == cudaSuccess;
   if (ok) {
     ok = cudaMemset(h->d_err, 0, sizeof(unsigned)) == cudaSuccess &&
-         cudaMemset(h->d_fp8, 0, sizeof(float) * (h->fp8_floats + nf + 1)) == cudaSuccess;
+         cudaMemset(h->d_fp8, 0, sizeof(float) * (h->fp8_floats + nf + 1)) == cudaSuccess &&
+         cudaMemset(h->d_fp4, 0, sizeof(float) * (2 * nf + 1)) == cudaSuccess;
     std::vector<float> ones(nf, 1.0f);
     if (ok && nf) ok = cudaMemcpy(h->d_fp8, ones.data(), nf * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
     if (ok) {
@@ -841,6 +919,7 @@ void esm_encoder_destroy(esm_encoder_t* h) {
   if (h->d_err) cudaFree(h->d_err);
   if (h->d_rope) cudaFree(h->d_rope);
   if (h->d_fp8) cudaFree(h->d_fp8);
+  if (h->d_fp4) cudaFree(h->d_fp4);
   h->drain_events();
   for (cudaEvent_t e : h->event_pool) cudaEventDestroy(e);
   delete h;
@@ -872,18 +951,24 @@ static size_t lm_head_bytes(const esm_encoder* h, int T, size_t* off_z2, size_t*
   return 2 * act + (((size_t)T * 4 + 255) & ~size_t(255));
 }
 
+esm_status esm_encoder_get_fp4_scales(const esm_encoder_t* h, float* host_buf, size_t n) {
+  if (!h || !host_buf || n != (size_t)h->cfg.num_layers * kNumFp8Tensors) return ESM_ERR_INVALID_ARG;
+  if (h->cfg.precision != ESM_FP8_E4M3) return ESM_ERR_UNSUPPORTED;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ESM_ERR_CUDA;
+  return cuda_status(cudaMemcpy(host_buf, h->d_fp4, n * sizeof(float), cudaMemcpyDeviceToHost));
+}
+
 esm_status esm_encoder_set_layer_precision(esm_encoder_t* h, const esm_precision* per_layer, int num_layers) {
   if (!h || !per_layer || num_layers != h->cfg.num_layers) return ESM_ERR_INVALID_ARG;
   std::vector<uint8_t> v((size_t)num_layers);
   for (int l = 0; l < num_layers; ++l) {
     const esm_precision p = per_layer[l];
-    if (p == ESM_FP4_E2M1) return ESM_ERR_UNSUPPORTED;
     if (h->cfg.precision == ESM_FP8_E4M3) {
-      if (p != ESM_FP8_E4M3 && p != ESM_BF16) return ESM_ERR_UNSUPPORTED;
+      if (p != ESM_FP8_E4M3 && p != ESM_BF16 && p != ESM_FP4_E2M1) return ESM_ERR_UNSUPPORTED;
     } else if (p != h->cfg.precision) {
       return ESM_ERR_UNSUPPORTED;
     }
-    v[l] = p == ESM_FP8_E4M3 ? 1 : 0;
+    v[l] = p == ESM_FP8_E4M3 ? 1 : p == ESM_FP4_E2M1 ? 2 : 0;
   }
   h->layer_fp8 = v;
   return ESM_OK;
@@ -1182,16 +1267,26 @@ esm_status esm_op_quantize_nvfp4(esm_encoder_t* h, const void* x, int rows, int 
       !aligned(amax, 4) || !aligned(scale, 4))
     return ESM_ERR_INVALID_ARG;
   if (rows == 0) return ESM_OK;
-  return cuda_status(launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(x), rows, cols, codes, scales, amax,
+  return cuda_status(launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(x), rows, rows, cols, codes, scales, amax,
                                            scale, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, const uint8_t* a_codes, const uint8_t* a_scales, const float* a_scale,
-                             const uint8_t* b_codes, const uint8_t* b_scales, const float* b_scale, const void* bias,
-                             float* out, int M, int N, int K, esm_stream_t stream) {
+esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, esm_epilogue epi, const uint8_t* a_codes, const uint8_t* a_scales,
+                             const float* a_scale, const uint8_t* b_codes, const uint8_t* b_scales,
+                             const float* b_scale, const void* bias, const int32_t* pos_id, void* out, int M, int N,
+                             int K, esm_stream_t stream) {
   if (!h || !a_codes || !a_scales || !a_scale || !b_codes || !b_scales || !b_scale || !out) return ESM_ERR_INVALID_ARG;
   if (h->cfg.precision == ESM_FP32) return ESM_ERR_UNSUPPORTED;
   if (M < 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 256) return ESM_ERR_INVALID_ARG;
+  int mode;
+  switch (epi) {
+    case ESM_EPI_BIAS_F32: mode = kFp4F32; break;
+    case ESM_EPI_RESIDUAL: mode = kFp4Residual; break;
+    case ESM_EPI_GELU: mode = kFp4Gelu; break;
+    case ESM_EPI_QKV_ROPE: mode = kFp4QkvRope; break;
+    default: return ESM_ERR_INVALID_ARG;
+  }
+  if (mode == kFp4QkvRope && (!pos_id || N != 3 * h->cfg.hidden)) return ESM_ERR_INVALID_ARG;
   if (!aligned(a_codes, 16) || !aligned(b_codes, 16) || !aligned(a_scales, 16) || !aligned(b_scales, 16) ||
       !aligned(out, 16) || (bias && !aligned(bias, 16)))
     return ESM_ERR_INVALID_ARG;
@@ -1199,8 +1294,16 @@ esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, const uint8_t* a_codes, const uin
   const CUtensorMap* ma = h->map(a_codes, (uint64_t)M, (uint64_t)K / 2, 128, 1);
   const CUtensorMap* mb = h->map(b_codes, (uint64_t)N, (uint64_t)K / 2, 128, 1);
   if (!ma || !mb) return ESM_ERR_CUDA;
-  return cuda_status(launch_gemm_nvfp4(ma, mb, a_scales, b_scales, a_scale, b_scale, bias, false, out, M, N, K,
-                                       h->d_err, reinterpret_cast<cudaStream_t>(stream)));
+  Fp4Epi ea{};
+  ea.bias = bias;
+  ea.out = out;
+  ea.rows_valid = M;
+  ea.pos_id = pos_id;
+  ea.rope = h->d_rope;
+  ea.rope_cols = 2 * h->cfg.hidden;
+  ea.max_pos = h->cfg.max_positions;
+  return cuda_status(launch_gemm_nvfp4(mode, ma, mb, a_scales, b_scales, a_scale, b_scale, ea, M, N, K, h->d_err,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,

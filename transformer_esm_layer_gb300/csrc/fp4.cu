@@ -85,10 +85,12 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __nv_bfloat16* __
   if ((threadIdx.x & 31) == 0) atomic_max_nonneg(amax, m);
 }
 
-// One thread per block of 16 values: the block's E4M3 scale and its eight code bytes.
-__global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int K,
-                                                             const float* amax, uint8_t* __restrict__ codes,
-                                                             uint8_t* __restrict__ sf, float* scale_out) {
+// One thread per block of 16 values: the block's E4M3 scale and its eight code bytes.  Rows
+// from rows_valid to rows (the padding to a multiple of 128) quantise as zeros.
+__global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows,
+                                                             int rows_valid, int K, const float* amax,
+                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                             float* scale_out) {
   const size_t blk = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   const int kb = K / 16;
   const float a = __ldg(amax);
@@ -96,9 +98,9 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
   if (blk == 0 && scale_out) *scale_out = S;
   if (blk >= (size_t)rows * kb) return;
   const int row = (int)(blk / kb), k16 = (int)(blk % kb);
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * K + (size_t)k16 * 16);
   float v[16];
-  {
+  if (row < rows_valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * K + (size_t)k16 * 16);
     float f[8];
     bf16x8(__ldg(src), f);
 #pragma unroll
@@ -106,6 +108,9 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
     bf16x8(__ldg(src + 1), f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[8 + i] = f[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
   }
   float bmax = 0.f;
 #pragma unroll
@@ -147,12 +152,16 @@ __host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <bool BIAS_F32>
+// Epilogue: v = acc / (S_A S_B) + bias for the rows below ea.rows_valid, then
+//   F32      out fp32 [M, N] = v;          RESIDUAL  out fp32 [M, N] += v;
+//   GELU     out bf16 [M, N] = GELU(v) (exact-erf, A&S 7.1.26);
+//   QKV_ROPE out bf16 [M, N] = v, with RoPE on the 64-column heads below ea.rope_cols at the
+//            row's position (the library's (cos, sin) table).
+template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, const float* a_scale,
-                      const float* b_scale, const void* __restrict__ bias, float* __restrict__ out, int M, int N,
-                      int K, unsigned* err) {
+                      const float* b_scale, Fp4Epi ea, int M, int N, int K, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Fp4Smem* sm = reinterpret_cast<Fp4Smem*>(base + BAR_OFF);
@@ -242,33 +251,75 @@ __global__ void __launch_bounds__(THREADS, 1)
     mma_commit(&sm->done);
   }
   __syncwarp();
-  // ---- epilogue (all four warps): row 32 w + lane of the tile, 128 fp32 columns
+  // ---- epilogue (all four warps): row 32 w + lane of the tile, 128 columns in two heads of 64
   const bool ok = mbar_wait_warp(&sm->done, 0);
   if (!ok && lane == 0) latch_error(err, ERRBIT_TIMEOUT);
   if (ok && !sm->abort) {
     tc_fence_after();
     const float inv = 1.f / (__ldg(a_scale) * __ldg(b_scale));
     const int row = m0 + warp * 32 + lane;
+    const bool live = row < ea.rows_valid;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    float4 cs[EPI == kFp4QkvRope ? 16 : 1];
+    if constexpr (EPI == kFp4QkvRope) {
+      int p = live ? __ldg(ea.pos_id + row) : 0;
+      p = p < 0 ? 0 : (p >= ea.max_pos ? ea.max_pos - 1 : p);
+      const float4* tab = reinterpret_cast<const float4*>(ea.rope) + p;  // group g at g * max_pos
+#pragma unroll
+      for (int g = 0; g < 16; ++g) cs[g] = __ldg(tab + (size_t)g * ea.max_pos);
+    }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      float v[32];
-      tmem_ld32(tmem + lane_off + (uint32_t)c, v);
-      if (row < M) {
-        float4* dst = reinterpret_cast<float4*>(out + (size_t)row * N + n0 + c);
+    for (int h = 0; h < BN; h += 64) {
+      float v[64];
+      {
+        float t0[32], t1[32];
+        tmem_ld32(tmem + lane_off + (uint32_t)h, t0);
+        tmem_ld32(tmem + lane_off + (uint32_t)h + 32, t1);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float b4[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int col = n0 + c + 4 * j + i;
-            b4[i] = bias == nullptr ? 0.f
-                                    : (BIAS_F32 ? __ldg(static_cast<const float*>(bias) + col)
-                                                : __bfloat162float(static_cast<const __nv_bfloat16*>(bias)[col]));
-          }
-          dst[j] = make_float4(v[4 * j] * inv + b4[0], v[4 * j + 1] * inv + b4[1], v[4 * j + 2] * inv + b4[2],
-                               v[4 * j + 3] * inv + b4[3]);
+        for (int i = 0; i < 32; ++i) {
+          v[i] = t0[i];
+          v[32 + i] = t1[i];
         }
+      }
+      if (!live) continue;
+      const int col0 = n0 + h;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float b = ea.bias ? __bfloat162float(static_cast<const __nv_bfloat16*>(ea.bias)[col0 + i]) : 0.f;
+        v[i] = v[i] * inv + b;
+      }
+      if constexpr (EPI == kFp4F32 || EPI == kFp4Residual) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ea.out) + (size_t)row * N + col0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if constexpr (EPI == kFp4Residual) {
+            const float4 x = dst[j];
+            o.x += x.x; o.y += x.y; o.z += x.z; o.w += x.w;
+          }
+          dst[j] = o;
+        }
+      } else {
+        if constexpr (EPI == kFp4Gelu) {
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) gelu2_as7126(v[i], v[i + 1]);
+        } else {
+          if (col0 < ea.rope_cols) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {  // pair (i, i + 32) of the head turns by its angle
+              const float4 t = cs[i >> 1];
+              const float c = (i & 1) ? t.z : t.x, sn = (i & 1) ? t.w : t.y;
+              const float x = v[i], y = v[32 + i];
+              v[i] = x * c - y * sn;
+              v[32 + i] = y * c + x * sn;
+            }
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ea.out) + (size_t)row * N + col0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                              pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
       }
     }
   }
@@ -282,43 +333,52 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                                  float* amax_scratch, float* scale, cudaStream_t st) {
+cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int rows_valid, int K, uint8_t* codes,
+                                  uint8_t* sf, float* amax, float* scale, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(float), st);
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
-  const size_t n8 = (size_t)rows * K / 8;
-  int grid = (int)((n8 + 255) / 256);
-  if (grid > 4096) grid = 4096;
-  nvfp4_amax_kernel<<<grid, 256, 0, st>>>(x, n8, amax_scratch);
+  const size_t n8 = (size_t)rows_valid * K / 8;
+  if (n8 > 0) {
+    int grid = (int)((n8 + 255) / 256);
+    if (grid > 4096) grid = 4096;
+    nvfp4_amax_kernel<<<grid, 256, 0, st>>>(x, n8, amax);
+  }
   const size_t blocks = (size_t)rows * (K / 16);
-  nvfp4_quantize_kernel<<<(unsigned)((blocks + 255) / 256), 256, 0, st>>>(x, rows, K, amax_scratch, codes, sf, scale);
+  nvfp4_quantize_kernel<<<(unsigned)((blocks + 255) / 256), 256, 0, st>>>(x, rows, rows_valid, K, amax, codes, sf,
+                                                                         scale);
   return cudaGetLastError();
 }
 
 int gemm_nvfp4_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_gemm_nvfp4(const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa, const uint8_t* sfb,
-                              const float* a_scale, const float* b_scale, const void* bias, bool bias_f32, float* out,
-                              int M, int N, int K, unsigned* err, cudaStream_t st) {
-  if (M <= 0) return cudaSuccess;
-  static bool configured[2] = {false, false};
-  if (!configured[bias_f32]) {
-    cudaError_t e = bias_f32 ? cudaFuncSetAttribute(gemm_nvfp4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    SMEM_BYTES)
-                             : cudaFuncSetAttribute(gemm_nvfp4_kernel<false>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+template <int EPI>
+static cudaError_t launch_epi(const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa, const uint8_t* sfb,
+                              const float* a_scale, const float* b_scale, const Fp4Epi& ea, int M, int N, int K,
+                              unsigned* err, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_nvfp4_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured[bias_f32] = true;
+    configured = true;
   }
-  const dim3 grid(N / BN, M / BM);
-  if (bias_f32)
-    gemm_nvfp4_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, sfa, sfb, a_scale, b_scale, bias, out, M, N,
-                                                               K, err);
-  else
-    gemm_nvfp4_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, sfa, sfb, a_scale, b_scale, bias, out, M,
-                                                                N, K, err);
+  gemm_nvfp4_kernel<EPI><<<dim3(N / BN, M / BM), THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, sfa, sfb, a_scale, b_scale, ea,
+                                                                            M, N, K, err);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_nvfp4(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa,
+                              const uint8_t* sfb, const float* a_scale, const float* b_scale, const Fp4Epi& ea, int M,
+                              int N, int K, unsigned* err, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  switch (epi) {
+    case kFp4F32: return launch_epi<kFp4F32>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
+    case kFp4Residual: return launch_epi<kFp4Residual>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
+    case kFp4Gelu: return launch_epi<kFp4Gelu>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
+    case kFp4QkvRope: return launch_epi<kFp4QkvRope>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace esm

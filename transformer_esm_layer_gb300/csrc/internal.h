@@ -152,18 +152,29 @@ constexpr int kLnFoldMaxJobs = 96;
 void launch_ln_fold(const LnFoldJob* jobs, int num_jobs, int k, cudaStream_t st);
 
 // ---------------------------------------------------------------- fp4.cu
-// NVFP4 operand of x [rows, K] bf16 (rows % 128 == 0, K % 256 == 0): E2M1 codes [rows, K/2]
-// bytes, E4M3 block scales in 512-byte atoms of 128 rows x 64 values, the tensor scale S and
-// the tensor's amax (device scalars).
-cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                                  float* amax, float* scale, cudaStream_t st);
-// out [M, N] fp32 = (A B^T) / (a_scale b_scale) + bias for NVFP4 operands A [M, K], B [N, K]
-// (tensor maps over the code bytes [rows, K/2] with a 128 x 128 box and the 128-byte swizzle);
+// NVFP4 operand of x [rows_valid, K] bf16, padded with zero rows to `rows` (rows % 128 == 0,
+// K % 256 == 0): E2M1 codes [rows, K/2] bytes, E4M3 block scales in 512-byte atoms of 128 rows
+// x 64 values, the tensor's amax and its scale S = 448 * 6 / amax (device scalars).
+cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int rows_valid, int K, uint8_t* codes,
+                                  uint8_t* sf, float* amax, float* scale, cudaStream_t st);
+// Epilogues of the NVFP4 GEMM (v = acc / (S_A S_B) + bias on rows below rows_valid).
+enum : int { kFp4F32 = 0, kFp4Residual = 1, kFp4Gelu = 2, kFp4QkvRope = 3 };
+struct Fp4Epi {
+  const void* bias;       // bf16 [N] or NULL
+  void* out;              // fp32 (F32, RESIDUAL) or bf16 (GELU, QKV_ROPE) [rows_valid, N]
+  int rows_valid;
+  const int32_t* pos_id;  // QKV_ROPE: [rows_valid]
+  const float2* rope;     // QKV_ROPE: the (cos, sin) table
+  int rope_cols;          // QKV_ROPE: columns below get RoPE
+  int max_pos;
+};
+// out = epilogue((A B^T) / (a_scale b_scale)) for NVFP4 operands A [M, K], B [N, K] (tensor
+// maps over the code bytes [rows, K/2] with a 128 x 128 box and the 128-byte swizzle);
 // M % 128 == 0, N % 128 == 0, K % 256 == 0.
 int gemm_nvfp4_smem_bytes();
-cudaError_t launch_gemm_nvfp4(const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa, const uint8_t* sfb,
-                              const float* a_scale, const float* b_scale, const void* bias, bool bias_f32, float* out,
-                              int M, int N, int K, unsigned* err, cudaStream_t st);
+cudaError_t launch_gemm_nvfp4(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa,
+                              const uint8_t* sfb, const float* a_scale, const float* b_scale, const Fp4Epi& ea, int M,
+                              int N, int K, unsigned* err, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention.cu
 // tcgen05 attention (head_dim 64): tm_qkv is a tensor map over qkv [T, 3d] bf16 with a
