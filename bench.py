@@ -47,9 +47,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--layers", type=int, default=None, help="fewer layers: small case for profiler captures only")
     ap.add_argument("--tokens", type=int, default=None, help="other batch size: small case for captures only")
-    ap.add_argument("--workload", choices=("esm650m", "esm650m_padded", "esm3b_fp8"), default="esm650m",
+    ap.add_argument("--workload", choices=("esm650m", "esm650m_padded", "esm3b_fp8", "esm3b_fp4"), default="esm650m",
                     help="esm650m (the headline), esm650m_padded (same sequences as [B,1024] with a key padding "
-                         "mask), esm3b_fp8 (3B encoder, E4M3 GEMMs, 32768 tokens)")
+                         "mask), esm3b_fp8 (3B encoder, E4M3 GEMMs, 32768 tokens), esm3b_fp4 (the same with NVFP4 "
+                         "GEMMs in every layer)")
     return ap.parse_args()
 
 
@@ -81,6 +82,9 @@ def workload_text(wl) -> str:
     g = wl.geometry
     size = {2560: "ESM-2 3B", 1280: "ESM-2 650M"}.get(g.hidden, "tiny ESM-style")
     prec = {"fp8": "E4M3 GEMMs with per-tensor delayed scaling (history 16)", "fp32": "fp32"}.get(wl.precision, "bf16")
+    if wl.layer_precision and set(wl.layer_precision) == {"fp4"}:
+        prec = ("NVFP4 GEMMs (E2M1 values, E4M3 scale per 16, per-tensor current scaling) in every layer, "
+                "bf16 attention and LayerNorm")
     lengths = (f"lengths {list(wl.lengths)}" if len(wl.lengths) <= 4 else
                "log-normal lengths (median 300, sigma 0.6) clipped to [32,1024]")
     txt = (f"{wl.name}: {size} encoder ({g.num_layers} layers, hidden {g.hidden}, {g.heads} heads, FFN {g.ffn}, "
@@ -176,6 +180,10 @@ def cpu_oracle_sample(wl, w64, seconds: float, prec: str = "bf16", enc=None):
     if prec == "fp8" and enc is not None:
         sc = enc.fp8_scales()
         kw["fp8_state"] = [{k: float(sc[l, i]) for i, k in enumerate(O.FP8_TENSORS)} for l in range(sc.shape[0])]
+        if wl.layer_precision and "fp4" in wl.layer_precision:
+            s4 = enc.fp4_scales()  # the last forward's scales: the whole batch's amaxes
+            kw["fp4_state"] = [({k: float(s4[l, i]) for i, k in enumerate(O.FP8_TENSORS)} if p == "fp4" else None)
+                               for l, p in enumerate(wl.layer_precision)]
     done, toks = [], 0
     t0 = time.perf_counter()
     for i in range(len(wl.lengths)):
@@ -315,6 +323,9 @@ def measure_forward(wl, dev, args, w_np=None, want_e2e=False, world=1, rank=0, g
     tok, cu = packed_inputs(tok_np, wl.lengths, device=dev)
     T, B, maxL = wl.total_tokens, len(wl.lengths), max(wl.lengths)
     enc = EsmEncoder.from_geometry(g, prec, final_ln=wl.final_ln)
+    fp4 = bool(wl.layer_precision) and set(wl.layer_precision) == {"fp4"}
+    if wl.layer_precision:
+        enc.set_layer_precision(list(wl.layer_precision))
     stream = torch.cuda.current_stream()
     torch.cuda.reset_peak_memory_stats(dev)
     if padded:
@@ -400,8 +411,10 @@ def measure_forward(wl, dev, args, w_np=None, want_e2e=False, world=1, rank=0, g
     for c_ in list(gemm_classes) + ["attention"]:
         m_ = per_kernel[c_]["ms_per_step"]
         per_kernel[c_]["tflops"] = executed[c_] / (m_ / 1e3) / 1e12 if m_ else None
-    # a contraction takes the peak of its own dtype: E4M3 = 2 x the measured bf16 (nominal 4.5 / 2.25)
-    dtype_mult = 2.0 if prec == "fp8" else 1.0
+    # a contraction takes the peak of its own dtype: E4M3 = 2 x the measured bf16 (nominal 4.5 / 2.25),
+    # NVFP4 = 6 x (nominal 13.5 / 2.25)
+    dtype_mult = 6.0 if fp4 else (2.0 if prec == "fp8" else 1.0)
+    peak_note = {6.0: " x 6 (NVFP4/bf16 nominal ratio)", 2.0: " x 2 (E4M3/bf16 nominal ratio)", 1.0: ""}[dtype_mult]
     peak_burst = float(pk["bf16_tflops"]) * dtype_mult
     peak_sust = float(pk["bf16_tflops_sustained"]) * dtype_mult
     roofline = None
@@ -412,10 +425,12 @@ def measure_forward(wl, dev, args, w_np=None, want_e2e=False, world=1, rank=0, g
         gemm_flops = sum(executed[c_] for c_ in gemm_classes)
         gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12
         traffic = gemm_traffic_record()
-        roofline = {"bound": "tensor", "kernel": f"gemm_tc_kernel (tcgen05 {'e4m3' if prec == 'fp8' else 'bf16'}, "
-                                                  "all four linear maps)",
+        kname = ("gemm_nvfp4_kernel (tcgen05 block-scaled E2M1, all four linear maps; the operand "
+                 "quantisation kernels are timed under 'other')" if fp4 else
+                 f"gemm_tc_kernel (tcgen05 {'e4m3' if prec == 'fp8' else 'bf16'}, all four linear maps)")
+        roofline = {"bound": "tensor", "kernel": kname,
                     "achieved": gemm_tflops, "peak": peak_burst, "unit": "TFLOP/s", "frac": gemm_tflops / peak_burst,
-                    "peak_source": f"bf16_tflops (burst), {pk_src}" + (" x 2 (E4M3/bf16 nominal ratio)" if prec == "fp8" else ""),
+                    "peak_source": f"bf16_tflops (burst), {pk_src}" + peak_note,
                     "peak_sustained": peak_sust, "frac_vs_sustained": gemm_tflops / peak_sust,
                     "flops_per_launch": gemm_flops / gemm_launches if gemm_launches else None,
                     "avg_launch_ms": gemm_ms / gemm_launches if gemm_launches else None,
@@ -433,12 +448,13 @@ def measure_forward(wl, dev, args, w_np=None, want_e2e=False, world=1, rank=0, g
            "steps": args.steps, "tflops": total_flops * (global_tokens / T) / (ms_step / 1e3) / 1e12,
            "mfu_vs_burst_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_burst,
            "mfu_vs_sustained_peak": total_flops / (ms_step / 1e3) / 1e12 / peak_sust,
-           "peak_dtype": "e4m3 (2 x measured bf16)" if prec == "fp8" else "bf16 (measured)",
+           "peak_dtype": ("nvfp4 (6 x measured bf16)" if fp4 else
+                          "e4m3 (2 x measured bf16)" if prec == "fp8" else "bf16 (measured)"),
            "algorithmic_gflop_per_step_per_gpu": total_flops / 1e9,
            "padded_over_packed_flops": (sum(executed.values()) / total_flops) if padded else None,
            "max_memory_allocated_gb": peak_mem / 2**30, "roofline": roofline, "attention_roofline": attn,
            "per_kernel": per_kernel, "launches_per_step": launches_per_step, "gpu_launches": launches,
-           "clocks": clocks, "dtype": {"fp8": "e4m3", "fp32": "f32"}.get(prec, "bf16"),
+           "clocks": clocks, "dtype": "e2m1" if fp4 else {"fp8": "e4m3", "fp32": "f32"}.get(prec, "bf16"),
            "timing": "CUDA graph replay of the whole forward" if not args.no_graph else "eager launches"}
     state = {"enc": enc, "dw": dw, "tok": tok, "cu": cu, "ws": ws, "out": out, "w_np": w_np, "tok_np": tok_np,
              "T": T, "B": B, "maxL": maxL, "stream": stream, "flops": flops, "total_flops": total_flops,
@@ -632,7 +648,7 @@ def run_ours(args):
             and args.tokens is None:
         del st
         configs = {}
-        for name in ("tiny_fp32", "layer650m", "esm650m_padded", "esm3b_fp8"):
+        for name in ("tiny_fp32", "layer650m", "esm650m_padded", "esm3b_fp8", "esm3b_fp4"):
             try:  # a side measurement: a failure here must not cost the benchmark line
                 wl2 = synth.make_workload(name)
                 reuse = w_np if name == "esm650m_padded" else None  # same model and seed as the headline
@@ -649,7 +665,8 @@ def run_ours(args):
         metric = {"esm650m": METRIC,
                   "esm650m_padded": "ESM-2 650M padded [B,1024] fwd tokens/s (real tokens) on 1 GB300; achieved "
                                     "TFLOP/s vs dense BF16 peak",
-                  "esm3b_fp8": "ESM-2 3B packed FP8 fwd tokens/s on 1 GB300; achieved TFLOP/s vs dense FP8 peak"
+                  "esm3b_fp8": "ESM-2 3B packed FP8 fwd tokens/s on 1 GB300; achieved TFLOP/s vs dense FP8 peak",
+                  "esm3b_fp4": "ESM-2 3B packed NVFP4 fwd tokens/s on 1 GB300; achieved TFLOP/s vs dense FP4 peak"
                   }[args.workload]
         line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": head["ms_per_step_median"],

@@ -17,6 +17,8 @@ Workloads (the sequence lengths include BOS and EOS):
 * ``esm650m_padded`` -- the ``esm650m`` sequences laid out as [B, 1024] with pad id 1.
 * ``esm3b_fp8``   -- the 36-layer 3B encoder (hidden 2560, 40 heads, FFN 10240), 32768
   packed tokens, seed 3.
+* ``esm3b_fp4``   -- the same model and batch with every layer's linear maps in NVFP4
+  (per-layer precision "fp4" on an FP8 encoder).
 
 The geometry follows the ESM-2 model card ("BioNeMo ESM-2", model overview: 650M has 33
 layers, 20 heads, hidden 1280; 3B has 36 layers, 40 heads, hidden 2560) and the NVIDIA
@@ -68,6 +70,7 @@ class Workload:
     seed: int
     lengths: List[int]
     padded_len: Optional[int] = None  # S for the padded [B, S] layout
+    layer_precision: Optional[List[str]] = None  # per-layer GEMM precision on an fp8 encoder
 
     @property
     def total_tokens(self) -> int:
@@ -143,9 +146,10 @@ def make_workload(name: str) -> Workload:
         rng = np.random.default_rng(2)
         return Workload(name, ESM2_650M, "bf16", True, 2, lognormal_lengths(rng, total=16384),
                         padded_len=1024)
-    if name == "esm3b_fp8":
+    if name in ("esm3b_fp8", "esm3b_fp4"):
         rng = np.random.default_rng(3)
-        return Workload(name, ESM2_3B, "fp8", True, 3, lognormal_lengths(rng, total=32768))
+        lp = ["fp4"] * ESM2_3B.num_layers if name == "esm3b_fp4" else None
+        return Workload(name, ESM2_3B, "fp8", True, 3, lognormal_lengths(rng, total=32768), layer_precision=lp)
     raise KeyError(name)
 
 
