@@ -342,15 +342,16 @@ esm_status run_fp4_layer(esm_encoder* h, const esm_weights* w, int l, int T, con
   uint8_t* a_codes = b + L.fp4;
   uint8_t* a_sf = a_codes + align256((size_t)tp * f / 2);
   uint8_t* w_codes = b + L.wq;
-  auto gemm = [&](int cls, int epi, const void* act, int K, const void* wt, int N, int sx, int sw, const void* bias,
-                  void* out) -> esm_status {
+  // act_ready: the kernel that wrote `act` accumulated its amax (from the zero set below)
+  auto gemm = [&](int cls, int epi, const void* act, bool act_ready, int K, const void* wt, int N, int sx, int sw,
+                  const void* bias, void* out, float* out_amax) -> esm_status {
     uint8_t* w_sf = w_codes + align256((size_t)N * K / 2);
     {
       ProfScope _ps(h, P_OTHER, st, 4);
       if (launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(act), tp, T, K, a_codes, a_sf, am + sx, sc + sx,
-                                st) != cudaSuccess ||
+                                act_ready, st) != cudaSuccess ||
           launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(wt), N, N, K, w_codes, w_sf, am + sw, sc + sw,
-                                st) != cudaSuccess)
+                                false, st) != cudaSuccess)
         return ESM_ERR_CUDA;
     }
     const CUtensorMap* ma = h->map(a_codes, (uint64_t)tp, (uint64_t)K / 2, 128, 1);
@@ -364,15 +365,21 @@ esm_status run_fp4_layer(esm_encoder* h, const esm_weights* w, int l, int T, con
     ea.rope = h->d_rope;
     ea.rope_cols = 2 * d;
     ea.max_pos = c.max_positions;
+    ea.amax = out_amax;
     cudaError_t e;
-    PROF(h, cls, st, 1, e = launch_gemm_nvfp4(epi, ma, mb, a_sf, w_sf, sc + sx, sc + sw, ea, tp, N, K, h->d_err, st));
+    PROF(h, cls, st, 1,
+         e = launch_gemm_nvfp4(epi, ma, mb, a_sf, w_sf, sc + sx, sc + sw, ea, tp, N, K, h->num_sms, h->d_err, st));
     return cuda_status(e);
   };
   esm_status s;
+  // the layer's amaxes start from zero; LN1, LN2 and fc1's GELU epilogue fold theirs in
+  if (cudaMemsetAsync(am, 0, kNumFp8Tensors * sizeof(float), st) != cudaSuccess) return ESM_ERR_CUDA;
   PROF(h, P_LN, st, 1,
-       launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, nullptr, nullptr,
-                        nullptr, nullptr, st));
-  if ((s = gemm(P_QKV, kFp4QkvRope, y, d, w->w_qkv[l], 3 * d, X_QKV, W_QKV, w->b_qkv[l], qkv)) != ESM_OK) return s;
+       launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, am + X_QKV,
+                        nullptr, nullptr, nullptr, st));
+  if ((s = gemm(P_QKV, kFp4QkvRope, y, true, d, w->w_qkv[l], 3 * d, X_QKV, W_QKV, w->b_qkv[l], qkv, nullptr)) !=
+      ESM_OK)
+    return s;
   {
     ProfScope _ps(h, P_ATTN, st, 1);
     const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
@@ -380,12 +387,13 @@ esm_status run_fp4_layer(esm_encoder* h, const esm_weights* w, int l, int T, con
     if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st) != cudaSuccess)
       return ESM_ERR_CUDA;
   }
-  if ((s = gemm(P_OPROJ, kFp4Residual, o, d, w->w_o[l], d, X_O, W_O, w->b_o[l], x)) != ESM_OK) return s;
+  if ((s = gemm(P_OPROJ, kFp4Residual, o, false, d, w->w_o[l], d, X_O, W_O, w->b_o[l], x, nullptr)) != ESM_OK)
+    return s;
   PROF(h, P_LN, st, 1,
-       launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, nullptr, nullptr,
+       launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, am + X_1, nullptr,
                         nullptr, nullptr, st));
-  if ((s = gemm(P_FC1, kFp4Gelu, y, d, w->w_1[l], f, X_1, W_1, w->b_1[l], u)) != ESM_OK) return s;
-  return gemm(P_FC2, kFp4Residual, u, f, w->w_2[l], d, X_2, W_2, w->b_2[l], x);
+  if ((s = gemm(P_FC1, kFp4Gelu, y, true, d, w->w_1[l], f, X_1, W_1, w->b_1[l], u, am + X_2)) != ESM_OK) return s;
+  return gemm(P_FC2, kFp4Residual, u, true, f, w->w_2[l], d, X_2, W_2, w->b_2[l], x, nullptr);
 }
 
 // The layer stack over an already indexed batch (pack buffers filled, x = embedding).
@@ -456,7 +464,7 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
     } else {
       PROF(h, P_LN, st, 1,
            launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_QKV,
-                            am + X_QKV, nullptr, nullptr, nullptr, st));
+                            fp8 ? am + X_QKV : nullptr, nullptr, nullptr, nullptr, st));
     }
     s = run_gemm(h, P_QKV, ESM_EPI_QKV_ROPE, y, fp8 ? (const void*)wq_qkv : w->w_qkv[l], w->b_qkv[l], qkv, pb.pos_id, T,
                  3 * d, d, fp8, act, sc + X_QKV, sc + W_QKV, nullptr, nullptr, st, -1, nullptr, nullptr,
@@ -492,7 +500,7 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
     } else {
       PROF(h, P_LN, st, 1,
            launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], pf32, y, fp8 ? Act::E4M3 : act, T, d, c.ln_eps, sc + X_1,
-                            am + X_1, nullptr, nullptr, nullptr, st));
+                            fp8 ? am + X_1 : nullptr, nullptr, nullptr, nullptr, st));
     }
     s = run_gemm(h, P_FC1, ESM_EPI_GELU, y, fp8 ? (const void*)wq_1 : w->w_1[l], w->b_1[l], u, nullptr, T, f, d, fp8,
                  fp8 ? Act::E4M3 : act, sc + X_1, sc + W_1, sc + X_2, am + X_2, st, -1, nullptr, nullptr,
@@ -1268,7 +1276,7 @@ esm_status esm_op_quantize_nvfp4(esm_encoder_t* h, const void* x, int rows, int 
     return ESM_ERR_INVALID_ARG;
   if (rows == 0) return ESM_OK;
   return cuda_status(launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(x), rows, rows, cols, codes, scales, amax,
-                                           scale, reinterpret_cast<cudaStream_t>(stream)));
+                                           scale, false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, esm_epilogue epi, const uint8_t* a_codes, const uint8_t* a_scales,
@@ -1302,8 +1310,8 @@ esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, esm_epilogue epi, const uint8_t* 
   ea.rope = h->d_rope;
   ea.rope_cols = 2 * h->cfg.hidden;
   ea.max_pos = h->cfg.max_positions;
-  return cuda_status(launch_gemm_nvfp4(mode, ma, mb, a_scales, b_scales, a_scale, b_scale, ea, M, N, K, h->d_err,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_gemm_nvfp4(mode, ma, mb, a_scales, b_scales, a_scale, b_scale, ea, M, N, K, h->num_sms,
+                                       h->d_err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 esm_status esm_op_attention(esm_encoder_t* h, const void* qkv, const int32_t* cu_seqlens, int num_seqs,

@@ -26,39 +26,44 @@
 namespace esm {
 namespace {
 
-constexpr int BM = 128, BN = 128;   // output tile of one CTA
+constexpr int BM = 128, BN = 256;   // output tile
 constexpr int STAGE_K = 256;        // E2M1 values per row per stage (128 bytes)
 constexpr int STAGES = 4;
 constexpr int ROW_BYTES = 128;
-constexpr int TILE_BYTES = 128 * ROW_BYTES;  // 16 KB: 128 rows of one stage
+constexpr int A_TILE = BM * ROW_BYTES;       // 16 KB
+constexpr int B_TILE = BN * ROW_BYTES;       // 32 KB (two 128-row halves)
 constexpr int ATOM_BYTES = 512;              // scales of 128 rows x 64 values
-constexpr int SF_STAGE_BYTES = 4 * ATOM_BYTES;  // 4 MMA k-steps of 64 values
-constexpr int THREADS = 128;
-constexpr uint32_t TMEM_COLS = 256;  // accumulator 128 + scale-factor ring 4 x (16 + 16)
-constexpr uint32_t COL_SF = 128;
+constexpr int SF_ROWS_BYTES = 4 * ATOM_BYTES;   // one 128-row block, the 4 MMA k-steps of a stage
+constexpr int EPI_WARPS = 8;                 // two per TMEM lane quarter, one 128-column half each
+constexpr int THREADS = 64 + 32 * EPI_WARPS; // producer warp, MMA warp, epilogue warps
+constexpr uint32_t TMEM_COLS = 512;          // accumulator 256 + scale-factor ring STAGES x 48
+constexpr uint32_t COL_SF = BN;              // stage s: SFA at +48 s + 4 ks, SFB at +48 s + 16 + 8 ks + 4 h
+constexpr uint32_t SF_COLS = 48;
+static_assert(COL_SF + SF_COLS * STAGES <= TMEM_COLS, "tensor memory");
 
 struct Fp4Smem {
-  uint64_t full[STAGES], empty[STAGES], done;
+  uint64_t full[STAGES], empty[STAGES], acc_full, acc_empty, done;
   uint32_t tmem_base;
   volatile int abort;
 };
-constexpr int A_OFF = 0, B_OFF = STAGES * TILE_BYTES, SFA_OFF = 2 * STAGES * TILE_BYTES,
-              SFB_OFF = SFA_OFF + STAGES * SF_STAGE_BYTES, BAR_OFF = SFB_OFF + STAGES * SF_STAGE_BYTES;
+constexpr int A_OFF = 0, B_OFF = STAGES * A_TILE, SFA_OFF = B_OFF + STAGES * B_TILE,
+              SFB_OFF = SFA_OFF + STAGES * SF_ROWS_BYTES, BAR_OFF = SFB_OFF + STAGES * 2 * SF_ROWS_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 1024 + 256;
+static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
 __device__ __forceinline__ size_t sf_offset(int row, int k16, int K) {
   const int rb = row >> 7, r = row & 127, ks = k16 >> 2, b = k16 & 3;
   return ((size_t)rb * (K / 64) + ks) * ATOM_BYTES + (r & 31) * 16 + (r >> 5) * 4 + b;
 }
 
-// E2M1 code of v (round to nearest, ties to the even code, saturating at 6): the 3-bit
-// magnitude code grows with the value (0, 0.5, 1, 1.5, 2, 3, 4, 6), so it counts the rounding
-// midpoints below |v|; a midpoint into an odd code is exclusive, into an even code inclusive.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  const float a = fabsf(v);
-  const uint32_t m = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                     (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.f);
-  return (v < 0.f ? 8u : 0u) | m;
+// Two values to E2M1 codes (round to nearest even, saturating at +-6), packed as one byte:
+// lo in bits 0-3, hi in bits 4-7 (the conversion puts its first source in the upper half).
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tmov.b16 %0, {t, 0};\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r & 0xFFu;
 }
 
 __device__ __forceinline__ void bf16x8(uint4 u, float (&f)[8]) {
@@ -118,9 +123,10 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16
   const __nv_fp8_e4m3 sb8(bmax / 6.f * S);  // round to nearest even, saturating at 448
   const float sb = static_cast<float>(sb8);
   uint32_t w[2] = {0u, 0u};
-  if (sb > 0.f) {
+  if (sb > 0.f) {  // (x S) / sb, two correctly rounded steps: x S / sb often lands exactly on an
+                   // E2M1 midpoint, which a reciprocal (x (S / sb)) would move off
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i >> 3] |= e2m1_code(v[i] * S / sb) << (4 * (i & 7));
+    for (int i = 0; i < 16; i += 2) w[i >> 3] |= e2m1x2(v[i] * S / sb, v[i + 1] * S / sb) << (4 * (i & 7));
   }
   *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + (size_t)k16 * 8) = make_uint2(w[0], w[1]);
   sf[sf_offset(row, k16, K)] = *reinterpret_cast<const uint8_t*>(&sb8);
@@ -132,6 +138,33 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Cluster multicast forms: the data lands at the same shared offset in every CTA of `mask`
+// (this cluster), each completing its bytes on the mbarrier at the same offset in that CTA.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                             uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+// Arrive once on the mbarrier at the same shared offset in every CTA of `mask` when all
+// previously issued tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(mask)
                : "memory");
 }
 
@@ -154,9 +187,62 @@ __host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
 
 // Epilogue: v = acc / (S_A S_B) + bias for the rows below ea.rows_valid, then
 //   F32      out fp32 [M, N] = v;          RESIDUAL  out fp32 [M, N] += v;
-//   GELU     out bf16 [M, N] = GELU(v) (exact-erf, A&S 7.1.26);
+//   GELU     out bf16 [M, N] = GELU(v) (exact-erf, A&S 7.1.26), and max |out| into ea.amax
+//            when given (the next operand's tensor amax);
 //   QKV_ROPE out bf16 [M, N] = v, with RoPE on the 64-column heads below ea.rope_cols at the
 //            row's position (the library's (cos, sin) table).
+template <int EPI>
+__device__ __forceinline__ void fp4_epilogue_store(float* v, int row, int col0, int N, const Fp4Epi& ea,
+                                                   float& amax) {
+  if constexpr (EPI == kFp4F32 || EPI == kFp4Residual) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ea.out) + (size_t)row * N + col0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      if constexpr (EPI == kFp4Residual) {
+        const float4 x = dst[j];
+        o.x += x.x; o.y += x.y; o.z += x.z; o.w += x.w;
+      }
+      dst[j] = o;
+    }
+  } else {
+    if constexpr (EPI == kFp4Gelu) {
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) gelu2_as7126(v[i], v[i + 1]);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    } else if (col0 < ea.rope_cols) {
+      int p = __ldg(ea.pos_id + row);
+      p = p < 0 ? 0 : (p >= ea.max_pos ? ea.max_pos - 1 : p);
+      const float4* tab = reinterpret_cast<const float4*>(ea.rope) + p;  // group g at g * max_pos
+#pragma unroll
+      for (int g = 0; g < 16; ++g) {  // pairs (2g, 2g + 32) and (2g + 1, 2g + 33) turn by their angles
+        const float4 t = __ldg(tab + (size_t)g * ea.max_pos);
+        const float x0 = v[2 * g], y0 = v[2 * g + 32], x1 = v[2 * g + 1], y1 = v[2 * g + 33];
+        v[2 * g] = x0 * t.x - y0 * t.y;
+        v[2 * g + 32] = y0 * t.x + x0 * t.y;
+        v[2 * g + 1] = x1 * t.z - y1 * t.w;
+        v[2 * g + 33] = y1 * t.z + x1 * t.w;
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ea.out) + (size_t)row * N + col0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                          pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+  }
+}
+
+// Persistent block-scaled GEMM: one CTA per SM walks the 128 x 256 output tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (column tiles fastest).  Warp 0 loads A (128 rows) and B (256
+// rows) code tiles by TMA and their scale-factor atoms by bulk copy into a STAGES-deep ring;
+// warp 1 copies each stage's scale factors into tensor memory and issues the four MMAs of 64
+// values (M 128, N 256) into the accumulator; warps 2-9 (lane quarter warp % 4, 128-column half
+// (warp - 2) / 4) load the finished accumulator into registers, hand it back at once, and run
+// the epilogue from registers while the next tile accumulates.  A 256-column tile doubles the
+// tensor work of a stage for 1.5x its bytes, so the ring holds enough work to cover the
+// delivery latency.  A half tile past N (N an odd multiple of 128) loads zero-filled codes and no
+// scales and stores nothing.
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -166,13 +252,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Fp4Smem* sm = reinterpret_cast<Fp4Smem*>(base + BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nb128 = N / 128;                    // 128-row blocks of B
+  const int tiles_n = (nb128 + 1) / 2, tiles = (M / BM) * tiles_n;
   const int kb_total = K / STAGE_K;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm->full[s], 1);
       mbar_init(&sm->empty[s], 1);
     }
+    mbar_init(&sm->acc_full, 1);
+    mbar_init(&sm->acc_empty, EPI_WARPS);
     mbar_init(&sm->done, 1);
     sm->abort = 0;
     fence_barrier_init();
@@ -187,141 +276,161 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer: A and B code tiles by TMA, their scale-factor atoms by bulk copy
-    int issued = 0;
-    for (int kb = 0; kb < kb_total && !sm->abort; ++kb, ++issued) {
-      const int s = kb % STAGES;
-      if (!mbar_wait(&sm->empty[s], ((uint32_t)(kb / STAGES) & 1u) ^ 1u)) {
-        latch_error(err, ERRBIT_TIMEOUT);
-        sm->abort = 1;
-        break;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer
+      uint32_t it = 0;
+      bool bad = false;
+      for (int t = blockIdx.x; t < tiles && !bad; t += gridDim.x) {
+        const int m0 = (t / tiles_n) * BM, nb0 = 2 * (t % tiles_n);
+        const bool hi_in = nb0 + 1 < nb128;  // the tile's second 128-row block of B exists
+        const uint8_t* sa = sfa + (size_t)(m0 / 128) * (K / 64) * ATOM_BYTES;
+        const uint8_t* sb0 = sfb + (size_t)nb0 * (K / 64) * ATOM_BYTES;
+        const uint32_t bytes = A_TILE + B_TILE + SF_ROWS_BYTES * (hi_in ? 3 : 2);
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          if (sm->abort || !mbar_wait(&sm->empty[s], ((it / STAGES) & 1u) ^ 1u)) {
+            bad = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm->full[s], bytes);
+          tma_load_2d(base + A_OFF + s * A_TILE, &tmA, kb * ROW_BYTES, m0, &sm->full[s]);
+          tma_load_2d(base + B_OFF + s * B_TILE, &tmB, kb * ROW_BYTES, nb0 * 128, &sm->full[s]);
+          tma_load_2d(base + B_OFF + s * B_TILE + B_TILE / 2, &tmB, kb * ROW_BYTES, nb0 * 128 + 128, &sm->full[s]);
+          bulk_load(base + SFA_OFF + s * SF_ROWS_BYTES, sa + (size_t)4 * kb * ATOM_BYTES, SF_ROWS_BYTES,
+                    &sm->full[s]);
+          bulk_load(base + SFB_OFF + s * 2 * SF_ROWS_BYTES, sb0 + (size_t)4 * kb * ATOM_BYTES, SF_ROWS_BYTES,
+                    &sm->full[s]);
+          if (hi_in)
+            bulk_load(base + SFB_OFF + s * 2 * SF_ROWS_BYTES + SF_ROWS_BYTES,
+                      sb0 + ((size_t)(K / 64) + 4 * kb) * ATOM_BYTES, SF_ROWS_BYTES, &sm->full[s]);
+        }
       }
-      mbar_arrive_expect_tx(&sm->full[s], 2 * TILE_BYTES + 2 * SF_STAGE_BYTES);
-      tma_load_2d(base + A_OFF + s * TILE_BYTES, &tmA, kb * ROW_BYTES, m0, &sm->full[s]);
-      tma_load_2d(base + B_OFF + s * TILE_BYTES, &tmB, kb * ROW_BYTES, n0, &sm->full[s]);
-      bulk_load(base + SFA_OFF + s * SF_STAGE_BYTES, sfa + ((size_t)(m0 / 128) * (K / 64) + 4 * kb) * ATOM_BYTES,
-                SF_STAGE_BYTES, &sm->full[s]);
-      bulk_load(base + SFB_OFF + s * SF_STAGE_BYTES, sfb + ((size_t)(n0 / 128) * (K / 64) + 4 * kb) * ATOM_BYTES,
-                SF_STAGE_BYTES, &sm->full[s]);
-    }
-    if (sm->abort)  // copies in flight land before the CTA may exit (bounded)
-      for (int k = issued - 1; k >= 0 && k >= issued - STAGES; --k)
-        if (!mbar_wait(&sm->full[k % STAGES], (uint32_t)(k / STAGES) & 1u)) break;
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer: per stage, the 8 scale-factor atoms into tensor memory, then the 4
-    // block-scaled MMAs of 64 values each (tcgen05.cp and tcgen05.mma of one thread execute
-    // in issue order)
-    constexpr uint32_t idesc = idesc_nvfp4(BM, BN);
-    const uint64_t adesc0 = make_sw128_desc(smem_u32(base + A_OFF));
-    const uint64_t bdesc0 = make_sw128_desc(smem_u32(base + B_OFF));
-    for (int kb = 0; kb < kb_total; ++kb) {
-      const int s = kb % STAGES;
-      if (!mbar_wait(&sm->full[s], (uint32_t)(kb / STAGES) & 1u)) {
-        latch_error(err, ERRBIT_TIMEOUT);
+      if (bad) {
+        if (!sm->abort) latch_error(err, ERRBIT_TIMEOUT);
         sm->abort = 1;
+        // copies in flight land before the CTA may exit (bounded): the last STAGES issued
+        for (uint32_t k = it; k > 0 && k + STAGES > it; --k)
+          if (!mbar_wait(&sm->full[(k - 1) % STAGES], ((k - 1) / STAGES) & 1u)) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer (tcgen05.cp and tcgen05.mma of one thread execute in issue order)
+      constexpr uint32_t idesc = idesc_nvfp4(BM, BN);
+      const uint64_t adesc0 = make_sw128_desc(smem_u32(base + A_OFF));
+      const uint64_t bdesc0 = make_sw128_desc(smem_u32(base + B_OFF));
+      uint32_t it = 0, j = 0;
+      bool bad = false;
+      for (int t = blockIdx.x; t < tiles && !bad; t += gridDim.x, ++j) {
+        if (sm->abort || !mbar_wait(&sm->acc_empty, (j & 1u) ^ 1u)) {
+          bad = true;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          if (sm->abort || !mbar_wait(&sm->full[s], (it / STAGES) & 1u)) {
+            bad = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_col = tmem + COL_SF + SF_COLS * (uint32_t)s;
+          const uint8_t* sfa_s = base + SFA_OFF + s * SF_ROWS_BYTES;
+          const uint8_t* sfb_s = base + SFB_OFF + s * 2 * SF_ROWS_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 4 * ks),
+                         "l"(sf_desc(smem_u32(sfa_s + ks * ATOM_BYTES)))
+                         : "memory");
+#pragma unroll
+            for (int h = 0; h < 2; ++h)  // B rows 0-127 and 128-255: columns +0..3 and +4..7
+              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 16 + 8 * ks + 4 * h),
+                           "l"(sf_desc(smem_u32(sfb_s + h * SF_ROWS_BYTES + ks * ATOM_BYTES)))
+                           : "memory");
+          }
+          const uint64_t ad = adesc0 + (uint64_t)((s * A_TILE) >> 4);
+          const uint64_t bd = bdesc0 + (uint64_t)((s * B_TILE) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {  // 64 values = 32 bytes of each 128-byte row
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.ne.b32 p, %6, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], "
+                "p;\n\t}" ::"r"(tmem),
+                "l"(ad + (uint64_t)(2 * ks)), "l"(bd + (uint64_t)(2 * ks)), "r"(idesc), "r"(sf_col + 4 * ks),
+                "r"(sf_col + 16 + 8 * ks), "r"((kb | ks) != 0 ? 1u : 0u)
+                : "memory");
+          }
+          mma_commit(&sm->empty[s]);
+        }
+        if (bad) break;
+        mma_commit(&sm->acc_full);
+      }
+      if (bad) {
+        if (!sm->abort) latch_error(err, ERRBIT_TIMEOUT);
+        sm->abort = 1;
+      }
+      mma_commit(&sm->done);  // completes once every MMA issued above has finished
+    }
+  } else {
+    // ---- epilogue warps: 32 rows x 128 columns each
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const float inv = 1.f / (__ldg(a_scale) * __ldg(b_scale));
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float amax = 0.f;
+    uint32_t j = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+      if (!mbar_wait_warp(&sm->acc_full, j & 1u)) {
+        if (lane == 0) {
+          if (!sm->abort) latch_error(err, ERRBIT_TIMEOUT);
+          sm->abort = 1;
+        }
         break;
       }
       tc_fence_after();
-      const uint32_t sf_col = tmem + COL_SF + 32u * (uint32_t)s;  // SFA at +4 ks, SFB at +16 + 4 ks
+      float v[128];
+      {
+        uint32_t r[4][32];
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t sa = smem_u32(base + SFA_OFF + s * SF_STAGE_BYTES + ks * ATOM_BYTES);
-        const uint32_t sb = smem_u32(base + SFB_OFF + s * SF_STAGE_BYTES + ks * ATOM_BYTES);
-        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 4 * ks), "l"(sf_desc(sa))
-                     : "memory");
-        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 16 + 4 * ks), "l"(sf_desc(sb))
-                     : "memory");
-      }
-      const uint64_t ad = adesc0 + (uint64_t)((s * TILE_BYTES) >> 4);
-      const uint64_t bd = bdesc0 + (uint64_t)((s * TILE_BYTES) >> 4);
+        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tmem + lane_off + (uint32_t)(128 * half + 32 * c), r[c]);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {  // 64 values = 32 bytes of each 128-byte row
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %6, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                tmem),
-            "l"(ad + (uint64_t)(2 * ks)), "l"(bd + (uint64_t)(2 * ks)), "r"(idesc), "r"(sf_col + 4 * ks),
-            "r"(sf_col + 16 + 4 * ks), "r"((kb | ks) != 0 ? 1u : 0u)
-            : "memory");
+        for (int c = 0; c < 4; ++c) tmem_ld_wait_regs(r[c]);  // one wait; each array tied to it
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[c][i]);
       }
-      mma_commit(&sm->empty[s]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->acc_empty);  // the accumulator is free for the next tile
+      const int row = (t / tiles_n) * BM + quarter * 32 + lane;
+      const int col_h = (t % tiles_n) * BN + 128 * half;
+      if (col_h >= N || row >= ea.rows_valid) continue;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float* vh = v + 64 * hh;
+        const int col0 = col_h + 64 * hh;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float bb = ea.bias ? __bfloat162float(static_cast<const __nv_bfloat16*>(ea.bias)[col0 + i]) : 0.f;
+          vh[i] = vh[i] * inv + bb;
+        }
+        fp4_epilogue_store<EPI>(vh, row, col0, N, ea, amax);
+      }
     }
-    mma_commit(&sm->done);
+    if constexpr (EPI == kFp4Gelu) {
+      if (ea.amax) {  // of the bf16 outputs: rounding is monotone, so round the maximum
+        amax = __bfloat162float(__float2bfloat16_rn(amax));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) atomic_max_nonneg(ea.amax, amax);
+      }
+    }
   }
   __syncwarp();
-  // ---- epilogue (all four warps): row 32 w + lane of the tile, 128 columns in two heads of 64
-  const bool ok = mbar_wait_warp(&sm->done, 0);
-  if (!ok && lane == 0) latch_error(err, ERRBIT_TIMEOUT);
-  if (ok && !sm->abort) {
-    tc_fence_after();
-    const float inv = 1.f / (__ldg(a_scale) * __ldg(b_scale));
-    const int row = m0 + warp * 32 + lane;
-    const bool live = row < ea.rows_valid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    float4 cs[EPI == kFp4QkvRope ? 16 : 1];
-    if constexpr (EPI == kFp4QkvRope) {
-      int p = live ? __ldg(ea.pos_id + row) : 0;
-      p = p < 0 ? 0 : (p >= ea.max_pos ? ea.max_pos - 1 : p);
-      const float4* tab = reinterpret_cast<const float4*>(ea.rope) + p;  // group g at g * max_pos
-#pragma unroll
-      for (int g = 0; g < 16; ++g) cs[g] = __ldg(tab + (size_t)g * ea.max_pos);
-    }
-#pragma unroll 1
-    for (int h = 0; h < BN; h += 64) {
-      float v[64];
-      {
-        float t0[32], t1[32];
-        tmem_ld32(tmem + lane_off + (uint32_t)h, t0);
-        tmem_ld32(tmem + lane_off + (uint32_t)h + 32, t1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = t0[i];
-          v[32 + i] = t1[i];
-        }
-      }
-      if (!live) continue;
-      const int col0 = n0 + h;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float b = ea.bias ? __bfloat162float(static_cast<const __nv_bfloat16*>(ea.bias)[col0 + i]) : 0.f;
-        v[i] = v[i] * inv + b;
-      }
-      if constexpr (EPI == kFp4F32 || EPI == kFp4Residual) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ea.out) + (size_t)row * N + col0);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          if constexpr (EPI == kFp4Residual) {
-            const float4 x = dst[j];
-            o.x += x.x; o.y += x.y; o.z += x.z; o.w += x.w;
-          }
-          dst[j] = o;
-        }
-      } else {
-        if constexpr (EPI == kFp4Gelu) {
-#pragma unroll
-          for (int i = 0; i < 64; i += 2) gelu2_as7126(v[i], v[i + 1]);
-        } else {
-          if (col0 < ea.rope_cols) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {  // pair (i, i + 32) of the head turns by its angle
-              const float4 t = cs[i >> 1];
-              const float c = (i & 1) ? t.z : t.x, sn = (i & 1) ? t.w : t.y;
-              const float x = v[i], y = v[32 + i];
-              v[i] = x * c - y * sn;
-              v[32 + i] = y * c + x * sn;
-            }
-          }
-        }
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ea.out) + (size_t)row * N + col0);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                              pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-      }
-    }
+  if (warp == 1) {  // every MMA has finished before its tensor memory is released
+    if (!mbar_wait_warp(&sm->done, 0) && lane == 0) latch_error(err, ERRBIT_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
@@ -334,12 +443,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace
 
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int rows_valid, int K, uint8_t* codes,
-                                  uint8_t* sf, float* amax, float* scale, cudaStream_t st) {
+                                  uint8_t* sf, float* amax, float* scale, bool amax_ready, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
-  if (e != cudaSuccess) return e;
   const size_t n8 = (size_t)rows_valid * K / 8;
-  if (n8 > 0) {
+  if (!amax_ready) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (!amax_ready && n8 > 0) {
     int grid = (int)((n8 + 255) / 256);
     if (grid > 4096) grid = 4096;
     nvfp4_amax_kernel<<<grid, 256, 0, st>>>(x, n8, amax);
@@ -355,7 +466,7 @@ int gemm_nvfp4_smem_bytes() { return SMEM_BYTES; }
 template <int EPI>
 static cudaError_t launch_epi(const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa, const uint8_t* sfb,
                               const float* a_scale, const float* b_scale, const Fp4Epi& ea, int M, int N, int K,
-                              unsigned* err, cudaStream_t st) {
+                              int num_sms, unsigned* err, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
@@ -363,20 +474,24 @@ static cudaError_t launch_epi(const CUtensorMap* tmA, const CUtensorMap* tmB, co
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  gemm_nvfp4_kernel<EPI><<<dim3(N / BN, M / BM), THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, sfa, sfb, a_scale, b_scale, ea,
-                                                                            M, N, K, err);
+  const long long tiles = (long long)(M / BM) * ((N / 128 + 1) / 2);
+  const unsigned grid = (unsigned)(tiles < num_sms ? tiles : num_sms);
+  gemm_nvfp4_kernel<EPI><<<grid, THREADS, SMEM_BYTES, st>>>(*tmA, *tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_nvfp4(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa,
                               const uint8_t* sfb, const float* a_scale, const float* b_scale, const Fp4Epi& ea, int M,
-                              int N, int K, unsigned* err, cudaStream_t st) {
+                              int N, int K, int num_sms, unsigned* err, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
+  if (num_sms <= 0) return cudaErrorInvalidValue;
   switch (epi) {
-    case kFp4F32: return launch_epi<kFp4F32>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
-    case kFp4Residual: return launch_epi<kFp4Residual>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
-    case kFp4Gelu: return launch_epi<kFp4Gelu>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
-    case kFp4QkvRope: return launch_epi<kFp4QkvRope>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, err, st);
+    case kFp4F32: return launch_epi<kFp4F32>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, num_sms, err, st);
+    case kFp4Residual:
+      return launch_epi<kFp4Residual>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, num_sms, err, st);
+    case kFp4Gelu: return launch_epi<kFp4Gelu>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, num_sms, err, st);
+    case kFp4QkvRope:
+      return launch_epi<kFp4QkvRope>(tmA, tmB, sfa, sfb, a_scale, b_scale, ea, M, N, K, num_sms, err, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -44,7 +44,7 @@ void launch_wait_timeout(unsigned long long limit_ns, unsigned* err, cudaStream_
 
 // ---------------------------------------------------------------- layernorm.cu
 // y = LN(x) * g + b. Params in f32 or bf16; output f32, bf16 or e4m3 (scaled by
-// *q_scale, max|y| into *amax).  With valid_* set, rows whose position is not below the
+// *q_scale); for e4m3 and bf16 outputs max|y| is folded into *amax when amax is non-null.  With valid_* set, rows whose position is not below the
 // segment's visible length are written as zero.
 void launch_layernorm(const float* x, const void* g, const void* b, bool param_f32, void* y, Act out,
                       int rows, int cols, float eps, const float* q_scale, float* amax,
@@ -154,9 +154,11 @@ void launch_ln_fold(const LnFoldJob* jobs, int num_jobs, int k, cudaStream_t st)
 // ---------------------------------------------------------------- fp4.cu
 // NVFP4 operand of x [rows_valid, K] bf16, padded with zero rows to `rows` (rows % 128 == 0,
 // K % 256 == 0): E2M1 codes [rows, K/2] bytes, E4M3 block scales in 512-byte atoms of 128 rows
-// x 64 values, the tensor's amax and its scale S = 448 * 6 / amax (device scalars).
+// x 64 values, the tensor's amax and its scale S = 448 * 6 / amax (device scalars).  With
+// amax_ready the amax was already accumulated (from zero) by the kernel that wrote x, and only
+// the scale and the codes are computed here.
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int rows_valid, int K, uint8_t* codes,
-                                  uint8_t* sf, float* amax, float* scale, cudaStream_t st);
+                                  uint8_t* sf, float* amax, float* scale, bool amax_ready, cudaStream_t st);
 // Epilogues of the NVFP4 GEMM (v = acc / (S_A S_B) + bias on rows below rows_valid).
 enum : int { kFp4F32 = 0, kFp4Residual = 1, kFp4Gelu = 2, kFp4QkvRope = 3 };
 struct Fp4Epi {
@@ -167,14 +169,15 @@ struct Fp4Epi {
   const float2* rope;     // QKV_ROPE: the (cos, sin) table
   int rope_cols;          // QKV_ROPE: columns below get RoPE
   int max_pos;
+  float* amax;            // GELU: max |bf16 out| is folded in here when non-null
 };
 // out = epilogue((A B^T) / (a_scale b_scale)) for NVFP4 operands A [M, K], B [N, K] (tensor
-// maps over the code bytes [rows, K/2] with a 128 x 128 box and the 128-byte swizzle);
-// M % 128 == 0, N % 128 == 0, K % 256 == 0.
+// maps over the code bytes [rows, K/2] with a 128-row x 128-byte box and the 128-byte swizzle);
+// M % 128 == 0, N % 128 == 0, K % 256 == 0.  Persistent: min(128 x 256 tiles, num_sms) CTAs.
 int gemm_nvfp4_smem_bytes();
 cudaError_t launch_gemm_nvfp4(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB, const uint8_t* sfa,
                               const uint8_t* sfb, const float* a_scale, const float* b_scale, const Fp4Epi& ea, int M,
-                              int N, int K, unsigned* err, cudaStream_t st);
+                              int N, int K, int num_sms, unsigned* err, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention.cu
 // tcgen05 attention (head_dim 64): tm_qkv is a tensor map over qkv [T, 3d] bf16 with a

@@ -5,8 +5,8 @@
 //
 // The row stays in registers (16-byte loads, cols/128 float4 per lane); mean and variance
 // are two exact passes over the registers, reduced with warp shuffles in fp32.  The output
-// is the next GEMM's operand: fp32, bf16, or E4M3 scaled by the delayed-scaling factor
-// (with the row's max |y| folded into the tensor amax).
+// is the next GEMM's operand: fp32, bf16, or E4M3 scaled by the delayed-scaling factor; for
+// E4M3 and bf16 outputs the rows' max |y| is folded into a tensor amax when one is given.
 #include "common.cuh"
 #include "internal.h"
 
@@ -92,16 +92,21 @@ __global__ void layernorm_kernel(const void* __restrict__ x, const void* __restr
       w.x = pack_bf16x2(o.x, o.y);
       w.y = pack_bf16x2(o.z, o.w);
       reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + off)[0] = w;
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
     } else {
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
       __nv_fp8x4_e4m3 q(make_float4(o.x * qs, o.y * qs, o.z * qs, o.w * qs));
       reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(y) + off)[0] = *reinterpret_cast<uint32_t*>(&q);
     }
   }
-  if constexpr (OUT == Act::E4M3) {
+  if constexpr (OUT == Act::E4M3 || OUT == Act::BF16) {
+    if (amax_out) {
+      // a bf16 output's amax is that of the rounded values: rounding is monotone, so round the max
+      if constexpr (OUT == Act::BF16) amax = __bfloat162float(__float2bfloat16_rn(amax));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0 && amax_out) atomic_max_nonneg(amax_out, amax);
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0) atomic_max_nonneg(amax_out, amax);
+    }
   }
 }
 
