@@ -75,6 +75,8 @@ def workload_for_rank(rank: int, tokens=None, layers=None, name: str = "esm650m"
         wl.seed = wl.seed * 1000 + rank
     if layers is not None and layers != wl.geometry.num_layers:
         wl.geometry = dataclasses.replace(wl.geometry, num_layers=layers)
+        if wl.layer_precision:
+            wl.layer_precision = [wl.layer_precision[i % len(wl.layer_precision)] for i in range(layers)]
     return wl
 
 
