@@ -342,19 +342,28 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         m_ref = m_new;
         // P = 2^(s*c - m) (hardware ex2) as bf16 pairs, computed while the previous P V may
         // still be reading the P columns
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // (scale-subtract and row sums two scores per f32x2 instruction)
+        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
         uint32_t w[KT / 32][16];
 #pragma unroll
         for (int ch = 0; ch < KT / 32; ++ch) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = fast_exp2(fmaf(sv[32 * ch + 2 * i], c, -m_ref));
-            const float p1 = fast_exp2(fmaf(sv[32 * ch + 2 * i + 1], c, -m_ref));
-            ls[i & 3] += p0 + p1;
+            float p0, p1;
+            f2_unpack(f2_fma(f2_pack(sv[32 * ch + 2 * i], sv[32 * ch + 2 * i + 1]), c2, nm2), p0, p1);
+            p0 = fast_exp2(p0);
+            p1 = fast_exp2(p1);
+            ls2[i & 1] = f2_add(ls2[i & 1], f2_pack(p0, p1));
             w[ch][i] = pack_bf16x2(p0, p1);
           }
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(ls2[0], a0, a1);
+          f2_unpack(ls2[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
         // P (and, within an item, O) may be rewritten once the previous P V is done
         if (g > 0) {
           if (!mbar_wait_warp(&sm->pv_done, (uint32_t)(g - 1) & 1u)) { ok = false; break; }
