@@ -48,6 +48,21 @@ __global__ void __launch_bounds__(256, N4 <= 10 ? 2 : 1) ln_bwd_kernel(const voi
   const int r0 = blockIdx.x * rows_per_block, r1 = min(rows, r0 + rows_per_block);
   for (int row = r0 + warp; row < r1; row += warps) {
     const float4* dr = reinterpret_cast<const float4*>(dy + (size_t)row * cols);
+    // the residual gradient of this row is read last: start it towards L2 now, and the
+    // next row of this warp as well (one 128-byte line per prefetch)
+    if ((lane & 7) == 0) {
+#pragma unroll
+      for (int i = 0; i < N4; ++i) {
+        const int c = i * 32 + lane;
+        if (c < n4) {
+          if (dres) prefetch_l2(dres + (size_t)row * cols + 4 * c);
+          if (row + warps < r1) {
+            if constexpr (!XBF16) prefetch_l2(static_cast<const float*>(xv) + (size_t)(row + warps) * cols + 4 * c);
+            prefetch_l2(dy + (size_t)(row + warps) * cols + 4 * c);
+          }
+        }
+      }
+    }
     float4 v[N4], d[N4];
     float s = 0.f;
 #pragma unroll
@@ -234,6 +249,31 @@ size_t bwd_partial_floats(int rows, int cols) {
 }
 size_t emb_bwd_partial_floats(int rows, int vocab, int d) { return (size_t)emb_chunks_for(rows) * vocab * d; }
 
+// LayerNorm backward grid: as many blocks as fit on the device at once (1 or 2 per SM, by
+// the dgamma/dbeta slices in shared memory), the rows split evenly between them, so every
+// SM streams the same number of rows; at most chunks_for(rows) blocks (the partial buffer's
+// size) and at least 8 rows per block (one per warp).
+struct LnBwdGrid {
+  int blocks, rows_per_block;
+};
+LnBwdGrid ln_bwd_grid(int rows, int cols) {
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms <= 0)
+      num_sms = 148;
+  }
+  const int warps = std::max(1, std::min(8, (int)(196608 / (8 * (size_t)cols))));
+  const size_t smem = (size_t)warps * 2 * cols * sizeof(float);
+  const int n4 = (cols / 4 + 31) / 32;
+  const int per_sm = (n4 <= 10 && 2 * (smem + 1024) <= 227 * 1024) ? 2 : 1;  // the kernel's launch bounds
+  int blocks = std::min(per_sm * num_sms, std::min(chunks_for(rows), std::max(1, (rows + 7) / 8)));
+  blocks = std::max(blocks, 1);
+  const int rpb = std::max(1, (rows + blocks - 1) / blocks);
+  return {std::max(1, (rows + rpb - 1) / rpb), rpb};
+}
+
 template <int N4, bool XBF16>
 cudaError_t ln_bwd_launch(const void* x, const void* gamma, bool gf32, const float* dy, const float* dres, float* dx,
                           float* partial, int rows, int cols, float eps, cudaStream_t st) {
@@ -245,9 +285,9 @@ cudaError_t ln_bwd_launch(const void* x, const void* gamma, bool gf32, const flo
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  const int blocks = (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
-  ln_bwd_kernel<N4, XBF16><<<blocks, 32 * warps, smem, st>>>(x, gamma, gf32, dy, dres, dx, partial, rows, cols,
-                                                            kLnRowsPerBlock, eps);
+  const LnBwdGrid g = ln_bwd_grid(rows, cols);
+  ln_bwd_kernel<N4, XBF16><<<g.blocks, 32 * warps, smem, st>>>(x, gamma, gf32, dy, dres, dx, partial, rows, cols,
+                                                              g.rows_per_block, eps);
   return cudaGetLastError();
 }
 
@@ -267,7 +307,7 @@ void ln_bwd_any(const void* x, const void* gamma, bool gf32, const float* dy, co
   else if (n4 <= 16) ln_bwd_launch<16, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
   else if (n4 <= 20) ln_bwd_launch<20, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
   else ln_bwd_launch<32, XBF16>(x, gamma, gf32, dy, dres, dx, partial, rows, cols, eps, st);
-  const int blocks = (rows + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
+  const int blocks = ln_bwd_grid(rows, cols).blocks;
   reduce_chunks(partial, blocks, (size_t)2 * cols, cols, 1.f, dgamma, st);
   reduce_chunks(partial + cols, blocks, (size_t)2 * cols, cols, 1.f, dbeta, st);
 }
