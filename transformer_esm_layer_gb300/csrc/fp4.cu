@@ -18,7 +18,7 @@
 //   scales one byte per 16 values, in 512-byte atoms of 128 rows x 64 values: atom
 //          (row / 128, k / 64) at byte ((row / 128) * (K / 64) + k / 64) * 512, and inside it
 //          row r (of the 128) and 16-value block b (of the 4) at (r % 32) * 16 + (r / 32) * 4 + b
-//          -- the arrangement tcgen05.cp.32x128b.warpx4 copies into tensor memory as the scale
+//          -- the arrangement each TMEM lane quarter holds as the scale
 //          factors of one M = 128 MMA (lane r % 32 of every lane quarter, column r / 32).
 #include "common.cuh"
 #include "internal.h"
@@ -35,14 +35,20 @@ constexpr int B_TILE = BN * ROW_BYTES;       // 32 KB (two 128-row halves)
 constexpr int ATOM_BYTES = 512;              // scales of 128 rows x 64 values
 constexpr int SF_ROWS_BYTES = 4 * ATOM_BYTES;   // one 128-row block, the 4 MMA k-steps of a stage
 constexpr int EPI_WARPS = 8;                 // two per TMEM lane quarter, one 128-column half each
-constexpr int THREADS = 64 + 32 * EPI_WARPS; // producer warp, MMA warp, epilogue warps
+constexpr int SF_WARP0 = 4;                  // warps 4-7 (lane quarters 0-3) write the scale factors
+constexpr int EPI_WARP0 = 8;                 // warps 8-15: epilogue
+constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+// Registers per thread at launch (65536 / 512) and after setmaxnreg: warpgroups 0 (producer,
+// MMA, two idle warps) and 1 (scale-factor warps) give registers to the epilogue warpgroups.
+constexpr int kRegsLaunch = 128, kRegsLow = 56, kRegsEpi = 200;
+static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsEpi == THREADS * kRegsLaunch, "register split");
 constexpr uint32_t TMEM_COLS = 512;          // accumulator 256 + scale-factor ring STAGES x 48
 constexpr uint32_t COL_SF = BN;              // stage s: SFA at +48 s + 4 ks, SFB at +48 s + 16 + 8 ks + 4 h
 constexpr uint32_t SF_COLS = 48;
 static_assert(COL_SF + SF_COLS * STAGES <= TMEM_COLS, "tensor memory");
 
 struct Fp4Smem {
-  uint64_t full[STAGES], empty[STAGES], acc_full, acc_empty, done;
+  uint64_t full[STAGES], empty[STAGES], sf_full[STAGES], acc_full, acc_empty, done;
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -141,42 +147,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-// Cluster multicast forms: the data lands at the same shared offset in every CTA of `mask`
-// (this cluster), each completing its bytes on the mbarrier at the same offset in that CTA.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar,
-                                               uint16_t mask) {
+// Warp-collective: 32 lanes x 16 consecutive 32-bit TMEM columns from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
-      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
-}
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                             uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-// Arrive once on the mbarrier at the same shared offset in every CTA of `mask` when all
-// previously issued tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(mask)
-               : "memory");
-}
-
-// Shared-memory descriptor of one 512-byte scale-factor atom (32 rows of 16 bytes, no
-// swizzle): 8-row core matrices of 128 bytes, consecutive along the rows.
-__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)(128u >> 4) << 16;          // leading byte offset
-  d |= (uint64_t)(128u >> 4) << 32;          // stride byte offset: next 8 rows
-  d |= (uint64_t)1u << 46;                   // descriptor version (tcgen05)
-  return d;                                  // swizzle mode 0: none
 }
 
 // Instruction descriptor, kind::mxf4nvf4 with block scaling: D f32, A and B E2M1 (format 1),
@@ -235,14 +213,17 @@ __device__ __forceinline__ void fp4_epilogue_store(float* v, int row, int col0, 
 
 // Persistent block-scaled GEMM: one CTA per SM walks the 128 x 256 output tiles t = blockIdx.x,
 // blockIdx.x + gridDim.x, ... (column tiles fastest).  Warp 0 loads A (128 rows) and B (256
-// rows) code tiles by TMA and their scale-factor atoms by bulk copy into a STAGES-deep ring;
-// warp 1 copies each stage's scale factors into tensor memory and issues the four MMAs of 64
-// values (M 128, N 256) into the accumulator; warps 2-9 (lane quarter warp % 4, 128-column half
-// (warp - 2) / 4) load the finished accumulator into registers, hand it back at once, and run
-// the epilogue from registers while the next tile accumulates.  A 256-column tile doubles the
-// tensor work of a stage for 1.5x its bytes, so the ring holds enough work to cover the
-// delivery latency.  A half tile past N (N an odd multiple of 128) loads zero-filled codes and no
-// scales and stores nothing.
+// rows) code tiles by TMA and their scale-factor atoms by bulk copy into a STAGES-deep ring.
+// Warps 4-7, one per TMEM lane quarter, write each stage's scale factors into tensor memory
+// with tcgen05.st (each lane quarter needs its own copy of the 32-row layout the MMA reads);
+// a tcgen05.cp per 512-byte atom would occupy the tensor pipe about as long as the MMAs.
+// Warp 1 issues the four MMAs of 64 values (M 128, N 256) of a stage once its codes and scale
+// factors are in place.  Warps 8-15 (lane quarter warp % 4, 128-column half (warp - 8) / 4)
+// load the finished accumulator into registers, hand it back at once, and run the epilogue
+// from registers while the next tile accumulates.  A 256-column tile doubles the tensor work
+// of a stage for 1.5x its bytes, so the ring holds enough work to cover the delivery latency.
+// A half tile past N (N an odd multiple of 128) loads zero-filled codes and no scales and
+// stores nothing.
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -259,6 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm->full[s], 1);
       mbar_init(&sm->empty[s], 1);
+      mbar_init(&sm->sf_full[s], 4);  // one arrival per scale-factor warp
     }
     mbar_init(&sm->acc_full, 1);
     mbar_init(&sm->acc_empty, EPI_WARPS);
@@ -275,6 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
+  if (warp < EPI_WARP0) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
 
   if (warp == 0) {
     if (lane == 0) {
@@ -316,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer (tcgen05.cp and tcgen05.mma of one thread execute in issue order)
+      // ---- MMA issuer
       constexpr uint32_t idesc = idesc_nvfp4(BM, BN);
       const uint64_t adesc0 = make_sw128_desc(smem_u32(base + A_OFF));
       const uint64_t bdesc0 = make_sw128_desc(smem_u32(base + B_OFF));
@@ -330,25 +313,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         for (int kb = 0; kb < kb_total; ++kb, ++it) {
           const int s = (int)(it % STAGES);
-          if (sm->abort || !mbar_wait(&sm->full[s], (it / STAGES) & 1u)) {
+          // the stage's codes have landed and its scale factors are in tensor memory
+          if (sm->abort || !mbar_wait(&sm->full[s], (it / STAGES) & 1u) ||
+              !mbar_wait(&sm->sf_full[s], (it / STAGES) & 1u)) {
             bad = true;
             break;
           }
           tc_fence_after();
           const uint32_t sf_col = tmem + COL_SF + SF_COLS * (uint32_t)s;
-          const uint8_t* sfa_s = base + SFA_OFF + s * SF_ROWS_BYTES;
-          const uint8_t* sfb_s = base + SFB_OFF + s * 2 * SF_ROWS_BYTES;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 4 * ks),
-                         "l"(sf_desc(smem_u32(sfa_s + ks * ATOM_BYTES)))
-                         : "memory");
-#pragma unroll
-            for (int h = 0; h < 2; ++h)  // B rows 0-127 and 128-255: columns +0..3 and +4..7
-              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sf_col + 16 + 8 * ks + 4 * h),
-                           "l"(sf_desc(smem_u32(sfb_s + h * SF_ROWS_BYTES + ks * ATOM_BYTES)))
-                           : "memory");
-          }
           const uint64_t ad = adesc0 + (uint64_t)((s * A_TILE) >> 4);
           const uint64_t bd = bdesc0 + (uint64_t)((s * B_TILE) >> 4);
 #pragma unroll
@@ -373,9 +345,58 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       mma_commit(&sm->done);  // completes once every MMA issued above has finished
     }
-  } else {
+  } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
+    // ---- scale-factor warps: lane quarter q = warp & 3.  TMEM columns of stage s (48): SFA
+    // k-step ks at +4 ks, SFB rows 128 h.. of k-step ks at +16 + 8 ks + 4 h; in each, lane
+    // 32 q + i holds the 16 bytes of row i of the 512-byte atom (the scales of rows i, 32 + i,
+    // 64 + i, 96 + i, four per row), the same in every lane quarter.
+    uint32_t it = 0;
+    bool bad = false;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    for (int t = blockIdx.x; t < tiles && !bad; t += gridDim.x) {
+      for (int kb = 0; kb < kb_total; ++kb, ++it) {
+        const int s = (int)(it % STAGES);
+        if (sm->abort || !mbar_wait_warp(&sm->full[s], (it / STAGES) & 1u)) {
+          bad = true;
+          break;
+        }
+        const uint8_t* sfa_s = base + SFA_OFF + s * SF_ROWS_BYTES + 16 * lane;
+        const uint8_t* sfb_s = base + SFB_OFF + s * 2 * SF_ROWS_BYTES + 16 * lane;
+        const uint32_t col = tmem + lane_off + COL_SF + SF_COLS * (uint32_t)s;
+        uint32_t r[16];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {  // SFA: columns +0..15
+          const uint4 u = *reinterpret_cast<const uint4*>(sfa_s + ks * ATOM_BYTES);
+          r[4 * ks] = u.x; r[4 * ks + 1] = u.y; r[4 * ks + 2] = u.z; r[4 * ks + 3] = u.w;
+        }
+        tmem_st16(col, r);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // SFB: columns +16..31 (ks 0, 1), +32..47 (ks 2, 3)
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 u =
+                  *reinterpret_cast<const uint4*>(sfb_s + h * SF_ROWS_BYTES + (2 * part + k2) * ATOM_BYTES);
+              const int o = 8 * k2 + 4 * h;
+              r[o] = u.x; r[o + 1] = u.y; r[o + 2] = u.z; r[o + 3] = u.w;
+            }
+          tmem_st16(col + 16 + 16 * part, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->sf_full[s]);
+      }
+    }
+    if (bad && lane == 0) {
+      if (!sm->abort) latch_error(err, ERRBIT_TIMEOUT);
+      sm->abort = 1;
+    }
+  } else if (warp >= EPI_WARP0) {
     // ---- epilogue warps: 32 rows x 128 columns each
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+    const int quarter = warp & 3, half = (warp - EPI_WARP0) >> 2;
     const float inv = 1.f / (__ldg(a_scale) * __ldg(b_scale));
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     float amax = 0.f;
