@@ -402,6 +402,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     float amax = 0.f;
     uint32_t j = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+      if constexpr (EPI == kFp4Residual) {  // this row's residual towards L2 while the tile accumulates
+        const int prow = (t / tiles_n) * BM + quarter * 32 + lane, pcol = (t % tiles_n) * BN + 128 * half;
+        if (prow < ea.rows_valid && pcol < N) {
+          const float* xr = static_cast<const float*>(ea.out) + (size_t)prow * N + pcol;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) prefetch_l2(xr + 32 * c);  // 4 x 128 bytes
+        }
+      }
       if (!mbar_wait_warp(&sm->acc_full, j & 1u)) {
         if (lane == 0) {
           if (!sm->abort) latch_error(err, ERRBIT_TIMEOUT);
