@@ -151,7 +151,12 @@ ESM_API esm_status esm_encoder_forward(esm_encoder_t* h, const esm_weights* w, c
 /* Same as esm_encoder_forward but token_ids, cu_seqlens and hidden_out are HOST
  * buffers: the call copies the inputs into the workspace, runs the forward and copies
  * the result back, all on `stream`, and returns after the stream has synchronised.
- * Pinned host memory gives asynchronous copies; pageable memory works too. */
+ * Pinned host memory gives asynchronous copies; pageable memory works too.  With pinned
+ * buffers (and profiling off) the handle keeps CUDA graphs of whole calls, up to 8, keyed by
+ * every pointer and size they bake in (host buffers, weights, workspace, the three sizes, the
+ * per-layer precision).  The second call with a key captures it on an internal stream, and
+ * later calls replay it on `stream`: the same work without ~170 separate kernel launches.  A
+ * capture that fails falls back to launching the kernels; the first call of a key always does. */
 ESM_API esm_status esm_encoder_forward_host(esm_encoder_t* h, const esm_weights* w,
                                     const int32_t* token_ids_host, const int32_t* cu_seqlens_host,
                                     int num_seqs, int total_tokens, int max_seqlen,

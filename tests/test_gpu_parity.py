@@ -357,6 +357,31 @@ def test_forward_host_matches_device_forward():
     assert np.array_equal(host_out, dev_out)
 
 
+def test_forward_host_pinned_graph_replays():
+    """With pinned host buffers esm_encoder_forward_host replays a CUDA graph of the whole call
+    from its second call on (the first runs eagerly).  Every call gives exactly the
+    device-buffer forward, including after a change of host buffers and inputs."""
+    from transformer_esm_layer_gb300.binding import DeviceWeights, packed_inputs
+    g = SMALL
+    enc = _enc(g, "bf16")
+    w = synth.model_weights(g, 7, "bf16", ln_random=True)
+    dw = DeviceWeights(w, "bf16")
+    ws = enc.workspace(400, 8, torch.device("cuda"))
+    for lengths, seed in (([33, 1, 200, 7], 7), ([90, 2, 5], 8)):
+        tok = synth.tokens_for_lengths(np.random.default_rng(seed), lengths)
+        t, cu = packed_inputs(tok, lengths)
+        dev_out = enc.forward(dw, t, cu, max(lengths)).view(torch.int16).cpu().numpy()
+        T = len(tok)
+        tok_h = torch.from_numpy(np.ascontiguousarray(tok, np.int32)).pin_memory()
+        cu_h = torch.from_numpy(synth.cu_seqlens_from_lengths(lengths)).pin_memory()
+        out_h = torch.zeros(T, g.hidden, dtype=torch.int16).pin_memory()
+        for call in range(4):  # eager, capture, replay, replay
+            out_h.zero_()
+            enc.forward_host(dw, tok_h.numpy(), cu_h.numpy(), max(lengths), out_h.numpy(), ws)
+            assert enc.check_status() == 0
+            assert np.array_equal(out_h.numpy(), dev_out), (lengths, call)
+
+
 def test_fp8_forward_one_layer_3b_width(margin):
     """One layer of the 3B geometry (hidden 2560, 40 heads, ffn 10240) with E4M3 GEMMs against
     the oracle with the same scales (5e-2; attention in bf16)."""

@@ -79,6 +79,16 @@ struct esm_encoder {
   int train_T = 0, train_B = 0, train_items = 0;
   const void* train_buf = nullptr;
   const void* train_ws = nullptr;
+  // esm_encoder_forward_host with pinned host buffers: CUDA graphs of whole calls, keyed by
+  // everything they bake in (host and device pointers, sizes, per-layer precision); a key is
+  // captured at its second call (the first, eager, does the one-time kernel configuration)
+  struct HostGraph {
+    std::vector<uintptr_t> key;
+    cudaGraphExec_t exec;
+  };
+  std::vector<HostGraph> host_graphs;              // oldest first, at most kHostGraphs
+  std::vector<std::vector<uintptr_t>> host_seen;   // keys called once, at most kHostGraphs
+  cudaStream_t cap_stream = nullptr;
   // measurement hooks
   bool profiling = false;
   long long launches[ESM_PROFILE_CLASSES] = {};
@@ -924,6 +934,8 @@ esm_status esm_encoder_create(const esm_config* cfg, esm_encoder_t** out) {
 
 void esm_encoder_destroy(esm_encoder_t* h) {
   if (!h) return;
+  for (auto& g : h->host_graphs) cudaGraphExecDestroy(g.exec);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->d_err) cudaFree(h->d_err);
   if (h->d_rope) cudaFree(h->d_rope);
   if (h->d_fp8) cudaFree(h->d_fp8);
@@ -1125,6 +1137,53 @@ esm_status esm_encoder_lm_head_backward(esm_encoder_t* h, const esm_lm_head* hea
   return cuda_status(cudaGetLastError());
 }
 
+namespace {
+
+constexpr size_t kHostGraphs = 8;
+
+bool host_pinned(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+std::vector<uintptr_t> host_graph_key(const esm_encoder* h, const esm_weights* w, const void* tok, const void* cu,
+                                      int B, int T, int max_seqlen, const void* out, const void* ws, size_t ws_bytes) {
+  std::vector<uintptr_t> k = {(uintptr_t)tok,  (uintptr_t)cu,       (uintptr_t)out,      (uintptr_t)B,
+                              (uintptr_t)T,    (uintptr_t)max_seqlen, (uintptr_t)ws,     (uintptr_t)ws_bytes,
+                              (uintptr_t)w->emb, (uintptr_t)w->lnf_g, (uintptr_t)w->lnf_b};
+  const void* const* arrs[] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o, w->b_o,
+                               w->ln2_g, w->ln2_b, w->w_1,   w->b_1,   w->w_2, w->b_2};
+  for (const void* const* a : arrs)
+    for (int l = 0; l < h->cfg.num_layers; ++l) k.push_back((uintptr_t)a[l]);
+  for (uint8_t p : h->layer_fp8) k.push_back(p);
+  return k;
+}
+
+// The work of one forward_host call, enqueued on st: inputs in, the forward, the output out.
+esm_status enqueue_host_call(esm_encoder* h, const esm_weights* w, const int32_t* tok_host, const int32_t* cu_host,
+                             int B, int T, int max_seqlen, void* out_host, void* workspace, size_t workspace_bytes,
+                             const WsLayout& L, cudaStream_t st) {
+  // the output staging lives in the qkv region, which is free once the last layer ran
+  const size_t out_bytes = (size_t)T * h->cfg.hidden * (h->cfg.precision == ESM_FP32 ? 4 : 2);
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  int32_t* dtok = reinterpret_cast<int32_t*>(b + L.stage_tok);
+  int32_t* dcu = reinterpret_cast<int32_t*>(b + L.stage_cu);
+  void* dout = b + L.qkv;
+  if (cudaMemcpyAsync(dtok, tok_host, 4 * (size_t)T, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dcu, cu_host, 4 * (size_t)(B + 1), cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return ESM_ERR_CUDA;
+  esm_status s = forward_impl(h, w, dtok, dcu, B, T, max_seqlen, dout, workspace, workspace_bytes, st);
+  if (s != ESM_OK) return s;
+  if (cudaMemcpyAsync(out_host, dout, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return ESM_ERR_CUDA;
+  return ESM_OK;
+}
+
+}  // namespace
+
 esm_status esm_encoder_forward_host(esm_encoder_t* h, const esm_weights* w, const int32_t* token_ids_host,
                                     const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int max_seqlen,
                                     void* hidden_out_host, void* workspace, size_t workspace_bytes,
@@ -1137,19 +1196,52 @@ esm_status esm_encoder_forward_host(esm_encoder_t* h, const esm_weights* w, cons
   WsLayout L;
   esm_status s = check_ws(h, total_tokens, num_seqs, workspace, workspace_bytes, &L);
   if (s != ESM_OK) return s;
-  // the output staging lives in the qkv region, which is free once the last layer ran
-  const size_t out_bytes = (size_t)total_tokens * h->cfg.hidden * (h->cfg.precision == ESM_FP32 ? 4 : 2);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* b = static_cast<uint8_t*>(workspace);
-  int32_t* dtok = reinterpret_cast<int32_t*>(b + L.stage_tok);
-  int32_t* dcu = reinterpret_cast<int32_t*>(b + L.stage_cu);
-  void* dout = b + L.qkv;
-  if (cudaMemcpyAsync(dtok, token_ids_host, 4 * (size_t)total_tokens, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dcu, cu_seqlens_host, 4 * (size_t)(num_seqs + 1), cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return ESM_ERR_CUDA;
-  s = forward_impl(h, w, dtok, dcu, num_seqs, total_tokens, max_seqlen, dout, workspace, workspace_bytes, st);
+  // Pinned host buffers: replay a graph of the whole call (the ~170 kernel launches of a
+  // forward cost more eagerly than as one graph).  Pageable buffers stay on the eager path.
+  if (!h->profiling && host_pinned(token_ids_host) && host_pinned(cu_seqlens_host) && host_pinned(hidden_out_host)) {
+    std::vector<uintptr_t> key = host_graph_key(h, w, token_ids_host, cu_seqlens_host, num_seqs, total_tokens,
+                                                max_seqlen, hidden_out_host, workspace, workspace_bytes);
+    for (const auto& g : h->host_graphs)
+      if (g.key == key) {
+        if (cudaGraphLaunch(g.exec, st) != cudaSuccess) return ESM_ERR_CUDA;
+        return cuda_status(cudaStreamSynchronize(st));
+      }
+    auto seen = std::find(h->host_seen.begin(), h->host_seen.end(), key);
+    if (seen != h->host_seen.end()) {  // second call of this key: capture it
+      h->host_seen.erase(seen);
+      bool ok = h->cap_stream || cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
+      cudaGraph_t graph = nullptr;
+      cudaGraphExec_t exec = nullptr;
+      if (ok && cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+        const esm_status cs = enqueue_host_call(h, w, token_ids_host, cu_seqlens_host, num_seqs, total_tokens,
+                                                max_seqlen, hidden_out_host, workspace, workspace_bytes, L,
+                                                h->cap_stream);
+        const cudaError_t ce = cudaStreamEndCapture(h->cap_stream, &graph);
+        ok = cs == ESM_OK && ce == cudaSuccess && graph != nullptr &&
+             cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+      } else {
+        ok = false;
+      }
+      if (graph) cudaGraphDestroy(graph);
+      cudaGetLastError();  // a capture that failed falls back to eager launches below
+      if (ok) {
+        if (h->host_graphs.size() >= kHostGraphs) {
+          cudaGraphExecDestroy(h->host_graphs.front().exec);
+          h->host_graphs.erase(h->host_graphs.begin());
+        }
+        h->host_graphs.push_back({std::move(key), exec});
+        if (cudaGraphLaunch(exec, st) != cudaSuccess) return ESM_ERR_CUDA;
+        return cuda_status(cudaStreamSynchronize(st));
+      }
+    } else {
+      if (h->host_seen.size() >= kHostGraphs) h->host_seen.erase(h->host_seen.begin());
+      h->host_seen.push_back(std::move(key));
+    }
+  }
+  s = enqueue_host_call(h, w, token_ids_host, cu_seqlens_host, num_seqs, total_tokens, max_seqlen, hidden_out_host,
+                        workspace, workspace_bytes, L, st);
   if (s != ESM_OK) return s;
-  if (cudaMemcpyAsync(hidden_out_host, dout, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return ESM_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(st));
 }
 
