@@ -93,6 +93,74 @@ def test_nvfp4_quantize_matches_oracle(enc):
     assert np.all(q[0, :16] == 0.0) and np.all(sb[0, 0] == 0.0)
 
 
+def _fp32_codes(x, K):
+    """E2M1 code nibbles (sign bit 3) and E4M3 block scales of a bf16 operand with every
+    decision taken in fp32 as the kernel takes it: S = RN(2688 / amax), sb = E4M3(RN(RN(bmax /
+    6) S)), q = E2M1(RN(RN(x S) / sb)) with ties to even; 0 for a block whose scale is 0."""
+    f = np.float32
+    x32 = x.astype(f)
+    S = f(2688.0) / np.abs(x32).max()
+    xb = x32.reshape(x.shape[0], K // 16, 16)
+    u = (np.abs(xb).max(axis=-1) / f(6.0)) * S
+    sb = F4.e4m3_round(u.astype(np.float64))
+    safe = np.where(sb > 0, sb, 1.0).astype(f)
+    q = (xb * S) / safe[..., None]                 # two fp32 steps, each correctly rounded
+    mag = F4.e2m1_round(np.abs(q).astype(np.float64))
+    idx = np.searchsorted(E2M1, mag)
+    nib = np.where(np.signbit(q), 8, 0) | idx
+    nib = np.where(sb[..., None] > 0, nib, 0)
+    return nib.reshape(x.shape[0], K), sb, S
+
+
+def test_nvfp4_quantize_fp32_decisions_exact(enc):
+    """Every code nibble and block scale equals the fp32 decision, on inputs built to hit
+    E2M1 rounding midpoints exactly: the amax is 21, so S = 2688 / 21 = 128 exactly; each
+    block's largest value is 3 sb / 64 for a chosen E4M3 scale sb (all 126 finite positive
+    ones), so the block scale is exactly sb; the other values are +-t sb / 128 for E2M1 values
+    and midpoints t (quotient exactly t, so ties to even decide) and their bf16 neighbours
+    one step up or down (quotients just off the midpoints), and a few -0 and bf16 subnormals.
+    A random operand follows.  This pins the kernel's quotient (a reciprocal corrected by an
+    FMA, no per-value division) to IEEE division."""
+    from tests._util import e4m3_table
+    rng = np.random.default_rng(56)
+    table = e4m3_table()
+    sbs = table[1:0x7F]
+    points = np.array([0.25, 0.5, 0.75, 1.0, 1.25, 1.5, 1.75, 2.0, 2.5, 3.0, 3.5, 4.0, 5.0, 6.0])
+    rows, K = 256, 768
+    nblk = rows * K // 16
+    blocks = np.zeros((nblk, 16))
+    sb_pick = sbs[np.arange(nblk) % len(sbs)]
+    blocks[:, 0] = 3 * sb_pick / 64
+    t = rng.choice(points, size=(nblk, 15)) * rng.choice([-1.0, 1.0], size=(nblk, 15))
+    bits = synth.f32_to_bf16_bits((t * sb_pick[:, None] / 128).astype(np.float32)).astype(np.int64)
+    step = rng.integers(-1, 2, size=bits.shape)                   # -1, 0, +1 bf16 steps
+    bits = np.where((bits & 0x7FFF) != 0, bits + step, bits)
+    vals = synth.bf16_bits_to_f32(bits.astype(np.uint16)).astype(np.float64)
+    blocks[:, 1:] = np.minimum(np.abs(vals), 3 * sb_pick[:, None] / 64) * np.sign(vals)
+    x = blocks.reshape(rows, K)
+    x[5, 17] = -0.0
+    x[6, 33] = synth.bf16_bits_to_f32(np.array([0x0003], np.uint16))[0]
+    x[0, 0] = 21.0                                                # the tensor's amax
+    x = _bf16(x)
+    for i, case in enumerate((x, _case(rng, rows, K))):
+        codes, scales, amax, scale = _quant(enc, case)
+        torch.cuda.synchronize()
+        c = codes.cpu().numpy().astype(np.int64)
+        nib = np.stack([c & 0xF, c >> 4], axis=-1).reshape(rows, K)
+        want, sb_want, S = _fp32_codes(case, K)
+        _, sb = _codes(codes.cpu().numpy(), scales.cpu().numpy(), rows, K)
+        assert float(scale.item()) == float(S) and (i > 0 or float(S) == 128.0)
+        assert np.array_equal(sb, sb_want)
+        # magnitudes exactly; the sign bit wherever the magnitude is not zero (a signed zero
+        # code has the value of an unsigned one)
+        bad = np.argwhere(((nib & 7) != (want & 7)) | (((want & 7) != 0) & ((nib & 8) != (want & 8))))
+        assert len(bad) == 0, (i, len(bad), bad[:5], nib[tuple(bad[0])], want[tuple(bad[0])])
+        if i == 0:   # the construction reached the ties it was built for
+            q_exact = case.reshape(rows, K // 16, 16) * 128.0 / np.where(sb_want > 0, sb_want, 1.0)[..., None]
+            ties = np.isin(np.abs(q_exact), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+            assert ties.sum() > 1000
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 1280), (384, 256, 512)])
 def test_nvfp4_gemm_exact_on_its_operands(enc, M, N, K):
     """fp32 accumulation of E2M1 x E2M1 products scaled by E4M3 x E4M3 block scales: exact

@@ -359,9 +359,9 @@ esm_status run_fp4_layer(esm_encoder* h, const esm_weights* w, int l, int T, con
     {
       ProfScope _ps(h, P_OTHER, st, 4);
       if (launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(act), tp, T, K, a_codes, a_sf, am + sx, sc + sx,
-                                act_ready, st) != cudaSuccess ||
+                                act_ready, h->num_sms, st) != cudaSuccess ||
           launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(wt), N, N, K, w_codes, w_sf, am + sw, sc + sw,
-                                false, st) != cudaSuccess)
+                                false, h->num_sms, st) != cudaSuccess)
         return ESM_ERR_CUDA;
     }
     const CUtensorMap* ma = h->map(a_codes, (uint64_t)tp, (uint64_t)K / 2, 128, 1);
@@ -1368,7 +1368,7 @@ esm_status esm_op_quantize_nvfp4(esm_encoder_t* h, const void* x, int rows, int 
     return ESM_ERR_INVALID_ARG;
   if (rows == 0) return ESM_OK;
   return cuda_status(launch_nvfp4_quantize(static_cast<const __nv_bfloat16*>(x), rows, rows, cols, codes, scales, amax,
-                                           scale, false, reinterpret_cast<cudaStream_t>(stream)));
+                                           scale, false, h->num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 esm_status esm_op_gemm_nvfp4(esm_encoder_t* h, esm_epilogue epi, const uint8_t* a_codes, const uint8_t* a_scales,

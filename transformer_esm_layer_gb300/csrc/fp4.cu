@@ -62,16 +62,6 @@ __device__ __forceinline__ size_t sf_offset(int row, int k16, int K) {
   return ((size_t)rb * (K / 64) + ks) * ATOM_BYTES + (r & 31) * 16 + (r >> 5) * 4 + b;
 }
 
-// Two values to E2M1 codes (round to nearest even, saturating at +-6), packed as one byte:
-// lo in bits 0-3, hi in bits 4-7 (the conversion puts its first source in the upper half).
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint16_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tmov.b16 %0, {t, 0};\n\t}"
-      : "=h"(r)
-      : "f"(hi), "f"(lo));
-  return r & 0xFFu;
-}
-
 __device__ __forceinline__ void bf16x8(uint4 u, float (&f)[8]) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
@@ -82,61 +72,137 @@ __device__ __forceinline__ void bf16x8(uint4 u, float (&f)[8]) {
   }
 }
 
+// max |x| over a bf16 tensor of n8 16-byte units: a grid of a few blocks per SM, four loads in
+// flight per thread, one atomic per block.
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __nv_bfloat16* __restrict__ x, size_t n8,
                                                          float* amax) {
+  const uint4* p = reinterpret_cast<const uint4*>(x);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   float m = 0.f;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    float f[8];
-    bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + i), f);
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    uint4 u[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
+    for (int k = 0; k < 4; ++k) u[k] = __ldg(p + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float f[8];
+      bf16x8(u[k], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+    }
+  }
+  for (; i < n8; i += stride) {
+    float f[8];
+    bf16x8(__ldg(p + i), f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) atomic_max_nonneg(amax, m);
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) atomic_max_nonneg(amax, m);
+  }
 }
 
-// One thread per block of 16 values: the block's E4M3 scale and its eight code bytes.  Rows
-// from rows_valid to rows (the padding to a multiple of 128) quantise as zeros.
+// Eight values to E2M1 codes (round to nearest even, saturating at +-6), q[0] in bits 0-3 up
+// to q[7] in bits 28-31.
+__device__ __forceinline__ uint32_t e2m1x8(const float* q) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
+}
+
+// One lane per block of 16 values (32 contiguous bytes), one warp per 512 values of a row,
+// QSEGS such segments per warp with their loads issued first.  The quotients x S / sb are
+// the correctly rounded fp32 quotient of the correctly rounded fp32 product, as two steps:
+// x S / sb often lands exactly on an E2M1 midpoint, and a product with the reciprocal alone
+// would move it off.  The quotient is y r corrected once by the exact residual y - sb (y r)
+// (Markstein's theorem on division through a correctly rounded reciprocal r = RN(1 / sb),
+// round to nearest), two values per f32x2 instruction; its sign is that of y (a zero
+// residual would otherwise turn -0 into +0).  Checked on GB300 against IEEE division over
+// every finite E4M3 divisor sb and every fp32 |y| below 16 sb: identical E2M1 codes, and
+// identical quotients for |y| >= sb / 16.  Lanes 4j gather the four scales of their 64-value
+// group.  Rows from rows_valid on (the padding to a multiple of 128) quantise as zeros.
+// grid (ceil(rows / 8), ceil(ceil(K / 512) / QSEGS)), 256 threads; K a multiple of 16.
+template <int QSEGS>
 __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows,
                                                              int rows_valid, int K, const float* amax,
                                                              uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                              float* scale_out) {
-  const size_t blk = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-  const int kb = K / 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  const int nseg = (K + 511) / 512;
   const float a = __ldg(amax);
   const float S = a > 0.f ? (448.f * 6.f) / a : 1.f;
-  if (blk == 0 && scale_out) *scale_out = S;
-  if (blk >= (size_t)rows * kb) return;
-  const int row = (int)(blk / kb), k16 = (int)(blk % kb);
-  float v[16];
-  if (row < rows_valid) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * K + (size_t)k16 * 16);
-    float f[8];
-    bf16x8(__ldg(src), f);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && scale_out) *scale_out = S;
+  if (row >= rows) return;  // whole warps
+  uint4 u[QSEGS][2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = f[i];
-    bf16x8(__ldg(src + 1), f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[8 + i] = f[i];
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  for (int j = 0; j < QSEGS; ++j) {
+    const int k0 = (blockIdx.y * QSEGS + j) * 512 + lane * 16;
+    u[j][0] = u[j][1] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows_valid && k0 < K) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * K + k0);
+      u[j][0] = __ldg(src);
+      u[j][1] = __ldg(src + 1);
+    }
   }
-  float bmax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
-  const __nv_fp8_e4m3 sb8(bmax / 6.f * S);  // round to nearest even, saturating at 448
-  const float sb = static_cast<float>(sb8);
-  uint32_t w[2] = {0u, 0u};
-  if (sb > 0.f) {  // (x S) / sb, two correctly rounded steps: x S / sb often lands exactly on an
-                   // E2M1 midpoint, which a reciprocal (x (S / sb)) would move off
+  for (int j = 0; j < QSEGS; ++j) {
+    const int seg = blockIdx.y * QSEGS + j;
+    if (seg >= nseg) break;  // the same for the whole warp
+    const int k0 = seg * 512 + lane * 16;
+    const uint32_t wd[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w, u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
+    float v[16];
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) w[i >> 3] |= e2m1x2(v[i] * S / sb, v[i + 1] * S / sb) << (4 * (i & 7));
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(wd[i] << 16);
+      v[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+    }
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+    const __nv_fp8_e4m3 sb8(bmax / 6.f * S);  // round to nearest even, saturating at 448
+    const float sb = static_cast<float>(sb8);
+    uint32_t w0 = 0u, w1 = 0u;
+    if (sb > 0.f) {
+      const float r = 1.f / sb;
+      const uint64_t S2 = f2_pack(S, S), r2 = f2_pack(r, r), nb2 = f2_pack(-sb, -sb);
+      float q[16];
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        const uint64_t y = f2_mul(f2_pack(v[i], v[i + 1]), S2);
+        const uint64_t q0 = f2_mul(y, r2);
+        const uint64_t e = f2_fma(q0, nb2, y);
+        const uint64_t qs = (f2_fma(e, r2, q0) & 0x7FFFFFFF7FFFFFFFull) | (y & 0x8000000080000000ull);
+        f2_unpack(qs, q[i], q[i + 1]);
+      }
+      w0 = e2m1x8(q);
+      w1 = e2m1x8(q + 8);
+    }
+    if (k0 < K) *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + k0 / 2) = make_uint2(w0, w1);
+    const uint32_t s0 = sb8.__x;
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, s0, 1), s2 = __shfl_down_sync(0xffffffffu, s0, 2),
+                   s3 = __shfl_down_sync(0xffffffffu, s0, 3);
+    if ((lane & 3) == 0 && k0 < K)
+      *reinterpret_cast<uint32_t*>(sf + sf_offset(row, k0 / 16, K)) = s0 | s1 << 8 | s2 << 16 | s3 << 24;
   }
-  *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + (size_t)k16 * 8) = make_uint2(w[0], w[1]);
-  sf[sf_offset(row, k16, K)] = *reinterpret_cast<const uint8_t*>(&sb8);
 }
+constexpr int kQuantSegs = 2;
 
 // 1-D bulk copy global -> shared completing `bytes` on the mbarrier (16-byte aligned, size a
 // multiple of 16).
@@ -472,7 +538,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace
 
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int rows_valid, int K, uint8_t* codes,
-                                  uint8_t* sf, float* amax, float* scale, bool amax_ready, cudaStream_t st) {
+                                  uint8_t* sf, float* amax, float* scale, bool amax_ready, int num_sms,
+                                  cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const size_t n8 = (size_t)rows_valid * K / 8;
   if (!amax_ready) {
@@ -480,13 +547,13 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int rows_val
     if (e != cudaSuccess) return e;
   }
   if (!amax_ready && n8 > 0) {
-    int grid = (int)((n8 + 255) / 256);
-    if (grid > 4096) grid = 4096;
+    const size_t need = (n8 + 1023) / 1024;  // at least four units per thread
+    const int grid = (int)(need < (size_t)num_sms * 8 ? need : (size_t)num_sms * 8);
     nvfp4_amax_kernel<<<grid, 256, 0, st>>>(x, n8, amax);
   }
-  const size_t blocks = (size_t)rows * (K / 16);
-  nvfp4_quantize_kernel<<<(unsigned)((blocks + 255) / 256), 256, 0, st>>>(x, rows, rows_valid, K, amax, codes, sf,
-                                                                         scale);
+  const int nseg = (K + 511) / 512;
+  const dim3 grid((unsigned)((rows + 7) / 8), (unsigned)((nseg + kQuantSegs - 1) / kQuantSegs));
+  nvfp4_quantize_kernel<kQuantSegs><<<grid, 256, 0, st>>>(x, rows, rows_valid, K, amax, codes, sf, scale);
   return cudaGetLastError();
 }
 

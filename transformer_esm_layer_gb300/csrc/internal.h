@@ -158,7 +158,8 @@ void launch_ln_fold(const LnFoldJob* jobs, int num_jobs, int k, cudaStream_t st)
 // amax_ready the amax was already accumulated (from zero) by the kernel that wrote x, and only
 // the scale and the codes are computed here.
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int rows, int rows_valid, int K, uint8_t* codes,
-                                  uint8_t* sf, float* amax, float* scale, bool amax_ready, cudaStream_t st);
+                                  uint8_t* sf, float* amax, float* scale, bool amax_ready, int num_sms,
+                                  cudaStream_t st);
 // Epilogues of the NVFP4 GEMM (v = acc / (S_A S_B) + bias on rows below rows_valid).
 enum : int { kFp4F32 = 0, kFp4Residual = 1, kFp4Gelu = 2, kFp4QkvRope = 3 };
 struct Fp4Epi {
@@ -187,7 +188,7 @@ int attention_tc_smem_bytes();
 // every query row (scores scaled by 1/sqrt(head_dim)), kept by the training forward for the
 // backward; lse_stride >= T.
 // The tensor map launch_attention_tc expects over qkv [T, 3d] bf16, encoded on the host
-// (no allocation); false if the driver's encoder is unavailable or rejects the layout.
+// (no allocation); false if the CUDA tensor-map encoder is unavailable or rejects the layout.
 bool encode_attention_qkv_map(const void* qkv, int total_tokens, int hidden, CUtensorMap* out);
 cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int d, int heads, int max_items,
                                 const PackBuffers& pb, const float* q_scale, float* amax, unsigned* err,
