@@ -506,10 +506,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int hh = 0; hh < 2; ++hh) {
         float* vh = v + 64 * hh;
         const int col0 = col_h + 64 * hh;
+        if (ea.bias) {  // 16-byte aligned (checked on the host), eight bf16 per load
+          const uint4* bp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ea.bias) + col0);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float bb = ea.bias ? __bfloat162float(static_cast<const __nv_bfloat16*>(ea.bias)[col0 + i]) : 0.f;
-          vh[i] = vh[i] * inv + bb;
+          for (int g = 0; g < 8; ++g) {
+            const uint4 u = __ldg(bp + g);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              vh[8 * g + 2 * k] = vh[8 * g + 2 * k] * inv + __uint_as_float(w[k] << 16);
+              vh[8 * g + 2 * k + 1] = vh[8 * g + 2 * k + 1] * inv + __uint_as_float(w[k] & 0xFFFF0000u);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) vh[i] *= inv;
         }
         fp4_epilogue_store<EPI>(vh, row, col0, N, ea, amax);
       }
