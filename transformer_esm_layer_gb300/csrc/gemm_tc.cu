@@ -442,24 +442,46 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         const uint32_t idesc = tile < full_tiles ? idesc_full : idesc_half;
-        for (int kb = 0; kb < kb_count; ++kb) {
+        // A stage whose operands have landed is issued; if the next one has landed too (a
+        // non-blocking test), its four MMAs follow back to back.  The issuing thread blocks
+        // while the tensor pipe's short queue is full, and the instructions between two
+        // stages (barrier test, fence, descriptors) could otherwise let the queue run dry when
+        // the epilogue warps on its scheduler are busy; a stage still in flight is not waited
+        // for, so delivery-bound GEMMs lose nothing.
+        for (int kb = 0; kb < kb_count;) {
+          const int stage1 = stage + 1 == S ? 0 : stage + 1;
+          const uint32_t phase1 = stage + 1 == S ? phase ^ 1u : phase;
           if (!mbar_wait(&sm->full[stage], phase)) {
             latch_error(err, ERRBIT_TIMEOUT);
             sm->abort = 1;
             break;
           }
+          const bool two = kb + 1 < kb_count && mbar_test(&sm->full[stage1], phase1);
           tc_fence_after();
-          const uint64_t ad0 = adesc0 + (uint64_t)((stage * A_STAGE) >> 4);
-          const uint64_t bd0 = bdesc0 + (uint64_t)((stage * B_STAGE) >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
-            const uint64_t ad = ad0 + kStepA * (uint64_t)k;
-            const uint64_t bd = bd0 + kStepB * (uint64_t)k;
-            if (FP8) mma_f8_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
-            else mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !two) break;
+            const int sg = h ? stage1 : stage;
+            const uint64_t ad0 = adesc0 + (uint64_t)((sg * A_STAGE) >> 4);
+            const uint64_t bd0 = bdesc0 + (uint64_t)((sg * B_STAGE) >> 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
+              const uint64_t ad = ad0 + kStepA * (uint64_t)k;
+              const uint64_t bd = bd0 + kStepB * (uint64_t)k;
+              if (FP8) mma_f8_pair(d_tmem, ad, bd, idesc, (kb | h | k) != 0);
+              else mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | h | k) != 0);
+            }
+            mma_commit_pair(&sm->empty[sg]);
           }
-          mma_commit_pair(&sm->empty[stage]);
-          if (++stage == S) { stage = 0; phase ^= 1; }
+          if (two) {
+            kb += 2;
+            stage = stage1 + 1 == S ? 0 : stage1 + 1;
+            phase = stage1 + 1 == S ? phase1 ^ 1u : phase1;
+          } else {
+            kb += 1;
+            stage = stage1;
+            phase = phase1;
+          }
         }
         if (sm->abort) break;
         mma_commit_pair(&sm->tfull[acc]);
