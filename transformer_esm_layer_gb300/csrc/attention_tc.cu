@@ -238,10 +238,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             mbar_test(&sm->v_full[gp % STG], (uint32_t)(gp / STG) & 1u)) {
           tc_fence_after();
           const bool first = (first_bits >> (gp & 31)) & 1u;
-          const uint64_t vd = vdesc0 + (uint64_t)((2 * (gp % STG) * TILE_BYTES) >> 4);
+          // descriptor arithmetic on the low word (the start-address field cannot carry): fewer
+          // instructions for the issuing thread between two MMAs
+          const uint32_t vlo = (uint32_t)vdesc0 + (uint32_t)((2 * (gp % STG) * TILE_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)  // 16 keys = 16 rows of V = 2048 bytes
-            mma_bf16_ts(tmem + COL_O, tmem + COL_P + 8 * k, vd + (uint64_t)(128 * k), idesc_pv,
+            mma_bf16_ts(tmem + COL_O, tmem + COL_P + 8 * k,
+                        (vdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(vlo + 128u * (uint32_t)k), idesc_pv,
                         (!first || k > 0) ? 1u : 0u);
           mma_commit(&sm->pv_done);
           mma_commit(&sm->v_empty[gp % STG]);
@@ -254,11 +257,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
               (gs == 0 || mbar_test(&sm->s_free, (uint32_t)(gs - 1) & 1u)) &&
               (js > 0 || mbar_test(&sm->q_full[qb], (uint32_t)(qi_s >> 1) & 1u))) {
             tc_fence_after();
-            const uint64_t ad = qdesc0 + (uint64_t)((qb * TILE_BYTES) >> 4);
-            const uint64_t bd = kdesc0 + (uint64_t)((2 * st * TILE_BYTES) >> 4);
+            const uint32_t alo = (uint32_t)qdesc0 + (uint32_t)((qb * TILE_BYTES) >> 4);
+            const uint32_t blo = (uint32_t)kdesc0 + (uint32_t)((2 * st * TILE_BYTES) >> 4);
 #pragma unroll
             for (int k = 0; k < DH / 16; ++k)  // 16 dims = 32 bytes of each 128-byte row
-              mma_bf16_ss(tmem + COL_S, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
+              mma_bf16_ss(tmem + COL_S, (qdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(alo + 2u * (uint32_t)k),
+                          (kdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(blo + 2u * (uint32_t)k), idesc_s, k > 0 ? 1u : 0u);
             mma_commit(&sm->s_full);
             mma_commit(&sm->k_empty[st]);
             if (js == 0) first_bits |= 1u << (gs & 31);

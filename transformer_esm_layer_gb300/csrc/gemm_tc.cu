@@ -462,12 +462,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int h = 0; h < 2; ++h) {
             if (h == 1 && !two) break;
             const int sg = h ? stage1 : stage;
-            const uint64_t ad0 = adesc0 + (uint64_t)((sg * A_STAGE) >> 4);
-            const uint64_t bd0 = bdesc0 + (uint64_t)((sg * B_STAGE) >> 4);
+            // descriptor arithmetic on the low word only (the start-address field cannot carry):
+            // fewer instructions for the issuing thread between two MMAs
+            const uint32_t alo = (uint32_t)adesc0 + (uint32_t)((sg * A_STAGE) >> 4);
+            const uint32_t blo = (uint32_t)bdesc0 + (uint32_t)((sg * B_STAGE) >> 4);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
-              const uint64_t ad = ad0 + kStepA * (uint64_t)k;
-              const uint64_t bd = bd0 + kStepB * (uint64_t)k;
+              const uint64_t ad = (adesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(alo + (uint32_t)kStepA * (uint32_t)k);
+              const uint64_t bd = (bdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(blo + (uint32_t)kStepB * (uint32_t)k);
               if (FP8) mma_f8_pair(d_tmem, ad, bd, idesc, (kb | h | k) != 0);
               else mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | h | k) != 0);
             }
