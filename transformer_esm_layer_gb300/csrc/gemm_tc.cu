@@ -668,8 +668,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float a[16], bq[16];
-            tmem_ld16(tbase + c * CH::kCols + 16 * h, a);
-            tmem_ld16(tbase + c * CH::kCols + 32 + 16 * h, bq);
+            {  // both 16-column halves of the pass in one TMEM round trip
+              uint32_t ra[16], rb[16];
+              asm volatile(
+                  "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+                  "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                  "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+                  "tcgen05.wait::ld.sync.aligned;"
+                  : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]), "=r"(ra[7]),
+                    "=r"(ra[8]), "=r"(ra[9]), "=r"(ra[10]), "=r"(ra[11]), "=r"(ra[12]), "=r"(ra[13]), "=r"(ra[14]), "=r"(ra[15]),
+                    "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]), "=r"(rb[7]),
+                    "=r"(rb[8]), "=r"(rb[9]), "=r"(rb[10]), "=r"(rb[11]), "=r"(rb[12]), "=r"(rb[13]), "=r"(rb[14]), "=r"(rb[15])
+                  : "r"(tbase + c * CH::kCols + 16 * h), "r"(tbase + c * CH::kCols + 32 + 16 * h)
+                  : "memory");
+#pragma unroll
+              for (int i = 0; i < 16; ++i) { a[i] = __uint_as_float(ra[i]); bq[i] = __uint_as_float(rb[i]); }
+            }
             if (h == 1 && c == nch - 1) release_acc();
             if (!FP8 && ea.ln_stats_in != nullptr) {
               ln_fold_apply<16>(ea, col + 16 * h, ln_rs, a);
