@@ -13,11 +13,11 @@
 //               (x = column of the head, y = token row);
 //   warp 2      TMA: the V tiles into their own 2-stage ring (a V stage frees only after its
 //               P V, a K stage right after its S, so K runs ahead of V).
-//   warp 1      one thread issues the MMAs of a global sequence of key tiles g:
-//               S(g) = Q K^T (M=128, N=128, K=64) into TMEM and O += P V (M=128, N=64,
-//               K=128; P read from TMEM, V an MN-major shared-memory operand), each as soon
-//               as its operands are ready.
-//   warp 3      no role (it completes warpgroup 0, which hands registers to warpgroup 1).
+//   warp 1      one thread issues S(g) = Q K^T (M=128, N=128, K=64) into TMEM for the
+//               global sequence of key tiles g, each as soon as its operands are ready;
+//   warp 3      one thread issues O += P V (M=128, N=64, K=128; P read from TMEM, V an
+//               MN-major shared-memory operand) for the same sequence.  Two issuers keep a
+//               ready S from waiting behind the P V MMAs the pipe is still accepting.
 //   warps 4..7  softmax (warpgroup 1, register budget raised with setmaxnreg): thread r owns
 //               query row r.  It reads its whole S row (128 scores) from TMEM into registers
 //               and immediately releases S, so the tensor core computes S(g+1) while this
@@ -57,7 +57,7 @@ struct AttnSmem {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[STG], k_empty[STG];  // K tile landed / read by its S = Q K^T
   uint64_t v_full[STG], v_empty[STG];  // V tile landed / read by its O += P V
-  uint64_t s_full, s_free, p_full, pv_done, mma_done;
+  uint64_t s_full, s_free, p_full, pv_done, mma_done, pv_fin;
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     mbar_init(&sm->p_full, 4);
     mbar_init(&sm->pv_done, 1);
     mbar_init(&sm->mma_done, 1);
+    mbar_init(&sm->pv_fin, 1);
     sm->abort = 0;
     fence_barrier_init();
   }
@@ -204,92 +205,73 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Two cursors over the global tile sequence: gs, the next S = Q K^T, and gp, the next
-    // O += P V (gp < gs).  Whichever has its operands ready is issued, the P V first: the
-    // softmax of tile gp+1 waits for it before storing its P, while S(gs) is usually ready
-    // long before it is needed.
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads issue to the one tensor pipe: warp 1 every S = Q K^T, warp 3 every
+    // O += P V, each in tile order and each blocking only on its own operands.  An issuing
+    // thread is held until the pipe accepts its MMA, so with one issuer an S that was ready
+    // waited behind the eight P V MMAs before it (and a ready P V behind an S).
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(QT, KT);
       constexpr uint32_t idesc_pv = idesc_bf16(QT, DH) | (1u << 16);  // B (= V) MN-major
+      const bool is_s = warp == 1;
       const uint64_t qdesc0 = make_sw128_desc(smem_u32(sQ));  // buffer b: + b * (TILE_BYTES >> 4)
       const uint64_t kdesc0 = make_sw128_desc(smem_u32(sK));  // stage s: + 2 s (TILE_BYTES >> 4)
       const uint64_t vdesc0 = make_sw128_desc(smem_u32(sV));
       bool ok = true;
-      int gs = 0, gp = 0;        // next S, next P V
-      int rnd_s = 0, it_s = item_at(0), js = 0, qi_s = 0, nkb_s = 0;
-      bool have_item = false;
-      uint32_t first_bits = 0;   // bit (g & 31): tile g is the first of its item
+      int g = 0, qi = 0;
       int4 nxt = load_item(pb, item_at(0), heads);
-      unsigned long long idle_since = 0;
-      uint32_t idle = 0;
-      while (true) {
-        if (!have_item && it_s < n_items) {
-          const Item x = make_item(nxt, it_s, heads);
-          if (item_at(rnd_s + 1) < n_items) nxt = load_item(pb, item_at(rnd_s + 1), heads);
-          nkb_s = x.nkb;
-          js = 0;
-          have_item = true;
-        }
-        if (!have_item && gp == gs) break;  // every tile issued
-        bool progressed = false;
-        if (gp < gs && mbar_test(&sm->p_full, (uint32_t)gp & 1u) &&
-            mbar_test(&sm->v_full[gp % STG], (uint32_t)(gp / STG) & 1u)) {
-          tc_fence_after();
-          const bool first = (first_bits >> (gp & 31)) & 1u;
-          // descriptor arithmetic on the low word (the start-address field cannot carry): fewer
-          // instructions for the issuing thread between two MMAs
-          const uint32_t vlo = (uint32_t)vdesc0 + (uint32_t)((2 * (gp % STG) * TILE_BYTES) >> 4);
-#pragma unroll
-          for (int k = 0; k < KT / 16; ++k)  // 16 keys = 16 rows of V = 2048 bytes
-            mma_bf16_ts(tmem + COL_O, tmem + COL_P + 8 * k,
-                        (vdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(vlo + 128u * (uint32_t)k), idesc_pv,
-                        (!first || k > 0) ? 1u : 0u);
-          mma_commit(&sm->pv_done);
-          mma_commit(&sm->v_empty[gp % STG]);
-          ++gp;
-          progressed = true;
-        } else if (have_item && gs - gp < 3) {
-          const int st = gs % STG;
-          const int qb = qi_s & 1;
-          if (mbar_test(&sm->k_full[st], (uint32_t)(gs / STG) & 1u) &&
-              (gs == 0 || mbar_test(&sm->s_free, (uint32_t)(gs - 1) & 1u)) &&
-              (js > 0 || mbar_test(&sm->q_full[qb], (uint32_t)(qi_s >> 1) & 1u))) {
+      for (int rnd = 0, it = item_at(0); it < n_items && ok && !sm->abort; it = item_at(++rnd), ++qi) {
+        const Item x = make_item(nxt, it, heads);
+        if (item_at(rnd + 1) < n_items) nxt = load_item(pb, item_at(rnd + 1), heads);  // prefetch
+        const int qb = qi & 1;
+        for (int j = 0; j < x.nkb; ++j, ++g) {
+          const int st = g % STG;
+          if (is_s) {
+            // the K tile has landed, the previous S has been read, the item's Q has landed
+            if (!mbar_wait(&sm->k_full[st], (uint32_t)(g / STG) & 1u) ||
+                (g > 0 && !mbar_wait(&sm->s_free, (uint32_t)(g - 1) & 1u)) ||
+                (j == 0 && !mbar_wait(&sm->q_full[qb], (uint32_t)(qi >> 1) & 1u))) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
+            // descriptor arithmetic on the low word (the start-address field cannot carry)
             const uint32_t alo = (uint32_t)qdesc0 + (uint32_t)((qb * TILE_BYTES) >> 4);
             const uint32_t blo = (uint32_t)kdesc0 + (uint32_t)((2 * st * TILE_BYTES) >> 4);
 #pragma unroll
             for (int k = 0; k < DH / 16; ++k)  // 16 dims = 32 bytes of each 128-byte row
               mma_bf16_ss(tmem + COL_S, (qdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(alo + 2u * (uint32_t)k),
-                          (kdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(blo + 2u * (uint32_t)k), idesc_s, k > 0 ? 1u : 0u);
+                          (kdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(blo + 2u * (uint32_t)k), idesc_s,
+                          k > 0 ? 1u : 0u);
             mma_commit(&sm->s_full);
             mma_commit(&sm->k_empty[st]);
-            if (js == 0) first_bits |= 1u << (gs & 31);
-            else first_bits &= ~(1u << (gs & 31));
-            ++gs;
-            if (++js == nkb_s) {
-              have_item = false;
-              it_s = item_at(++rnd_s);
-              ++qi_s;
+          } else {
+            // P of this tile is in tensor memory and its V tile has landed
+            if (!mbar_wait(&sm->p_full, (uint32_t)g & 1u) || !mbar_wait(&sm->v_full[st], (uint32_t)(g / STG) & 1u)) {
+              ok = false;
+              break;
             }
-            progressed = true;
+            tc_fence_after();
+            const uint32_t vlo = (uint32_t)vdesc0 + (uint32_t)((2 * st * TILE_BYTES) >> 4);
+#pragma unroll
+            for (int k = 0; k < KT / 16; ++k)  // 16 keys = 16 rows of V = 2048 bytes
+              mma_bf16_ts(tmem + COL_O, tmem + COL_P + 8 * k,
+                          (vdesc0 & 0xFFFFFFFF00000000ull) | (uint64_t)(vlo + 128u * (uint32_t)k), idesc_pv,
+                          (j > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&sm->pv_done);
+            mma_commit(&sm->v_empty[st]);
           }
-        }
-        if (progressed) {
-          idle = 0;
-        } else if ((++idle & 63u) == 1u) {  // bounded: give up after the wait limit idle
-          const unsigned long long now = globaltimer_ns();
-          if (idle == 1u) idle_since = now;
-          else if (now - idle_since > kWaitLimitNs) { ok = false; break; }
         }
       }
       if (!ok) {
         latch_error(err, ERRBIT_TIMEOUT);
         sm->abort = 1;
       }
-      mma_commit(&sm->mma_done);
-      mbar_wait(&sm->mma_done, 0);
+      // every MMA of this thread has completed before tensor memory may be released
+      uint64_t* fin = is_s ? &sm->mma_done : &sm->pv_fin;
+      mma_commit(fin);
+      mbar_wait(fin, 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
