@@ -51,9 +51,12 @@ constexpr int TMEM_COLS = 2 * BN;              // two accumulators
 // which leaves room for a 5-stage operand ring.  The residual epilogue moves its fp32
 // chunks through the load/store unit one chunk per warp at a time, so one staging chunk
 // per half suffices and the ring gets a 6th stage (its long-K launch streams A from HBM).
+// The QKV and fc1 launches (K = hidden = 1280 at 650M) run as fast on a 4-stage ring as on 5
+// (measured), so they keep 4.
 template <int EPI>
 struct Plan {
-  static constexpr int kStages = (EPI == ESM_EPI_RESIDUAL) ? 6 : 5;
+  static constexpr int kStages =
+      (EPI == ESM_EPI_RESIDUAL) ? 6 : ((EPI == ESM_EPI_QKV_ROPE || EPI == ESM_EPI_GELU) ? 4 : 5);
   static constexpr int kEBufs = (EPI == ESM_EPI_RESIDUAL) ? 1 : 2;  // staging chunks per half
   static constexpr int kSmemBytes =
       kStages * (A_STAGE + B_STAGE) + 2 * kEBufs * E_BUF + 1024 /*align*/ + 256 /*barriers*/;
