@@ -520,8 +520,11 @@ def run_ours(args):
         out_h = torch.empty(T, g.hidden, dtype=enc.out_dtype).pin_memory()
         out_view = out_h.view(torch.int16 if enc.out_dtype == torch.bfloat16 else torch.int32).numpy()
         tok_view, cu_view = tok_h.numpy(), cu_h.numpy()
-        n_e2e = min(args.steps, 10)
-        enc.forward_host(dw, tok_view, cu_view, maxL, out_view, ws, stream=stream)
+        n_e2e = args.steps
+        # two untimed calls: the first runs eagerly, the second captures the call's CUDA graph
+        # (pinned buffers), which later calls replay
+        for _ in range(2):
+            enc.forward_host(dw, tok_view, cu_view, maxL, out_view, ws, stream=stream)
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
