@@ -391,6 +391,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       uint8_t* stage = sQ + (qi & 1) * TILE_BYTES;
       constexpr int kUnits = (OUT == Act::BF16) ? 8 : 4;  // 16-byte units per output row
       if constexpr (OUT == Act::BF16) {
+        if (amax_out != nullptr && r < x.qrows) {  // max |O| of this row: max |acc| / l
+          float m = 0.f;
+#pragma unroll
+          for (int i = 0; i < DH; ++i) m = fmaxf(m, fabsf(__uint_as_float(u[i >> 5][i & 31])));
+          amax = fmaxf(amax, m * inv);
+        }
 #pragma unroll
         for (int i = 0; i < DH / 8; ++i) {
           const uint32_t* w = &u[i >> 2][(i & 3) * 8];
@@ -440,7 +446,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
     }
-    if constexpr (OUT == Act::E4M3) {
+    if (OUT == Act::E4M3 || amax_out != nullptr) {
+      // a bf16 output's amax is that of the rounded values: rounding is monotone, so round the max
+      if constexpr (OUT == Act::BF16) amax = __bfloat162float(__float2bfloat16_rn(amax));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
       if (lane == 0) atomic_max_nonneg(amax_out, amax);

@@ -382,7 +382,7 @@ esm_status run_fp4_layer(esm_encoder* h, const esm_weights* w, int l, int T, con
     return cuda_status(e);
   };
   esm_status s;
-  // the layer's amaxes start from zero; LN1, LN2 and fc1's GELU epilogue fold theirs in
+  // the layer's amaxes start from zero; LN1, LN2, the attention and fc1's GELU epilogue fold theirs in
   if (cudaMemsetAsync(am, 0, kNumFp8Tensors * sizeof(float), st) != cudaSuccess) return ESM_ERR_CUDA;
   PROF(h, P_LN, st, 1,
        launch_layernorm(x, w->ln1_g[l], w->ln1_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, am + X_QKV,
@@ -394,10 +394,11 @@ esm_status run_fp4_layer(esm_encoder* h, const esm_weights* w, int l, int T, con
     ProfScope _ps(h, P_ATTN, st, 1);
     const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
     if (!tq) return ESM_ERR_CUDA;
-    if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, nullptr, h->d_err, st) != cudaSuccess)
+    // the attention output's amax comes from the attention kernel (so its quantisation is one pass)
+    if (launch_attention_tc(tq, o, Act::BF16, d, H, L.max_items, pb, nullptr, am + X_O, h->d_err, st) != cudaSuccess)
       return ESM_ERR_CUDA;
   }
-  if ((s = gemm(P_OPROJ, kFp4Residual, o, false, d, w->w_o[l], d, X_O, W_O, w->b_o[l], x, nullptr)) != ESM_OK)
+  if ((s = gemm(P_OPROJ, kFp4Residual, o, true, d, w->w_o[l], d, X_O, W_O, w->b_o[l], x, nullptr)) != ESM_OK)
     return s;
   PROF(h, P_LN, st, 1,
        launch_layernorm(x, w->ln2_g[l], w->ln2_b[l], false, y, Act::BF16, T, d, c.ln_eps, nullptr, am + X_1, nullptr,
@@ -487,8 +488,8 @@ esm_status run_layers(esm_encoder* h, const esm_weights* w, int T, int max_items
       else {
         const CUtensorMap* tq = h->map(qkv, (uint64_t)T, (uint64_t)3 * d, 128, 2);
         if (!tq) return ESM_ERR_CUDA;
-        if (launch_attention_tc(tq, o, fp8 ? Act::E4M3 : Act::BF16, d, H, max_items, pb, sc + X_O, am + X_O,
-                                h->d_err, st) != cudaSuccess)
+        if (launch_attention_tc(tq, o, fp8 ? Act::E4M3 : Act::BF16, d, H, max_items, pb, sc + X_O,
+                                fp8 ? am + X_O : nullptr, h->d_err, st) != cudaSuccess)
           return ESM_ERR_CUDA;
       }
     }
