@@ -111,7 +111,9 @@ __device__ __forceinline__ Item make_item(int4 w, int it, int heads) {
   return x;
 }
 
-template <Act OUT>
+// AMAX: a bf16 output also records its max |value| into amax_out (compiled only into the
+// instantiation that needs it, so the others keep their registers).
+template <Act OUT, bool AMAX = false>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm, void* __restrict__ o, int d, int heads,
                         PackBuffers pb, const float* q_scale, float* amax_out, float* __restrict__ lse,
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       uint8_t* stage = sQ + (qi & 1) * TILE_BYTES;
       constexpr int kUnits = (OUT == Act::BF16) ? 8 : 4;  // 16-byte units per output row
       if constexpr (OUT == Act::BF16) {
-        if (amax_out != nullptr && r < x.qrows) {  // max |O| of this row: max |acc| / l
+        if (AMAX && r < x.qrows) {  // max |O| of this row: max |acc| / l
           float m = 0.f;
 #pragma unroll
           for (int i = 0; i < DH; ++i) m = fmaxf(m, fabsf(__uint_as_float(u[i >> 5][i & 31])));
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       latch_error(err, ERRBIT_TIMEOUT);
       sm->abort = 1;
     }
-    if (OUT == Act::E4M3 || amax_out != nullptr) {
+    if constexpr (OUT == Act::E4M3 || AMAX) {
       // a bf16 output's amax is that of the rounded values: rounding is monotone, so round the max
       if constexpr (OUT == Act::BF16) amax = __bfloat162float(__float2bfloat16_rn(amax));
 #pragma unroll
@@ -472,13 +474,15 @@ cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int
                                 cudaStream_t st, float* lse, int lse_stride) {
   if (max_items <= 0) return cudaSuccess;
   static int num_sms = 0;
-  static bool configured[2] = {false, false};
-  const int which = out == Act::E4M3 ? 1 : 0;
+  static bool configured[3] = {false, false, false};
+  const int which = out == Act::E4M3 ? 1 : (amax != nullptr ? 2 : 0);
   if (!configured[which]) {
-    cudaError_t e = which ? cudaFuncSetAttribute(attention_tc_kernel<Act::E4M3>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
-                          : cudaFuncSetAttribute(attention_tc_kernel<Act::BF16>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = which == 1 ? cudaFuncSetAttribute(attention_tc_kernel<Act::E4M3>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
+                    : which == 2 ? cudaFuncSetAttribute(attention_tc_kernel<Act::BF16, true>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
+                                 : cudaFuncSetAttribute(attention_tc_kernel<Act::BF16>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[which] = true;
   }
@@ -492,9 +496,12 @@ cudaError_t launch_attention_tc(const CUtensorMap* tm_qkv, void* o, Act out, int
   const long long items = (long long)max_items * heads;
   const long long cap = (long long)CTAS_PER_SM * num_sms;
   const unsigned grid = (unsigned)(items < cap ? items : cap);
-  if (which)
+  if (which == 1)
     attention_tc_kernel<Act::E4M3><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, lse,
                                                                       lse_stride, err);
+  else if (which == 2)
+    attention_tc_kernel<Act::BF16, true><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax,
+                                                                            lse, lse_stride, err);
   else
     attention_tc_kernel<Act::BF16><<<grid, THREADS, SMEM_BYTES, st>>>(*tm_qkv, o, d, heads, pb, q_scale, amax, lse,
                                                                       lse_stride, err);
