@@ -99,24 +99,68 @@ __global__ void __launch_bounds__(256, N4 <= 10 ? 2 : 1) ln_bwd_kernel(const voi
     }
     const float mg = wsum(sg) / (float)cols, mgx = wsum(sgx) / (float)cols;
     float4* out = reinterpret_cast<float4*>(dx + (size_t)row * cols);
-    const float4* res = dres ? reinterpret_cast<const float4*>(dres + (size_t)row * cols) : nullptr;
+    if constexpr (N4 > 20) {
+      // widest rows (1 block per SM, registers at the limit): one pass, the residual
+      // gradient read element by element before the store that may overwrite it
+      const float4* res = dres ? reinterpret_cast<const float4*>(dres + (size_t)row * cols) : nullptr;
 #pragma unroll
-    for (int i = 0; i < N4; ++i) {
-      const int c = i * 32 + lane;
-      if (c < n4) {
-        const float4 gm = ld_param4(gamma, 4 * c, gf32);
-        float4 o = res ? res[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-        o.x += rstd * (d[i].x * gm.x - mg - v[i].x * mgx);
-        o.y += rstd * (d[i].y * gm.y - mg - v[i].y * mgx);
-        o.z += rstd * (d[i].z * gm.z - mg - v[i].z * mgx);
-        o.w += rstd * (d[i].w * gm.w - mg - v[i].w * mgx);
-        out[c] = o;
-        float4 a = mine[c], b = mine[n4 + c];
-        a.x = fmaf(d[i].x, v[i].x, a.x); a.y = fmaf(d[i].y, v[i].y, a.y);
-        a.z = fmaf(d[i].z, v[i].z, a.z); a.w = fmaf(d[i].w, v[i].w, a.w);
-        b.x += d[i].x; b.y += d[i].y; b.z += d[i].z; b.w += d[i].w;
-        mine[c] = a;
-        mine[n4 + c] = b;
+      for (int i = 0; i < N4; ++i) {
+        const int c = i * 32 + lane;
+        if (c < n4) {
+          const float4 gm = ld_param4(gamma, 4 * c, gf32);
+          float4 o = res ? res[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+          o.x += rstd * (d[i].x * gm.x - mg - v[i].x * mgx);
+          o.y += rstd * (d[i].y * gm.y - mg - v[i].y * mgx);
+          o.z += rstd * (d[i].z * gm.z - mg - v[i].z * mgx);
+          o.w += rstd * (d[i].w * gm.w - mg - v[i].w * mgx);
+          out[c] = o;
+          float4 a = mine[c], b = mine[n4 + c];
+          a.x = fmaf(d[i].x, v[i].x, a.x); a.y = fmaf(d[i].y, v[i].y, a.y);
+          a.z = fmaf(d[i].z, v[i].z, a.z); a.w = fmaf(d[i].w, v[i].w, a.w);
+          b.x += d[i].x; b.y += d[i].y; b.z += d[i].z; b.w += d[i].w;
+          mine[c] = a;
+          mine[n4 + c] = b;
+        }
+      }
+    } else {
+      // dgamma/dbeta slices first; then d becomes this row's dx increment and v is free
+#pragma unroll
+      for (int i = 0; i < N4; ++i) {
+        const int c = i * 32 + lane;
+        if (c < n4) {
+          const float4 gm = ld_param4(gamma, 4 * c, gf32);
+          float4 a = mine[c], b = mine[n4 + c];
+          a.x = fmaf(d[i].x, v[i].x, a.x); a.y = fmaf(d[i].y, v[i].y, a.y);
+          a.z = fmaf(d[i].z, v[i].z, a.z); a.w = fmaf(d[i].w, v[i].w, a.w);
+          b.x += d[i].x; b.y += d[i].y; b.z += d[i].z; b.w += d[i].w;
+          mine[c] = a;
+          mine[n4 + c] = b;
+          d[i].x = rstd * (d[i].x * gm.x - mg - v[i].x * mgx);
+          d[i].y = rstd * (d[i].y * gm.y - mg - v[i].y * mgx);
+          d[i].z = rstd * (d[i].z * gm.z - mg - v[i].z * mgx);
+          d[i].w = rstd * (d[i].w * gm.w - mg - v[i].w * mgx);
+        }
+      }
+      if (dres) {
+        // the residual gradient may alias dx: every load of the row is issued before its
+        // first store, so the loads overlap instead of waiting one by one behind the stores
+        const float4* res = reinterpret_cast<const float4*>(dres + (size_t)row * cols);
+#pragma unroll
+        for (int i = 0; i < N4; ++i) {
+          const int c = i * 32 + lane;
+          if (c < n4) v[i] = res[c];
+        }
+#pragma unroll
+        for (int i = 0; i < N4; ++i) {
+          const int c = i * 32 + lane;
+          if (c < n4) out[c] = make_float4(v[i].x + d[i].x, v[i].y + d[i].y, v[i].z + d[i].z, v[i].w + d[i].w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < N4; ++i) {
+          const int c = i * 32 + lane;
+          if (c < n4) out[c] = d[i];
+        }
       }
     }
   }
