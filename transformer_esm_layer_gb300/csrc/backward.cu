@@ -202,25 +202,27 @@ __global__ void __launch_bounds__(128) colsum_kernel(const void* __restrict__ sr
 }
 
 // out[i] = scale * sum_k partial[k * stride + i] in a fixed order: a block owns 32
-// consecutive i; warp w adds the chunks k = w, w + 8, ... (lane = i, coalesced), then the
-// eight warp sums are added in warp order.
-__global__ void __launch_bounds__(256) reduce_chunks_kernel(const float* __restrict__ partial, int chunks,
-                                                            size_t stride, int n, float scale,
-                                                            float* __restrict__ out) {
-  __shared__ float part[8][32];
+// consecutive i; warp w of kReduceWarps adds the chunks k = w, w + kReduceWarps, ... (lane =
+// i, coalesced), then the warp sums are added in warp order.  The sums have few columns
+// (a block per 32) and hundreds of chunks, so the block is wide: more loads in flight.
+constexpr int kReduceWarps = 32;
+__global__ void __launch_bounds__(32 * kReduceWarps) reduce_chunks_kernel(const float* __restrict__ partial, int chunks,
+                                                                          size_t stride, int n, float scale,
+                                                                          float* __restrict__ out) {
+  __shared__ float part[kReduceWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 32 + lane;
   float a = 0.f;
   if (i < n) {
 #pragma unroll 4
-    for (int k = warp; k < chunks; k += 8) a += __ldg(partial + (size_t)k * stride + i);
+    for (int k = warp; k < chunks; k += kReduceWarps) a += __ldg(partial + (size_t)k * stride + i);
   }
   part[warp][lane] = a;
   __syncthreads();
   if (warp == 0 && i < n) {
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) t += part[w][lane];
+    for (int w = 0; w < kReduceWarps; ++w) t += part[w][lane];
     out[i] = t * scale;
   }
 }
@@ -282,7 +284,8 @@ void reduce_chunks(const float* partial, int chunks, size_t stride, size_t n, fl
   if (chunks <= 16 && n % 4 == 0 && stride % 4 == 0)
     reduce_few_chunks_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, st>>>(partial, chunks, stride, n, scale, out);
   else
-    reduce_chunks_kernel<<<(unsigned)((n + 31) / 32), 256, 0, st>>>(partial, chunks, stride, (int)n, scale, out);
+    reduce_chunks_kernel<<<(unsigned)((n + 31) / 32), 32 * kReduceWarps, 0, st>>>(partial, chunks, stride, (int)n, scale,
+                                                                                 out);
 }
 
 constexpr int kLnRowsPerBlock = 64;
