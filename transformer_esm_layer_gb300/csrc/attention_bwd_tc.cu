@@ -505,19 +505,23 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// D[h, t] = sum_c dO[t, h*64 + c] * O[t, h*64 + c] (one thread per (token, head); head-major).
+// D[h, t] = sum_c dO[t, h*64 + c] * O[t, h*64 + c] (head-major).  Eight lanes per (token,
+// head): lane p dots columns 8p..8p+7 (one 16-byte load of each operand, so the eight lanes
+// read the head's 128 contiguous bytes together), then three shuffle steps add the eight
+// partial sums.  Every lane reaches the shuffles (no early return).
+static_assert(DH == 64, "eight 16-byte pieces per head row");
 __global__ void attention_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                           float* __restrict__ dsum, int T, int d, int heads) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)T * heads) return;
-  const long long t = i / heads;
-  const int h = (int)(i % heads);
-  const uint4* a = reinterpret_cast<const uint4*>(o + t * d + h * DH);
-  const uint4* b = reinterpret_cast<const uint4*>(dout + t * d + h * DH);
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long i = g >> 3;
+  const int p = (int)(g & 7);
+  const bool ok = i < (long long)T * heads;
+  const long long t = ok ? i / heads : 0;
+  const int h = ok ? (int)(i % heads) : 0;
   float acc = 0.f;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint4 x = __ldg(a + u), y = __ldg(b + u);
+  if (ok) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(o + t * d + h * DH) + p);
+    const uint4 y = __ldg(reinterpret_cast<const uint4*>(dout + t * d + h * DH) + p);
     const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&x);
     const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&y);
 #pragma unroll
@@ -527,7 +531,10 @@ __global__ void attention_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ o, c
       acc = fmaf(xf.y, yf.y, acc);
     }
   }
-  dsum[(size_t)h * T + t] = acc;
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  if (ok && p == 0) dsum[(size_t)h * T + t] = acc;
 }
 
 // dq = dq_acc / 8 with RoPE undone (pairs (j, j + 32) turned back by their angle) -> the q
@@ -589,7 +596,7 @@ cudaError_t launch_attention_bwd_tc(const CUtensorMap* tm_qkv, const CUtensorMap
     configured = true;
   }
   const long long th = (long long)T * heads;
-  attention_bwd_dsum_kernel<<<(unsigned)((th + 255) / 256), 256, 0, st>>>(o, dout, dsum, T, d, heads);
+  attention_bwd_dsum_kernel<<<(unsigned)((8 * th + 255) / 256), 256, 0, st>>>(o, dout, dsum, T, d, heads);
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * d, st);
   if (e != cudaSuccess) return e;
   const long long items = (long long)max_items * heads;
