@@ -6,10 +6,12 @@
 //   logits[t, v] = z[t] . emb[v] + bias[v]
 //   loss[t]      = log(sum_v exp(logits[t, v])) - logits[t, target[t]]   (0 if target = -100)
 //
-// One warp per token, persistent grid; the whole embedding (vocab x hidden) sits in shared
-// memory.  Lane l holds the 16-byte units l, l + 32, ... of the token's row; each logit is a
-// warp-wide sum, kept by lane v % 32.  The loss sum is a separate one-block reduction in a
-// fixed order, so it is bitwise reproducible.
+// bf16 (hidden a multiple of 128): the logits are a [T, hidden] x [hidden, vocab] contraction
+// on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), 16 tokens per warp, the
+// table in shared memory.  fp32: one warp per token, persistent grid; the whole embedding
+// (vocab x hidden) sits in shared memory, lane l holds the 16-byte units l, l + 32, ... of the
+// token's row and each logit is a warp-wide sum, kept by lane v % 32.  The loss sum is a
+// separate one-block reduction in a fixed order, so it is bitwise reproducible.
 #include "common.cuh"
 #include "internal.h"
 
@@ -113,6 +115,165 @@ __global__ void __launch_bounds__(256) lm_logits_kernel(const void* __restrict__
       if (lane == 0) token_loss[t] = tg == kIgnore ? 0.f : (m + logf(se)) - l_src;
     }
   }
+}
+
+// D += A B for one m16n8k16 tile: A 16 x 16 bf16 (row-major fragment a0..a3), B 16 x 8 bf16
+// (column-major fragment b0, b1), D 16 x 8 fp32.  Lane (g, t) = (lane / 4, lane % 4) holds
+// A[g][2t, 2t+1], A[g+8][2t, 2t+1], A[g][2t+8, 2t+9], A[g+8][2t+8, 2t+9], B[2t, 2t+1][g],
+// B[2t+8, 2t+9][g] and D[g][2t, 2t+1], D[g+8][2t, 2t+1] (lower column in the lower half).
+__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16 logits and loss on the tensor cores.  A warp takes 16 tokens (rows r0 = 16 grp + g and
+// r1 = r0 + 8 of its group); the vocabulary is padded with zero rows to NB blocks of 8.  In
+// each 32-column slice of the hidden dimension lane (g, t) reads columns 8t..8t+7 of rows r0,
+// r1 and of table rows 8 nb + g as one 16-byte unit each, and the slice's two k-steps give
+// columns 8t + {0,1 | 2,3} and 8t + {4,5 | 6,7} the k positions {2t, 2t+1 | 2t+8, 2t+9} that
+// the instruction assigns to lane t, in A and in B alike, so every column of the slice is
+// summed exactly once.  Table rows lie row_bytes apart with row_bytes = 64 (mod 512), so the
+// eight rows one instruction reads fall in distinct banks.  A logit of row r0 (r1) sits in
+// D[g][.] (D[g+8][.]) of its block: the row's max, sum of exponentials and target logit
+// reduce over the four lanes of a quad.  Rows past T load row T - 1 and are never written.
+template <int NB>
+__global__ void __launch_bounds__(128) lm_logits_mma_kernel(const __nv_bfloat16* __restrict__ z,
+                                                            const __nv_bfloat16* __restrict__ emb,
+                                                            const __nv_bfloat16* __restrict__ bias, int T, int d, int V,
+                                                            int row_bytes, const int32_t* __restrict__ targets,
+                                                            float* logits, float* token_loss, unsigned* err) {
+  extern __shared__ __align__(16) uint8_t smem_e[];
+  const int units = d / 8;  // 16-byte units per row
+  for (int i = threadIdx.x; i < 8 * NB * units; i += blockDim.x) {
+    const int r = i / units, u = i - r * units;
+    const uint4 val = r < V ? __ldg(reinterpret_cast<const uint4*>(emb) + (size_t)r * units + u) : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(smem_e + (size_t)r * row_bytes + 16 * u) = val;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int warps = blockDim.x >> 5;
+  float bv[NB][2];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int v = 8 * nb + 2 * t + j;
+      bv[nb][j] = v < V ? __bfloat162float(bias[v]) : 0.f;
+    }
+  const uint8_t* eb = smem_e + (size_t)g * row_bytes + 16 * t;
+  const int groups = (T + 15) / 16;
+  for (int grp = blockIdx.x * warps + (threadIdx.x >> 5); grp < groups; grp += gridDim.x * warps) {
+    const int r0 = 16 * grp + g, r1 = r0 + 8;
+    const uint4* z0 = reinterpret_cast<const uint4*>(z + (size_t)min(r0, T - 1) * d) + t;
+    const uint4* z1 = reinterpret_cast<const uint4*>(z + (size_t)min(r1, T - 1) * d) + t;
+    float acc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+#pragma unroll 1
+    for (int kb = 0; kb < d / 32; kb += 4) {  // four slices per step: eight 16-byte loads in flight
+      uint4 pa[4], pb[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pa[j] = __ldg(z0 + 4 * (kb + j));
+        pb[j] = __ldg(z1 + 4 * (kb + j));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const uint4 q = *reinterpret_cast<const uint4*>(eb + (size_t)(8 * nb) * row_bytes + 64 * (kb + j));
+          mma_16816_bf16(acc[nb], pa[j].x, pb[j].x, pa[j].y, pb[j].y, q.x, q.y);
+          mma_16816_bf16(acc[nb], pa[j].z, pb[j].z, pa[j].w, pb[j].w, q.z, q.w);
+        }
+      }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        acc[nb][j] += bv[nb][j];
+        acc[nb][2 + j] += bv[nb][j];
+        if (8 * nb + 2 * t + j < V) {
+          m0 = fmaxf(m0, acc[nb][j]);
+          m1 = fmaxf(m1, acc[nb][2 + j]);
+        }
+      }
+    if (logits) {
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int v = 8 * nb + 2 * t + j;
+          if (v < V) {
+            if (r0 < T) logits[(size_t)r0 * V + v] = acc[nb][j];
+            if (r1 < T) logits[(size_t)r1 * V + v] = acc[nb][2 + j];
+          }
+        }
+    }
+    if (token_loss) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+      int tg0 = (targets && r0 < T) ? targets[r0] : kIgnore;
+      int tg1 = (targets && r1 < T) ? targets[r1] : kIgnore;
+      if (tg0 != kIgnore && (tg0 < 0 || tg0 >= V)) {
+        if (t == 0) latch_error(err, ERRBIT_TOKEN);
+        tg0 = kIgnore;
+      }
+      if (tg1 != kIgnore && (tg1 < 0 || tg1 >= V)) {
+        if (t == 0) latch_error(err, ERRBIT_TOKEN);
+        tg1 = kIgnore;
+      }
+      float s0 = 0.f, s1 = 0.f, own0 = 0.f, own1 = 0.f;  // own: the target's logit (one lane of the quad)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int v = 8 * nb + 2 * t + j;
+          if (v < V) {
+            s0 += expf(acc[nb][j] - m0);
+            s1 += expf(acc[nb][2 + j] - m1);
+          }
+          if (v == tg0) own0 = acc[nb][j];
+          if (v == tg1) own1 = acc[nb][2 + j];
+        }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        own0 += __shfl_xor_sync(0xffffffffu, own0, o);
+        own1 += __shfl_xor_sync(0xffffffffu, own1, o);
+      }
+      if (t == 0) {
+        if (r0 < T) token_loss[r0] = tg0 == kIgnore ? 0.f : (m0 + logf(s0)) - own0;
+        if (r1 < T) token_loss[r1] = tg1 == kIgnore ? 0.f : (m1 + logf(s1)) - own1;
+      }
+    }
+  }
+}
+
+// Table row pitch of lm_logits_mma_kernel: 2 d bytes rounded up to 64 (mod 512).
+int lm_mma_row_bytes(int d) { return 2 * d + (((64 - 2 * d) % 512) + 512) % 512; }
+
+template <int NB>
+void launch_mma_nb(int num_sms, const void* z, const void* emb, const void* bias, int T, int d, int V,
+                   const int32_t* targets, float* logits, float* token_loss, unsigned* err, cudaStream_t st) {
+  const int rb = lm_mma_row_bytes(d);
+  const size_t smem = (size_t)8 * NB * rb;
+  cudaFuncSetAttribute(lm_logits_mma_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int per_sm = smem <= 110 * 1024 ? 2 : 1;
+  const int warps = 4, groups = (T + 15) / 16;
+  int grid = std::min(num_sms * per_sm, (groups + warps - 1) / warps);
+  grid = std::max(grid, 1);
+  lm_logits_mma_kernel<NB><<<grid, 32 * warps, smem, st>>>(
+      static_cast<const __nv_bfloat16*>(z), static_cast<const __nv_bfloat16*>(emb),
+      static_cast<const __nv_bfloat16*>(bias), T, d, V, rb, targets, logits, token_loss, err);
 }
 
 // Sum of the per-token losses and count of scored tokens: one block, fixed order.
@@ -314,7 +475,20 @@ cudaError_t launch_lm_logits(const void* z, bool bf16, const void* emb, const vo
                              const int32_t* targets, float* logits, float* token_loss, float* loss_sum, int* count,
                              int num_sms, unsigned* err, cudaStream_t st) {
   const size_t smem = lm_logits_smem_bytes(V, d, bf16);
-  if (T > 0) {
+  const int nb = (V + 7) / 8;
+  if (T > 0 && bf16 && d % 128 == 0 && nb >= 1 && nb <= 8 &&
+      (size_t)8 * nb * lm_mma_row_bytes(d) <= 227 * 1024) {
+    switch (nb) {
+      case 1: launch_mma_nb<1>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+      case 2: launch_mma_nb<2>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+      case 3: launch_mma_nb<3>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+      case 4: launch_mma_nb<4>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+      case 5: launch_mma_nb<5>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+      case 6: launch_mma_nb<6>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+      case 7: launch_mma_nb<7>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+      default: launch_mma_nb<8>(num_sms, z, emb, bias, T, d, V, targets, logits, token_loss, err, st); break;
+    }
+  } else if (T > 0) {
     const int per_sm = smem <= 100 * 1024 ? 2 : 1;
     int grid = num_sms * per_sm;
     const int need = (T + 7) / 8;
