@@ -3,6 +3,8 @@
 Tolerances (relative L2 over all compared elements): fp32 1e-4, bf16 1e-2, FP8 5e-2 for
 final hidden states; packing indices bit-exact.  Kernel-level checks use tighter bounds
 derived from the arithmetic (stated at each test)."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -678,11 +680,16 @@ def _lm_case(g, precision, seed, T):
 
 
 @pytest.mark.parametrize("precision,g,T,tol", [("bf16", synth.ESM2_650M, 1000, 1e-2), ("bf16", SMALL, 333, 1e-2),
+                                               ("bf16", dataclasses.replace(SMALL, vocab=8), 257, 1e-2),
+                                               ("bf16", dataclasses.replace(SMALL, vocab=20), 100, 1e-2),
+                                               ("bf16", dataclasses.replace(SMALL, vocab=64), 333, 1e-2),
                                                ("fp32", synth.TINY, 77, 1e-5)])
 def test_lm_head_logits_and_loss(precision, g, T, tol):
     """Logits (relative L2) and masked cross-entropy against the float64 oracle; the scored
     count is exact.  bf16: the dense output and the LayerNorm output are rounded to bf16
-    (~2^-9 relative each), so logits agree to ~1e-2."""
+    (~2^-9 relative each), so logits agree to ~1e-2.  The bf16 logits run in blocks of 8
+    vocabulary rows: vocabularies of 8, 20 (a partly padded block) and 64 (eight blocks)
+    besides the model's 33."""
     from transformer_esm_layer_gb300.binding import DeviceLmHead
     enc = _enc(g, precision)
     head, h, targets = _lm_case(g, precision, 21, T)
