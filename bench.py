@@ -560,6 +560,22 @@ def run_ours(args):
                "scored_tokens": int(cnt.item()),
                "mean_loss_random_weights": float(lsum.item()) / max(1, int(cnt.item()))}
         del hws, logits
+        # the head's backward from the mean masked loss: recomputed head forward, dL/d(hidden)
+        # and every head parameter's gradient
+        from transformer_esm_layer_gb300.binding import LM_HEAD_NAMES
+        dhid = torch.empty(T, g.hidden, dtype=torch.float32, device=dev)
+        hgrads = {k: torch.empty(tuple(lm.t[k].shape), dtype=torch.float32, device=dev) for k in LM_HEAD_NAMES}
+        bws = enc.lm_head_backward_workspace(T, dev)
+        bwd_call = lambda: enc.lm_head_backward(lm, out, tg, d_hidden=dhid, grads=hgrads, loss_sum=lsum, count=cnt,
+                                                workspace=bws, stream=stream)
+        for _ in range(3):
+            bwd_call()
+        per_b, tot_b = _timed_replays(bwd_call, 10, stream)
+        enc.check(stream)
+        mlm["backward_call"] = "esm_encoder_lm_head_backward (head forward recomputed, dL/d(hidden), head gradients)"
+        mlm["backward_ms_per_call"] = tot_b / 10
+        mlm["backward_ms_per_call_median"] = statistics.median(per_b)
+        del dhid, hgrads, bws
 
     # ---------------------------------------------------------------- training step (forward that keeps
     # its activations + backward: every parameter's gradient), same batch

@@ -510,6 +510,13 @@ class EsmEncoder:
                     "esm_op_attention_backward")
         return dqkv
 
+    def lm_head_backward_workspace(self, T: int, device="cuda"):
+        import torch
+        n = ctypes.c_size_t()
+        self._raise(self.lib.esm_encoder_lm_head_backward_workspace_size(self.handle, T, ctypes.byref(n)),
+                    "esm_encoder_lm_head_backward_workspace_size")
+        return torch.empty(int(n.value), dtype=torch.uint8, device=device)
+
     def lm_head_backward(self, head: "DeviceLmHead", hidden, targets, d_hidden=None, grads=None, loss_sum=None,
                          count=None, workspace=None, stream=None, loss_count=None):
         """esm_encoder_lm_head_backward: dL/d(hidden) (float32 [T, hidden]) and the head's
@@ -524,10 +531,7 @@ class EsmEncoder:
         if grads is None:
             grads = {k: torch.empty(tuple(head.t[k].shape), dtype=torch.float32, device=dev) for k in LM_HEAD_NAMES}
         if workspace is None:
-            n = ctypes.c_size_t()
-            self._raise(self.lib.esm_encoder_lm_head_backward_workspace_size(self.handle, T, ctypes.byref(n)),
-                        "esm_encoder_lm_head_backward_workspace_size")
-            workspace = torch.empty(int(n.value), dtype=torch.uint8, device=dev)
+            workspace = self.lm_head_backward_workspace(T, dev)
         gs = EsmLmHeadGrads(*[grads[k].data_ptr() for k in LM_HEAD_NAMES])
         self._raise(self.lib.esm_encoder_lm_head_backward(self.handle, ctypes.byref(head.struct), _ptr(hidden), T,
                                                           _ptr(targets), _ptr(d_hidden), ctypes.byref(gs),

@@ -225,7 +225,7 @@ void reduce_chunks(const float* partial, int chunks, size_t stride, size_t n, fl
 // LayerNorm backward of a bf16 input x (no residual gradient added): dx, dgamma, dbeta.
 void launch_ln_bwd_bf16in(const void* x, const void* gamma, bool gf32, const float* dy, float* dx, float* dgamma,
                           float* dbeta, float* partial, int rows, int cols, float eps, cudaStream_t st);
-// dz = du * GELU'(a) (a: bf16 pre-activation; dz bf16).
+// dz = du * GELU'(a) (a: bf16 pre-activation; dz bf16); n % 4 == 0, buffers 16-byte aligned.
 void launch_gelu_bwd(const float* du, const __nv_bfloat16* a, __nv_bfloat16* dz, size_t n, cudaStream_t st);
 // Masked-LM head backward, output stage: dlogits of the mean masked cross-entropy (count =
 // number of scored tokens, device), dz = dlogits * emb (fp32 [T, d]), the tied embedding's

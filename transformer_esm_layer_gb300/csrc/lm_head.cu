@@ -333,76 +333,99 @@ __global__ void __launch_bounds__(256) lm_dlogits_kernel(const float* __restrict
   if (lane + 32 < V) out[lane + 32] = (ehi * inv - (lane + 32 == tg ? 1.f : 0.f)) * sc;
 }
 
-// dz[t, :] = sum_v dl[t, v] emb[v, :] (bf16 table in shared memory, fp32 out).  One warp per
-// token; lane l owns the 8-column units l, l + 32, ... of the row.
-template <int NU>
-__global__ void __launch_bounds__(256) lm_dz_kernel(const float* __restrict__ dl, const void* __restrict__ emb,
+// dz[t, :] = sum_v dl[t, v] emb[v, :] (bf16 table, fp32 out).  A block owns 64 tokens x 128
+// columns: the table's 128 columns (as fp32) and the 64 tokens' dl rows (transposed, so a
+// thread's eight tokens are contiguous) sit in shared memory; thread (w, l) keeps tokens
+// 8w..8w+7 x columns 4l..4l+3 in registers and adds the vocabulary rows in order v = 0, 1, ...
+constexpr int kDzTok = 64, kDzCols = 128, kDzTStride = kDzTok + 4;
+__global__ void __launch_bounds__(256) lm_dz_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ emb,
                                                     int T, int d, int V, float* __restrict__ dz) {
-  extern __shared__ __align__(16) uint8_t smem_e[];
-  const int units = d / 8;
-  {
-    const uint4* src = static_cast<const uint4*>(emb);
-    uint4* dst = reinterpret_cast<uint4*>(smem_e);
-    for (int i = threadIdx.x; i < V * units; i += blockDim.x) dst[i] = __ldg(src + i);
+  extern __shared__ __align__(16) float smem_f[];
+  float* se = smem_f;                          // [V][kDzCols]
+  float* sdt = smem_f + (size_t)V * kDzCols;   // [V][kDzTStride]: dl of token t0 + i at [v][i]
+  const int c_base = blockIdx.x * kDzCols, t0 = blockIdx.y * kDzTok;
+  const int nt = min(kDzTok, T - t0), nc = min(kDzCols, d - c_base);
+  for (int i = threadIdx.x; i < V * kDzCols; i += blockDim.x) {
+    const int v = i / kDzCols, c = i - v * kDzCols;
+    se[i] = c < nc ? __bfloat162float(emb[(size_t)v * d + c_base + c]) : 0.f;
+  }
+  for (int i = threadIdx.x; i < kDzTok * V; i += blockDim.x) {
+    const int t = i / V, v = i - t * V;
+    sdt[v * kDzTStride + t] = t < nt ? dl[(size_t)(t0 + t) * V + v] : 0.f;
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
-  const uint4* e16 = reinterpret_cast<const uint4*>(smem_e);
-  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
-    const float dlo = lane < V ? dl[(size_t)t * V + lane] : 0.f;
-    const float dhi = lane + 32 < V ? dl[(size_t)t * V + lane + 32] : 0.f;
-    float acc[NU][8];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  float acc[8][4];
 #pragma unroll
-    for (int i = 0; i < NU; ++i)
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  for (int v = 0; v < V; ++v) {
+    const float4 e = *reinterpret_cast<const float4*>(se + v * kDzCols + 4 * l);
+    const float4 g0 = *reinterpret_cast<const float4*>(sdt + v * kDzTStride + 8 * w);
+    const float4 g1 = *reinterpret_cast<const float4*>(sdt + v * kDzTStride + 8 * w + 4);
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
-    for (int v = 0; v < V; ++v) {
-      const float g = __shfl_sync(0xffffffffu, v < 32 ? dlo : dhi, v & 31);
-#pragma unroll
-      for (int i = 0; i < NU; ++i) {
-        const int c = i * 32 + lane;
-        if (c < units) {
-          float e[8];
-          unpack<true>(e16[v * units + c], e);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(g, e[k], acc[i][k]);
-        }
-      }
+    for (int i = 0; i < 8; ++i) {
+      acc[i][0] = fmaf(g[i], e.x, acc[i][0]);
+      acc[i][1] = fmaf(g[i], e.y, acc[i][1]);
+      acc[i][2] = fmaf(g[i], e.z, acc[i][2]);
+      acc[i][3] = fmaf(g[i], e.w, acc[i][3]);
     }
-    float4* out = reinterpret_cast<float4*>(dz + (size_t)t * d);
+  }
+  if (4 * l < nc) {
 #pragma unroll
-    for (int i = 0; i < NU; ++i) {
-      const int c = i * 32 + lane;
-      if (c < units) {
-        out[2 * c] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        out[2 * c + 1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int t = 8 * w + i;
+      if (t < nt)
+        *reinterpret_cast<float4*>(dz + (size_t)(t0 + t) * d + c_base + 4 * l) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
   }
 }
 
 // Partial sums over one chunk of tokens of the tied embedding's gradient
 // demb[v, c] = sum_t dl[t, v] z[t, c] (z bf16) and, in the blocks of column tile 0, of the
-// vocabulary bias's gradient dbias[v] = sum_t dl[t, v]; each thread owns one column and adds
-// the chunk's tokens in order.
-__global__ void __launch_bounds__(128) lm_demb_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ z,
+// vocabulary bias's gradient dbias[v] = sum_t dl[t, v].  A block owns 128 columns of one
+// chunk (the chunk's dl rows in shared memory); thread (w, l) keeps columns 4l..4l+3 of the
+// vocabulary rows w, w + 8, ... (V <= 64) in registers and adds the chunk's tokens in order.
+__global__ void __launch_bounds__(256) lm_demb_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ z,
                                                       int T, int d, int V, int chunk_rows, float* __restrict__ pe,
                                                       float* __restrict__ pb) {
-  extern __shared__ float sdl[];  // [chunk_rows][V] then acc [V][blockDim.x]
-  float* acc = sdl + (size_t)chunk_rows * V;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  extern __shared__ float sdl[];  // [chunk_rows][V]
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 128 + 4 * l;
   const int chunk = blockIdx.y;
   const int t0 = chunk * chunk_rows, t1 = min(T, t0 + chunk_rows);
   for (int i = threadIdx.x; i < (t1 - t0) * V; i += blockDim.x) sdl[i] = dl[(size_t)t0 * V + i];
-  for (int v = 0; v < V; ++v) acc[v * blockDim.x + threadIdx.x] = 0.f;
   __syncthreads();
-  if (c < d) {
+  if (c0 < d) {  // d % 4 == 0: the thread's four columns are in the row
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll 4
     for (int t = t0; t < t1; ++t) {
-      const float zv = __bfloat162float(z[(size_t)t * d + c]);
+      const uint2 zz = __ldg(reinterpret_cast<const uint2*>(z + (size_t)t * d + c0));
+      const float2 za = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zz.x));
+      const float2 zb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zz.y));
       const float* g = sdl + (size_t)(t - t0) * V;
-      for (int v = 0; v < V; ++v) acc[v * blockDim.x + threadIdx.x] = fmaf(g[v], zv, acc[v * blockDim.x + threadIdx.x]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int v = w + 8 * j;
+        if (v < V) {
+          const float gv = g[v];
+          acc[j][0] = fmaf(gv, za.x, acc[j][0]);
+          acc[j][1] = fmaf(gv, za.y, acc[j][1]);
+          acc[j][2] = fmaf(gv, zb.x, acc[j][2]);
+          acc[j][3] = fmaf(gv, zb.y, acc[j][3]);
+        }
+      }
     }
-    for (int v = 0; v < V; ++v) pe[((size_t)chunk * V + v) * d + c] = acc[v * blockDim.x + threadIdx.x];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int v = w + 8 * j;
+      if (v < V)
+        *reinterpret_cast<float4*>(pe + ((size_t)chunk * V + v) * d + c0) =
+            make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+    }
   }
   if (blockIdx.x == 0 && (int)threadIdx.x < V) {
     float b = 0.f;
@@ -429,27 +452,16 @@ cudaError_t launch_lm_backward_head(const float* logits, const int32_t* targets,
     return cudaGetLastError();
   }
   lm_dlogits_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, targets, count, T, V, dl);
-  const size_t smem = (size_t)V * d * 2;
-  const int nu = (d / 8 + 31) / 32;
-  int grid = num_sms * (smem <= 100 * 1024 ? 2 : 1);
-  if (grid > (T + 7) / 8) grid = (T + 7) / 8;
-#define ESM_LM_DZ(N)                                                                                   \
-  do {                                                                                                 \
-    cudaFuncSetAttribute(lm_dz_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
-    lm_dz_kernel<N><<<grid, 256, smem, st>>>(dl, emb, T, d, V, dz);                                   \
-  } while (0)
-  if (nu <= 1) ESM_LM_DZ(1);
-  else if (nu <= 2) ESM_LM_DZ(2);
-  else if (nu <= 4) ESM_LM_DZ(4);
-  else if (nu <= 8) ESM_LM_DZ(8);
-  else ESM_LM_DZ(16);
-#undef ESM_LM_DZ
+  const size_t smem = sizeof(float) * (size_t)V * (kDzCols + kDzTStride);
+  cudaFuncSetAttribute(lm_dz_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  lm_dz_kernel<<<dim3((d + kDzCols - 1) / kDzCols, (T + kDzTok - 1) / kDzTok), 256, smem, st>>>(
+      dl, static_cast<const __nv_bfloat16*>(emb), T, d, V, dz);
   const int chunks = (T + kLmChunkRows - 1) / kLmChunkRows;
   float* pe = partial;
   float* pb = partial + (size_t)chunks * V * d;
-  const size_t smem2 = sizeof(float) * ((size_t)kLmChunkRows * V + (size_t)V * 128);
+  const size_t smem2 = sizeof(float) * (size_t)kLmChunkRows * V;
   cudaFuncSetAttribute(lm_demb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-  lm_demb_kernel<<<dim3((d + 127) / 128, chunks), 128, smem2, st>>>(dl, z, T, d, V, kLmChunkRows, pe, pb);
+  lm_demb_kernel<<<dim3((d + 127) / 128, chunks), 256, smem2, st>>>(dl, z, T, d, V, kLmChunkRows, pe, pb);
   reduce_chunks(pe, chunks, (size_t)V * d, (size_t)V * d, 1.f, demb, st);
   reduce_chunks(pb, chunks, (size_t)V, (size_t)V, 1.f, dbias, st);
   return cudaGetLastError();
