@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(256) lm_demb_kernel(const float* __restrict__ 
     float acc[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int t = t0; t < t1; ++t) {
       const uint2 zz = __ldg(reinterpret_cast<const uint2*>(z + (size_t)t * d + c0));
       const float2 za = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zz.x));
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(256) lm_demb_kernel(const float* __restrict__ 
 
 }  // namespace
 
-constexpr int kLmChunkRows = 256;
+constexpr int kLmChunkRows = 128;  // tokens per partial sum of the embedding's gradient
 
 size_t lm_backward_partial_floats(int T, int V, int d) {
   const size_t chunks = T <= 0 ? 1 : (T + kLmChunkRows - 1) / kLmChunkRows;
